@@ -1,0 +1,419 @@
+#!/usr/bin/env python
+"""Decode-step benchmark: one JSON line on stdout (rank 0).
+
+A step is one pass of the hot path for the whole batch: ``kvc_append`` (k_t, v_t
+at position t, RoPE if configured) followed by ``kvc_decode_attn`` (split-K
+decode attention of the new query over its cached window).  The default workload
+is full-cache MHA decode in bf16: 32 requests, 32 query = 32 KV heads, head_dim
+128, contiguous cache of 8192, context 4096 plus one token per step; after 128
+steps every request is trimmed back to 4096 (one ``kvc_trim``), so contexts cycle
+through 4097..4224 keys.  Inputs are synthetic (seeded N(0,1), keys x 1/sqrt 2).
+
+value    = decode-attention KV bytes per second over the timed steps (whole job),
+           KV bytes = sum over requests and KV heads of keys x d x 2 (K and V) x 2 B.
+e2e      = the same metric through the C ABI with host buffers: every step copies
+           q, k, v from pinned host memory and the output back, inside the timing.
+roofline = the decode-attention call (split-K kernel + combine) timed with CUDA
+           events on its stream; algorithmic bytes = KV bytes + q + out per call.
+
+--impl reference times the CPU oracle instead (fp64 attention by definition, on
+the host cores) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_HBM_GBS = 6800.0
+METRIC = "decode-attention KV bytes/s (GB/s, % of HBM peak) and decode steps/s at 1 GB300"
+
+
+def hbm_peak():
+    try:
+        with open(PEAKS_FILE) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                                          "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9 and parts[0].isdigit() and int(parts[0]) == self.gpu_index:
+                self.rows.append(parts)
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in self.rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in self.rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+def gpu_index(local_rank: int) -> int:
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    ids = [x for x in vis.split(",") if x.strip()]
+    if ids and all(x.strip().isdigit() for x in ids) and local_rank < len(ids):
+        return int(ids[local_rank])
+    return local_rank
+
+
+# ----------------------------------------------------------------------------- workloads
+
+def kv_bytes_per_step(nkeys_per_request, Hkv, d, elem=2):
+    return sum(nkeys_per_request) * Hkv * d * 2 * elem
+
+
+class FullCacheBench:
+    """Full-cache MHA decode, bf16: B=32, H=32, d=128, contiguous 8192, context 4096 + steps."""
+
+    CYCLE = 128
+
+    def __init__(self, device):
+        import torch
+        from kv_cache_decode_ring_gb300 import kvc
+        from kv_cache_decode_ring_gb300 import workloads as wl
+        self.torch, self.kvc = torch, kvc
+        self.w = w = wl.full_cache_mha()
+        self.ctx = w.extra["context"]
+        self.cache = kvc.Cache.from_workload(w, device=device)
+        k, v = w.prefill_chunk(0, self.ctx, device=device)
+        self.cache.append_rows(k, v)
+        del k, v
+        steps = [w.step_qkv(s, device=device) for s in range(self.CYCLE)]
+        self.q = [s[0] for s in steps]
+        self.k = [s[1] for s in steps]
+        self.v = [s[2] for s in steps]
+        self.out = torch.empty_like(self.q[0])
+        self.i = 0
+        torch.cuda.synchronize()
+        self.cuts = [self.ctx] * w.batch
+
+    def units(self, i):
+        """KV bytes read by the decode of global step i (context ctx + i mod CYCLE + 1)."""
+        n = self.ctx + (i % self.CYCLE) + 1
+        return kv_bytes_per_step([n] * self.w.batch, self.w.n_kv_heads, self.w.head_dim)
+
+    def io_bytes(self):
+        w = self.w
+        return (2 * w.batch * w.n_q_heads * w.head_dim) * 2      # q read + out write (bf16)
+
+    def launches_per_step(self):
+        return 3                                                 # append, split-K decode, combine
+
+    def step(self, i, ev=None):
+        j = i % self.CYCLE
+        extra = 0
+        if j == 0 and i > 0:
+            self.cache.trim(self.cuts)
+            extra = 1
+        self.cache.append(self.k[j], self.v[j])
+        if ev is not None:
+            ev[0].record()
+        self.cache.decode(self.q[j], self.out)
+        if ev is not None:
+            ev[1].record()
+        return extra
+
+    # end-to-end: host inputs, copies inside the timing
+    def e2e_setup(self):
+        torch = self.torch
+        self.hq = [t.cpu().pin_memory() for t in self.q]
+        self.hk = [t.cpu().pin_memory() for t in self.k]
+        self.hv = [t.cpu().pin_memory() for t in self.v]
+        self.hout = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+        self.dq = torch.empty_like(self.q[0])
+        self.dk = torch.empty_like(self.k[0])
+        self.dv = torch.empty_like(self.v[0])
+        return sum(t.numel() * t.element_size() for t in (self.hq[0], self.hk[0], self.hv[0])), \
+            self.hout.numel() * self.hout.element_size()
+
+    def e2e_step(self, i):
+        j = i % self.CYCLE
+        if j == 0 and i > 0:
+            self.cache.trim(self.cuts)
+        self.dq.copy_(self.hq[j], non_blocking=True)
+        self.dk.copy_(self.hk[j], non_blocking=True)
+        self.dv.copy_(self.hv[j], non_blocking=True)
+        self.cache.append(self.dk, self.dv)
+        self.cache.decode(self.dq, self.out)
+        self.hout.copy_(self.out, non_blocking=True)
+
+    def reset(self):
+        self.cache.trim(self.cuts)
+        self.torch.cuda.synchronize()
+
+    def config(self):
+        w = self.w
+        return {"workload": w.name, "batch": w.batch, "n_q_heads": w.n_q_heads, "n_kv_heads": w.n_kv_heads,
+                "head_dim": w.head_dim, "layout": "contiguous", "max_seq_len": w.capacity,
+                "context": "%d + step (cycles %d..%d keys)" % (self.ctx, self.ctx + 1, self.ctx + self.CYCLE),
+                "l2": "inputs larger than L2: %.2f GB of K/V read per step vs 129 MB L2" % (self.units(0) / 1e9)}
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+def oracle_sample(w, seconds: float, threads: int, heads_per_call=None):
+    """Time the oracle's fp64 attention (C, OpenMP) on (request, KV head) problems of the
+    workload at context ctx+1; returns (GB/s of KV bytes, seconds, problems, description)."""
+    import numpy as np
+    from kv_cache_decode_ring_gb300 import workloads as wl
+    from oracle import numerics as nm
+    ctx = w.extra.get("context", 4096) + 1
+    d, g = w.head_dim, w.n_q_heads // w.n_kv_heads
+    nprob = heads_per_call or max(threads, 8)
+    k = wl.as_numpy(w.keys((nprob, ctx, d), "cpu-sample"))
+    v = wl.as_numpy(w.values((nprob, ctx, d), "cpu-sample"))
+    q = wl.as_numpy(w.queries((nprob, g, d), "cpu-sample"))
+    qf = nm.bf16_to_f32(q).astype(np.float64)
+    ks = [k[i] for i in range(nprob)]
+    vs = [v[i] for i in range(nprob)]
+    done, t0 = 0, time.perf_counter()
+    while True:
+        nm.attend_many([qf[i] for i in range(nprob)], ks, vs, [ctx - 1] * nprob, 0, None, nthreads=threads)
+        done += nprob
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    by = done * ctx * d * 2 * 2
+    desc = ("%d (request, KV head) problems of %d query heads at %d keys, d=%d, bf16 inputs, fp64 math"
+            % (done, g, ctx, d))
+    return by / el / 1e9, el, done, desc
+
+
+# ----------------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="kvc", choices=["kvc", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        return run_reference(args, world, threads)
+
+    import torch
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+
+    from __graft_entry__ import build
+    build()
+    bench = FullCacheBench("cuda")
+    peak, peak_kind = hbm_peak()
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    # warm-up
+    launches = 0
+    for i in range(args.warmup):
+        bench.step(i)
+    bench.reset()
+
+    # timed region
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    t0e, t1e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(gpu_index(local_rank))
+    sampler.start()
+    time.sleep(0.3)
+    barrier()
+    wall0 = time.perf_counter()
+    t0e.record()
+    units = 0
+    for i in range(K):
+        launches += bench.launches_per_step() + bench.step(i, ev[i])
+        units += bench.units(i)
+    t1e.record()
+    barrier()
+    wall = time.perf_counter() - wall0
+    sampler.stop()
+    ms_total = t0e.elapsed_time(t1e)
+    attn_ms = [a.elapsed_time(b) for a, b in ev]
+    times = torch.tensor([ms_total], device="cuda", dtype=torch.float64)
+    tot_units = torch.tensor([float(units)], device="cuda", dtype=torch.float64)
+    if dist is not None:
+        dist.all_reduce(times, op=dist.ReduceOp.MAX)
+        dist.all_reduce(tot_units, op=dist.ReduceOp.SUM)
+    ms_total = float(times.item())
+    value = float(tot_units.item()) / (ms_total / 1e3) / 1e9
+    steps_per_s = K / (ms_total / 1e3)
+
+    # roofline of the decode-attention call
+    attn_bytes = sum(bench.units(i) + bench.io_bytes() for i in range(K)) / K
+    attn_avg_ms = sum(attn_ms) / len(attn_ms)
+    achieved = attn_bytes / (attn_avg_ms / 1e3) / 1e9
+
+    # end-to-end through the ABI with host buffers
+    e2e = None
+    if not args.no_e2e:
+        bench.reset()
+        hb, db = bench.e2e_setup()
+        Ke = min(K, 400)
+        for i in range(3):
+            bench.e2e_step(i)
+        bench.reset()
+        barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        eu = 0
+        for i in range(Ke):
+            bench.e2e_step(i)
+            eu += bench.units(i)
+        b.record()
+        barrier()
+        ems = torch.tensor([a.elapsed_time(b)], device="cuda", dtype=torch.float64)
+        eut = torch.tensor([float(eu)], device="cuda", dtype=torch.float64)
+        if dist is not None:
+            dist.all_reduce(ems, op=dist.ReduceOp.MAX)
+            dist.all_reduce(eut, op=dist.ReduceOp.SUM)
+        e2e = {"value": round(float(eut.item()) / (float(ems.item()) / 1e3) / 1e9, 2), "unit": "GB/s",
+               "h2d_bytes_per_step": hb, "d2h_bytes_per_step": db, "steps": Ke}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        gbps, el, nprob, desc = oracle_sample(bench.w, args.cpu_seconds, threads)
+        cpu = {"value": round(gbps, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+               "sample": desc + ", %.1f s" % el}
+
+    clocks = sampler.summary()
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": round(ms_total / K, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "steps_per_s": round(steps_per_s, 2), "hbm_frac_of_" + peak_kind: round(value / peak, 4),
+            "config": bench.config(),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": None,
+                         "kernel": "kvc_decode_attn (split-K decode + combine)", "peak_kind": peak_kind,
+                         "bytes_per_launch": int(attn_bytes), "avg_launch_ms": round(attn_avg_ms, 5)},
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
+            "wall_s": round(wall, 3),
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def run_reference(args, world, threads):
+    from kv_cache_decode_ring_gb300 import workloads as wl
+    from oracle import numerics as nm
+    nm.build()
+    w = wl.full_cache_mha()
+    # size each step so the whole run stays within about a minute; at most one full
+    # decode step (B x Hkv problems) per step, drawn from a pool of 64 distinct problems
+    budget = 60.0 / (args.steps + args.warmup)
+    _, el, n, _ = oracle_sample(w, 0.0, threads, heads_per_call=threads)
+    per_prob = el / max(n, 1)
+    per_step = max(1, min(w.batch * w.n_kv_heads, int(budget / per_prob)))
+    import numpy as np
+    ctx = w.extra["context"] + 1
+    d, g = w.head_dim, w.n_q_heads // w.n_kv_heads
+    pool = min(64, per_step)
+    k = wl.as_numpy(w.keys((pool, ctx, d), "ref-sample"))
+    v = wl.as_numpy(w.values((pool, ctx, d), "ref-sample"))
+    q = nm.bf16_to_f32(wl.as_numpy(w.queries((pool, g, d), "ref-sample"))).astype(np.float64)
+    ks = [k[i % pool] for i in range(per_step)]
+    vs = [v[i % pool] for i in range(per_step)]
+    qs = [q[i % pool] for i in range(per_step)]
+    for _ in range(args.warmup):
+        nm.attend_many(qs, ks, vs, [ctx - 1] * per_step, 0, None, nthreads=threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        nm.attend_many(qs, ks, vs, [ctx - 1] * per_step, 0, None, nthreads=threads)
+    el = time.perf_counter() - t0
+    by = args.steps * per_step * ctx * d * 2 * 2
+    value = by / el / 1e9
+    full_step = kv_bytes_per_step([ctx] * w.batch, w.n_kv_heads, d)
+    sample = ("each step: %d of the %d (request, KV head) problems of one decode step at %d keys (fp64 oracle)"
+              % (per_step, w.batch * w.n_kv_heads, ctx))
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "steps_per_s": round(value * 1e9 / full_step, 6),
+            "config": {"workload": w.name, "batch": w.batch, "n_q_heads": w.n_q_heads, "n_kv_heads": w.n_kv_heads,
+                       "head_dim": d, "context": ctx},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

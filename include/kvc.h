@@ -1,0 +1,202 @@
+/*
+ * kvc.h -- C ABI of libkvc, a single-GPU (GB300, sm_103a) library for one
+ * autoregressive decode step over a KV cache.
+ *
+ * Sources of the operations, cited by page title and section:
+ *   [LEAN]    "用Lean4形式化验证滑动窗口KV Cache的正确性" (framerc.cn/news/4505248)
+ *   [PREFIX]  "LLM 機制實驗（五）：改了歷史，能否只重算變化的後綴？"
+ *             (huhohoo.com/zh-TW/docs/llm/longest-prefix-reuse)
+ *   [LOOP]    "KV Cache 自回归生成推理（增量更新与状态拼接）" (airsota.com/?p=549)
+ *   [WITCERT] "WitCert: Sound Runtime Risk Observability and Gating for
+ *             KV-Cache Quantization" (agifrontier.github.io tutorial)
+ *
+ * Conventions
+ *  - Ownership: the caller owns every device buffer (the cache state, inputs,
+ *    outputs) and the stream.  The library owns only the small host handle.
+ *    kvc_create() and kvc_destroy() neither allocate nor free device memory.
+ *  - Pointers named d_* are device pointers, h_* host pointers.  Device
+ *    inputs must be 16-byte aligned and densely packed in the stated layout.
+ *  - Streams: kvc_stream_t is a cudaStream_t (NULL = the legacy default
+ *    stream).  Compute calls only enqueue work and return; none waits for the
+ *    GPU, except kvc_create (uploads tables), kvc_export and
+ *    kvc_device_status (read back).  One handle serves one stream at a time:
+ *    calls on one handle from different streams race on its state.
+ *  - Element types: KVC_F32 = IEEE fp32, KVC_BF16 = bfloat16.  q, k, v and
+ *    out all use the cache dtype.
+ *  - Positions are absolute, 0-based, signed 32-bit; -1 marks an empty slot.
+ *  - Errors: every entry point returns a KVC_* status.  Arguments are checked
+ *    on the host before anything is enqueued; a failed call changes nothing.
+ *    Kernels also check their own bounds and set a sticky device error word
+ *    (read by kvc_device_status) instead of writing out of bounds.
+ */
+#ifndef KVC_H
+#define KVC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct kvc_handle* kvc_t;
+typedef void* kvc_stream_t; /* a cudaStream_t */
+
+/* ---- status codes ---------------------------------------------------- */
+#define KVC_OK 0
+#define KVC_ERR_ARG 1          /* null pointer, bad shape/dtype/size, call out of order */
+#define KVC_ERR_CAPACITY 2     /* contiguous cache full: position >= max_seq_len
+                                  ([LOOP] §三 "assert pos < max_seq_len"), or a
+                                  position beyond the RoPE table */
+#define KVC_ERR_EVICTED 3      /* trim needs rows the cache no longer holds exactly:
+                                  evicted from a ring ([PREFIX] "為什麼滑窗部分命中必須回退")
+                                  or already folded into an INT8 block */
+#define KVC_ERR_CUDA 4         /* a CUDA runtime call failed */
+#define KVC_ERR_UNSUPPORTED 5  /* valid request this build does not implement */
+#define KVC_ERR_DEVICE 6       /* a kernel flagged an error (see kvc_device_status) */
+
+/* ---- configuration --------------------------------------------------- */
+enum { KVC_F32 = 0, KVC_BF16 = 1 };
+enum { KVC_CONTIGUOUS = 0, KVC_RING = 1 };
+enum { KVC_QUANT_NONE = 0, KVC_QUANT_INT8 = 1 };
+
+typedef struct {
+    int32_t dtype;        /* KVC_F32 or KVC_BF16 */
+    int32_t layout;       /* KVC_CONTIGUOUS: slot = position, capacity = max_seq_len
+                             ([LOOP] §三, preallocated (B, H, max_S, D) buffers);
+                             KVC_RING: slot = position mod W, capacity = W
+                             ([LEAN] §3.4 ring buffer, §2.3 lastWindow) */
+    int32_t kv_quant;     /* KVC_QUANT_NONE, or KVC_QUANT_INT8 (bf16 contiguous
+                             caches only; [WITCERT]) */
+    int32_t batch;        /* B >= 1 requests */
+    int32_t n_q_heads;    /* Hq >= 1 */
+    int32_t n_kv_heads;   /* Hkv >= 1, Hq % Hkv == 0; query head h reads KV head h / (Hq/Hkv) */
+    int32_t head_dim;     /* d: even, 2..256; INT8 needs d % 16 == 0 */
+    int32_t capacity;     /* slots per (request, KV head); INT8 needs capacity % 16 == 0 */
+    int32_t window;       /* attention window W: 0 = full history (contiguous only);
+                             a ring must use 0 or its capacity.  The query at
+                             position t sees positions [max(0, t-W+1), t] ([LEAN] §2.1). */
+    int32_t max_position; /* RoPE table length; every position must stay below it.
+                             0 = capacity (contiguous).  Required for a ring with RoPE. */
+    float rope_base;      /* rotary base (e.g. 10000); 0 = keys and queries not rotated */
+    int32_t max_chunk;    /* largest n for kvc_chunk_attn (sizes its workspace) */
+} kvc_config;
+
+/* Bytes of the device state buffer for `cfg` (cache rows, positions,
+ * next_position, RoPE table, INT8 arrays, split-K workspace).
+ * Returns KVC_ERR_ARG for an invalid configuration. */
+int kvc_state_bytes(const kvc_config* cfg, size_t* bytes);
+
+/* Bind a handle to a caller-allocated device buffer of at least
+ * kvc_state_bytes() bytes (256-byte aligned) on the current device.  Sets
+ * every position to -1 and every next_position to 0, and uploads the RoPE
+ * table; waits for `stream`.  The buffer must outlive the handle. */
+int kvc_create(const kvc_config* cfg, void* d_state, size_t bytes, kvc_stream_t stream,
+               kvc_t* out);
+
+/* Release the host handle (the device buffer stays the caller's). */
+int kvc_destroy(kvc_t h);
+
+/* Append one token to every request ([LOOP] §三 step: write cache[pos];
+ * [LEAN] §3.3 step).  d_k, d_v: [B][Hkv][d], keys not yet rotated.  For each
+ * request: pos = next_position; the key is rotated at pos (if RoPE) and
+ * rounded to the cache dtype; k, v go to slot pos (contiguous) or pos mod W
+ * (ring); positions[slot] = pos; next_position = pos + 1.  INT8: the row goes
+ * to the request's exact tail block; the 16th row of a block quantizes the
+ * block and writes its witnesses.  KVC_ERR_CAPACITY if a contiguous cache is
+ * full (nothing is written). */
+int kvc_append(kvc_t h, const void* d_k, const void* d_v, kvc_stream_t stream);
+
+/* Append up to n tokens per request, in order, from d_k, d_v [B][Hkv][n][d]
+ * (prefill).  h_counts (host, B entries, NULL = n for all) limits request b to
+ * its first h_counts[b] rows.  Same per-row semantics as kvc_append; on a ring
+ * only the rows that stay resident are written. */
+int kvc_append_rows(kvc_t h, const void* d_k, const void* d_v, int32_t n,
+                    const int32_t* h_counts, kvc_stream_t stream);
+
+/* Decode attention for the newest token of every request ([LOOP] §三 step;
+ * [LEAN] §2.1).  d_q: [B][Hq][d] not yet rotated; the query sits at
+ * t = next_position - 1, is rotated at t (if RoPE) in fp32, and attends to the
+ * cached positions [max(0, t-W+1), t]:
+ *     out = softmax(q . K^T / sqrt(d)) . V            d_out: [B][Hq][d]
+ * evaluated as split-K flash decoding with an online softmax and a cross-split
+ * combine, fp32 accumulation.  Needs at least one cached token per request, and
+ * on a ring an append after any trim.
+ * INT8 caches also return, per (request, query head), the witness bound
+ * ([WITCERT] "频带酉性与双层证书"):
+ *     c_t = (1/sqrt d) sum_b ||q_b|| w_{t,b}   for every cached token in the window,
+ *     d_cmax[b][h] = max_t c_t,  d_tanh[b][h] >= tanh(max_t c_t),
+ * computed with upward rounding so that c_t >= |q . r_t| / sqrt(d) for the
+ * stored residual r_t, hence attention total variation <= d_tanh
+ * ([WITCERT] "为什么在线监控 KV 误差如此困难？").  d_ct (nullable) receives c_t
+ * as [B][Hq][capacity] indexed by slot (slots outside the window untouched).
+ * For non-quantized caches d_cmax/d_tanh (nullable) receive 0 and d_ct must
+ * be NULL. */
+int kvc_decode_attn(kvc_t h, const void* d_q, void* d_out, float* d_cmax, float* d_tanh,
+                    float* d_ct, kvc_stream_t stream);
+
+/* Continue every request from next_position = h_cut[b] ([PREFIX]
+ * "哪些東西必須一起裁剪": keep k[:cut], v[:cut], positions[:cut]; next_position
+ * = cut).  h_cut: host, B entries, 0 <= cut <= next_position.  Rows at
+ * positions >= cut are dropped (positions set to -1).  A ring accepts the cut
+ * only if every position the next query needs is still resident, i.e. with
+ * lo = max(0, cut-W+1): lo == cut or lo >= max(0, next_position-W); an INT8
+ * cache only if no quantized block is split (cut % 16 == 0 or cut within the
+ * exact tail).  Otherwise KVC_ERR_EVICTED and nothing changes. */
+int kvc_trim(kvc_t h, const int32_t* h_cut, kvc_stream_t stream);
+
+/* Chunked causal suffix attention after a trim ([PREFIX] model.chunk(tokens[cut:],
+ * cache)).  Appends n rows per request at positions cut .. cut+n-1 (as
+ * kvc_append_rows) and answers every suffix query i at p = cut + i over
+ * positions [max(0, p-W+1), p]:
+ *     d_q [B][n][Hq][d], d_k, d_v [B][n][Hkv][d]  ->  d_out [B][n][Hq][d].
+ * Row i equals what kvc_decode_attn returns for that query after appending
+ * rows 0..i.  Contiguous bf16 caches without INT8; n <= max_chunk. */
+int kvc_chunk_attn(kvc_t h, const void* d_q, const void* d_k, const void* d_v, int32_t n,
+                   void* d_out, kvc_stream_t stream);
+
+/* Bit-exact readback of one state array for tests and debug asserts
+ * ([LEAN] §6.3: export the cache and compare it with the specification).
+ * Copies into h_dst (exactly kvc_export_bytes() bytes) and waits for `stream`. */
+enum {
+    KVC_EXPORT_K = 0,             /* [B][Hkv][capacity][d] cache dtype (non-INT8) */
+    KVC_EXPORT_V = 1,
+    KVC_EXPORT_POSITIONS = 2,     /* int32 [B][capacity] */
+    KVC_EXPORT_NEXT_POSITION = 3, /* int32 [B] */
+    KVC_EXPORT_KQ = 4,            /* int8 [B][Hkv][capacity][d]          (INT8) */
+    KVC_EXPORT_VQ = 5,
+    KVC_EXPORT_SK = 6,            /* fp32 [B][Hkv][capacity/16]           (INT8) */
+    KVC_EXPORT_SV = 7,
+    KVC_EXPORT_WITNESS = 8,       /* fp16 [B][Hkv][capacity][16]          (INT8) */
+    KVC_EXPORT_KTAIL = 9,         /* bf16 [B][Hkv][16][d] exact tail rows (INT8) */
+    KVC_EXPORT_VTAIL = 10
+};
+int kvc_export_bytes(kvc_t h, int32_t which, size_t* bytes);
+int kvc_export(kvc_t h, int32_t which, void* h_dst, size_t bytes, kvc_stream_t stream);
+
+/* Host mirror of next_position (B entries), kept by the handle.  Enqueued but
+ * unexecuted work is already counted. */
+int kvc_next_positions(kvc_t h, int32_t* h_out);
+
+/* Waits for `stream`, then returns the device error word (0 = none; bit 0: a
+ * kernel met a position outside the cache or RoPE table; bit 1: a bounded wait
+ * gave up) and clears it. */
+int kvc_device_status(kvc_t h, kvc_stream_t stream, int32_t* h_status);
+
+/* Host only.  Rows of a stored prefill that a new query can reuse ([PREFIX]
+ * "先看一次歷史編輯", "查詢流程與快取所有權", "為什麼滑窗部分命中必須回退"):
+ * cut = length of the longest contiguous common prefix of old and new IDs,
+ * at most n_new - 1 (the last query token is always recomputed).  With ring != 0
+ * only a full match of the cached prefix followed by new tokens is reused
+ * (cut = n_old), otherwise cut = 0.  KVC_ERR_ARG if n_new < 1, n_old < 0 or a
+ * pointer is NULL where its count is positive. */
+int kvc_prefix_cut(const int64_t* h_old_ids, int32_t n_old, const int64_t* h_new_ids,
+                   int32_t n_new, int32_t ring, int32_t* h_cut);
+
+/* Static description of a status code. */
+const char* kvc_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVC_H */

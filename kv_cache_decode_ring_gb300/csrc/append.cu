@@ -1,0 +1,362 @@
+// append.cu -- cache writes: append one token or many rows, trim, INT8 block
+// quantization with residual witnesses.
+//
+// [LOOP] §三 "KVCacheManager.step": write k_t, v_t at cache[:, :, pos]; pos < max_seq_len.
+// [LEAN] §3.3 step / §3.4 ringToList: a ring of W slots, slot = position mod W,
+//        each slot keeps its absolute position (§3.2 KV Cell).
+// [PREFIX] "哪些東西必須一起裁剪": trim keeps rows [:cut] and sets next_position = cut.
+// [WITCERT] "频带酉性与双层证书": per-token, per-band residual norms w_{t,b} (16 x fp16);
+//        "SGLang 生产级落地与闭环门控修复": per-block scales; the write kernel
+//        quantizes and records the band norms.
+#include "kvc_internal.h"
+
+namespace kvc {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kMaxGroup = 1024;  // requests per launch when per-request values ride in params
+
+struct Group {
+    int32_t val[kMaxGroup];  // counts (append) or cuts (trim)
+    int b0, nb;
+};
+
+__device__ __forceinline__ void flag(uint32_t* hdr, uint32_t bit) { atomicOr(hdr, bit); }
+
+__device__ __forceinline__ bool position_ok(const AppendArgs& a, long long p) {
+    if (p < 0 || p > 0x7fffffffLL) return false;
+    if (!a.ring && p >= a.S) return false;
+    if (a.rope && p >= a.P) return false;
+    return true;
+}
+
+// Stored value of element pair (2i, 2i+1) of a key row at position p.
+__device__ __forceinline__ void key_pair(const AppendArgs& a, const void* src, size_t off, int i,
+                                         int p, float& y0, float& y1) {
+    float x0 = ld_elem(src, off + 2 * i, a.bf16), x1 = ld_elem(src, off + 2 * i + 1, a.bf16);
+    if (a.rope) {
+        rope_pair(x0, x1, a.rope[(size_t)p * (a.d / 2) + i], y0, y1);
+    } else {
+        y0 = x0; y1 = x1;
+    }
+}
+
+__device__ __forceinline__ void store_pair(void* dst, size_t off, float y0, float y1, int bf16) {
+    if (bf16) {
+        __nv_bfloat162 t;
+        t.x = __float2bfloat16_rn(y0);
+        t.y = __float2bfloat16_rn(y1);
+        *reinterpret_cast<__nv_bfloat162*>(static_cast<__nv_bfloat16*>(dst) + off) = t;
+    } else {
+        *reinterpret_cast<float2*>(static_cast<float*>(dst) + off) = make_float2(y0, y1);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// INT8: quantize one 16-row block held in shared memory (fp32 copies of the
+// exact bf16 values) and write codes, scales and witnesses.  All threads of the
+// CTA take part.  s = amax/127 (IEEE division); code = clamp(rint(x/s), +-127);
+// residual r = x - code*s is exact in fp32 (|r| <= s/2 on the grid of s), so one
+// fma computes it exactly; band norms are summed in index order with every
+// operation rounded toward +inf and stored as fp16 rounded up, so the witness
+// is never below the true residual norm.
+// ---------------------------------------------------------------------------
+__device__ void quantize_block(const AppendArgs& a, const float* sK, const float* sV, float* red,
+                               int b, int h, int blk) {
+    const int d = a.d, n = kQBlock * d;
+    float mk = 0.f, mv = 0.f;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        mk = fmaxf(mk, fabsf(sK[i]));
+        mv = fmaxf(mv, fabsf(sV[i]));
+    }
+    for (int o = 16; o; o >>= 1) {
+        mk = fmaxf(mk, __shfl_xor_sync(0xffffffffu, mk, o));
+        mv = fmaxf(mv, __shfl_xor_sync(0xffffffffu, mv, o));
+    }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    __syncthreads();
+    if (lane == 0) { red[warp] = mk; red[32 + warp] = mv; }
+    __syncthreads();
+    mk = 0.f; mv = 0.f;
+    for (int w = 0; w < nw; ++w) { mk = fmaxf(mk, red[w]); mv = fmaxf(mv, red[32 + w]); }
+    const float s_k = __fdiv_rn(mk, 127.0f), s_v = __fdiv_rn(mv, 127.0f);
+    const size_t bh = (size_t)b * a.Hkv + h;
+    const size_t row0 = bh * a.S + (size_t)blk * kQBlock;
+    if (threadIdx.x == 0) {
+        a.sk[bh * (a.S / kQBlock) + blk] = s_k;
+        a.sv[bh * (a.S / kQBlock) + blk] = s_v;
+    }
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        int ck = 0, cv = 0;
+        if (s_k != 0.f) ck = max(-127, min(127, __float2int_rn(__fdiv_rn(sK[i], s_k))));
+        if (s_v != 0.f) cv = max(-127, min(127, __float2int_rn(__fdiv_rn(sV[i], s_v))));
+        a.kq[row0 * d + i] = (int8_t)ck;
+        a.vq[row0 * d + i] = (int8_t)cv;
+    }
+    // witnesses: one thread per (row, band)
+    const int bw = d / kBands;
+    for (int rb = threadIdx.x; rb < kQBlock * kBands; rb += blockDim.x) {
+        const int r = rb / kBands, band = rb % kBands;
+        float acc = 0.f;
+        for (int j = band * bw; j < (band + 1) * bw; ++j) {
+            const float x = sK[r * d + j];
+            int c = 0;
+            if (s_k != 0.f) c = max(-127, min(127, __float2int_rn(__fdiv_rn(x, s_k))));
+            const float res = __fmaf_rn(-(float)c, s_k, x);   // exact
+            acc = __fadd_ru(acc, __fmul_ru(res, res));
+        }
+        a.wit[(row0 + r) * kBands + band] = __float2half_ru(__fsqrt_ru(acc));
+    }
+}
+
+// One token per request.  CTA b writes every KV head of request b, then
+// advances next_position[b] (one writer per request: no cross-CTA race).
+__global__ void __launch_bounds__(kThreads) append_token_kernel(const AppendArgs a) {
+    extern __shared__ float smem[];
+    const int b = blockIdx.x;
+    const int p = a.next_pos[b];
+    if (!position_ok(a, p)) {
+        if (threadIdx.x == 0) flag(a.hdr, kErrPosition);
+        return;
+    }
+    const int d = a.d, half = d / 2;
+    const int slot = a.ring ? p % a.S : p;
+    if (!a.int8) {
+        for (int idx = threadIdx.x; idx < a.Hkv * half; idx += blockDim.x) {
+            const int h = idx / half, i = idx % half;
+            const size_t src = ((size_t)b * a.Hkv + h) * d;
+            const size_t dst = (((size_t)b * a.Hkv + h) * a.S + slot) * d;
+            float y0, y1;
+            key_pair(a, a.k, src, i, p, y0, y1);
+            store_pair(a.kc, dst + 2 * i, y0, y1, a.bf16);
+            store_pair(a.vc, dst + 2 * i, ld_elem(a.v, src + 2 * i, a.bf16),
+                       ld_elem(a.v, src + 2 * i + 1, a.bf16), a.bf16);
+        }
+    } else {
+        // INT8 tier (bf16 only): the row joins the exact tail; the 16th row of a
+        // block quantizes the whole block.
+        float* sK = smem;
+        float* sV = smem + kQBlock * d;
+        float* red = smem + 2 * kQBlock * d;
+        const int tslot = p % kQBlock;
+        const bool complete = tslot == kQBlock - 1;
+        for (int h = 0; h < a.Hkv; ++h) {
+            const size_t src = ((size_t)b * a.Hkv + h) * d;
+            const size_t tail = ((size_t)b * a.Hkv + h) * kQBlock * d;
+            for (int i = threadIdx.x; i < half; i += blockDim.x) {
+                float y0, y1;
+                key_pair(a, a.k, src, i, p, y0, y1);
+                const __nv_bfloat16 k0 = __float2bfloat16_rn(y0), k1 = __float2bfloat16_rn(y1);
+                const __nv_bfloat16 v0 = __float2bfloat16_rn(ld_elem(a.v, src + 2 * i, 1));
+                const __nv_bfloat16 v1 = __float2bfloat16_rn(ld_elem(a.v, src + 2 * i + 1, 1));
+                a.ktail[tail + (size_t)tslot * d + 2 * i] = k0;
+                a.ktail[tail + (size_t)tslot * d + 2 * i + 1] = k1;
+                a.vtail[tail + (size_t)tslot * d + 2 * i] = v0;
+                a.vtail[tail + (size_t)tslot * d + 2 * i + 1] = v1;
+                if (complete) {
+                    sK[tslot * d + 2 * i] = __bfloat162float(k0);
+                    sK[tslot * d + 2 * i + 1] = __bfloat162float(k1);
+                    sV[tslot * d + 2 * i] = __bfloat162float(v0);
+                    sV[tslot * d + 2 * i + 1] = __bfloat162float(v1);
+                }
+            }
+            if (complete) {
+                for (int i = threadIdx.x; i < (kQBlock - 1) * d; i += blockDim.x) {
+                    sK[i] = __bfloat162float(a.ktail[tail + i]);
+                    sV[i] = __bfloat162float(a.vtail[tail + i]);
+                }
+                __syncthreads();
+                quantize_block(a, sK, sV, red, b, h, p / kQBlock);
+                __syncthreads();
+            }
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        a.pos[(size_t)b * a.S + slot] = p;
+        a.next_pos[b] = p + 1;
+    }
+}
+
+// Many rows per request (non-INT8).  CTA (row tile, KV head, request) writes
+// rows; next_position is only read here and advanced by advance_kernel.
+__global__ void __launch_bounds__(kThreads) append_rows_kernel(const AppendArgs a, const Group g) {
+    const int bi = blockIdx.z, b = g.b0 + bi, h = blockIdx.y;
+    const int cnt = g.val[bi];
+    const int np = a.next_pos[b];
+    const int d = a.d, half = d / 2;
+    const int rows_per_cta = kThreads / half > 0 ? kThreads / half : 1;
+    const int r = blockIdx.x * rows_per_cta + threadIdx.x / half;
+    const int i = threadIdx.x % half;
+    if (threadIdx.x >= rows_per_cta * half || r >= cnt) return;
+    if (a.ring && r < cnt - a.S) return;            // overwritten later in this call
+    const long long p = (long long)np + r;
+    if (!position_ok(a, p)) {
+        flag(a.hdr, kErrPosition);
+        return;
+    }
+    const int slot = a.ring ? (int)(p % a.S) : (int)p;
+    const size_t src = (((size_t)b * a.Hkv + h) * a.n + r) * d;
+    const size_t dst = (((size_t)b * a.Hkv + h) * a.S + slot) * d;
+    float y0, y1;
+    key_pair(a, a.k, src, i, (int)p, y0, y1);
+    store_pair(a.kc, dst + 2 * i, y0, y1, a.bf16);
+    store_pair(a.vc, dst + 2 * i, ld_elem(a.v, src + 2 * i, a.bf16), ld_elem(a.v, src + 2 * i + 1, a.bf16),
+               a.bf16);
+    if (h == 0 && i == 0) a.pos[(size_t)b * a.S + slot] = (int)p;
+}
+
+// INT8 rows, phase 1: every 16-position block that the new rows complete.
+// CTA (block index from floor(np/16), KV head, request).  Rows below np come
+// from the tail, the rest from the input.  Phase 2 (tail_kernel) writes the
+// rows of a still-incomplete last block after this kernel has read the tail.
+__global__ void __launch_bounds__(kThreads) quantize_rows_kernel(const AppendArgs a, const Group g) {
+    extern __shared__ float smem[];
+    const int bi = blockIdx.z, b = g.b0 + bi, h = blockIdx.y;
+    const int cnt = g.val[bi];
+    const int np = a.next_pos[b];
+    const int blk = np / kQBlock + blockIdx.x;
+    const int p0 = blk * kQBlock;
+    if (p0 + kQBlock > np + cnt) return;             // block not completed by this call
+    if (!position_ok(a, (long long)p0 + kQBlock - 1)) {
+        if (threadIdx.x == 0) flag(a.hdr, kErrPosition);
+        return;
+    }
+    const int d = a.d, half = d / 2;
+    float* sK = smem;
+    float* sV = smem + kQBlock * d;
+    float* red = smem + 2 * kQBlock * d;
+    const size_t tail = ((size_t)b * a.Hkv + h) * kQBlock * d;
+    for (int idx = threadIdx.x; idx < kQBlock * half; idx += blockDim.x) {
+        const int r = idx / half, i = idx % half, p = p0 + r;
+        float k0, k1, v0, v1;
+        if (p < np) {
+            k0 = __bfloat162float(a.ktail[tail + (size_t)r * d + 2 * i]);
+            k1 = __bfloat162float(a.ktail[tail + (size_t)r * d + 2 * i + 1]);
+            v0 = __bfloat162float(a.vtail[tail + (size_t)r * d + 2 * i]);
+            v1 = __bfloat162float(a.vtail[tail + (size_t)r * d + 2 * i + 1]);
+        } else {
+            const size_t src = (((size_t)b * a.Hkv + h) * a.n + (p - np)) * d;
+            key_pair(a, a.k, src, i, p, k0, k1);
+            k0 = __bfloat162float(__float2bfloat16_rn(k0));
+            k1 = __bfloat162float(__float2bfloat16_rn(k1));
+            v0 = ld_elem(a.v, src + 2 * i, 1);
+            v1 = ld_elem(a.v, src + 2 * i + 1, 1);
+        }
+        sK[r * d + 2 * i] = k0; sK[r * d + 2 * i + 1] = k1;
+        sV[r * d + 2 * i] = v0; sV[r * d + 2 * i + 1] = v1;
+    }
+    __syncthreads();
+    quantize_block(a, sK, sV, red, b, h, blk);
+    if (h == 0)
+        for (int r = threadIdx.x; r < kQBlock; r += blockDim.x) a.pos[(size_t)b * a.S + p0 + r] = p0 + r;
+}
+
+// INT8 rows, phase 2 (one CTA per request): rows of the last, incomplete block
+// go to the exact tail; then next_position advances.
+__global__ void __launch_bounds__(kThreads) tail_kernel(const AppendArgs a, const Group g) {
+    const int bi = blockIdx.x, b = g.b0 + bi;
+    const int cnt = g.val[bi];
+    const int np = a.next_pos[b];
+    const int end = np + cnt;
+    const int first = max(np, (end / kQBlock) * kQBlock);   // rows of the incomplete block
+    const int d = a.d, half = d / 2;
+    for (int idx = threadIdx.x; idx < a.Hkv * (end - first) * half; idx += blockDim.x) {
+        const int h = idx / ((end - first) * half);
+        const int rem = idx % ((end - first) * half);
+        const int p = first + rem / half, i = rem % half;
+        if (!position_ok(a, p)) { flag(a.hdr, kErrPosition); continue; }
+        const size_t src = (((size_t)b * a.Hkv + h) * a.n + (p - np)) * d;
+        const size_t tail = (((size_t)b * a.Hkv + h) * kQBlock + p % kQBlock) * d;
+        float k0, k1;
+        key_pair(a, a.k, src, i, p, k0, k1);
+        a.ktail[tail + 2 * i] = __float2bfloat16_rn(k0);
+        a.ktail[tail + 2 * i + 1] = __float2bfloat16_rn(k1);
+        a.vtail[tail + 2 * i] = __float2bfloat16_rn(ld_elem(a.v, src + 2 * i, 1));
+        a.vtail[tail + 2 * i + 1] = __float2bfloat16_rn(ld_elem(a.v, src + 2 * i + 1, 1));
+        if (h == 0 && i == 0 && p < a.S) a.pos[(size_t)b * a.S + p] = p;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) a.next_pos[b] = end;
+}
+
+__global__ void advance_kernel(int32_t* next_pos, const Group g) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < g.nb) next_pos[g.b0 + i] += g.val[i];
+}
+
+// Trim: CTA per request.  Contiguous: slots [cut, old next_position) become
+// empty.  Ring: every slot holding a position >= cut becomes empty.
+__global__ void trim_kernel(int32_t* next_pos, int32_t* pos, const Group g, int S, int ring) {
+    const int bi = blockIdx.x, b = g.b0 + bi;
+    const int cut = g.val[bi];
+    const int np = next_pos[b];
+    int32_t* pb = pos + (size_t)b * S;
+    if (ring) {
+        for (int s = threadIdx.x; s < S; s += blockDim.x)
+            if (pb[s] >= cut) pb[s] = -1;
+    } else {
+        for (int s = cut + threadIdx.x; s < np && s < S; s += blockDim.x) pb[s] = -1;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) next_pos[b] = cut;
+}
+
+size_t quant_smem(int d) { return (size_t)(2 * kQBlock * d + 64) * sizeof(float); }
+
+}  // namespace
+
+cudaError_t launch_append_token(const AppendArgs& a, cudaStream_t st) {
+    const size_t smem = a.int8 ? quant_smem(a.d) : 0;
+    append_token_kernel<<<a.B, kThreads, smem, st>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_append_rows_group(const AppendArgs& a, const Group& g, cudaStream_t st) {
+    if (!a.int8) {
+        const int half = a.d / 2;
+        const int rows_per_cta = kThreads / half > 0 ? kThreads / half : 1;
+        dim3 grid((a.n + rows_per_cta - 1) / rows_per_cta, a.Hkv, g.nb);
+        append_rows_kernel<<<grid, kThreads, 0, st>>>(a, g);
+        advance_kernel<<<(g.nb + 255) / 256, 256, 0, st>>>(a.next_pos, g);
+    } else {
+        dim3 grid((a.n + kQBlock - 1) / kQBlock + 1, a.Hkv, g.nb);
+        quantize_rows_kernel<<<grid, kThreads, quant_smem(a.d), st>>>(a, g);
+        tail_kernel<<<g.nb, kThreads, 0, st>>>(a, g);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace kvc
+
+namespace kvc {
+
+// Host side of the grouped launches: per-request values travel in kernel
+// parameters (no staging copies), kMaxGroup requests per launch.
+cudaError_t launch_append_rows_counts(const AppendArgs& a, const int32_t* counts, cudaStream_t st) {
+    for (int b0 = 0; b0 < a.B; b0 += kMaxGroup) {
+        Group g;
+        g.b0 = b0;
+        g.nb = a.B - b0 < kMaxGroup ? a.B - b0 : kMaxGroup;
+        for (int i = 0; i < g.nb; ++i) g.val[i] = counts[b0 + i];
+        cudaError_t e = launch_append_rows_group(a, g, st);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+cudaError_t launch_trim_cuts(int32_t* next_pos, int32_t* pos, const int32_t* cuts, int B, int S,
+                             int ring, cudaStream_t st) {
+    for (int b0 = 0; b0 < B; b0 += kMaxGroup) {
+        Group g;
+        g.b0 = b0;
+        g.nb = B - b0 < kMaxGroup ? B - b0 : kMaxGroup;
+        for (int i = 0; i < g.nb; ++i) g.val[i] = cuts[b0 + i];
+        trim_kernel<<<g.nb, 256, 0, st>>>(next_pos, pos, g, S, ring);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace kvc

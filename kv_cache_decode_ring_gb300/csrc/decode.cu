@@ -1,0 +1,131 @@
+// decode.cu -- split-K decode attention for one new query per request, and the
+// cross-split combine.
+//
+// out = softmax(q . K^T / sqrt(d)) . V over the cached window of the newest
+// token ([LOOP] §三 step; [LEAN] §2.1 with the window mask).  The key range of
+// request b is split into chunks of `split` keys; each chunk yields, per query
+// head, (m, l, acc[d]) with m the chunk's maximum logit (log2 domain), l the
+// sum of 2^(logit - m) and acc the correspondingly weighted sum of values.  The
+// combine rescales the chunks to a common maximum:
+//     m* = max m_s,  out = sum_s 2^(m_s - m*) acc_s / sum_s 2^(m_s - m*) l_s.
+// GQA: the g query heads of a KV head are served by the same CTA, so every K/V
+// row is read from memory once per KV head.  Single-query decode needs no
+// causal mask: every cached row precedes the query ([LOOP] §六).
+#include "kvc_internal.h"
+
+namespace kvc {
+
+cudaError_t launch_decode_fast(const DecodeArgs& a, cudaStream_t st);  // decode_fast.cu
+bool fast_decode_supported(const DecodeArgs& a);
+
+namespace {
+
+constexpr int kThreads = 128;
+
+// Rotated query of KV head `kvh` of request b (g heads) into shared memory, fp32.
+__device__ void load_query(const DecodeArgs& a, int b, int kvh, int t, int bf16, float* q) {
+    const int d = a.d, half = d / 2;
+    for (int idx = threadIdx.x; idx < a.g * half; idx += blockDim.x) {
+        const int hh = idx / half, i = idx % half;
+        const size_t off = ((size_t)b * a.Hq + (size_t)kvh * a.g + hh) * d;
+        const float x0 = ld_elem(a.q, off + 2 * i, bf16), x1 = ld_elem(a.q, off + 2 * i + 1, bf16);
+        float y0 = x0, y1 = x1;
+        if (a.rope) rope_pair(x0, x1, a.rope[(size_t)t * half + i], y0, y1);
+        q[hh * d + 2 * i] = y0;
+        q[hh * d + 2 * i + 1] = y1;
+    }
+}
+
+// Generic kernel: any dtype, any even d <= 256, any group size.  CTA =
+// (chunk of kGenericSplit keys, KV head, request).  Straightforward two-pass
+// evaluation of its chunk in shared memory.
+template <int BF16>
+__global__ void __launch_bounds__(kThreads) decode_generic_kernel(const DecodeArgs a) {
+    extern __shared__ float smem[];
+    const int b = blockIdx.z, kvh = blockIdx.y, chunk = blockIdx.x;
+    const int len = a.next_pos[b];
+    int lo, hi;
+    key_range(len, a.S, a.W, a.ring, lo, hi);
+    const int k0 = lo + chunk * a.split;
+    if (k0 >= hi) return;
+    const int nk = min(hi - k0, a.split);
+    const int d = a.d, g = a.g;
+    float* q = smem;               // [g][d]
+    float* s = smem + g * d;       // [g][split]
+    load_query(a, b, kvh, len - 1, BF16, q);
+    __syncthreads();
+    const size_t base = ((size_t)b * a.Hkv + kvh) * a.S;
+    for (int idx = threadIdx.x; idx < g * nk; idx += blockDim.x) {
+        const int hh = idx / nk, j = idx % nk;
+        const size_t row = (base + k0 + j) * d;
+        float acc = 0.f;
+        for (int i = 0; i < d; ++i) acc = fmaf(q[hh * d + i], ld_elem(a.k, row + i, BF16), acc);
+        s[hh * a.split + j] = acc * a.scale_log2;
+    }
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    for (int hh = warp; hh < g; hh += nw) {
+        float m = -INFINITY;
+        for (int j = lane; j < nk; j += 32) m = fmaxf(m, s[hh * a.split + j]);
+        for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        float l = 0.f;
+        for (int j = lane; j < nk; j += 32) {
+            const float p = exp2f(s[hh * a.split + j] - m);
+            s[hh * a.split + j] = p;
+            l += p;
+        }
+        for (int o = 16; o; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+        if (lane == 0)
+            a.part_ml[((size_t)b * a.Hq + (size_t)kvh * g + hh) * a.max_splits + chunk] = make_float2(m, l);
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < g * d; idx += blockDim.x) {
+        const int hh = idx / d, i = idx % d;
+        float acc = 0.f;
+        for (int j = 0; j < nk; ++j) acc = fmaf(s[hh * a.split + j], ld_elem(a.v, (base + k0 + j) * d + i, BF16), acc);
+        a.part_acc[(((size_t)b * a.Hq + (size_t)kvh * g + hh) * a.max_splits + chunk) * d + i] = acc;
+    }
+}
+
+// Combine: CTA per (query head, request); threads over d.
+__global__ void __launch_bounds__(kThreads) combine_kernel(const CombineArgs c) {
+    const int hq = blockIdx.x, b = blockIdx.y;
+    const int len = c.next_pos[b];
+    int lo, hi;
+    key_range(len, c.S, c.W, c.ring, lo, hi);
+    const int ns = (hi - lo + c.split - 1) / c.split;
+    const size_t row = (size_t)b * c.Hq + hq;
+    const float2* ml = c.part_ml + row * c.max_splits;
+    float mx = -INFINITY;
+    for (int s = 0; s < ns; ++s) mx = fmaxf(mx, ml[s].x);
+    float L = 0.f;
+    for (int s = 0; s < ns; ++s) L += ml[s].y * exp2f(ml[s].x - mx);
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    for (int i = threadIdx.x; i < c.d; i += blockDim.x) {
+        float acc = 0.f;
+        for (int s = 0; s < ns; ++s) acc = fmaf(c.part_acc[(row * c.max_splits + s) * c.d + i], exp2f(ml[s].x - mx), acc);
+        const float o = acc * inv;
+        if (c.bf16) static_cast<__nv_bfloat16*>(c.out)[row * c.d + i] = __float2bfloat16_rn(o);
+        else static_cast<float*>(c.out)[row * c.d + i] = o;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeArgs& a, const CombineArgs& c, bool fast, cudaStream_t st) {
+    if (fast) {
+        cudaError_t e = launch_decode_fast(a, st);
+        if (e != cudaSuccess) return e;
+    } else {
+        dim3 grid(a.max_splits, a.Hkv, a.B);
+        const size_t smem = (size_t)a.g * (a.d + a.split) * sizeof(float);
+        if (c.bf16) decode_generic_kernel<1><<<grid, kThreads, smem, st>>>(a);
+        else decode_generic_kernel<0><<<grid, kThreads, smem, st>>>(a);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    combine_kernel<<<dim3(a.Hq, a.B), kThreads, 0, st>>>(c);
+    return cudaGetLastError();
+}
+
+}  // namespace kvc

@@ -1,0 +1,385 @@
+// kvc_api.cu -- the C ABI (include/kvc.h): argument checks, state layout, host
+// mirror of next_position, RoPE table, and kernel launches.
+#include <cmath>
+#include <cstring>
+#include <new>
+
+#include "kvc_internal.h"
+
+namespace kvc {
+
+cudaError_t launch_append_rows_counts(const AppendArgs& a, const int32_t* counts, cudaStream_t st);
+cudaError_t launch_trim_cuts(int32_t* next_pos, int32_t* pos, const int32_t* cuts, int B, int S,
+                             int ring, cudaStream_t st);
+bool fast_decode_supported(const DecodeArgs& a);
+cudaError_t launch_int8_decode(kvc_handle* h, const void* q, void* out, float* cmax, float* tanh_out,
+                               float* ct, cudaStream_t st);
+cudaError_t launch_chunk(kvc_handle* h, const void* q, void* out, int n, cudaStream_t st);
+
+namespace {
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+}  // namespace
+
+bool make_shape(const kvc_config& c, Shape* s) {
+    if (c.dtype != KVC_F32 && c.dtype != KVC_BF16) return false;
+    if (c.layout != KVC_CONTIGUOUS && c.layout != KVC_RING) return false;
+    if (c.kv_quant != KVC_QUANT_NONE && c.kv_quant != KVC_QUANT_INT8) return false;
+    if (c.batch < 1 || c.n_q_heads < 1 || c.n_kv_heads < 1) return false;
+    if (c.n_q_heads % c.n_kv_heads) return false;
+    if (c.head_dim < 2 || c.head_dim > 256 || (c.head_dim & 1)) return false;
+    if (c.capacity < 1 || c.window < 0 || c.max_position < 0 || c.max_chunk < 0) return false;
+    if (!(c.rope_base >= 0.f) || std::isinf(c.rope_base)) return false;
+    const bool ring = c.layout == KVC_RING;
+    if (ring && c.window != 0 && c.window != c.capacity) return false;
+    const bool int8 = c.kv_quant == KVC_QUANT_INT8;
+    if (int8 && (c.dtype != KVC_BF16 || ring || c.head_dim % kBands || c.capacity % kQBlock)) return false;
+    const bool rope = c.rope_base > 0.f;
+    int P = 0;
+    if (rope) {
+        P = c.max_position ? c.max_position : (ring ? 0 : c.capacity);
+        if (P < 1) return false;
+    }
+    s->B = c.batch; s->Hq = c.n_q_heads; s->Hkv = c.n_kv_heads; s->g = c.n_q_heads / c.n_kv_heads;
+    s->d = c.head_dim; s->S = c.capacity; s->W = ring ? c.capacity : c.window;
+    s->P = P; s->ring = ring; s->int8 = int8; s->rope = rope; s->bf16 = c.dtype == KVC_BF16;
+    s->elem = s->bf16 ? 2 : 4;
+    s->split = kGenericSplit;
+    if (s->bf16 && !int8 && (s->d == 64 || s->d == 128) && s->g <= 8) s->split = kFastSplit;
+    const long long keys = (s->W > 0 && s->W < s->S) ? s->W : s->S;
+    s->max_splits = (int)((keys + s->split - 1) / s->split);
+    return true;
+}
+
+Layout make_layout(const Shape& s) {
+    Layout L{};
+    size_t o = 0;
+    auto take = [&](size_t bytes) { size_t at = o; o = align256(o + bytes); return at; };
+    const size_t B = s.B, Hkv = s.Hkv, S = s.S, d = s.d, Hq = s.Hq;
+    L.hdr = take(256);
+    L.next_pos = take(B * 4);
+    L.pos = take(B * S * 4);
+    if (!s.int8) {
+        L.k = take(B * Hkv * S * d * s.elem);
+        L.v = take(B * Hkv * S * d * s.elem);
+    } else {
+        L.kq = take(B * Hkv * S * d);
+        L.vq = take(B * Hkv * S * d);
+        L.sk = take(B * Hkv * (S / kQBlock) * 4);
+        L.sv = take(B * Hkv * (S / kQBlock) * 4);
+        L.wit = take(B * Hkv * S * kBands * 2);
+        L.ktail = take(B * Hkv * kQBlock * d * 2);
+        L.vtail = take(B * Hkv * kQBlock * d * 2);
+    }
+    L.rope = take((size_t)s.P * (d / 2) * 8);
+    L.part_ml = take(B * Hq * s.max_splits * 8);
+    L.part_acc = take(B * Hq * s.max_splits * d * 4);
+    L.total = o;
+    return L;
+}
+
+}  // namespace kvc
+
+using namespace kvc;
+
+namespace {
+
+inline cudaStream_t S_(kvc_stream_t s) { return static_cast<cudaStream_t>(s); }
+
+template <typename T>
+T* at(kvc_handle* h, size_t off) { return reinterpret_cast<T*>(h->state + off); }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// {cos, sin} of angle p * base^(-(2i)/d) (double), each rounded once to fp32.
+void rope_table(double base, int d, int P, float2* out) {
+    const int half = d / 2;
+    std::vector<double> theta(half);
+    for (int i = 0; i < half; ++i) theta[i] = std::pow(base, (double)(-2 * i) / (double)d);
+    for (int p = 0; p < P; ++p)
+        for (int i = 0; i < half; ++i) {
+            const double ang = (double)p * theta[i];
+            out[(size_t)p * half + i] = make_float2((float)std::cos(ang), (float)std::sin(ang));
+        }
+}
+
+AppendArgs append_args(kvc_handle* h, const void* k, const void* v, int n) {
+    const Shape& s = h->sh;
+    AppendArgs a{};
+    a.k = k; a.v = v; a.n = n;
+    a.next_pos = at<int32_t>(h, h->L.next_pos);
+    a.pos = at<int32_t>(h, h->L.pos);
+    if (!s.int8) { a.kc = h->state + h->L.k; a.vc = h->state + h->L.v; }
+    else {
+        a.kq = at<int8_t>(h, h->L.kq); a.vq = at<int8_t>(h, h->L.vq);
+        a.sk = at<float>(h, h->L.sk); a.sv = at<float>(h, h->L.sv);
+        a.wit = at<__half>(h, h->L.wit);
+        a.ktail = at<__nv_bfloat16>(h, h->L.ktail); a.vtail = at<__nv_bfloat16>(h, h->L.vtail);
+    }
+    a.rope = s.rope ? at<float2>(h, h->L.rope) : nullptr;
+    a.hdr = at<uint32_t>(h, h->L.hdr);
+    a.B = s.B; a.Hkv = s.Hkv; a.d = s.d; a.S = s.S; a.P = s.P;
+    a.ring = s.ring; a.bf16 = s.bf16; a.int8 = s.int8;
+    return a;
+}
+
+// Highest position the append of counts[b] rows would reach must fit.
+int check_capacity(kvc_handle* h, const int32_t* counts, int n) {
+    const Shape& s = h->sh;
+    for (int b = 0; b < s.B; ++b) {
+        const long long c = counts ? counts[b] : n;
+        if (c <= 0) continue;
+        const long long last = (long long)h->np[b] + c - 1;
+        if (last > 0x7ffffffeLL) return KVC_ERR_CAPACITY;
+        if (!s.ring && last >= s.S) return KVC_ERR_CAPACITY;
+        if (s.rope && last >= s.P) return KVC_ERR_CAPACITY;
+    }
+    return KVC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* kvc_strerror(int code) {
+    switch (code) {
+        case KVC_OK: return "ok";
+        case KVC_ERR_ARG: return "invalid argument";
+        case KVC_ERR_CAPACITY: return "cache capacity or RoPE table exceeded";
+        case KVC_ERR_EVICTED: return "rows needed after the trim are no longer held exactly";
+        case KVC_ERR_CUDA: return "CUDA runtime error";
+        case KVC_ERR_UNSUPPORTED: return "not supported for this configuration";
+        case KVC_ERR_DEVICE: return "a kernel reported an error";
+        default: return "unknown status";
+    }
+}
+
+int kvc_state_bytes(const kvc_config* cfg, size_t* bytes) {
+    if (!cfg || !bytes) return KVC_ERR_ARG;
+    Shape s;
+    if (!make_shape(*cfg, &s)) return KVC_ERR_ARG;
+    *bytes = make_layout(s).total;
+    return KVC_OK;
+}
+
+int kvc_create(const kvc_config* cfg, void* d_state, size_t bytes, kvc_stream_t stream, kvc_t* out) {
+    if (!cfg || !d_state || !out) return KVC_ERR_ARG;
+    if (reinterpret_cast<uintptr_t>(d_state) & 255u) return KVC_ERR_ARG;
+    Shape s;
+    if (!make_shape(*cfg, &s)) return KVC_ERR_ARG;
+    Layout L = make_layout(s);
+    if (bytes < L.total) return KVC_ERR_ARG;
+    kvc_handle* h = new (std::nothrow) kvc_handle();
+    if (!h) return KVC_ERR_ARG;
+    h->cfg = *cfg; h->sh = s; h->L = L; h->state = static_cast<char*>(d_state); h->bytes = bytes;
+    h->np.assign(s.B, 0);
+    h->ring_needs_append = false;
+    if (cudaGetDevice(&h->device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess) {
+        delete h;
+        return KVC_ERR_CUDA;
+    }
+    cudaStream_t st = S_(stream);
+    cudaError_t e = cudaMemsetAsync(h->state, 0, L.total, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(h->state + L.pos, 0xff, (size_t)s.B * s.S * 4, st);
+    if (e == cudaSuccess && s.rope) {
+        std::vector<float2> tab((size_t)s.P * (s.d / 2));
+        rope_table((double)cfg->rope_base, s.d, s.P, tab.data());
+        e = cudaMemcpyAsync(h->state + L.rope, tab.data(), tab.size() * sizeof(float2),
+                            cudaMemcpyHostToDevice, st);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    }
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) { delete h; return KVC_ERR_CUDA; }
+    *out = h;
+    return KVC_OK;
+}
+
+int kvc_destroy(kvc_t h) {
+    if (!h) return KVC_ERR_ARG;
+    delete h;
+    return KVC_OK;
+}
+
+int kvc_append(kvc_t h, const void* d_k, const void* d_v, kvc_stream_t stream) {
+    if (!h || !d_k || !d_v || !aligned16(d_k) || !aligned16(d_v)) return KVC_ERR_ARG;
+    int rc = check_capacity(h, nullptr, 1);
+    if (rc) return rc;
+    AppendArgs a = append_args(h, d_k, d_v, 1);
+    if (launch_append_token(a, S_(stream)) != cudaSuccess) return KVC_ERR_CUDA;
+    for (auto& p : h->np) ++p;
+    h->ring_needs_append = false;
+    return KVC_OK;
+}
+
+int kvc_append_rows(kvc_t h, const void* d_k, const void* d_v, int32_t n, const int32_t* h_counts,
+                    kvc_stream_t stream) {
+    if (!h || n < 0 || !aligned16(d_k) || !aligned16(d_v)) return KVC_ERR_ARG;
+    if (n == 0) return KVC_OK;
+    if (!d_k || !d_v) return KVC_ERR_ARG;
+    const Shape& s = h->sh;
+    h->counts.assign(s.B, n);
+    if (h_counts)
+        for (int b = 0; b < s.B; ++b) {
+            if (h_counts[b] < 0 || h_counts[b] > n) return KVC_ERR_ARG;
+            h->counts[b] = h_counts[b];
+        }
+    int rc = check_capacity(h, h->counts.data(), n);
+    if (rc) return rc;
+    AppendArgs a = append_args(h, d_k, d_v, n);
+    if (launch_append_rows_counts(a, h->counts.data(), S_(stream)) != cudaSuccess) return KVC_ERR_CUDA;
+    bool any = false;
+    for (int b = 0; b < s.B; ++b) { h->np[b] += h->counts[b]; any |= h->counts[b] > 0; }
+    if (any) h->ring_needs_append = false;
+    return KVC_OK;
+}
+
+int kvc_decode_attn(kvc_t h, const void* d_q, void* d_out, float* d_cmax, float* d_tanh, float* d_ct,
+                    kvc_stream_t stream) {
+    if (!h || !d_q || !d_out || !aligned16(d_q) || !aligned16(d_out)) return KVC_ERR_ARG;
+    const Shape& s = h->sh;
+    for (int b = 0; b < s.B; ++b)
+        if (h->np[b] < 1) return KVC_ERR_ARG;                 // nothing cached to attend to
+    if (s.ring && h->ring_needs_append) return KVC_ERR_ARG;
+    cudaStream_t st = S_(stream);
+    if (s.int8) {
+        if (launch_int8_decode(h, d_q, d_out, d_cmax, d_tanh, d_ct, st) != cudaSuccess) return KVC_ERR_CUDA;
+        return KVC_OK;
+    }
+    if (d_ct) return KVC_ERR_ARG;
+    DecodeArgs a{};
+    a.q = d_q; a.k = h->state + h->L.k; a.v = h->state + h->L.v;
+    a.next_pos = at<int32_t>(h, h->L.next_pos);
+    a.rope = s.rope ? at<float2>(h, h->L.rope) : nullptr;
+    a.part_ml = at<float2>(h, h->L.part_ml);
+    a.part_acc = at<float>(h, h->L.part_acc);
+    a.hdr = at<uint32_t>(h, h->L.hdr);
+    a.B = s.B; a.Hq = s.Hq; a.Hkv = s.Hkv; a.g = s.g; a.d = s.d; a.S = s.S; a.W = s.W;
+    a.max_splits = s.max_splits; a.split = s.split; a.ring = s.ring;
+    a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)s.d));
+    CombineArgs c{};
+    c.part_ml = a.part_ml; c.part_acc = a.part_acc; c.next_pos = a.next_pos; c.out = d_out;
+    c.B = s.B; c.Hq = s.Hq; c.d = s.d; c.S = s.S; c.W = s.W; c.max_splits = s.max_splits;
+    c.split = s.split; c.ring = s.ring; c.bf16 = s.bf16;
+    const bool fast = s.split == kFastSplit && fast_decode_supported(a);
+    if (launch_decode(a, c, fast, st) != cudaSuccess) return KVC_ERR_CUDA;
+    if (d_cmax && cudaMemsetAsync(d_cmax, 0, (size_t)s.B * s.Hq * 4, st) != cudaSuccess) return KVC_ERR_CUDA;
+    if (d_tanh && cudaMemsetAsync(d_tanh, 0, (size_t)s.B * s.Hq * 4, st) != cudaSuccess) return KVC_ERR_CUDA;
+    return KVC_OK;
+}
+
+int kvc_trim(kvc_t h, const int32_t* h_cut, kvc_stream_t stream) {
+    if (!h || !h_cut) return KVC_ERR_ARG;
+    const Shape& s = h->sh;
+    for (int b = 0; b < s.B; ++b) {
+        const int cut = h_cut[b], np = h->np[b];
+        if (cut < 0 || cut > np) return KVC_ERR_ARG;
+        if (s.ring) {
+            const int lo = cut - s.S + 1 > 0 ? cut - s.S + 1 : 0;
+            const int resident = np - s.S > 0 ? np - s.S : 0;
+            if (!(lo == cut || lo >= resident)) return KVC_ERR_EVICTED;
+        }
+        if (s.int8 && (cut % kQBlock) && cut < (np / kQBlock) * kQBlock) return KVC_ERR_EVICTED;
+    }
+    if (launch_trim_cuts(at<int32_t>(h, h->L.next_pos), at<int32_t>(h, h->L.pos), h_cut, s.B, s.S, s.ring,
+                         S_(stream)) != cudaSuccess)
+        return KVC_ERR_CUDA;
+    for (int b = 0; b < s.B; ++b) h->np[b] = h_cut[b];
+    if (s.ring) h->ring_needs_append = true;
+    return KVC_OK;
+}
+
+int kvc_chunk_attn(kvc_t h, const void* d_q, const void* d_k, const void* d_v, int32_t n, void* d_out,
+                   kvc_stream_t stream) {
+    if (!h || !d_q || !d_k || !d_v || !d_out || n < 1) return KVC_ERR_ARG;
+    if (!aligned16(d_q) || !aligned16(d_k) || !aligned16(d_v) || !aligned16(d_out)) return KVC_ERR_ARG;
+    const Shape& s = h->sh;
+    if (s.ring || s.int8 || !s.bf16) return KVC_ERR_UNSUPPORTED;
+    if (n > h->cfg.max_chunk) return KVC_ERR_ARG;
+    int rc = check_capacity(h, nullptr, n);
+    if (rc) return rc;
+    (void)d_out;
+    return KVC_ERR_UNSUPPORTED;
+}
+
+int kvc_export_bytes(kvc_t h, int32_t which, size_t* bytes) {
+    if (!h || !bytes) return KVC_ERR_ARG;
+    const Shape& s = h->sh;
+    const size_t B = s.B, Hkv = s.Hkv, S = s.S, d = s.d;
+    switch (which) {
+        case KVC_EXPORT_K: case KVC_EXPORT_V:
+            if (s.int8) return KVC_ERR_ARG;
+            *bytes = B * Hkv * S * d * s.elem; return KVC_OK;
+        case KVC_EXPORT_POSITIONS: *bytes = B * S * 4; return KVC_OK;
+        case KVC_EXPORT_NEXT_POSITION: *bytes = B * 4; return KVC_OK;
+        default: break;
+    }
+    if (!s.int8) return KVC_ERR_ARG;
+    switch (which) {
+        case KVC_EXPORT_KQ: case KVC_EXPORT_VQ: *bytes = B * Hkv * S * d; return KVC_OK;
+        case KVC_EXPORT_SK: case KVC_EXPORT_SV: *bytes = B * Hkv * (S / kQBlock) * 4; return KVC_OK;
+        case KVC_EXPORT_WITNESS: *bytes = B * Hkv * S * kBands * 2; return KVC_OK;
+        case KVC_EXPORT_KTAIL: case KVC_EXPORT_VTAIL: *bytes = B * Hkv * kQBlock * d * 2; return KVC_OK;
+        default: return KVC_ERR_ARG;
+    }
+}
+
+int kvc_export(kvc_t h, int32_t which, void* h_dst, size_t bytes, kvc_stream_t stream) {
+    size_t need = 0;
+    int rc = kvc_export_bytes(h, which, &need);
+    if (rc) return rc;
+    if (!h_dst || bytes != need) return KVC_ERR_ARG;
+    size_t off = 0;
+    switch (which) {
+        case KVC_EXPORT_K: off = h->L.k; break;
+        case KVC_EXPORT_V: off = h->L.v; break;
+        case KVC_EXPORT_POSITIONS: off = h->L.pos; break;
+        case KVC_EXPORT_NEXT_POSITION: off = h->L.next_pos; break;
+        case KVC_EXPORT_KQ: off = h->L.kq; break;
+        case KVC_EXPORT_VQ: off = h->L.vq; break;
+        case KVC_EXPORT_SK: off = h->L.sk; break;
+        case KVC_EXPORT_SV: off = h->L.sv; break;
+        case KVC_EXPORT_WITNESS: off = h->L.wit; break;
+        case KVC_EXPORT_KTAIL: off = h->L.ktail; break;
+        case KVC_EXPORT_VTAIL: off = h->L.vtail; break;
+        default: return KVC_ERR_ARG;
+    }
+    cudaStream_t st = S_(stream);
+    if (cudaMemcpyAsync(h_dst, h->state + off, need, cudaMemcpyDeviceToHost, st) != cudaSuccess) return KVC_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return KVC_ERR_CUDA;
+    return KVC_OK;
+}
+
+int kvc_next_positions(kvc_t h, int32_t* h_out) {
+    if (!h || !h_out) return KVC_ERR_ARG;
+    std::memcpy(h_out, h->np.data(), h->np.size() * 4);
+    return KVC_OK;
+}
+
+int kvc_device_status(kvc_t h, kvc_stream_t stream, int32_t* h_status) {
+    if (!h || !h_status) return KVC_ERR_ARG;
+    cudaStream_t st = S_(stream);
+    uint32_t word = 0;
+    if (cudaMemcpyAsync(&word, h->state + h->L.hdr, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess) return KVC_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return KVC_ERR_CUDA;
+    if (word && cudaMemsetAsync(h->state + h->L.hdr, 0, 4, st) != cudaSuccess) return KVC_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return KVC_ERR_CUDA;
+    *h_status = (int32_t)word;
+    return KVC_OK;
+}
+
+int kvc_prefix_cut(const int64_t* h_old_ids, int32_t n_old, const int64_t* h_new_ids, int32_t n_new,
+                   int32_t ring, int32_t* h_cut) {
+    if (!h_cut || n_new < 1 || n_old < 0 || !h_new_ids || (n_old > 0 && !h_old_ids)) return KVC_ERR_ARG;
+    int32_t lcp = 0;
+    const int32_t m = n_old < n_new ? n_old : n_new;
+    while (lcp < m && h_old_ids[lcp] == h_new_ids[lcp]) ++lcp;
+    int32_t cut = lcp;
+    if (ring) cut = (lcp == n_old && n_new > n_old) ? n_old : 0;
+    if (cut > n_new - 1) cut = n_new - 1;
+    *h_cut = cut;
+    return KVC_OK;
+}
+
+}  // extern "C"

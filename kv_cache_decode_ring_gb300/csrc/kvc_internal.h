@@ -1,0 +1,129 @@
+// kvc_internal.h -- state layout, handle, kernel argument blocks and device
+// helpers shared by the libkvc translation units.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+#include <vector>
+
+#include "../../include/kvc.h"
+
+namespace kvc {
+
+constexpr int kQBlock = 16;           // tokens per INT8 quantization block
+constexpr int kBands = 16;            // witness bands per key row
+constexpr int kGenericSplit = 64;     // keys per split, generic decode kernel
+constexpr int kFastSplit = 256;       // keys per split, bf16 fast decode kernel
+constexpr uint32_t kErrPosition = 1u; // device error bits (sticky, cleared by kvc_device_status)
+constexpr uint32_t kErrWait = 2u;
+
+// Byte offsets of the arrays inside the caller's state buffer (256-B aligned).
+struct Layout {
+    size_t hdr;       // uint32[64]: [0] error word, [1] work counter, [2] done counter
+    size_t next_pos;  // int32 [B]
+    size_t pos;       // int32 [B][S]
+    size_t k, v;      // [B][Hkv][S][d] cache dtype            (non-INT8)
+    size_t kq, vq;    // int8 [B][Hkv][S][d]                   (INT8)
+    size_t sk, sv;    // f32  [B][Hkv][S/16]                   (INT8)
+    size_t wit;       // f16  [B][Hkv][S][16]                  (INT8)
+    size_t ktail, vtail;  // bf16 [B][Hkv][16][d]              (INT8)
+    size_t rope;      // float2 [P][d/2] {cos, sin}
+    size_t part_ml;   // float2 [B][Hq][max_splits] {m (log2 domain), l}
+    size_t part_acc;  // float  [B][Hq][max_splits][d]
+    size_t total;
+};
+
+struct Shape {
+    int B, Hq, Hkv, g, d, S, W;  // W = attention window in positions (0 = full)
+    int P;                       // RoPE table rows (0 = no RoPE)
+    int elem;                    // bytes per cache element (non-INT8)
+    bool ring, int8, rope, bf16;
+    int split;                   // keys per split of the decode kernel in use
+    int max_splits;
+};
+
+bool make_shape(const kvc_config& c, Shape* s);
+Layout make_layout(const Shape& s);
+
+// Arguments of the decode kernels (everything by value; no host pointers).
+struct DecodeArgs {
+    const void* q;        // [B][Hq][d] cache dtype
+    const void* k;        // cache rows (non-INT8)
+    const void* v;
+    const int32_t* next_pos;
+    const float2* rope;   // nullptr = no RoPE
+    float2* part_ml;
+    float* part_acc;
+    uint32_t* hdr;
+    int B, Hq, Hkv, g, d, S, W, max_splits, split;
+    int ring;
+    float scale_log2;     // log2(e) / sqrt(d)
+};
+
+struct CombineArgs {
+    const float2* part_ml;
+    const float* part_acc;
+    const int32_t* next_pos;
+    void* out;            // [B][Hq][d] cache dtype
+    int B, Hq, d, S, W, max_splits, split, ring, bf16;
+};
+
+struct AppendArgs {
+    const void* k;        // [B][Hkv][n][d]  (n = 1 for a single token)
+    const void* v;
+    int n;                // rows in the input per request
+    int32_t* next_pos;
+    int32_t* pos;
+    void* kc;             // cache rows (non-INT8)
+    void* vc;
+    int8_t* kq; int8_t* vq; float* sk; float* sv; __half* wit;
+    __nv_bfloat16* ktail; __nv_bfloat16* vtail;
+    const float2* rope;
+    uint32_t* hdr;
+    int B, Hkv, d, S, P, ring, bf16, int8;
+};
+
+// ---- launchers (one per translation unit) ----------------------------------
+cudaError_t launch_append_token(const AppendArgs& a, cudaStream_t st);
+cudaError_t launch_decode(const DecodeArgs& d, const CombineArgs& c, bool fast, cudaStream_t st);
+
+// ---- device helpers -----------------------------------------------------------
+__device__ __forceinline__ float ld_elem(const void* p, size_t i, int bf16) {
+    return bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(p)[i])
+                : static_cast<const float*>(p)[i];
+}
+
+// RoPE on one interleaved pair, fp32, each product and the sum rounded once:
+//   y0 = x0*c - x1*s,  y1 = x1*c + x0*s.
+__device__ __forceinline__ void rope_pair(float x0, float x1, float2 cs, float& y0, float& y1) {
+    y0 = __fsub_rn(__fmul_rn(x0, cs.x), __fmul_rn(x1, cs.y));
+    y1 = __fadd_rn(__fmul_rn(x1, cs.x), __fmul_rn(x0, cs.y));
+}
+
+// Cached key slots of request b attended by its newest token (next_position - 1):
+// a ring holds the window in slots [0, min(len, W)); a contiguous cache in
+// slots [len - min(len, W), len).
+__device__ __forceinline__ void key_range(int len, int S, int W, int ring, int& lo, int& hi) {
+    if (ring) { lo = 0; hi = len < S ? len : S; }
+    else { hi = len; lo = (W > 0 && len > W) ? len - W : 0; }
+}
+
+}  // namespace kvc
+
+// Opaque handle behind kvc_t.
+struct kvc_handle {
+    kvc_config cfg;
+    kvc::Shape sh;
+    kvc::Layout L;
+    char* state;
+    size_t bytes;
+    int device;
+    int num_sms;
+    std::vector<int32_t> np;      // host mirror of next_position
+    bool ring_needs_append;        // a ring was trimmed and has not appended since
+    std::vector<int32_t> counts;   // host staging for append_rows counts
+};

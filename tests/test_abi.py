@@ -1,0 +1,92 @@
+"""The C-ABI library loads, exports every entry point include/kvc.h declares, and its
+host-only logic is right (CPU only: no kernel is launched here)."""
+import os
+import re
+import subprocess
+
+import pytest
+
+from kv_cache_decode_ring_gb300 import build as kbuild
+from kv_cache_decode_ring_gb300 import kvc
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    kbuild.build()
+    return kvc.lib()
+
+
+def declared():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\**(kvc_\w+)\s*\(", src, flags=re.M))
+    return sorted(names)
+
+
+def test_header_declares_the_boundary():
+    names = declared()
+    for want in ["kvc_create", "kvc_append", "kvc_trim", "kvc_decode_attn", "kvc_chunk_attn"]:
+        assert want in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", kvc.library_path()], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (kvc_\w+)", out))
+    missing = [n for n in declared() if n not in exported]
+    assert not missing, missing
+    for n in declared():
+        assert hasattr(lib, n)
+
+
+def test_state_bytes_validation(lib):
+    ok = kvc.make_config("bf16", "contiguous", None, 32, 32, 32, 128, 8192)
+    n = kvc.kvc_state_bytes(ok)
+    assert n >= 2 * 32 * 32 * 8192 * 128 * 2 + 32 * 8192 * 4
+    bad = [
+        kvc.make_config("bf16", "contiguous", None, 2, 3, 2, 128, 64),          # Hq % Hkv
+        kvc.make_config("bf16", "contiguous", None, 1, 1, 1, 7, 64),            # odd head_dim
+        kvc.make_config("bf16", "ring", None, 1, 1, 1, 128, 64, window=32),     # ring window != W
+        kvc.make_config("bf16", "ring", None, 1, 1, 1, 128, 64, rope_base=1e4),  # ring RoPE needs max_position
+        kvc.make_config("f32", "contiguous", "int8", 1, 1, 1, 128, 64),         # INT8 needs bf16
+        kvc.make_config("bf16", "contiguous", "int8", 1, 1, 1, 128, 60),        # INT8 capacity % 16
+        kvc.make_config("bf16", "ring", "int8", 1, 1, 1, 128, 64),              # INT8 contiguous only
+        kvc.make_config("bf16", "contiguous", None, 0, 1, 1, 128, 64),          # empty batch
+    ]
+    for c in bad:
+        with pytest.raises(kvc.KvcError) as e:
+            kvc.kvc_state_bytes(c)
+        assert e.value.code == kvc.KVC_ERR_ARG
+
+
+def test_prefix_cut_matches_golden(lib):
+    import test_oracle_listmodel as golden
+    for name, old, new, ring, cut, _, _ in golden.read_cases():
+        if old == "store":
+            continue
+        assert kvc.kvc_prefix_cut([int(x) for x in old.split()], new, bool(ring)) == cut, name
+    with pytest.raises(kvc.KvcError):
+        kvc.kvc_prefix_cut([1, 2], [])
+    with pytest.raises(TypeError):
+        kvc.kvc_prefix_cut([1, 2], [1.0, 2])
+
+
+def test_prefix_cut_matches_oracle_exhaustively(lib):
+    import itertools
+    from oracle.listmodel import prefix_cut
+    alphabet = [1, 2]
+    for n_old in range(0, 5):
+        for n_new in range(1, 5):
+            for old in itertools.product(alphabet, repeat=n_old):
+                for new in itertools.product(alphabet, repeat=n_new):
+                    for ring in (False, True):
+                        assert kvc.kvc_prefix_cut(list(old), list(new), ring) == prefix_cut(list(old), list(new), ring)
+
+
+def test_strerror(lib):
+    for code in range(7):
+        assert kvc.kvc_strerror(code)
