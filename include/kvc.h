@@ -21,8 +21,9 @@
  *    GPU, except kvc_create (uploads tables), kvc_export and
  *    kvc_device_status (read back).  One handle serves one stream at a time:
  *    calls on one handle from different streams race on its state.
- *  - Element types: KVC_F32 = IEEE fp32, KVC_BF16 = bfloat16.  q, k, v and
- *    out all use the cache dtype.
+ *  - Element types: KVC_F32 = IEEE fp32, KVC_BF16 = bfloat16.  q, k and v
+ *    use the cache dtype; outputs use kvc_config.out_dtype (default: the
+ *    cache dtype).
  *  - Positions are absolute, 0-based, signed 32-bit; -1 marks an empty slot.
  *  - Errors: every entry point returns a KVC_* status.  Arguments are checked
  *    on the host before anything is enqueued; a failed call changes nothing.
@@ -80,6 +81,9 @@ typedef struct {
                              0 = capacity (contiguous).  Required for a ring with RoPE. */
     float rope_base;      /* rotary base (e.g. 10000); 0 = keys and queries not rotated */
     int32_t max_chunk;    /* largest n for kvc_chunk_attn (sizes its workspace) */
+    int32_t out_dtype;    /* attention outputs: 0 = the cache dtype, else KVC_F32 or
+                             KVC_BF16 (+1 is added so that 0 keeps the default):
+                             pass KVC_F32 + 1 or KVC_BF16 + 1 */
 } kvc_config;
 
 /* Bytes of the device state buffer for `cfg` (cache rows, positions,
@@ -120,7 +124,7 @@ int kvc_append_rows(kvc_t h, const void* d_k, const void* d_v, int32_t n,
  * cached positions [max(0, t-W+1), t]:
  *     out = softmax(q . K^T / sqrt(d)) . V            d_out: [B][Hq][d]
  * evaluated as split-K flash decoding with an online softmax and a cross-split
- * combine, fp32 accumulation.  Needs at least one cached token per request, and
+ * combine, fp32 accumulation, rounded once to the output dtype.  Needs at least one cached token per request, and
  * on a ring an append after any trim.
  * INT8 caches also return, per (request, query head), the witness bound
  * ([WITCERT] "频带酉性与双层证书"):

@@ -30,6 +30,7 @@ bool make_shape(const kvc_config& c, Shape* s) {
     if (c.n_q_heads % c.n_kv_heads) return false;
     if (c.head_dim < 2 || c.head_dim > 256 || (c.head_dim & 1)) return false;
     if (c.capacity < 1 || c.window < 0 || c.max_position < 0 || c.max_chunk < 0) return false;
+    if (c.out_dtype != 0 && c.out_dtype != KVC_F32 + 1 && c.out_dtype != KVC_BF16 + 1) return false;
     if (!(c.rope_base >= 0.f) || std::isinf(c.rope_base)) return false;
     const bool ring = c.layout == KVC_RING;
     if (ring && c.window != 0 && c.window != c.capacity) return false;
@@ -45,6 +46,7 @@ bool make_shape(const kvc_config& c, Shape* s) {
     s->d = c.head_dim; s->S = c.capacity; s->W = ring ? c.capacity : c.window;
     s->P = P; s->ring = ring; s->int8 = int8; s->rope = rope; s->bf16 = c.dtype == KVC_BF16;
     s->elem = s->bf16 ? 2 : 4;
+    s->out_bf16 = c.out_dtype == 0 ? s->bf16 : c.out_dtype == KVC_BF16 + 1;
     s->split = kGenericSplit;
     if (s->bf16 && !int8 && (s->d == 64 || s->d == 128) && s->g <= 8) s->split = kFastSplit;
     const long long keys = (s->W > 0 && s->W < s->S) ? s->W : s->S;
@@ -261,7 +263,7 @@ int kvc_decode_attn(kvc_t h, const void* d_q, void* d_out, float* d_cmax, float*
     CombineArgs c{};
     c.part_ml = a.part_ml; c.part_acc = a.part_acc; c.next_pos = a.next_pos; c.out = d_out;
     c.B = s.B; c.Hq = s.Hq; c.d = s.d; c.S = s.S; c.W = s.W; c.max_splits = s.max_splits;
-    c.split = s.split; c.ring = s.ring; c.bf16 = s.bf16;
+    c.split = s.split; c.ring = s.ring; c.bf16 = s.out_bf16;
     const bool fast = s.split == kFastSplit && fast_decode_supported(a);
     if (launch_decode(a, c, fast, st) != cudaSuccess) return KVC_ERR_CUDA;
     if (d_cmax && cudaMemsetAsync(d_cmax, 0, (size_t)s.B * s.Hq * 4, st) != cudaSuccess) return KVC_ERR_CUDA;

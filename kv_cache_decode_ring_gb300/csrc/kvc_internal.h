@@ -17,7 +17,7 @@ namespace kvc {
 constexpr int kQBlock = 16;           // tokens per INT8 quantization block
 constexpr int kBands = 16;            // witness bands per key row
 constexpr int kGenericSplit = 64;     // keys per split, generic decode kernel
-constexpr int kFastSplit = 256;       // keys per split, bf16 fast decode kernel
+constexpr int kFastSplit = 128;       // keys per split, bf16 fast decode kernel
 constexpr uint32_t kErrPosition = 1u; // device error bits (sticky, cleared by kvc_device_status)
 constexpr uint32_t kErrWait = 2u;
 
@@ -42,6 +42,7 @@ struct Shape {
     int P;                       // RoPE table rows (0 = no RoPE)
     int elem;                    // bytes per cache element (non-INT8)
     bool ring, int8, rope, bf16;
+    bool out_bf16;               // attention outputs in bf16 (else fp32)
     int split;                   // keys per split of the decode kernel in use
     int max_splits;
 };

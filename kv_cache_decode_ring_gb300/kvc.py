@@ -40,7 +40,8 @@ class kvc_config(ctypes.Structure):
     _fields_ = [("dtype", ctypes.c_int32), ("layout", ctypes.c_int32), ("kv_quant", ctypes.c_int32),
                 ("batch", ctypes.c_int32), ("n_q_heads", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("capacity", ctypes.c_int32), ("window", ctypes.c_int32),
-                ("max_position", ctypes.c_int32), ("rope_base", ctypes.c_float), ("max_chunk", ctypes.c_int32)]
+                ("max_position", ctypes.c_int32), ("rope_base", ctypes.c_float), ("max_chunk", ctypes.c_int32),
+                ("out_dtype", ctypes.c_int32)]
 
 
 EXPORTED = ["kvc_state_bytes", "kvc_create", "kvc_destroy", "kvc_append", "kvc_append_rows",
@@ -123,12 +124,15 @@ def kvc_strerror(code: int) -> str:
 
 
 def make_config(dtype="bf16", layout="contiguous", kv_quant=None, batch=1, n_q_heads=1, n_kv_heads=1,
-                head_dim=128, capacity=1, window=0, max_position=0, rope_base=0.0, max_chunk=0) -> kvc_config:
+                head_dim=128, capacity=1, window=0, max_position=0, rope_base=0.0, max_chunk=0,
+                out_dtype=None) -> kvc_config:
+    """``out_dtype``: None (the cache dtype), "f32" or "bf16"."""
+    od = 0 if out_dtype is None else (KVC_F32 + 1 if out_dtype == "f32" else KVC_BF16 + 1)
     return kvc_config(KVC_BF16 if dtype == "bf16" else KVC_F32,
                       KVC_RING if layout == "ring" else KVC_CONTIGUOUS,
                       KVC_QUANT_INT8 if kv_quant == "int8" else KVC_QUANT_NONE,
                       batch, n_q_heads, n_kv_heads, head_dim, capacity, window, max_position,
-                      float(rope_base), max_chunk)
+                      float(rope_base), max_chunk, od)
 
 
 def kvc_state_bytes(cfg: kvc_config) -> int:
@@ -225,14 +229,18 @@ class Cache:
     def __init__(self, cfg: kvc_config, device="cuda", stream=None):
         self.cfg = cfg
         self.torch_dtype = torch.bfloat16 if cfg.dtype == KVC_BF16 else torch.float32
+        if cfg.out_dtype == 0:
+            self.out_dtype = self.torch_dtype
+        else:
+            self.out_dtype = torch.float32 if cfg.out_dtype == KVC_F32 + 1 else torch.bfloat16
         nbytes = kvc_state_bytes(cfg)
         self.state = torch.empty(nbytes, dtype=torch.uint8, device=device)
         self.h = kvc_create(cfg, self.state, stream)
 
     @classmethod
-    def from_workload(cls, w, max_chunk=0, max_position=0, device="cuda"):
+    def from_workload(cls, w, max_chunk=0, max_position=0, device="cuda", out_dtype=None):
         cfg = make_config(w.dtype, w.layout, w.quant, w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.capacity,
-                          0 if w.layout == "ring" else w.window, max_position, w.rope_base, max_chunk)
+                          0 if w.layout == "ring" else w.window, max_position, w.rope_base, max_chunk, out_dtype)
         return cls(cfg, device)
 
     def close(self):
@@ -272,8 +280,8 @@ class Cache:
     def decode(self, q, out=None, cmax=None, tanh=None, ct=None, stream=None):
         _dev(q, self.torch_dtype, (self.B, self.Hq, self.d), "q")
         if out is None:
-            out = torch.empty_like(q)
-        _dev(out, self.torch_dtype, (self.B, self.Hq, self.d), "out")
+            out = torch.empty(q.shape, dtype=self.out_dtype, device=q.device)
+        _dev(out, self.out_dtype, (self.B, self.Hq, self.d), "out")
         kvc_decode_attn(self.h, q, out, cmax, tanh, ct, stream)
         return out
 
@@ -288,7 +296,8 @@ class Cache:
         _dev(k, self.torch_dtype, (self.B, n, self.Hkv, self.d), "k")
         _dev(v, self.torch_dtype, (self.B, n, self.Hkv, self.d), "v")
         if out is None:
-            out = torch.empty_like(q)
+            out = torch.empty(q.shape, dtype=self.out_dtype, device=q.device)
+        _dev(out, self.out_dtype, (self.B, n, self.Hq, self.d), "out")
         kvc_chunk_attn(self.h, q, k, v, n, out, stream)
         return out
 

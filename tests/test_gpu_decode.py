@@ -138,8 +138,11 @@ def test_ring_trim_rules_on_device():
         cache.trim([20])                          # positions 5..19 were overwritten
     assert e.value.code == kvc.KVC_ERR_EVICTED
     check_state(cache, model, w)                  # a refused trim changes nothing
-    cache.trim([35])
-    model.trim([35])
+    with pytest.raises(kvc.KvcError) as e:
+        cache.trim([35])                          # needs 20..34, the ring holds 24..39
+    assert e.value.code == kvc.KVC_ERR_EVICTED
+    cache.trim([39])                              # needs 24..38: all resident
+    model.trim([39])
     check_state(cache, model, w)
     with pytest.raises(kvc.KvcError) as e:        # a ring must append before decoding again
         cache.decode(w.step_qkv(0)[0].cuda())
@@ -167,3 +170,24 @@ def test_capacity_and_argument_errors():
     with pytest.raises(ValueError):
         cache.decode(q.cuda().float())            # wrong dtype caught by the binding
     assert cache.device_status() == 0
+
+
+@pytest.mark.parametrize("case", [CASES[1], CASES[4], CASES[3]], ids=lambda c: c[0] + "-out-f32")
+def test_f32_outputs_strict_tolerance(case):
+    # bf16 cache, fp32 outputs: no output rounding, so the plain 2e-3 bound applies
+    name, Hq, Hkv, d, layout, cap, window, rope = case
+    w = wl.small(name, B=3, Hq=Hq, Hkv=Hkv, d=d, layout=layout, capacity=cap, window=window,
+                 rope_base=rope, seed=41)
+    cache = kvc.Cache.from_workload(w, max_position=4096 if layout == "ring" else 0, out_dtype="f32")
+    model = oracle_for(w)
+    lengths = [1, 200, 390]
+    k, v = w.prefill_chunk(0, max(lengths))
+    cache.append_rows(k.cuda(), v.cuda(), counts=lengths)
+    model.append_rows(host(k), host(v), lengths)
+    for s in range(2):
+        q, k1, v1 = w.step_qkv(s)
+        cache.append(k1.cuda(), v1.cuda())
+        model.append(host(k1), host(v1))
+        out = cache.decode(q.cuda())
+        assert out.dtype == torch.float32
+        assert_close(out, model.decode(host(q)), "bf16", "decode f32 out")

@@ -1,0 +1,157 @@
+"""Parity at the workloads' full sizes, in the launch configuration bench.py times.
+
+The oracle cannot redo every head, so sampled (request, head) outputs are checked
+one by one against fp64 attention over the generator's own rows (never the GPU
+cache), plus closed-form checks of positions that hold at any size.
+
+Full-cache MHA decode: B=32, H=32, d=128, contiguous 8192, context 4096 + 128 steps.
+Sliding-window GQA decode: B=64, Hq=32, Hkv=8, d=128, ring W=4096, RoPE 10000,
+per-request lengths L_b uniform in [1, 32768]; and one request run from
+position 0 to 32767 through the not-full, exactly-full and first-replacement steps.
+"""
+import numpy as np
+import pytest
+import torch
+
+from kv_cache_decode_ring_gb300 import kvc
+from kv_cache_decode_ring_gb300 import workloads as wl
+from oracle import numerics as nm
+
+from _parity import assert_close, host, oracle_for
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from kv_cache_decode_ring_gb300 import build
+    build.build()
+
+
+def _rows(model, x_np, positions):
+    return model.stored_rows(x_np, positions).astype(np.float64)
+
+
+def test_full_cache_mha_sampled():
+    w = wl.full_cache_mha()
+    ctx = w.extra["context"]
+    cache = kvc.Cache.from_workload(w)
+    model = oracle_for(w)            # used for its row and query definitions only
+    k, v = w.prefill_chunk(0, ctx, device="cuda")
+    cache.append_rows(k, v)
+    rng = np.random.default_rng(0)
+    sample = [(0, 0), (31, 31), (7, 19)] + [tuple(x) for x in rng.integers(0, 32, (9, 2))]
+    hk = {bh: host(k[bh[0], bh[1]]) for bh in sample}
+    hv = {bh: host(v[bh[0], bh[1]]) for bh in sample}
+    steps_k, steps_v = {bh: [] for bh in sample}, {bh: [] for bh in sample}
+    check_at = {0, 1, 63, 127}
+    for s in range(128):
+        q, k1, v1 = w.step_qkv(s, device="cuda")
+        cache.append(k1, v1)
+        out = cache.decode(q)
+        for bh in sample:
+            steps_k[bh].append(host(k1[bh[0], bh[1]]))
+            steps_v[bh].append(host(v1[bh[0], bh[1]]))
+        if s not in check_at:
+            continue
+        t = ctx + s
+        o = out.float().cpu()
+        for (b, h) in sample:
+            K = np.concatenate([_rows(model, hk[(b, h)], np.arange(ctx)),
+                                _rows(model, np.stack(steps_k[(b, h)]), np.arange(ctx, t + 1))])
+            V = np.concatenate([nm.bf16_to_f32(hv[(b, h)]), nm.bf16_to_f32(np.stack(steps_v[(b, h)]))]).astype(np.float64)
+            qr = model.query_rows(host(q[b, h])[None], [t]).astype(np.float64)
+            ref = nm.attend(qr, K, V, t, 0)
+            assert_close(o[b, h][None], ref, "bf16", "full-cache step %d (b=%d, h=%d)" % (s, b, h))
+    # positions after 128 steps: slot p holds p for p < ctx + 128 (closed form, every request)
+    pos = cache.export(kvc.KVC_EXPORT_POSITIONS)
+    want = np.where(np.arange(w.capacity) < ctx + 128, np.arange(w.capacity), -1)
+    assert np.array_equal(pos, np.broadcast_to(want, pos.shape))
+    assert cache.device_status() == 0
+
+
+def _ring_positions_ok(pos_row, length, W):
+    """Slot s holds the largest p < length with p = s mod W (or -1)."""
+    s = np.arange(W)
+    last = length - 1
+    want = last - ((last - s) % W)
+    want = np.where(want >= 0, want, -1)
+    return np.array_equal(pos_row, want)
+
+
+def test_sliding_window_gqa_sampled():
+    w = wl.sliding_window_gqa()
+    W, Lmax = w.capacity, w.extra["max_len"]
+    lengths = w.extra["lengths"]                   # current token at L_b - 1
+    cache = kvc.Cache.from_workload(w, max_position=Lmax)
+    model = oracle_for(w)
+    rng = np.random.default_rng(1)
+    bs = sorted(set([int(np.argmax(lengths)), int(np.argmin(lengths))] + list(rng.integers(0, 64, 6))))
+    hs = [0, 3, 7]
+    keep_k = {(b, h): [] for b in bs for h in hs}
+    keep_v = {(b, h): [] for b in bs for h in hs}
+    chunk = 4096
+    for c in range((Lmax + chunk - 1) // chunk):
+        counts = [int(min(max(L - 1 - c * chunk, 0), chunk)) for L in lengths]
+        if not any(counts):
+            continue
+        k, v = w.prefill_chunk(c, chunk, device="cuda")
+        cache.append_rows(k, v, counts=counts)
+        for b in bs:
+            lo = max(0, lengths[b] - W) - c * chunk   # first window row inside this chunk
+            a_, z_ = max(0, lo), counts[b]
+            if z_ > a_:
+                for h in hs:
+                    keep_k[(b, h)].append((c * chunk + a_, host(k[b, h, a_:z_])))
+                    keep_v[(b, h)].append((c * chunk + a_, host(v[b, h, a_:z_])))
+        del k, v
+    q, k1, v1 = w.step_qkv(0, device="cuda")
+    cache.append(k1, v1)
+    out = cache.decode(q).float().cpu()
+    g = w.n_q_heads // w.n_kv_heads
+    pos = cache.export(kvc.KVC_EXPORT_POSITIONS)
+    for b in range(64):
+        assert _ring_positions_ok(pos[b], lengths[b], W), b
+    for b in bs:
+        t = lengths[b] - 1
+        lo = max(0, t - W + 1)
+        for h in hs:
+            parts_k = [(p0, x) for p0, x in keep_k[(b, h)]]
+            Kin = np.concatenate([x for _, x in parts_k] + [host(k1[b, h])[None]]) if parts_k else host(k1[b, h])[None]
+            Vin = np.concatenate([x for _, x in keep_v[(b, h)]] + [host(v1[b, h])[None]])
+            assert Kin.shape[0] == t + 1 - lo
+            K = _rows(model, Kin, np.arange(lo, t + 1))
+            V = nm.bf16_to_f32(Vin).astype(np.float64)
+            qr = model.query_rows(host(q[b, h * g:(h + 1) * g]), np.full(g, t)).astype(np.float64)
+            ref = nm.attend(qr, K, V, t, W, p0=lo)
+            assert_close(out[b, h * g:(h + 1) * g], ref, "bf16", "sliding b=%d h=%d L=%d" % (b, h, lengths[b]))
+    assert cache.device_status() == 0
+
+
+def test_one_request_through_the_ring_phases():
+    base = wl.sliding_window_gqa()
+    W = base.capacity
+    w = wl.small("ring-long", B=1, Hq=32, Hkv=8, d=128, layout="ring", capacity=W, window=W,
+                 rope_base=10000.0, seed=29)
+    cache = kvc.Cache.from_workload(w, max_position=32768)
+    model = oracle_for(w)
+    check = {0, W - 2, W - 1, W, W + 1, 2 * W, 32767}
+    hist_k, hist_v = [], []
+    for t in range(32768):
+        q, k1, v1 = w.step_qkv(t, device="cuda")
+        cache.append(k1, v1)
+        hist_k.append(host(k1[0])); hist_v.append(host(v1[0]))
+        if t not in check:
+            continue
+        out = cache.decode(q).float().cpu()
+        lo = max(0, t - W + 1)
+        for h in (0, 5):
+            Kin = np.stack([x[h] for x in hist_k[lo:t + 1]])
+            K = _rows(model, Kin, np.arange(lo, t + 1))
+            V = nm.bf16_to_f32(np.stack([x[h] for x in hist_v[lo:t + 1]])).astype(np.float64)
+            qr = model.query_rows(host(q[0, h * 4:(h + 1) * 4]), np.full(4, t)).astype(np.float64)
+            ref = nm.attend(qr, K, V, t, W, p0=lo)
+            assert_close(out[0, h * 4:(h + 1) * 4], ref, "bf16", "ring t=%d h=%d" % (t, h))
+        pos = cache.export(kvc.KVC_EXPORT_POSITIONS)[0]
+        assert _ring_positions_ok(pos, t + 1, W), t
+    assert cache.device_status() == 0
