@@ -139,6 +139,40 @@ int kvc_append_rows(kvc_t h, const void* d_k, const void* d_v, int32_t n,
 int kvc_decode_attn(kvc_t h, const void* d_q, void* d_out, float* d_cmax, float* d_tanh,
                     float* d_ct, kvc_stream_t stream);
 
+/* Decode attention that allocates nothing (the pages have no counterpart; this
+ * is a deployment variant of kvc_decode_attn).
+ *
+ * Who it is for: callers that cannot call cudaMalloc while they decode. Examples:
+ *   - a serving engine that reserved all device memory for its KV pool;
+ *   - a runtime whose own allocator owns every device buffer;
+ *   - host code that must not wait on the allocator's device synchronisation.
+ *
+ * What it does: the same computation and result as kvc_decode_attn (out
+ * only; bf16/fp32 caches, not INT8).  The split-K partials go to a fixed
+ * array of KVC_NOALLOC_SCRATCH_BYTES inside the library, not to the state
+ * buffer's workspace.  The caller passes q and out; the cache is the handle's.
+ *
+ * The fixed array:
+ *   - Every GPU that loads the library holds it until the process exits.
+ *   - The first call on a device looks up the array's device address with that
+ *     device current.  Make that first call before any stream capture.
+ *   - Every call shares the array and overwrites it.  Each call writes every
+ *     partial it reads, so nothing has to start at zero.
+ *   - Calls that overlap on the GPU race on the array, even on different
+ *     handles or streams: serialise them.
+ *
+ * Errors:
+ *   - KVC_ERR_CAPACITY if the problem needs more than the array holds, that is
+ *     if B*Hq*splits*(8 + 4*d) bytes (+ alignment) exceed KVC_NOALLOC_SCRATCH_BYTES,
+ *     with splits = ceil(min(capacity, window) / 128) for bf16 d=64/128 caches,
+ *     else / 64.
+ *   - KVC_ERR_ARG for the cases kvc_decode_attn refuses, or if the current device
+ *     is not the handle's.
+ *   - KVC_ERR_UNSUPPORTED for an INT8 cache.
+ * It calls no cudaMalloc, cudaFree or other allocating routine. */
+#define KVC_NOALLOC_SCRATCH_BYTES (64u << 20)
+int kvc_decode_attn_noalloc(kvc_t h, const void* d_q, void* d_out, kvc_stream_t stream);
+
 /* Continue every request from next_position = h_cut[b] ([PREFIX]
  * "哪些東西必須一起裁剪": keep k[:cut], v[:cut], positions[:cut]; next_position
  * = cut).  h_cut: host, B entries, 0 <= cut <= next_position.  Rows at

@@ -81,6 +81,7 @@ def lib() -> ctypes.CDLL:
                 "kvc_next_positions": [P, P],
                 "kvc_device_status": [P, P, ctypes.POINTER(i32)],
                 "kvc_prefix_cut": [P, i32, P, i32, i32, ctypes.POINTER(i32)],
+                "kvc_decode_attn_noalloc": [P, P, P, P],
             }
             for name, args in sig.items():
                 fn = getattr(L, name)
@@ -168,6 +169,18 @@ def kvc_decode_attn(h, q, out, cmax=None, tanh=None, ct=None, stream=None) -> No
     _check(lib().kvc_decode_attn(h, _dev(q, name="q"), _dev(out, name="out"), _dev(cmax, torch.float32, name="cmax"),
                                  _dev(tanh, torch.float32, name="tanh"), _dev(ct, torch.float32, name="ct"),
                                  _stream(stream)), "kvc_decode_attn")
+
+
+KVC_NOALLOC_SCRATCH_BYTES = 64 << 20
+
+
+def kvc_decode_attn_noalloc(h, q, out, stream=None) -> None:
+    """Decode attention whose split-K scratch is the library's fixed device array.
+
+    For callers that cannot allocate device memory while they decode; see
+    include/kvc.h.  Calls that overlap on the GPU share (and race on) that array."""
+    _check(lib().kvc_decode_attn_noalloc(h, _dev(q, name="q"), _dev(out, name="out"), _stream(stream)),
+           "kvc_decode_attn_noalloc")
 
 
 def kvc_trim(h, cuts: Sequence[int], stream=None) -> None:
