@@ -124,12 +124,14 @@ class FullCacheBench:
 
     CYCLE = 128
 
-    def __init__(self, device):
+    def __init__(self, device, batch=None):
         import torch
         from kv_cache_decode_ring_gb300 import kvc
         from kv_cache_decode_ring_gb300 import workloads as wl
         self.torch, self.kvc = torch, kvc
         self.w = w = wl.full_cache_mha()
+        if batch:
+            w.batch = batch                   # smaller case for profiler captures
         self.ctx = w.extra["context"]
         self.cache = kvc.Cache.from_workload(w, device=device)
         k, v = w.prefill_chunk(0, self.ctx, device=device)
@@ -247,6 +249,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--batch", type=int, default=0, help="override the batch (profiling a smaller case)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -269,7 +272,7 @@ def main():
 
     from __graft_entry__ import build
     build()
-    bench = FullCacheBench("cuda")
+    bench = FullCacheBench("cuda", args.batch)
     peak, peak_kind = hbm_peak()
 
     def barrier():

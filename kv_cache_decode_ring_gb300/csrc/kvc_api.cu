@@ -36,6 +36,10 @@ bool make_shape(const kvc_config& c, Shape* s) {
     if (ring && c.window != 0 && c.window != c.capacity) return false;
     const bool int8 = c.kv_quant == KVC_QUANT_INT8;
     if (int8 && (c.dtype != KVC_BF16 || ring || c.head_dim % kBands || c.capacity % kQBlock)) return false;
+    if (int8) {
+        const int g = c.n_q_heads / c.n_kv_heads;
+        if ((c.head_dim != 64 && c.head_dim != 128) || (g != 1 && g != 2 && g != 4 && g != 8)) return false;
+    }
     const bool rope = c.rope_base > 0.f;
     int P = 0;
     if (rope) {
@@ -51,6 +55,11 @@ bool make_shape(const kvc_config& c, Shape* s) {
     if (s->bf16 && !int8 && (s->d == 64 || s->d == 128) && s->g <= 8) s->split = kFastSplit;
     const long long keys = (s->W > 0 && s->W < s->S) ? s->W : s->S;
     s->max_splits = (int)((keys + s->split - 1) / s->split);
+    if (int8) {
+        // quantized splits of kInt8Split keys plus one split for the exact tail rows
+        s->split = kInt8Split;
+        s->max_splits = (int)((keys + kInt8Split - 1) / kInt8Split) + 1;
+    }
     return true;
 }
 
@@ -77,6 +86,7 @@ Layout make_layout(const Shape& s) {
     L.rope = take((size_t)s.P * (d / 2) * 8);
     L.part_ml = take(B * Hq * s.max_splits * 8);
     L.part_acc = take(B * Hq * s.max_splits * d * 4);
+    if (s.int8) L.part_c = take(B * Hq * s.max_splits * 4);
     L.total = o;
     return L;
 }

@@ -18,6 +18,7 @@ constexpr int kQBlock = 16;           // tokens per INT8 quantization block
 constexpr int kBands = 16;            // witness bands per key row
 constexpr int kGenericSplit = 64;     // keys per split, generic decode kernel
 constexpr int kFastSplit = 128;       // keys per split, bf16 fast decode kernel
+constexpr int kInt8Split = 128;       // keys per quantized split, INT8 decode kernel
 constexpr uint32_t kErrPosition = 1u; // device error bits (sticky, cleared by kvc_device_status)
 constexpr uint32_t kErrWait = 2u;
 
@@ -34,6 +35,7 @@ struct Layout {
     size_t rope;      // float2 [P][d/2] {cos, sin}
     size_t part_ml;   // float2 [B][Hq][max_splits] {m (log2 domain), l}
     size_t part_acc;  // float  [B][Hq][max_splits][d]
+    size_t part_c;    // float  [B][Hq][max_splits] max_t c_t of the split   (INT8)
     size_t total;
 };
 

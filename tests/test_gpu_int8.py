@@ -1,0 +1,137 @@
+"""GPU parity of the INT8 tier: block quantizer and witnesses bit-exact, fused decode
+within tolerance of attention over the dequantized cache, and the bound sound.
+
+[WITCERT] "WitCert: Sound Runtime Risk Observability and Gating for KV-Cache Quantization"
+  "频带酉性与双层证书": w_{t,b} = ||r_{t,b}||, c_t = (1/sqrt d) sum_b ||q_b|| w_{t,b} >= |q.r_t|/sqrt d
+  "为什么在线监控 KV 误差如此困难？": TV <= tanh(max |eps|)
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from kv_cache_decode_ring_gb300 import kvc
+from kv_cache_decode_ring_gb300 import workloads as wl
+from oracle import numerics as nm
+from oracle.model import NBANDS, QBLOCK, DecodeOracle
+
+from _parity import assert_close, host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from kv_cache_decode_ring_gb300 import build
+    build.build()
+
+
+def _oracle(w):
+    return DecodeOracle(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, "contiguous", w.capacity, 0,
+                        w.rope_base, "bf16", "int8")
+
+
+def check_int8_state(cache, model, requests=None):
+    """Codes, scales, witnesses of every complete block and the exact tail rows, bit-exact."""
+    KQ = cache.export(kvc.KVC_EXPORT_KQ); VQ = cache.export(kvc.KVC_EXPORT_VQ)
+    SK = cache.export(kvc.KVC_EXPORT_SK); SV = cache.export(kvc.KVC_EXPORT_SV)
+    WT = cache.export(kvc.KVC_EXPORT_WITNESS)
+    KT = cache.export(kvc.KVC_EXPORT_KTAIL); VT = cache.export(kvc.KVC_EXPORT_VTAIL)
+    pos = cache.export(kvc.KVC_EXPORT_POSITIONS)
+    assert np.array_equal(pos, model.expected_positions())
+    for b in (range(model.B) if requests is None else requests):
+        n = model.length(b)
+        nfull = n // QBLOCK * QBLOCK
+        for h in range(model.Hkv):
+            for blk in range(nfull // QBLOCK):
+                sK, cK, sV, cV, wit = model.quantized_block(b, h, blk)
+                sl = slice(blk * QBLOCK, (blk + 1) * QBLOCK)
+                assert SK[b, h, blk] == sK and SV[b, h, blk] == sV, (b, h, blk)
+                assert np.array_equal(KQ[b, h, sl], cK) and np.array_equal(VQ[b, h, sl], cV), (b, h, blk)
+                assert np.array_equal(WT[b, h, sl], wit), (b, h, blk)
+            for p in range(nfull, n):
+                assert np.array_equal(KT[b, h, p % QBLOCK], nm.f32_to_bf16(model.hk[b][p][h])), (b, h, p)
+                assert np.array_equal(VT[b, h, p % QBLOCK], nm.f32_to_bf16(model.hv[b][p][h])), (b, h, p)
+
+
+def check_decode(cache, model, q, heads=None):
+    B, Hq = model.B, model.Hq
+    out = torch.empty((B, Hq, model.d), dtype=torch.float32, device="cuda")
+    cmax = torch.full((B, Hq), -1.0, device="cuda")
+    th = torch.full((B, Hq), -1.0, device="cuda")
+    ct = torch.full((B, Hq, cache.S), -7.0, device="cuda")
+    kvc.kvc_decode_attn(cache.h, q.cuda(), out, cmax, th, ct)
+    res = model.decode_int8(host(q), heads)
+    cm, tc, ctn = cmax.cpu().numpy(), th.cpu().numpy(), ct.cpu().numpy()
+    for (b, hq), r in res.items():
+        assert_close(out[b, hq][None], r["out"][None], "bf16", "int8 decode b=%d h=%d" % (b, hq))
+        n = model.length(b)
+        c_gpu = ctn[b, hq, :n].astype(np.float64)
+        # the bound on every token: sound (>= |q.r|/sqrt d and >= the exact c_t) and tight
+        assert np.all(c_gpu >= r["eps"]), (b, hq)
+        assert np.all(c_gpu >= r["c"] * (1 - 1e-12)), (b, hq)
+        assert np.all(c_gpu <= r["c"] * (1 + 1e-5) + 1e-30), (b, hq)
+        assert cm[b, hq] >= r["cmax"] * (1 - 1e-12) and cm[b, hq] <= r["cmax"] * (1 + 1e-5) + 1e-30
+        assert tc[b, hq] >= math.tanh(cm[b, hq]) * (1 - 1e-7) and tc[b, hq] <= 1.0
+        assert r["tv"] <= tc[b, hq], (b, hq, r["tv"], tc[b, hq])
+    return out
+
+
+@pytest.mark.parametrize("d,Hq,Hkv", [(128, 8, 2), (64, 8, 1), (128, 4, 4)])
+def test_int8_prefill_decode_parity(d, Hq, Hkv):
+    w = wl.small("int8-%d-%d-%d" % (d, Hq, Hkv), B=3, Hq=Hq, Hkv=Hkv, d=d, capacity=512, rope_base=10000.0,
+                 quant="int8", seed=19, outliers=(4, 20.0))
+    cache = kvc.Cache.from_workload(w, out_dtype="f32")
+    model = _oracle(w)
+    lengths = [1, 37, 300]
+    k, v = w.prefill_chunk(0, max(lengths))
+    cache.append_rows(k.cuda(), v.cuda(), counts=lengths)
+    model.append_rows(host(k), host(v), lengths)
+    check_int8_state(cache, model)
+    for s in range(20):                          # crosses block completions on single appends
+        q, k1, v1 = w.step_qkv(s)
+        cache.append(k1.cuda(), v1.cuda())
+        model.append(host(k1), host(v1))
+        if s % 4 == 3 or s == 0:
+            check_int8_state(cache, model)
+        check_decode(cache, model, q)
+    assert cache.device_status() == 0
+
+
+def test_int8_trim_rules_and_continue():
+    w = wl.small("int8-trim", B=2, Hq=4, Hkv=2, d=128, capacity=256, rope_base=10000.0, quant="int8", seed=5)
+    cache = kvc.Cache.from_workload(w, out_dtype="f32")
+    model = _oracle(w)
+    k, v = w.prefill_chunk(0, 100)
+    cache.append_rows(k.cuda(), v.cuda(), counts=[100, 70])
+    model.append_rows(host(k), host(v), [100, 70])
+    with pytest.raises(kvc.KvcError) as e:
+        cache.trim([90, 70])                     # 90 splits the quantized block 80..95
+    assert e.value.code == kvc.KVC_ERR_EVICTED
+    cache.trim([98, 64])                         # 98: inside the exact tail; 64: a block boundary
+    model.trim([98, 64])
+    check_int8_state(cache, model)
+    for s in range(20):
+        q, k1, v1 = w.step_qkv(s)
+        cache.append(k1.cuda(), v1.cuda())
+        model.append(host(k1), host(v1))
+        check_decode(cache, model, q)
+    check_int8_state(cache, model)
+
+
+def test_int8_zero_residual_gives_zero_bound():
+    # keys on their blocks' quantization grid: residual 0, witnesses 0, bound 0
+    w = wl.small("int8-exact", B=1, Hq=2, Hkv=1, d=128, capacity=64, rope_base=0.0, quant="int8", seed=2)
+    cache = kvc.Cache.from_workload(w, out_dtype="f32")
+    model = _oracle(w)
+    rng = np.random.default_rng(4)
+    c = rng.integers(-126, 127, (1, 1, 48, 128)).astype(np.float32)
+    c[..., 0] = 127.0
+    k = torch.from_numpy(c / 16).to(torch.bfloat16)
+    v = torch.from_numpy(rng.standard_normal((1, 1, 48, 128)).astype(np.float32)).to(torch.bfloat16)
+    cache.append_rows(k.cuda(), v.cuda())
+    model.append_rows(host(k), host(v), [48])
+    assert not cache.export(kvc.KVC_EXPORT_WITNESS).any()
+    q = w.queries((1, 2, 128), "zero-residual")
+    check_decode(cache, model, q)
