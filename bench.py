@@ -119,37 +119,23 @@ def kv_bytes_per_step(nkeys_per_request, Hkv, d, elem=2):
     return sum(nkeys_per_request) * Hkv * d * 2 * elem
 
 
-class FullCacheBench:
-    """Full-cache MHA decode, bf16: B=32, H=32, d=128, contiguous 8192, context 4096 + steps."""
+class DecodeBench:
+    """Common driver: a cache, a cycle of per-step inputs on the device, and the step
+    ``kvc_append`` + ``kvc_decode_attn``.  Subclasses fill the cache and count bytes."""
 
-    CYCLE = 128
+    CYCLE = 64
+    kernel = "kvc_decode_attn (split-K decode + combine)"
 
-    def __init__(self, device, batch=None):
+    def _inputs(self, device):
         import torch
-        from kv_cache_decode_ring_gb300 import kvc
-        from kv_cache_decode_ring_gb300 import workloads as wl
-        self.torch, self.kvc = torch, kvc
-        self.w = w = wl.full_cache_mha()
-        if batch:
-            w.batch = batch                   # smaller case for profiler captures
-        self.ctx = w.extra["context"]
-        self.cache = kvc.Cache.from_workload(w, device=device)
-        k, v = w.prefill_chunk(0, self.ctx, device=device)
-        self.cache.append_rows(k, v)
-        del k, v
+        w = self.w
         steps = [w.step_qkv(s, device=device) for s in range(self.CYCLE)]
         self.q = [s[0] for s in steps]
         self.k = [s[1] for s in steps]
         self.v = [s[2] for s in steps]
         self.out = torch.empty_like(self.q[0])
-        self.i = 0
+        self.done = 0
         torch.cuda.synchronize()
-        self.cuts = [self.ctx] * w.batch
-
-    def units(self, i):
-        """KV bytes read by the decode of global step i (context ctx + i mod CYCLE + 1)."""
-        n = self.ctx + (i % self.CYCLE) + 1
-        return kv_bytes_per_step([n] * self.w.batch, self.w.n_kv_heads, self.w.head_dim)
 
     def io_bytes(self):
         w = self.w
@@ -158,23 +144,26 @@ class FullCacheBench:
     def launches_per_step(self):
         return 3                                                 # append, split-K decode, combine
 
-    def step(self, i, ev=None):
-        j = i % self.CYCLE
-        extra = 0
-        if j == 0 and i > 0:
-            self.cache.trim(self.cuts)
-            extra = 1
+    def before_step(self):
+        return 0                                                 # extra launches (e.g. a trim)
+
+    def decode(self, q):
+        self.cache.decode(q, self.out)
+
+    def step(self, ev=None):
+        j = self.done % self.CYCLE
+        extra = self.before_step()
         self.cache.append(self.k[j], self.v[j])
         if ev is not None:
             ev[0].record()
-        self.cache.decode(self.q[j], self.out)
+        self.decode(self.q[j])
         if ev is not None:
             ev[1].record()
+        self.done += 1
         return extra
 
-    # end-to-end: host inputs, copies inside the timing
     def e2e_setup(self):
-        torch = self.torch
+        import torch
         self.hq = [t.cpu().pin_memory() for t in self.q]
         self.hk = [t.cpu().pin_memory() for t in self.k]
         self.hv = [t.cpu().pin_memory() for t in self.v]
@@ -185,39 +174,170 @@ class FullCacheBench:
         return sum(t.numel() * t.element_size() for t in (self.hq[0], self.hk[0], self.hv[0])), \
             self.hout.numel() * self.hout.element_size()
 
-    def e2e_step(self, i):
-        j = i % self.CYCLE
-        if j == 0 and i > 0:
-            self.cache.trim(self.cuts)
+    def e2e_step(self):
+        j = self.done % self.CYCLE
+        self.before_step()
         self.dq.copy_(self.hq[j], non_blocking=True)
         self.dk.copy_(self.hk[j], non_blocking=True)
         self.dv.copy_(self.hv[j], non_blocking=True)
         self.cache.append(self.dk, self.dv)
-        self.cache.decode(self.dq, self.out)
+        self.decode(self.dq)
         self.hout.copy_(self.out, non_blocking=True)
+        self.done += 1
+
+
+class FullCacheBench(DecodeBench):
+    """Full-cache MHA decode, bf16: B=32, H=32, d=128, contiguous 8192, context 4096 + steps;
+    every 128 steps the requests are trimmed back to 4096."""
+
+    CYCLE = 128
+
+    def __init__(self, device, batch=None, total_steps=0):
+        from kv_cache_decode_ring_gb300 import kvc
+        from kv_cache_decode_ring_gb300 import workloads as wl
+        self.w = w = wl.full_cache_mha()
+        if batch:
+            w.batch = batch                   # smaller case for profiler captures
+        self.ctx = w.extra["context"]
+        self.cache = kvc.Cache.from_workload(w, device=device)
+        k, v = w.prefill_chunk(0, self.ctx, device=device)
+        self.cache.append_rows(k, v)
+        del k, v
+        self.cuts = [self.ctx] * w.batch
+        self._inputs(device)
+
+    def before_step(self):
+        if self.done % self.CYCLE == 0 and self.done > 0:
+            self.cache.trim(self.cuts)
+            return 1
+        return 0
+
+    def units(self):
+        """KV bytes read by the decode of the step about to run (the cycle position is done mod 128)."""
+        n = self.ctx + (self.done % self.CYCLE) + 1
+        return kv_bytes_per_step([n] * self.w.batch, self.w.n_kv_heads, self.w.head_dim)
 
     def reset(self):
+        import torch
         self.cache.trim(self.cuts)
-        self.torch.cuda.synchronize()
+        self.done = 0
+        torch.cuda.synchronize()
+
+    def cpu_problem(self):
+        return self.ctx + 1, 1
 
     def config(self):
         w = self.w
         return {"workload": w.name, "batch": w.batch, "n_q_heads": w.n_q_heads, "n_kv_heads": w.n_kv_heads,
                 "head_dim": w.head_dim, "layout": "contiguous", "max_seq_len": w.capacity,
                 "context": "%d + step (cycles %d..%d keys)" % (self.ctx, self.ctx + 1, self.ctx + self.CYCLE),
-                "l2": "inputs larger than L2: %.2f GB of K/V read per step vs 129 MB L2" % (self.units(0) / 1e9)}
+                "l2": "inputs larger than L2: %.2f GB of K/V read per step vs 129 MB L2"
+                      % (kv_bytes_per_step([self.ctx + 1] * w.batch, w.n_kv_heads, w.head_dim) / 1e9)}
+
+
+class SlidingWindowBench(DecodeBench):
+    """Sliding-window GQA decode, bf16: B=64, Hq=32, Hkv=8, d=128, ring W=4096, RoPE 10000,
+    request b starts at position L_b - 1 (L_b uniform in [1, 32768]) and advances one token a step."""
+
+    def __init__(self, device, batch=None, total_steps=0):
+        from kv_cache_decode_ring_gb300 import kvc
+        from kv_cache_decode_ring_gb300 import workloads as wl
+        self.w = w = wl.sliding_window_gqa()
+        self.W = w.capacity
+        self.L = list(w.extra["lengths"])
+        maxp = w.extra["max_len"] + total_steps + 64
+        self.cache = kvc.Cache.from_workload(w, max_position=maxp, device=device)
+        chunk = 4096
+        for c in range((max(self.L) + chunk - 1) // chunk):
+            counts = [int(min(max(L - 1 - c * chunk, 0), chunk)) for L in self.L]
+            if any(counts):
+                k, v = w.prefill_chunk(c, chunk, device=device)
+                self.cache.append_rows(k, v, counts=counts)
+                del k, v
+        self._inputs(device)
+
+    def units(self):
+        n = [min(L + self.done, self.W) for L in self.L]
+        return kv_bytes_per_step(n, self.w.n_kv_heads, self.w.head_dim)
+
+    def reset(self):
+        import torch
+        torch.cuda.synchronize()              # a ring keeps advancing; nothing to undo
+
+    def cpu_problem(self):
+        return self.W, self.w.n_q_heads // self.w.n_kv_heads
+
+    def config(self):
+        w = self.w
+        return {"workload": w.name, "batch": w.batch, "n_q_heads": w.n_q_heads, "n_kv_heads": w.n_kv_heads,
+                "head_dim": w.head_dim, "layout": "ring", "window": self.W, "rope_base": w.rope_base,
+                "context": "L_b - 1 + step, L_b uniform in [1, 32768] (seed 23)",
+                "l2": "inputs larger than L2: %.2f GB of K/V read per step vs 129 MB L2" % (self.units() / 1e9)}
+
+
+class Int8Bench(DecodeBench):
+    """INT8 KV with witnesses: B=8, Hq=32, Hkv=8, d=128, context 131072 prefilled through the
+    block quantizer; each step appends one token and runs the fused decode + bound."""
+
+    kernel = "kvc_decode_attn INT8 (fused decode + witness bound + combine)"
+
+    def __init__(self, device, batch=None, total_steps=0):
+        import torch
+        from kv_cache_decode_ring_gb300 import kvc
+        from kv_cache_decode_ring_gb300 import workloads as wl
+        self.w = w = wl.int8_witness()
+        self.ctx = w.extra["context"]
+        w.capacity = self.ctx + 16 * ((total_steps + 16 + 15) // 16)
+        self.cache = kvc.Cache.from_workload(w, device=device)
+        chunk = 8192
+        for c in range(self.ctx // chunk):
+            k, v = w.prefill_chunk(c, chunk, device=device)
+            self.cache.append_rows(k, v)
+            del k, v
+        B, Hq = w.batch, w.n_q_heads
+        self.cmax = torch.empty((B, Hq), device=device)
+        self.tanh = torch.empty((B, Hq), device=device)
+        self._inputs(device)
+
+    def decode(self, q):
+        self.cache.decode(q, self.out, self.cmax, self.tanh)
+
+    def units(self):
+        """Bytes the fused decode reads: codes, witnesses and scales of complete blocks, exact tail rows."""
+        w = self.w
+        n = self.ctx + self.done + 1
+        nfull = n // 16 * 16
+        per_head = nfull * (2 * w.head_dim + 32) + (nfull // 16) * 8 + (n - nfull) * 4 * w.head_dim
+        return w.batch * w.n_kv_heads * per_head
+
+    def reset(self):
+        import torch
+        torch.cuda.synchronize()
+
+    def cpu_problem(self):
+        return 4096, self.w.n_q_heads // self.w.n_kv_heads
+
+    def config(self):
+        w = self.w
+        return {"workload": w.name, "batch": w.batch, "n_q_heads": w.n_q_heads, "n_kv_heads": w.n_kv_heads,
+                "head_dim": w.head_dim, "layout": "contiguous int8 + witnesses", "context": "131072 + step",
+                "l2": "inputs larger than L2: %.2f GB read per step vs 129 MB L2" % (self.units() / 1e9)}
+
+
+BENCHES = {"full-cache-mha": FullCacheBench, "sliding-window-gqa": SlidingWindowBench, "int8-witness": Int8Bench}
 
 
 # ----------------------------------------------------------------------------- CPU oracle
 
-def oracle_sample(w, seconds: float, threads: int, heads_per_call=None):
+def oracle_sample(w, seconds: float, threads: int, heads_per_call=None, problem=None):
     """Time the oracle's fp64 attention (C, OpenMP) on (request, KV head) problems of the
-    workload at context ctx+1; returns (GB/s of KV bytes, seconds, problems, description)."""
+    workload (``problem`` = (keys, query heads per KV head)); returns (GB/s of KV bytes,
+    seconds, problems, description)."""
     import numpy as np
     from kv_cache_decode_ring_gb300 import workloads as wl
     from oracle import numerics as nm
-    ctx = w.extra.get("context", 4096) + 1
-    d, g = w.head_dim, w.n_q_heads // w.n_kv_heads
+    ctx, g = problem if problem else (w.extra.get("context", 4096) + 1, w.n_q_heads // w.n_kv_heads)
+    d = w.head_dim
     nprob = heads_per_call or max(threads, 8)
     k = wl.as_numpy(w.keys((nprob, ctx, d), "cpu-sample"))
     v = wl.as_numpy(w.values((nprob, ctx, d), "cpu-sample"))
@@ -250,6 +370,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--batch", type=int, default=0, help="override the batch (profiling a smaller case)")
+    ap.add_argument("--workload", default="full-cache-mha", choices=sorted(BENCHES),
+                    help="full-cache-mha (the headline line), sliding-window-gqa or int8-witness")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -272,7 +394,8 @@ def main():
 
     from __graft_entry__ import build
     build()
-    bench = FullCacheBench("cuda", args.batch)
+    e2e_steps = 0 if args.no_e2e else min(args.steps, 400) + 3
+    bench = BENCHES[args.workload]("cuda", args.batch, args.warmup + args.steps + e2e_steps)
     peak, peak_kind = hbm_peak()
 
     def barrier():
@@ -283,7 +406,7 @@ def main():
     # warm-up
     launches = 0
     for i in range(args.warmup):
-        bench.step(i)
+        bench.step()
     bench.reset()
 
     # timed region
@@ -297,9 +420,12 @@ def main():
     wall0 = time.perf_counter()
     t0e.record()
     units = 0
+    step_units = []
     for i in range(K):
-        launches += bench.launches_per_step() + bench.step(i, ev[i])
-        units += bench.units(i)
+        u = bench.units()
+        launches += bench.launches_per_step() + bench.step(ev[i])
+        units += u
+        step_units.append(u)
     t1e.record()
     barrier()
     wall = time.perf_counter() - wall0
@@ -316,7 +442,7 @@ def main():
     steps_per_s = K / (ms_total / 1e3)
 
     # roofline of the decode-attention call
-    attn_bytes = sum(bench.units(i) + bench.io_bytes() for i in range(K)) / K
+    attn_bytes = sum(u + bench.io_bytes() for u in step_units) / K
     attn_avg_ms = sum(attn_ms) / len(attn_ms)
     achieved = attn_bytes / (attn_avg_ms / 1e3) / 1e9
 
@@ -327,15 +453,15 @@ def main():
         hb, db = bench.e2e_setup()
         Ke = min(K, 400)
         for i in range(3):
-            bench.e2e_step(i)
+            bench.e2e_step()
         bench.reset()
         barrier()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
         eu = 0
         for i in range(Ke):
-            bench.e2e_step(i)
-            eu += bench.units(i)
+            eu += bench.units()
+            bench.e2e_step()
         b.record()
         barrier()
         ems = torch.tensor([a.elapsed_time(b)], device="cuda", dtype=torch.float64)
@@ -348,7 +474,7 @@ def main():
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        gbps, el, nprob, desc = oracle_sample(bench.w, args.cpu_seconds, threads)
+        gbps, el, nprob, desc = oracle_sample(bench.w, args.cpu_seconds, threads, problem=bench.cpu_problem())
         cpu = {"value": round(gbps, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
                "sample": desc + ", %.1f s" % el}
 
@@ -362,7 +488,7 @@ def main():
             "config": bench.config(),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": None,
-                         "kernel": "kvc_decode_attn (split-K decode + combine)", "peak_kind": peak_kind,
+                         "kernel": bench.kernel, "peak_kind": peak_kind,
                          "bytes_per_launch": int(attn_bytes), "avg_launch_ms": round(attn_avg_ms, 5)},
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
             "wall_s": round(wall, 3),

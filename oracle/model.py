@@ -230,70 +230,83 @@ class DecodeOracle:
         return sK, cK, sV, cV, wit
 
     def int8_view(self, b, h, lo=0, hi=None):
-        """Rows [lo, hi) of (b, h) as attention sees them in the INT8 tier.
-
-        Returns (K_deq, V_deq, K_exact, resid, wit_values): dequantized rows
-        (code*s, exact in fp64) for complete blocks and exact bf16 rows for the
-        tail; the exact stored keys; the key residual (0 in the tail); the witness
-        values (0 in the tail).  ``lo`` must be a block boundary.
-        """
+        """Rows [lo, hi) of (b, h) as attention sees them in the INT8 tier (see :func:`int8_rows`)."""
         n = self.length(b)
         hi = n if hi is None else hi
-        assert lo % QBLOCK == 0
-        nfull = (n // QBLOCK) * QBLOCK
-        Kd, Vd, Kx, R, W = [], [], [], [], []
-        for blk in range(lo // QBLOCK, (hi + QBLOCK - 1) // QBLOCK):
-            p_lo = blk * QBLOCK
-            p_hi = min(p_lo + QBLOCK, hi)
-            kx = np.stack([self.hk[b][p][h] for p in range(p_lo, p_hi)]).astype(np.float64)
-            vx = np.stack([self.hv[b][p][h] for p in range(p_lo, p_hi)]).astype(np.float64)
-            if p_lo + QBLOCK <= nfull:
-                sK, cK, sV, cV, wit = self.quantized_block(b, h, blk)
-                m = p_hi - p_lo
-                kd = cK[:m].astype(np.float64) * np.float64(sK)
-                vd = cV[:m].astype(np.float64) * np.float64(sV)
-                Kd.append(kd); Vd.append(vd); Kx.append(kx)
-                R.append(kx - kd); W.append(nm.f16_values(wit[:m]))
-            else:
-                Kd.append(kx); Vd.append(vx); Kx.append(kx)
-                R.append(np.zeros_like(kx)); W.append(np.zeros((p_hi - p_lo, NBANDS)))
-        cat = lambda xs, w: np.concatenate(xs) if xs else np.zeros((0, w))  # noqa: E731
-        return (cat(Kd, self.d), cat(Vd, self.d), cat(Kx, self.d), cat(R, self.d), cat(W, NBANDS))
+        K = np.stack([self.hk[b][p][h] for p in range(lo, hi)]) if hi > lo else np.zeros((0, self.d), np.float32)
+        V = np.stack([self.hv[b][p][h] for p in range(lo, hi)]) if hi > lo else np.zeros((0, self.d), np.float32)
+        return int8_rows(K, V, lo, (n // QBLOCK) * QBLOCK)
 
     def decode_int8(self, q, heads=None):
-        """INT8-tier decode of the newest token for the listed (b, query head) pairs.
-
-        Returns a dict (b, hq) -> {"out": attention over the dequantized cache
-        (fp64), "out_exact": over the exact bf16 cache, "c": c_t per key in the
-        window, "eps": |q . r_t| / sqrt(d) per key, "tv": total variation between
-        the exact and the dequantized softmax, "cmax": max_t c_t, "q": the fp32
-        rotated query}.  c_t = (1/sqrt d) sum_b ||q_b|| w_{t,b} ([WITCERT]
-        "频带酉性与双层证书"); all of it in fp64 from the fp32 query and the stored
-        witness values.
-        """
+        """INT8-tier decode of the newest token for the listed (b, query head) pairs
+        (all by default); see :func:`int8_decode_one` for the returned fields."""
         res = {}
         if heads is None:
             heads = [(b, hq) for b in range(self.B) for hq in range(self.Hq)]
-        bw = self.d // NBANDS
         for (b, hq) in heads:
             t = self.length(b) - 1
             qf = self.query_rows(np.asarray(q)[b, hq:hq + 1], np.full(1, t))[0]
-            q64 = qf.astype(np.float64)
             lo = 0 if not self.window else max(0, t - self.window + 1)
             lo_blk = (lo // QBLOCK) * QBLOCK
-            Kd, Vd, Kx, R, W = self.int8_view(b, hq // self.g, lo_blk, t + 1)
-            Vx = np.stack([self.hv[b][p][hq // self.g] for p in range(lo_blk, t + 1)]).astype(np.float64)
-            out = nm.attend(q64, Kd, Vd, t, self.window, p0=lo_blk)[0]
-            out_exact = nm.attend(q64, Kx, Vx, t, self.window, p0=lo_blk)[0]
-            p_deq = nm.softmax_weights(q64, Kd, t, self.window, p0=lo_blk)
-            p_ex = nm.softmax_weights(q64, Kx, t, self.window, p0=lo_blk)
-            qn = np.sqrt((q64.reshape(NBANDS, bw) ** 2).sum(axis=1))
-            c = (W * qn[None, :]).sum(axis=1) / math.sqrt(self.d)
-            eps = np.abs(R @ q64) / math.sqrt(self.d)
-            vis = slice(lo - lo_blk, None)
-            res[(b, hq)] = {
-                "out": out, "out_exact": out_exact, "c": c[vis], "eps": eps[vis],
-                "tv": 0.5 * np.abs(p_ex - p_deq).sum(), "cmax": float(c[vis].max()) if c[vis].size else 0.0,
-                "q": qf,
-            }
+            h = hq // self.g
+            K = np.stack([self.hk[b][p][h] for p in range(lo_blk, t + 1)])
+            V = np.stack([self.hv[b][p][h] for p in range(lo_blk, t + 1)])
+            res[(b, hq)] = int8_decode_one(qf, K, V, lo_blk, t, self.window, (self.length(b) // QBLOCK) * QBLOCK)
         return res
+
+
+def int8_rows(K, V, p0, nfull):
+    """Rows at positions p0.. of one (request, KV head) as the INT8 tier holds them.
+
+    ``K``, ``V``: [n, d] exact stored rows (fp32 values of the bf16 cache); ``p0`` a
+    block boundary; positions below ``nfull`` lie in complete blocks.  Returns
+    (K_deq, V_deq, K_exact, resid, wit_values), all fp64: complete blocks
+    dequantized (code * s, exact in fp64) with their key residuals and witness
+    values; the exact tail rows with residual 0 and witness 0
+    ([WITCERT] "频带酉性与双层证书"; "SGLang 生产级落地与闭环门控修复").
+    """
+    n, d = K.shape
+    assert p0 % QBLOCK == 0
+    Kd = K.astype(np.float64).copy()
+    Vd = V.astype(np.float64).copy()
+    R = np.zeros((n, d))
+    Wt = np.zeros((n, NBANDS))
+    for r0 in range(0, n, QBLOCK):
+        if p0 + r0 + QBLOCK > nfull or r0 + QBLOCK > n:
+            break
+        sl = slice(r0, r0 + QBLOCK)
+        sK, cK = nm.quantize_block(K[sl])
+        sV, cV = nm.quantize_block(V[sl])
+        Kd[sl] = cK.astype(np.float64) * np.float64(sK)
+        Vd[sl] = cV.astype(np.float64) * np.float64(sV)
+        R[sl] = K[sl].astype(np.float64) - Kd[sl]
+        Wt[sl] = np.stack([nm.f16_values(nm.witness_row(K[r0 + i], cK[i], sK, NBANDS)) for i in range(QBLOCK)])
+    return Kd, Vd, K.astype(np.float64), R, Wt
+
+
+def int8_decode_one(qf, K, V, p0, t, window, nfull):
+    """INT8-tier decode of one query row over rows p0..t of one KV head, fp64.
+
+    Returns {"out": attention over the dequantized rows, "out_exact": over the
+    exact bf16 rows, "c": c_t per key in the window, "eps": |q . r_t| / sqrt(d),
+    "tv": total variation between the exact and the dequantized softmax,
+    "cmax": max_t c_t, "q": the fp32 query}.  c_t = (1/sqrt d) sum_b ||q_b|| w_{t,b}
+    ([WITCERT] "频带酉性与双层证书") from the fp32 query and the stored witnesses.
+    """
+    d = K.shape[1]
+    bw = d // NBANDS
+    q64 = np.asarray(qf, dtype=np.float64)
+    Kd, Vd, Kx, R, W = int8_rows(K, V, p0, nfull)
+    Vx = V.astype(np.float64)
+    out = nm.attend(q64, Kd, Vd, t, window, p0=p0)[0]
+    out_exact = nm.attend(q64, Kx, Vx, t, window, p0=p0)[0]
+    p_deq = nm.softmax_weights(q64, Kd, t, window, p0=p0)
+    p_ex = nm.softmax_weights(q64, Kx, t, window, p0=p0)
+    qn = np.sqrt((q64.reshape(NBANDS, bw) ** 2).sum(axis=1))
+    c = (W * qn[None, :]).sum(axis=1) / math.sqrt(d)
+    eps = np.abs(R @ q64) / math.sqrt(d)
+    lo = 0 if not window else max(0, t - window + 1)
+    vis = slice(lo - p0, None)
+    return {"out": out, "out_exact": out_exact, "c": c[vis], "eps": eps[vis],
+            "tv": 0.5 * np.abs(p_ex - p_deq).sum(), "cmax": float(c[vis].max()) if c[vis].size else 0.0,
+            "q": qf}

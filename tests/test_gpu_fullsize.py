@@ -155,3 +155,63 @@ def test_one_request_through_the_ring_phases():
         pos = cache.export(kvc.KVC_EXPORT_POSITIONS)[0]
         assert _ring_positions_ok(pos, t + 1, W), t
     assert cache.device_status() == 0
+
+
+def test_int8_witness_sampled():
+    # INT8 KV with witnesses: B=8, Hq=32, Hkv=8, d=128, context 131072 prefilled through the
+    # block quantizer, then 16 one-token steps (the last completes a block)
+    import math
+    from oracle.model import QBLOCK, int8_decode_one
+    w = wl.int8_witness()
+    ctx = w.extra["context"]
+    cache = kvc.Cache.from_workload(w)
+    model = oracle_for(w)
+    g = w.n_q_heads // w.n_kv_heads
+    sample = [(0, 0), (5, 6)]
+    keep = {bh: ([], []) for bh in sample}
+    chunk = 8192
+    for c in range(ctx // chunk):
+        k, v = w.prefill_chunk(c, chunk, device="cuda")
+        cache.append_rows(k, v)
+        for (b, h) in sample:
+            keep[(b, h)][0].append(host(k[b, h])); keep[(b, h)][1].append(host(v[b, h]))
+        del k, v
+    cmax = torch.empty((w.batch, w.n_q_heads), device="cuda")
+    th = torch.empty((w.batch, w.n_q_heads), device="cuda")
+    for s in range(16):
+        q, k1, v1 = w.step_qkv(s, device="cuda")
+        cache.append(k1, v1)
+        out = cache.decode(q, None, cmax, th)
+        for (b, h) in sample:
+            keep[(b, h)][0].append(host(k1[b, h])[None]); keep[(b, h)][1].append(host(v1[b, h])[None])
+        if s not in (0, 15):
+            continue
+        t = ctx + s
+        nfull = (t + 1) // QBLOCK * QBLOCK
+        o, cm, tc = out.float().cpu(), cmax.cpu().numpy(), th.cpu().numpy()
+        for (b, h) in sample:
+            Kin = np.concatenate(keep[(b, h)][0]); Vin = np.concatenate(keep[(b, h)][1])
+            K = model.stored_rows(Kin, np.arange(t + 1))
+            V = nm.bf16_to_f32(Vin)
+            for hq in (h * g, h * g + g - 1):
+                qr = model.query_rows(host(q[b, hq])[None], [t])[0]
+                r = int8_decode_one(qr, K, V, 0, t, 0, nfull)
+                assert_close(o[b, hq][None], r["out"][None], "bf16", "int8 full s=%d b=%d h=%d" % (s, b, hq))
+                assert cm[b, hq] >= r["cmax"] * (1 - 1e-12) and cm[b, hq] <= r["cmax"] * (1 + 1e-5)
+                assert tc[b, hq] >= math.tanh(cm[b, hq]) * (1 - 1e-7) and r["tv"] <= tc[b, hq]
+                assert np.all(r["eps"] <= r["c"] * (1 + 1e-12))
+    # a sample of blocks bit-exact: codes, scales, witnesses
+    from oracle import numerics as onm
+    KQ = cache.export(kvc.KVC_EXPORT_KQ); SK = cache.export(kvc.KVC_EXPORT_SK)
+    WT = cache.export(kvc.KVC_EXPORT_WITNESS)
+    for (b, h) in sample:
+        Kin = np.concatenate(keep[(b, h)][0])
+        n = Kin.shape[0]
+        for blk in (0, 1, 4095, 8191, n // QBLOCK - 1):
+            pos = np.arange(blk * QBLOCK, (blk + 1) * QBLOCK)
+            Kb = model.stored_rows(Kin[pos], pos)
+            sK, cK = onm.quantize_block(Kb)
+            assert SK[b, h, blk] == sK and np.array_equal(KQ[b, h, pos], cK), (b, h, blk)
+            wit = np.stack([onm.witness_row(Kb[i], cK[i], sK) for i in range(QBLOCK)])
+            assert np.array_equal(WT[b, h, pos], wit), (b, h, blk)
+    assert cache.device_status() == 0
