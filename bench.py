@@ -47,6 +47,15 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def tensor_peak():
+    """Dense bf16 TFLOP/s sustained over a seconds-long loop (the timed region is one)."""
+    try:
+        with open(PEAKS_FILE) as f:
+            return float(json.load(f)["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return 1700.0, "fallback"
+
+
 # ----------------------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -125,6 +134,9 @@ class DecodeBench:
 
     CYCLE = 64
     kernel = "kvc_decode_attn (split-K decode + combine)"
+    metric = METRIC
+    unit = "GB/s"
+    bound = "hbm"
 
     def _inputs(self, device):
         import torch
@@ -324,7 +336,104 @@ class Int8Bench(DecodeBench):
                 "l2": "inputs larger than L2: %.2f GB read per step vs 129 MB L2" % (self.units() / 1e9)}
 
 
-BENCHES = {"full-cache-mha": FullCacheBench, "sliding-window-gqa": SlidingWindowBench, "int8-witness": Int8Bench}
+class ChunkBench(DecodeBench):
+    """Prefix-reuse suffix recompute, bf16: 16 requests, Hq=32, Hkv=8, d=128, prefix 8192 rows
+    (RoPE 10000), cuts uniform in [0, 8191] (seed 7).  A step trims every request to its cut and
+    runs kvc_chunk_attn on a 512-token suffix (append, rotate, causal tcgen05 attention)."""
+
+    kernel = "kvc_chunk_attn (suffix append + query rotation + tcgen05 causal attention)"
+    metric = "chunked suffix attention FLOP/s (TFLOP/s, % of bf16 tensor peak) at 1 GB300"
+    unit = "TFLOP/s"
+    bound = "tensor"
+
+    def __init__(self, device, batch=None, total_steps=0, windowed=False):
+        import torch
+        from kv_cache_decode_ring_gb300 import kvc
+        from kv_cache_decode_ring_gb300 import workloads as wl
+        self.w = w = wl.prefix_reuse(windowed)
+        self.n = w.extra["suffix"]
+        self.cache = kvc.Cache.from_workload(w, max_chunk=self.n, device=device)
+        pre = w.extra["prefix"]
+        for c in range(pre // 2048):
+            k, v = w.keys((w.batch, w.n_kv_heads, 2048, w.head_dim), "prefix%d" % c, device), \
+                w.values((w.batch, w.n_kv_heads, 2048, w.head_dim), "prefix%d" % c, device)
+            self.cache.append_rows(k, v)
+            del k, v
+        self.cuts = list(w.extra["cuts"])
+        B, n, Hq, Hkv, d = w.batch, self.n, w.n_q_heads, w.n_kv_heads, w.head_dim
+        self.q = w.queries((B, n, Hq, d), "suffix", device)
+        self.k = w.keys((B, n, Hkv, d), "suffix", device)
+        self.v = w.values((B, n, Hkv, d), "suffix", device)
+        self.out = torch.empty_like(self.q)
+        self.done = 0
+        W = w.window
+        keys = 0
+        for c in self.cuts:
+            for i in range(n):
+                p = c + i
+                keys += p + 1 - (max(0, p - W + 1) if W else 0)
+        self.flops = 4.0 * keys * Hq * d
+        torch.cuda.synchronize()
+
+    def launches_per_step(self):
+        return 5                                   # trim, append rows, advance, rotate q, attention
+
+    def step(self, ev=None):
+        self.cache.trim(self.cuts)
+        if ev is not None:
+            ev[0].record()
+        self.cache.chunk(self.q, self.k, self.v, self.out)
+        if ev is not None:
+            ev[1].record()
+        self.done += 1
+        return 0
+
+    def units(self):
+        return self.flops
+
+    def io_bytes(self):
+        return 0
+
+    def e2e_setup(self):
+        import torch
+        self.hq, self.hk, self.hv = (t.cpu().pin_memory() for t in (self.q, self.k, self.v))
+        self.hout = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+        self.dq, self.dk, self.dv = (torch.empty_like(t) for t in (self.q, self.k, self.v))
+        return sum(t.numel() * t.element_size() for t in (self.hq, self.hk, self.hv)), \
+            self.hout.numel() * self.hout.element_size()
+
+    def e2e_step(self):
+        self.cache.trim(self.cuts)
+        self.dq.copy_(self.hq, non_blocking=True)
+        self.dk.copy_(self.hk, non_blocking=True)
+        self.dv.copy_(self.hv, non_blocking=True)
+        self.cache.chunk(self.dq, self.dk, self.dv, self.out)
+        self.hout.copy_(self.out, non_blocking=True)
+        self.done += 1
+
+    def reset(self):
+        import torch
+        torch.cuda.synchronize()
+
+    def cpu_problem(self):
+        return 4096, self.w.n_q_heads // self.w.n_kv_heads
+
+    def config(self):
+        w = self.w
+        return {"workload": w.name, "batch": w.batch, "n_q_heads": w.n_q_heads, "n_kv_heads": w.n_kv_heads,
+                "head_dim": w.head_dim, "prefix": w.extra["prefix"], "suffix": self.n, "window": w.window,
+                "cuts": "uniform in [0, 8191], seed 7", "gflop_per_step": round(self.flops / 1e9, 2),
+                "l2": "K/V of a step %.2f GB (> 129 MB L2)"
+                      % (sum(c + self.n for c in self.cuts) * w.n_kv_heads * w.head_dim * 4 / 1e9)}
+
+
+class ChunkWindowBench(ChunkBench):
+    def __init__(self, device, batch=None, total_steps=0):
+        super().__init__(device, batch, total_steps, windowed=True)
+
+
+BENCHES = {"full-cache-mha": FullCacheBench, "sliding-window-gqa": SlidingWindowBench, "int8-witness": Int8Bench,
+           "prefix-reuse": ChunkBench, "prefix-reuse-w4096": ChunkWindowBench}
 
 
 # ----------------------------------------------------------------------------- CPU oracle
@@ -396,7 +505,8 @@ def main():
     build()
     e2e_steps = 0 if args.no_e2e else min(args.steps, 400) + 3
     bench = BENCHES[args.workload]("cuda", args.batch, args.warmup + args.steps + e2e_steps)
-    peak, peak_kind = hbm_peak()
+    peak, peak_kind = hbm_peak() if bench.bound == "hbm" else tensor_peak()
+    scale = 1e9 if bench.unit == "GB/s" else 1e12
 
     def barrier():
         if dist is not None:
@@ -438,13 +548,13 @@ def main():
         dist.all_reduce(times, op=dist.ReduceOp.MAX)
         dist.all_reduce(tot_units, op=dist.ReduceOp.SUM)
     ms_total = float(times.item())
-    value = float(tot_units.item()) / (ms_total / 1e3) / 1e9
+    value = float(tot_units.item()) / (ms_total / 1e3) / scale
     steps_per_s = K / (ms_total / 1e3)
 
     # roofline of the decode-attention call
     attn_bytes = sum(u + bench.io_bytes() for u in step_units) / K
     attn_avg_ms = sum(attn_ms) / len(attn_ms)
-    achieved = attn_bytes / (attn_avg_ms / 1e3) / 1e9
+    achieved = attn_bytes / (attn_avg_ms / 1e3) / scale
 
     # end-to-end through the ABI with host buffers
     e2e = None
@@ -469,7 +579,7 @@ def main():
         if dist is not None:
             dist.all_reduce(ems, op=dist.ReduceOp.MAX)
             dist.all_reduce(eut, op=dist.ReduceOp.SUM)
-        e2e = {"value": round(float(eut.item()) / (float(ems.item()) / 1e3) / 1e9, 2), "unit": "GB/s",
+        e2e = {"value": round(float(eut.item()) / (float(ems.item()) / 1e3) / scale, 2), "unit": bench.unit,
                "h2d_bytes_per_step": hb, "d2h_bytes_per_step": db, "steps": Ke}
 
     cpu = None
@@ -481,12 +591,12 @@ def main():
     clocks = sampler.summary()
     if rank == 0:
         line = {
-            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
+            "metric": bench.metric, "value": round(value, 2), "unit": bench.unit, "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": round(ms_total / K, 5), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "steps_per_s": round(steps_per_s, 2), "hbm_frac_of_" + peak_kind: round(value / peak, 4),
+            "steps_per_s": round(steps_per_s, 2), "frac_of_%s_peak" % peak_kind: round(value / peak, 4),
             "config": bench.config(),
-            "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+            "roofline": {"bound": bench.bound, "achieved": round(achieved, 2), "peak": peak, "unit": bench.unit,
                          "frac": round(achieved / peak, 4), "traffic": None,
                          "kernel": bench.kernel, "peak_kind": peak_kind,
                          "bytes_per_launch": int(attn_bytes), "avg_launch_ms": round(attn_avg_ms, 5)},

@@ -196,7 +196,7 @@ __global__ void __launch_bounds__(kThreads) append_rows_kernel(const AppendArgs 
         return;
     }
     const int slot = a.ring ? (int)(p % a.S) : (int)p;
-    const size_t src = (((size_t)b * a.Hkv + h) * a.n + r) * d;
+    const size_t src = (size_t)b * a.sb + (size_t)h * a.sh + (size_t)r * a.sr;
     const size_t dst = (((size_t)b * a.Hkv + h) * a.S + slot) * d;
     float y0, y1;
     key_pair(a, a.k, src, i, (int)p, y0, y1);
@@ -236,7 +236,7 @@ __global__ void __launch_bounds__(kThreads) quantize_rows_kernel(const AppendArg
             v0 = __bfloat162float(a.vtail[tail + (size_t)r * d + 2 * i]);
             v1 = __bfloat162float(a.vtail[tail + (size_t)r * d + 2 * i + 1]);
         } else {
-            const size_t src = (((size_t)b * a.Hkv + h) * a.n + (p - np)) * d;
+            const size_t src = (size_t)b * a.sb + (size_t)h * a.sh + (size_t)(p - np) * a.sr;
             key_pair(a, a.k, src, i, p, k0, k1);
             k0 = __bfloat162float(__float2bfloat16_rn(k0));
             k1 = __bfloat162float(__float2bfloat16_rn(k1));
@@ -266,7 +266,7 @@ __global__ void __launch_bounds__(kThreads) tail_kernel(const AppendArgs a, cons
         const int rem = idx % ((end - first) * half);
         const int p = first + rem / half, i = rem % half;
         if (!position_ok(a, p)) { flag(a.hdr, kErrPosition); continue; }
-        const size_t src = (((size_t)b * a.Hkv + h) * a.n + (p - np)) * d;
+        const size_t src = (size_t)b * a.sb + (size_t)h * a.sh + (size_t)(p - np) * a.sr;
         const size_t tail = (((size_t)b * a.Hkv + h) * kQBlock + p % kQBlock) * d;
         float k0, k1;
         key_pair(a, a.k, src, i, p, k0, k1);

@@ -50,6 +50,7 @@ bool make_shape(const kvc_config& c, Shape* s) {
     s->d = c.head_dim; s->S = c.capacity; s->W = ring ? c.capacity : c.window;
     s->P = P; s->ring = ring; s->int8 = int8; s->rope = rope; s->bf16 = c.dtype == KVC_BF16;
     s->elem = s->bf16 ? 2 : 4;
+    s->max_chunk = c.max_chunk;
     s->out_bf16 = c.out_dtype == 0 ? s->bf16 : c.out_dtype == KVC_BF16 + 1;
     s->split = kGenericSplit;
     if (s->bf16 && !int8 && (s->d == 64 || s->d == 128) && s->g <= 8) s->split = kFastSplit;
@@ -87,6 +88,7 @@ Layout make_layout(const Shape& s) {
     L.part_ml = take(B * Hq * s.max_splits * 8);
     L.part_acc = take(B * Hq * s.max_splits * d * 4);
     if (s.int8) L.part_c = take(B * Hq * s.max_splits * 4);
+    if (s.max_chunk > 0) L.qrot = take(2 * B * (size_t)s.max_chunk * Hq * d * 2);   // hi and lo terms
     L.total = o;
     return L;
 }
@@ -120,6 +122,7 @@ AppendArgs append_args(kvc_handle* h, const void* k, const void* v, int n) {
     const Shape& s = h->sh;
     AppendArgs a{};
     a.k = k; a.v = v; a.n = n;
+    a.sb = (size_t)s.Hkv * n * s.d; a.sh = (size_t)n * s.d; a.sr = s.d;   // [B][Hkv][n][d]
     a.next_pos = at<int32_t>(h, h->L.next_pos);
     a.pos = at<int32_t>(h, h->L.pos);
     if (!s.int8) { a.kc = h->state + h->L.k; a.vc = h->state + h->L.v; }
@@ -307,12 +310,20 @@ int kvc_chunk_attn(kvc_t h, const void* d_q, const void* d_k, const void* d_v, i
     if (!h || !d_q || !d_k || !d_v || !d_out || n < 1) return KVC_ERR_ARG;
     if (!aligned16(d_q) || !aligned16(d_k) || !aligned16(d_v) || !aligned16(d_out)) return KVC_ERR_ARG;
     const Shape& s = h->sh;
-    if (s.ring || s.int8 || !s.bf16) return KVC_ERR_UNSUPPORTED;
-    if (n > h->cfg.max_chunk) return KVC_ERR_ARG;
+    if (!chunk_supported(s)) return KVC_ERR_UNSUPPORTED;
+    if (n > s.max_chunk) return KVC_ERR_ARG;
     int rc = check_capacity(h, nullptr, n);
     if (rc) return rc;
-    (void)d_out;
-    return KVC_ERR_UNSUPPORTED;
+    // the suffix rows join the cache first (rotated keys, positions cut .. cut+n-1) ...
+    cudaStream_t st = S_(stream);
+    h->counts.assign(s.B, n);
+    AppendArgs a = append_args(h, d_k, d_v, n);
+    a.sb = (size_t)n * s.Hkv * s.d; a.sh = s.d; a.sr = (size_t)s.Hkv * s.d;   // [B][n][Hkv][d]
+    if (launch_append_rows_counts(a, h->counts.data(), st) != cudaSuccess) return KVC_ERR_CUDA;
+    for (auto& p : h->np) p += n;
+    // ... then every suffix query attends over its window
+    if (launch_chunk(h, d_q, d_out, n, st) != cudaSuccess) return KVC_ERR_CUDA;
+    return KVC_OK;
 }
 
 int kvc_export_bytes(kvc_t h, int32_t which, size_t* bytes) {

@@ -36,6 +36,7 @@ struct Layout {
     size_t part_ml;   // float2 [B][Hq][max_splits] {m (log2 domain), l}
     size_t part_acc;  // float  [B][Hq][max_splits][d]
     size_t part_c;    // float  [B][Hq][max_splits] max_t c_t of the split   (INT8)
+    size_t qrot;      // bf16 [2][B][max_chunk][Hq][d] rotated suffix queries, hi and lo terms
     size_t total;
 };
 
@@ -47,6 +48,7 @@ struct Shape {
     bool out_bf16;               // attention outputs in bf16 (else fp32)
     int split;                   // keys per split of the decode kernel in use
     int max_splits;
+    int max_chunk;               // largest suffix of kvc_chunk_attn (0 = none)
 };
 
 bool make_shape(const kvc_config& c, Shape* s);
@@ -76,9 +78,10 @@ struct CombineArgs {
 };
 
 struct AppendArgs {
-    const void* k;        // [B][Hkv][n][d]  (n = 1 for a single token)
+    const void* k;        // row r of KV head h of request b at b*sb + h*sh + r*sr
     const void* v;
     int n;                // rows in the input per request
+    size_t sb, sh, sr;    // element strides of the input (row elements are contiguous)
     int32_t* next_pos;
     int32_t* pos;
     void* kc;             // cache rows (non-INT8)
@@ -93,6 +96,7 @@ struct AppendArgs {
 // ---- launchers (one per translation unit) ----------------------------------
 cudaError_t launch_append_token(const AppendArgs& a, cudaStream_t st);
 cudaError_t launch_decode(const DecodeArgs& d, const CombineArgs& c, bool fast, cudaStream_t st);
+bool chunk_supported(const Shape& s);
 
 // ---- device helpers -----------------------------------------------------------
 __device__ __forceinline__ float ld_elem(const void* p, size_t i, int bf16) {

@@ -1,0 +1,108 @@
+"""GPU parity of kvc_chunk_attn (trim, then chunked causal/windowed suffix attention).
+
+[PREFIX] "LLM 機制實驗（五）：改了歷史，能否只重算變化的後綴？": trim K/V/positions to
+`cut`, continue from next_position = cut with model.chunk(tokens[cut:]); the result
+must equal a full recompute, and keeping the stale next_position must diverge.
+"""
+import numpy as np
+import pytest
+import torch
+
+from kv_cache_decode_ring_gb300 import kvc
+from kv_cache_decode_ring_gb300 import workloads as wl
+from oracle import numerics as nm
+
+from _parity import assert_close, check_state, host, oracle_for
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from kv_cache_decode_ring_gb300 import build
+    build.build()
+
+
+def _prefilled(w, lengths, cuts, max_chunk, out_dtype=None):
+    cache = kvc.Cache.from_workload(w, max_chunk=max_chunk, out_dtype=out_dtype)
+    model = oracle_for(w)
+    k, v = w.prefill_chunk(0, max(lengths))
+    cache.append_rows(k.cuda(), v.cuda(), counts=lengths)
+    model.append_rows(host(k), host(v), lengths)
+    cache.trim(cuts)
+    model.trim(cuts)
+    return cache, model
+
+
+def _suffix(w, n, tag="suffix"):
+    B, Hq, Hkv, d = w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim
+    return (w.queries((B, n, Hq, d), tag), w.keys((B, n, Hkv, d), tag), w.values((B, n, Hkv, d), tag))
+
+
+@pytest.mark.parametrize("window", [0, 100])
+def test_chunk_matches_recompute(window):
+    w = wl.small("chunk-w%d" % window, B=3, Hq=8, Hkv=2, d=128, capacity=1024, window=window,
+                 rope_base=10000.0, seed=17)
+    lengths, cuts, n = [600, 300, 40], [413, 0, 40], 200
+    cache, model = _prefilled(w, lengths, cuts, n, out_dtype="f32")
+    q, k, v = _suffix(w, n)
+    out = cache.chunk(q.cuda(), k.cuda(), v.cuda())
+    torch.cuda.synchronize()
+    ref = model.chunk(host(q), host(k), host(v))
+    err = np.abs(out.double().cpu().numpy() - ref)
+    print("chunk max abs err %.3e, max rel excess %.3f" % (err.max(), (err / (2e-3 + 2e-3 * np.abs(ref))).max()))
+    assert_close(out, ref, "bf16", "chunk W=%d" % window)
+    check_state(cache, model, w)
+    assert list(cache.next_positions()) == [c + n for c in cuts]
+    assert cache.device_status() == 0
+
+
+def test_chunk_rows_equal_one_token_decodes():
+    # row i of the chunk equals a decode of the same query at position cut + i
+    w = wl.small("chunk-vs-decode", B=2, Hq=8, Hkv=2, d=128, capacity=512, rope_base=10000.0, seed=3)
+    lengths, cuts, n = [300, 129], [257, 129], 130
+    a, _ = _prefilled(w, lengths, cuts, n, out_dtype="f32")
+    b, _ = _prefilled(w, lengths, cuts, n, out_dtype="f32")
+    q, k, v = _suffix(w, n)
+    out = a.chunk(q.cuda(), k.cuda(), v.cuda()).cpu()
+    for i in range(n):
+        b.append(k[:, i].contiguous().cuda(), v[:, i].contiguous().cuda())
+        if i % 13 == 0 or i == n - 1:
+            d = b.decode(q[:, i].contiguous().cuda()).cpu()
+            assert_close(out[:, i], d.double().numpy(), "bf16", "chunk row %d vs decode" % i)
+
+
+def test_stale_next_position_diverges():
+    # planted on the CPU: the same trimmed rows, suffix rotated from the old length
+    w = wl.small("chunk-stale", B=2, Hq=4, Hkv=1, d=128, capacity=512, rope_base=10000.0, seed=9)
+    lengths, cuts, n = [300, 300], [120, 0], 64
+    cache, model = _prefilled(w, lengths, cuts, n, out_dtype="f32")
+    q, k, v = _suffix(w, n)
+    out = cache.chunk(q.cuda(), k.cuda(), v.cuda()).double().cpu().numpy()
+    hk, hv = host(k), host(v)
+    # the prefix rows of request 0 as stored, plus the suffix encoded at positions 300 + i
+    K = [model.hk[0][p][0] for p in range(cuts[0])]
+    V = [model.hv[0][p][0] for p in range(cuts[0])]
+    stale = np.zeros((n, 4, 128))
+    for i in range(n):
+        K.append(model.stored_rows(hk[0, i], [lengths[0] + i])[0])
+        V.append(nm.bf16_to_f32(hv[0, i])[0])
+        qr = model.query_rows(host(q)[0, i], np.full(4, lengths[0] + i)).astype(np.float64)
+        stale[i] = nm.attend(qr, np.stack(K).astype(np.float64), np.stack(V).astype(np.float64), len(K) - 1)
+    excess = np.abs(stale - out[0]) - (2e-3 + 2e-3 * np.abs(out[0]))
+    assert excess.max() > 0, "the stale-position control must exceed the tolerance"
+
+
+def test_chunk_rejects_bad_shapes():
+    w = wl.small("chunk-bad", B=1, Hq=2, Hkv=1, d=64, capacity=128, rope_base=0.0)
+    cache = kvc.Cache.from_workload(w, max_chunk=16)
+    q, k, v = _suffix(w, 8)
+    with pytest.raises(kvc.KvcError) as e:
+        cache.chunk(q.cuda(), k.cuda(), v.cuda())   # d=64: not built for the tensor-core path
+    assert e.value.code == kvc.KVC_ERR_UNSUPPORTED
+    w2 = wl.small("chunk-big", B=1, Hq=2, Hkv=1, d=128, capacity=128, rope_base=0.0)
+    c2 = kvc.Cache.from_workload(w2, max_chunk=16)
+    q, k, v = _suffix(w2, 32)
+    with pytest.raises(kvc.KvcError) as e:
+        c2.chunk(q.cuda(), k.cuda(), v.cuda())      # n > max_chunk
+    assert e.value.code == kvc.KVC_ERR_ARG

@@ -215,3 +215,56 @@ def test_int8_witness_sampled():
             wit = np.stack([onm.witness_row(Kb[i], cK[i], sK) for i in range(QBLOCK)])
             assert np.array_equal(WT[b, h, pos], wit), (b, h, blk)
     assert cache.device_status() == 0
+
+
+@pytest.mark.parametrize("windowed", [False, True], ids=["full", "w4096"])
+def test_prefix_reuse_sampled(windowed):
+    # 16 requests with an 8192-token prefix (Hq=32, Hkv=8, d=128, RoPE 10000), trimmed at seeded
+    # cuts in [0, 8191], then a 512-token suffix by kvc_chunk_attn; sampled rows against the oracle,
+    # and the stale-next_position control (planted on the CPU) must exceed the tolerance
+    w = wl.prefix_reuse(windowed)
+    n, pre, W = w.extra["suffix"], w.extra["prefix"], w.window
+    cuts = w.extra["cuts"]
+    cache = kvc.Cache.from_workload(w, max_chunk=n)
+    model = oracle_for(w)
+    g = w.n_q_heads // w.n_kv_heads
+    reqs = [int(np.argmin(cuts)), int(np.argmax(cuts)), 3, 11]
+    hs = [0, 7]                                        # KV heads sampled
+    keep = {(r, h): [] for r in reqs for h in hs}
+    for c in range(pre // 2048):
+        k = w.keys((w.batch, w.n_kv_heads, 2048, w.head_dim), "prefix%d" % c, "cuda")
+        v = w.values((w.batch, w.n_kv_heads, 2048, w.head_dim), "prefix%d" % c, "cuda")
+        cache.append_rows(k, v)
+        for (r, h) in keep:
+            keep[(r, h)].append((host(k[r, h]), host(v[r, h])))
+        del k, v
+    cache.trim(cuts)
+    q = w.queries((w.batch, n, w.n_q_heads, w.head_dim), "suffix", "cuda")
+    k = w.keys((w.batch, n, w.n_kv_heads, w.head_dim), "suffix", "cuda")
+    v = w.values((w.batch, n, w.n_kv_heads, w.head_dim), "suffix", "cuda")
+    out = cache.chunk(q, k, v).float().cpu().numpy().astype(np.float64)
+    hq_, hk_, hv_ = host(q), host(k), host(v)
+    for (r, h) in keep:
+        cut = cuts[r]
+        Kpre = np.concatenate([a for a, _ in keep[(r, h)]])[:cut]
+        Vpre = np.concatenate([b for _, b in keep[(r, h)]])[:cut]
+        Kall = np.concatenate([Kpre, hk_[r, :, h]])
+        Vall = np.concatenate([Vpre, hv_[r, :, h]])
+        K = model.stored_rows(Kall, np.arange(cut + n)).astype(np.float64)
+        V = nm.bf16_to_f32(Vall).astype(np.float64)
+        Kst = np.concatenate([K[:cut], model.stored_rows(hk_[r, :, h], pre + np.arange(n)).astype(np.float64)])
+        worst_stale = -np.inf
+        for i in (0, 1, 127, 128, 255, 511):
+            p = cut + i
+            qr = model.query_rows(hq_[r, i, h * g:(h + 1) * g], np.full(g, p)).astype(np.float64)
+            ref = nm.attend(qr, K[:p + 1], V[:p + 1], p, W)
+            got = out[r, i, h * g:(h + 1) * g]
+            err = np.abs(got - ref) - (2e-3 + 2e-3 * np.abs(ref) + np.ldexp(1.0, np.floor(np.log2(np.maximum(np.abs(ref), 1e-30))).astype(int) - 8))
+            assert err.max() <= 0, (r, h, i, err.max())
+            # stale next_position: same rows, suffix encoded from the old length `pre`
+            qs = model.query_rows(hq_[r, i, h * g:(h + 1) * g], np.full(g, pre + i)).astype(np.float64)
+            stale = nm.attend(qs, Kst[:p + 1], V[:p + 1], p, W)
+            worst_stale = max(worst_stale, (np.abs(stale - got) - (2e-3 + 2e-3 * np.abs(got))).max())
+        if cut > 0:
+            assert worst_stale > 0, ("stale control within tolerance", r, h, cut)
+    assert cache.device_status() == 0
