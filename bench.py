@@ -35,6 +35,28 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+CSRC = os.path.join(ROOT, "kv_cache_decode_ring_gb300", "csrc")
+
+# DRAM traffic (ncu dram__bytes_read.sum + dram__bytes_write.sum) per algorithmic byte of the
+# dominant kernel, from the captures summarised in profiles/; valid only while the kernel
+# source is the one captured (sha256 prefix), otherwise the JSON line reports null.
+TRAFFIC_PER_BYTE = {
+    "full-cache-mha": ("decode_fast.cu", "7dea6b0b22669787", 273041152 / 268697600),
+    "sliding-window-gqa": ("decode_fast.cu", "7dea6b0b22669787", (1059193000 + 33679616) / 1059586048),
+    "int8-witness": ("int8.cu", "8825f47a8e965b16", (2420415000 + 135907584) / 2420342784),
+}
+
+
+def traffic_per_launch(workload, bytes_per_launch):
+    import hashlib
+    entry = TRAFFIC_PER_BYTE.get(workload)
+    if not entry:
+        return None
+    src, sha, ratio = entry
+    with open(os.path.join(CSRC, src), "rb") as f:
+        if hashlib.sha256(f.read()).hexdigest()[:16] != sha:
+            return None
+    return int(ratio * bytes_per_launch)
 FALLBACK_HBM_GBS = 6800.0
 METRIC = "decode-attention KV bytes/s (GB/s, % of HBM peak) and decode steps/s at 1 GB300"
 
@@ -597,7 +619,8 @@ def main():
             "steps_per_s": round(steps_per_s, 2), "frac_of_%s_peak" % peak_kind: round(value / peak, 4),
             "config": bench.config(),
             "roofline": {"bound": bench.bound, "achieved": round(achieved, 2), "peak": peak, "unit": bench.unit,
-                         "frac": round(achieved / peak, 4), "traffic": None,
+                         "frac": round(achieved / peak, 4),
+                         "traffic": traffic_per_launch(args.workload, attn_bytes),
                          "kernel": bench.kernel, "peak_kind": peak_kind,
                          "bytes_per_launch": int(attn_bytes), "avg_launch_ms": round(attn_avg_ms, 5)},
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
