@@ -113,13 +113,16 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineArgs c) 
 }  // namespace
 
 cudaError_t launch_decode(const DecodeArgs& a, const CombineArgs& c, bool fast, cudaStream_t st) {
-    if (fast) {
+    if (a.split == kGqaSplit && gqa_decode_supported(a.d, a.g)) {
+        cudaError_t e = launch_decode_gqa(a, st);
+        if (e != cudaSuccess) return e;
+    } else if (fast) {
         cudaError_t e = launch_decode_fast(a, st);
         if (e != cudaSuccess) return e;
     } else {
         dim3 grid(a.max_splits, a.Hkv, a.B);
         const size_t smem = (size_t)a.g * (a.d + a.split) * sizeof(float);
-        if (c.bf16) decode_generic_kernel<1><<<grid, kThreads, smem, st>>>(a);
+        if (a.bf16) decode_generic_kernel<1><<<grid, kThreads, smem, st>>>(a);
         else decode_generic_kernel<0><<<grid, kThreads, smem, st>>>(a);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;

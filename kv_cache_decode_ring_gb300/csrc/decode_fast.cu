@@ -34,20 +34,32 @@ constexpr int kSplitKeys = kWarps * kTile;  // keys per CTA split
 
 template <int D, int G>
 struct Cfg {
-    static constexpr int LPR = D / 8;                 // lanes per row (one 16-B chunk each)
-    static constexpr int RPP = 32 / LPR;              // rows (key groups) per warp
+    // scores: a lane holds QD dims of a key row for all G heads (16 for G <= 4, else 8,
+    // bounding the query registers at 64), as the 16-byte chunks r, r + LPR, ... of the
+    // row, so that the LPR lanes of a row read one contiguous 16*LPR-byte run per load
+    static constexpr int QD = G <= 4 ? 16 : 8;
+    static constexpr int LPR = D / QD;                // score lanes per row
+    static constexpr int RPP = 32 / LPR;              // key groups per warp
     static constexpr int KPG = kTile / RPP;           // keys per group per tile
     static constexpr int KB0 = 2 * LPR / G;
     static constexpr int KB = KB0 < KPG ? (KB0 < 1 ? 1 : KB0) : KPG;  // keys per reduce batch
     static constexpr int M = KB * G;                  // partial sums per lane per batch
     static constexpr int OUT = M / LPR;               // finished scores per lane per batch
+    // P.V: a lane holds 8 output dims of every head
+    static constexpr int LPR2 = D / 8;
+    static constexpr int RPP2 = 32 / LPR2;
     static constexpr int ROWB = D * 2;
     static constexpr int TILEB = kTile * ROWB;        // bytes of one warp's K (or V) tile
     static constexpr int PARTB = G * (D + 2) * 4;     // one warp's partial (m, l, acc)
     static_assert(M % LPR == 0 && OUT >= 1, "batch shape");
     static_assert(PARTB <= TILEB, "partial must fit in the warp's K tile");
-    static constexpr size_t SMEM = 2 * (size_t)kWarps * TILEB + (size_t)kWarps * kTile * G * 4 + kWarps * 8 + 128;
+    static constexpr int OFF_P = 2 * kWarps * TILEB;                    // scores [warp][kTile][G]
+    static constexpr int OFF_Q = OFF_P + kWarps * kTile * G * 4;        // rotated scaled query [G][D]
+    static constexpr int OFF_BAR = OFF_Q + G * D * 4;
+    static constexpr size_t SMEM = OFF_BAR + kWarps * 8 + 128;
 };
+
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 
 template <int D, int G>
 __global__ void __launch_bounds__(kWarps * 32, 3) decode_fast_kernel(const DecodeArgs a) {
@@ -55,8 +67,9 @@ __global__ void __launch_bounds__(kWarps * 32, 3) decode_fast_kernel(const Decod
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char* sK = smem;                                   // [warp][kTile][D] bf16
     unsigned char* sV = smem + kWarps * C::TILEB;               // [warp][kTile][D] bf16
-    float* sP = reinterpret_cast<float*>(smem + 2 * kWarps * C::TILEB);   // [warp][kTile][G]
-    uint64_t* bar = reinterpret_cast<uint64_t*>(sP + kWarps * kTile * G);  // [warp]
+    float* sP = reinterpret_cast<float*>(smem + C::OFF_P);     // [warp][kTile][G]
+    float* sQ = reinterpret_cast<float*>(smem + C::OFF_Q);     // [G][D]
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.z, kvh = blockIdx.y;
@@ -66,51 +79,63 @@ __global__ void __launch_bounds__(kWarps * 32, 3) decode_fast_kernel(const Decod
     const int nsplit = (hi - lo + kSplitKeys - 1) / kSplitKeys;
     if ((int)blockIdx.x >= nsplit) return;
 
-    if (threadIdx.x < kWarps) mbar_init(&bar[threadIdx.x], 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    __syncthreads();
-
-    // Query chunk of this lane for all G heads, rotated at t = len - 1, fp32,
-    // pre-multiplied by log2(e)/sqrt(d).
-    const int r = lane % C::LPR, grp = lane / C::LPR;
-    float q[G][8];
-    {
-        const int t = len - 1;
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-            const size_t off = ((size_t)b * a.Hq + (size_t)kvh * G + h) * D + r * 8;
-            const uint4 u = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q) + off);
-            float x[8];
-            bf16x8_to_f32(u, x);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                float y0 = x[2 * j], y1 = x[2 * j + 1];
-                if (a.rope) rope_pair(x[2 * j], x[2 * j + 1], a.rope[(size_t)t * (D / 2) + r * 4 + j], y0, y1);
-                q[h][2 * j] = y0 * a.scale_log2;
-                q[h][2 * j + 1] = y1 * a.scale_log2;
-            }
-        }
-    }
-
+    const int warp_ = threadIdx.x >> 5;
     const size_t head_row0 = ((size_t)b * a.Hkv + kvh) * a.S;
     const __nv_bfloat16* Kg = static_cast<const __nv_bfloat16*>(a.k);
     const __nv_bfloat16* Vg = static_cast<const __nv_bfloat16*>(a.v);
-    unsigned char* myK = sK + warp * C::TILEB;
-    unsigned char* myV = sV + warp * C::TILEB;
+    unsigned char* myK = sK + warp_ * C::TILEB;
+    unsigned char* myV = sV + warp_ * C::TILEB;
+    // lane 0 of each warp: copy its K/V rows of `split` (returns the key count)
+    auto issue = [&](int split) {
+        const int k0 = lo + split * kSplitKeys + warp_ * kTile;
+        const int nk = max(0, min(kTile, hi - k0));
+        if ((threadIdx.x & 31) == 0 && nk > 0) {
+            const uint32_t bytes = (uint32_t)nk * C::ROWB;
+            mbar_arrive_expect_tx(&bar[warp_], 2 * bytes);
+            bulk_copy_g2s(myK, Kg + (head_row0 + k0) * D, bytes, &bar[warp_]);
+            bulk_copy_g2s(myV, Vg + (head_row0 + k0) * D, bytes, &bar[warp_]);
+        }
+    };
+    if ((threadIdx.x & 31) == 0) {
+        mbar_init(&bar[warp_], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncwarp();
+    issue(blockIdx.x);                       // the first split's rows start moving at once
+
+    // Query of the G heads, rotated at t = len - 1, fp32, times log2(e)/sqrt(d): once per CTA
+    {
+        const int t = len - 1;
+        for (int idx = threadIdx.x; idx < G * D / 2; idx += blockDim.x) {
+            const int h = idx / (D / 2), i = idx % (D / 2);
+            const size_t off = ((size_t)b * a.Hq + (size_t)kvh * G + h) * D + 2 * i;
+            const float x0 = ld_elem(a.q, off, 1), x1 = ld_elem(a.q, off + 1, 1);
+            float y0 = x0, y1 = x1;
+            if (a.rope) rope_pair(x0, x1, a.rope[(size_t)t * (D / 2) + i], y0, y1);
+            sQ[h * D + 2 * i] = y0 * a.scale_log2;
+            sQ[h * D + 2 * i + 1] = y1 * a.scale_log2;
+        }
+    }
+    __syncthreads();
+
+    const int r = lane % C::LPR, grp = lane / C::LPR;          // score mapping
+    const int r2 = lane % C::LPR2, grp2 = lane / C::LPR2;      // P.V mapping
+    float q[G][C::QD];
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+#pragma unroll
+        for (int e = 0; e < C::QD; e += 4) {
+            const int dim = (r + (e / 8) * C::LPR) * 8 + (e % 8);
+            const float4 f = *reinterpret_cast<const float4*>(sQ + h * D + dim);
+            q[h][e] = f.x; q[h][e + 1] = f.y; q[h][e + 2] = f.z; q[h][e + 3] = f.w;
+        }
+
     float* myP = sP + warp * kTile * G;
     uint32_t phase = 0;
 
     for (int split = blockIdx.x; split < nsplit; split += gridDim.x) {
         const int k0 = lo + split * kSplitKeys + warp * kTile;
         const int nk = max(0, min(kTile, hi - k0));
-
-        // ---- issue this warp's copies
-        if (lane == 0 && nk > 0) {
-            const uint32_t bytes = (uint32_t)nk * C::ROWB;
-            mbar_arrive_expect_tx(&bar[warp], 2 * bytes);
-            bulk_copy_g2s(myK, Kg + (head_row0 + k0) * D, bytes, &bar[warp]);
-            bulk_copy_g2s(myV, Vg + (head_row0 + k0) * D, bytes, &bar[warp]);
-        }
         float m_w[G], l_w[G], acc[G][8];
 #pragma unroll
         for (int h = 0; h < G; ++h) {
@@ -137,18 +162,19 @@ __global__ void __launch_bounds__(kWarps * 32, 3) decode_fast_kernel(const Decod
 #pragma unroll
                 for (int k = 0; k < C::KB; ++k) {
                     const int t = grp * C::KPG + kb + k;
-                    const uint4 u = *reinterpret_cast<const uint4*>(myK + t * C::ROWB + r * 16);
-                    float x[8];
-                    bf16x8_to_f32(u, x);
+                    float x[C::QD];
+#pragma unroll
+                    for (int e = 0; e < C::QD; e += 8) {
+                        const uint4 u = *reinterpret_cast<const uint4*>(myK + t * C::ROWB + (r + (e / 8) * C::LPR) * 16);
+                        bf16x8_to_f32(u, x + e);
+                    }
 #pragma unroll
                     for (int h = 0; h < G; ++h) {
-                        float s0 = q[h][0] * x[0], s1 = q[h][1] * x[1];
+                        float2 s2 = make_float2(0.f, 0.f);
 #pragma unroll
-                        for (int e = 2; e < 8; e += 2) {
-                            s0 = fmaf(q[h][e], x[e], s0);
-                            s1 = fmaf(q[h][e + 1], x[e + 1], s1);
-                        }
-                        part[k * G + h] = s0 + s1;
+                        for (int e = 0; e < C::QD; e += 2)
+                            s2 = ffma2(make_float2(q[h][e], q[h][e + 1]), make_float2(x[e], x[e + 1]), s2);
+                        part[k * G + h] = s2.x + s2.y;
                     }
                 }
                 // reduce-scatter: after the step with mask m, lanes with that bit set keep the
@@ -187,20 +213,27 @@ __global__ void __launch_bounds__(kWarps * 32, 3) decode_fast_kernel(const Decod
                 l_w[h] = l;
             }
             __syncwarp();
-            // ---- P.V: lane owns dims [8r, 8r+8) of every head for keys of its group
-            for (int t = grp; t < nk; t += C::RPP) {
-                const uint4 u = *reinterpret_cast<const uint4*>(myV + t * C::ROWB + r * 16);
+            // ---- P.V: lane owns dims [8 r2, 8 r2 + 8) of every head for keys of its group
+            for (int t = grp2; t < nk; t += C::RPP2) {
+                const uint4 u = *reinterpret_cast<const uint4*>(myV + t * C::ROWB + r2 * 16);
                 float x[8];
                 bf16x8_to_f32(u, x);
+                float pv[G];
+#pragma unroll
+                for (int h = 0; h < G; ++h) pv[h] = myP[t * G + h];
 #pragma unroll
                 for (int h = 0; h < G; ++h) {
-                    const float p = myP[t * G + h];
+                    const float2 pp = make_float2(pv[h], pv[h]);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) acc[h][e] = fmaf(p, x[e], acc[h][e]);
+                    for (int e = 0; e < 8; e += 2) {
+                        const float2 rr = ffma2(pp, make_float2(x[e], x[e + 1]), make_float2(acc[h][e], acc[h][e + 1]));
+                        acc[h][e] = rr.x;
+                        acc[h][e + 1] = rr.y;
+                    }
                 }
             }
 #pragma unroll
-            for (int mask = C::LPR; mask < 32; mask <<= 1)
+            for (int mask = C::LPR2; mask < 32; mask <<= 1)
 #pragma unroll
                 for (int h = 0; h < G; ++h)
 #pragma unroll
@@ -209,12 +242,12 @@ __global__ void __launch_bounds__(kWarps * 32, 3) decode_fast_kernel(const Decod
         // ---- this warp's partial into its own K tile (done with K)
         __syncwarp();
         float* part_w = reinterpret_cast<float*>(myK);       // [G][2 + D]
-        if (grp == 0) {
+        if (grp2 == 0) {
 #pragma unroll
             for (int h = 0; h < G; ++h) {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) part_w[h * (D + 2) + 2 + r * 8 + e] = acc[h][e];
-                if (r == 0) { part_w[h * (D + 2)] = m_w[h]; part_w[h * (D + 2) + 1] = l_w[h]; }
+                for (int e = 0; e < 8; ++e) part_w[h * (D + 2) + 2 + r2 * 8 + e] = acc[h][e];
+                if (r2 == 0) { part_w[h * (D + 2)] = m_w[h]; part_w[h * (D + 2) + 1] = l_w[h]; }
             }
         }
         __syncthreads();
@@ -225,22 +258,23 @@ __global__ void __launch_bounds__(kWarps * 32, 3) decode_fast_kernel(const Decod
 #pragma unroll
             for (int w = 0; w < kWarps; ++w)
                 mx = fmaxf(mx, reinterpret_cast<const float*>(sK + w * C::TILEB)[h * (D + 2)]);
-            float l = 0.f, s = 0.f;
+            float l = 0.f, sacc = 0.f;
 #pragma unroll
             for (int w = 0; w < kWarps; ++w) {
                 const float* pw = reinterpret_cast<const float*>(sK + w * C::TILEB) + h * (D + 2);
                 const float f = pw[0] == -INFINITY ? 0.f : exp2f(pw[0] - mx);
                 l += pw[1] * f;
-                s += pw[2 + i] * f;
+                sacc += pw[2 + i] * f;
             }
             const size_t row = ((size_t)b * a.Hq + (size_t)kvh * G + h) * a.max_splits + split;
-            a.part_acc[row * D + i] = s;
+            a.part_acc[row * D + i] = sacc;
             if (i == 0) a.part_ml[row] = make_float2(mx, l);
         }
         // shared memory is rewritten by the next split's copies: order these generic
         // accesses before the async-proxy writes
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncthreads();
+        if (split + (int)gridDim.x < nsplit) issue(split + gridDim.x);
     }
 }
 

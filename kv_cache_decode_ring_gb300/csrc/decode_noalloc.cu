@@ -81,7 +81,7 @@ extern "C" int kvc_decode_attn_noalloc(kvc_t h, const void* d_q, void* d_out, kv
     a.part_acc = reinterpret_cast<float*>(static_cast<unsigned char*>(base) + ml_bytes);
     a.hdr = reinterpret_cast<uint32_t*>(h->state + h->L.hdr);
     a.B = s.B; a.Hq = s.Hq; a.Hkv = s.Hkv; a.g = s.g; a.d = s.d; a.S = s.S; a.W = s.W;
-    a.max_splits = s.max_splits; a.split = s.split; a.ring = s.ring;
+    a.max_splits = s.max_splits; a.split = s.split; a.ring = s.ring; a.bf16 = s.bf16;
     a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)s.d));
     CombineArgs c{};
     c.part_ml = a.part_ml; c.part_acc = a.part_acc; c.next_pos = a.next_pos; c.out = d_out;

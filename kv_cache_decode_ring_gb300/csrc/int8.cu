@@ -32,7 +32,7 @@
 namespace kvc {
 namespace {
 
-constexpr int kWarps = 4;
+constexpr int kWarps = 8;
 constexpr int kTile = 32;       // keys per warp = two blocks
 static_assert(kWarps * kTile == kInt8Split, "split shape");
 
@@ -77,33 +77,51 @@ __device__ __forceinline__ void s8x4_to_f32(uint32_t w, float* f) {
     f[3] = __uint_as_float(__byte_perm(u, 0x4b000000u, 0x7653)) - 8388736.0f;
 }
 
+// dp4a with unsigned bytes in a and signed bytes in b
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
 template <int D, int G>
 struct I8 {
-    static constexpr int LPR = D / 8;             // lanes per row, 8 codes (8 bytes) each
-    static constexpr int RPP = 32 / LPR;          // key groups per warp
+    static constexpr int LPR = D / 16;            // score lanes per row, 16 codes (one 16-B load) each
+    static constexpr int RPP = 32 / LPR;          // key groups per warp for the scores
     static constexpr int KPG = kTile / RPP;       // keys per group
     static constexpr int KB0 = 2 * LPR / G;
     static constexpr int KB = KB0 < KPG ? (KB0 < 1 ? 1 : KB0) : KPG;
-    static constexpr int M = KB * G;
-    static constexpr int OUT = M / LPR;
-    static constexpr int BW = D / kBands;         // dims per band
+    static constexpr int M = KB * G;              // int32 partial scores per lane per batch
+    static constexpr int OUT = M / LPR;           // finished scores per lane per batch
+    static constexpr int LPR2 = D / 8;            // P.V lanes per row, 8 codes each
+    static constexpr int RPP2 = 32 / LPR2;
     static constexpr int TILEB = kTile * D;       // one warp's codes (K or V)
     static constexpr int WITB = kTile * kBands * 2;
     static constexpr int WARPB = 2 * TILEB + WITB;
     static constexpr int PARTF = G * (D + 3);     // floats of one warp's partial (m, l, c, acc)
     static_assert(M % LPR == 0 && OUT >= 1, "batch shape");
     static_assert(PARTF * 4 <= WARPB, "partial must fit in the warp's tiles");
-    static constexpr size_t SMEM = (size_t)kWarps * WARPB + (size_t)kWarps * kTile * G * 4 +
-                                   (size_t)kWarps * G * kBands * 4 + kWarps * 8 + 128;
+    // shared memory after the warps' tiles: scores [warp][kTile][G] (also the fp32 query
+    // during preparation), query bytes hi/lo [G][D/4] words, band norms [G][16],
+    // score factors [G], barriers [warp]
+    static constexpr int OFF_P = kWarps * WARPB;
+    static constexpr int PBYTES = (kWarps * kTile * G > G * D ? kWarps * kTile * G : G * D) * 4;
+    static constexpr int OFF_QW = OFF_P + PBYTES;
+    static constexpr int OFF_NQ = OFF_QW + 2 * G * (D / 4) * 4;
+    static constexpr int OFF_F = OFF_NQ + G * kBands * 4;
+    static constexpr int OFF_BAR = OFF_F + ((G * 4 + 15) / 16) * 16;
+    static constexpr size_t SMEM = OFF_BAR + kWarps * 8 + 128;
 };
 
 template <int D, int G>
-__global__ void __launch_bounds__(kWarps * 32, G >= 8 ? 3 : 4) int8_decode_kernel(const Int8Args a) {
+__global__ void __launch_bounds__(kWarps * 32, 2) int8_decode_kernel(const Int8Args a) {
     using C = I8<D, G>;
     extern __shared__ __align__(128) unsigned char smem[];
-    float* sP = reinterpret_cast<float*>(smem + kWarps * C::WARPB);      // [warp][kTile][G]
-    float* sNQ = sP + kWarps * kTile * G;                                 // [warp][G][16] band norms
-    uint64_t* bar = reinterpret_cast<uint64_t*>(sNQ + kWarps * G * kBands);
+    float* sP = reinterpret_cast<float*>(smem + C::OFF_P);              // [warp][kTile][G]
+    uint32_t* sQW = reinterpret_cast<uint32_t*>(smem + C::OFF_QW);      // [2][G][D/4] query bytes
+    float* sNQ = reinterpret_cast<float*>(smem + C::OFF_NQ);            // [G][16] band norms
+    float* sF = reinterpret_cast<float*>(smem + C::OFF_F);              // [G] score factors
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);     // [warp]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.z, kvh = blockIdx.y, split = blockIdx.x;
@@ -170,12 +188,12 @@ __global__ void __launch_bounds__(kWarps * 32, G >= 8 ? 3 : 4) int8_decode_kerne
     }
 
     // ---- quantized split ----------------------------------------------------
-    const int r = lane % C::LPR, grp = lane / C::LPR;
+    const int r = lane % C::LPR, grp = lane / C::LPR;          // score mapping
+    const int r2 = lane % C::LPR2, grp2 = lane / C::LPR2;      // P.V mapping
     unsigned char* myK = smem + warp * C::WARPB;
     unsigned char* myV = myK + C::TILEB;
     const __half* myW = reinterpret_cast<const __half*>(myV + C::TILEB);
     float* myP = sP + warp * kTile * G;
-    float* myNQ = sNQ + warp * G * kBands;
     const int k0 = split * kInt8Split + warp * kTile;
     const int nk = max(0, min(kTile, nfull - k0));
     const size_t row0 = ((size_t)b * a.Hkv + kvh) * a.S;
@@ -186,42 +204,56 @@ __global__ void __launch_bounds__(kWarps * 32, G >= 8 ? 3 : 4) int8_decode_kerne
         bulk_copy_g2s((void*)myW, a.wit + (row0 + k0) * kBands, (uint32_t)(nk * kBands * 2), &bar[warp]);
     }
 
-    // query: rotated fp32; scaled copy for the scores, band norms (rounded up) for the bound
-    float q[G][8];
+    // ---- query preparation, once per CTA while the copies fly:
+    //  rotated fp32 query; per head a 16-bit integer copy q ~ s_q * (256 hi + lo) for the
+    //  scores (exact int32 dot products with the codes); band norms of the fp32 query,
+    //  rounded up, for the bound
+    float* qf = sP;                                           // [G][D] before the scores use it
+    for (int idx = threadIdx.x; idx < G * D / 2; idx += blockDim.x) {
+        const int h = idx / (D / 2), i = idx % (D / 2);
+        const size_t off = (rowq0 + h) * D + 2 * i;
+        const float x0 = ld_elem(a.q, off, 1), x1 = ld_elem(a.q, off + 1, 1);
+        float y0 = x0, y1 = x1;
+        if (a.rope) rope_pair(x0, x1, a.rope[(size_t)t_q * (D / 2) + i], y0, y1);
+        qf[h * D + 2 * i] = y0;
+        qf[h * D + 2 * i + 1] = y1;
+    }
+    __syncthreads();
+    for (int h = warp; h < G; h += kWarps) {
+        float amax = 0.f;
+        for (int i = lane; i < D; i += 32) amax = fmaxf(amax, fabsf(qf[h * D + i]));
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-        const size_t off = (rowq0 + h) * D + r * 8;
-        const uint4 u = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q) + off);
-        float x[8];
-        bf16x8_to_f32(u, x);
+        for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        const float sq = amax > 0.f ? amax / 32767.f : 0.f;
+        const float inv = amax > 0.f ? 32767.f / amax : 0.f;
+        for (int wd = lane; wd < D / 4; wd += 32) {
+            uint32_t hi = 0, lo = 0;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            float y0 = x[2 * j], y1 = x[2 * j + 1];
-            if (a.rope) rope_pair(x[2 * j], x[2 * j + 1], a.rope[(size_t)t_q * (D / 2) + r * 4 + j], y0, y1);
-            q[h][2 * j] = y0;
-            q[h][2 * j + 1] = y1;
-        }
-        if (grp == 0) {
-#pragma unroll
-            for (int bb = 0; bb < 8 / C::BW; ++bb) {
-                float ss = 0.f;
-#pragma unroll
-                for (int e = bb * C::BW; e < (bb + 1) * C::BW; ++e) ss = __fadd_ru(ss, __fmul_ru(q[h][e], q[h][e]));
-                myNQ[h * kBands + r * (8 / C::BW) + bb] = __fsqrt_ru(ss);
+            for (int e = 0; e < 4; ++e) {
+                const int qi = max(-32767, min(32767, __float2int_rn(qf[h * D + 4 * wd + e] * inv)));
+                hi |= (uint32_t)((qi >> 8) & 0xff) << (8 * e);
+                lo |= (uint32_t)(qi & 0xff) << (8 * e);
             }
+            sQW[h * (D / 4) + wd] = hi;
+            sQW[G * (D / 4) + h * (D / 4) + wd] = lo;
         }
-#pragma unroll
-        for (int e = 0; e < 8; ++e) q[h][e] *= a.scale_log2;
+        if (lane < kBands) {
+            float ss = 0.f;
+            for (int e = lane * (D / kBands); e < (lane + 1) * (D / kBands); ++e)
+                ss = __fadd_ru(ss, __fmul_ru(qf[h * D + e], qf[h * D + e]));
+            sNQ[h * kBands + lane] = __fsqrt_ru(ss);
+        }
+        if (lane == 0) sF[h] = sq * a.scale_log2;
     }
-    __syncwarp();
-    // band norms of the heads whose scores this lane ends up owning
-    float nq[C::OUT][kBands];
+    __syncthreads();
+    uint32_t qhi[G][4], qlo[G][4];
 #pragma unroll
-    for (int j = 0; j < C::OUT; ++j) {
-        const int h = (r * C::OUT + j) % G;
+    for (int h = 0; h < G; ++h)
 #pragma unroll
-        for (int bb = 0; bb < kBands; ++bb) nq[j][bb] = myNQ[h * kBands + bb];
-    }
+        for (int e = 0; e < 4; ++e) {
+            qhi[h][e] = sQW[h * (D / 4) + r * 4 + e];
+            qlo[h][e] = sQW[G * (D / 4) + h * (D / 4) + r * 4 + e];
+        }
 
     float m_w[G], l_w[G], c_w[G], acc[G][8];
 #pragma unroll
@@ -241,25 +273,25 @@ __global__ void __launch_bounds__(kWarps * 32, G >= 8 ? 3 : 4) int8_decode_kerne
     if (nk > 0 && ok) {
         const float* skb = a.sk + ((size_t)b * a.Hkv + kvh) * (a.S / kQBlock) + k0 / kQBlock;
         const float* svb = a.sv + ((size_t)b * a.Hkv + kvh) * (a.S / kQBlock) + k0 / kQBlock;
+        // ---- scores: exact int32 dot products of the query bytes with the codes
 #pragma unroll
         for (int kb = 0; kb < C::KPG; kb += C::KB) {
-            float part[C::M];
+            int part[C::M];
 #pragma unroll
             for (int k = 0; k < C::KB; ++k) {
                 const int t = grp * C::KPG + kb + k;
-                const uint2 u = *reinterpret_cast<const uint2*>(myK + t * D + r * 8);
-                float x[8];
-                s8x4_to_f32(u.x, x);
-                s8x4_to_f32(u.y, x + 4);
+                const uint4 u = *reinterpret_cast<const uint4*>(myK + t * D + r * 16);
 #pragma unroll
                 for (int h = 0; h < G; ++h) {
-                    float s0 = q[h][0] * x[0], s1 = q[h][1] * x[1];
-#pragma unroll
-                    for (int e = 2; e < 8; e += 2) {
-                        s0 = fmaf(q[h][e], x[e], s0);
-                        s1 = fmaf(q[h][e + 1], x[e + 1], s1);
-                    }
-                    part[k * G + h] = s0 + s1;
+                    int hi = __dp4a((int)qhi[h][0], (int)u.x, 0);
+                    int lo = dp4a_us(qlo[h][0], u.x, 0);
+                    hi = __dp4a((int)qhi[h][1], (int)u.y, hi);
+                    lo = dp4a_us(qlo[h][1], u.y, lo);
+                    hi = __dp4a((int)qhi[h][2], (int)u.z, hi);
+                    lo = dp4a_us(qlo[h][2], u.z, lo);
+                    hi = __dp4a((int)qhi[h][3], (int)u.w, hi);
+                    lo = dp4a_us(qlo[h][3], u.w, lo);
+                    part[k * G + h] = hi * 256 + lo;
                 }
             }
 #pragma unroll
@@ -267,8 +299,8 @@ __global__ void __launch_bounds__(kWarps * 32, G >= 8 ? 3 : 4) int8_decode_kerne
                 const bool upper = (r & mask) != 0;
 #pragma unroll
                 for (int j = 0; j < cnt / 2; ++j) {
-                    const float keep = upper ? part[j + cnt / 2] : part[j];
-                    const float send = upper ? part[j] : part[j + cnt / 2];
+                    const int keep = upper ? part[j + cnt / 2] : part[j];
+                    const int send = upper ? part[j] : part[j + cnt / 2];
                     part[j] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
                 }
             }
@@ -277,60 +309,85 @@ __global__ void __launch_bounds__(kWarps * 32, G >= 8 ? 3 : 4) int8_decode_kerne
                 const int o = r * C::OUT + j;
                 const int t = grp * C::KPG + kb + o / G;
                 const int h = o % G;
-                if (t < nk) {
-                    myP[t * G + h] = part[j] * skb[t / kQBlock];
-                    // the bound for (t, h): every operation rounded up
-                    const __half2* w2 = reinterpret_cast<const __half2*>(myW + t * kBands);
-                    float c = 0.f;
-#pragma unroll
-                    for (int bb = 0; bb < kBands / 2; ++bb) {
-                        const float2 w = __half22float2(w2[bb]);
-                        c = __fmaf_ru(nq[j][2 * bb], w.x, c);
-                        c = __fmaf_ru(nq[j][2 * bb + 1], w.y, c);
-                    }
-                    c = __fmul_ru(c, a.inv_sqrt_d_up);
-                    c_w[h] = fmaxf(c_w[h], c);
-                    if (a.ct) a.ct[(rowq0 + h) * a.S + k0 + t] = c;
-                } else {
-                    myP[t * G + h] = -INFINITY;
-                }
+                myP[t * G + h] = (t < nk) ? (float)part[j] * (sF[h] * skb[t / kQBlock]) : -INFINITY;
             }
         }
         __syncwarp();
-        // softmax over the warp's keys (lane = key); p' = p * s_V folds the value scale
+        // ---- lane = key: softmax weights, the value scale folded into p, and the bound
+        float pk[G];
+        float smax[G];
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-            const float s = myP[lane * G + h];
-            float mx = s;
+            const float sv = myP[lane * G + h];
+            float mx = sv;
 #pragma unroll
             for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-            const float p = exp2f(s - mx);
-            myP[lane * G + h] = lane < nk ? p * svb[lane / kQBlock] : 0.f;
-            float l = p;
+            smax[h] = mx;
+            pk[h] = exp2f(sv - mx);                   // masked keys: 2^-inf = 0
+        }
+        if (lane < nk) {
+            const float vs = svb[lane / kQBlock];
+            const uint4* wr = reinterpret_cast<const uint4*>(myW + lane * kBands);
+            float wf[kBands];
 #pragma unroll
-            for (int o = 16; o; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-            m_w[h] = mx;
-            l_w[h] = l;
+            for (int c2 = 0; c2 < 2; ++c2) {
+                const uint4 u = wr[c2];
+                const uint32_t ww[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&ww[e]));
+                    wf[c2 * 8 + 2 * e] = f.x;
+                    wf[c2 * 8 + 2 * e + 1] = f.y;
+                }
+            }
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                myP[lane * G + h] = pk[h] * vs;
+                float c = 0.f;
+#pragma unroll
+                for (int bb = 0; bb < kBands; ++bb) c = __fmaf_ru(sNQ[h * kBands + bb], wf[bb], c);
+                c = __fmul_ru(c, a.inv_sqrt_d_up);
+                c_w[h] = fmaxf(c_w[h], c);
+                if (a.ct) a.ct[(rowq0 + h) * a.S + k0 + lane] = c;
+            }
+        } else {
+#pragma unroll
+            for (int h = 0; h < G; ++h) myP[lane * G + h] = 0.f;
+        }
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            float l = pk[h];
             float cm = c_w[h];
 #pragma unroll
-            for (int o = 16; o; o >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o));
+            for (int o = 16; o; o >>= 1) {
+                l += __shfl_xor_sync(0xffffffffu, l, o);
+                cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o));
+            }
+            m_w[h] = smax[h];
+            l_w[h] = l;
             c_w[h] = cm;
         }
         __syncwarp();
-        for (int t = grp; t < nk; t += C::RPP) {
-            const uint2 u = *reinterpret_cast<const uint2*>(myV + t * D + r * 8);
+        // ---- P.V: lane owns dims [8 r2, 8 r2 + 8) of every head, keys of its group
+        for (int t = grp2; t < nk; t += C::RPP2) {
+            const uint2 u = *reinterpret_cast<const uint2*>(myV + t * D + r2 * 8);
             float x[8];
             s8x4_to_f32(u.x, x);
             s8x4_to_f32(u.y, x + 4);
 #pragma unroll
             for (int h = 0; h < G; ++h) {
                 const float p = myP[t * G + h];
+                const float2 pp = make_float2(p, p);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) acc[h][e] = fmaf(p, x[e], acc[h][e]);
+                for (int e = 0; e < 8; e += 2) {
+                    const float2 r_ = __ffma2_rn(pp, make_float2(x[e], x[e + 1]), make_float2(acc[h][e], acc[h][e + 1]));
+                    acc[h][e] = r_.x;
+                    acc[h][e + 1] = r_.y;
+                }
             }
         }
 #pragma unroll
-        for (int mask = C::LPR; mask < 32; mask <<= 1)
+        for (int mask = C::LPR2; mask < 32; mask <<= 1)
 #pragma unroll
             for (int h = 0; h < G; ++h)
 #pragma unroll
@@ -338,12 +395,12 @@ __global__ void __launch_bounds__(kWarps * 32, G >= 8 ? 3 : 4) int8_decode_kerne
     }
     __syncwarp();
     float* part_w = reinterpret_cast<float*>(myK);             // [G][3 + D]
-    if (grp == 0) {
+    if (grp2 == 0) {
 #pragma unroll
         for (int h = 0; h < G; ++h) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) part_w[h * (D + 3) + 3 + r * 8 + e] = acc[h][e];
-            if (r == 0) {
+            for (int e = 0; e < 8; ++e) part_w[h * (D + 3) + 3 + r2 * 8 + e] = acc[h][e];
+            if (r2 == 0) {
                 part_w[h * (D + 3)] = m_w[h];
                 part_w[h * (D + 3) + 1] = l_w[h];
                 part_w[h * (D + 3) + 2] = c_w[h];
@@ -360,16 +417,16 @@ __global__ void __launch_bounds__(kWarps * 32, G >= 8 ? 3 : 4) int8_decode_kerne
             mx = fmaxf(mx, pw[0]);
             cm = fmaxf(cm, pw[2]);
         }
-        float l = 0.f, s = 0.f;
+        float l = 0.f, sacc = 0.f;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) {
             const float* pw = reinterpret_cast<const float*>(smem + w * C::WARPB) + h * (D + 3);
             const float f = pw[0] == -INFINITY ? 0.f : exp2f(pw[0] - mx);
             l += pw[1] * f;
-            s += pw[3 + i] * f;
+            sacc += pw[3 + i] * f;
         }
         const size_t row = (rowq0 + h) * a.max_splits + split;
-        a.part_acc[row * D + i] = s;
+        a.part_acc[row * D + i] = sacc;
         if (i == 0) { a.part_ml[row] = make_float2(mx, l); a.part_c[row] = cm; }
     }
 }

@@ -54,6 +54,7 @@ bool make_shape(const kvc_config& c, Shape* s) {
     s->out_bf16 = c.out_dtype == 0 ? s->bf16 : c.out_dtype == KVC_BF16 + 1;
     s->split = kGenericSplit;
     if (s->bf16 && !int8 && (s->d == 64 || s->d == 128) && s->g <= 8) s->split = kFastSplit;
+    if (s->bf16 && !int8 && gqa_decode_supported(s->d, s->g)) s->split = kGqaSplit;
     const long long keys = (s->W > 0 && s->W < s->S) ? s->W : s->S;
     s->max_splits = (int)((keys + s->split - 1) / s->split);
     if (int8) {
@@ -271,7 +272,7 @@ int kvc_decode_attn(kvc_t h, const void* d_q, void* d_out, float* d_cmax, float*
     a.part_acc = at<float>(h, h->L.part_acc);
     a.hdr = at<uint32_t>(h, h->L.hdr);
     a.B = s.B; a.Hq = s.Hq; a.Hkv = s.Hkv; a.g = s.g; a.d = s.d; a.S = s.S; a.W = s.W;
-    a.max_splits = s.max_splits; a.split = s.split; a.ring = s.ring;
+    a.max_splits = s.max_splits; a.split = s.split; a.ring = s.ring; a.bf16 = s.bf16;
     a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)s.d));
     CombineArgs c{};
     c.part_ml = a.part_ml; c.part_acc = a.part_acc; c.next_pos = a.next_pos; c.out = d_out;

@@ -18,7 +18,8 @@ constexpr int kQBlock = 16;           // tokens per INT8 quantization block
 constexpr int kBands = 16;            // witness bands per key row
 constexpr int kGenericSplit = 64;     // keys per split, generic decode kernel
 constexpr int kFastSplit = 128;       // keys per split, bf16 fast decode kernel
-constexpr int kInt8Split = 128;       // keys per quantized split, INT8 decode kernel
+constexpr int kInt8Split = 256;       // keys per quantized split, INT8 decode kernel
+constexpr int kGqaSplit = 256;        // keys per split, bf16 decode kernel for 4 or 8 heads per KV head
 constexpr uint32_t kErrPosition = 1u; // device error bits (sticky, cleared by kvc_device_status)
 constexpr uint32_t kErrWait = 2u;
 
@@ -66,6 +67,7 @@ struct DecodeArgs {
     uint32_t* hdr;
     int B, Hq, Hkv, g, d, S, W, max_splits, split;
     int ring;
+    int bf16;             // cache dtype (1 = bf16, 0 = fp32)
     float scale_log2;     // log2(e) / sqrt(d)
 };
 
@@ -97,6 +99,8 @@ struct AppendArgs {
 cudaError_t launch_append_token(const AppendArgs& a, cudaStream_t st);
 cudaError_t launch_decode(const DecodeArgs& d, const CombineArgs& c, bool fast, cudaStream_t st);
 bool chunk_supported(const Shape& s);
+bool gqa_decode_supported(int d, int g);
+cudaError_t launch_decode_gqa(const DecodeArgs& a, cudaStream_t st);
 
 // ---- device helpers -----------------------------------------------------------
 __device__ __forceinline__ float ld_elem(const void* p, size_t i, int bf16) {

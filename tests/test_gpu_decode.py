@@ -172,7 +172,7 @@ def test_capacity_and_argument_errors():
     assert cache.device_status() == 0
 
 
-@pytest.mark.parametrize("case", [CASES[1], CASES[4], CASES[3]], ids=lambda c: c[0] + "-out-f32")
+@pytest.mark.parametrize("case", [CASES[1], CASES[4], CASES[3], CASES[6]], ids=lambda c: c[0] + "-out-f32")
 def test_f32_outputs_strict_tolerance(case):
     # bf16 cache, fp32 outputs: no output rounding, so the plain 2e-3 bound applies
     name, Hq, Hkv, d, layout, cap, window, rope = case
