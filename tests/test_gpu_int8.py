@@ -48,7 +48,7 @@ def check_int8_state(cache, model, requests=None):
                 sK, cK, sV, cV, wit = model.quantized_block(b, h, blk)
                 sl = slice(blk * QBLOCK, (blk + 1) * QBLOCK)
                 assert SK[b, h, blk] == sK and SV[b, h, blk] == sV, (b, h, blk)
-                assert np.array_equal(KQ[b, h, sl], cK) and np.array_equal(VQ[b, h, sl], cV), (b, h, blk)
+                assert np.array_equal(KQ[b, h, sl], cK) and np.array_equal(VQ[b, h, blk], cV.T), (b, h, blk)
                 assert np.array_equal(WT[b, h, sl], wit), (b, h, blk)
             for p in range(nfull, n):
                 assert np.array_equal(KT[b, h, p % QBLOCK], nm.f32_to_bf16(model.hk[b][p][h])), (b, h, p)
@@ -78,7 +78,9 @@ def check_decode(cache, model, q, heads=None):
     return out
 
 
-@pytest.mark.parametrize("d,Hq,Hkv", [(128, 8, 2), (64, 8, 1), (128, 4, 4)])
+# every group size the fused kernel instantiates (1, 2, 4, 8), at both head dims
+@pytest.mark.parametrize("d,Hq,Hkv", [(128, 8, 2), (64, 8, 1), (128, 4, 4), (64, 4, 4), (128, 4, 2),
+                                      (64, 4, 2), (128, 16, 2), (64, 8, 2)])
 def test_int8_prefill_decode_parity(d, Hq, Hkv):
     w = wl.small("int8-%d-%d-%d" % (d, Hq, Hkv), B=3, Hq=Hq, Hkv=Hkv, d=d, capacity=512, rope_base=10000.0,
                  quant="int8", seed=19, outliers=(4, 20.0))
