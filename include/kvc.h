@@ -201,8 +201,9 @@ enum {
     KVC_EXPORT_V = 1,
     KVC_EXPORT_POSITIONS = 2,     /* int32 [B][capacity] */
     KVC_EXPORT_NEXT_POSITION = 3, /* int32 [B] */
-    KVC_EXPORT_KQ = 4,            /* int8 [B][Hkv][capacity][d]          (INT8) */
-    KVC_EXPORT_VQ = 5,            /* int8 [B][Hkv][capacity/16][d][16]: dim-major per block */
+    KVC_EXPORT_KQ = 4,            /* int8 [B][Hkv][capacity][d] signed codes (INT8; stored
+                                     biased and in the decode's block order, converted here) */
+    KVC_EXPORT_VQ = 5,            /* int8 [B][Hkv][capacity][d], as KQ */
     KVC_EXPORT_SK = 6,            /* fp32 [B][Hkv][capacity/16]           (INT8) */
     KVC_EXPORT_SV = 7,
     KVC_EXPORT_WITNESS = 8,       /* fp16 [B][Hkv][capacity][16]          (INT8) */

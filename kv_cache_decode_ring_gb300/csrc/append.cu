@@ -86,15 +86,16 @@ __device__ void quantize_block(const AppendArgs& a, const float* sK, const float
         a.sk[bh * (a.S / kQBlock) + blk] = s_k;
         a.sv[bh * (a.S / kQBlock) + blk] = s_v;
     }
-    // K codes row-major [16][d]; V codes dim-major within the block [d][16], so that
-    // the decode kernel reads 16 tokens of one dim as one 16-byte word run
+    // codes stored biased (c + 128) at the block positions kq_offset / vq_offset
+    uint8_t* kb = reinterpret_cast<uint8_t*>(a.kq) + row0 * d;
+    uint8_t* vb = reinterpret_cast<uint8_t*>(a.vq) + row0 * d;
     for (int i = threadIdx.x; i < n; i += blockDim.x) {
         int ck = 0, cv = 0;
         if (s_k != 0.f) ck = max(-127, min(127, __float2int_rn(__fdiv_rn(sK[i], s_k))));
         if (s_v != 0.f) cv = max(-127, min(127, __float2int_rn(__fdiv_rn(sV[i], s_v))));
         const int t = i / d, dim = i % d;
-        a.kq[row0 * d + i] = (int8_t)ck;
-        a.vq[row0 * d + dim * kQBlock + t] = (int8_t)cv;
+        kb[kq_offset(d, t, dim)] = (uint8_t)(ck + 128);
+        vb[vq_offset(d, t, dim)] = (uint8_t)(cv + 128);
     }
     // witnesses: one thread per (row, band)
     const int bw = d / kBands;

@@ -9,9 +9,10 @@
 // they fold into scalars: the score of key t in block m is s_K[m] (q . code_t),
 // and block m contributes s_V[m] sum_t p_t code_t to the output.
 //
-// Layout read per (request, KV head): K codes int8 [S][d], V codes int8 per
-// 16-token block dim-major [S/16][d][16], scales fp32 [S/16], witnesses fp16
-// [S][16], exact bf16 tail [16][d] for the rows of the incomplete block.
+// Layout read per (request, KV head): per 16-token block 16*d K code bytes and
+// 16*d V code bytes (biased, in the block orders of kq_offset / vq_offset),
+// fp16 witnesses [S][16], fp32 scales [S/16]; exact bf16 tail [16][d] for the
+// rows of the incomplete block.
 //
 // Kernel shape: CTA = 4 warps = a split of 256 tokens (16 blocks); each warp
 // streams its 4 blocks through two shared-memory stages (codes and witnesses by
@@ -19,20 +20,23 @@
 // softmax over the warp's blocks, warps merged at the end.  One extra split
 // handles the exact tail rows (c_t = 0 there).
 //
-// Arithmetic, chosen to spend few instructions per cached byte:
-//  * scores: the rotated fp32 query of each head is carried as a 16-bit
-//    integer q ~ s_q (256 hi + lo) (s_q = max|q| / 32767, round to nearest);
-//    dp4a on the raw K codes gives the exact int32 dot product per head, then
-//    one multiply by s_q * s_K * log2(e)/sqrt(d);
-//  * P.V: per block and head the weights are carried as 16-bit integers
-//    relative to the block's largest weight, and dp4a over 4 tokens of one dim
-//    at a time (the dim-major V layout) gives the exact int32 block sum, scaled
-//    back by max_p * s_V / 32767 into fp32 accumulators;
-//  * the bound with every operation rounded toward +inf from the fp32 query
-//    (band norms, products with the witnesses, their sum, an upward 1/sqrt(d));
-//    tanh gets two ulps of headroom over CUDA tanhf's documented error.
-// The integer query and weights change the output by about 2^-16 relative,
-// far inside the bf16 tolerance; the bound is evaluated with the fp32 query.
+// Both contractions of a block run on the tensor cores as fp16 MMAs with fp32
+// accumulation (m16n8k16), operands built in registers:
+//  * codes -> fp16 exactly: a byte permute makes 1024 + u from the biased byte
+//    u = c + 128 and one half2 add subtracts 1152;
+//  * scores, transposed: S^T[16 tokens][cols] = K[16][d] . Q^T[d][cols] where the
+//    columns are (head, hi) and (head, lo): the rotated query, scaled by a power
+//    of two, split into two fp16 parts (about 22 significant bits).  The result
+//    fragment leaves lane L the whole scores of head L%4 for tokens L/4 and
+//    L/4 + 8, so the block maximum is a 3-step shuffle among 8 lanes;
+//  * P.V, transposed: O^T[d][cols] += V^T[d][16] . P^T[16][cols], P = the block's
+//    softmax weights times s_V / (the warp's largest s_V), again as fp16 hi + lo.
+//    Lane L accumulates the output of the same head L%4, so the online-softmax
+//    rescale is local to the lane.
+// The bound is evaluated in fp32 from the fp32 query with every operation
+// rounded toward +inf (band norms, products with the witnesses, their sums, an
+// upward 1/sqrt(d)); tanh gets two ulps of headroom over CUDA tanhf's documented
+// error.  Query and weight splits change the output by about 2^-22 relative.
 #include <cmath>
 
 #include "async_copy.h"
@@ -77,54 +81,73 @@ struct Int8CombineArgs {
     int B, Hq, d, max_splits, out_bf16;
 };
 
-// dp4a with unsigned bytes in a and signed bytes in b
-__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
-    int d;
-    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-    return d;
+// D (16x8, fp32) += A (16x16, fp16, row) . B (16x8, fp16, col)
+__device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Four biased code bytes u = c + 128 -> two half2 words holding the exact codes:
+// lo = (c0, c1), hi = (c2, c3).  0x64 above a byte u is the fp16 1024 + u.
+__device__ __forceinline__ void codes_to_half2(uint32_t u, uint32_t& lo, uint32_t& hi) {
+    uint32_t x, y;
+    asm("prmt.b32 %0, %1, 0x64646464, 0x5140;" : "=r"(x) : "r"(u));
+    asm("prmt.b32 %0, %1, 0x64646464, 0x7362;" : "=r"(y) : "r"(u));
+    const __half2 off = __halves2half2(__ushort_as_half(0xE480), __ushort_as_half(0xE480));  // -1152
+    const __half2 a = __hadd2(*reinterpret_cast<const __half2*>(&x), off);
+    const __half2 b = __hadd2(*reinterpret_cast<const __half2*>(&y), off);
+    lo = *reinterpret_cast<const uint32_t*>(&a);
+    hi = *reinterpret_cast<const uint32_t*>(&b);
+}
+
+// x = hi + lo with hi = fp16(x) and lo = fp16(x - hi)
+__device__ __forceinline__ void split_half(float x, __half& hi, __half& lo) {
+    hi = __float2half_rn(x);
+    lo = __float2half_rn(x - __half2float(hi));
 }
 
 template <int D, int G>
 struct I8 {
-    static constexpr int LPR = D / 16;            // score lanes per row, 16 codes each
-    static constexpr int RPP = 32 / LPR;          // key groups per warp for the scores
-    static constexpr int KPG = kQBlock / RPP;     // keys per group per block
-    static constexpr int KB0 = 2 * LPR / G;
-    static constexpr int KB = KB0 < KPG ? (KB0 < 1 ? 1 : KB0) : KPG;
-    static constexpr int M = KB * G;              // int32 partial scores per lane per batch
-    // finished scores per lane per batch; with fewer partials than lanes (M < LPR) the
-    // last reduction steps are all-reduces and LPR/M lanes share each score
-    static constexpr int OUT = M >= LPR ? M / LPR : 1;
-    static constexpr int SHARE = M >= LPR ? 1 : LPR / M;
-    static constexpr int DPL = D / 32;            // output dims per lane for P.V
-    static constexpr int CB = kQBlock * D;        // bytes of one block's codes (K or V)
+    static constexpr int KS = D / 16;               // k-steps of the score MMA (= m-tiles of P.V)
+    static constexpr int NT = (2 * G + 7) / 8;      // 8-column tiles of (head, hi|lo) columns
+    static constexpr int HPL = NT;                  // heads per lane (L%4, and 4 + L%4)
+    static constexpr int KW = D / 16;               // K code words per lane per row (= KS)
+    static constexpr int VW = D / 8;                // V code words per lane
+    static constexpr int CB = kQBlock * D;          // bytes of one block's codes (K or V)
     static constexpr int WB = kQBlock * kBands * 2;
     static constexpr int STAGEB = 2 * CB + WB;
     static constexpr int WARPB = 2 * STAGEB;
-    static constexpr int PARTF = G * (D + 3);     // floats of one warp's partial (m, l, c, acc)
-    static_assert(KPG >= 1 && (M % LPR == 0 || LPR % M == 0), "batch shape");
+    static constexpr int PARTF = G * (D + 3);       // floats of one warp's partial (m, l, c, acc)
     static_assert(PARTF * 4 <= WARPB, "partial must fit in the warp's stages");
-    // after the warps' stages: scores [warp][16][G] (the fp32 query during preparation),
-    // weight bytes [warp][G][2][16], query bytes [2][G][D/4] words, band norms [G][16],
-    // score factors [G], barriers [warp][2]
+    // P^T staging per warp and column tile: 8 rows of 16 fp16 tokens; row n at
+    // 32 n + 16 (n >= 4) bytes, so the lanes' stores and 8-byte loads are free of
+    // bank conflicts
+    static constexpr int PROWB = 288;
+    // after the warps' stages: P^T staging [warp][NT] (the fp32 query during
+    // preparation), fp16 query [2G][D], band norms [G][20], score factors [G],
+    // barriers [warp][2]
     static constexpr int OFF_P = kWarps * WARPB;
-    static constexpr int PBYTES = (kWarps * kQBlock * G > G * D ? kWarps * kQBlock * G : G * D) * 4;
-    static constexpr int OFF_PW = OFF_P + PBYTES;
-    static constexpr int OFF_QW = OFF_PW + kWarps * G * 2 * kQBlock;
-    static constexpr int OFF_NQ = OFF_QW + 2 * G * (D / 4) * 4;
-    static constexpr int OFF_F = OFF_NQ + G * kBands * 4;
+    static constexpr int PBYTES = (kWarps * NT * PROWB > G * D * 4 ? kWarps * NT * PROWB : G * D * 4);
+    static constexpr int OFF_QH = OFF_P + ((PBYTES + 15) / 16) * 16;
+    static constexpr int OFF_NQ = OFF_QH + 2 * G * D * 2;
+    static constexpr int OFF_F = OFF_NQ + G * 20 * 4;       // norms padded to 20 floats a head
     static constexpr int OFF_BAR = OFF_F + ((G * 4 + 15) / 16) * 16;
     static constexpr size_t SMEM = OFF_BAR + kWarps * 2 * 8 + 128;
 };
 
+__device__ __forceinline__ int prow(int n) { return 32 * n + (n >= 4 ? 16 : 0); }
+
 template <int D, int G>
-__global__ void __launch_bounds__(kWarps * 32, G >= 8 ? (D >= 128 ? 2 : 3) : 4) int8_decode_kernel(const Int8Args a) {
+__global__ void __launch_bounds__(kWarps * 32, G >= 8 ? (D >= 128 ? 3 : 4) : 4) int8_decode_kernel(const Int8Args a) {
     using C = I8<D, G>;
     extern __shared__ __align__(128) unsigned char smem[];
-    float* sP = reinterpret_cast<float*>(smem + C::OFF_P);              // [warp][16][G]
-    unsigned char* sPW = smem + C::OFF_PW;                               // [warp][G][2][16] weight bytes
-    uint32_t* sQW = reinterpret_cast<uint32_t*>(smem + C::OFF_QW);      // [2][G][D/4] query bytes
-    float* sNQ = reinterpret_cast<float*>(smem + C::OFF_NQ);            // [G][16] band norms
+    unsigned char* sPm = smem + C::OFF_P;                                // [warp][NT] P^T staging
+    __half* sQh = reinterpret_cast<__half*>(smem + C::OFF_QH);          // [2G][D]: row 2h hi, 2h + 1 lo
+    float* sNQ = reinterpret_cast<float*>(smem + C::OFF_NQ);            // [G][20] band norms
     float* sF = reinterpret_cast<float*>(smem + C::OFF_F);              // [G] score factors
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);     // [warp][2]
 
@@ -188,6 +211,7 @@ __global__ void __launch_bounds__(kWarps * 32, G >= 8 ? (D >= 128 ? 2 : 3) : 4) 
         return;
     }
 
+
     // ---- quantized split ----------------------------------------------------
     const size_t bh = (size_t)b * a.Hkv + kvh;
     const size_t row0 = bh * a.S;
@@ -215,10 +239,23 @@ __global__ void __launch_bounds__(kWarps * 32, G >= 8 ? (D >= 128 ? 2 : 3) : 4) 
     issue(0);
     issue(1);
 
+    // block scales of this warp's tiles: lane i < 4 holds tile i's s_K and its s_V
+    // relative to the warp's largest s_V, times 2^15 (keeps the fp16 weights normal)
+    float skv = 0.f, rvv = 0.f;
+    if (lane < kTilesPerWarp && tile_ok(lane)) {
+        skv = a.sk[bh * (a.S / kQBlock) + tile_blk(lane)];
+        rvv = a.sv[bh * (a.S / kQBlock) + tile_blk(lane)];
+    }
+    float svmax = rvv;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) svmax = fmaxf(svmax, __shfl_xor_sync(0xffffffffu, svmax, o));
+    rvv = svmax > 0.f ? rvv / svmax * 32768.f : 0.f;
+
     // ---- query preparation, once per CTA while the copies fly: rotated fp32
-    // query; per head its 16-bit integer copy for the scores and the band norms
-    // of the fp32 query, rounded up, for the bound
-    float* qf = sP;                                           // [G][D] until the scores use it
+    // query; per head a power-of-two scale 2^e putting max|q| in [2^14, 2^15),
+    // the scaled query as fp16 hi + lo, and the band norms of the fp32 query,
+    // rounded up, for the bound
+    float* qf = reinterpret_cast<float*>(sPm);                 // [G][D] until the P staging uses it
     for (int idx = threadIdx.x; idx < G * D / 2; idx += blockDim.x) {
         const int h = idx / (D / 2), i = idx % (D / 2);
         const size_t off = (rowq0 + h) * D + 2 * i;
@@ -234,53 +271,65 @@ __global__ void __launch_bounds__(kWarps * 32, G >= 8 ? (D >= 128 ? 2 : 3) : 4) 
         for (int i = lane; i < D; i += 32) amax = fmaxf(amax, fabsf(qf[h * D + i]));
 #pragma unroll
         for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        const float inv = amax > 0.f ? 32767.f / amax : 0.f;
-        for (int wd = lane; wd < D / 4; wd += 32) {
-            uint32_t hi = 0, lo = 0;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int qi = max(-32767, min(32767, __float2int_rn(qf[h * D + 4 * wd + e] * inv)));
-                hi |= (uint32_t)((qi >> 8) & 0xff) << (8 * e);
-                lo |= (uint32_t)(qi & 0xff) << (8 * e);
-            }
-            sQW[h * (D / 4) + wd] = hi;
-            sQW[G * (D / 4) + h * (D / 4) + wd] = lo;
+        int ex = 0;
+        frexpf(amax, &ex);                                    // amax = m 2^ex, m in [1/2, 1)
+        const int e = max(-126, min(126, 15 - ex));
+        const float up = __int_as_float((127 + e) << 23), down = __int_as_float((127 - e) << 23);
+        for (int i = lane; i < D; i += 32) {
+            __half hi, lo;
+            split_half(qf[h * D + i] * up, hi, lo);
+            sQh[(2 * h) * D + i] = hi;
+            sQh[(2 * h + 1) * D + i] = lo;
         }
         if (lane < kBands) {
             float ss = 0.f;
-            for (int e = lane * (D / kBands); e < (lane + 1) * (D / kBands); ++e)
-                ss = __fadd_ru(ss, __fmul_ru(qf[h * D + e], qf[h * D + e]));
-            sNQ[h * kBands + lane] = __fsqrt_ru(ss);
+            for (int e2 = lane * (D / kBands); e2 < (lane + 1) * (D / kBands); ++e2)
+                ss = __fadd_ru(ss, __fmul_ru(qf[h * D + e2], qf[h * D + e2]));
+            sNQ[h * 20 + lane] = __fsqrt_ru(ss);
         }
-        if (lane == 0) sF[h] = (amax > 0.f ? amax / 32767.f : 0.f) * a.scale_log2;
+        if (lane == 0) sF[h] = (amax > 0.f ? down : 0.f) * a.scale_log2;
     }
     __syncthreads();
-    const int r = lane % C::LPR, grp = lane / C::LPR;
-    uint32_t qhi[G][4], qlo[G][4];
-#pragma unroll
-    for (int h = 0; h < G; ++h)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            qhi[h][e] = sQW[h * (D / 4) + r * 4 + e];
-            qlo[h][e] = sQW[G * (D / 4) + h * (D / 4) + r * 4 + e];
-        }
 
-    float* myP = sP + warp * kQBlock * G;
-    unsigned char* myPW = sPW + warp * G * 2 * kQBlock;
-    float m_w[G], l_w[G], c_w[G], acc[G][C::DPL];
+    // ---- per-lane fragments: g = L/4 (MMA group), qd = L%4
+    const int g = lane >> 2, qd = lane & 3;
+    // score B operand (Q^T): column n = 8 nt + g = (head n/2, hi|lo n%2); k-step s
+    // covers the dims qd (D/4) + 4 s .. + 3 in the lane's registers
+    uint32_t qb[C::NT][C::KS][2];
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-        m_w[h] = -INFINITY; l_w[h] = 0.f; c_w[h] = 0.f;
+    for (int nt = 0; nt < C::NT; ++nt) {
+        const int n = 8 * nt + g;
 #pragma unroll
-        for (int e = 0; e < C::DPL; ++e) acc[h][e] = 0.f;
+        for (int s = 0; s < C::KS; ++s) {
+            uint2 v = make_uint2(0u, 0u);
+            if (n < 2 * G) v = *reinterpret_cast<const uint2*>(sQh + n * D + qd * (D / 4) + 4 * s);
+            qb[nt][s][0] = v.x;
+            qb[nt][s][1] = v.y;
+        }
     }
+    // the lane's heads (4 nt + qd; those >= G only carry dummy values)
+    float fq[C::HPL];
+#pragma unroll
+    for (int nt = 0; nt < C::HPL; ++nt) fq[nt] = sF[min(4 * nt + qd, G - 1)];
+
+    unsigned char* myPm = sPm + warp * C::NT * C::PROWB;
+    float m_w[C::HPL], l_w[C::HPL], c_w[C::HPL];
+    float acc[C::KS][C::NT][4];
+#pragma unroll
+    for (int nt = 0; nt < C::HPL; ++nt) { m_w[nt] = -INFINITY; l_w[nt] = 0.f; c_w[nt] = 0.f; }
+#pragma unroll
+    for (int mt = 0; mt < C::KS; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < C::NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[mt][nt][e] = 0.f;
+
     for (int i = 0; i < kTilesPerWarp; ++i) {
         if (!tile_ok(i)) break;                   // later tiles of this warp are empty too
         const unsigned char* tK = myS + (i & 1) * C::STAGEB;
         const unsigned char* tV = tK + C::CB;
-        const __half* tW = reinterpret_cast<const __half*>(tK + 2 * C::CB);
-        const int blk = tile_blk(i);
-        const int p0 = blk * kQBlock;
+        const uint4* tW = reinterpret_cast<const uint4*>(tK + 2 * C::CB);
+        const int p0 = tile_blk(i) * kQBlock;
         if (!mbar_wait(&myBar[i & 1], (uint32_t)((i >> 1) & 1))) {
             // give up: flag it, and let this stage's copy and the other stage's
             // (if issued) land before the stages are reused for the partial
@@ -289,160 +338,148 @@ __global__ void __launch_bounds__(kWarps * 32, G >= 8 ? (D >= 128 ? 2 : 3) : 4) 
             if (i + 1 < kTilesPerWarp && tile_ok(i + 1)) mbar_wait(&myBar[(i + 1) & 1], (uint32_t)(((i + 1) >> 1) & 1));
             break;
         }
-        const float s_k = a.sk[bh * (a.S / kQBlock) + blk];
-        const float s_v = a.sv[bh * (a.S / kQBlock) + blk];
-        // ---- scores: exact int32 dot products of the query bytes with the codes
+        const float s_k = __shfl_sync(0xffffffffu, skv, i);
+        const float r_v = __shfl_sync(0xffffffffu, rvv, i);
+
+        // ---- scores S^T = K Q^T: rows g and g + 8 of the block, D/64 16-byte
+        // chunks each (at d = 128 odd rows hold their chunk pairs swapped)
+        uint32_t kw0[C::KW], kw1[C::KW];
 #pragma unroll
-        for (int kb = 0; kb < C::KPG; kb += C::KB) {
-            int part[C::M];
+        for (int j = 0; j < C::KW / 4; ++j) {
+            const int ch = (C::KW / 4) * qd + (D == 128 ? (j ^ (g & 1)) : j);
+            const uint4 u0 = *reinterpret_cast<const uint4*>(tK + g * D + ch * 16);
+            const uint4 u1 = *reinterpret_cast<const uint4*>(tK + (g + 8) * D + ch * 16);
+            kw0[4 * j] = u0.x; kw0[4 * j + 1] = u0.y; kw0[4 * j + 2] = u0.z; kw0[4 * j + 3] = u0.w;
+            kw1[4 * j] = u1.x; kw1[4 * j + 1] = u1.y; kw1[4 * j + 2] = u1.z; kw1[4 * j + 3] = u1.w;
+        }
+        float sacc[C::NT][4];
 #pragma unroll
-            for (int k = 0; k < C::KB; ++k) {
-                const int t = grp * C::KPG + kb + k;
-                const uint4 u = *reinterpret_cast<const uint4*>(tK + t * D + r * 16);
+        for (int nt = 0; nt < C::NT; ++nt)
 #pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    int hs = __dp4a((int)qhi[h][0], (int)u.x, 0);
-                    int ls = dp4a_us(qlo[h][0], u.x, 0);
-                    hs = __dp4a((int)qhi[h][1], (int)u.y, hs);
-                    ls = dp4a_us(qlo[h][1], u.y, ls);
-                    hs = __dp4a((int)qhi[h][2], (int)u.z, hs);
-                    ls = dp4a_us(qlo[h][2], u.z, ls);
-                    hs = __dp4a((int)qhi[h][3], (int)u.w, hs);
-                    ls = dp4a_us(qlo[h][3], u.w, ls);
-                    part[k * G + h] = hs * 256 + ls;
+            for (int e = 0; e < 4; ++e) sacc[nt][e] = 0.f;
+#pragma unroll
+        for (int s = 0; s < C::KS; ++s) {
+            uint32_t a0, a1, a2, a3;
+            codes_to_half2(kw0[s], a0, a2);
+            codes_to_half2(kw1[s], a1, a3);
+#pragma unroll
+            for (int nt = 0; nt < C::NT; ++nt) mma_f16(sacc[nt], a0, a1, a2, a3, qb[nt][s][0], qb[nt][s][1]);
+        }
+
+        // ---- online softmax of the lane's head over tokens g, g + 8; weights
+        // times r_v into the P^T staging as fp16 hi + lo; and the bound
+        float alpha[C::HPL];
+        bool rescale = false;
+#pragma unroll
+        for (int nt = 0; nt < C::HPL; ++nt) {
+            const float f = fq[nt] * s_k;
+            const float s0 = (sacc[nt][0] + sacc[nt][1]) * f;
+            const float s1 = (sacc[nt][2] + sacc[nt][3]) * f;
+            float bm = fmaxf(s0, s1);
+            bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
+            bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
+            bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
+            const float mn = fmaxf(m_w[nt], bm);
+            alpha[nt] = exp2f(m_w[nt] - mn);          // 0 while the maximum was -inf
+            rescale |= alpha[nt] != 1.f;
+            m_w[nt] = mn;
+            const float e0 = exp2f(s0 - mn), e1 = exp2f(s1 - mn);
+            l_w[nt] = fmaf(l_w[nt], alpha[nt], e0 + e1);
+            __half h0, l0, h1, l1;
+            split_half(e0 * r_v, h0, l0);
+            split_half(e1 * r_v, h1, l1);
+            unsigned char* pt = myPm + nt * C::PROWB;
+            *reinterpret_cast<__half*>(pt + prow(2 * qd) + 2 * g) = h0;
+            *reinterpret_cast<__half*>(pt + prow(2 * qd + 1) + 2 * g) = l0;
+            *reinterpret_cast<__half*>(pt + prow(2 * qd) + 2 * (g + 8)) = h1;
+            *reinterpret_cast<__half*>(pt + prow(2 * qd + 1) + 2 * (g + 8)) = l1;
+
+            // bound of tokens g, g + 8 for head hq, every operation rounded up
+            const int hq = 4 * nt + qd;
+            const float4* nq = reinterpret_cast<const float4*>(sNQ + min(hq, G - 1) * 20);
+            float cb[2];
+#pragma unroll
+            for (int tt = 0; tt < 2; ++tt) {
+                float2 c2 = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const uint4 u = tW[(g + 8 * tt) * 2 + c];
+                    const float4 na = nq[2 * c], nb = nq[2 * c + 1];
+                    c2 = __ffma2_ru(make_float2(na.x, na.y), __half22float2(*reinterpret_cast<const __half2*>(&u.x)), c2);
+                    c2 = __ffma2_ru(make_float2(na.z, na.w), __half22float2(*reinterpret_cast<const __half2*>(&u.y)), c2);
+                    c2 = __ffma2_ru(make_float2(nb.x, nb.y), __half22float2(*reinterpret_cast<const __half2*>(&u.z)), c2);
+                    c2 = __ffma2_ru(make_float2(nb.z, nb.w), __half22float2(*reinterpret_cast<const __half2*>(&u.w)), c2);
                 }
+                cb[tt] = __fmul_ru(__fadd_ru(c2.x, c2.y), a.inv_sqrt_d_up);
             }
-#pragma unroll
-            for (int mask = C::LPR / 2, cnt = C::M; mask >= 1; mask >>= 1, cnt >>= 1) {
-                if (cnt >= 2) {
-                    const bool upper = (r & mask) != 0;
-#pragma unroll
-                    for (int j = 0; j < cnt / 2; ++j) {
-                        const int keep = upper ? part[j + cnt / 2] : part[j];
-                        const int send = upper ? part[j] : part[j + cnt / 2];
-                        part[j] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
-                    }
-                } else {
-                    part[0] += __shfl_xor_sync(0xffffffffu, part[0], mask);
-                }
+            c_w[nt] = fmaxf(c_w[nt], fmaxf(cb[0], cb[1]));
+            if (a.ct && hq < G) {
+                a.ct[(rowq0 + hq) * a.S + p0 + g] = cb[0];
+                a.ct[(rowq0 + hq) * a.S + p0 + g + 8] = cb[1];
             }
-            if (r % C::SHARE == 0) {
+        }
+        if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
-                for (int j = 0; j < C::OUT; ++j) {
-                    const int o = r / C::SHARE * C::OUT + j;
-                    const int t = grp * C::KPG + kb + o / G;
-                    const int h = o % G;
-                    myP[t * G + h] = (float)part[j] * (sF[h] * s_k);
-                }
-            }
+            for (int mt = 0; mt < C::KS; ++mt)
+#pragma unroll
+                for (int nt = 0; nt < C::NT; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) acc[mt][nt][e] *= alpha[nt];
         }
         __syncwarp();
-        // ---- two heads per pass, lane = (token lane & 15, head h + lane / 16):
-        // online softmax, weights as 16-bit integers relative to the block maximum,
-        // and the bound of the token
-        // (one head: both halves evaluate head 0 and only the lower half writes)
-        constexpr int HP = G >= 2 ? 2 : 1;
-        const int t = lane & 15, half = lane >> 4;
-        const bool writer = G >= 2 || half == 0;
-        float alpha[G], wscale[G];
+
+        // ---- P.V: O^T += V^T P^T; B operand = P^T column g, tokens 4 qd .. + 3
+        uint2 pb[C::NT];
 #pragma unroll
-        for (int h = 0; h < G; h += HP) {
-            const int hh = G >= 2 ? h + half : 0;
-            const float s = myP[t * G + hh];
-            float mx = s;
+        for (int nt = 0; nt < C::NT; ++nt)
+            pb[nt] = *reinterpret_cast<const uint2*>(myPm + nt * C::PROWB + prow(g) + 8 * qd);
+        constexpr int CPR = D / 32;                  // 16-byte chunks of the lane's V run
+        const int swz = (lane / (8 / CPR)) % CPR;
+        uint32_t vw[C::VW];
 #pragma unroll
-            for (int o = 8; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-            const float m_lo = __shfl_sync(0xffffffffu, mx, 0), m_hi = __shfl_sync(0xffffffffu, mx, 16);
-            const float mn0 = fmaxf(m_w[h], m_lo);
-            const float mn1 = G >= 2 ? fmaxf(m_w[(h + 1) % G], m_hi) : mn0;
-            const float mn = half ? mn1 : mn0;
-            const float p = exp2f(s - mn);
-            float ls = p, pm = p;
-#pragma unroll
-            for (int o = 8; o; o >>= 1) {
-                ls += __shfl_xor_sync(0xffffffffu, ls, o);
-                pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, o));
-            }
-            // 16-bit weight bytes: w = rint(p / pm * 32767) = 256 hi + lo
-            const int wi = pm > 0.f ? min(32767, __float2int_rn(p * (32767.f / pm))) : 0;
-            if (writer) {
-                myPW[(hh * 2 + 0) * kQBlock + t] = (unsigned char)(wi >> 8);
-                myPW[(hh * 2 + 1) * kQBlock + t] = (unsigned char)(wi & 0xff);
-            }
-            const float l_lo = __shfl_sync(0xffffffffu, ls, 0), l_hi = __shfl_sync(0xffffffffu, ls, 16);
-            const float pm_lo = __shfl_sync(0xffffffffu, pm, 0), pm_hi = __shfl_sync(0xffffffffu, pm, 16);
-            alpha[h] = exp2f(m_w[h] - mn0);           // 0 while the maximum was -inf
-            l_w[h] = l_w[h] * alpha[h] + l_lo;
-            m_w[h] = mn0;
-            wscale[h] = pm_lo * s_v * (1.f / 32767.f);
-            if constexpr (G >= 2) {
-                alpha[h + 1] = exp2f(m_w[h + 1] - mn1);
-                l_w[h + 1] = l_w[h + 1] * alpha[h + 1] + l_hi;
-                m_w[h + 1] = mn1;
-                wscale[h + 1] = pm_hi * s_v * (1.f / 32767.f);
-            }
-            // the bound of token t for head hh, every operation rounded up
-            const uint4* wr = reinterpret_cast<const uint4*>(tW + t * kBands);
-            const float4* nq = reinterpret_cast<const float4*>(sNQ + hh * kBands);
-            float c = 0.f;
-#pragma unroll
-            for (int c2 = 0; c2 < 2; ++c2) {
-                const uint4 u = wr[c2];
-                const uint32_t ww[4] = {u.x, u.y, u.z, u.w};
-                const float4 n0 = nq[2 * c2], n1 = nq[2 * c2 + 1];
-                const float nn[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&ww[e]));
-                    c = __fmaf_ru(nn[2 * e], f.x, c);
-                    c = __fmaf_ru(nn[2 * e + 1], f.y, c);
-                }
-            }
-            c = __fmul_ru(c, a.inv_sqrt_d_up);
-            if (a.ct && writer) a.ct[(rowq0 + hh) * a.S + p0 + t] = c;
-            float cm = c;
-#pragma unroll
-            for (int o = 8; o; o >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o));
-            c_w[h] = fmaxf(c_w[h], __shfl_sync(0xffffffffu, cm, 0));
-            if constexpr (G >= 2) c_w[h + 1] = fmaxf(c_w[h + 1], __shfl_sync(0xffffffffu, cm, 16));
+        for (int j = 0; j < CPR; ++j) {
+            const uint4 u = *reinterpret_cast<const uint4*>(tV + lane * (D / 2) + ((j ^ swz) << 4));
+            vw[4 * j] = u.x; vw[4 * j + 1] = u.y; vw[4 * j + 2] = u.z; vw[4 * j + 3] = u.w;
         }
-        __syncwarp();
-        // ---- P.V: lane owns dims lane + 32 j; dp4a over 4 tokens of one dim at a time
-        const uint32_t* pw = reinterpret_cast<const uint32_t*>(myPW);
 #pragma unroll
-        for (int j = 0; j < C::DPL; ++j) {
-            const uint4 v = *reinterpret_cast<const uint4*>(tV + (lane + 32 * j) * kQBlock);
+        for (int mt = 0; mt < C::KS; ++mt) {
+            uint32_t a0, a1, a2, a3;
+            codes_to_half2(vw[2 * mt], a0, a2);           // dim 16 mt + g
+            codes_to_half2(vw[2 * mt + 1], a1, a3);       // dim 16 mt + 8 + g
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
-                const uint4 wh = *reinterpret_cast<const uint4*>(pw + (h * 2 + 0) * 4);
-                const uint4 wl = *reinterpret_cast<const uint4*>(pw + (h * 2 + 1) * 4);
-                int hs = dp4a_us(wh.x, v.x, 0);
-                int ls = dp4a_us(wl.x, v.x, 0);
-                hs = dp4a_us(wh.y, v.y, hs);
-                ls = dp4a_us(wl.y, v.y, ls);
-                hs = dp4a_us(wh.z, v.z, hs);
-                ls = dp4a_us(wl.z, v.z, ls);
-                hs = dp4a_us(wh.w, v.w, hs);
-                ls = dp4a_us(wl.w, v.w, ls);
-                acc[h][j] = fmaf(acc[h][j], alpha[h], (float)(hs * 256 + ls) * wscale[h]);
-            }
+            for (int nt = 0; nt < C::NT; ++nt) mma_f16(acc[mt][nt], a0, a1, a2, a3, pb[nt].x, pb[nt].y);
         }
-        // this stage is free once every lane is past its reads: refill it
+        // this stage and the staging are free once every lane is past its reads
         __syncwarp();
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         if (i + 2 < kTilesPerWarp) issue(i + 2);
     }
-    // ---- this warp's partial into its stage buffers (all issued copies were awaited)
+
+    // ---- this warp's partial into its stage buffers (all issued copies were awaited):
+    // l and the bound's maximum over the 8 lanes of a head; output = (hi + lo) columns
     __syncwarp();
     float* part_w = reinterpret_cast<float*>(myS);             // [G][3 + D]
+    const float oscale = svmax * (1.f / 32768.f);
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
+    for (int nt = 0; nt < C::HPL; ++nt) {
+        float l = l_w[nt], c = c_w[nt];
 #pragma unroll
-        for (int j = 0; j < C::DPL; ++j) part_w[h * (D + 3) + 3 + lane + 32 * j] = acc[h][j];
-        if (lane == 0) {
-            part_w[h * (D + 3)] = m_w[h];
-            part_w[h * (D + 3) + 1] = l_w[h];
-            part_w[h * (D + 3) + 2] = c_w[h];
+        for (int o = 4; o < 32; o <<= 1) {
+            l += __shfl_xor_sync(0xffffffffu, l, o);
+            c = fmaxf(c, __shfl_xor_sync(0xffffffffu, c, o));
+        }
+        const int hq = 4 * nt + qd;
+        if (hq < G) {
+#pragma unroll
+            for (int mt = 0; mt < C::KS; ++mt) {
+                part_w[hq * (D + 3) + 3 + 16 * mt + g] = (acc[mt][nt][0] + acc[mt][nt][1]) * oscale;
+                part_w[hq * (D + 3) + 3 + 16 * mt + 8 + g] = (acc[mt][nt][2] + acc[mt][nt][3]) * oscale;
+            }
+            if (g == 0) {
+                part_w[hq * (D + 3)] = m_w[nt];
+                part_w[hq * (D + 3) + 1] = l;
+                part_w[hq * (D + 3) + 2] = c;
+            }
         }
     }
     __syncthreads();

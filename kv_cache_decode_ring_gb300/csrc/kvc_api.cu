@@ -2,6 +2,7 @@
 // mirror of next_position, RoPE table, and kernel launches.
 #include <cmath>
 #include <cstring>
+#include <vector>
 #include <new>
 
 #include "kvc_internal.h"
@@ -370,8 +371,26 @@ int kvc_export(kvc_t h, int32_t which, void* h_dst, size_t bytes, kvc_stream_t s
         default: return KVC_ERR_ARG;
     }
     cudaStream_t st = S_(stream);
-    if (cudaMemcpyAsync(h_dst, h->state + off, need, cudaMemcpyDeviceToHost, st) != cudaSuccess) return KVC_ERR_CUDA;
+    const bool codes = which == KVC_EXPORT_KQ || which == KVC_EXPORT_VQ;
+    std::vector<uint8_t> raw(codes ? need : 0);
+    void* dst = codes ? static_cast<void*>(raw.data()) : h_dst;
+    if (cudaMemcpyAsync(dst, h->state + off, need, cudaMemcpyDeviceToHost, st) != cudaSuccess) return KVC_ERR_CUDA;
     if (cudaStreamSynchronize(st) != cudaSuccess) return KVC_ERR_CUDA;
+    if (codes) {
+        // stored biased in the decode's block order; exported signed, token-major [S][d]
+        const int d = h->sh.d;
+        const size_t blocks = need / ((size_t)kQBlock * d);
+        int8_t* out = static_cast<int8_t*>(h_dst);
+        for (size_t blk = 0; blk < blocks; ++blk) {
+            const uint8_t* src = raw.data() + blk * kQBlock * d;
+            int8_t* o = out + blk * kQBlock * d;
+            for (int t = 0; t < kQBlock; ++t)
+                for (int x = 0; x < d; ++x) {
+                    const int at = which == KVC_EXPORT_KQ ? kq_offset(d, t, x) : vq_offset(d, t, x);
+                    o[t * d + x] = (int8_t)((int)src[at] - 128);
+                }
+        }
+    }
     return KVC_OK;
 }
 

@@ -102,6 +102,28 @@ bool chunk_supported(const Shape& s);
 bool gqa_decode_supported(int d, int g);
 cudaError_t launch_decode_gqa(const DecodeArgs& a, cudaStream_t st);
 
+// ---- INT8 code storage --------------------------------------------------------
+// Inside one 16-token block of one (request, KV head) the 16*d code bytes are
+// stored biased, u = c + 128 (bit pattern c ^ 0x80), so that the decode turns a
+// byte into the fp16 value 1024 + u with one byte permute.  Byte offsets of code
+// (token t of the block, dim x), for d in {64, 128}:
+//  K: token-major rows of d bytes; at d = 128 the 16-byte chunks of odd rows are
+//     swapped pairwise (chunk c at c ^ 1), so that the decode's 16-byte row loads
+//     hit every bank group once.
+//  V: ordered for the decode's P.V operand fragments: lane L = 4 (x mod 8) + t/4
+//     owns a d/2-byte run holding word f = x/8 (tokens 4 (t/4) .. +3 of dim x),
+//     its 16-byte chunks XOR-swizzled by lane so that 8 lanes' loads hit 8 groups.
+__host__ __device__ __forceinline__ int kq_offset(int d, int t, int x) {
+    const int sw = d == 128 ? (t & 1) : 0;
+    return t * d + (((x >> 4) ^ sw) << 4) + (x & 15);
+}
+__host__ __device__ __forceinline__ int vq_offset(int d, int t, int x) {
+    const int lane = 4 * (x & 7) + (t >> 2), f = x >> 3;
+    const int cpr = d / 32;                          // 16-byte chunks per lane run
+    const int swz = (lane / (8 / cpr)) % cpr;
+    return lane * (d / 2) + (((f >> 2) ^ swz) << 4) + ((f & 3) << 2) + (t & 3);
+}
+
 // ---- device helpers -----------------------------------------------------------
 __device__ __forceinline__ float ld_elem(const void* p, size_t i, int bf16) {
     return bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(p)[i])

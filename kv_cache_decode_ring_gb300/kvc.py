@@ -322,7 +322,7 @@ class Cache:
         arr = raw.view(self._EXPORT_DTYPES[which])
         shapes = {KVC_EXPORT_POSITIONS: (self.B, self.S), KVC_EXPORT_NEXT_POSITION: (self.B,),
                   KVC_EXPORT_KQ: (self.B, self.Hkv, self.S, self.d),
-                  KVC_EXPORT_VQ: (self.B, self.Hkv, self.S // 16, self.d, 16),
+                  KVC_EXPORT_VQ: (self.B, self.Hkv, self.S, self.d),
                   KVC_EXPORT_SK: (self.B, self.Hkv, self.S // 16), KVC_EXPORT_SV: (self.B, self.Hkv, self.S // 16),
                   KVC_EXPORT_WITNESS: (self.B, self.Hkv, self.S, 16), KVC_EXPORT_KTAIL: (self.B, self.Hkv, 16, self.d),
                   KVC_EXPORT_VTAIL: (self.B, self.Hkv, 16, self.d)}

@@ -48,7 +48,7 @@ def check_int8_state(cache, model, requests=None):
                 sK, cK, sV, cV, wit = model.quantized_block(b, h, blk)
                 sl = slice(blk * QBLOCK, (blk + 1) * QBLOCK)
                 assert SK[b, h, blk] == sK and SV[b, h, blk] == sV, (b, h, blk)
-                assert np.array_equal(KQ[b, h, sl], cK) and np.array_equal(VQ[b, h, blk], cV.T), (b, h, blk)
+                assert np.array_equal(KQ[b, h, sl], cK) and np.array_equal(VQ[b, h, sl], cV), (b, h, blk)
                 assert np.array_equal(WT[b, h, sl], wit), (b, h, blk)
             for p in range(nfull, n):
                 assert np.array_equal(KT[b, h, p % QBLOCK], nm.f32_to_bf16(model.hk[b][p][h])), (b, h, p)
