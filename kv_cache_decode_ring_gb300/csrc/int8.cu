@@ -14,9 +14,9 @@
 // fp16 witnesses [S][16], fp32 scales [S/16]; exact bf16 tail [16][d] for the
 // rows of the incomplete block.
 //
-// Kernel shape: CTA = 4 warps = a split of 256 tokens (16 blocks); each warp
-// streams its 4 blocks through two shared-memory stages (codes and witnesses by
-// bulk copy on the stage's mbarrier), so copies overlap arithmetic; online
+// Kernel shape: CTA = 4 warps = a split of 1024 tokens (64 blocks); each warp
+// streams its 16 blocks through three shared-memory stages (codes and witnesses
+// by bulk copy on the stage's mbarrier), so copies overlap arithmetic; online
 // softmax over the warp's blocks, warps merged at the end.  One extra split
 // handles the exact tail rows (c_t = 0 there).
 //
@@ -32,7 +32,10 @@
 //  * P.V, transposed: O^T[d][cols] += V^T[d][16] . P^T[16][cols], P = the block's
 //    softmax weights times s_V / (the warp's largest s_V), again as fp16 hi + lo.
 //    Lane L accumulates the output of the same head L%4, so the online-softmax
-//    rescale is local to the lane.
+//    rescale is local to the lane.  The reference maximum moves only when a
+//    block exceeds it by more than 2^8 (log2 domain), so weights stay <= 2^8 and
+//    the accumulators are rescaled rarely; the weights carry a 2^7 scale, which
+//    keeps them normal fp16 numbers below 2^15.
 // The bound is evaluated in fp32 from the fp32 query with every operation
 // rounded toward +inf (band norms, products with the witnesses, their sums, an
 // upward 1/sqrt(d)); tanh gets two ulps of headroom over CUDA tanhf's documented
@@ -46,8 +49,11 @@ namespace kvc {
 namespace {
 
 constexpr int kWarps = 4;
-constexpr int kTilesPerWarp = 4;           // one 16-token block per tile
+constexpr int kTilesPerWarp = 16;          // one 16-token block per tile
+constexpr int kStages = 3;                 // per warp
+constexpr float kLazyMax = 8.f;            // log2-domain headroom of the reference maximum
 static_assert(kWarps * kTilesPerWarp * kQBlock == kInt8Split, "split shape");
+static_assert(kTilesPerWarp <= 32, "one tile's scales per lane");
 
 struct Int8Args {
     const void* q;
@@ -104,6 +110,13 @@ __device__ __forceinline__ void codes_to_half2(uint32_t u, uint32_t& lo, uint32_
     hi = *reinterpret_cast<const uint32_t*>(&b);
 }
 
+// 2^x with the hardware approximation (relative error about 2^-22; 2^-inf = 0)
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // x = hi + lo with hi = fp16(x) and lo = fp16(x - hi)
 __device__ __forceinline__ void split_half(float x, __half& hi, __half& lo) {
     hi = __float2half_rn(x);
@@ -120,7 +133,7 @@ struct I8 {
     static constexpr int CB = kQBlock * D;          // bytes of one block's codes (K or V)
     static constexpr int WB = kQBlock * kBands * 2;
     static constexpr int STAGEB = 2 * CB + WB;
-    static constexpr int WARPB = 2 * STAGEB;
+    static constexpr int WARPB = kStages * STAGEB;
     static constexpr int PARTF = G * (D + 3);       // floats of one warp's partial (m, l, c, acc)
     static_assert(PARTF * 4 <= WARPB, "partial must fit in the warp's stages");
     // P^T staging per warp and column tile: 8 rows of 16 fp16 tokens; row n at
@@ -129,27 +142,27 @@ struct I8 {
     static constexpr int PROWB = 288;
     // after the warps' stages: P^T staging [warp][NT] (the fp32 query during
     // preparation), fp16 query [2G][D], band norms [G][20], score factors [G],
-    // barriers [warp][2]
+    // barriers [warp][kStages]
     static constexpr int OFF_P = kWarps * WARPB;
     static constexpr int PBYTES = (kWarps * NT * PROWB > G * D * 4 ? kWarps * NT * PROWB : G * D * 4);
     static constexpr int OFF_QH = OFF_P + ((PBYTES + 15) / 16) * 16;
     static constexpr int OFF_NQ = OFF_QH + 2 * G * D * 2;
     static constexpr int OFF_F = OFF_NQ + G * 20 * 4;       // norms padded to 20 floats a head
     static constexpr int OFF_BAR = OFF_F + ((G * 4 + 15) / 16) * 16;
-    static constexpr size_t SMEM = OFF_BAR + kWarps * 2 * 8 + 128;
+    static constexpr size_t SMEM = OFF_BAR + kWarps * kStages * 8 + 128;
 };
 
 __device__ __forceinline__ int prow(int n) { return 32 * n + (n >= 4 ? 16 : 0); }
 
 template <int D, int G>
-__global__ void __launch_bounds__(kWarps * 32, G >= 8 ? (D >= 128 ? 3 : 4) : 4) int8_decode_kernel(const Int8Args a) {
+__global__ void __launch_bounds__(kWarps * 32, D >= 128 ? 3 : 4) int8_decode_kernel(const Int8Args a) {
     using C = I8<D, G>;
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char* sPm = smem + C::OFF_P;                                // [warp][NT] P^T staging
     __half* sQh = reinterpret_cast<__half*>(smem + C::OFF_QH);          // [2G][D]: row 2h hi, 2h + 1 lo
     float* sNQ = reinterpret_cast<float*>(smem + C::OFF_NQ);            // [G][20] band norms
     float* sF = reinterpret_cast<float*>(smem + C::OFF_F);              // [G] score factors
-    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);     // [warp][2]
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);     // [warp][kStages]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.z, kvh = blockIdx.y, split = blockIdx.x;
@@ -216,31 +229,32 @@ __global__ void __launch_bounds__(kWarps * 32, G >= 8 ? (D >= 128 ? 3 : 4) : 4) 
     const size_t bh = (size_t)b * a.Hkv + kvh;
     const size_t row0 = bh * a.S;
     unsigned char* myS = smem + warp * C::WARPB;
-    uint64_t* myBar = bar + warp * 2;
+    uint64_t* myBar = bar + warp * kStages;
     // block of this warp's tile i (tiles of the 4 warps interleaved)
     auto tile_blk = [&](int i) { return (split * kInt8Split) / kQBlock + i * kWarps + warp; };
     auto tile_ok = [&](int i) { return (tile_blk(i) + 1) * kQBlock <= nfull; };
     auto issue = [&](int i) {
         if (lane == 0 && tile_ok(i)) {
             const size_t p0 = (size_t)tile_blk(i) * kQBlock;
-            unsigned char* st = myS + (i & 1) * C::STAGEB;
-            mbar_arrive_expect_tx(&myBar[i & 1], (uint32_t)C::STAGEB);
-            bulk_copy_g2s(st, a.kq + (row0 + p0) * D, C::CB, &myBar[i & 1]);
-            bulk_copy_g2s(st + C::CB, a.vq + (row0 + p0) * D, C::CB, &myBar[i & 1]);
-            bulk_copy_g2s(st + 2 * C::CB, a.wit + (row0 + p0) * kBands, C::WB, &myBar[i & 1]);
+            const int sg = i % kStages;
+            unsigned char* st = myS + sg * C::STAGEB;
+            mbar_arrive_expect_tx(&myBar[sg], (uint32_t)C::STAGEB);
+            bulk_copy_g2s(st, a.kq + (row0 + p0) * D, C::CB, &myBar[sg]);
+            bulk_copy_g2s(st + C::CB, a.vq + (row0 + p0) * D, C::CB, &myBar[sg]);
+            bulk_copy_g2s(st + 2 * C::CB, a.wit + (row0 + p0) * kBands, C::WB, &myBar[sg]);
         }
     };
     if (lane == 0) {
-        mbar_init(&myBar[0], 1);
-        mbar_init(&myBar[1], 1);
+#pragma unroll
+        for (int sg = 0; sg < kStages; ++sg) mbar_init(&myBar[sg], 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncwarp();
-    issue(0);
-    issue(1);
+#pragma unroll
+    for (int i = 0; i < kStages; ++i) issue(i);
 
-    // block scales of this warp's tiles: lane i < 4 holds tile i's s_K and its s_V
-    // relative to the warp's largest s_V, times 2^15 (keeps the fp16 weights normal)
+    // block scales of this warp's tiles: lane i < 16 holds tile i's s_K and its s_V
+    // relative to the warp's largest s_V, times 2^7
     float skv = 0.f, rvv = 0.f;
     if (lane < kTilesPerWarp && tile_ok(lane)) {
         skv = a.sk[bh * (a.S / kQBlock) + tile_blk(lane)];
@@ -249,7 +263,7 @@ __global__ void __launch_bounds__(kWarps * 32, G >= 8 ? (D >= 128 ? 3 : 4) : 4) 
     float svmax = rvv;
 #pragma unroll
     for (int o = 16; o; o >>= 1) svmax = fmaxf(svmax, __shfl_xor_sync(0xffffffffu, svmax, o));
-    rvv = svmax > 0.f ? rvv / svmax * 32768.f : 0.f;
+    rvv = svmax > 0.f ? rvv / svmax * 128.f : 0.f;
 
     // ---- query preparation, once per CTA while the copies fly: rotated fp32
     // query; per head a power-of-two scale 2^e putting max|q| in [2^14, 2^15),
@@ -326,16 +340,19 @@ __global__ void __launch_bounds__(kWarps * 32, G >= 8 ? (D >= 128 ? 3 : 4) : 4) 
 
     for (int i = 0; i < kTilesPerWarp; ++i) {
         if (!tile_ok(i)) break;                   // later tiles of this warp are empty too
-        const unsigned char* tK = myS + (i & 1) * C::STAGEB;
+        const int sg = i % kStages;
+        const uint32_t par = (uint32_t)((i / kStages) & 1);
+        const unsigned char* tK = myS + sg * C::STAGEB;
         const unsigned char* tV = tK + C::CB;
         const uint4* tW = reinterpret_cast<const uint4*>(tK + 2 * C::CB);
         const int p0 = tile_blk(i) * kQBlock;
-        if (!mbar_wait(&myBar[i & 1], (uint32_t)((i >> 1) & 1))) {
-            // give up: flag it, and let this stage's copy and the other stage's
+        if (!mbar_wait(&myBar[sg], par)) {
+            // give up: flag it, and let this stage's copy and the later stages'
             // (if issued) land before the stages are reused for the partial
             if (lane == 0) atomicOr(a.hdr, kErrWait);
-            mbar_wait(&myBar[i & 1], (uint32_t)((i >> 1) & 1));
-            if (i + 1 < kTilesPerWarp && tile_ok(i + 1)) mbar_wait(&myBar[(i + 1) & 1], (uint32_t)(((i + 1) >> 1) & 1));
+            mbar_wait(&myBar[sg], par);
+            for (int j = i + 1; j < i + kStages && j < kTilesPerWarp; ++j)
+                if (tile_ok(j)) mbar_wait(&myBar[j % kStages], (uint32_t)((j / kStages) & 1));
             break;
         }
         const float s_k = __shfl_sync(0xffffffffu, skv, i);
@@ -379,11 +396,11 @@ __global__ void __launch_bounds__(kWarps * 32, G >= 8 ? (D >= 128 ? 3 : 4) : 4) 
             bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
             bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
             bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
-            const float mn = fmaxf(m_w[nt], bm);
-            alpha[nt] = exp2f(m_w[nt] - mn);          // 0 while the maximum was -inf
+            const float mn = bm > m_w[nt] + kLazyMax ? bm : m_w[nt];
+            alpha[nt] = ex2(m_w[nt] - mn);            // 0 while the maximum was -inf
             rescale |= alpha[nt] != 1.f;
             m_w[nt] = mn;
-            const float e0 = exp2f(s0 - mn), e1 = exp2f(s1 - mn);
+            const float e0 = ex2(s0 - mn), e1 = ex2(s1 - mn);
             l_w[nt] = fmaf(l_w[nt], alpha[nt], e0 + e1);
             __half h0, l0, h1, l1;
             split_half(e0 * r_v, h0, l0);
@@ -418,7 +435,7 @@ __global__ void __launch_bounds__(kWarps * 32, G >= 8 ? (D >= 128 ? 3 : 4) : 4) 
                 a.ct[(rowq0 + hq) * a.S + p0 + g + 8] = cb[1];
             }
         }
-        if (__any_sync(0xffffffffu, rescale)) {
+        if (__any_sync(0xffffffffu, rescale) && i > 0) {     // at i = 0 the accumulators are 0
 #pragma unroll
             for (int mt = 0; mt < C::KS; ++mt)
 #pragma unroll
@@ -452,14 +469,14 @@ __global__ void __launch_bounds__(kWarps * 32, G >= 8 ? (D >= 128 ? 3 : 4) : 4) 
         // this stage and the staging are free once every lane is past its reads
         __syncwarp();
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        if (i + 2 < kTilesPerWarp) issue(i + 2);
+        if (i + kStages < kTilesPerWarp) issue(i + kStages);
     }
 
     // ---- this warp's partial into its stage buffers (all issued copies were awaited):
     // l and the bound's maximum over the 8 lanes of a head; output = (hi + lo) columns
     __syncwarp();
     float* part_w = reinterpret_cast<float*>(myS);             // [G][3 + D]
-    const float oscale = svmax * (1.f / 32768.f);
+    const float oscale = svmax * (1.f / 128.f);
 #pragma unroll
     for (int nt = 0; nt < C::HPL; ++nt) {
         float l = l_w[nt], c = c_w[nt];

@@ -18,7 +18,7 @@ constexpr int kQBlock = 16;           // tokens per INT8 quantization block
 constexpr int kBands = 16;            // witness bands per key row
 constexpr int kGenericSplit = 64;     // keys per split, generic decode kernel
 constexpr int kFastSplit = 128;       // keys per split, bf16 fast decode kernel
-constexpr int kInt8Split = 256;       // keys per quantized split, INT8 decode kernel
+constexpr int kInt8Split = 1024;      // keys per quantized split, INT8 decode kernel
 constexpr int kGqaSplit = 256;        // keys per split, bf16 decode kernel for 4 or 8 heads per KV head
 constexpr uint32_t kErrPosition = 1u; // device error bits (sticky, cleared by kvc_device_status)
 constexpr uint32_t kErrWait = 2u;
