@@ -1,6 +1,8 @@
-// async_copy.h -- inline-PTX helpers for bulk global->shared copies that
-// complete on an mbarrier, and bounded waits on those barriers.
+// async_copy.h -- inline-PTX helpers for bulk and tiled-tensor global->shared
+// copies that complete on an mbarrier, and bounded waits on those barriers.
 #pragma once
+
+#include <cuda.h>
 
 #include <cstdint>
 
@@ -41,6 +43,22 @@ __device__ __forceinline__ uint64_t global_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
+}
+
+// Tiled tensor copies (cp.async.bulk.tensor) into shared memory, completing on
+// the mbarrier; c0 is the innermost coordinate.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, int c0, int c1, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* tm, int c0, int c1, int c2, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+        : "memory");
 }
 
 // Bounded wait for phase `parity` of an mbarrier: about one second at most.

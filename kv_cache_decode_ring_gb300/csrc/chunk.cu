@@ -62,21 +62,7 @@ struct ChunkArgs {
     float scale_log2;
 };
 
-// ---- tcgen05 / TMA wrappers -------------------------------------------------
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, int c0, int c1, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
-        : "memory");
-}
-
-__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* tm, int c0, int c1, int c2, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
-        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
-        : "memory");
-}
-
+// ---- tcgen05 wrappers -------------------------------------------------------
 // Shared-memory matrix descriptor, 128-byte swizzle, sm_100 format:
 // start address >> 4 (bits 0-13), leading-dimension byte offset >> 4 (16-29),
 // stride-dimension byte offset >> 4 (32-45), version 1 (46-47), layout 2 =
@@ -421,8 +407,10 @@ EncodeTiled encoder() {
     return fn;
 }
 
-bool make_map(CUtensorMap* tm, void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
-              const cuuint32_t* box) {
+}  // namespace
+
+bool make_tensor_map_bf16(CUtensorMap* tm, void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+                          const cuuint32_t* box) {
     EncodeTiled enc = encoder();
     if (!enc) return false;
     cuuint32_t es[3] = {1, 1, 1};
@@ -430,8 +418,6 @@ bool make_map(CUtensorMap* tm, void* base, int rank, const cuuint64_t* dims, con
                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
            CUDA_SUCCESS;
 }
-
-}  // namespace
 
 bool chunk_supported(const Shape& s) { return s.bf16 && !s.int8 && !s.ring && s.d == kD; }
 
@@ -453,9 +439,9 @@ cudaError_t launch_chunk(kvc_handle* h, const void* q, void* out, int n, cudaStr
     const cuuint64_t kdims[2] = {(cuuint64_t)s.d, (cuuint64_t)s.B * s.Hkv * s.S};
     const cuuint64_t kstr[1] = {(cuuint64_t)s.d * 2};
     const cuuint32_t kbox[2] = {64, kBN};
-    if (!make_map(&tq, qr, 3, qdims, qstr, qbox) || !make_map(&tql, qlo, 3, qdims, qstr, qbox) ||
-        !make_map(&tk, h->state + h->L.k, 2, kdims, kstr, kbox) ||
-        !make_map(&tv, h->state + h->L.v, 2, kdims, kstr, kbox))
+    if (!make_tensor_map_bf16(&tq, qr, 3, qdims, qstr, qbox) || !make_tensor_map_bf16(&tql, qlo, 3, qdims, qstr, qbox) ||
+        !make_tensor_map_bf16(&tk, h->state + h->L.k, 2, kdims, kstr, kbox) ||
+        !make_tensor_map_bf16(&tv, h->state + h->L.v, 2, kdims, kstr, kbox))
         return cudaErrorInvalidValue;
     static bool attr = false;
     if (!attr) {

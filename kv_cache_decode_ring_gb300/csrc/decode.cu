@@ -112,9 +112,10 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineArgs c) 
 
 }  // namespace
 
-cudaError_t launch_decode(const DecodeArgs& a, const CombineArgs& c, bool fast, cudaStream_t st) {
+cudaError_t launch_decode(const DecodeArgs& a, const CombineArgs& c, bool fast, const KvMaps* maps, cudaStream_t st) {
     if (a.split == kGqaSplit && gqa_decode_supported(a.d, a.g)) {
-        cudaError_t e = launch_decode_gqa(a, st);
+        if (!maps) return cudaErrorInvalidValue;
+        cudaError_t e = launch_decode_gqa(a, *maps, st);
         if (e != cudaSuccess) return e;
     } else if (fast) {
         cudaError_t e = launch_decode_fast(a, st);

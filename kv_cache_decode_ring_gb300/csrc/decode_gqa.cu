@@ -4,19 +4,24 @@
 // Same mathematics as decode.cu ([LOOP] §三 step; [LEAN] §2.1 window mask), with
 // the per-split partials (m, l, acc) merged by the combine kernel.
 //
-// With g query heads on every K/V byte the arithmetic per byte is 4g/2 FMAs, so
-// the kernel must keep HBM busy while it computes.  A warp therefore streams its
-// keys through two shared-memory stages of 16 keys (K and V rows contiguous in
-// the cache, one cp.async.bulk each, completing on the stage's mbarrier): while
-// it computes one tile the next is in flight.  The warp keeps an online softmax
-// (running maximum, sum and rescaled accumulators) over its tiles; the CTA's 4
-// warps merge at the end of the 256-key split.
-//  * scores: lane = (run of 16-byte chunks of the row, key group); partial dot
-//    products for all g heads in packed fp32 FMAs, reduce-scatter across the
-//    lanes of a row;
-//  * P.V: lane = 8 output dims of every head, packed fp32 FMAs;
-//  * the rotated, scaled query is prepared once per CTA in shared memory, after
-//    the first copies are already in flight.
+// CTA = 4 warps = a split of 512 keys.  A warp streams its 8 tiles of 16 keys
+// through three shared-memory stages: a tile is d/64 tensor copies of 64 dims x
+// 16 rows from K and as many from V, written with the 128-byte swizzle (16-byte
+// chunk c of row r at c ^ (r mod 8)), so the 8 row addresses of an ldmatrix fall
+// into 8 different bank groups.  Rows past the window's last key are copied too
+// (the cache is zero-initialised, so they are finite) and their scores masked.
+// Both contractions run on the tensor cores (mma m16n8k16, bf16 operands, fp32
+// accumulation), operands loaded straight from the stage with ldmatrix:
+//  * scores, transposed: S^T[16 keys][cols] = K[16][d] . Q^T[d][cols], where the
+//    columns are (head, hi) and (head, lo): the rotated query times
+//    log2(e)/sqrt(d), split into two bf16 parts (about 16 significant bits).
+//    Lane L receives the whole scores of head L%4 (and 4 + L%4) for keys L/4 and
+//    L/4 + 8;
+//  * P.V, transposed: O^T[d][cols] += V^T[d][16] . P^T[16][cols] (V^T by
+//    ldmatrix.trans), P as bf16 hi + lo.  Lane L accumulates the same heads it
+//    scored, so the online-softmax rescale is local to the lane.
+// The reference maximum moves only when a tile exceeds it by more than 2^8 (log2
+// domain), so weights stay <= 2^8 and the accumulators are rarely rescaled.
 // Every mbarrier wait is bounded (about 1 s); on expiry the device error word is
 // set and the split's arithmetic is skipped.
 #include "async_copy.h"
@@ -27,41 +32,76 @@ namespace {
 
 constexpr int kWarps = 4;
 constexpr int kTileKeys = 16;                            // keys per stage
-constexpr int kTilesPerWarp = 4;
-constexpr int kSplit = kWarps * kTilesPerWarp * kTileKeys;   // 256 keys per CTA
+constexpr int kTilesPerWarp = 8;
+constexpr int kStages = 3;                               // per warp
+constexpr float kLazyMax = 8.f;                          // log2-domain headroom of the reference maximum
+constexpr int kSplit = kWarps * kTilesPerWarp * kTileKeys;   // 512 keys per CTA
 static_assert(kSplit == kGqaSplit, "split shape");
+
+// 2^x with the hardware approximation (relative error about 2^-22; 2^-inf = 0)
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// D (16x8, fp32) += A (16x16, bf16, row) . B (16x8, bf16, col)
+__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
+}
+
+// x = hi + lo with hi = bf16(x) and lo = bf16(x - hi)
+__device__ __forceinline__ void split_bf16(float x, __nv_bfloat16& hi, __nv_bfloat16& lo) {
+    hi = __float2bfloat16_rn(x);
+    lo = __float2bfloat16_rn(x - __bfloat162float(hi));
+}
 
 template <int D, int G>
 struct GqaCfg {
-    static constexpr int QD = G <= 4 ? 16 : 8;           // score dims per lane
-    static constexpr int LPR = D / QD;                   // score lanes per row
-    static constexpr int RPP = 32 / LPR;                 // key groups per warp
-    static constexpr int KPG = kTileKeys / RPP;          // keys per group per tile
-    static constexpr int KB0 = 2 * LPR / G;
-    static constexpr int KB = KB0 < KPG ? (KB0 < 1 ? 1 : KB0) : KPG;
-    static constexpr int M = KB * G;
-    static constexpr int OUT = M / LPR;
-    static constexpr int LPR2 = D / 8;                   // P.V lanes per row
-    static constexpr int RPP2 = 32 / LPR2;
-    static constexpr int ROWB = D * 2;
-    static constexpr int HALF = kTileKeys * ROWB;        // K (or V) rows of one stage
+    static constexpr int KS = D / 16;                    // k-steps of the scores = m-tiles of P.V
+    static constexpr int NT = (2 * G + 7) / 8;           // 8-column tiles of (head, hi|lo) columns
+    static constexpr int NBOX = D / 64;                  // tensor-copy boxes per 16-row tile
+    static constexpr int BOXB = kTileKeys * 128;         // bytes of one box (16 rows of 64 bf16)
+    static constexpr int HALF = NBOX * BOXB;             // K (or V) rows of one stage
     static constexpr int STAGEB = 2 * HALF;
-    static constexpr int WARPB = 2 * STAGEB;             // two stages
+    static constexpr int WARPB = kStages * STAGEB;
     static constexpr int PARTB = G * (D + 2) * 4;
-    static_assert(KPG >= 1 && M % LPR == 0 && OUT >= 1, "batch shape");
     static_assert(PARTB <= WARPB, "partial must fit in the warp's stages");
-    static constexpr int OFF_P = kWarps * WARPB;                          // scores [warp][16][G]
-    static constexpr int OFF_Q = OFF_P + kWarps * kTileKeys * G * 4;      // query [G][D]
-    static constexpr int OFF_BAR = OFF_Q + G * D * 4;                     // [warp][stage]
-    static constexpr size_t SMEM = OFF_BAR + kWarps * 2 * 8 + 128;
+    // P^T staging per warp and column tile: 8 rows (columns) of 16 keys, bf16, 48-byte
+    // stride (the lanes' 2-byte stores and 4-byte fragment loads are conflict-free)
+    static constexpr int PRSTR = 48;
+    static constexpr int PTILE = 8 * PRSTR;
+    static constexpr int OFF_P = kWarps * WARPB;                          // [warp][NT] P^T staging
+    static constexpr int PBYTES = kWarps * NT * PTILE > G * D * 4 ? kWarps * NT * PTILE : G * D * 4;
+    static constexpr int OFF_Q = OFF_P + ((PBYTES + 15) / 16) * 16;      // bf16 query [2G][D]
+    static constexpr int OFF_BAR = OFF_Q + 2 * G * D * 2;                 // [warp][stage]
+    static constexpr size_t SMEM = OFF_BAR + kWarps * kStages * 8 + 1024;   // + base alignment
+    static_assert(HALF % 1024 == 0 && OFF_P % 1024 == 0, "swizzled boxes need 1024-byte alignment");
 };
 
 template <int D, int G>
-__global__ void __launch_bounds__(kWarps * 32, 3) decode_gqa_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(kWarps * 32, 2)
+    decode_gqa_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                      const DecodeArgs a) {
     using C = GqaCfg<D, G>;
-    extern __shared__ __align__(128) unsigned char smem[];
-    float* sP = reinterpret_cast<float*>(smem + C::OFF_P);
-    float* sQ = reinterpret_cast<float*>(smem + C::OFF_Q);
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    unsigned char* sPm = smem + C::OFF_P;
+    __nv_bfloat16* sQb = reinterpret_cast<__nv_bfloat16*>(smem + C::OFF_Q);   // row 2h hi, 2h + 1 lo
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -72,35 +112,39 @@ __global__ void __launch_bounds__(kWarps * 32, 3) decode_gqa_kernel(const Decode
     const int nsplit = (hi - lo + kSplit - 1) / kSplit;
     if (split >= nsplit) return;
 
-    const size_t head_row0 = ((size_t)b * a.Hkv + kvh) * a.S;
-    const __nv_bfloat16* Kg = static_cast<const __nv_bfloat16*>(a.k);
-    const __nv_bfloat16* Vg = static_cast<const __nv_bfloat16*>(a.v);
+    const int head_row0 = (b * a.Hkv + kvh) * a.S;       // tensor-map row of key slot 0
     unsigned char* myS = smem + warp * C::WARPB;
-    uint64_t* myBar = bar + warp * 2;
+    uint64_t* myBar = bar + warp * kStages;
     // keys of this warp's tile i: 16 consecutive rows, tiles of the 4 warps interleaved
     auto tile_k0 = [&](int i) { return lo + split * kSplit + (i * kWarps + warp) * kTileKeys; };
     auto tile_nk = [&](int i) { return max(0, min(kTileKeys, hi - tile_k0(i))); };
+    // lane 0: the tile's K and V boxes (always 16 full rows) on the stage's barrier
     auto issue = [&](int i) {
-        const int k0 = tile_k0(i), nk = tile_nk(i);
-        if (lane == 0 && nk > 0) {
-            unsigned char* st = myS + (i & 1) * C::STAGEB;
-            const uint32_t bytes = (uint32_t)nk * C::ROWB;
-            mbar_arrive_expect_tx(&myBar[i & 1], 2 * bytes);
-            bulk_copy_g2s(st, Kg + (head_row0 + k0) * D, bytes, &myBar[i & 1]);
-            bulk_copy_g2s(st + C::HALF, Vg + (head_row0 + k0) * D, bytes, &myBar[i & 1]);
+        if (lane == 0 && tile_nk(i) > 0) {
+            const int sg = i % kStages;
+            unsigned char* st = myS + sg * C::STAGEB;
+            const int row = head_row0 + tile_k0(i);
+            mbar_arrive_expect_tx(&myBar[sg], (uint32_t)C::STAGEB);
+#pragma unroll
+            for (int j = 0; j < C::NBOX; ++j) {
+                tma_load_2d(st + j * C::BOXB, &tmK, 64 * j, row, &myBar[sg]);
+                tma_load_2d(st + C::HALF + j * C::BOXB, &tmV, 64 * j, row, &myBar[sg]);
+            }
         }
     };
     if (lane == 0) {
-        mbar_init(&myBar[0], 1);
-        mbar_init(&myBar[1], 1);
+#pragma unroll
+        for (int sg = 0; sg < kStages; ++sg) mbar_init(&myBar[sg], 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncwarp();
-    issue(0);
-    issue(1);
+#pragma unroll
+    for (int i = 0; i < kStages; ++i) issue(i);
 
-    // the query of the G heads, rotated at t = len - 1, times log2(e)/sqrt(d)
+    // the query of the G heads, rotated at t = len - 1, times log2(e)/sqrt(d), as
+    // bf16 hi + lo rows (fp32 staging in the P area meanwhile)
     {
+        float* qf = reinterpret_cast<float*>(sPm);
         const int t = len - 1;
         for (int idx = threadIdx.x; idx < G * D / 2; idx += blockDim.x) {
             const int h = idx / (D / 2), i = idx % (D / 2);
@@ -108,153 +152,154 @@ __global__ void __launch_bounds__(kWarps * 32, 3) decode_gqa_kernel(const Decode
             const float x0 = ld_elem(a.q, off, 1), x1 = ld_elem(a.q, off + 1, 1);
             float y0 = x0, y1 = x1;
             if (a.rope) rope_pair(x0, x1, a.rope[(size_t)t * (D / 2) + i], y0, y1);
-            sQ[h * D + 2 * i] = y0 * a.scale_log2;
-            sQ[h * D + 2 * i + 1] = y1 * a.scale_log2;
+            qf[h * D + 2 * i] = y0 * a.scale_log2;
+            qf[h * D + 2 * i + 1] = y1 * a.scale_log2;
         }
+        __syncthreads();
+        for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
+            const int h = idx / D, i = idx % D;
+            __nv_bfloat16 qh, ql;
+            split_bf16(qf[idx], qh, ql);
+            sQb[(2 * h) * D + i] = qh;
+            sQb[(2 * h + 1) * D + i] = ql;
+        }
+        __syncthreads();
     }
-    __syncthreads();
-    const int r = lane % C::LPR, grp = lane / C::LPR;
-    const int r2 = lane % C::LPR2, grp2 = lane / C::LPR2;
-    float q[G][C::QD];
-#pragma unroll
-    for (int h = 0; h < G; ++h)
-#pragma unroll
-        for (int e = 0; e < C::QD; e += 4) {
-            const int dim = (r + (e / 8) * C::LPR) * 8 + (e % 8);
-            const float4 f = *reinterpret_cast<const float4*>(sQ + h * D + dim);
-            q[h][e] = f.x; q[h][e + 1] = f.y; q[h][e + 2] = f.z; q[h][e + 3] = f.w;
-        }
 
-    float* myP = sP + warp * kTileKeys * G;
-    float m_w[G], l_w[G], acc[G][8];
+    // ---- per-lane fragments: g = L/4 (MMA group), qd = L%4
+    const int g = lane >> 2, qd = lane & 3;
+    uint32_t qb[C::NT][C::KS][2];                 // Q^T operand: column 8 nt + g, k-step s
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-        m_w[h] = -INFINITY; l_w[h] = 0.f;
+    for (int nt = 0; nt < C::NT; ++nt)
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[h][e] = 0.f;
-    }
-    bool ok = true;
-    for (int i = 0; i < kTilesPerWarp && ok; ++i) {
+        for (int s = 0; s < C::KS; ++s) {
+            const __nv_bfloat16* row = sQb + (8 * nt + g) * D + 16 * s + 2 * qd;
+            qb[nt][s][0] = *reinterpret_cast<const uint32_t*>(row);
+            qb[nt][s][1] = *reinterpret_cast<const uint32_t*>(row + 8);
+        }
+    // ldmatrix row addresses: matrix mi = lane / 8 supplies row rr = lane % 8 (+ 8);
+    // 16-byte chunk c of a row sits at c ^ rr
+    const int mi = lane >> 3, rr = lane & 7;
+    const uint32_t krow = (uint32_t)((rr + 8 * (mi & 1)) * 128), kch = (uint32_t)(mi >> 1);
+    const uint32_t vrow = (uint32_t)((rr + 8 * (mi >> 1)) * 128), vch = (uint32_t)(mi & 1);
+    unsigned char* myPm = sPm + warp * C::NT * C::PTILE;
+
+    float m_w[C::NT], l_w[C::NT];
+    float acc[C::KS][C::NT][4];
+#pragma unroll
+    for (int nt = 0; nt < C::NT; ++nt) { m_w[nt] = -INFINITY; l_w[nt] = 0.f; }
+#pragma unroll
+    for (int mt = 0; mt < C::KS; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < C::NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[mt][nt][e] = 0.f;
+
+    for (int i = 0; i < kTilesPerWarp; ++i) {
         const int nk = tile_nk(i);
         if (nk == 0) break;                       // later tiles of this warp are empty too
-        const unsigned char* tK = myS + (i & 1) * C::STAGEB;
-        const unsigned char* tV = tK + C::HALF;
-        ok = mbar_wait(&myBar[i & 1], (uint32_t)((i >> 1) & 1));
-        if (!ok) {
+        const int sg = i % kStages;
+        const uint32_t par = (uint32_t)((i / kStages) & 1);
+        unsigned char* tK = myS + sg * C::STAGEB;
+        unsigned char* tV = tK + C::HALF;
+        if (!mbar_wait(&myBar[sg], par)) {
+            // give up: flag it, and let this stage's copy and the later stages'
+            // (if issued) land before the stages are reused for the partial
             if (lane == 0) atomicOr(a.hdr, kErrWait);
-            mbar_wait(&myBar[i & 1], (uint32_t)((i >> 1) & 1));
+            mbar_wait(&myBar[sg], par);
+            for (int j = i + 1; j < i + kStages && j < kTilesPerWarp; ++j)
+                if (tile_nk(j) > 0) mbar_wait(&myBar[j % kStages], (uint32_t)((j / kStages) & 1));
             break;
         }
-        // ---- scores of the tile
+        // ---- scores S^T = K Q^T
+        const uint32_t kbase = smem_u32(tK) + krow;
+        float sacc[C::NT][4];
 #pragma unroll
-        for (int kb = 0; kb < C::KPG; kb += C::KB) {
-            float part[C::M];
+        for (int nt = 0; nt < C::NT; ++nt)
 #pragma unroll
-            for (int k = 0; k < C::KB; ++k) {
-                const int t = grp * C::KPG + kb + k;
-                float x[C::QD];
+            for (int e = 0; e < 4; ++e) sacc[nt][e] = 0.f;
 #pragma unroll
-                for (int e = 0; e < C::QD; e += 8) {
-                    const uint4 u = *reinterpret_cast<const uint4*>(tK + t * C::ROWB + (r + (e / 8) * C::LPR) * 16);
-                    bf16x8_to_f32(u, x + e);
-                }
+        for (int s = 0; s < C::KS; ++s) {
+            uint32_t af[4];
+            ldsm_x4(af, kbase + (s >> 2) * C::BOXB + (((uint32_t)(((s & 3) << 1)) + kch) ^ (uint32_t)rr) * 16);
 #pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    float2 s2 = make_float2(0.f, 0.f);
+            for (int nt = 0; nt < C::NT; ++nt) mma_bf16(sacc[nt], af, qb[nt][s][0], qb[nt][s][1]);
+        }
+        // ---- online softmax of the lane's heads over keys g, g + 8; weights into the
+        // P^T staging as bf16 hi + lo
+        float alpha[C::NT];
+        bool rescale = false;
 #pragma unroll
-                    for (int e = 0; e < C::QD; e += 2)
-                        s2 = __ffma2_rn(make_float2(q[h][e], q[h][e + 1]), make_float2(x[e], x[e + 1]), s2);
-                    part[k * G + h] = s2.x + s2.y;
-                }
-            }
+        for (int nt = 0; nt < C::NT; ++nt) {
+            const float s0 = g < nk ? sacc[nt][0] + sacc[nt][1] : -INFINITY;
+            const float s1 = g + 8 < nk ? sacc[nt][2] + sacc[nt][3] : -INFINITY;
+            float bm = fmaxf(s0, s1);
+            bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
+            bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
+            bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
+            const float mn = bm > m_w[nt] + kLazyMax ? bm : m_w[nt];
+            alpha[nt] = ex2(m_w[nt] - mn);            // 0 while the maximum was -inf
+            rescale |= alpha[nt] != 1.f;
+            m_w[nt] = mn;
+            const float e0 = ex2(s0 - mn), e1 = ex2(s1 - mn);     // masked keys: 0
+            l_w[nt] = fmaf(l_w[nt], alpha[nt], e0 + e1);
+            __nv_bfloat16 h0, l0, h1, l1;
+            split_bf16(e0, h0, l0);
+            split_bf16(e1, h1, l1);
+            unsigned char* pt = myPm + nt * C::PTILE;
+            *reinterpret_cast<__nv_bfloat16*>(pt + (2 * qd) * C::PRSTR + 2 * g) = h0;
+            *reinterpret_cast<__nv_bfloat16*>(pt + (2 * qd + 1) * C::PRSTR + 2 * g) = l0;
+            *reinterpret_cast<__nv_bfloat16*>(pt + (2 * qd) * C::PRSTR + 2 * (g + 8)) = h1;
+            *reinterpret_cast<__nv_bfloat16*>(pt + (2 * qd + 1) * C::PRSTR + 2 * (g + 8)) = l1;
+        }
+        if (__any_sync(0xffffffffu, rescale) && i > 0) {     // at i = 0 the accumulators are 0
 #pragma unroll
-            for (int mask = C::LPR / 2, cnt = C::M; mask >= 1; mask >>= 1, cnt >>= 1) {
-                const bool upper = (r & mask) != 0;
+            for (int mt = 0; mt < C::KS; ++mt)
 #pragma unroll
-                for (int j = 0; j < cnt / 2; ++j) {
-                    const float keep = upper ? part[j + cnt / 2] : part[j];
-                    const float send = upper ? part[j] : part[j + cnt / 2];
-                    part[j] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
-                }
-            }
+                for (int nt = 0; nt < C::NT; ++nt)
 #pragma unroll
-            for (int j = 0; j < C::OUT; ++j) {
-                const int o = r * C::OUT + j;
-                const int t = grp * C::KPG + kb + o / G;
-                myP[t * G + (o % G)] = (t < nk) ? part[j] : -INFINITY;
-            }
+                    for (int e = 0; e < 4; ++e) acc[mt][nt][e] *= alpha[nt];
         }
         __syncwarp();
-        // ---- online softmax, two heads per pass: lane = (key lane & 15, head + lane >> 4)
-        float alpha[G];
+        // ---- P.V: O^T += V^T P^T; B operand = P^T column g, keys 2 qd, +1 and 2 qd + 8, +9
+        uint32_t pb[C::NT][2];
 #pragma unroll
-        for (int h = 0; h < G; h += 2) {
-            const int hh = h + (lane >> 4), t = lane & 15;
-            const float s = myP[t * G + hh];
-            float mx = s;
-#pragma unroll
-            for (int o = 8; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-            const float m_lo = __shfl_sync(0xffffffffu, mx, 0), m_hi = __shfl_sync(0xffffffffu, mx, 16);
-            const float mn0 = fmaxf(m_w[h], m_lo), mn1 = fmaxf(m_w[h + 1], m_hi);
-            const float mn = (lane >> 4) ? mn1 : mn0;
-            const float p = exp2f(s - mn);                // masked keys: 2^-inf = 0
-            myP[t * G + hh] = p;
-            float ls = p;
-#pragma unroll
-            for (int o = 8; o; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
-            const float l_lo = __shfl_sync(0xffffffffu, ls, 0), l_hi = __shfl_sync(0xffffffffu, ls, 16);
-            alpha[h] = exp2f(m_w[h] - mn0);               // 0 while the maximum was -inf
-            alpha[h + 1] = exp2f(m_w[h + 1] - mn1);
-            l_w[h] = l_w[h] * alpha[h] + l_lo;
-            l_w[h + 1] = l_w[h + 1] * alpha[h + 1] + l_hi;
-            m_w[h] = mn0;
-            m_w[h + 1] = mn1;
+        for (int nt = 0; nt < C::NT; ++nt) {
+            const unsigned char* pr = myPm + nt * C::PTILE + g * C::PRSTR + 4 * qd;
+            pb[nt][0] = *reinterpret_cast<const uint32_t*>(pr);
+            pb[nt][1] = *reinterpret_cast<const uint32_t*>(pr + 16);
         }
-        __syncwarp();
-        // ---- P.V, after rescaling the accumulators to the new maxima
+        const uint32_t vbase = smem_u32(tV) + vrow;
 #pragma unroll
-        for (int h = 0; h < G; ++h)
+        for (int mt = 0; mt < C::KS; ++mt) {
+            uint32_t af[4];
+            ldsm_x4_trans(af, vbase + (mt >> 2) * C::BOXB + (((uint32_t)(((mt & 3) << 1)) + vch) ^ (uint32_t)rr) * 16);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) acc[h][e] *= alpha[h];
-        for (int t = grp2; t < nk; t += C::RPP2) {
-            const uint4 u = *reinterpret_cast<const uint4*>(tV + t * C::ROWB + r2 * 16);
-            float x[8];
-            bf16x8_to_f32(u, x);
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-                const float pv = myP[t * G + h];
-                const float2 pp = make_float2(pv, pv);
-#pragma unroll
-                for (int e = 0; e < 8; e += 2) {
-                    const float2 rr = __ffma2_rn(pp, make_float2(x[e], x[e + 1]), make_float2(acc[h][e], acc[h][e + 1]));
-                    acc[h][e] = rr.x;
-                    acc[h][e + 1] = rr.y;
-                }
-            }
+            for (int nt = 0; nt < C::NT; ++nt) mma_bf16(acc[mt][nt], af, pb[nt][0], pb[nt][1]);
         }
-        // this stage is free once every lane is past its reads: refill it
+        // this stage and the staging are free once every lane is past its reads
         __syncwarp();
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        if (i + 2 < kTilesPerWarp) issue(i + 2);
+        if (i + kStages < kTilesPerWarp) issue(i + kStages);
     }
-#pragma unroll
-    for (int mask = C::LPR2; mask < 32; mask <<= 1)
-#pragma unroll
-        for (int h = 0; h < G; ++h)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[h][e] += __shfl_xor_sync(0xffffffffu, acc[h][e], mask);
 
-    // ---- this warp's partial into its own stage buffers (the copies it issued are
-    // complete: every issued tile was waited for, except after a timeout)
+    // ---- this warp's partial into its own stage buffers (every issued tile was
+    // waited for): l summed over the 8 lanes of a head; output = hi + lo columns
     __syncwarp();
     float* part_w = reinterpret_cast<float*>(myS);        // [G][2 + D]
-    if (grp2 == 0) {
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
+    for (int nt = 0; nt < C::NT; ++nt) {
+        float l = l_w[nt];
+        l += __shfl_xor_sync(0xffffffffu, l, 4);
+        l += __shfl_xor_sync(0xffffffffu, l, 8);
+        l += __shfl_xor_sync(0xffffffffu, l, 16);
+        const int h = 4 * nt + qd;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) part_w[h * (D + 2) + 2 + r2 * 8 + e] = acc[h][e];
-            if (r2 == 0) { part_w[h * (D + 2)] = m_w[h]; part_w[h * (D + 2) + 1] = l_w[h]; }
+        for (int mt = 0; mt < C::KS; ++mt) {
+            part_w[h * (D + 2) + 2 + 16 * mt + g] = acc[mt][nt][0] + acc[mt][nt][1];
+            part_w[h * (D + 2) + 2 + 16 * mt + 8 + g] = acc[mt][nt][2] + acc[mt][nt][3];
         }
+        if (g == 0) { part_w[h * (D + 2)] = m_w[nt]; part_w[h * (D + 2) + 1] = l; }
     }
     __syncthreads();
     for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
@@ -278,7 +323,7 @@ __global__ void __launch_bounds__(kWarps * 32, 3) decode_gqa_kernel(const Decode
 }
 
 template <int D, int G>
-cudaError_t launch_t(const DecodeArgs& a, cudaStream_t st) {
+cudaError_t launch_t(const DecodeArgs& a, const KvMaps& m, cudaStream_t st) {
     using C = GqaCfg<D, G>;
     static bool attr = false;
     if (!attr) {
@@ -287,7 +332,7 @@ cudaError_t launch_t(const DecodeArgs& a, cudaStream_t st) {
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    decode_gqa_kernel<D, G><<<dim3(a.max_splits, a.Hkv, a.B), kWarps * 32, C::SMEM, st>>>(a);
+    decode_gqa_kernel<D, G><<<dim3(a.max_splits, a.Hkv, a.B), kWarps * 32, C::SMEM, st>>>(m.k, m.v, a);
     return cudaGetLastError();
 }
 
@@ -295,9 +340,9 @@ cudaError_t launch_t(const DecodeArgs& a, cudaStream_t st) {
 
 bool gqa_decode_supported(int d, int g) { return (d == 64 || d == 128) && (g == 4 || g == 8); }
 
-cudaError_t launch_decode_gqa(const DecodeArgs& a, cudaStream_t st) {
+cudaError_t launch_decode_gqa(const DecodeArgs& a, const KvMaps& m, cudaStream_t st) {
 #define KVC_CASE(D, G) \
-    if (a.d == D && a.g == G) return launch_t<D, G>(a, st);
+    if (a.d == D && a.g == G) return launch_t<D, G>(a, m, st);
     KVC_CASE(128, 4) KVC_CASE(128, 8) KVC_CASE(64, 4) KVC_CASE(64, 8)
 #undef KVC_CASE
     return cudaErrorInvalidValue;

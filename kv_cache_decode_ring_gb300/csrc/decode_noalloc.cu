@@ -88,6 +88,8 @@ extern "C" int kvc_decode_attn_noalloc(kvc_t h, const void* d_q, void* d_out, kv
     c.B = s.B; c.Hq = s.Hq; c.d = s.d; c.S = s.S; c.W = s.W; c.max_splits = s.max_splits;
     c.split = s.split; c.ring = s.ring; c.bf16 = s.out_bf16;
     const bool fast = s.split == kFastSplit && fast_decode_supported(a);
-    if (launch_decode(a, c, fast, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KVC_ERR_CUDA;
+    if (launch_decode(a, c, fast, h->has_kv_maps ? &h->kv_maps : nullptr, static_cast<cudaStream_t>(stream)) !=
+        cudaSuccess)
+        return KVC_ERR_CUDA;
     return KVC_OK;
 }

@@ -55,7 +55,9 @@ bool make_shape(const kvc_config& c, Shape* s) {
     s->out_bf16 = c.out_dtype == 0 ? s->bf16 : c.out_dtype == KVC_BF16 + 1;
     s->split = kGenericSplit;
     if (s->bf16 && !int8 && (s->d == 64 || s->d == 128) && s->g <= 8) s->split = kFastSplit;
-    if (s->bf16 && !int8 && gqa_decode_supported(s->d, s->g)) s->split = kGqaSplit;
+    // (its tensor copies address cache rows with signed 32-bit coordinates)
+    if (s->bf16 && !int8 && gqa_decode_supported(s->d, s->g) && (long long)s->B * s->Hkv * s->S < (1ll << 31))
+        s->split = kGqaSplit;
     const long long keys = (s->W > 0 && s->W < s->S) ? s->W : s->S;
     s->max_splits = (int)((keys + s->split - 1) / s->split);
     if (int8) {
@@ -192,6 +194,19 @@ int kvc_create(const kvc_config* cfg, void* d_state, size_t bytes, kvc_stream_t 
     h->cfg = *cfg; h->sh = s; h->L = L; h->state = static_cast<char*>(d_state); h->bytes = bytes;
     h->np.assign(s.B, 0);
     h->ring_needs_append = false;
+    h->has_kv_maps = false;
+    if (s.split == kGqaSplit) {
+        // the GQA decode reads 16-row tiles of the K and V caches by tensor copy
+        const cuuint64_t dims[2] = {(cuuint64_t)s.d, (cuuint64_t)s.B * s.Hkv * s.S};
+        const cuuint64_t strides[1] = {(cuuint64_t)s.d * 2};
+        const cuuint32_t box[2] = {64, 16};
+        if (!make_tensor_map_bf16(&h->kv_maps.k, h->state + L.k, 2, dims, strides, box) ||
+            !make_tensor_map_bf16(&h->kv_maps.v, h->state + L.v, 2, dims, strides, box)) {
+            delete h;
+            return KVC_ERR_CUDA;
+        }
+        h->has_kv_maps = true;
+    }
     if (cudaGetDevice(&h->device) != cudaSuccess ||
         cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess) {
         delete h;
@@ -280,7 +295,7 @@ int kvc_decode_attn(kvc_t h, const void* d_q, void* d_out, float* d_cmax, float*
     c.B = s.B; c.Hq = s.Hq; c.d = s.d; c.S = s.S; c.W = s.W; c.max_splits = s.max_splits;
     c.split = s.split; c.ring = s.ring; c.bf16 = s.out_bf16;
     const bool fast = s.split == kFastSplit && fast_decode_supported(a);
-    if (launch_decode(a, c, fast, st) != cudaSuccess) return KVC_ERR_CUDA;
+    if (launch_decode(a, c, fast, h->has_kv_maps ? &h->kv_maps : nullptr, st) != cudaSuccess) return KVC_ERR_CUDA;
     if (d_cmax && cudaMemsetAsync(d_cmax, 0, (size_t)s.B * s.Hq * 4, st) != cudaSuccess) return KVC_ERR_CUDA;
     if (d_tanh && cudaMemsetAsync(d_tanh, 0, (size_t)s.B * s.Hq * 4, st) != cudaSuccess) return KVC_ERR_CUDA;
     return KVC_OK;

@@ -2,6 +2,7 @@
 // helpers shared by the libkvc translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -19,7 +20,7 @@ constexpr int kBands = 16;            // witness bands per key row
 constexpr int kGenericSplit = 64;     // keys per split, generic decode kernel
 constexpr int kFastSplit = 128;       // keys per split, bf16 fast decode kernel
 constexpr int kInt8Split = 1024;      // keys per quantized split, INT8 decode kernel
-constexpr int kGqaSplit = 256;        // keys per split, bf16 decode kernel for 4 or 8 heads per KV head
+constexpr int kGqaSplit = 512;        // keys per split, bf16 decode kernel for 4 or 8 heads per KV head
 constexpr uint32_t kErrPosition = 1u; // device error bits (sticky, cleared by kvc_device_status)
 constexpr uint32_t kErrWait = 2u;
 
@@ -95,12 +96,23 @@ struct AppendArgs {
     int B, Hkv, d, S, P, ring, bf16, int8;
 };
 
+// Tensor maps over the whole K and V caches, rows [B*Hkv*S][d] bf16, boxes of 64
+// elements x 16 rows, 128-byte swizzle (the GQA decode's tiles).
+struct KvMaps {
+    CUtensorMap k, v;
+};
+
+// bf16 tensor map with 128-byte swizzle (cuTensorMapEncodeTiled); false on failure
+bool make_tensor_map_bf16(CUtensorMap* tm, void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+                          const cuuint32_t* box);
+
 // ---- launchers (one per translation unit) ----------------------------------
 cudaError_t launch_append_token(const AppendArgs& a, cudaStream_t st);
-cudaError_t launch_decode(const DecodeArgs& d, const CombineArgs& c, bool fast, cudaStream_t st);
+// maps: required when the GQA kernel serves the shape (split == kGqaSplit)
+cudaError_t launch_decode(const DecodeArgs& d, const CombineArgs& c, bool fast, const KvMaps* maps, cudaStream_t st);
 bool chunk_supported(const Shape& s);
 bool gqa_decode_supported(int d, int g);
-cudaError_t launch_decode_gqa(const DecodeArgs& a, cudaStream_t st);
+cudaError_t launch_decode_gqa(const DecodeArgs& a, const KvMaps& maps, cudaStream_t st);
 
 // ---- INT8 code storage --------------------------------------------------------
 // Inside one 16-token block of one (request, KV head) the 16*d code bytes are
@@ -159,4 +171,6 @@ struct kvc_handle {
     std::vector<int32_t> np;      // host mirror of next_position
     bool ring_needs_append;        // a ring was trimmed and has not appended since
     std::vector<int32_t> counts;   // host staging for append_rows counts
+    kvc::KvMaps kv_maps;           // built at create when the GQA decode serves the shape
+    bool has_kv_maps;
 };
