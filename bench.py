@@ -277,6 +277,9 @@ class SlidingWindowBench(DecodeBench):
         from kv_cache_decode_ring_gb300 import kvc
         from kv_cache_decode_ring_gb300 import workloads as wl
         self.w = w = wl.sliding_window_gqa()
+        if batch:
+            w.batch = batch                   # smaller case for profiler captures: the first requests
+            w.extra["lengths"] = w.extra["lengths"][:batch]
         self.W = w.capacity
         self.L = list(w.extra["lengths"])
         maxp = w.extra["max_len"] + total_steps + 64
@@ -320,6 +323,8 @@ class Int8Bench(DecodeBench):
         from kv_cache_decode_ring_gb300 import kvc
         from kv_cache_decode_ring_gb300 import workloads as wl
         self.w = w = wl.int8_witness()
+        if batch:
+            w.batch = batch                   # smaller case for profiler captures
         self.ctx = w.extra["context"]
         w.capacity = self.ctx + 16 * ((total_steps + 16 + 15) // 16)
         self.cache = kvc.Cache.from_workload(w, device=device)

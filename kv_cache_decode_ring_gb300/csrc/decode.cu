@@ -87,9 +87,31 @@ __global__ void __launch_bounds__(kThreads) decode_generic_kernel(const DecodeAr
     }
 }
 
-// Combine: CTA per (query head, request); threads over d.
-__global__ void __launch_bounds__(kThreads) combine_kernel(const CombineArgs c) {
+// Combine: CTA per (query head, request), 8 warps.  The block reduces the
+// split maxima and denominators; then warp w sums splits w, w + 8, ... with lanes
+// over d (enough loads in flight to hide L2 latency), and the warps' sums meet
+// in shared memory.
+constexpr int kCombineWarps = 8;
+
+__device__ __forceinline__ float block_reduce(float v, bool is_max, float* red) {
+    for (int o = 16; o; o >>= 1) {
+        const float w = __shfl_xor_sync(0xffffffffu, v, o);
+        v = is_max ? fmaxf(v, w) : v + w;
+    }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    __syncthreads();                                   // red may still be read by a previous reduction
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    v = red[0];
+    for (int w = 1; w < kCombineWarps; ++w) v = is_max ? fmaxf(v, red[w]) : v + red[w];
+    return v;
+}
+
+__global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const CombineArgs c) {
+    __shared__ float red[kCombineWarps];
+    __shared__ float sacc[kCombineWarps][256];
     const int hq = blockIdx.x, b = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int len = c.next_pos[b];
     int lo, hi;
     key_range(len, c.S, c.W, c.ring, lo, hi);
@@ -97,14 +119,32 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineArgs c) 
     const size_t row = (size_t)b * c.Hq + hq;
     const float2* ml = c.part_ml + row * c.max_splits;
     float mx = -INFINITY;
-    for (int s = 0; s < ns; ++s) mx = fmaxf(mx, ml[s].x);
+    for (int s = threadIdx.x; s < ns; s += blockDim.x) mx = fmaxf(mx, ml[s].x);
+    mx = block_reduce(mx, true, red);
     float L = 0.f;
-    for (int s = 0; s < ns; ++s) L += ml[s].y * exp2f(ml[s].x - mx);
+    for (int s = threadIdx.x; s < ns; s += blockDim.x) L += ml[s].y * exp2f(ml[s].x - mx);
+    L = block_reduce(L, false, red);
+    float acc[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+#pragma unroll 8
+    for (int s = warp; s < ns; s += kCombineWarps) {
+        const float f = exp2f(ml[s].x - mx);
+        const float* pa = c.part_acc + (row * c.max_splits + s) * c.d;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (lane + 32 * j < c.d) acc[j] = fmaf(pa[lane + 32 * j], f, acc[j]);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        if (lane + 32 * j < c.d) sacc[warp][lane + 32 * j] = acc[j];
+    __syncthreads();
     const float inv = L > 0.f ? 1.f / L : 0.f;
     for (int i = threadIdx.x; i < c.d; i += blockDim.x) {
-        float acc = 0.f;
-        for (int s = 0; s < ns; ++s) acc = fmaf(c.part_acc[(row * c.max_splits + s) * c.d + i], exp2f(ml[s].x - mx), acc);
-        const float o = acc * inv;
+        float o = 0.f;
+#pragma unroll
+        for (int w = 0; w < kCombineWarps; ++w) o += sacc[w][i];
+        o *= inv;
         if (c.bf16) static_cast<__nv_bfloat16*>(c.out)[row * c.d + i] = __float2bfloat16_rn(o);
         else static_cast<float*>(c.out)[row * c.d + i] = o;
     }
@@ -128,7 +168,7 @@ cudaError_t launch_decode(const DecodeArgs& a, const CombineArgs& c, bool fast, 
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    combine_kernel<<<dim3(a.Hq, a.B), kThreads, 0, st>>>(c);
+    combine_kernel<<<dim3(a.Hq, a.B), kCombineWarps * 32, 0, st>>>(c);
     return cudaGetLastError();
 }
 

@@ -531,31 +531,68 @@ __device__ __forceinline__ float tanh_up(float x) {
     return fminf(t, 1.f);
 }
 
-__global__ void __launch_bounds__(128) int8_combine_kernel(const Int8CombineArgs c) {
+// Combine: CTA per (query head, request), 8 warps.  The block reduces the split
+// maxima, denominators and bound maxima; then warp w sums splits w, w + 8, ...
+// with lanes over d, and the warps' sums meet in shared memory.
+constexpr int kCombineWarps = 8;
+
+__device__ __forceinline__ float block_reduce(float v, bool is_max, float* red) {
+    for (int o = 16; o; o >>= 1) {
+        const float w = __shfl_xor_sync(0xffffffffu, v, o);
+        v = is_max ? fmaxf(v, w) : v + w;
+    }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    __syncthreads();                                   // red may still be read by a previous reduction
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    v = red[0];
+    for (int w = 1; w < kCombineWarps; ++w) v = is_max ? fmaxf(v, red[w]) : v + red[w];
+    return v;
+}
+
+__global__ void __launch_bounds__(kCombineWarps * 32) int8_combine_kernel(const Int8CombineArgs c) {
+    __shared__ float red[kCombineWarps];
+    __shared__ float sacc[kCombineWarps][128];
     const int hq = blockIdx.x, b = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int len = c.next_pos[b];
     const int nfull = len & ~(kQBlock - 1);
+    // quantized splits at 0 .. nsq - 1, the exact tail split (if any) at nsq
     const int ns = (nfull + kInt8Split - 1) / kInt8Split + (len > nfull ? 1 : 0);
-    const int nsq = (nfull + kInt8Split - 1) / kInt8Split;
     const size_t row = (size_t)b * c.Hq + hq;
-    // the tail split sits at index nsq; the quantized ones at 0..nsq-1
+    const float2* ml = c.part_ml + row * c.max_splits;
+    const float* pc = c.part_c + row * c.max_splits;
     float mx = -INFINITY, cm = 0.f;
-    for (int s = 0; s < ns; ++s) {
-        const int idx = s < nsq ? s : nsq;
-        mx = fmaxf(mx, c.part_ml[row * c.max_splits + idx].x);
-        cm = fmaxf(cm, c.part_c[row * c.max_splits + idx]);
+    for (int s = threadIdx.x; s < ns; s += blockDim.x) {
+        mx = fmaxf(mx, ml[s].x);
+        cm = fmaxf(cm, pc[s]);
     }
+    mx = block_reduce(mx, true, red);
+    cm = block_reduce(cm, true, red);
     float L = 0.f;
-    for (int s = 0; s < ns; ++s) {
-        const float2 ml = c.part_ml[row * c.max_splits + s];
-        L += ml.y * exp2f(ml.x - mx);
+    for (int s = threadIdx.x; s < ns; s += blockDim.x) L += ml[s].y * exp2f(ml[s].x - mx);
+    L = block_reduce(L, false, red);
+    float acc[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[j] = 0.f;
+#pragma unroll 8
+    for (int s = warp; s < ns; s += kCombineWarps) {
+        const float f = exp2f(ml[s].x - mx);
+        const float* pa = c.part_acc + (row * c.max_splits + s) * c.d;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (lane + 32 * j < c.d) acc[j] = fmaf(pa[lane + 32 * j], f, acc[j]);
     }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        if (lane + 32 * j < c.d) sacc[warp][lane + 32 * j] = acc[j];
+    __syncthreads();
     const float inv = L > 0.f ? 1.f / L : 0.f;
     for (int i = threadIdx.x; i < c.d; i += blockDim.x) {
-        float acc = 0.f;
-        for (int s = 0; s < ns; ++s)
-            acc = fmaf(c.part_acc[(row * c.max_splits + s) * c.d + i], exp2f(c.part_ml[row * c.max_splits + s].x - mx), acc);
-        const float o = acc * inv;
+        float o = 0.f;
+#pragma unroll
+        for (int w = 0; w < kCombineWarps; ++w) o += sacc[w][i];
+        o *= inv;
         if (c.out_bf16) static_cast<__nv_bfloat16*>(c.out)[row * c.d + i] = __float2bfloat16_rn(o);
         else static_cast<float*>(c.out)[row * c.d + i] = o;
     }
@@ -614,7 +651,7 @@ cudaError_t launch_int8_decode(kvc_handle* h, const void* q, void* out, float* c
     c.part_ml = a.part_ml; c.part_acc = a.part_acc; c.part_c = a.part_c; c.next_pos = a.next_pos;
     c.out = out; c.cmax = cmax; c.tanh_out = tanh_out;
     c.B = s.B; c.Hq = s.Hq; c.d = s.d; c.max_splits = s.max_splits; c.out_bf16 = s.out_bf16;
-    int8_combine_kernel<<<dim3(s.Hq, s.B), 128, 0, st>>>(c);
+    int8_combine_kernel<<<dim3(s.Hq, s.B), kCombineWarps * 32, 0, st>>>(c);
     return cudaGetLastError();
 }
 
