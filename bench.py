@@ -363,6 +363,47 @@ class Int8Bench(DecodeBench):
                 "l2": "inputs larger than L2: %.2f GB read per step vs 129 MB L2" % (self.units() / 1e9)}
 
 
+class Bf16AtInt8ShapeBench(DecodeBench):
+    """The bf16 decode at the INT8 workload's shape (B=8, Hq=32, Hkv=8, d=128, context 131072,
+    same keys with outlier channels and RoPE), for comparison with the INT8 tier: the same
+    tokens cost 512 B per KV head in bf16 against 288.5 B quantized."""
+
+    def __init__(self, device, batch=None, total_steps=0):
+        from kv_cache_decode_ring_gb300 import kvc
+        from kv_cache_decode_ring_gb300 import workloads as wl
+        self.w = w = wl.int8_witness()
+        w.quant = None
+        w.name = "bf16-at-int8-shape"
+        if batch:
+            w.batch = batch                   # smaller case for profiler captures
+        self.ctx = w.extra["context"]
+        w.capacity = self.ctx + total_steps + 16
+        self.cache = kvc.Cache.from_workload(w, device=device)
+        chunk = 8192
+        for c in range(self.ctx // chunk):
+            k, v = w.prefill_chunk(c, chunk, device=device)
+            self.cache.append_rows(k, v)
+            del k, v
+        self._inputs(device)
+
+    def units(self):
+        w = self.w
+        return kv_bytes_per_step([self.ctx + self.done + 1] * w.batch, w.n_kv_heads, w.head_dim)
+
+    def reset(self):
+        import torch
+        torch.cuda.synchronize()
+
+    def cpu_problem(self):
+        return 4096, self.w.n_q_heads // self.w.n_kv_heads
+
+    def config(self):
+        w = self.w
+        return {"workload": w.name, "batch": w.batch, "n_q_heads": w.n_q_heads, "n_kv_heads": w.n_kv_heads,
+                "head_dim": w.head_dim, "layout": "contiguous bf16", "context": "131072 + step",
+                "l2": "inputs larger than L2: %.2f GB read per step vs 129 MB L2" % (self.units() / 1e9)}
+
+
 class ChunkBench(DecodeBench):
     """Prefix-reuse suffix recompute, bf16: 16 requests, Hq=32, Hkv=8, d=128, prefix 8192 rows
     (RoPE 10000), cuts uniform in [0, 8191] (seed 7).  A step trims every request to its cut and
@@ -378,6 +419,9 @@ class ChunkBench(DecodeBench):
         from kv_cache_decode_ring_gb300 import kvc
         from kv_cache_decode_ring_gb300 import workloads as wl
         self.w = w = wl.prefix_reuse(windowed)
+        if batch:
+            w.batch = batch                   # smaller case for profiler captures: the first requests
+            w.extra["cuts"] = w.extra["cuts"][:batch]
         self.n = w.extra["suffix"]
         self.cache = kvc.Cache.from_workload(w, max_chunk=self.n, device=device)
         pre = w.extra["prefix"]
@@ -460,6 +504,7 @@ class ChunkWindowBench(ChunkBench):
 
 
 BENCHES = {"full-cache-mha": FullCacheBench, "sliding-window-gqa": SlidingWindowBench, "int8-witness": Int8Bench,
+           "bf16-at-int8-shape": Bf16AtInt8ShapeBench,
            "prefix-reuse": ChunkBench, "prefix-reuse-w4096": ChunkWindowBench}
 
 

@@ -9,14 +9,21 @@
 // run of cache rows.
 //
 // This is a dense contraction, so it runs on the 5th-generation tensor cores:
-//  * CTA = 128 query rows of one query head (4 warps, thread = row);
-//  * Q, K, V tiles arrive by TMA (128-byte swizzle), K/V double-buffered;
+//  * CTA = 128 query rows of one query head (4 warps, thread = row); tiles of
+//    64 keys;
+//  * Q, K, V tiles arrive by TMA (128-byte swizzle); three K and three V stages;
 //  * S = Q K^T and O += P V are tcgen05.mma (bf16 in, fp32 accumulate) issued
-//    by one thread into tensor memory (S: 128 columns, O: 128 columns);
+//    by one thread into tensor memory (two 64-column S buffers, 128-column O);
+//  * software pipeline: S of tile j + 1 is issued before the softmax of tile j
+//    and P V of tile j after it, so the tensor cores work while the threads run
+//    the softmax; two P buffers let P of tile j + 1 be written while P V of
+//    tile j still reads its own;
 //  * each thread reads its S row from tensor memory, applies the causal and
 //    window masks by absolute position, runs the online softmax in fp32 (log2
-//    domain), rescales its O row in tensor memory when its running maximum
-//    grows, and writes its P row to shared memory for the next MMA;
+//    domain) and writes its P row to shared memory for the next MMA.  A row's
+//    reference maximum moves only when a tile exceeds it by more than 2^8, so
+//    the O rescale in tensor memory (which must wait for the pending P V) is
+//    rare;
 //  * the rotated query and P are not exact in bf16, so each enters its MMA as
 //    two bf16 terms (hi, lo) accumulated in fp32 (about 16 significant bits);
 //  * K/V tiles are walked backwards from the diagonal;
@@ -35,24 +42,31 @@ namespace kvc {
 namespace {
 
 constexpr int kBM = 128;          // query rows per CTA
-constexpr int kBN = 128;          // keys per tile
+constexpr int kBN = 64;           // keys per tile
 constexpr int kD = 128;           // head dim of this kernel
-constexpr int kThreads = 128;
-constexpr int kTile = kBM * kD * 2;   // 32 KB: two 64-column halves of [128 rows][128 B]
-constexpr int kHalf = kTile / 2;
+constexpr int kSoftmaxWarps = 8;   // two per tensor-memory lane group
+constexpr int kThreads = (kSoftmaxWarps + 1) * 32;   // + one producer warp
+constexpr int kStages = 3;        // K and V tile stages
+constexpr float kLazyMax = 8.f;   // log2-domain headroom of a row's reference maximum
+constexpr int kQTile = kBM * kD * 2;     // 32 KB: two 64-dim halves of [128 rows][128 B]
+constexpr int kQHalf = kQTile / 2;
+constexpr int kKVTile = kBN * kD * 2;    // 16 KB: two 64-dim halves of [64 rows][128 B]
+constexpr int kKVHalf = kKVTile / 2;
+constexpr int kPTile = kBM * kBN * 2;    // 16 KB: [128 rows][64 keys] bf16, one 128-B swizzle column
 // Operands that are not exact bf16 (the rotated query and the softmax weights)
 // enter the MMAs as two bf16 terms, hi = bf16(x) and lo = bf16(x - hi), both
-// accumulated in fp32: about 16 significant bits instead of 8.  P_hi reuses the
-// K stage of its tile (free once S is computed, refilled only after P V completes).
-constexpr int OFF_Q = 0;                   // Q hi
-constexpr int OFF_QLO = OFF_Q + kTile;     // Q lo
-constexpr int OFF_K = OFF_QLO + kTile;     // 2 stages (stage j%2 also holds P hi of tile j)
-constexpr int OFF_V = OFF_K + 2 * kTile;   // 2 stages
-constexpr int OFF_P = OFF_V + 2 * kTile;   // P lo
-constexpr int OFF_BAR = OFF_P + kTile;     // q, kv[2], s, o
-constexpr int OFF_MISC = OFF_BAR + 64;     // tensor memory base, abort flag
-constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;
-constexpr uint32_t kTmemCols = 256;        // S: [0, 128), O: [128, 256)
+// accumulated in fp32: about 16 significant bits instead of 8.
+constexpr int OFF_Q = 0;                          // Q hi
+constexpr int OFF_QLO = OFF_Q + kQTile;           // Q lo
+constexpr int OFF_K = OFF_QLO + kQTile;           // kStages K tiles
+constexpr int OFF_V = OFF_K + kStages * kKVTile;  // kStages V tiles
+constexpr int OFF_P = OFF_V + kStages * kKVTile;  // 2 buffers of (P hi, P lo)
+constexpr int OFF_BAR = OFF_P + 4 * kPTile;       // q, k[3], v[3], s[2], o[2], p[2], done
+constexpr int kBars = 14;
+constexpr int OFF_MISC = OFF_BAR + 8 * kBars;     // tensor memory base, abort flag
+constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+static_assert(SMEM_BYTES <= 232448, "shared memory per block");
+constexpr uint32_t kTmemCols = 256;               // S buffers: [0, 64), [64, 128); O: [128, 256)
 
 struct ChunkArgs {
     const int32_t* next_pos;   // after the append: cut + n
@@ -131,16 +145,20 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// 2^x with the hardware approximation (relative error about 2^-22; 2^-inf = 0)
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     __nv_bfloat162 t = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<uint32_t*>(&t);
 }
 
-// All threads wait on the same barrier phase; if any of them gave up, all of them know.
-__device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity, uint32_t* hdr) {
-    const bool ok = mbar_wait(bar, parity);
-    if (!ok && (threadIdx.x & 31) == 0) atomicOr(hdr, kErrWait);
-    return __syncthreads_and(ok ? 1 : 0) != 0;
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -155,10 +173,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     unsigned char* sK = smem + OFF_K;
     unsigned char* sV = smem + OFF_V;
     unsigned char* sP = smem + OFF_P;
-    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + OFF_BAR);   // [0] q, [1..2] kv, [3] s, [4] o
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+    uint64_t* bq = bar;          // Q landed
+    uint64_t* bk = bar + 1;      // [stage] K tile landed
+    uint64_t* bv = bar + 4;      // [stage] V tile landed
+    uint64_t* bs = bar + 7;      // [buffer] S = Q K^T complete
+    uint64_t* bo = bar + 9;      // [buffer] O += P V complete (P buffer and V stage free again)
+    uint64_t* bp = bar + 11;     // [buffer] P written and S read by the 8 softmax warps
+    uint64_t* bdone = bar + 13;  // every MMA issued so far complete (abort path)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
 
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int b = blockIdx.z, hq = blockIdx.y, i0 = blockIdx.x * kBM;
     const int kvh = hq / a.g;
     const int np = a.next_pos[b];
@@ -170,10 +196,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int head_row0 = (b * a.Hkv + kvh) * a.S;
 
     if (tid == 0) {
-        for (int i = 0; i < 5; ++i) mbar_init(&bar[i], 1);
+        for (int i = 0; i < kBars; ++i) mbar_init(&bar[i], i == 11 || i == 12 ? kSoftmaxWarps : 1);
+        *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 0) {
+    if (warp == kSoftmaxWarps) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
                      ::"r"(smem_u32(tmem_slot)), "r"(kTmemCols) : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
@@ -182,158 +209,232 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tS = tmem, tO = tmem + 128;
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const uint32_t tO = tmem + 128;
 
-    // ---- loads: Q once, the first two K/V tiles
-    if (tid == 0) {
-        mbar_arrive_expect_tx(&bar[0], 2 * kTile);
-        tma_load_3d(sQ, &tmQ, 0, hq, b * a.n + i0, &bar[0]);
-        tma_load_3d(sQ + kHalf, &tmQ, 64, hq, b * a.n + i0, &bar[0]);
-        tma_load_3d(sQlo, &tmQlo, 0, hq, b * a.n + i0, &bar[0]);
-        tma_load_3d(sQlo + kHalf, &tmQlo, 64, hq, b * a.n + i0, &bar[0]);
-        for (int j = 0; j < 2 && j < ntiles; ++j) {
-            const int kbase = p_last + 1 - kBN * (j + 1);
-            mbar_arrive_expect_tx(&bar[1 + j], 2 * kTile);
-            tma_load_2d(sK + j * kTile, &tmK, 0, head_row0 + kbase, &bar[1 + j]);
-            tma_load_2d(sK + j * kTile + kHalf, &tmK, 64, head_row0 + kbase, &bar[1 + j]);
-            tma_load_2d(sV + j * kTile, &tmV, 0, head_row0 + kbase, &bar[1 + j]);
-            tma_load_2d(sV + j * kTile + kHalf, &tmV, 64, head_row0 + kbase, &bar[1 + j]);
-        }
-    }
-    bool ok = wait_all(&bar[0], 0, a.hdr);
+    if (warp == kSoftmaxWarps) {
+        // ================= producer: one thread issues every copy and every MMA
+        if (lane == 0) {
+            constexpr uint32_t idesc_qk = instr_desc(kBM, kBN, false);
+            constexpr uint32_t idesc_pv = instr_desc(kBM, kD, true);
+            auto kbase_of = [&](int j) { return p_last + 1 - kBN * (j + 1); };
+            auto load_k = [&](int j) {
+                const int st = j % kStages;
+                mbar_arrive_expect_tx(&bk[st], kKVTile);
+                tma_load_2d(sK + st * kKVTile, &tmK, 0, head_row0 + kbase_of(j), &bk[st]);
+                tma_load_2d(sK + st * kKVTile + kKVHalf, &tmK, 64, head_row0 + kbase_of(j), &bk[st]);
+            };
+            auto load_v = [&](int j) {
+                const int st = j % kStages;
+                mbar_arrive_expect_tx(&bv[st], kKVTile);
+                tma_load_2d(sV + st * kKVTile, &tmV, 0, head_row0 + kbase_of(j), &bv[st]);
+                tma_load_2d(sV + st * kKVTile + kKVHalf, &tmV, 64, head_row0 + kbase_of(j), &bv[st]);
+            };
+            // S_j = Q_hi K_j^T + Q_lo K_j^T into S buffer j % 2
+            auto issue_s = [&](int j) {
+                const uint32_t q0 = smem_u32(sQ), q1 = smem_u32(sQlo), k0 = smem_u32(sK + (j % kStages) * kKVTile);
+                const uint32_t d = tmem + 64 * (j & 1);
+#pragma unroll
+                for (int s = 0; s < kD / 16; ++s) {
+                    const uint32_t oq = (s >> 2) * kQHalf + (s & 3) * 32, ok = (s >> 2) * kKVHalf + (s & 3) * 32;
+                    mma_bf16(d, smem_desc(q0 + oq, 16), smem_desc(k0 + ok, 16), idesc_qk, s > 0);
+                }
+#pragma unroll
+                for (int s = 0; s < kD / 16; ++s) {
+                    const uint32_t oq = (s >> 2) * kQHalf + (s & 3) * 32, ok = (s >> 2) * kKVHalf + (s & 3) * 32;
+                    mma_bf16(d, smem_desc(q1 + oq, 16), smem_desc(k0 + ok, 16), idesc_qk, 1);
+                }
+                mma_commit(&bs[j & 1]);
+            };
+            // O += P_hi V_j + P_lo V_j (P buffer j % 2)
+            auto issue_pv = [&](int j) {
+                const uint32_t ph = smem_u32(sP + (j & 1) * 2 * kPTile), pl = ph + kPTile;
+                const uint32_t v0 = smem_u32(sV + (j % kStages) * kKVTile);
+#pragma unroll
+                for (int s2 = 0; s2 < kBN / 16; ++s2)
+                    mma_bf16(tO, smem_desc(ph + s2 * 32, 16), smem_desc(v0 + s2 * 2048, kKVHalf), idesc_pv,
+                             (j > 0 || s2 > 0));
+#pragma unroll
+                for (int s2 = 0; s2 < kBN / 16; ++s2)
+                    mma_bf16(tO, smem_desc(pl + s2 * 32, 16), smem_desc(v0 + s2 * 2048, kKVHalf), idesc_pv, 1);
+                mma_commit(&bo[j & 1]);
+            };
 
-    const int row = tid;                       // query row of this thread = tensor-memory lane
-    const int p = cut + i0 + row;              // its absolute position
-    const bool row_valid = row < rows;
-    const int key_lo = a.W > 0 ? max(0, p - a.W + 1) : 0;
-    float m = -INFINITY, l = 0.f;
-    constexpr uint32_t idesc_qk = instr_desc(kBM, kBN, false);
-    constexpr uint32_t idesc_pv = instr_desc(kBM, kD, true);
-
-    for (int j = 0; j < ntiles && ok; ++j) {
-        const int st = j & 1;
-        const int kbase = p_last + 1 - kBN * (j + 1);
-        // ---- S = Q K^T
-        if (tid == 0) {
-            ok = mbar_wait(&bar[1 + st], (uint32_t)((j >> 1) & 1));
-            if (ok) {
+            bool ok = true;
+            // copies issued and awaited so far (an abort drains the rest before exit)
+            int k_issued = 0, v_issued = 0, k_waited = 0, v_waited = 0;
+            bool q_waited = false;
+            mbar_arrive_expect_tx(bq, 2 * kQTile);
+            tma_load_3d(sQ, &tmQ, 0, hq, b * a.n + i0, bq);
+            tma_load_3d(sQ + kQHalf, &tmQ, 64, hq, b * a.n + i0, bq);
+            tma_load_3d(sQlo, &tmQlo, 0, hq, b * a.n + i0, bq);
+            tma_load_3d(sQlo + kQHalf, &tmQlo, 64, hq, b * a.n + i0, bq);
+            for (int j = 0; j < kStages && j < ntiles; ++j) { load_k(j); load_v(j); k_issued = v_issued = j + 1; }
+            ok = q_waited = mbar_wait(bq, 0);
+            for (int j = 0; j < 2 && j < ntiles && ok; ++j) {
+                ok = mbar_wait(&bk[j], 0);
+                if (ok) { k_waited = j + 1; fence_after(); issue_s(j); }
+            }
+            for (int j = 0; j < ntiles && ok; ++j) {
+                if (*abort_flag) { ok = false; break; }
+                // K stage of tile j is free once S_j is complete: fetch tile j + kStages
+                ok = mbar_wait(&bs[j & 1], (uint32_t)((j >> 1) & 1));
+                if (!ok) break;
+                if (j + kStages < ntiles) { load_k(j + kStages); k_issued = j + kStages + 1; }
+                // V stage of tile j - 2 is free once its P V is complete: fetch tile j + 1
+                if (j >= 2 && j + 1 < ntiles) {
+                    ok = mbar_wait(&bo[j & 1], (uint32_t)(((j - 2) >> 1) & 1));
+                    if (!ok) break;
+                    load_v(j + 1);
+                    v_issued = j + 2;
+                }
+                // O += P_j V_j once the softmax warps wrote P_j and V_j landed
+                ok = mbar_wait(&bp[j & 1], (uint32_t)((j >> 1) & 1)) &&
+                     mbar_wait(&bv[j % kStages], (uint32_t)((j / kStages) & 1));
+                if (!ok) break;
+                v_waited = j + 1;
                 fence_after();
-                const uint32_t q0 = smem_u32(sQ), q1 = smem_u32(sQlo), k0 = smem_u32(sK + st * kTile);
-#pragma unroll
-                for (int s = 0; s < kD / 16; ++s) {
-                    const uint32_t off = (s >> 2) * kHalf + (s & 3) * 32;
-                    mma_bf16(tS, smem_desc(q0 + off, 16), smem_desc(k0 + off, 16), idesc_qk, s > 0);
+                issue_pv(j);
+                // S_{j+2} into S buffer j % 2 (read by the softmax warps: bp above)
+                if (j + 2 < ntiles) {
+                    ok = mbar_wait(&bk[(j + 2) % kStages], (uint32_t)(((j + 2) / kStages) & 1));
+                    if (!ok) break;
+                    k_waited = j + 3;
+                    fence_after();
+                    issue_s(j + 2);
                 }
-#pragma unroll
-                for (int s = 0; s < kD / 16; ++s) {
-                    const uint32_t off = (s >> 2) * kHalf + (s & 3) * 32;
-                    mma_bf16(tS, smem_desc(q1 + off, 16), smem_desc(k0 + off, 16), idesc_qk, 1);
-                }
-                mma_commit(&bar[3]);
-            } else {
+            }
+            if (!ok) {
+                *abort_flag = 1;
                 atomicOr(a.hdr, kErrWait);
+                // let every copy still in flight land before the CTA can exit
+                if (!q_waited) mbar_wait(bq, 0);
+                for (int t = k_waited; t < k_issued; ++t) mbar_wait(&bk[t % kStages], (uint32_t)((t / kStages) & 1));
+                for (int t = v_waited; t < v_issued; ++t) mbar_wait(&bv[t % kStages], (uint32_t)((t / kStages) & 1));
             }
         }
-        if (!__syncthreads_and(ok ? 1 : 0)) { ok = false; break; }
-        ok = wait_all(&bar[3], (uint32_t)(j & 1), a.hdr);
-        if (!ok) break;
-        fence_after();
-        // ---- softmax on this thread's row
-        float s[kBN];
-#pragma unroll
-        for (int c = 0; c < kBN; c += 32) tmem_ld32(tS + lane_off + c, s + c);
-        float mx = m;
-#pragma unroll
-        for (int c = 0; c < kBN; ++c) {
-            const int key = kbase + c;
-            const bool vis = row_valid && key >= key_lo && key <= p;
-            s[c] = vis ? s[c] * a.scale_log2 : -INFINITY;
-            mx = fmaxf(mx, s[c]);
-        }
-        const float base = mx == -INFINITY ? 0.f : mx;
-        const float alpha = exp2f(m - base);          // 0 when m = -inf
-        float rs = 0.f;
-#pragma unroll
-        for (int c = 0; c < kBN; ++c) {
-            s[c] = exp2f(s[c] - base);
-            rs += s[c];
-        }
-        l = l * alpha + rs;
-        // O holds the previous tiles at the old maximum: rescale the rows whose maximum
-        // grew.  tcgen05.ld/st are warp-collective (.sync.aligned), so the whole warp
-        // takes part whenever any of its rows needs it; the others scale by 1.
-        const bool grow = j > 0 && alpha != 1.f;
-        if (__any_sync(0xffffffffu, grow)) {
-            const float f = grow ? alpha : 1.f;
-#pragma unroll
-            for (int c = 0; c < kD; c += 32) {
-                float o[32];
-                tmem_ld32(tO + lane_off + c, o);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) o[e] *= f;
-                tmem_st32(tO + lane_off + c, o);
-            }
-        }
-        m = mx;
-        // P row -> shared memory as hi and lo bf16 terms, K-major 128-byte swizzle
-        unsigned char* sPhi = sK + st * kTile;
-#pragma unroll
-        for (int c = 0; c < kBN / 8; ++c) {
-            uint32_t hi[4], lo[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const __nv_bfloat162 h2 = __floats2bfloat162_rn(s[8 * c + 2 * e], s[8 * c + 2 * e + 1]);
-                const float2 hf = __bfloat1622float2(h2);
-                hi[e] = *reinterpret_cast<const uint32_t*>(&h2);
-                lo[e] = pack_bf16(s[8 * c + 2 * e] - hf.x, s[8 * c + 2 * e + 1] - hf.y);
-            }
-            const int off = (c >> 3) * kHalf + row * 128 + (((c & 7) ^ (row & 7)) * 16);
-            *reinterpret_cast<uint4*>(sPhi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-            *reinterpret_cast<uint4*>(sP + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        fence_before();
-        __syncthreads();
-        // ---- O += P V
-        if (tid == 0) {
+    } else {
+        // ================= softmax warps: warp w serves rows 32 (w % 4) .. + 31 (its
+        // tensor-memory lanes) and keys 32 (w / 4) .. + 31 of every tile
+        const int lg = warp & 3, hf = warp >> 2;
+        const int row = 32 * lg + lane;            // query row = tensor-memory lane
+        const uint32_t lane_off = (uint32_t)(32 * lg) << 16;
+        const int p = cut + i0 + row;               // its absolute position
+        const bool row_valid = row < rows;
+        const int key_lo = a.W > 0 ? max(0, p - a.W + 1) : 0;
+        const int key_lo_max = a.W > 0 ? max(0, p_last - a.W + 1) : 0;   // the CTA's largest key_lo
+        float m_ref = -INFINITY, l = 0.f;
+        bool fail = false;
+        for (int j = 0; j < ntiles; ++j) {
+            bool w = mbar_wait(&bs[j & 1], (uint32_t)((j >> 1) & 1)) && !*abort_flag;
+            if (!__all_sync(0xffffffffu, w)) { fail = true; break; }
             fence_after();
-            const uint32_t ph = smem_u32(sK + st * kTile), pl = smem_u32(sP), v0 = smem_u32(sV + st * kTile);
+            // both warps of a row pair read the whole tile, so they agree on its maximum
+            float sm[kBN / 2], so[kBN / 2];
+            const uint32_t tSj = tmem + 64 * (j & 1) + lane_off;
+            tmem_ld32(tSj + 32 * hf, sm);
+            tmem_ld32(tSj + 32 * (1 - hf), so);
+            const int kb = p_last + 1 - kBN * (j + 1);
+            const int km = kb + 32 * hf, ko = kb + 32 * (1 - hf);    // first key of each half
+            float mx = -INFINITY;
+            if (kb >= key_lo_max && kb + kBN - 1 <= p_first) {
+                // every key of the tile is visible to every row of the CTA
 #pragma unroll
-            for (int s2 = 0; s2 < kBN / 16; ++s2) {
-                const uint32_t aoff = (s2 >> 2) * kHalf + (s2 & 3) * 32;
-                mma_bf16(tO, smem_desc(ph + aoff, 16), smem_desc(v0 + s2 * 2048, kHalf), idesc_pv, (j > 0 || s2 > 0));
-            }
+                for (int c = 0; c < kBN / 2; ++c) mx = fmaxf(mx, fmaxf(sm[c], so[c]));
+            } else {
 #pragma unroll
-            for (int s2 = 0; s2 < kBN / 16; ++s2) {
-                const uint32_t aoff = (s2 >> 2) * kHalf + (s2 & 3) * 32;
-                mma_bf16(tO, smem_desc(pl + aoff, 16), smem_desc(v0 + s2 * 2048, kHalf), idesc_pv, 1);
+                for (int c = 0; c < kBN / 2; ++c) {
+                    const bool vm = row_valid && km + c >= key_lo && km + c <= p;
+                    const bool vo = row_valid && ko + c >= key_lo && ko + c <= p;
+                    sm[c] = vm ? sm[c] : -INFINITY;
+                    mx = fmaxf(mx, fmaxf(sm[c], vo ? so[c] : -INFINITY));
+                }
             }
-            mma_commit(&bar[4]);
+            // the reference maximum moves only when the tile exceeds it by more than kLazyMax
+            bool grow = false;
+            float alpha = 1.f;
+            if (mx > m_ref + kLazyMax) {           // also the first visible tile (m_ref = -inf)
+                grow = m_ref != -INFINITY;        // O and l hold earlier tiles only then
+                alpha = grow ? exp2f(m_ref - mx) : 1.f;
+                m_ref = mx;
+            }
+            const float base = m_ref == -INFINITY ? 0.f : m_ref;
+            float2 rs2 = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int c = 0; c < kBN / 2; c += 2) {
+                sm[c] = ex2(sm[c] - base);         // masked keys: 0
+                sm[c + 1] = ex2(sm[c + 1] - base);
+                rs2 = __fadd2_rn(rs2, make_float2(sm[c], sm[c + 1]));
+            }
+            l = l * alpha + (rs2.x + rs2.y);
+            // P buffer j % 2 was last read by P V of tile j - 2; O may be rescaled only
+            // once P V of tile j - 1 is complete (tcgen05.ld/st: whole warps)
+            const bool any_grow = __any_sync(0xffffffffu, grow);
+            bool w2 = j < 2 || mbar_wait(&bo[j & 1], (uint32_t)(((j - 2) >> 1) & 1));
+            if (any_grow) w2 = w2 && mbar_wait(&bo[(j - 1) & 1], (uint32_t)(((j - 1) >> 1) & 1));
+            if (!__all_sync(0xffffffffu, w2)) { fail = true; break; }
+            if (any_grow) {
+                fence_after();
+                const float f = grow ? alpha : 1.f;
+#pragma unroll
+                for (int c = 0; c < kD / 2; c += 32) {
+                    float o[32];
+                    tmem_ld32(tO + lane_off + 64 * hf + c, o);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] *= f;
+                    tmem_st32(tO + lane_off + 64 * hf + c, o);
+                }
+            }
+            // this warp's 32 keys of the P row -> shared memory as hi and lo bf16 terms,
+            // K-major 128-byte swizzle
+            unsigned char* sPhi = sP + (j & 1) * 2 * kPTile;
+#pragma unroll
+            for (int c = 0; c < kBN / 16; ++c) {
+                uint32_t hi[4], lo2[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 x = make_float2(sm[8 * c + 2 * e], sm[8 * c + 2 * e + 1]);
+                    const __nv_bfloat162 h2 = __floats2bfloat162_rn(x.x, x.y);
+                    const float2 r = __ffma2_rn(__bfloat1622float2(h2), make_float2(-1.f, -1.f), x);   // x - hi, exact
+                    hi[e] = *reinterpret_cast<const uint32_t*>(&h2);
+                    lo2[e] = pack_bf16(r.x, r.y);
+                }
+                const int off = row * 128 + (((4 * hf + c) ^ (row & 7)) * 16);
+                *reinterpret_cast<uint4*>(sPhi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<uint4*>(sPhi + kPTile + off) = make_uint4(lo2[0], lo2[1], lo2[2], lo2[3]);
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bp[j & 1]);
         }
-        ok = wait_all(&bar[4], (uint32_t)(j & 1), a.hdr);
-        if (!ok) break;
-        fence_after();
-        // ---- refill this stage with tile j + 2
-        if (tid == 0 && j + 2 < ntiles) {
-            const int kb2 = p_last + 1 - kBN * (j + 3);
-            mbar_arrive_expect_tx(&bar[1 + st], 2 * kTile);
-            tma_load_2d(sK + st * kTile, &tmK, 0, head_row0 + kb2, &bar[1 + st]);
-            tma_load_2d(sK + st * kTile + kHalf, &tmK, 64, head_row0 + kb2, &bar[1 + st]);
-            tma_load_2d(sV + st * kTile, &tmV, 0, head_row0 + kb2, &bar[1 + st]);
-            tma_load_2d(sV + st * kTile + kHalf, &tmV, 64, head_row0 + kb2, &bar[1 + st]);
+        // the last P V complete before O is read
+        if (!fail && ntiles > 0) {
+            const bool w = mbar_wait(&bo[(ntiles - 1) & 1], (uint32_t)(((ntiles - 1) >> 1) & 1));
+            fail = !__all_sync(0xffffffffu, w);
         }
+        if (fail) {
+            if (lane == 0) atomicOr(a.hdr, kErrWait);
+            *abort_flag = 1;
+        }
+        // partial row sums meet in the (now idle) K stages
+        reinterpret_cast<float*>(sK)[hf * kBM + row] = l;
     }
-
-    // ---- epilogue: O / l; every lane reads (warp-collective), valid rows store
-    if (ok) {
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        const size_t orow = (((size_t)b * a.n + i0 + row) * a.Hq + hq) * kD;
+    __syncthreads();
+    const bool aborted = *abort_flag != 0;
+    if (warp < kSoftmaxWarps && !aborted) {
+        // ---- epilogue: O / l; warp w stores columns 64 (w / 4) .. + 63 of its rows
+        const int lg = warp & 3, hf = warp >> 2;
+        const int row = 32 * lg + lane;
+        const uint32_t lane_off = (uint32_t)(32 * lg) << 16;
+        fence_after();
+        const float L = reinterpret_cast<const float*>(sK)[row] + reinterpret_cast<const float*>(sK)[kBM + row];
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        const size_t orow = (((size_t)b * a.n + i0 + row) * a.Hq + hq) * kD + 64 * hf;
 #pragma unroll
-        for (int c = 0; c < kD; c += 32) {
+        for (int c = 0; c < kD / 2; c += 32) {
             float o[32];
-            tmem_ld32(tO + lane_off + c, o);
-            if (!row_valid) continue;
+            tmem_ld32(tO + lane_off + 64 * hf + c, o);
+            if (row >= rows) continue;
             if (a.out_bf16) {
                 uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + orow + c);
 #pragma unroll
@@ -352,25 +453,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                     dst[e] = make_float4(o[4 * e] * inv, o[4 * e + 1] * inv, o[4 * e + 2] * inv, o[4 * e + 3] * inv);
             }
         }
-    } else if (!ok) {
-        // make sure no tensor-core operation still targets our columns before freeing them
-        if (tid == 0) {
-            mbar_wait(&bar[3], 0);
-            mbar_wait(&bar[4], 0);
-        }
+    }
+    if (warp == kSoftmaxWarps && aborted && lane == 0) {
+        // make sure no tensor-core operation still targets our columns before freeing
+        // them: a commit tracks every MMA this thread issued
+        mma_commit(bdone);
+        mbar_wait(bdone, 0);
     }
     fence_before();
     __syncthreads();
-    if (warp == 0) {
+    if (warp == kSoftmaxWarps) {
         fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
     }
 }
 
-// Query rows rotated at their positions (fp32 rule of the cache keys), split into
+// Query rows rotated at their positions (fp32 rule of the cache keys), times
+// log2(e)/sqrt(d) (so that Q K^T is the logit in the log2 domain), split into
 // bf16 hi = bf16(y) and lo = bf16(y - hi).
 __global__ void rope_q_kernel(const __nv_bfloat16* q, __nv_bfloat16* qr, __nv_bfloat16* qlo,
-                              const int32_t* next_pos, const float2* rope, int n, int Hq, int d) {
+                              const int32_t* next_pos, const float2* rope, int n, int Hq, int d, float scale) {
     const int b = blockIdx.y;
     const int cut = next_pos[b] - n;
     const size_t per_b = (size_t)n * Hq * (d / 2);
@@ -381,6 +483,8 @@ __global__ void rope_q_kernel(const __nv_bfloat16* q, __nv_bfloat16* qr, __nv_bf
         const float x0 = __bfloat162float(q[off]), x1 = __bfloat162float(q[off + 1]);
         float y0 = x0, y1 = x1;
         if (rope) rope_pair(x0, x1, rope[(size_t)(cut + i) * (d / 2) + pr], y0, y1);
+        y0 *= scale;
+        y1 *= scale;
         const __nv_bfloat16 h0 = __float2bfloat16_rn(y0), h1 = __float2bfloat16_rn(y1);
         qr[off] = h0;
         qr[off + 1] = h1;
@@ -427,8 +531,9 @@ cudaError_t launch_chunk(kvc_handle* h, const void* q, void* out, int n, cudaStr
     __nv_bfloat16* qlo = qr + (size_t)s.B * s.max_chunk * s.Hq * s.d;
     const int32_t* np = reinterpret_cast<const int32_t*>(h->state + h->L.next_pos);
     const float2* rope = s.rope ? reinterpret_cast<const float2*>(h->state + h->L.rope) : nullptr;
+    const float scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)s.d));
     rope_q_kernel<<<dim3(128, s.B), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(q), qr, qlo, np, rope, n, s.Hq,
-                                                  s.d);
+                                                  s.d, scale_log2);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
