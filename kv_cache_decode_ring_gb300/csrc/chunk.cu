@@ -11,7 +11,8 @@
 // This is a dense contraction, so it runs on the 5th-generation tensor cores:
 //  * CTA = 128 query rows of one query head (4 warps, thread = row); tiles of
 //    64 keys;
-//  * Q, K, V tiles arrive by TMA (128-byte swizzle); three K and three V stages;
+//  * Q, K, V tiles arrive by TMA (128-byte swizzle); four K and four V stages,
+//    each refilled as soon as the MMA that read it completes;
 //  * S = Q K^T and O += P V are tcgen05.mma (bf16 in, fp32 accumulate) issued
 //    by one thread into tensor memory (two 64-column S buffers, 128-column O);
 //  * software pipeline: S of tile j + 1 is issued before the softmax of tile j
@@ -42,31 +43,36 @@ namespace kvc {
 namespace {
 
 constexpr int kBM = 128;          // query rows per CTA
-constexpr int kBN = 64;           // keys per tile
+constexpr int kBN = 128;          // keys per tile
 constexpr int kD = 128;           // head dim of this kernel
 constexpr int kSoftmaxWarps = 8;   // two per tensor-memory lane group
 constexpr int kThreads = (kSoftmaxWarps + 1) * 32;   // + one producer warp
-constexpr int kStages = 3;        // K and V tile stages
+constexpr int kKStages = 3;       // K tile stages (free once S of the tile is complete)
+constexpr int kVStages = 2;       // V tile stages (free once P V of the tile is complete)
 constexpr float kLazyMax = 8.f;   // log2-domain headroom of a row's reference maximum
-constexpr int kQTile = kBM * kD * 2;     // 32 KB: two 64-dim halves of [128 rows][128 B]
-constexpr int kQHalf = kQTile / 2;
-constexpr int kKVTile = kBN * kD * 2;    // 16 KB: two 64-dim halves of [64 rows][128 B]
-constexpr int kKVHalf = kKVTile / 2;
-constexpr int kPTile = kBM * kBN * 2;    // 16 KB: [128 rows][64 keys] bf16, one 128-B swizzle column
+constexpr int kTileB = 128 * kD * 2;     // 32 KB: two 64-dim halves of [128 rows][128 B]
+constexpr int kHalfB = kTileB / 2;
 // Operands that are not exact bf16 (the rotated query and the softmax weights)
 // enter the MMAs as two bf16 terms, hi = bf16(x) and lo = bf16(x - hi), both
 // accumulated in fp32: about 16 significant bits instead of 8.
-constexpr int OFF_Q = 0;                          // Q hi
-constexpr int OFF_QLO = OFF_Q + kQTile;           // Q lo
-constexpr int OFF_K = OFF_QLO + kQTile;           // kStages K tiles
-constexpr int OFF_V = OFF_K + kStages * kKVTile;  // kStages V tiles
-constexpr int OFF_P = OFF_V + kStages * kKVTile;  // 2 buffers of (P hi, P lo)
-constexpr int OFF_BAR = OFF_P + 4 * kPTile;       // q, k[3], v[3], s[2], o[2], p[2], done
-constexpr int kBars = 14;
-constexpr int OFF_MISC = OFF_BAR + 8 * kBars;     // tensor memory base, abort flag
+constexpr int OFF_Q = 0;                              // Q hi; after the copy into tensor memory:
+                                                      // row-maximum exchange, then row sums
+constexpr int OFF_QLO = OFF_Q + kTileB;               // Q lo
+constexpr int OFF_K = OFF_QLO + kTileB;               // kKStages K tiles
+constexpr int OFF_V = OFF_K + kKStages * kTileB;      // kVStages V tiles
+constexpr int OFF_BAR = OFF_V + kVStages * kTileB;    // q, k[3], v[2], s[2], o[2], p[2], done, q in tmem
+constexpr int kBars = 1 + kKStages + kVStages + 2 + 2 + 2 + 1 + 1;
+constexpr int OFF_MISC = OFF_BAR + 8 * kBars;         // tensor memory base, abort flag
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory per block");
-constexpr uint32_t kTmemCols = 256;               // S buffers: [0, 64), [64, 128); O: [128, 256)
+// Tensor memory (512 columns, 128 lanes = query rows):
+//   S/P buffers [0, 128), [128, 256): S of a tile in fp32; the softmax warp serving
+//     keys 64 h .. + 63 overwrites its 64 columns with P as bf16 pairs (hi in the first
+//     32, lo in the next 32), the A operand of P V;
+//   O [256, 384) fp32; Q hi [384, 448) and Q lo [448, 512) as bf16 pairs, the A
+//   operand of S.  Only K and V tiles are shared-memory operands.
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColO = 256, kColQ = 384, kColQlo = 448;
 
 struct ChunkArgs {
     const int32_t* next_pos;   // after the append: cut + n
@@ -94,11 +100,14 @@ __host__ __device__ constexpr uint32_t instr_desc(int M, int N, bool b_mn) {
            ((uint32_t)(M >> 4) << 24);
 }
 
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, int acc) {
+// D (tensor memory) (+)= A (tensor memory, bf16 pairs along columns, row m in lane m)
+// . B (shared memory descriptor)
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                            int acc) {
     asm volatile(
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
-        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(acc)
         : "memory");
 }
 
@@ -152,6 +161,22 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// 16 consecutive 32-bit columns of this thread's tensor-memory lane
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+        "%14, %15, %16};"
+        ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+          "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t* v) {
+    tmem_st16(taddr, v);
+    tmem_st16(taddr + 16, v + 16);
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     __nv_bfloat162 t = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<uint32_t*>(&t);
@@ -159,6 +184,16 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Barrier `id` over the 64 threads of a warp pair; returns the OR of `pred` over them.
+__device__ __forceinline__ bool pair_sync_or(int id, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n barrier.red.or.pred q, %2, 64, p;\n"
+        " selp.u32 %0, 1, 0, q;\n}\n"
+        : "=r"(r) : "r"((uint32_t)pred), "r"(id) : "memory");
+    return r != 0;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -172,15 +207,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     unsigned char* sQlo = smem + OFF_QLO;
     unsigned char* sK = smem + OFF_K;
     unsigned char* sV = smem + OFF_V;
-    unsigned char* sP = smem + OFF_P;
+    float* xmax = reinterpret_cast<float*>(smem + OFF_Q);   // [parity][half][row], after Q left
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
-    uint64_t* bq = bar;          // Q landed
-    uint64_t* bk = bar + 1;      // [stage] K tile landed
-    uint64_t* bv = bar + 4;      // [stage] V tile landed
-    uint64_t* bs = bar + 7;      // [buffer] S = Q K^T complete
-    uint64_t* bo = bar + 9;      // [buffer] O += P V complete (P buffer and V stage free again)
-    uint64_t* bp = bar + 11;     // [buffer] P written and S read by the 8 softmax warps
-    uint64_t* bdone = bar + 13;  // every MMA issued so far complete (abort path)
+    uint64_t* bq = bar;                      // Q landed
+    uint64_t* bk = bar + 1;                  // [stage] K tile landed
+    uint64_t* bv = bk + kKStages;            // [stage] V tile landed
+    uint64_t* bs = bv + kVStages;            // [buffer] S = Q K^T complete
+    uint64_t* bo = bs + 2;                   // [buffer] O += P V complete
+    uint64_t* bp = bo + 2;                   // [buffer] P written by the 8 softmax warps
+    uint64_t* bdone = bp + 2;                // every MMA issued so far complete (abort path)
+    uint64_t* bqt = bdone + 1;               // Q copied into tensor memory by the 8 softmax warps
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
 
@@ -196,7 +232,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int head_row0 = (b * a.Hkv + kvh) * a.S;
 
     if (tid == 0) {
-        for (int i = 0; i < kBars; ++i) mbar_init(&bar[i], i == 11 || i == 12 ? kSoftmaxWarps : 1);
+        for (int i = 0; i < kBars; ++i) mbar_init(&bar[i], 1);
+        for (int i = 0; i < 2; ++i) mbar_init(&bp[i], kSoftmaxWarps);
+        mbar_init(bqt, kSoftmaxWarps);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -209,7 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tO = tmem + 128;
+    const uint32_t tO = tmem + kColO;
 
     if (warp == kSoftmaxWarps) {
         // ================= producer: one thread issues every copy and every MMA
@@ -218,44 +256,48 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idesc_pv = instr_desc(kBM, kD, true);
             auto kbase_of = [&](int j) { return p_last + 1 - kBN * (j + 1); };
             auto load_k = [&](int j) {
-                const int st = j % kStages;
-                mbar_arrive_expect_tx(&bk[st], kKVTile);
-                tma_load_2d(sK + st * kKVTile, &tmK, 0, head_row0 + kbase_of(j), &bk[st]);
-                tma_load_2d(sK + st * kKVTile + kKVHalf, &tmK, 64, head_row0 + kbase_of(j), &bk[st]);
+                const int st = j % kKStages;
+                mbar_arrive_expect_tx(&bk[st], kTileB);
+                tma_load_2d(sK + st * kTileB, &tmK, 0, head_row0 + kbase_of(j), &bk[st]);
+                tma_load_2d(sK + st * kTileB + kHalfB, &tmK, 64, head_row0 + kbase_of(j), &bk[st]);
             };
             auto load_v = [&](int j) {
-                const int st = j % kStages;
-                mbar_arrive_expect_tx(&bv[st], kKVTile);
-                tma_load_2d(sV + st * kKVTile, &tmV, 0, head_row0 + kbase_of(j), &bv[st]);
-                tma_load_2d(sV + st * kKVTile + kKVHalf, &tmV, 64, head_row0 + kbase_of(j), &bv[st]);
+                const int st = j % kVStages;
+                mbar_arrive_expect_tx(&bv[st], kTileB);
+                tma_load_2d(sV + st * kTileB, &tmV, 0, head_row0 + kbase_of(j), &bv[st]);
+                tma_load_2d(sV + st * kTileB + kHalfB, &tmV, 64, head_row0 + kbase_of(j), &bv[st]);
             };
-            // S_j = Q_hi K_j^T + Q_lo K_j^T into S buffer j % 2
+            // descriptors of stage 0; stage and k-step offsets move only the start address
+            // field (bytes / 16, no carry: shared addresses stay below 256 KB)
+            const uint64_t kdesc0 = smem_desc(smem_u32(sK), 16), vdesc0 = smem_desc(smem_u32(sV), kHalfB);
+            // S_j = Q_hi K_j^T + Q_lo K_j^T into S/P buffer j % 2 (Q: dims 16 s .. + 15 in
+            // columns 8 s .. + 7 of its region)
             auto issue_s = [&](int j) {
-                const uint32_t q0 = smem_u32(sQ), q1 = smem_u32(sQlo), k0 = smem_u32(sK + (j % kStages) * kKVTile);
-                const uint32_t d = tmem + 64 * (j & 1);
+                const uint64_t kd = kdesc0 + (uint64_t)((j % kKStages) * (kTileB >> 4));
+                const uint32_t d = tmem + 128 * (j & 1);
 #pragma unroll
-                for (int s = 0; s < kD / 16; ++s) {
-                    const uint32_t oq = (s >> 2) * kQHalf + (s & 3) * 32, ok = (s >> 2) * kKVHalf + (s & 3) * 32;
-                    mma_bf16(d, smem_desc(q0 + oq, 16), smem_desc(k0 + ok, 16), idesc_qk, s > 0);
-                }
+                for (int s = 0; s < kD / 16; ++s)
+                    mma_bf16_ts(d, tmem + kColQ + 8 * s, kd + (uint64_t)(((s >> 2) * kHalfB + (s & 3) * 32) >> 4),
+                                idesc_qk, s > 0);
 #pragma unroll
-                for (int s = 0; s < kD / 16; ++s) {
-                    const uint32_t oq = (s >> 2) * kQHalf + (s & 3) * 32, ok = (s >> 2) * kKVHalf + (s & 3) * 32;
-                    mma_bf16(d, smem_desc(q1 + oq, 16), smem_desc(k0 + ok, 16), idesc_qk, 1);
-                }
+                for (int s = 0; s < kD / 16; ++s)
+                    mma_bf16_ts(d, tmem + kColQlo + 8 * s, kd + (uint64_t)(((s >> 2) * kHalfB + (s & 3) * 32) >> 4),
+                                idesc_qk, 1);
                 mma_commit(&bs[j & 1]);
             };
-            // O += P_hi V_j + P_lo V_j (P buffer j % 2)
+            // O += P_hi V_j + P_lo V_j: keys 16 s2 .. + 15 of P sit in columns
+            // 64 (s2 / 4) + 8 (s2 % 4) .. + 7 of S/P buffer j % 2 (lo 32 columns further)
             auto issue_pv = [&](int j) {
-                const uint32_t ph = smem_u32(sP + (j & 1) * 2 * kPTile), pl = ph + kPTile;
-                const uint32_t v0 = smem_u32(sV + (j % kStages) * kKVTile);
+                const uint32_t pb = tmem + 128 * (j & 1);
+                const uint64_t vd = vdesc0 + (uint64_t)((j % kVStages) * (kTileB >> 4));
 #pragma unroll
                 for (int s2 = 0; s2 < kBN / 16; ++s2)
-                    mma_bf16(tO, smem_desc(ph + s2 * 32, 16), smem_desc(v0 + s2 * 2048, kKVHalf), idesc_pv,
-                             (j > 0 || s2 > 0));
+                    mma_bf16_ts(tO, pb + 64 * (s2 >> 2) + 8 * (s2 & 3), vd + (uint64_t)((s2 * 2048) >> 4), idesc_pv,
+                                (j > 0 || s2 > 0));
 #pragma unroll
                 for (int s2 = 0; s2 < kBN / 16; ++s2)
-                    mma_bf16(tO, smem_desc(pl + s2 * 32, 16), smem_desc(v0 + s2 * 2048, kKVHalf), idesc_pv, 1);
+                    mma_bf16_ts(tO, pb + 64 * (s2 >> 2) + 32 + 8 * (s2 & 3), vd + (uint64_t)((s2 * 2048) >> 4),
+                                idesc_pv, 1);
                 mma_commit(&bo[j & 1]);
             };
 
@@ -263,40 +305,40 @@ __global__ void __launch_bounds__(kThreads, 1)
             // copies issued and awaited so far (an abort drains the rest before exit)
             int k_issued = 0, v_issued = 0, k_waited = 0, v_waited = 0;
             bool q_waited = false;
-            mbar_arrive_expect_tx(bq, 2 * kQTile);
+            mbar_arrive_expect_tx(bq, 2 * kTileB);
             tma_load_3d(sQ, &tmQ, 0, hq, b * a.n + i0, bq);
-            tma_load_3d(sQ + kQHalf, &tmQ, 64, hq, b * a.n + i0, bq);
+            tma_load_3d(sQ + kHalfB, &tmQ, 64, hq, b * a.n + i0, bq);
             tma_load_3d(sQlo, &tmQlo, 0, hq, b * a.n + i0, bq);
-            tma_load_3d(sQlo + kQHalf, &tmQlo, 64, hq, b * a.n + i0, bq);
-            for (int j = 0; j < kStages && j < ntiles; ++j) { load_k(j); load_v(j); k_issued = v_issued = j + 1; }
+            tma_load_3d(sQlo + kHalfB, &tmQlo, 64, hq, b * a.n + i0, bq);
+            for (int j = 0; j < kKStages && j < ntiles; ++j) { load_k(j); k_issued = j + 1; }
+            for (int j = 0; j < kVStages && j < ntiles; ++j) { load_v(j); v_issued = j + 1; }
             ok = q_waited = mbar_wait(bq, 0);
+            ok = ok && mbar_wait(bqt, 0);            // the softmax warps moved Q into tensor memory
             for (int j = 0; j < 2 && j < ntiles && ok; ++j) {
                 ok = mbar_wait(&bk[j], 0);
                 if (ok) { k_waited = j + 1; fence_after(); issue_s(j); }
             }
             for (int j = 0; j < ntiles && ok; ++j) {
                 if (*abort_flag) { ok = false; break; }
-                // K stage of tile j is free once S_j is complete: fetch tile j + kStages
-                ok = mbar_wait(&bs[j & 1], (uint32_t)((j >> 1) & 1));
+                // P_j written: the softmax warps read S_j, so S_j is complete and the K stage
+                // of tile j is free: fetch K of tile j + kKStages
+                ok = mbar_wait(&bp[j & 1], (uint32_t)((j >> 1) & 1));
                 if (!ok) break;
-                if (j + kStages < ntiles) { load_k(j + kStages); k_issued = j + kStages + 1; }
-                // V stage of tile j - 2 is free once its P V is complete: fetch tile j + 1
-                if (j >= 2 && j + 1 < ntiles) {
-                    ok = mbar_wait(&bo[j & 1], (uint32_t)(((j - 2) >> 1) & 1));
-                    if (!ok) break;
-                    load_v(j + 1);
-                    v_issued = j + 2;
-                }
-                // O += P_j V_j once the softmax warps wrote P_j and V_j landed
-                ok = mbar_wait(&bp[j & 1], (uint32_t)((j >> 1) & 1)) &&
-                     mbar_wait(&bv[j % kStages], (uint32_t)((j / kStages) & 1));
+                if (j + kKStages < ntiles) { load_k(j + kKStages); k_issued = j + kKStages + 1; }
+                // O += P_j V_j
+                ok = mbar_wait(&bv[j % kVStages], (uint32_t)((j / kVStages) & 1));
                 if (!ok) break;
                 v_waited = j + 1;
                 fence_after();
                 issue_pv(j);
-                // S_{j+2} into S buffer j % 2 (read by the softmax warps: bp above)
                 if (j + 2 < ntiles) {
-                    ok = mbar_wait(&bk[(j + 2) % kStages], (uint32_t)(((j + 2) / kStages) & 1));
+                    // S_{j+2} overwrites P_j's buffer: wait for P V_j (which also frees the
+                    // V stage of tile j), then fetch V of tile j + 2 and issue S_{j+2}
+                    ok = mbar_wait(&bo[j & 1], (uint32_t)((j >> 1) & 1));
+                    if (!ok) break;
+                    load_v(j + 2);
+                    v_issued = j + 3;
+                    ok = mbar_wait(&bk[(j + 2) % kKStages], (uint32_t)(((j + 2) / kKStages) & 1));
                     if (!ok) break;
                     k_waited = j + 3;
                     fence_after();
@@ -308,13 +350,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 atomicOr(a.hdr, kErrWait);
                 // let every copy still in flight land before the CTA can exit
                 if (!q_waited) mbar_wait(bq, 0);
-                for (int t = k_waited; t < k_issued; ++t) mbar_wait(&bk[t % kStages], (uint32_t)((t / kStages) & 1));
-                for (int t = v_waited; t < v_issued; ++t) mbar_wait(&bv[t % kStages], (uint32_t)((t / kStages) & 1));
+                for (int t = k_waited; t < k_issued; ++t) mbar_wait(&bk[t % kKStages], (uint32_t)((t / kKStages) & 1));
+                for (int t = v_waited; t < v_issued; ++t) mbar_wait(&bv[t % kVStages], (uint32_t)((t / kVStages) & 1));
             }
         }
     } else {
         // ================= softmax warps: warp w serves rows 32 (w % 4) .. + 31 (its
-        // tensor-memory lanes) and keys 32 (w / 4) .. + 31 of every tile
+        // tensor-memory lanes) and keys 64 (w / 4) .. + 63 of every tile; the two warps of
+        // a row pair exchange their halves' maxima through shared memory
         const int lg = warp & 3, hf = warp >> 2;
         const int row = 32 * lg + lane;            // query row = tensor-memory lane
         const uint32_t lane_off = (uint32_t)(32 * lg) << 16;
@@ -322,34 +365,64 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool row_valid = row < rows;
         const int key_lo = a.W > 0 ? max(0, p - a.W + 1) : 0;
         const int key_lo_max = a.W > 0 ? max(0, p_last - a.W + 1) : 0;   // the CTA's largest key_lo
+        const int pair_bar = 1 + lg;               // named barrier of the pair (0 = __syncthreads)
         float m_ref = -INFINITY, l = 0.f;
         bool fail = false;
-        for (int j = 0; j < ntiles; ++j) {
-            bool w = mbar_wait(&bs[j & 1], (uint32_t)((j >> 1) & 1)) && !*abort_flag;
-            if (!__all_sync(0xffffffffu, w)) { fail = true; break; }
-            fence_after();
-            // both warps of a row pair read the whole tile, so they agree on its maximum
-            float sm[kBN / 2], so[kBN / 2];
-            const uint32_t tSj = tmem + 64 * (j & 1) + lane_off;
-            tmem_ld32(tSj + 32 * hf, sm);
-            tmem_ld32(tSj + 32 * (1 - hf), so);
-            const int kb = p_last + 1 - kBN * (j + 1);
-            const int km = kb + 32 * hf, ko = kb + 32 * (1 - hf);    // first key of each half
-            float mx = -INFINITY;
-            if (kb >= key_lo_max && kb + kBN - 1 <= p_first) {
-                // every key of the tile is visible to every row of the CTA
+        {
+            // this warp's half of its rows' query (dims 64 hf .. + 63, hi and lo) from the
+            // swizzled shared-memory tile into tensor memory, bf16 pairs along columns
+            const bool w = __all_sync(0xffffffffu, mbar_wait(bq, 0));
+            if (w) {
+                uint32_t qh[32], ql[32];
 #pragma unroll
-                for (int c = 0; c < kBN / 2; ++c) mx = fmaxf(mx, fmaxf(sm[c], so[c]));
+                for (int c = 0; c < 8; ++c) {
+                    const int off = hf * kHalfB + row * 128 + ((c ^ (row & 7)) * 16);
+                    const uint4 u = *reinterpret_cast<const uint4*>(sQ + off);
+                    const uint4 v = *reinterpret_cast<const uint4*>(sQlo + off);
+                    qh[4 * c] = u.x; qh[4 * c + 1] = u.y; qh[4 * c + 2] = u.z; qh[4 * c + 3] = u.w;
+                    ql[4 * c] = v.x; ql[4 * c + 1] = v.y; ql[4 * c + 2] = v.z; ql[4 * c + 3] = v.w;
+                }
+                tmem_st32u(tmem + kColQ + 32 * hf + lane_off, qh);
+                tmem_st32u(tmem + kColQlo + 32 * hf + lane_off, ql);
+                fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bqt);
             } else {
+                fail = true;                      // the producer gives up waiting for bqt
+            }
+            // the Q area becomes the exchange buffer once every warp has copied its part
+            fail = fail || !__all_sync(0xffffffffu, mbar_wait(bqt, 0));
+        }
+        for (int j = 0; j < ntiles; ++j) {
+            // (1) S_j complete; this warp's 64 scores of the row
+            bool w = !fail && mbar_wait(&bs[j & 1], (uint32_t)((j >> 1) & 1)) && !*abort_flag;
+            w = __all_sync(0xffffffffu, w);
+            float sm[kBN / 2];
+            float mx = -INFINITY;
+            const int kb = p_last + 1 - kBN * (j + 1) + 64 * hf;         // first key of this half
+            const uint32_t tSj = tmem + 128 * (j & 1) + 64 * hf + lane_off;
+            if (w) {
+                fence_after();
+                tmem_ld32(tSj, sm);
+                tmem_ld32(tSj + 32, sm + 32);
+                if (kb - 64 * hf >= key_lo_max && kb - 64 * hf + kBN - 1 <= p_first) {
+                    // every key of the tile is visible to every row of the CTA
 #pragma unroll
-                for (int c = 0; c < kBN / 2; ++c) {
-                    const bool vm = row_valid && km + c >= key_lo && km + c <= p;
-                    const bool vo = row_valid && ko + c >= key_lo && ko + c <= p;
-                    sm[c] = vm ? sm[c] : -INFINITY;
-                    mx = fmaxf(mx, fmaxf(sm[c], vo ? so[c] : -INFINITY));
+                    for (int c = 0; c < kBN / 2; ++c) mx = fmaxf(mx, sm[c]);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < kBN / 2; ++c) {
+                        const bool vis = row_valid && kb + c >= key_lo && kb + c <= p;
+                        sm[c] = vis ? sm[c] : -INFINITY;
+                        mx = fmaxf(mx, sm[c]);
+                    }
                 }
             }
-            // the reference maximum moves only when the tile exceeds it by more than kLazyMax
+            // (2) exchange the halves' maxima (and any failure) with the partner warp
+            xmax[((j & 1) * 2 + hf) * kBM + row] = mx;
+            if (pair_sync_or(pair_bar, !w)) { fail = true; break; }
+            mx = fmaxf(mx, xmax[((j & 1) * 2 + (1 - hf)) * kBM + row]);
+            // (3) the reference maximum moves only when the tile exceeds it by more than kLazyMax
             bool grow = false;
             float alpha = 1.f;
             if (mx > m_ref + kLazyMax) {           // also the first visible tile (m_ref = -inf)
@@ -366,43 +439,39 @@ __global__ void __launch_bounds__(kThreads, 1)
                 rs2 = __fadd2_rn(rs2, make_float2(sm[c], sm[c + 1]));
             }
             l = l * alpha + (rs2.x + rs2.y);
-            // P buffer j % 2 was last read by P V of tile j - 2; O may be rescaled only
-            // once P V of tile j - 1 is complete (tcgen05.ld/st: whole warps)
+            // (4) O may be rescaled only once P V of tile j - 1 is complete
+            // (tcgen05.ld/st: whole warps)
             const bool any_grow = __any_sync(0xffffffffu, grow);
-            bool w2 = j < 2 || mbar_wait(&bo[j & 1], (uint32_t)(((j - 2) >> 1) & 1));
-            if (any_grow) w2 = w2 && mbar_wait(&bo[(j - 1) & 1], (uint32_t)(((j - 1) >> 1) & 1));
-            if (!__all_sync(0xffffffffu, w2)) { fail = true; break; }
             if (any_grow) {
-                fence_after();
-                const float f = grow ? alpha : 1.f;
+                if (!__all_sync(0xffffffffu, mbar_wait(&bo[(j - 1) & 1], (uint32_t)(((j - 1) >> 1) & 1)))) {
+                    fail = true;                   // the partner learns at the next exchange
+                } else {
+                    fence_after();
+                    const float f = grow ? alpha : 1.f;
 #pragma unroll
-                for (int c = 0; c < kD / 2; c += 32) {
-                    float o[32];
-                    tmem_ld32(tO + lane_off + 64 * hf + c, o);
+                    for (int c = 0; c < kD / 2; c += 32) {
+                        float o[32];
+                        tmem_ld32(tO + lane_off + 64 * hf + c, o);
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] *= f;
-                    tmem_st32(tO + lane_off + 64 * hf + c, o);
+                        for (int e = 0; e < 32; ++e) o[e] *= f;
+                        tmem_st32(tO + lane_off + 64 * hf + c, o);
+                    }
                 }
             }
-            // this warp's 32 keys of the P row -> shared memory as hi and lo bf16 terms,
-            // K-major 128-byte swizzle
-            unsigned char* sPhi = sP + (j & 1) * 2 * kPTile;
+            if (fail) continue;                    // skip the write; the next exchange ends the loop
+            // (5) this warp's 64 keys of the P row over its own S columns: hi and lo bf16
+            // pairs (keys 64 hf + 2 e, + 1 in column e; lo 32 columns further)
+            uint32_t hi[32], lo2[32];
 #pragma unroll
-            for (int c = 0; c < kBN / 16; ++c) {
-                uint32_t hi[4], lo2[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 x = make_float2(sm[8 * c + 2 * e], sm[8 * c + 2 * e + 1]);
-                    const __nv_bfloat162 h2 = __floats2bfloat162_rn(x.x, x.y);
-                    const float2 r = __ffma2_rn(__bfloat1622float2(h2), make_float2(-1.f, -1.f), x);   // x - hi, exact
-                    hi[e] = *reinterpret_cast<const uint32_t*>(&h2);
-                    lo2[e] = pack_bf16(r.x, r.y);
-                }
-                const int off = row * 128 + (((4 * hf + c) ^ (row & 7)) * 16);
-                *reinterpret_cast<uint4*>(sPhi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                *reinterpret_cast<uint4*>(sPhi + kPTile + off) = make_uint4(lo2[0], lo2[1], lo2[2], lo2[3]);
+            for (int e = 0; e < 32; ++e) {
+                const float2 x = make_float2(sm[2 * e], sm[2 * e + 1]);
+                const __nv_bfloat162 h2 = __floats2bfloat162_rn(x.x, x.y);
+                const float2 r = __ffma2_rn(__bfloat1622float2(h2), make_float2(-1.f, -1.f), x);   // x - hi, exact
+                hi[e] = *reinterpret_cast<const uint32_t*>(&h2);
+                lo2[e] = pack_bf16(r.x, r.y);
             }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            tmem_st32u(tSj, hi);
+            tmem_st32u(tSj + 32, lo2);
             fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bp[j & 1]);
@@ -416,8 +485,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) atomicOr(a.hdr, kErrWait);
             *abort_flag = 1;
         }
-        // partial row sums meet in the (now idle) K stages
-        reinterpret_cast<float*>(sK)[hf * kBM + row] = l;
+        // partial row sums of the two halves meet in the (idle) Q lo area
+        reinterpret_cast<float*>(smem + OFF_QLO)[hf * kBM + row] = l;
     }
     __syncthreads();
     const bool aborted = *abort_flag != 0;
@@ -427,7 +496,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = 32 * lg + lane;
         const uint32_t lane_off = (uint32_t)(32 * lg) << 16;
         fence_after();
-        const float L = reinterpret_cast<const float*>(sK)[row] + reinterpret_cast<const float*>(sK)[kBM + row];
+        const float* lsum = reinterpret_cast<const float*>(smem + OFF_QLO);
+        const float L = lsum[row] + lsum[kBM + row];
         const float inv = L > 0.f ? 1.f / L : 0.f;
         const size_t orow = (((size_t)b * a.n + i0 + row) * a.Hq + hq) * kD + 64 * hf;
 #pragma unroll
