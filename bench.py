@@ -37,17 +37,21 @@ if ROOT not in sys.path:
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 CSRC = os.path.join(ROOT, "kv_cache_decode_ring_gb300", "csrc")
 
-# DRAM traffic (ncu dram__bytes_read.sum + dram__bytes_write.sum) per algorithmic byte of the
-# dominant kernel, from the captures summarised in profiles/; valid only while the kernel
-# source is the one captured (sha256 prefix), otherwise the JSON line reports null.
+# DRAM traffic (ncu dram__bytes_read.sum + dram__bytes_write.sum) of the dominant kernel
+# per byte of the bench's traffic basis (the decode call's algorithmic bytes; for the chunk
+# kernel the K/V bytes of the step), from the small-case captures summarised in profiles/;
+# valid only while the kernel source is the one captured (sha256 prefix), otherwise the
+# JSON line reports null.
 TRAFFIC_PER_BYTE = {
-    "full-cache-mha": ("decode_fast.cu", "7dea6b0b22669787", 273041152 / 268697600),
-    "sliding-window-gqa": ("decode_fast.cu", "7dea6b0b22669787", (1059193000 + 33679616) / 1059586048),
-    "int8-witness": ("int8.cu", "8825f47a8e965b16", (2420415000 + 135907584) / 2420342784),
+    "full-cache-mha": ("decode_fast.cu", "f13499b510292e2d", (268699392 + 4494080) / 268632064),
+    "sliding-window-gqa": ("decode_gqa.cu", "2239c895c0ccf520", (268109824 + 4902144) / 268148736),
+    "int8-witness": ("int8.cu", "c8b085cbc8257fc3", (302596864 + 4367104) / 302551040),
+    "bf16-at-int8-shape": ("decode_gqa.cu", "2239c895c0ccf520", (536982272 + 6691584) / 536907776),
+    "prefix-reuse": ("chunk.cu", "424df5ecd9751daa", (39883008 + 86784) / 22773760),
 }
 
 
-def traffic_per_launch(workload, bytes_per_launch):
+def traffic_per_launch(workload, basis_bytes):
     import hashlib
     entry = TRAFFIC_PER_BYTE.get(workload)
     if not entry:
@@ -56,7 +60,7 @@ def traffic_per_launch(workload, bytes_per_launch):
     with open(os.path.join(CSRC, src), "rb") as f:
         if hashlib.sha256(f.read()).hexdigest()[:16] != sha:
             return None
-    return int(ratio * bytes_per_launch)
+    return int(ratio * basis_bytes)
 FALLBACK_HBM_GBS = 6800.0
 METRIC = "decode-attention KV bytes/s (GB/s, % of HBM peak) and decode steps/s at 1 GB300"
 
@@ -174,6 +178,9 @@ class DecodeBench:
     def io_bytes(self):
         w = self.w
         return (2 * w.batch * w.n_q_heads * w.head_dim) * 2      # q read + out write (bf16)
+
+    def traffic_basis(self, attn_bytes):
+        return attn_bytes                                        # DRAM traffic scales with these
 
     def launches_per_step(self):
         return 3                                                 # append, split-K decode, combine
@@ -449,6 +456,10 @@ class ChunkBench(DecodeBench):
     def launches_per_step(self):
         return 5                                   # trim, append rows, advance, rotate q, attention
 
+    def traffic_basis(self, flops):
+        w = self.w                                 # the K/V rows a step's attention reads
+        return sum(c + self.n for c in self.cuts) * w.n_kv_heads * w.head_dim * 4
+
     def step(self, ev=None):
         self.cache.trim(self.cuts)
         if ev is not None:
@@ -670,7 +681,7 @@ def main():
             "config": bench.config(),
             "roofline": {"bound": bench.bound, "achieved": round(achieved, 2), "peak": peak, "unit": bench.unit,
                          "frac": round(achieved / peak, 4),
-                         "traffic": traffic_per_launch(args.workload, attn_bytes),
+                         "traffic": traffic_per_launch(args.workload, bench.traffic_basis(attn_bytes)),
                          "kernel": bench.kernel, "peak_kind": peak_kind,
                          "bytes_per_launch": int(attn_bytes), "avg_launch_ms": round(attn_avg_ms, 5)},
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
