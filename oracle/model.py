@@ -16,7 +16,10 @@ are stored as given.  The query is rotated the same way and kept in fp32.
 INT8 tier ([WITCERT] "频带酉性与双层证书" and "SGLang 生产级落地与闭环门控修复"):
 complete 16-position blocks of a contiguous cache hold INT8 codes with one fp32
 scale for K and one for V plus 16 fp16 witnesses per key row; the rows of the
-incomplete last block stay exact (bf16) with witness 0.
+incomplete last block stay exact (bf16) with witness 0.  A block restored by the
+gated fallback ("SGLang 生产级落地与闭环门控修复": swap in the lossless block
+from the full-precision backing store, zero its witnesses) is held exact as
+well, with residual 0 and witness 0.
 
 [LEAN]    "用Lean4形式化验证滑动窗口KV Cache的正确性" (framerc.cn/news/4505248)
 [PREFIX]  "LLM 機制實驗（五）：改了歷史，能否只重算變化的後綴？" (huhohoo.com)
@@ -71,6 +74,8 @@ class DecodeOracle:
         self.hk: List[List[np.ndarray]] = [[] for _ in range(B)]
         self.hv: List[List[np.ndarray]] = [[] for _ in range(B)]
         self.rings = [RingBuffer(capacity) for _ in range(B)] if layout == "ring" else None
+        # INT8 blocks restored to full precision: restored[b][kv_head] = set of block indices
+        self.restored = [[set() for _ in range(Hkv)] for _ in range(B)]
 
     # ------------------------------------------------------------ rows
     def stored_rows(self, x, positions) -> np.ndarray:
@@ -136,6 +141,8 @@ class DecodeOracle:
             del self.hv[b][cut:]
             if self.rings is not None:
                 self.rings[b].truncate(n - cut, cut % self.capacity)
+            for h in range(self.Hkv):          # restored blocks past the cut leave with their rows
+                self.restored[b][h] = {blk for blk in self.restored[b][h] if (blk + 1) * QBLOCK <= cut}
 
     # ------------------------------------------------------------ attention
     def _history(self, b, kv_head, lo=0, hi=None):
@@ -235,7 +242,15 @@ class DecodeOracle:
         hi = n if hi is None else hi
         K = np.stack([self.hk[b][p][h] for p in range(lo, hi)]) if hi > lo else np.zeros((0, self.d), np.float32)
         V = np.stack([self.hv[b][p][h] for p in range(lo, hi)]) if hi > lo else np.zeros((0, self.d), np.float32)
-        return int8_rows(K, V, lo, (n // QBLOCK) * QBLOCK)
+        return int8_rows(K, V, lo, (n // QBLOCK) * QBLOCK, self.restored[b][h])
+
+    def restore(self, blocks):
+        """Gated fallback ("SGLang 生产级落地与闭环门控修复"): hold the listed complete
+        blocks, (request, KV head, block index) triples, exact again from then on."""
+        for b, h, blk in blocks:
+            if (blk + 1) * QBLOCK > (self.length(b) // QBLOCK) * QBLOCK:
+                raise OracleError("arg", "block %d of request %d is not complete" % (blk, b))
+            self.restored[b][h].add(blk)
 
     def decode_int8(self, q, heads=None):
         """INT8-tier decode of the newest token for the listed (b, query head) pairs
@@ -251,19 +266,21 @@ class DecodeOracle:
             h = hq // self.g
             K = np.stack([self.hk[b][p][h] for p in range(lo_blk, t + 1)])
             V = np.stack([self.hv[b][p][h] for p in range(lo_blk, t + 1)])
-            res[(b, hq)] = int8_decode_one(qf, K, V, lo_blk, t, self.window, (self.length(b) // QBLOCK) * QBLOCK)
+            res[(b, hq)] = int8_decode_one(qf, K, V, lo_blk, t, self.window, (self.length(b) // QBLOCK) * QBLOCK,
+                                           self.restored[b][h])
         return res
 
 
-def int8_rows(K, V, p0, nfull):
+def int8_rows(K, V, p0, nfull, restored=()):
     """Rows at positions p0.. of one (request, KV head) as the INT8 tier holds them.
 
     ``K``, ``V``: [n, d] exact stored rows (fp32 values of the bf16 cache); ``p0`` a
-    block boundary; positions below ``nfull`` lie in complete blocks.  Returns
-    (K_deq, V_deq, K_exact, resid, wit_values), all fp64: complete blocks
-    dequantized (code * s, exact in fp64) with their key residuals and witness
-    values; the exact tail rows with residual 0 and witness 0
-    ([WITCERT] "频带酉性与双层证书"; "SGLang 生产级落地与闭环门控修复").
+    block boundary; positions below ``nfull`` lie in complete blocks; ``restored``
+    holds the block indices (position // 16) brought back to full precision by the
+    gated fallback.  Returns (K_deq, V_deq, K_exact, resid, wit_values), all fp64:
+    complete blocks dequantized (code * s, exact in fp64) with their key residuals
+    and witness values; the exact tail rows and restored blocks with residual 0 and
+    witness 0 ([WITCERT] "频带酉性与双层证书"; "SGLang 生产级落地与闭环门控修复").
     """
     n, d = K.shape
     assert p0 % QBLOCK == 0
@@ -274,6 +291,8 @@ def int8_rows(K, V, p0, nfull):
     for r0 in range(0, n, QBLOCK):
         if p0 + r0 + QBLOCK > nfull or r0 + QBLOCK > n:
             break
+        if (p0 + r0) // QBLOCK in restored:
+            continue
         sl = slice(r0, r0 + QBLOCK)
         sK, cK = nm.quantize_block(K[sl])
         sV, cV = nm.quantize_block(V[sl])
@@ -284,7 +303,7 @@ def int8_rows(K, V, p0, nfull):
     return Kd, Vd, K.astype(np.float64), R, Wt
 
 
-def int8_decode_one(qf, K, V, p0, t, window, nfull):
+def int8_decode_one(qf, K, V, p0, t, window, nfull, restored=()):
     """INT8-tier decode of one query row over rows p0..t of one KV head, fp64.
 
     Returns {"out": attention over the dequantized rows, "out_exact": over the
@@ -296,7 +315,7 @@ def int8_decode_one(qf, K, V, p0, t, window, nfull):
     d = K.shape[1]
     bw = d // NBANDS
     q64 = np.asarray(qf, dtype=np.float64)
-    Kd, Vd, Kx, R, W = int8_rows(K, V, p0, nfull)
+    Kd, Vd, Kx, R, W = int8_rows(K, V, p0, nfull, restored)
     Vx = V.astype(np.float64)
     out = nm.attend(q64, Kd, Vd, t, window, p0=p0)[0]
     out_exact = nm.attend(q64, Kx, Vx, t, window, p0=p0)[0]
@@ -310,3 +329,36 @@ def int8_decode_one(qf, K, V, p0, t, window, nfull):
     return {"out": out, "out_exact": out_exact, "c": c[vis], "eps": eps[vis],
             "tv": 0.5 * np.abs(p_ex - p_deq).sum(), "cmax": float(c[vis].max()) if c[vis].size else 0.0,
             "q": qf}
+
+
+# ---------------------------------------------------------------------- gated fallback
+def block_risk(c_heads, nfull):
+    """Risk of every complete block of one (request, KV head): the largest c_t of its
+    16 tokens over the KV head's query heads ("SGLang 生产级落地与闭环门控修复": a
+    block whose accumulated risk crosses the water line is swapped back in).
+
+    ``c_heads``: [g, n] c_t of positions 0..n-1 for the g query heads; returns
+    [nfull // 16] floats.
+    """
+    c = np.asarray(c_heads, dtype=np.float64)
+    nb = nfull // QBLOCK
+    return np.array([c[:, blk * QBLOCK:(blk + 1) * QBLOCK].max() if c.size else 0.0 for blk in range(nb)])
+
+
+def gate_select(risk, tau, budget=None):
+    """Blocks to restore: every (request, KV head, block) whose risk gives
+    tanh(risk) > tau, highest risk first (ties: smaller (request, head, block)),
+    cut to ``budget`` blocks ("SGLang 生产级落地与闭环门控修复": triggered by the
+    certificate, ranked by risk score and truncated).
+
+    ``risk``: {(b, h): [nblk] array}.
+    """
+    cand = []
+    for (b, h), r in sorted(risk.items()):
+        for blk, x in enumerate(np.asarray(r, dtype=np.float64)):
+            if math.tanh(x) > tau:
+                cand.append((-x, b, h, blk))
+    cand.sort()
+    if budget is not None:
+        cand = cand[:budget]
+    return [(b, h, blk) for _, b, h, blk in cand]
