@@ -68,7 +68,7 @@ typedef struct {
                              KVC_RING: slot = position mod W, capacity = W
                              ([LEAN] §3.4 ring buffer, §2.3 lastWindow) */
     int32_t kv_quant;     /* KVC_QUANT_NONE, or KVC_QUANT_INT8 (bf16 contiguous
-                             caches only; [WITCERT]) */
+                             caches with window 0 only; [WITCERT]) */
     int32_t batch;        /* B >= 1 requests */
     int32_t n_q_heads;    /* Hq >= 1 */
     int32_t n_kv_heads;   /* Hkv >= 1, Hq % Hkv == 0; query head h reads KV head h / (Hq/Hkv) */
@@ -84,6 +84,8 @@ typedef struct {
     int32_t out_dtype;    /* attention outputs: 0 = the cache dtype, else KVC_F32 or
                              KVC_BF16 (+1 is added so that 0 keeps the default):
                              pass KVC_F32 + 1 or KVC_BF16 + 1 */
+    int32_t int8_exact_blocks; /* INT8 only: capacity of the pool of blocks restored
+                             to full precision by kvc_int8_restore (0 = none) */
 } kvc_config;
 
 /* Bytes of the device state buffer for `cfg` (cache rows, positions,
@@ -193,6 +195,43 @@ int kvc_trim(kvc_t h, const int32_t* h_cut, kvc_stream_t stream);
 int kvc_chunk_attn(kvc_t h, const void* d_q, const void* d_k, const void* d_v, int32_t n,
                    void* d_out, kvc_stream_t stream);
 
+/* ---- gated fallback of the INT8 tier ----------------------------------
+ * [WITCERT] "SGLang 生产级落地与闭环门控修复": once the risk of a head or a block
+ * crosses the water line, the lossless block is swapped in from the full-precision
+ * backing store and its witness is zeroed; in the saturated zone blocks are ranked by
+ * risk and truncated.  Three steps, each usable alone:
+ *   kvc_int8_block_risk  (device) the risk of every complete block from a decode's c_t;
+ *   kvc_int8_gate        (host)   which blocks to restore;
+ *   kvc_int8_restore     (device) restore them.
+ * A restored block is served exactly (bf16) from a pool inside the state buffer
+ * (kvc_config.int8_exact_blocks entries); its tokens get c_t = 0 from then on.  A
+ * trim that drops a restored block returns its pool entry. */
+
+/* d_risk[b][h][k] = max over the query heads of KV head h and the 16 tokens of block
+ * k of d_ct[b][hq][t] (the per-token bound of the last kvc_decode_attn on this cache,
+ * [B][Hq][capacity] fp32), for every complete block of request b; 0 elsewhere.
+ * d_risk: fp32 [B][Hkv][capacity/16], device.  Async on `stream`.
+ * KVC_ERR_ARG: not an INT8 cache, or a null pointer. */
+int kvc_int8_block_risk(kvc_t h, const float* d_ct, float* d_risk, kvc_stream_t stream);
+
+/* Host only.  Every (request, KV head, block) of h_risk ([B][Hkv][nblk] fp32, host)
+ * with tanh(risk) > tau (both in double), highest risk first, ties broken by the smaller
+ * (request, head, block); at most max_blocks of them into h_sel ([max_blocks][3]
+ * int32 triples); their number into *h_n_sel.  KVC_ERR_ARG: bad sizes or pointers. */
+int kvc_int8_gate(const float* h_risk, int32_t B, int32_t Hkv, int32_t nblk, double tau, int32_t max_blocks,
+                  int32_t* h_sel, int32_t* h_n_sel);
+
+/* Restore the n blocks listed in h_blocks ([n][3] int32 (request, KV head, block),
+ * host): copy each block's 16 rows of K and V from the full-precision backing store
+ * d_k_full / d_v_full (bf16 [B][Hkv][capacity][d], device: the rows an exact cache
+ * holds, keys rotated) into the pool, zero the block's witnesses, and serve its
+ * tokens from the pool in every later decode.  Blocks already restored are skipped.
+ * KVC_ERR_ARG: not an INT8 cache, null pointer, or a block that is not complete;
+ * KVC_ERR_CAPACITY: the pool has too few free entries, or a (request, KV head) would
+ * hold more than 1024 restored blocks (nothing is restored then). */
+int kvc_int8_restore(kvc_t h, const int32_t* h_blocks, int32_t n, const void* d_k_full, const void* d_v_full,
+                     kvc_stream_t stream);
+
 /* Bit-exact readback of one state array for tests and debug asserts
  * ([LEAN] §6.3: export the cache and compare it with the specification).
  * Copies into h_dst (exactly kvc_export_bytes() bytes) and waits for `stream`. */
@@ -208,7 +247,9 @@ enum {
     KVC_EXPORT_SV = 7,
     KVC_EXPORT_WITNESS = 8,       /* fp16 [B][Hkv][capacity][16]          (INT8) */
     KVC_EXPORT_KTAIL = 9,         /* bf16 [B][Hkv][16][d] exact tail rows (INT8) */
-    KVC_EXPORT_VTAIL = 10
+    KVC_EXPORT_VTAIL = 10,
+    KVC_EXPORT_XMAP = 11          /* int32 [B][Hkv][capacity/16]: pool entry of a restored
+                                     block, -1 = quantized (INT8) */
 };
 int kvc_export_bytes(kvc_t h, int32_t which, size_t* bytes);
 int kvc_export(kvc_t h, int32_t which, void* h_dst, size_t bytes, kvc_stream_t stream);

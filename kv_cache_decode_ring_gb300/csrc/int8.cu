@@ -18,7 +18,9 @@
 // streams its 16 blocks through three shared-memory stages (codes and witnesses
 // by bulk copy on the stage's mbarrier), so copies overlap arithmetic; online
 // softmax over the warp's blocks, warps merged at the end.  One extra split
-// handles the exact tail rows (c_t = 0 there).
+// handles the exact rows (c_t = 0 there): the tail of the incomplete block and the
+// blocks restored to full precision by the gated fallback (int8_gate.cu), which
+// the quantized splits skip.
 //
 // Both contractions of a block run on the tensor cores as fp16 MMAs with fp32
 // accumulation (m16n8k16), operands built in registers:
@@ -64,6 +66,9 @@ struct Int8Args {
     const __half* wit;
     const __nv_bfloat16* ktail;
     const __nv_bfloat16* vtail;
+    const int32_t* xmap;            // [B][Hkv][S/16] pool entry of a restored block, -1 = quantized
+    const int32_t* xn;              // [B][Hkv] restored blocks
+    const __nv_bfloat16* xpool;     // [entry][2][16][d] K and V rows of restored blocks
     const int32_t* next_pos;
     const float2* rope;
     float2* part_ml;
@@ -81,10 +86,11 @@ struct Int8CombineArgs {
     const float* part_acc;
     const float* part_c;
     const int32_t* next_pos;
+    const int32_t* xn;              // [B][Hkv] restored blocks (they join the exact-rows split)
     void* out;
     float* cmax;        // nullable
     float* tanh_out;    // nullable
-    int B, Hq, d, max_splits, out_bf16;
+    int B, Hq, Hkv, d, max_splits, out_bf16;
 };
 
 // D (16x8, fp32) += A (16x16, fp16, row) . B (16x8, fp16, col)
@@ -170,16 +176,22 @@ __global__ void __launch_bounds__(kWarps * 32, D >= 128 ? 3 : 4) int8_decode_ker
     const int nfull = len & ~(kQBlock - 1);
     const int nsq = (nfull + kInt8Split - 1) / kInt8Split;
     const bool tail_split = split == nsq;
-    if (split > nsq || (tail_split && len == nfull)) return;
+    if (split > nsq || (tail_split && len == nfull && a.xn[(size_t)b * a.Hkv + kvh] == 0)) return;
     const int t_q = len - 1;
     const size_t rowq0 = (size_t)b * a.Hq + (size_t)kvh * G;    // first query row of the group
 
     if (tail_split) {
-        // ---- exact bf16 tail rows [nfull, len): warp 0, lane = row; c_t = 0
+        // ---- exact rows, served in bf16 with c_t = 0: the tail [nfull, len) and every
+        // block restored by the gated fallback.  Warp 0, 32 rows at a time, online
+        // softmax over the chunks; lane = row for the scores, lane = dims for P.V.
         if (warp != 0) return;
+        const size_t bh = (size_t)b * a.Hkv + kvh;
         const int nt = len - nfull;
+        const int nblk = a.S / kQBlock;
         float* qs = reinterpret_cast<float*>(smem);          // [G][D] scaled query
-        float* pt = qs + G * D;                              // [16][G]
+        float* pt = qs + G * D;                              // [32][G] weights of a chunk
+        int* xk = reinterpret_cast<int*>(pt + 32 * G);       // [nx] restored block index
+        int* xe = xk + kMaxRestored;                         // [nx] its pool entry
         for (int idx = lane; idx < G * D / 2; idx += 32) {
             const int h = idx / (D / 2), i = idx % (D / 2);
             const size_t off = (rowq0 + h) * D + 2 * i;
@@ -189,41 +201,95 @@ __global__ void __launch_bounds__(kWarps * 32, D >= 128 ? 3 : 4) int8_decode_ker
             qs[h * D + 2 * i] = y0 * a.scale_log2;
             qs[h * D + 2 * i + 1] = y1 * a.scale_log2;
         }
+        // restored blocks of this (request, KV head), in block order
+        int nx = 0;
+        if (a.xn[bh] > 0) {
+            for (int k0 = 0; k0 < nfull / kQBlock; k0 += 32) {
+                const int k = k0 + lane;
+                const int e = k < nfull / kQBlock ? a.xmap[bh * nblk + k] : -1;
+                const unsigned m = __ballot_sync(0xffffffffu, e >= 0);
+                const int at = nx + __popc(m & ((1u << lane) - 1));
+                if (e >= 0 && at < kMaxRestored) { xk[at] = k; xe[at] = e; }
+                nx = min(kMaxRestored, nx + __popc(m));
+            }
+        }
         __syncwarp();
-        const size_t tail0 = ((size_t)b * a.Hkv + kvh) * kQBlock * D;
-        float s[G];
+        const size_t tail0 = bh * kQBlock * D;
+        const int total = nt + kQBlock * nx;
+        // row r: tail row r, or row (r - nt) % 16 of restored block (r - nt) / 16
+        auto row_ptr = [&](int r, bool v) -> const __nv_bfloat16* {
+            if (r < nt) return (v ? a.vtail : a.ktail) + tail0 + (size_t)r * D;
+            const int j = (r - nt) / kQBlock, rr = (r - nt) % kQBlock;
+            return a.xpool + ((size_t)xe[j] * 2 + (v ? 1 : 0)) * kQBlock * D + (size_t)rr * D;
+        };
+        auto row_pos = [&](int r) { return r < nt ? nfull + r : xk[(r - nt) / kQBlock] * kQBlock + (r - nt) % kQBlock; };
+        float m[G], l[G], acc[G][D / 32];
 #pragma unroll
-        for (int h = 0; h < G; ++h) s[h] = -INFINITY;
-        if (lane < nt) {
+        for (int h = 0; h < G; ++h) {
+            m[h] = -INFINITY; l[h] = 0.f;
+#pragma unroll
+            for (int e = 0; e < D / 32; ++e) acc[h][e] = 0.f;
+        }
+        for (int r0 = 0; r0 < total; r0 += 32) {
+            const int r = r0 + lane;
+            const bool valid = r < total;
+            float s[G];
+#pragma unroll
+            for (int h = 0; h < G; ++h) s[h] = -INFINITY;
+            if (valid) {
+                const __nv_bfloat16* kr = row_ptr(r, false);
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    float x = 0.f;
+                    for (int i = 0; i < D; ++i) x = fmaf(qs[h * D + i], __bfloat162float(kr[i]), x);
+                    s[h] = x;
+                }
+                if (a.ct) {
+                    const int p = row_pos(r);
+#pragma unroll
+                    for (int h = 0; h < G; ++h) a.ct[(rowq0 + h) * a.S + p] = 0.f;
+                }
+            }
+            float alpha[G];
 #pragma unroll
             for (int h = 0; h < G; ++h) {
-                float acc = 0.f;
-                for (int i = 0; i < D; ++i) acc = fmaf(qs[h * D + i], __bfloat162float(a.ktail[tail0 + lane * D + i]), acc);
-                s[h] = acc;
+                float mx = s[h];
+                for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                const float mn = fmaxf(m[h], mx);                 // finite: the chunk has a valid row
+                alpha[h] = exp2f(m[h] - mn);                      // 0 on the first chunk
+                const float p = valid ? exp2f(s[h] - mn) : 0.f;
+                float ls = p;
+                for (int o = 16; o; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
+                l[h] = l[h] * alpha[h] + ls;
+                m[h] = mn;
+                pt[lane * G + h] = p;
             }
+            __syncwarp();
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+#pragma unroll
+                for (int e = 0; e < D / 32; ++e) acc[h][e] *= alpha[h];
+            const int nrow = min(32, total - r0);
+            for (int j = 0; j < nrow; ++j) {
+                const __nv_bfloat16* vr = row_ptr(r0 + j, true);
+#pragma unroll
+                for (int e = 0; e < D / 32; ++e) {
+                    const float v = __bfloat162float(vr[lane + 32 * e]);
+#pragma unroll
+                    for (int h = 0; h < G; ++h) acc[h][e] = fmaf(pt[j * G + h], v, acc[h][e]);
+                }
+            }
+            __syncwarp();
         }
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-            float mx = s[h];
-            for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-            const float p = lane < nt ? exp2f(s[h] - mx) : 0.f;
-            float l = p;
-            for (int o = 16; o; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-            if (lane < kQBlock) pt[lane * G + h] = p;
             const size_t row = (rowq0 + h) * a.max_splits + split;
-            if (lane == 0) { a.part_ml[row] = make_float2(mx, l); a.part_c[row] = 0.f; }
-            if (a.ct && lane < nt) a.ct[(rowq0 + h) * a.S + nfull + lane] = 0.f;
-        }
-        __syncwarp();
-        for (int idx = lane; idx < G * D; idx += 32) {
-            const int h = idx / D, i = idx % D;
-            float acc = 0.f;
-            for (int t = 0; t < nt; ++t) acc = fmaf(pt[t * G + h], __bfloat162float(a.vtail[tail0 + t * D + i]), acc);
-            a.part_acc[((rowq0 + h) * a.max_splits + split) * D + i] = acc;
+            if (lane == 0) { a.part_ml[row] = make_float2(m[h], l[h]); a.part_c[row] = 0.f; }
+#pragma unroll
+            for (int e = 0; e < D / 32; ++e) a.part_acc[row * D + lane + 32 * e] = acc[h][e];
         }
         return;
     }
-
 
     // ---- quantized split ----------------------------------------------------
     const size_t bh = (size_t)b * a.Hkv + kvh;
@@ -256,9 +322,11 @@ __global__ void __launch_bounds__(kWarps * 32, D >= 128 ? 3 : 4) int8_decode_ker
     // block scales of this warp's tiles: lane i < 16 holds tile i's s_K and its s_V
     // relative to the warp's largest s_V, times 2^7
     float skv = 0.f, rvv = 0.f;
+    int xmv = -1;                                     // >= 0: restored, served by the exact split
     if (lane < kTilesPerWarp && tile_ok(lane)) {
         skv = a.sk[bh * (a.S / kQBlock) + tile_blk(lane)];
         rvv = a.sv[bh * (a.S / kQBlock) + tile_blk(lane)];
+        xmv = a.xmap[bh * (a.S / kQBlock) + tile_blk(lane)];
     }
     float svmax = rvv;
 #pragma unroll
@@ -358,113 +426,116 @@ __global__ void __launch_bounds__(kWarps * 32, D >= 128 ? 3 : 4) int8_decode_ker
         const float s_k = __shfl_sync(0xffffffffu, skv, i);
         const float r_v = __shfl_sync(0xffffffffu, rvv, i);
 
-        // ---- scores S^T = K Q^T: rows g and g + 8 of the block, D/64 16-byte
-        // chunks each (at d = 128 odd rows hold their chunk pairs swapped)
-        uint32_t kw0[C::KW], kw1[C::KW];
-#pragma unroll
-        for (int j = 0; j < C::KW / 4; ++j) {
-            const int ch = (C::KW / 4) * qd + (D == 128 ? (j ^ (g & 1)) : j);
-            const uint4 u0 = *reinterpret_cast<const uint4*>(tK + g * D + ch * 16);
-            const uint4 u1 = *reinterpret_cast<const uint4*>(tK + (g + 8) * D + ch * 16);
-            kw0[4 * j] = u0.x; kw0[4 * j + 1] = u0.y; kw0[4 * j + 2] = u0.z; kw0[4 * j + 3] = u0.w;
-            kw1[4 * j] = u1.x; kw1[4 * j + 1] = u1.y; kw1[4 * j + 2] = u1.z; kw1[4 * j + 3] = u1.w;
-        }
-        float sacc[C::NT][4];
-#pragma unroll
-        for (int nt = 0; nt < C::NT; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) sacc[nt][e] = 0.f;
-#pragma unroll
-        for (int s = 0; s < C::KS; ++s) {
-            uint32_t a0, a1, a2, a3;
-            codes_to_half2(kw0[s], a0, a2);
-            codes_to_half2(kw1[s], a1, a3);
-#pragma unroll
-            for (int nt = 0; nt < C::NT; ++nt) mma_f16(sacc[nt], a0, a1, a2, a3, qb[nt][s][0], qb[nt][s][1]);
-        }
+        // a block restored by the gated fallback is served by the exact-rows split
+        if (__shfl_sync(0xffffffffu, xmv, i) < 0) {
+            // ---- scores S^T = K Q^T: rows g and g + 8 of the block, D/64 16-byte
+            // chunks each (at d = 128 odd rows hold their chunk pairs swapped)
+            uint32_t kw0[C::KW], kw1[C::KW];
+    #pragma unroll
+            for (int j = 0; j < C::KW / 4; ++j) {
+                const int ch = (C::KW / 4) * qd + (D == 128 ? (j ^ (g & 1)) : j);
+                const uint4 u0 = *reinterpret_cast<const uint4*>(tK + g * D + ch * 16);
+                const uint4 u1 = *reinterpret_cast<const uint4*>(tK + (g + 8) * D + ch * 16);
+                kw0[4 * j] = u0.x; kw0[4 * j + 1] = u0.y; kw0[4 * j + 2] = u0.z; kw0[4 * j + 3] = u0.w;
+                kw1[4 * j] = u1.x; kw1[4 * j + 1] = u1.y; kw1[4 * j + 2] = u1.z; kw1[4 * j + 3] = u1.w;
+            }
+            float sacc[C::NT][4];
+    #pragma unroll
+            for (int nt = 0; nt < C::NT; ++nt)
+    #pragma unroll
+                for (int e = 0; e < 4; ++e) sacc[nt][e] = 0.f;
+    #pragma unroll
+            for (int s = 0; s < C::KS; ++s) {
+                uint32_t a0, a1, a2, a3;
+                codes_to_half2(kw0[s], a0, a2);
+                codes_to_half2(kw1[s], a1, a3);
+    #pragma unroll
+                for (int nt = 0; nt < C::NT; ++nt) mma_f16(sacc[nt], a0, a1, a2, a3, qb[nt][s][0], qb[nt][s][1]);
+            }
 
-        // ---- online softmax of the lane's head over tokens g, g + 8; weights
-        // times r_v into the P^T staging as fp16 hi + lo; and the bound
-        float alpha[C::HPL];
-        bool rescale = false;
-#pragma unroll
-        for (int nt = 0; nt < C::HPL; ++nt) {
-            const float f = fq[nt] * s_k;
-            const float s0 = (sacc[nt][0] + sacc[nt][1]) * f;
-            const float s1 = (sacc[nt][2] + sacc[nt][3]) * f;
-            float bm = fmaxf(s0, s1);
-            bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
-            bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
-            bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
-            const float mn = bm > m_w[nt] + kLazyMax ? bm : m_w[nt];
-            alpha[nt] = ex2(m_w[nt] - mn);            // 0 while the maximum was -inf
-            rescale |= alpha[nt] != 1.f;
-            m_w[nt] = mn;
-            const float e0 = ex2(s0 - mn), e1 = ex2(s1 - mn);
-            l_w[nt] = fmaf(l_w[nt], alpha[nt], e0 + e1);
-            __half h0, l0, h1, l1;
-            split_half(e0 * r_v, h0, l0);
-            split_half(e1 * r_v, h1, l1);
-            unsigned char* pt = myPm + nt * C::PROWB;
-            *reinterpret_cast<__half*>(pt + prow(2 * qd) + 2 * g) = h0;
-            *reinterpret_cast<__half*>(pt + prow(2 * qd + 1) + 2 * g) = l0;
-            *reinterpret_cast<__half*>(pt + prow(2 * qd) + 2 * (g + 8)) = h1;
-            *reinterpret_cast<__half*>(pt + prow(2 * qd + 1) + 2 * (g + 8)) = l1;
+            // ---- online softmax of the lane's head over tokens g, g + 8; weights
+            // times r_v into the P^T staging as fp16 hi + lo; and the bound
+            float alpha[C::HPL];
+            bool rescale = false;
+    #pragma unroll
+            for (int nt = 0; nt < C::HPL; ++nt) {
+                const float f = fq[nt] * s_k;
+                const float s0 = (sacc[nt][0] + sacc[nt][1]) * f;
+                const float s1 = (sacc[nt][2] + sacc[nt][3]) * f;
+                float bm = fmaxf(s0, s1);
+                bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
+                bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
+                bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
+                const float mn = bm > m_w[nt] + kLazyMax ? bm : m_w[nt];
+                alpha[nt] = ex2(m_w[nt] - mn);            // 0 while the maximum was -inf
+                rescale |= alpha[nt] != 1.f;
+                m_w[nt] = mn;
+                const float e0 = ex2(s0 - mn), e1 = ex2(s1 - mn);
+                l_w[nt] = fmaf(l_w[nt], alpha[nt], e0 + e1);
+                __half h0, l0, h1, l1;
+                split_half(e0 * r_v, h0, l0);
+                split_half(e1 * r_v, h1, l1);
+                unsigned char* pt = myPm + nt * C::PROWB;
+                *reinterpret_cast<__half*>(pt + prow(2 * qd) + 2 * g) = h0;
+                *reinterpret_cast<__half*>(pt + prow(2 * qd + 1) + 2 * g) = l0;
+                *reinterpret_cast<__half*>(pt + prow(2 * qd) + 2 * (g + 8)) = h1;
+                *reinterpret_cast<__half*>(pt + prow(2 * qd + 1) + 2 * (g + 8)) = l1;
 
-            // bound of tokens g, g + 8 for head hq, every operation rounded up
-            const int hq = 4 * nt + qd;
-            const float4* nq = reinterpret_cast<const float4*>(sNQ + min(hq, G - 1) * 20);
-            float cb[2];
-#pragma unroll
-            for (int tt = 0; tt < 2; ++tt) {
-                float2 c2 = make_float2(0.f, 0.f);
-#pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    const uint4 u = tW[(g + 8 * tt) * 2 + c];
-                    const float4 na = nq[2 * c], nb = nq[2 * c + 1];
-                    c2 = __ffma2_ru(make_float2(na.x, na.y), __half22float2(*reinterpret_cast<const __half2*>(&u.x)), c2);
-                    c2 = __ffma2_ru(make_float2(na.z, na.w), __half22float2(*reinterpret_cast<const __half2*>(&u.y)), c2);
-                    c2 = __ffma2_ru(make_float2(nb.x, nb.y), __half22float2(*reinterpret_cast<const __half2*>(&u.z)), c2);
-                    c2 = __ffma2_ru(make_float2(nb.z, nb.w), __half22float2(*reinterpret_cast<const __half2*>(&u.w)), c2);
+                // bound of tokens g, g + 8 for head hq, every operation rounded up
+                const int hq = 4 * nt + qd;
+                const float4* nq = reinterpret_cast<const float4*>(sNQ + min(hq, G - 1) * 20);
+                float cb[2];
+    #pragma unroll
+                for (int tt = 0; tt < 2; ++tt) {
+                    float2 c2 = make_float2(0.f, 0.f);
+    #pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        const uint4 u = tW[(g + 8 * tt) * 2 + c];
+                        const float4 na = nq[2 * c], nb = nq[2 * c + 1];
+                        c2 = __ffma2_ru(make_float2(na.x, na.y), __half22float2(*reinterpret_cast<const __half2*>(&u.x)), c2);
+                        c2 = __ffma2_ru(make_float2(na.z, na.w), __half22float2(*reinterpret_cast<const __half2*>(&u.y)), c2);
+                        c2 = __ffma2_ru(make_float2(nb.x, nb.y), __half22float2(*reinterpret_cast<const __half2*>(&u.z)), c2);
+                        c2 = __ffma2_ru(make_float2(nb.z, nb.w), __half22float2(*reinterpret_cast<const __half2*>(&u.w)), c2);
+                    }
+                    cb[tt] = __fmul_ru(__fadd_ru(c2.x, c2.y), a.inv_sqrt_d_up);
                 }
-                cb[tt] = __fmul_ru(__fadd_ru(c2.x, c2.y), a.inv_sqrt_d_up);
+                c_w[nt] = fmaxf(c_w[nt], fmaxf(cb[0], cb[1]));
+                if (a.ct && hq < G) {
+                    a.ct[(rowq0 + hq) * a.S + p0 + g] = cb[0];
+                    a.ct[(rowq0 + hq) * a.S + p0 + g + 8] = cb[1];
+                }
             }
-            c_w[nt] = fmaxf(c_w[nt], fmaxf(cb[0], cb[1]));
-            if (a.ct && hq < G) {
-                a.ct[(rowq0 + hq) * a.S + p0 + g] = cb[0];
-                a.ct[(rowq0 + hq) * a.S + p0 + g + 8] = cb[1];
+            if (__any_sync(0xffffffffu, rescale) && i > 0) {     // at i = 0 the accumulators are 0
+    #pragma unroll
+                for (int mt = 0; mt < C::KS; ++mt)
+    #pragma unroll
+                    for (int nt = 0; nt < C::NT; ++nt)
+    #pragma unroll
+                        for (int e = 0; e < 4; ++e) acc[mt][nt][e] *= alpha[nt];
             }
-        }
-        if (__any_sync(0xffffffffu, rescale) && i > 0) {     // at i = 0 the accumulators are 0
-#pragma unroll
-            for (int mt = 0; mt < C::KS; ++mt)
-#pragma unroll
-                for (int nt = 0; nt < C::NT; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) acc[mt][nt][e] *= alpha[nt];
-        }
-        __syncwarp();
+            __syncwarp();
 
-        // ---- P.V: O^T += V^T P^T; B operand = P^T column g, tokens 4 qd .. + 3
-        uint2 pb[C::NT];
-#pragma unroll
-        for (int nt = 0; nt < C::NT; ++nt)
-            pb[nt] = *reinterpret_cast<const uint2*>(myPm + nt * C::PROWB + prow(g) + 8 * qd);
-        constexpr int CPR = D / 32;                  // 16-byte chunks of the lane's V run
-        const int swz = (lane / (8 / CPR)) % CPR;
-        uint32_t vw[C::VW];
-#pragma unroll
-        for (int j = 0; j < CPR; ++j) {
-            const uint4 u = *reinterpret_cast<const uint4*>(tV + lane * (D / 2) + ((j ^ swz) << 4));
-            vw[4 * j] = u.x; vw[4 * j + 1] = u.y; vw[4 * j + 2] = u.z; vw[4 * j + 3] = u.w;
-        }
-#pragma unroll
-        for (int mt = 0; mt < C::KS; ++mt) {
-            uint32_t a0, a1, a2, a3;
-            codes_to_half2(vw[2 * mt], a0, a2);           // dim 16 mt + g
-            codes_to_half2(vw[2 * mt + 1], a1, a3);       // dim 16 mt + 8 + g
-#pragma unroll
-            for (int nt = 0; nt < C::NT; ++nt) mma_f16(acc[mt][nt], a0, a1, a2, a3, pb[nt].x, pb[nt].y);
+            // ---- P.V: O^T += V^T P^T; B operand = P^T column g, tokens 4 qd .. + 3
+            uint2 pb[C::NT];
+    #pragma unroll
+            for (int nt = 0; nt < C::NT; ++nt)
+                pb[nt] = *reinterpret_cast<const uint2*>(myPm + nt * C::PROWB + prow(g) + 8 * qd);
+            constexpr int CPR = D / 32;                  // 16-byte chunks of the lane's V run
+            const int swz = (lane / (8 / CPR)) % CPR;
+            uint32_t vw[C::VW];
+    #pragma unroll
+            for (int j = 0; j < CPR; ++j) {
+                const uint4 u = *reinterpret_cast<const uint4*>(tV + lane * (D / 2) + ((j ^ swz) << 4));
+                vw[4 * j] = u.x; vw[4 * j + 1] = u.y; vw[4 * j + 2] = u.z; vw[4 * j + 3] = u.w;
+            }
+    #pragma unroll
+            for (int mt = 0; mt < C::KS; ++mt) {
+                uint32_t a0, a1, a2, a3;
+                codes_to_half2(vw[2 * mt], a0, a2);           // dim 16 mt + g
+                codes_to_half2(vw[2 * mt + 1], a1, a3);       // dim 16 mt + 8 + g
+    #pragma unroll
+                for (int nt = 0; nt < C::NT; ++nt) mma_f16(acc[mt][nt], a0, a1, a2, a3, pb[nt].x, pb[nt].y);
+            }
         }
         // this stage and the staging are free once every lane is past its reads
         __syncwarp();
@@ -558,7 +629,8 @@ __global__ void __launch_bounds__(kCombineWarps * 32) int8_combine_kernel(const 
     const int len = c.next_pos[b];
     const int nfull = len & ~(kQBlock - 1);
     // quantized splits at 0 .. nsq - 1, the exact tail split (if any) at nsq
-    const int ns = (nfull + kInt8Split - 1) / kInt8Split + (len > nfull ? 1 : 0);
+    const int kvh = hq / (c.Hq / c.Hkv);
+    const int ns = (nfull + kInt8Split - 1) / kInt8Split + (len > nfull || c.xn[(size_t)b * c.Hkv + kvh] > 0 ? 1 : 0);
     const size_t row = (size_t)b * c.Hq + hq;
     const float2* ml = c.part_ml + row * c.max_splits;
     const float* pc = c.part_c + row * c.max_splits;
@@ -630,6 +702,9 @@ cudaError_t launch_int8_decode(kvc_handle* h, const void* q, void* out, float* c
     a.wit = reinterpret_cast<const __half*>(h->state + h->L.wit);
     a.ktail = reinterpret_cast<const __nv_bfloat16*>(h->state + h->L.ktail);
     a.vtail = reinterpret_cast<const __nv_bfloat16*>(h->state + h->L.vtail);
+    a.xmap = reinterpret_cast<const int32_t*>(h->state + h->L.xmap);
+    a.xn = reinterpret_cast<const int32_t*>(h->state + h->L.xn);
+    a.xpool = reinterpret_cast<const __nv_bfloat16*>(h->state + h->L.xpool);
     a.next_pos = reinterpret_cast<const int32_t*>(h->state + h->L.next_pos);
     a.rope = s.rope ? reinterpret_cast<const float2*>(h->state + h->L.rope) : nullptr;
     a.part_ml = reinterpret_cast<float2*>(h->state + h->L.part_ml);
@@ -648,9 +723,9 @@ cudaError_t launch_int8_decode(kvc_handle* h, const void* q, void* out, float* c
 #undef KVC_CASE
     if (e != cudaSuccess) return e;
     Int8CombineArgs c{};
-    c.part_ml = a.part_ml; c.part_acc = a.part_acc; c.part_c = a.part_c; c.next_pos = a.next_pos;
+    c.part_ml = a.part_ml; c.part_acc = a.part_acc; c.part_c = a.part_c; c.next_pos = a.next_pos; c.xn = a.xn;
     c.out = out; c.cmax = cmax; c.tanh_out = tanh_out;
-    c.B = s.B; c.Hq = s.Hq; c.d = s.d; c.max_splits = s.max_splits; c.out_bf16 = s.out_bf16;
+    c.B = s.B; c.Hq = s.Hq; c.Hkv = s.Hkv; c.d = s.d; c.max_splits = s.max_splits; c.out_bf16 = s.out_bf16;
     int8_combine_kernel<<<dim3(s.Hq, s.B), kCombineWarps * 32, 0, st>>>(c);
     return cudaGetLastError();
 }

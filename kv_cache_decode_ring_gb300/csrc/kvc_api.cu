@@ -36,7 +36,9 @@ bool make_shape(const kvc_config& c, Shape* s) {
     const bool ring = c.layout == KVC_RING;
     if (ring && c.window != 0 && c.window != c.capacity) return false;
     const bool int8 = c.kv_quant == KVC_QUANT_INT8;
-    if (int8 && (c.dtype != KVC_BF16 || ring || c.head_dim % kBands || c.capacity % kQBlock)) return false;
+    if (int8 && (c.dtype != KVC_BF16 || ring || c.window != 0 || c.head_dim % kBands || c.capacity % kQBlock))
+        return false;
+    if (c.int8_exact_blocks < 0 || (!int8 && c.int8_exact_blocks != 0)) return false;
     if (int8) {
         const int g = c.n_q_heads / c.n_kv_heads;
         if ((c.head_dim != 64 && c.head_dim != 128) || (g != 1 && g != 2 && g != 4 && g != 8)) return false;
@@ -52,6 +54,7 @@ bool make_shape(const kvc_config& c, Shape* s) {
     s->P = P; s->ring = ring; s->int8 = int8; s->rope = rope; s->bf16 = c.dtype == KVC_BF16;
     s->elem = s->bf16 ? 2 : 4;
     s->max_chunk = c.max_chunk;
+    s->xpool = c.int8_exact_blocks;
     s->out_bf16 = c.out_dtype == 0 ? s->bf16 : c.out_dtype == KVC_BF16 + 1;
     s->split = kGenericSplit;
     if (s->bf16 && !int8 && (s->d == 64 || s->d == 128) && s->g <= 8) s->split = kFastSplit;
@@ -87,6 +90,9 @@ Layout make_layout(const Shape& s) {
         L.wit = take(B * Hkv * S * kBands * 2);
         L.ktail = take(B * Hkv * kQBlock * d * 2);
         L.vtail = take(B * Hkv * kQBlock * d * 2);
+        L.xmap = take(B * Hkv * (S / kQBlock) * 4);
+        L.xn = take(B * Hkv * 4);
+        L.xpool = take((size_t)s.xpool * 2 * kQBlock * d * 2);
     }
     L.rope = take((size_t)s.P * (d / 2) * 8);
     L.part_ml = take(B * Hq * s.max_splits * 8);
@@ -215,6 +221,13 @@ int kvc_create(const kvc_config* cfg, void* d_state, size_t bytes, kvc_stream_t 
     cudaStream_t st = S_(stream);
     cudaError_t e = cudaMemsetAsync(h->state, 0, L.total, st);
     if (e == cudaSuccess) e = cudaMemsetAsync(h->state + L.pos, 0xff, (size_t)s.B * s.S * 4, st);
+    if (e == cudaSuccess && s.int8) {
+        const size_t nb = (size_t)s.B * s.Hkv * (s.S / kQBlock);
+        e = cudaMemsetAsync(h->state + L.xmap, 0xff, nb * 4, st);
+        h->xmap_h.assign(nb, -1);
+        h->xn_h.assign((size_t)s.B * s.Hkv, 0);
+        for (int i = s.xpool - 1; i >= 0; --i) h->xfree.push_back(i);
+    }
     if (e == cudaSuccess && s.rope) {
         std::vector<float2> tab((size_t)s.P * (s.d / 2));
         rope_table((double)cfg->rope_base, s.d, s.P, tab.data());
@@ -317,6 +330,7 @@ int kvc_trim(kvc_t h, const int32_t* h_cut, kvc_stream_t stream) {
     if (launch_trim_cuts(at<int32_t>(h, h->L.next_pos), at<int32_t>(h, h->L.pos), h_cut, s.B, s.S, s.ring,
                          S_(stream)) != cudaSuccess)
         return KVC_ERR_CUDA;
+    if (s.int8 && int8_drop_restored(h, h_cut, S_(stream)) != cudaSuccess) return KVC_ERR_CUDA;
     for (int b = 0; b < s.B; ++b) h->np[b] = h_cut[b];
     if (s.ring) h->ring_needs_append = true;
     return KVC_OK;
@@ -361,6 +375,7 @@ int kvc_export_bytes(kvc_t h, int32_t which, size_t* bytes) {
         case KVC_EXPORT_SK: case KVC_EXPORT_SV: *bytes = B * Hkv * (S / kQBlock) * 4; return KVC_OK;
         case KVC_EXPORT_WITNESS: *bytes = B * Hkv * S * kBands * 2; return KVC_OK;
         case KVC_EXPORT_KTAIL: case KVC_EXPORT_VTAIL: *bytes = B * Hkv * kQBlock * d * 2; return KVC_OK;
+        case KVC_EXPORT_XMAP: *bytes = B * Hkv * (S / kQBlock) * 4; return KVC_OK;
         default: return KVC_ERR_ARG;
     }
 }
@@ -383,6 +398,7 @@ int kvc_export(kvc_t h, int32_t which, void* h_dst, size_t bytes, kvc_stream_t s
         case KVC_EXPORT_WITNESS: off = h->L.wit; break;
         case KVC_EXPORT_KTAIL: off = h->L.ktail; break;
         case KVC_EXPORT_VTAIL: off = h->L.vtail; break;
+        case KVC_EXPORT_XMAP: off = h->L.xmap; break;
         default: return KVC_ERR_ARG;
     }
     cudaStream_t st = S_(stream);

@@ -21,6 +21,7 @@ constexpr int kGenericSplit = 64;     // keys per split, generic decode kernel
 constexpr int kFastSplit = 128;       // keys per split, bf16 fast decode kernel
 constexpr int kInt8Split = 1024;      // keys per quantized split, INT8 decode kernel
 constexpr int kGqaSplit = 512;        // keys per split, bf16 decode kernel for 4 or 8 heads per KV head
+constexpr int kMaxRestored = 1024;    // INT8 blocks restored to full precision per (request, KV head)
 constexpr uint32_t kErrPosition = 1u; // device error bits (sticky, cleared by kvc_device_status)
 constexpr uint32_t kErrWait = 2u;
 
@@ -34,6 +35,9 @@ struct Layout {
     size_t sk, sv;    // f32  [B][Hkv][S/16]                   (INT8)
     size_t wit;       // f16  [B][Hkv][S][16]                  (INT8)
     size_t ktail, vtail;  // bf16 [B][Hkv][16][d]              (INT8)
+    size_t xmap;      // int32 [B][Hkv][S/16] pool entry of a restored block, -1 = quantized (INT8)
+    size_t xn;        // int32 [B][Hkv] restored blocks per (request, KV head)        (INT8)
+    size_t xpool;     // bf16 [pool][2][16][d] K and V rows of the restored blocks    (INT8)
     size_t rope;      // float2 [P][d/2] {cos, sin}
     size_t part_ml;   // float2 [B][Hq][max_splits] {m (log2 domain), l}
     size_t part_acc;  // float  [B][Hq][max_splits][d]
@@ -51,6 +55,7 @@ struct Shape {
     int split;                   // keys per split of the decode kernel in use
     int max_splits;
     int max_chunk;               // largest suffix of kvc_chunk_attn (0 = none)
+    int xpool;                   // entries of the INT8 exact-block pool
 };
 
 bool make_shape(const kvc_config& c, Shape* s);
@@ -108,6 +113,8 @@ bool make_tensor_map_bf16(CUtensorMap* tm, void* base, int rank, const cuuint64_
 
 // ---- launchers (one per translation unit) ----------------------------------
 cudaError_t launch_append_token(const AppendArgs& a, cudaStream_t st);
+// INT8 gated fallback (int8_gate.cu): drop restored blocks that a trim removed
+cudaError_t int8_drop_restored(kvc_handle* h, const int32_t* h_cut, cudaStream_t st);
 // maps: required when the GQA kernel serves the shape (split == kGqaSplit)
 cudaError_t launch_decode(const DecodeArgs& d, const CombineArgs& c, bool fast, const KvMaps* maps, cudaStream_t st);
 bool chunk_supported(const Shape& s);
@@ -173,4 +180,7 @@ struct kvc_handle {
     std::vector<int32_t> counts;   // host staging for append_rows counts
     kvc::KvMaps kv_maps;           // built at create when the GQA decode serves the shape
     bool has_kv_maps;
+    // INT8 gated fallback: host mirrors of the block map and the per-head counts, and
+    // the free pool entries
+    std::vector<int32_t> xmap_h, xn_h, xfree;
 };

@@ -24,7 +24,7 @@ KVC_F32, KVC_BF16 = 0, 1
 KVC_CONTIGUOUS, KVC_RING = 0, 1
 KVC_QUANT_NONE, KVC_QUANT_INT8 = 0, 1
 (KVC_EXPORT_K, KVC_EXPORT_V, KVC_EXPORT_POSITIONS, KVC_EXPORT_NEXT_POSITION, KVC_EXPORT_KQ, KVC_EXPORT_VQ,
- KVC_EXPORT_SK, KVC_EXPORT_SV, KVC_EXPORT_WITNESS, KVC_EXPORT_KTAIL, KVC_EXPORT_VTAIL) = range(11)
+ KVC_EXPORT_SK, KVC_EXPORT_SV, KVC_EXPORT_WITNESS, KVC_EXPORT_KTAIL, KVC_EXPORT_VTAIL, KVC_EXPORT_XMAP) = range(12)
 
 _STATUS_NAMES = {1: "KVC_ERR_ARG", 2: "KVC_ERR_CAPACITY", 3: "KVC_ERR_EVICTED", 4: "KVC_ERR_CUDA",
                  5: "KVC_ERR_UNSUPPORTED", 6: "KVC_ERR_DEVICE"}
@@ -41,12 +41,13 @@ class kvc_config(ctypes.Structure):
                 ("batch", ctypes.c_int32), ("n_q_heads", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("capacity", ctypes.c_int32), ("window", ctypes.c_int32),
                 ("max_position", ctypes.c_int32), ("rope_base", ctypes.c_float), ("max_chunk", ctypes.c_int32),
-                ("out_dtype", ctypes.c_int32)]
+                ("out_dtype", ctypes.c_int32), ("int8_exact_blocks", ctypes.c_int32)]
 
 
 EXPORTED = ["kvc_state_bytes", "kvc_create", "kvc_destroy", "kvc_append", "kvc_append_rows",
             "kvc_decode_attn", "kvc_trim", "kvc_chunk_attn", "kvc_export_bytes", "kvc_export",
-            "kvc_next_positions", "kvc_device_status", "kvc_prefix_cut", "kvc_strerror"]
+            "kvc_next_positions", "kvc_device_status", "kvc_prefix_cut", "kvc_strerror",
+            "kvc_int8_block_risk", "kvc_int8_gate", "kvc_int8_restore"]
 
 _lock = threading.Lock()
 _lib = None
@@ -82,6 +83,9 @@ def lib() -> ctypes.CDLL:
                 "kvc_device_status": [P, P, ctypes.POINTER(i32)],
                 "kvc_prefix_cut": [P, i32, P, i32, i32, ctypes.POINTER(i32)],
                 "kvc_decode_attn_noalloc": [P, P, P, P],
+                "kvc_int8_block_risk": [P, P, P, P],
+                "kvc_int8_gate": [P, i32, i32, i32, ctypes.c_double, i32, P, ctypes.POINTER(i32)],
+                "kvc_int8_restore": [P, P, i32, P, P, P],
             }
             for name, args in sig.items():
                 fn = getattr(L, name)
@@ -126,14 +130,15 @@ def kvc_strerror(code: int) -> str:
 
 def make_config(dtype="bf16", layout="contiguous", kv_quant=None, batch=1, n_q_heads=1, n_kv_heads=1,
                 head_dim=128, capacity=1, window=0, max_position=0, rope_base=0.0, max_chunk=0,
-                out_dtype=None) -> kvc_config:
-    """``out_dtype``: None (the cache dtype), "f32" or "bf16"."""
+                out_dtype=None, int8_exact_blocks=0) -> kvc_config:
+    """``out_dtype``: None (the cache dtype), "f32" or "bf16"; ``int8_exact_blocks``: pool
+    entries for blocks the gated fallback restores (INT8 caches)."""
     od = 0 if out_dtype is None else (KVC_F32 + 1 if out_dtype == "f32" else KVC_BF16 + 1)
     return kvc_config(KVC_BF16 if dtype == "bf16" else KVC_F32,
                       KVC_RING if layout == "ring" else KVC_CONTIGUOUS,
                       KVC_QUANT_INT8 if kv_quant == "int8" else KVC_QUANT_NONE,
                       batch, n_q_heads, n_kv_heads, head_dim, capacity, window, max_position,
-                      float(rope_base), max_chunk, od)
+                      float(rope_base), max_chunk, od, int(int8_exact_blocks))
 
 
 def kvc_state_bytes(cfg: kvc_config) -> int:
@@ -169,6 +174,31 @@ def kvc_decode_attn(h, q, out, cmax=None, tanh=None, ct=None, stream=None) -> No
     _check(lib().kvc_decode_attn(h, _dev(q, name="q"), _dev(out, name="out"), _dev(cmax, torch.float32, name="cmax"),
                                  _dev(tanh, torch.float32, name="tanh"), _dev(ct, torch.float32, name="ct"),
                                  _stream(stream)), "kvc_decode_attn")
+
+
+def kvc_int8_block_risk(h, ct, risk, stream=None) -> None:
+    _check(lib().kvc_int8_block_risk(h, _dev(ct, torch.float32, name="ct"), _dev(risk, torch.float32, name="risk"),
+                                     _stream(stream)), "kvc_int8_block_risk")
+
+
+def kvc_int8_gate(risk: np.ndarray, tau: float, max_blocks: int) -> np.ndarray:
+    """Host selection: [n, 3] int32 (request, KV head, block) triples, highest risk first."""
+    r = np.ascontiguousarray(np.asarray(risk, dtype=np.float32))
+    if r.ndim != 3:
+        raise ValueError("risk must be [B, Hkv, nblk]")
+    sel = np.zeros((max(int(max_blocks), 1), 3), dtype=np.int32)
+    n = ctypes.c_int32(0)
+    _check(lib().kvc_int8_gate(r.ctypes.data_as(ctypes.c_void_p), r.shape[0], r.shape[1], r.shape[2],
+                               ctypes.c_double(tau), int(max_blocks), sel.ctypes.data_as(ctypes.c_void_p),
+                               ctypes.byref(n)), "kvc_int8_gate")
+    return sel[:n.value].copy()
+
+
+def kvc_int8_restore(h, blocks, k_full, v_full, stream=None) -> None:
+    b = np.ascontiguousarray(np.asarray(blocks, dtype=np.int32).reshape(-1, 3))
+    _check(lib().kvc_int8_restore(h, b.ctypes.data_as(ctypes.c_void_p) if len(b) else None, len(b),
+                                  _dev(k_full, torch.bfloat16, name="k_full"),
+                                  _dev(v_full, torch.bfloat16, name="v_full"), _stream(stream)), "kvc_int8_restore")
 
 
 KVC_NOALLOC_SCRATCH_BYTES = 64 << 20
@@ -237,7 +267,8 @@ class Cache:
 
     _EXPORT_DTYPES = {KVC_EXPORT_POSITIONS: np.int32, KVC_EXPORT_NEXT_POSITION: np.int32, KVC_EXPORT_KQ: np.int8,
                       KVC_EXPORT_VQ: np.int8, KVC_EXPORT_SK: np.float32, KVC_EXPORT_SV: np.float32,
-                      KVC_EXPORT_WITNESS: np.uint16, KVC_EXPORT_KTAIL: np.uint16, KVC_EXPORT_VTAIL: np.uint16}
+                      KVC_EXPORT_WITNESS: np.uint16, KVC_EXPORT_KTAIL: np.uint16, KVC_EXPORT_VTAIL: np.uint16,
+                      KVC_EXPORT_XMAP: np.int32}
 
     def __init__(self, cfg: kvc_config, device="cuda", stream=None):
         self.cfg = cfg
@@ -251,9 +282,10 @@ class Cache:
         self.h = kvc_create(cfg, self.state, stream)
 
     @classmethod
-    def from_workload(cls, w, max_chunk=0, max_position=0, device="cuda", out_dtype=None):
+    def from_workload(cls, w, max_chunk=0, max_position=0, device="cuda", out_dtype=None, int8_exact_blocks=0):
         cfg = make_config(w.dtype, w.layout, w.quant, w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.capacity,
-                          0 if w.layout == "ring" else w.window, max_position, w.rope_base, max_chunk, out_dtype)
+                          0 if w.layout == "ring" else w.window, max_position, w.rope_base, max_chunk, out_dtype,
+                          int8_exact_blocks)
         return cls(cfg, device)
 
     def close(self):
@@ -325,11 +357,27 @@ class Cache:
                   KVC_EXPORT_VQ: (self.B, self.Hkv, self.S, self.d),
                   KVC_EXPORT_SK: (self.B, self.Hkv, self.S // 16), KVC_EXPORT_SV: (self.B, self.Hkv, self.S // 16),
                   KVC_EXPORT_WITNESS: (self.B, self.Hkv, self.S, 16), KVC_EXPORT_KTAIL: (self.B, self.Hkv, 16, self.d),
-                  KVC_EXPORT_VTAIL: (self.B, self.Hkv, 16, self.d)}
+                  KVC_EXPORT_VTAIL: (self.B, self.Hkv, 16, self.d),
+                  KVC_EXPORT_XMAP: (self.B, self.Hkv, self.S // 16)}
         return arr.reshape(shapes[which])
 
     def next_positions(self) -> np.ndarray:
         return kvc_next_positions(self.h, self.B)
+
+    # gated fallback of the INT8 tier
+    def block_risk(self, ct, risk=None, stream=None):
+        """Per complete block, the largest c_t over its tokens and the KV head's query heads."""
+        _dev(ct, torch.float32, (self.B, self.Hq, self.S), "ct")
+        if risk is None:
+            risk = torch.empty((self.B, self.Hkv, self.S // 16), dtype=torch.float32, device=ct.device)
+        _dev(risk, torch.float32, (self.B, self.Hkv, self.S // 16), "risk")
+        kvc_int8_block_risk(self.h, ct, risk, stream)
+        return risk
+
+    def restore(self, blocks, k_full, v_full, stream=None):
+        _dev(k_full, torch.bfloat16, (self.B, self.Hkv, self.S, self.d), "k_full")
+        _dev(v_full, torch.bfloat16, (self.B, self.Hkv, self.S, self.d), "v_full")
+        kvc_int8_restore(self.h, blocks, k_full, v_full, stream)
 
     def device_status(self, stream=None) -> int:
         return kvc_device_status(self.h, stream)

@@ -56,6 +56,9 @@ def test_state_bytes_validation(lib):
         kvc.make_config("bf16", "contiguous", "int8", 1, 1, 1, 128, 60),        # INT8 capacity % 16
         kvc.make_config("bf16", "ring", "int8", 1, 1, 1, 128, 64),              # INT8 contiguous only
         kvc.make_config("bf16", "contiguous", None, 0, 1, 1, 128, 64),          # empty batch
+        kvc.make_config("bf16", "contiguous", "int8", 1, 4, 1, 128, 64, window=32),   # INT8 attends to all
+        kvc.make_config("bf16", "contiguous", None, 1, 1, 1, 128, 64, int8_exact_blocks=4),  # pool needs INT8
+        kvc.make_config("bf16", "contiguous", "int8", 1, 4, 1, 128, 64, int8_exact_blocks=-1),
     ]
     for c in bad:
         with pytest.raises(kvc.KvcError) as e:
@@ -90,3 +93,21 @@ def test_prefix_cut_matches_oracle_exhaustively(lib):
 def test_strerror(lib):
     for code in range(7):
         assert kvc.kvc_strerror(code)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_int8_gate_matches_oracle_selection(lib, seed):
+    # the host gate of the C ABI against the oracle's selection on the same fp32 risks,
+    # including ties, values at atanh(tau) and budgets
+    import math
+    import numpy as np
+    from oracle.model import gate_select
+    rng = np.random.default_rng(seed)
+    B, H, nb = int(rng.integers(1, 4)), int(rng.integers(1, 4)), int(rng.integers(0, 40))
+    pool = np.array([0.0, 0.05, 0.2, math.atanh(0.2), 0.25, 0.7, 0.7, 3.0], dtype=np.float32)
+    risk = rng.choice(pool, (B, H, nb)).astype(np.float32)
+    for tau in (0.0, 0.2, 0.5):
+        for budget in (0, 1, 5, B * H * nb + 1):
+            got = kvc.kvc_int8_gate(risk, tau, budget)
+            want = gate_select({(b, h): risk[b, h] for b in range(B) for h in range(H)}, tau, budget)
+            assert [tuple(x) for x in got] == want, (tau, budget)

@@ -49,7 +49,10 @@ def check_int8_state(cache, model, requests=None):
                 sl = slice(blk * QBLOCK, (blk + 1) * QBLOCK)
                 assert SK[b, h, blk] == sK and SV[b, h, blk] == sV, (b, h, blk)
                 assert np.array_equal(KQ[b, h, sl], cK) and np.array_equal(VQ[b, h, sl], cV), (b, h, blk)
-                assert np.array_equal(WT[b, h, sl], wit), (b, h, blk)
+                if blk in model.restored[b][h]:
+                    assert not WT[b, h, sl].any(), (b, h, blk)     # the gated fallback zeroed them
+                else:
+                    assert np.array_equal(WT[b, h, sl], wit), (b, h, blk)
             for p in range(nfull, n):
                 assert np.array_equal(KT[b, h, p % QBLOCK], nm.f32_to_bf16(model.hk[b][p][h])), (b, h, p)
                 assert np.array_equal(VT[b, h, p % QBLOCK], nm.f32_to_bf16(model.hv[b][p][h])), (b, h, p)
@@ -158,3 +161,115 @@ def test_int8_zero_residual_gives_zero_bound():
     assert not cache.export(kvc.KVC_EXPORT_WITNESS).any()
     q = w.queries((1, 2, 128), "zero-residual")
     check_decode(cache, model, q)
+
+
+def _backing_store(w, k, v, lengths, extra):
+    """Full-precision rows of the same tokens: a bf16 cache fed the same appends (the
+    caller's backing store), exported and put back on the device."""
+    import copy
+    wb = copy.copy(w)
+    wb.quant = None
+    full = kvc.Cache.from_workload(wb)
+    full.append_rows(k.cuda(), v.cuda(), counts=lengths)
+    for k1, v1 in extra:
+        full.append(k1.cuda(), v1.cuda())
+    kf = torch.from_numpy(full.export(kvc.KVC_EXPORT_K).view(np.int16)).view(torch.bfloat16).cuda()
+    vf = torch.from_numpy(full.export(kvc.KVC_EXPORT_V).view(np.int16)).view(torch.bfloat16).cuda()
+    return kf, vf
+
+
+def test_int8_gated_fallback():
+    # [WITCERT] "SGLang 生产级落地与闭环门控修复": risk from the decode's c_t, gate at tau,
+    # restore the chosen blocks from the backing store; their tokens become exact (c_t = 0)
+    # and every head's tanh(max c_t) drops to tau or below
+    tau = 0.2
+    w = wl.small("int8-gate", B=2, Hq=8, Hkv=2, d=128, capacity=512, rope_base=10000.0, quant="int8",
+                 seed=13, outliers=(4, 20.0))
+    cache = kvc.Cache.from_workload(w, out_dtype="f32", int8_exact_blocks=96)
+    model = _oracle(w)
+    lengths = [300, 263]
+    k, v = w.prefill_chunk(0, max(lengths))
+    cache.append_rows(k.cuda(), v.cuda(), counts=lengths)
+    model.append_rows(host(k), host(v), lengths)
+    q, k1, v1 = w.step_qkv(0)
+    cache.append(k1.cuda(), v1.cuda())
+    model.append(host(k1), host(v1))
+    B, Hq, S = w.batch, w.n_q_heads, cache.S
+    out = torch.empty((B, Hq, w.head_dim), dtype=torch.float32, device="cuda")
+    cmax = torch.empty((B, Hq), device="cuda")
+    th = torch.empty((B, Hq), device="cuda")
+    ct = torch.zeros((B, Hq, S), device="cuda")
+    kvc.kvc_decode_attn(cache.h, q.cuda(), out, cmax, th, ct)
+    assert th.max().item() > tau                                   # the outlier channels make it risky
+    # block risk: the block maximum of the decode's own c_t, bit-exact
+    risk = cache.block_risk(ct).cpu().numpy()
+    ctn = ct.cpu().numpy()
+    g = Hq // w.n_kv_heads
+    for b in range(B):
+        nfull = model.length(b) // QBLOCK * QBLOCK
+        for h in range(w.n_kv_heads):
+            for blk in range(S // QBLOCK):
+                want = ctn[b, h * g:(h + 1) * g, blk * 16:blk * 16 + 16].max() if (blk + 1) * 16 <= nfull else 0.0
+                assert risk[b, h, blk] == want, (b, h, blk)
+    sel = kvc.kvc_int8_gate(risk, tau, 1000)
+    assert 0 < len(sel) <= 96
+    top = kvc.kvc_int8_gate(risk, tau, 5)                           # a budget keeps the riskiest
+    assert np.array_equal(top, sel[:5])
+    kf, vf = _backing_store(w, k, v, lengths, [(k1, v1)])
+    cache.restore(sel, kf, vf)
+    model.restore([tuple(x) for x in sel])
+    xm = cache.export(kvc.KVC_EXPORT_XMAP)
+    ent = [xm[b, h, blk] for b, h, blk in sel]
+    assert min(ent) >= 0 and len(set(ent)) == len(ent) and (xm >= 0).sum() == len(sel)
+    check_int8_state(cache, model)
+    # the same query again: restored tokens are exact with c_t = 0; every head under tau
+    res = model.decode_int8(host(q))
+    ct2 = torch.full((B, Hq, S), -7.0, device="cuda")
+    kvc.kvc_decode_attn(cache.h, q.cuda(), out, cmax, th, ct2)
+    ctn2 = ct2.cpu().numpy()
+    assert np.all(th.cpu().numpy() <= tau)
+    for b, h, blk in sel:
+        assert np.all(ctn2[b, h * g:(h + 1) * g, blk * 16:blk * 16 + 16] == 0.0)
+    for (b, hq), r in res.items():
+        assert_close(out[b, hq][None], r["out"][None], "bf16", "gated decode b=%d h=%d" % (b, hq))
+    check_decode(cache, model, q)
+    # later steps, then a trim that drops the restored blocks past the cut
+    steps = [(k1, v1)]
+    for s in range(1, 4):
+        q, k1, v1 = w.step_qkv(s)
+        cache.append(k1.cuda(), v1.cuda())
+        model.append(host(k1), host(v1))
+        check_decode(cache, model, q)
+    cuts = [160, 64]
+    cache.trim(cuts)
+    model.trim(cuts)
+    xm = cache.export(kvc.KVC_EXPORT_XMAP)
+    for b in range(B):
+        for h in range(w.n_kv_heads):
+            live = {blk for blk in range(S // 16) if xm[b, h, blk] >= 0}
+            assert live == model.restored[b][h], (b, h)
+    check_int8_state(cache, model)
+    for s in range(4, 8):
+        q, k1, v1 = w.step_qkv(s)
+        cache.append(k1.cuda(), v1.cuda())
+        model.append(host(k1), host(v1))
+        check_decode(cache, model, q)
+    assert cache.device_status() == 0
+
+
+def test_int8_restore_errors():
+    w = wl.small("int8-gate-err", B=1, Hq=4, Hkv=1, d=64, capacity=128, rope_base=0.0, quant="int8", seed=3)
+    cache = kvc.Cache.from_workload(w, out_dtype="f32", int8_exact_blocks=2)
+    k, v = w.prefill_chunk(0, 70)
+    cache.append_rows(k.cuda(), v.cuda())
+    kf, vf = _backing_store(w, k, v, None, [])
+    with pytest.raises(kvc.KvcError) as e:
+        cache.restore([(0, 0, 4)], kf, vf)                 # block 4 = positions 64..79: incomplete
+    assert e.value.code == kvc.KVC_ERR_ARG
+    with pytest.raises(kvc.KvcError) as e:
+        cache.restore([(0, 0, 0), (0, 0, 1), (0, 0, 2)], kf, vf)     # pool of 2
+    assert e.value.code == kvc.KVC_ERR_CAPACITY
+    assert (cache.export(kvc.KVC_EXPORT_XMAP) < 0).all()            # nothing restored
+    cache.restore([(0, 0, 1), (0, 0, 1)], kf, vf)                    # duplicates count once
+    cache.restore([(0, 0, 1), (0, 0, 3)], kf, vf)                    # already restored: skipped
+    assert (cache.export(kvc.KVC_EXPORT_XMAP) >= 0).sum() == 2
