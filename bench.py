@@ -334,7 +334,7 @@ class Int8Bench(DecodeBench):
             w.batch = batch                   # smaller case for profiler captures
         self.ctx = w.extra["context"]
         w.capacity = self.ctx + 16 * ((total_steps + 16 + 15) // 16)
-        self.cache = kvc.Cache.from_workload(w, device=device)
+        self.cache = kvc.Cache.from_workload(w, device=device, int8_exact_blocks=self.pool_blocks())
         chunk = 8192
         for c in range(self.ctx // chunk):
             k, v = w.prefill_chunk(c, chunk, device=device)
@@ -345,16 +345,20 @@ class Int8Bench(DecodeBench):
         self.tanh = torch.empty((B, Hq), device=device)
         self._inputs(device)
 
+    def pool_blocks(self):
+        return 0
+
     def decode(self, q):
         self.cache.decode(q, self.out, self.cmax, self.tanh)
 
     def units(self):
-        """Bytes the fused decode reads: codes, witnesses and scales of complete blocks, exact tail rows."""
+        """Bytes the fused decode reads: codes, witnesses and scales of complete blocks, exact tail rows
+        (and the bf16 rows of blocks restored by the gated fallback)."""
         w = self.w
         n = self.ctx + self.done + 1
         nfull = n // 16 * 16
         per_head = nfull * (2 * w.head_dim + 32) + (nfull // 16) * 8 + (n - nfull) * 4 * w.head_dim
-        return w.batch * w.n_kv_heads * per_head
+        return w.batch * w.n_kv_heads * per_head + getattr(self, "restored", 0) * 16 * 4 * w.head_dim
 
     def reset(self):
         import torch
@@ -368,6 +372,69 @@ class Int8Bench(DecodeBench):
         return {"workload": w.name, "batch": w.batch, "n_q_heads": w.n_q_heads, "n_kv_heads": w.n_kv_heads,
                 "head_dim": w.head_dim, "layout": "contiguous int8 + witnesses", "context": "131072 + step",
                 "l2": "inputs larger than L2: %.2f GB read per step vs 129 MB L2" % (self.units() / 1e9)}
+
+
+class Int8GatedBench(Int8Bench):
+    """The INT8 workload after one gated fallback: a decode with per-token c_t, block risk,
+    gate at tau = 0.2 with a budget of 1 % of the complete blocks (highest risk first),
+    restore from a bf16 backing store; then the same decode steps as the INT8 bench, with
+    the restored blocks served exactly.  The gate's own cost (risk, selection, restore) is
+    reported in the config."""
+
+    TAU = 0.2
+    BUDGET_FRAC = 0.01
+
+    def pool_blocks(self):
+        w = self.w
+        return max(1, int(self.BUDGET_FRAC * w.batch * w.n_kv_heads * (w.extra["context"] // 16)))
+
+    def __init__(self, device, batch=None, total_steps=0):
+        import copy
+        import time
+        import numpy as np
+        import torch
+        from kv_cache_decode_ring_gb300 import kvc
+        super().__init__(device, batch, total_steps)
+        w = self.w
+        # backing store: the same tokens in a bf16 cache, exported to device tensors
+        wb = copy.copy(w)
+        wb.quant = None
+        full = kvc.Cache.from_workload(wb, device=device)
+        for c in range(self.ctx // 8192):
+            k, v = w.prefill_chunk(c, 8192, device=device)
+            full.append_rows(k, v)
+            del k, v
+        kf = torch.from_numpy(full.export(kvc.KVC_EXPORT_K).view(np.int16)).view(torch.bfloat16).to(device)
+        vf = torch.from_numpy(full.export(kvc.KVC_EXPORT_V).view(np.int16)).view(torch.bfloat16).to(device)
+        full.close()
+        del full
+        torch.cuda.empty_cache()
+        # one decode with c_t, then the gate
+        B, Hq = w.batch, w.n_q_heads
+        ct = torch.zeros((B, Hq, self.cache.S), device=device)
+        self.cache.decode(self.q[0], self.out, self.cmax, self.tanh, ct)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        risk = self.cache.block_risk(ct).cpu().numpy()
+        t1 = time.perf_counter()
+        sel = kvc.kvc_int8_gate(risk, self.TAU, self.pool_blocks())
+        t2 = time.perf_counter()
+        self.cache.restore(sel, kf, vf)
+        torch.cuda.synchronize()
+        t3 = time.perf_counter()
+        self.restored = len(sel)
+        self.risky = int((np.tanh(risk.astype(np.float64)) > self.TAU).sum())
+        self.gate_ms = {"risk_and_readback": round((t1 - t0) * 1e3, 3), "select": round((t2 - t1) * 1e3, 3),
+                        "restore": round((t3 - t2) * 1e3, 3)}
+        del ct, kf, vf
+        torch.cuda.empty_cache()
+
+    def config(self):
+        c = super().config()
+        c["workload"] = "int8-witness-gated"
+        c["gate"] = {"tau": self.TAU, "budget_blocks": self.pool_blocks(), "risky_blocks": self.risky,
+                     "restored_blocks": self.restored, "ms": self.gate_ms}
+        return c
 
 
 class Bf16AtInt8ShapeBench(DecodeBench):
@@ -515,7 +582,7 @@ class ChunkWindowBench(ChunkBench):
 
 
 BENCHES = {"full-cache-mha": FullCacheBench, "sliding-window-gqa": SlidingWindowBench, "int8-witness": Int8Bench,
-           "bf16-at-int8-shape": Bf16AtInt8ShapeBench,
+           "bf16-at-int8-shape": Bf16AtInt8ShapeBench, "int8-witness-gated": Int8GatedBench,
            "prefix-reuse": ChunkBench, "prefix-reuse-w4096": ChunkWindowBench}
 
 

@@ -18,9 +18,9 @@
 // streams its 16 blocks through three shared-memory stages (codes and witnesses
 // by bulk copy on the stage's mbarrier), so copies overlap arithmetic; online
 // softmax over the warp's blocks, warps merged at the end.  One extra split
-// handles the exact rows (c_t = 0 there): the tail of the incomplete block and the
-// blocks restored to full precision by the gated fallback (int8_gate.cu), which
-// the quantized splits skip.
+// handles the exact tail rows of the incomplete block (c_t = 0 there).  Blocks
+// restored to full precision by the gated fallback are skipped here and served
+// by the exact-block decode (int8_exact.cu), whose splits follow.
 //
 // Both contractions of a block run on the tensor cores as fp16 MMAs with fp32
 // accumulation (m16n8k16), operands built in registers:
@@ -181,17 +181,15 @@ __global__ void __launch_bounds__(kWarps * 32, D >= 128 ? 3 : 4) int8_decode_ker
     const size_t rowq0 = (size_t)b * a.Hq + (size_t)kvh * G;    // first query row of the group
 
     if (tail_split) {
-        // ---- exact rows, served in bf16 with c_t = 0: the tail [nfull, len) and every
-        // block restored by the gated fallback.  Warp 0, 32 rows at a time, online
-        // softmax over the chunks; lane = row for the scores, lane = dims for P.V.
+        // ---- exact tail rows [nfull, len), served in bf16 with c_t = 0.  Warp 0, 32 rows
+        // at a time, online softmax over the chunks; lane = row for the scores, lane =
+        // dims for P.V.  With no tail rows (a head with restored blocks) it writes the
+        // empty partial, so the combine reads contiguous splits.
         if (warp != 0) return;
         const size_t bh = (size_t)b * a.Hkv + kvh;
         const int nt = len - nfull;
-        const int nblk = a.S / kQBlock;
         float* qs = reinterpret_cast<float*>(smem);          // [G][D] scaled query
         float* pt = qs + G * D;                              // [32][G] weights of a chunk
-        int* xk = reinterpret_cast<int*>(pt + 32 * G);       // [nx] restored block index
-        int* xe = xk + kMaxRestored;                         // [nx] its pool entry
         for (int idx = lane; idx < G * D / 2; idx += 32) {
             const int h = idx / (D / 2), i = idx % (D / 2);
             const size_t off = (rowq0 + h) * D + 2 * i;
@@ -201,28 +199,11 @@ __global__ void __launch_bounds__(kWarps * 32, D >= 128 ? 3 : 4) int8_decode_ker
             qs[h * D + 2 * i] = y0 * a.scale_log2;
             qs[h * D + 2 * i + 1] = y1 * a.scale_log2;
         }
-        // restored blocks of this (request, KV head), in block order
-        int nx = 0;
-        if (a.xn[bh] > 0) {
-            for (int k0 = 0; k0 < nfull / kQBlock; k0 += 32) {
-                const int k = k0 + lane;
-                const int e = k < nfull / kQBlock ? a.xmap[bh * nblk + k] : -1;
-                const unsigned m = __ballot_sync(0xffffffffu, e >= 0);
-                const int at = nx + __popc(m & ((1u << lane) - 1));
-                if (e >= 0 && at < kMaxRestored) { xk[at] = k; xe[at] = e; }
-                nx = min(kMaxRestored, nx + __popc(m));
-            }
-        }
         __syncwarp();
         const size_t tail0 = bh * kQBlock * D;
-        const int total = nt + kQBlock * nx;
-        // row r: tail row r, or row (r - nt) % 16 of restored block (r - nt) / 16
-        auto row_ptr = [&](int r, bool v) -> const __nv_bfloat16* {
-            if (r < nt) return (v ? a.vtail : a.ktail) + tail0 + (size_t)r * D;
-            const int j = (r - nt) / kQBlock, rr = (r - nt) % kQBlock;
-            return a.xpool + ((size_t)xe[j] * 2 + (v ? 1 : 0)) * kQBlock * D + (size_t)rr * D;
-        };
-        auto row_pos = [&](int r) { return r < nt ? nfull + r : xk[(r - nt) / kQBlock] * kQBlock + (r - nt) % kQBlock; };
+        const int total = nt;
+        auto row_ptr = [&](int r, bool v) { return (v ? a.vtail : a.ktail) + tail0 + (size_t)r * D; };
+        auto row_pos = [&](int r) { return nfull + r; };
         float m[G], l[G], acc[G][D / 32];
 #pragma unroll
         for (int h = 0; h < G; ++h) {
@@ -630,7 +611,10 @@ __global__ void __launch_bounds__(kCombineWarps * 32) int8_combine_kernel(const 
     const int nfull = len & ~(kQBlock - 1);
     // quantized splits at 0 .. nsq - 1, the exact tail split (if any) at nsq
     const int kvh = hq / (c.Hq / c.Hkv);
-    const int ns = (nfull + kInt8Split - 1) / kInt8Split + (len > nfull || c.xn[(size_t)b * c.Hkv + kvh] > 0 ? 1 : 0);
+    const int nx = c.xn[(size_t)b * c.Hkv + kvh];
+    // quantized splits, the exact-rows split (if it ran), the exact-block splits
+    const int ns = (nfull + kInt8Split - 1) / kInt8Split + (len > nfull || nx > 0 ? 1 : 0) +
+                   (nx + kExactBlocksPerCta - 1) / kExactBlocksPerCta;
     const size_t row = (size_t)b * c.Hq + hq;
     const float2* ml = c.part_ml + row * c.max_splits;
     const float* pc = c.part_c + row * c.max_splits;
@@ -722,6 +706,7 @@ cudaError_t launch_int8_decode(kvc_handle* h, const void* q, void* out, float* c
     KVC_CASE(64, 1) KVC_CASE(64, 2) KVC_CASE(64, 4) KVC_CASE(64, 8)
 #undef KVC_CASE
     if (e != cudaSuccess) return e;
+    if (s.xpool > 0 && (e = launch_int8_exact(h, q, ct, st)) != cudaSuccess) return e;
     Int8CombineArgs c{};
     c.part_ml = a.part_ml; c.part_acc = a.part_acc; c.part_c = a.part_c; c.next_pos = a.next_pos; c.xn = a.xn;
     c.out = out; c.cmax = cmax; c.tanh_out = tanh_out;

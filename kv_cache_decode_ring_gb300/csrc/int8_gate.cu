@@ -8,9 +8,10 @@
 //    heads of its KV head (from a decode's per-token bound);
 //  * the gate picks every block with tanh(risk) > tau, highest risk first, up to a
 //    budget (host);
-//  * a restored block's 16 K and V rows go to a pool entry in the state buffer, its
-//    witnesses become 0 and the block map points at the entry; the INT8 decode then
-//    serves those tokens exactly (c_t = 0) in its exact-rows split.
+//  * a restored block's 16 K and V rows go, bf16 and unchanged, to a pool entry in the
+//    state buffer; its witnesses become 0, the block map points at the entry and the
+//    block joins its head's list; the quantized decode skips it and the exact-block
+//    decode (int8_exact.cu) serves its tokens exactly (c_t = 0).
 #include <algorithm>
 #include <cmath>
 #include <cstring>
@@ -46,29 +47,32 @@ constexpr int kRestoreBatch = 256;        // blocks per launch (kernel parameter
 struct RestoreList {
     int n;
     int4 e[kRestoreBatch];                // (request, KV head, block, pool entry)
+    int slot[kRestoreBatch];              // position in the head's list of restored blocks
 };
 
-// CTA per block: K and V rows into the pool entry, witnesses to 0, block map entry
+// CTA per block: the 16 K and V rows, bf16 and unchanged, into the pool entry in the
+// exact-block decode's order; witnesses to 0; block map and list entries
 __global__ void __launch_bounds__(256) restore_kernel(const RestoreList L, const __nv_bfloat16* kfull,
                                                       const __nv_bfloat16* vfull, __nv_bfloat16* xpool,
-                                                      __half* wit, int32_t* xmap, int32_t* xn, int Hkv, int S,
-                                                      int d) {
+                                                      __half* wit, int32_t* xmap, int32_t* xn, int32_t* xlist,
+                                                      int32_t* xent, int Hkv, int S, int d) {
     if ((int)blockIdx.x >= L.n) return;
     const int4 e = L.e[blockIdx.x];
     const size_t row0 = ((size_t)e.x * Hkv + e.y) * S + (size_t)e.z * kQBlock;
-    __nv_bfloat16* dst = xpool + (size_t)e.w * 2 * kQBlock * d;
-    const uint4* ks = reinterpret_cast<const uint4*>(kfull + row0 * d);
-    const uint4* vs = reinterpret_cast<const uint4*>(vfull + row0 * d);
-    uint4* kd = reinterpret_cast<uint4*>(dst);
-    uint4* vd = reinterpret_cast<uint4*>(dst + kQBlock * d);
-    for (int i = threadIdx.x; i < kQBlock * d / 8; i += blockDim.x) {
-        kd[i] = ks[i];
-        vd[i] = vs[i];
+    unsigned char* kd = reinterpret_cast<unsigned char*>(xpool + (size_t)e.w * 2 * kQBlock * d);
+    unsigned char* vd = kd + kQBlock * d * 2;
+    for (int i = threadIdx.x; i < kQBlock * d; i += blockDim.x) {
+        const int t = i / d, x = i % d;
+        *reinterpret_cast<__nv_bfloat16*>(kd + xk_offset(d, t, x)) = kfull[row0 * d + i];
+        *reinterpret_cast<__nv_bfloat16*>(vd + xv_offset(d, t, x)) = vfull[row0 * d + i];
     }
     for (int i = threadIdx.x; i < kQBlock * kBands; i += blockDim.x) wit[row0 * kBands + i] = __float2half(0.f);
     if (threadIdx.x == 0) {
-        xmap[((size_t)e.x * Hkv + e.y) * (S / kQBlock) + e.z] = e.w;
-        atomicAdd(&xn[e.x * Hkv + e.y], 1);
+        const size_t head = (size_t)e.x * Hkv + e.y;
+        xmap[head * (S / kQBlock) + e.z] = e.w;
+        xlist[head * kMaxRestored + L.slot[blockIdx.x]] = e.z;
+        xent[head * kMaxRestored + L.slot[blockIdx.x]] = e.w;
+        atomicAdd(&xn[head], 1);
     }
 }
 
@@ -80,17 +84,37 @@ cudaError_t int8_drop_restored(kvc_handle* h, const int32_t* h_cut, cudaStream_t
     int32_t* xmap = reinterpret_cast<int32_t*>(h->state + h->L.xmap);
     bool changed = false;
     for (int b = 0; b < s.B; ++b)
-        for (int hh = 0; hh < s.Hkv; ++hh)
+        for (int hh = 0; hh < s.Hkv; ++hh) {
+            const size_t head = (size_t)b * s.Hkv + hh;
+            bool head_changed = false;
             for (int blk = 0; blk < nblk; ++blk) {
-                const size_t i = ((size_t)b * s.Hkv + hh) * nblk + blk;
+                const size_t i = head * nblk + blk;
                 if (h->xmap_h[i] < 0 || (blk + 1) * kQBlock <= h_cut[b]) continue;
                 h->xfree.push_back(h->xmap_h[i]);
                 h->xmap_h[i] = -1;
-                h->xn_h[(size_t)b * s.Hkv + hh] -= 1;
+                h->xn_h[head] -= 1;
                 cudaError_t e = cudaMemsetAsync(xmap + i, 0xff, 4, st);
                 if (e != cudaSuccess) return e;
-                changed = true;
+                head_changed = true;
             }
+            if (!head_changed) continue;
+            // the head's list keeps its surviving blocks, in their order
+            int n = 0;
+            for (int j = 0; j < kMaxRestored && n < h->xn_h[head]; ++j) {
+                const int32_t blk = h->xlist_h[head * kMaxRestored + j];
+                if (h->xmap_h[head * nblk + blk] != h->xent_h[head * kMaxRestored + j]) continue;
+                h->xlist_h[head * kMaxRestored + n] = blk;
+                h->xent_h[head * kMaxRestored + n] = h->xent_h[head * kMaxRestored + j];
+                ++n;
+            }
+            for (const auto& pr : {std::make_pair(h->L.xlist, &h->xlist_h), std::make_pair(h->L.xent, &h->xent_h)}) {
+                cudaError_t e = cudaMemcpyAsync(h->state + pr.first + head * kMaxRestored * 4,
+                                                pr.second->data() + head * kMaxRestored, (size_t)n * 4,
+                                                cudaMemcpyHostToDevice, st);
+                if (e != cudaSuccess) return e;
+            }
+            changed = true;
+        }
     if (!changed) return cudaSuccess;
     return cudaMemcpyAsync(h->state + h->L.xn, h->xn_h.data(), h->xn_h.size() * 4, cudaMemcpyHostToDevice, st);
 }
@@ -112,16 +136,19 @@ extern "C" int kvc_int8_gate(const float* h_risk, int32_t B, int32_t Hkv, int32_
                              int32_t max_blocks, int32_t* h_sel, int32_t* h_n_sel) {
     if (!h_risk || !h_n_sel || B < 1 || Hkv < 1 || nblk < 0 || max_blocks < 0 || (max_blocks > 0 && !h_sel))
         return KVC_ERR_ARG;
-    struct Cand { float r; int32_t b, h, k; };
+    struct Cand { float r; int32_t b, h, k; size_t idx; };
     std::vector<Cand> c;
     for (int32_t b = 0; b < B; ++b)
         for (int32_t hh = 0; hh < Hkv; ++hh)
             for (int32_t k = 0; k < nblk; ++k) {
                 const float r = h_risk[((size_t)b * Hkv + hh) * nblk + k];
-                if (std::tanh((double)r) > tau) c.push_back({r, b, hh, k});
+                if (std::tanh((double)r) > tau) c.push_back({r, b, hh, k, 0});
             }
-    std::stable_sort(c.begin(), c.end(), [](const Cand& x, const Cand& y) { return x.r > y.r; });
+    // highest risk first; ties in (request, head, block) order, the order of c
+    for (size_t i = 0; i < c.size(); ++i) c[i].idx = i;
     const int32_t n = (int32_t)std::min<size_t>(c.size(), (size_t)max_blocks);
+    std::partial_sort(c.begin(), c.begin() + n, c.end(),
+                      [](const Cand& x, const Cand& y) { return x.r > y.r || (x.r == y.r && x.idx < y.idx); });
     for (int32_t i = 0; i < n; ++i) {
         h_sel[3 * i] = c[i].b;
         h_sel[3 * i + 1] = c[i].h;
@@ -155,21 +182,29 @@ extern "C" int kvc_int8_restore(kvc_t h, const int32_t* h_blocks, int32_t n, con
         for (const auto& e : todo)
             if (++per[(size_t)e.x * s.Hkv + e.y] > kMaxRestored) return KVC_ERR_CAPACITY;
     }
-    for (auto& e : todo) {
+    std::vector<int> slots(todo.size());
+    for (size_t i = 0; i < todo.size(); ++i) {
+        int4& e = todo[i];
+        const size_t head = (size_t)e.x * s.Hkv + e.y;
         e.w = h->xfree.back();
         h->xfree.pop_back();
-        h->xmap_h[((size_t)e.x * s.Hkv + e.y) * nblk + e.z] = e.w;
-        h->xn_h[(size_t)e.x * s.Hkv + e.y] += 1;
+        h->xmap_h[head * nblk + e.z] = e.w;
+        slots[i] = h->xn_h[head];
+        h->xlist_h[head * kMaxRestored + slots[i]] = e.z;
+        h->xent_h[head * kMaxRestored + slots[i]] = e.w;
+        h->xn_h[head] += 1;
     }
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     for (size_t i0 = 0; i0 < todo.size(); i0 += kRestoreBatch) {
         RestoreList L;
         L.n = (int)std::min<size_t>(kRestoreBatch, todo.size() - i0);
         std::memcpy(L.e, todo.data() + i0, L.n * sizeof(int4));
+        std::memcpy(L.slot, slots.data() + i0, L.n * sizeof(int));
         restore_kernel<<<L.n, 256, 0, st>>>(
             L, static_cast<const __nv_bfloat16*>(d_k_full), static_cast<const __nv_bfloat16*>(d_v_full),
             reinterpret_cast<__nv_bfloat16*>(h->state + h->L.xpool), reinterpret_cast<__half*>(h->state + h->L.wit),
             reinterpret_cast<int32_t*>(h->state + h->L.xmap), reinterpret_cast<int32_t*>(h->state + h->L.xn),
+            reinterpret_cast<int32_t*>(h->state + h->L.xlist), reinterpret_cast<int32_t*>(h->state + h->L.xent),
             s.Hkv, s.S, s.d);
         if (cudaGetLastError() != cudaSuccess) return KVC_ERR_CUDA;
     }

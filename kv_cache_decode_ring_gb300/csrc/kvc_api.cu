@@ -64,9 +64,10 @@ bool make_shape(const kvc_config& c, Shape* s) {
     const long long keys = (s->W > 0 && s->W < s->S) ? s->W : s->S;
     s->max_splits = (int)((keys + s->split - 1) / s->split);
     if (int8) {
-        // quantized splits of kInt8Split keys plus one split for the exact tail rows
+        // quantized splits of kInt8Split keys, one split for the exact tail rows and,
+        // with a pool, the splits of the exact-block decode
         s->split = kInt8Split;
-        s->max_splits = (int)((keys + kInt8Split - 1) / kInt8Split) + 1;
+        s->max_splits = (int)((keys + kInt8Split - 1) / kInt8Split) + 1 + (s->xpool > 0 ? kExactSplits : 0);
     }
     return true;
 }
@@ -92,6 +93,8 @@ Layout make_layout(const Shape& s) {
         L.vtail = take(B * Hkv * kQBlock * d * 2);
         L.xmap = take(B * Hkv * (S / kQBlock) * 4);
         L.xn = take(B * Hkv * 4);
+        L.xlist = take(B * Hkv * kMaxRestored * 4);
+        L.xent = take(B * Hkv * kMaxRestored * 4);
         L.xpool = take((size_t)s.xpool * 2 * kQBlock * d * 2);
     }
     L.rope = take((size_t)s.P * (d / 2) * 8);
@@ -226,6 +229,8 @@ int kvc_create(const kvc_config* cfg, void* d_state, size_t bytes, kvc_stream_t 
         e = cudaMemsetAsync(h->state + L.xmap, 0xff, nb * 4, st);
         h->xmap_h.assign(nb, -1);
         h->xn_h.assign((size_t)s.B * s.Hkv, 0);
+        h->xlist_h.assign((size_t)s.B * s.Hkv * kMaxRestored, 0);
+        h->xent_h.assign((size_t)s.B * s.Hkv * kMaxRestored, 0);
         for (int i = s.xpool - 1; i >= 0; --i) h->xfree.push_back(i);
     }
     if (e == cudaSuccess && s.rope) {

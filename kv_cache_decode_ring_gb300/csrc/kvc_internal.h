@@ -22,6 +22,8 @@ constexpr int kFastSplit = 128;       // keys per split, bf16 fast decode kernel
 constexpr int kInt8Split = 1024;      // keys per quantized split, INT8 decode kernel
 constexpr int kGqaSplit = 512;        // keys per split, bf16 decode kernel for 4 or 8 heads per KV head
 constexpr int kMaxRestored = 1024;    // INT8 blocks restored to full precision per (request, KV head)
+constexpr int kExactBlocksPerCta = 64; // restored blocks one CTA of the exact-block decode serves
+constexpr int kExactSplits = kMaxRestored / kExactBlocksPerCta;   // their split slots per query head
 constexpr uint32_t kErrPosition = 1u; // device error bits (sticky, cleared by kvc_device_status)
 constexpr uint32_t kErrWait = 2u;
 
@@ -37,7 +39,9 @@ struct Layout {
     size_t ktail, vtail;  // bf16 [B][Hkv][16][d]              (INT8)
     size_t xmap;      // int32 [B][Hkv][S/16] pool entry of a restored block, -1 = quantized (INT8)
     size_t xn;        // int32 [B][Hkv] restored blocks per (request, KV head)        (INT8)
-    size_t xpool;     // bf16 [pool][2][16][d] K and V rows of the restored blocks    (INT8)
+    size_t xlist;     // int32 [B][Hkv][kMaxRestored] their block indices, then      (INT8)
+    size_t xent;      // int32 [B][Hkv][kMaxRestored] their pool entries              (INT8)
+    size_t xpool;     // bf16 [pool][2][16 d] K and V rows, xk_offset / xv_offset     (INT8)
     size_t rope;      // float2 [P][d/2] {cos, sin}
     size_t part_ml;   // float2 [B][Hq][max_splits] {m (log2 domain), l}
     size_t part_acc;  // float  [B][Hq][max_splits][d]
@@ -115,6 +119,8 @@ bool make_tensor_map_bf16(CUtensorMap* tm, void* base, int rank, const cuuint64_
 cudaError_t launch_append_token(const AppendArgs& a, cudaStream_t st);
 // INT8 gated fallback (int8_gate.cu): drop restored blocks that a trim removed
 cudaError_t int8_drop_restored(kvc_handle* h, const int32_t* h_cut, cudaStream_t st);
+// INT8 exact-block decode (int8_exact.cu): the restored blocks' splits
+cudaError_t launch_int8_exact(kvc_handle* h, const void* q, float* ct, cudaStream_t st);
 // maps: required when the GQA kernel serves the shape (split == kGqaSplit)
 cudaError_t launch_decode(const DecodeArgs& d, const CombineArgs& c, bool fast, const KvMaps* maps, cudaStream_t st);
 bool chunk_supported(const Shape& s);
@@ -141,6 +147,25 @@ __host__ __device__ __forceinline__ int vq_offset(int d, int t, int x) {
     const int cpr = d / 32;                          // 16-byte chunks per lane run
     const int swz = (lane / (8 / cpr)) % cpr;
     return lane * (d / 2) + (((f >> 2) ^ swz) << 4) + ((f & 3) << 2) + (t & 3);
+}
+
+// Restored (exact) blocks live in the pool as bf16 in the order of the exact-block
+// decode's MMA operand fragments; byte offsets inside the K half and the V half of a
+// pool entry for (token t of the block, dim x), d in {64, 128}:
+//  K: rows of 2d bytes; the 16-byte chunk c (8 dims) of row t sits at c ^ s, with
+//     s = 2 (c / 8) + (t mod 2) at d = 128 and s = t mod 2 at d = 64;
+//  V: lane L = 4 (x mod 8) + t/4 owns d/16 chunks of 16 bytes, one per group of 16
+//     dims (x/16), XOR-swizzled by lane; inside a chunk the words are (dim 16i + L/4:
+//     tokens 4 (L mod 4) + 0,1), (... + 2,3), (dim 16i + 8 + L/4: + 0,1), (... + 2,3).
+__host__ __device__ __forceinline__ int xk_offset(int d, int t, int x) {
+    const int c = x >> 3;
+    const int s = d == 128 ? (((c >> 3) << 1) | (t & 1)) : (t & 1);
+    return t * 2 * d + ((c ^ s) << 4) + (x & 7) * 2;
+}
+__host__ __device__ __forceinline__ int xv_offset(int d, int t, int x) {
+    const int lane = 4 * (x & 7) + (t >> 2), i = x >> 4, j = (x >> 3) & 1, q = t & 3;
+    const int swz = d == 128 ? (lane & 7) : ((lane >> 1) & 3);
+    return lane * (d / 16) * 16 + ((i ^ swz) << 4) + (j * 2 + (q >> 1)) * 4 + (q & 1) * 2;
 }
 
 // ---- device helpers -----------------------------------------------------------
@@ -183,4 +208,5 @@ struct kvc_handle {
     // INT8 gated fallback: host mirrors of the block map and the per-head counts, and
     // the free pool entries
     std::vector<int32_t> xmap_h, xn_h, xfree;
+    std::vector<int32_t> xlist_h, xent_h;   // mirrors of the per-head lists
 };
