@@ -86,6 +86,13 @@ typedef struct {
                              pass KVC_F32 + 1 or KVC_BF16 + 1 */
     int32_t int8_exact_blocks; /* INT8 only: capacity of the pool of blocks restored
                              to full precision by kvc_int8_restore (0 = none) */
+    int32_t page_pool;    /* paged K/V storage ([LEAN] §6.1 block table; [LOOP] §八 Q1,
+                             16-token pages mapped on demand): 0 = each
+                             request owns `capacity` slots; > 0 = K and V live in a pool
+                             of page_pool pages of 16 slots (all KV heads of one request)
+                             mapped by a per-request block table, allocated on append and
+                             freed by trim.  Not with INT8 or kvc_chunk_attn; capacity
+                             (the per-request logical slots) must be a multiple of 16. */
 } kvc_config;
 
 /* Bytes of the device state buffer for `cfg` (cache rows, positions,
@@ -248,8 +255,11 @@ enum {
     KVC_EXPORT_WITNESS = 8,       /* fp16 [B][Hkv][capacity][16]          (INT8) */
     KVC_EXPORT_KTAIL = 9,         /* bf16 [B][Hkv][16][d] exact tail rows (INT8) */
     KVC_EXPORT_VTAIL = 10,
-    KVC_EXPORT_XMAP = 11          /* int32 [B][Hkv][capacity/16]: pool entry of a restored
+    KVC_EXPORT_XMAP = 11,         /* int32 [B][Hkv][capacity/16]: pool entry of a restored
                                      block, -1 = quantized (INT8) */
+    KVC_EXPORT_PAGE_TABLE = 12    /* int32 [B][capacity/16]: physical page of each logical
+                                     page, -1 = none (paged caches; K and V exports are
+                                     gathered through it into [B][Hkv][capacity][d]) */
 };
 int kvc_export_bytes(kvc_t h, int32_t which, size_t* bytes);
 int kvc_export(kvc_t h, int32_t which, void* h_dst, size_t bytes, kvc_stream_t stream);

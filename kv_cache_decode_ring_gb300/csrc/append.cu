@@ -8,6 +8,10 @@
 // [WITCERT] "频带酉性与双层证书": per-token, per-band residual norms w_{t,b} (16 x fp16);
 //        "SGLang 生产级落地与闭环门控修复": per-block scales; the write kernel
 //        quantizes and records the band norms.
+#include <algorithm>
+#include <cstring>
+#include <vector>
+
 #include "kvc_internal.h"
 
 namespace kvc {
@@ -129,7 +133,7 @@ __global__ void __launch_bounds__(kThreads) append_token_kernel(const AppendArgs
         for (int idx = threadIdx.x; idx < a.Hkv * half; idx += blockDim.x) {
             const int h = idx / half, i = idx % half;
             const size_t src = ((size_t)b * a.Hkv + h) * d;
-            const size_t dst = (((size_t)b * a.Hkv + h) * a.S + slot) * d;
+            const size_t dst = kv_row(a.table, b, h, slot, a.Hkv, a.S) * d;
             float y0, y1;
             key_pair(a, a.k, src, i, p, y0, y1);
             store_pair(a.kc, dst + 2 * i, y0, y1, a.bf16);
@@ -201,7 +205,7 @@ __global__ void __launch_bounds__(kThreads) append_rows_kernel(const AppendArgs 
     }
     const int slot = a.ring ? (int)(p % a.S) : (int)p;
     const size_t src = (size_t)b * a.sb + (size_t)h * a.sh + (size_t)r * a.sr;
-    const size_t dst = (((size_t)b * a.Hkv + h) * a.S + slot) * d;
+    const size_t dst = kv_row(a.table, b, h, slot, a.Hkv, a.S) * d;
     float y0, y1;
     key_pair(a, a.k, src, i, (int)p, y0, y1);
     store_pair(a.kc, dst + 2 * i, y0, y1, a.bf16);
@@ -308,7 +312,71 @@ __global__ void trim_kernel(int32_t* next_pos, int32_t* pos, const Group g, int 
 
 size_t quant_smem(int d) { return (size_t)(2 * kQBlock * d + 64) * sizeof(float); }
 
+// ---- paged caches: the block table ------------------------------------------
+constexpr int kTableBatch = 256;
+
+struct TableUpdates {
+    int n;
+    int2 e[kTableBatch];                  // (table index, physical page)
+};
+
+__global__ void table_update_kernel(const TableUpdates u, int32_t* table) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < u.n) table[u.e[i].x] = u.e[i].y;
+}
+
 }  // namespace
+
+// Map the pages that slots [from[b], to[b]) of every request b need (a ring's slots
+// wrap modulo S), from the host free list; the device table follows on `st`.  On
+// exhaustion nothing is mapped and *status = KVC_ERR_CAPACITY.
+cudaError_t map_pages(kvc_handle* h, const std::vector<int>& from, const std::vector<int>& to, cudaStream_t st,
+                      int* status) {
+    const Shape& s = h->sh;
+    const int np = s.S / kPage;
+    std::vector<int> need;                 // table indices to map, in request and page order
+    for (int b = 0; b < s.B; ++b) {
+        const long long lo = from[b], hi = to[b];
+        if (hi <= lo) continue;
+        for (int lp = 0; lp < np; ++lp) {
+            const size_t idx = (size_t)b * np + lp;
+            if (h->table_h[idx] >= 0) continue;
+            bool touch;
+            if (!s.ring) {
+                touch = (long long)lp * kPage < hi && (long long)(lp + 1) * kPage > lo;
+            } else if (hi - lo >= s.S) {
+                touch = true;
+            } else {                           // slots lo % S .. (hi - 1) % S, possibly wrapping
+                const long long a0 = lo % s.S, a1 = (hi - 1) % s.S;
+                const long long p0 = (long long)lp * kPage, p1 = p0 + kPage - 1;
+                touch = a0 <= a1 ? (p0 <= a1 && p1 >= a0) : (p1 >= a0 || p0 <= a1);
+            }
+            if (touch) need.push_back((int)idx);
+        }
+    }
+    *status = KVC_OK;
+    if (need.empty()) return cudaSuccess;
+    if (need.size() > h->page_free.size()) { *status = KVC_ERR_CAPACITY; return cudaSuccess; }
+    std::vector<int2> upd;
+    for (int idx : need) {
+        const int page = h->page_free.back();
+        h->page_free.pop_back();
+        h->table_h[idx] = page;
+        upd.push_back(make_int2(idx, page));
+    }
+    int32_t* table = reinterpret_cast<int32_t*>(h->state + h->L.table);
+    if (upd.size() > 4 * (size_t)kTableBatch)      // a large prefill: the whole table at once
+        return cudaMemcpyAsync(table, h->table_h.data(), h->table_h.size() * 4, cudaMemcpyHostToDevice, st);
+    for (size_t i0 = 0; i0 < upd.size(); i0 += kTableBatch) {
+        TableUpdates u;
+        u.n = (int)std::min<size_t>(kTableBatch, upd.size() - i0);
+        std::memcpy(u.e, upd.data() + i0, u.n * sizeof(int2));
+        table_update_kernel<<<1, kTableBatch, 0, st>>>(u, table);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
 
 cudaError_t launch_append_token(const AppendArgs& a, cudaStream_t st) {
     const size_t smem = a.int8 ? quant_smem(a.d) : 0;

@@ -54,10 +54,9 @@ __global__ void __launch_bounds__(kThreads) decode_generic_kernel(const DecodeAr
     float* s = smem + g * d;       // [g][split]
     load_query(a, b, kvh, len - 1, BF16, q);
     __syncthreads();
-    const size_t base = ((size_t)b * a.Hkv + kvh) * a.S;
     for (int idx = threadIdx.x; idx < g * nk; idx += blockDim.x) {
         const int hh = idx / nk, j = idx % nk;
-        const size_t row = (base + k0 + j) * d;
+        const size_t row = kv_row(a.table, b, kvh, k0 + j, a.Hkv, a.S) * d;
         float acc = 0.f;
         for (int i = 0; i < d; ++i) acc = fmaf(q[hh * d + i], ld_elem(a.k, row + i, BF16), acc);
         s[hh * a.split + j] = acc * a.scale_log2;
@@ -82,7 +81,8 @@ __global__ void __launch_bounds__(kThreads) decode_generic_kernel(const DecodeAr
     for (int idx = threadIdx.x; idx < g * d; idx += blockDim.x) {
         const int hh = idx / d, i = idx % d;
         float acc = 0.f;
-        for (int j = 0; j < nk; ++j) acc = fmaf(s[hh * a.split + j], ld_elem(a.v, (base + k0 + j) * d + i, BF16), acc);
+        for (int j = 0; j < nk; ++j)
+            acc = fmaf(s[hh * a.split + j], ld_elem(a.v, kv_row(a.table, b, kvh, k0 + j, a.Hkv, a.S) * d + i, BF16), acc);
         a.part_acc[(((size_t)b * a.Hq + (size_t)kvh * g + hh) * a.max_splits + chunk) * d + i] = acc;
     }
 }
@@ -115,6 +115,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Combi
     const int len = c.next_pos[b];
     int lo, hi;
     key_range(len, c.S, c.W, c.ring, lo, hi);
+    if (c.align_lo) lo &= ~(kPage - 1);             // the paged GQA decode's split origin
     const int ns = (hi - lo + c.split - 1) / c.split;
     const size_t row = (size_t)b * c.Hq + hq;
     const float2* ml = c.part_ml + row * c.max_splits;

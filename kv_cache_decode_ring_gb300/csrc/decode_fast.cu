@@ -92,8 +92,19 @@ __global__ void __launch_bounds__(kWarps * 32, 3) decode_fast_kernel(const Decod
         if ((threadIdx.x & 31) == 0 && nk > 0) {
             const uint32_t bytes = (uint32_t)nk * C::ROWB;
             mbar_arrive_expect_tx(&bar[warp_], 2 * bytes);
-            bulk_copy_g2s(myK, Kg + (head_row0 + k0) * D, bytes, &bar[warp_]);
-            bulk_copy_g2s(myV, Vg + (head_row0 + k0) * D, bytes, &bar[warp_]);
+            if (!a.table) {
+                bulk_copy_g2s(myK, Kg + (head_row0 + k0) * D, bytes, &bar[warp_]);
+                bulk_copy_g2s(myV, Vg + (head_row0 + k0) * D, bytes, &bar[warp_]);
+            } else {
+                // paged: one copy per run of rows inside one page
+                for (int r = 0; r < nk;) {
+                    const int run = min(nk - r, kPage - (k0 + r) % kPage);
+                    const size_t row = kv_row(a.table, b, kvh, k0 + r, a.Hkv, a.S);
+                    bulk_copy_g2s(myK + r * C::ROWB, Kg + row * D, (uint32_t)run * C::ROWB, &bar[warp_]);
+                    bulk_copy_g2s(myV + r * C::ROWB, Vg + row * D, (uint32_t)run * C::ROWB, &bar[warp_]);
+                    r += run;
+                }
+            }
         }
     };
     if ((threadIdx.x & 31) == 0) {

@@ -109,21 +109,23 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     const int len = a.next_pos[b];
     int lo, hi;
     key_range(len, a.S, a.W, a.ring, lo, hi);
-    const int nsplit = (hi - lo + kSplit - 1) / kSplit;
+    // a paged cache aligns its tiles to pages (keys before the window are masked)
+    const int lo_t = a.table ? (lo & ~(kPage - 1)) : lo;
+    const int nsplit = (hi - lo_t + kSplit - 1) / kSplit;
     if (split >= nsplit) return;
 
-    const int head_row0 = (b * a.Hkv + kvh) * a.S;       // tensor-map row of key slot 0
+    const int head_row0 = (b * a.Hkv + kvh) * a.S;       // tensor-map row of key slot 0 (unpaged)
     unsigned char* myS = smem + warp * C::WARPB;
     uint64_t* myBar = bar + warp * kStages;
     // keys of this warp's tile i: 16 consecutive rows, tiles of the 4 warps interleaved
-    auto tile_k0 = [&](int i) { return lo + split * kSplit + (i * kWarps + warp) * kTileKeys; };
+    auto tile_k0 = [&](int i) { return lo_t + split * kSplit + (i * kWarps + warp) * kTileKeys; };
     auto tile_nk = [&](int i) { return max(0, min(kTileKeys, hi - tile_k0(i))); };
     // lane 0: the tile's K and V boxes (always 16 full rows) on the stage's barrier
     auto issue = [&](int i) {
         if (lane == 0 && tile_nk(i) > 0) {
             const int sg = i % kStages;
             unsigned char* st = myS + sg * C::STAGEB;
-            const int row = head_row0 + tile_k0(i);
+            const int row = a.table ? (int)kv_row(a.table, b, kvh, tile_k0(i), a.Hkv, a.S) : head_row0 + tile_k0(i);
             mbar_arrive_expect_tx(&myBar[sg], (uint32_t)C::STAGEB);
 #pragma unroll
             for (int j = 0; j < C::NBOX; ++j) {
@@ -198,6 +200,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     for (int i = 0; i < kTilesPerWarp; ++i) {
         const int nk = tile_nk(i);
         if (nk == 0) break;                       // later tiles of this warp are empty too
+        const int kmin = lo - tile_k0(i);         // keys of the tile before the window
         const int sg = i % kStages;
         const uint32_t par = (uint32_t)((i / kStages) & 1);
         unsigned char* tK = myS + sg * C::STAGEB;
@@ -231,8 +234,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
         bool rescale = false;
 #pragma unroll
         for (int nt = 0; nt < C::NT; ++nt) {
-            const float s0 = g < nk ? sacc[nt][0] + sacc[nt][1] : -INFINITY;
-            const float s1 = g + 8 < nk ? sacc[nt][2] + sacc[nt][3] : -INFINITY;
+            const float s0 = g < nk && g >= kmin ? sacc[nt][0] + sacc[nt][1] : -INFINITY;
+            const float s1 = g + 8 < nk && g + 8 >= kmin ? sacc[nt][2] + sacc[nt][3] : -INFINITY;
             float bm = fmaxf(s0, s1);
             bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
             bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));

@@ -39,6 +39,7 @@ bool make_shape(const kvc_config& c, Shape* s) {
     if (int8 && (c.dtype != KVC_BF16 || ring || c.window != 0 || c.head_dim % kBands || c.capacity % kQBlock))
         return false;
     if (c.int8_exact_blocks < 0 || (!int8 && c.int8_exact_blocks != 0)) return false;
+    if (c.page_pool < 0 || (c.page_pool > 0 && (int8 || c.capacity % kPage))) return false;
     if (int8) {
         const int g = c.n_q_heads / c.n_kv_heads;
         if ((c.head_dim != 64 && c.head_dim != 128) || (g != 1 && g != 2 && g != 4 && g != 8)) return false;
@@ -55,14 +56,16 @@ bool make_shape(const kvc_config& c, Shape* s) {
     s->elem = s->bf16 ? 2 : 4;
     s->max_chunk = c.max_chunk;
     s->xpool = c.int8_exact_blocks;
+    s->pages = c.page_pool;
     s->out_bf16 = c.out_dtype == 0 ? s->bf16 : c.out_dtype == KVC_BF16 + 1;
     s->split = kGenericSplit;
     if (s->bf16 && !int8 && (s->d == 64 || s->d == 128) && s->g <= 8) s->split = kFastSplit;
     // (its tensor copies address cache rows with signed 32-bit coordinates)
-    if (s->bf16 && !int8 && gqa_decode_supported(s->d, s->g) && (long long)s->B * s->Hkv * s->S < (1ll << 31))
-        s->split = kGqaSplit;
+    const long long rows = s->pages ? (long long)s->pages * s->Hkv * kPage : (long long)s->B * s->Hkv * s->S;
+    if (s->bf16 && !int8 && gqa_decode_supported(s->d, s->g) && rows < (1ll << 31)) s->split = kGqaSplit;
     const long long keys = (s->W > 0 && s->W < s->S) ? s->W : s->S;
-    s->max_splits = (int)((keys + s->split - 1) / s->split);
+    // a paged cache may start its splits up to one page before the window
+    s->max_splits = (int)((keys + s->split - 1) / s->split) + (s->pages > 0 ? 1 : 0);
     if (int8) {
         // quantized splits of kInt8Split keys, one split for the exact tail rows and,
         // with a pool, the splits of the exact-block decode
@@ -81,8 +84,10 @@ Layout make_layout(const Shape& s) {
     L.next_pos = take(B * 4);
     L.pos = take(B * S * 4);
     if (!s.int8) {
-        L.k = take(B * Hkv * S * d * s.elem);
-        L.v = take(B * Hkv * S * d * s.elem);
+        const size_t rows = s.pages ? (size_t)s.pages * Hkv * kPage : B * Hkv * S;
+        L.k = take(rows * d * s.elem);
+        L.v = take(rows * d * s.elem);
+        if (s.pages) L.table = take(B * (S / kPage) * 4);
     } else {
         L.kq = take(B * Hkv * S * d);
         L.vq = take(B * Hkv * S * d);
@@ -147,6 +152,7 @@ AppendArgs append_args(kvc_handle* h, const void* k, const void* v, int n) {
     }
     a.rope = s.rope ? at<float2>(h, h->L.rope) : nullptr;
     a.hdr = at<uint32_t>(h, h->L.hdr);
+    a.table = s.pages ? at<int32_t>(h, h->L.table) : nullptr;
     a.B = s.B; a.Hkv = s.Hkv; a.d = s.d; a.S = s.S; a.P = s.P;
     a.ring = s.ring; a.bf16 = s.bf16; a.int8 = s.int8;
     return a;
@@ -206,7 +212,8 @@ int kvc_create(const kvc_config* cfg, void* d_state, size_t bytes, kvc_stream_t 
     h->has_kv_maps = false;
     if (s.split == kGqaSplit) {
         // the GQA decode reads 16-row tiles of the K and V caches by tensor copy
-        const cuuint64_t dims[2] = {(cuuint64_t)s.d, (cuuint64_t)s.B * s.Hkv * s.S};
+        const cuuint64_t dims[2] = {(cuuint64_t)s.d,
+                                    s.pages ? (cuuint64_t)s.pages * s.Hkv * kPage : (cuuint64_t)s.B * s.Hkv * s.S};
         const cuuint64_t strides[1] = {(cuuint64_t)s.d * 2};
         const cuuint32_t box[2] = {64, 16};
         if (!make_tensor_map_bf16(&h->kv_maps.k, h->state + L.k, 2, dims, strides, box) ||
@@ -224,6 +231,19 @@ int kvc_create(const kvc_config* cfg, void* d_state, size_t bytes, kvc_stream_t 
     cudaStream_t st = S_(stream);
     cudaError_t e = cudaMemsetAsync(h->state, 0, L.total, st);
     if (e == cudaSuccess) e = cudaMemsetAsync(h->state + L.pos, 0xff, (size_t)s.B * s.S * 4, st);
+    if (e == cudaSuccess && s.pages) {
+        // every logical page unmapped; the free pages in a fixed shuffled order, so
+        // that requests' pages interleave in the pool
+        e = cudaMemsetAsync(h->state + L.table, 0xff, (size_t)s.B * (s.S / kPage) * 4, st);
+        h->table_h.assign((size_t)s.B * (s.S / kPage), -1);
+        h->page_free.resize(s.pages);
+        for (int i = 0; i < s.pages; ++i) h->page_free[i] = i;
+        uint64_t x = 0x9E3779B97F4A7C15ull;
+        for (int i = s.pages - 1; i > 0; --i) {
+            x ^= x << 13; x ^= x >> 7; x ^= x << 17;
+            std::swap(h->page_free[i], h->page_free[x % (uint64_t)(i + 1)]);
+        }
+    }
     if (e == cudaSuccess && s.int8) {
         const size_t nb = (size_t)s.B * s.Hkv * (s.S / kQBlock);
         e = cudaMemsetAsync(h->state + L.xmap, 0xff, nb * 4, st);
@@ -256,6 +276,13 @@ int kvc_append(kvc_t h, const void* d_k, const void* d_v, kvc_stream_t stream) {
     if (!h || !d_k || !d_v || !aligned16(d_k) || !aligned16(d_v)) return KVC_ERR_ARG;
     int rc = check_capacity(h, nullptr, 1);
     if (rc) return rc;
+    if (h->sh.pages) {
+        std::vector<int> to(h->np.begin(), h->np.end());
+        for (auto& t : to) ++t;
+        if (map_pages(h, std::vector<int>(h->np.begin(), h->np.end()), to, S_(stream), &rc) != cudaSuccess)
+            return KVC_ERR_CUDA;
+        if (rc) return rc;
+    }
     AppendArgs a = append_args(h, d_k, d_v, 1);
     if (launch_append_token(a, S_(stream)) != cudaSuccess) return KVC_ERR_CUDA;
     for (auto& p : h->np) ++p;
@@ -277,6 +304,12 @@ int kvc_append_rows(kvc_t h, const void* d_k, const void* d_v, int32_t n, const 
         }
     int rc = check_capacity(h, h->counts.data(), n);
     if (rc) return rc;
+    if (s.pages) {
+        std::vector<int> from(h->np.begin(), h->np.end()), to(from);
+        for (int b = 0; b < s.B; ++b) to[b] += h->counts[b];
+        if (map_pages(h, from, to, S_(stream), &rc) != cudaSuccess) return KVC_ERR_CUDA;
+        if (rc) return rc;
+    }
     AppendArgs a = append_args(h, d_k, d_v, n);
     if (launch_append_rows_counts(a, h->counts.data(), S_(stream)) != cudaSuccess) return KVC_ERR_CUDA;
     bool any = false;
@@ -305,6 +338,7 @@ int kvc_decode_attn(kvc_t h, const void* d_q, void* d_out, float* d_cmax, float*
     a.part_ml = at<float2>(h, h->L.part_ml);
     a.part_acc = at<float>(h, h->L.part_acc);
     a.hdr = at<uint32_t>(h, h->L.hdr);
+    a.table = s.pages ? at<int32_t>(h, h->L.table) : nullptr;
     a.B = s.B; a.Hq = s.Hq; a.Hkv = s.Hkv; a.g = s.g; a.d = s.d; a.S = s.S; a.W = s.W;
     a.max_splits = s.max_splits; a.split = s.split; a.ring = s.ring; a.bf16 = s.bf16;
     a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)s.d));
@@ -312,6 +346,7 @@ int kvc_decode_attn(kvc_t h, const void* d_q, void* d_out, float* d_cmax, float*
     c.part_ml = a.part_ml; c.part_acc = a.part_acc; c.next_pos = a.next_pos; c.out = d_out;
     c.B = s.B; c.Hq = s.Hq; c.d = s.d; c.S = s.S; c.W = s.W; c.max_splits = s.max_splits;
     c.split = s.split; c.ring = s.ring; c.bf16 = s.out_bf16;
+    c.align_lo = s.pages > 0 && s.split == kGqaSplit;
     const bool fast = s.split == kFastSplit && fast_decode_supported(a);
     if (launch_decode(a, c, fast, h->has_kv_maps ? &h->kv_maps : nullptr, st) != cudaSuccess) return KVC_ERR_CUDA;
     if (d_cmax && cudaMemsetAsync(d_cmax, 0, (size_t)s.B * s.Hq * 4, st) != cudaSuccess) return KVC_ERR_CUDA;
@@ -336,6 +371,22 @@ int kvc_trim(kvc_t h, const int32_t* h_cut, kvc_stream_t stream) {
                          S_(stream)) != cudaSuccess)
         return KVC_ERR_CUDA;
     if (s.int8 && int8_drop_restored(h, h_cut, S_(stream)) != cudaSuccess) return KVC_ERR_CUDA;
+    if (s.pages && !s.ring) {
+        // a contiguous cache returns the pages that lie wholly past the cut
+        bool freed = false;
+        const int npg = s.S / kPage;
+        for (int b = 0; b < s.B; ++b)
+            for (int lp = (h_cut[b] + kPage - 1) / kPage; lp < npg; ++lp) {
+                int32_t& e = h->table_h[(size_t)b * npg + lp];
+                if (e < 0) continue;
+                h->page_free.push_back(e);
+                e = -1;
+                freed = true;
+            }
+        if (freed && cudaMemcpyAsync(h->state + h->L.table, h->table_h.data(), h->table_h.size() * 4,
+                                     cudaMemcpyHostToDevice, S_(stream)) != cudaSuccess)
+            return KVC_ERR_CUDA;
+    }
     for (int b = 0; b < s.B; ++b) h->np[b] = h_cut[b];
     if (s.ring) h->ring_needs_append = true;
     return KVC_OK;
@@ -346,7 +397,7 @@ int kvc_chunk_attn(kvc_t h, const void* d_q, const void* d_k, const void* d_v, i
     if (!h || !d_q || !d_k || !d_v || !d_out || n < 1) return KVC_ERR_ARG;
     if (!aligned16(d_q) || !aligned16(d_k) || !aligned16(d_v) || !aligned16(d_out)) return KVC_ERR_ARG;
     const Shape& s = h->sh;
-    if (!chunk_supported(s)) return KVC_ERR_UNSUPPORTED;
+    if (!chunk_supported(s) || s.pages) return KVC_ERR_UNSUPPORTED;
     if (n > s.max_chunk) return KVC_ERR_ARG;
     int rc = check_capacity(h, nullptr, n);
     if (rc) return rc;
@@ -371,6 +422,9 @@ int kvc_export_bytes(kvc_t h, int32_t which, size_t* bytes) {
             if (s.int8) return KVC_ERR_ARG;
             *bytes = B * Hkv * S * d * s.elem; return KVC_OK;
         case KVC_EXPORT_POSITIONS: *bytes = B * S * 4; return KVC_OK;
+        case KVC_EXPORT_PAGE_TABLE:
+            if (!s.pages) return KVC_ERR_ARG;
+            *bytes = B * (S / kPage) * 4; return KVC_OK;
         case KVC_EXPORT_NEXT_POSITION: *bytes = B * 4; return KVC_OK;
         default: break;
     }
@@ -404,9 +458,30 @@ int kvc_export(kvc_t h, int32_t which, void* h_dst, size_t bytes, kvc_stream_t s
         case KVC_EXPORT_KTAIL: off = h->L.ktail; break;
         case KVC_EXPORT_VTAIL: off = h->L.vtail; break;
         case KVC_EXPORT_XMAP: off = h->L.xmap; break;
+        case KVC_EXPORT_PAGE_TABLE: off = h->L.table; break;
         default: return KVC_ERR_ARG;
     }
     cudaStream_t st = S_(stream);
+    if (h->sh.pages && (which == KVC_EXPORT_K || which == KVC_EXPORT_V)) {
+        // gather the logical [B][Hkv][S][d] rows through the block table (zeros where unmapped)
+        const Shape& s = h->sh;
+        const size_t rowb = (size_t)s.d * s.elem, npg = s.S / kPage;
+        std::vector<uint8_t> pool((size_t)s.pages * s.Hkv * kPage * rowb);
+        if (cudaMemcpyAsync(pool.data(), h->state + off, pool.size(), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+            return KVC_ERR_CUDA;
+        if (cudaStreamSynchronize(st) != cudaSuccess) return KVC_ERR_CUDA;
+        uint8_t* out = static_cast<uint8_t*>(h_dst);
+        std::memset(out, 0, need);
+        for (int b = 0; b < s.B; ++b)
+            for (size_t lp = 0; lp < npg; ++lp) {
+                const int page = h->table_h[b * npg + lp];
+                if (page < 0) continue;
+                for (int hh = 0; hh < s.Hkv; ++hh)
+                    std::memcpy(out + (((size_t)b * s.Hkv + hh) * s.S + lp * kPage) * rowb,
+                                pool.data() + (((size_t)page * s.Hkv + hh) * kPage) * rowb, kPage * rowb);
+            }
+        return KVC_OK;
+    }
     const bool codes = which == KVC_EXPORT_KQ || which == KVC_EXPORT_VQ;
     std::vector<uint8_t> raw(codes ? need : 0);
     void* dst = codes ? static_cast<void*>(raw.data()) : h_dst;

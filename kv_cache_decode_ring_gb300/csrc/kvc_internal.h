@@ -16,6 +16,7 @@
 namespace kvc {
 
 constexpr int kQBlock = 16;           // tokens per INT8 quantization block
+constexpr int kPage = 16;             // slots per page of a paged cache
 constexpr int kBands = 16;            // witness bands per key row
 constexpr int kGenericSplit = 64;     // keys per split, generic decode kernel
 constexpr int kFastSplit = 128;       // keys per split, bf16 fast decode kernel
@@ -32,7 +33,8 @@ struct Layout {
     size_t hdr;       // uint32[64]: [0] error word, [1] work counter, [2] done counter
     size_t next_pos;  // int32 [B]
     size_t pos;       // int32 [B][S]
-    size_t k, v;      // [B][Hkv][S][d] cache dtype            (non-INT8)
+    size_t k, v;      // [B][Hkv][S][d] cache dtype (non-INT8); paged: [pages][Hkv][16][d]
+    size_t table;     // int32 [B][S/16] physical page of each logical page, -1 = none (paged)
     size_t kq, vq;    // int8 [B][Hkv][S][d]                   (INT8)
     size_t sk, sv;    // f32  [B][Hkv][S/16]                   (INT8)
     size_t wit;       // f16  [B][Hkv][S][16]                  (INT8)
@@ -60,6 +62,7 @@ struct Shape {
     int max_splits;
     int max_chunk;               // largest suffix of kvc_chunk_attn (0 = none)
     int xpool;                   // entries of the INT8 exact-block pool
+    int pages;                   // pages of a paged cache (0 = not paged)
 };
 
 bool make_shape(const kvc_config& c, Shape* s);
@@ -75,6 +78,7 @@ struct DecodeArgs {
     float2* part_ml;
     float* part_acc;
     uint32_t* hdr;
+    const int32_t* table; // paged caches: the block table (else nullptr)
     int B, Hq, Hkv, g, d, S, W, max_splits, split;
     int ring;
     int bf16;             // cache dtype (1 = bf16, 0 = fp32)
@@ -87,6 +91,7 @@ struct CombineArgs {
     const int32_t* next_pos;
     void* out;            // [B][Hq][d] cache dtype
     int B, Hq, d, S, W, max_splits, split, ring, bf16;
+    int align_lo;         // splits start at the window start rounded down to a page
 };
 
 struct AppendArgs {
@@ -102,6 +107,7 @@ struct AppendArgs {
     __nv_bfloat16* ktail; __nv_bfloat16* vtail;
     const float2* rope;
     uint32_t* hdr;
+    const int32_t* table; // paged caches: the block table (else nullptr)
     int B, Hkv, d, S, P, ring, bf16, int8;
 };
 
@@ -119,6 +125,9 @@ bool make_tensor_map_bf16(CUtensorMap* tm, void* base, int rank, const cuuint64_
 cudaError_t launch_append_token(const AppendArgs& a, cudaStream_t st);
 // INT8 gated fallback (int8_gate.cu): drop restored blocks that a trim removed
 cudaError_t int8_drop_restored(kvc_handle* h, const int32_t* h_cut, cudaStream_t st);
+// paged caches (append.cu): map the pages that slots [from, to) of each request need
+cudaError_t map_pages(kvc_handle* h, const std::vector<int>& from, const std::vector<int>& to, cudaStream_t st,
+                      int* status);
 // INT8 exact-block decode (int8_exact.cu): the restored blocks' splits
 cudaError_t launch_int8_exact(kvc_handle* h, const void* q, float* ct, cudaStream_t st);
 // maps: required when the GQA kernel serves the shape (split == kGqaSplit)
@@ -181,6 +190,15 @@ __device__ __forceinline__ void rope_pair(float x0, float x1, float2 cs, float& 
     y1 = __fadd_rn(__fmul_rn(x1, cs.x), __fmul_rn(x0, cs.y));
 }
 
+// Row (in rows of d elements) holding slot `slot` of (request b, KV head h): a
+// request's own run of S rows, or row slot % 16 of the head's part of its page.
+__device__ __forceinline__ size_t kv_row(const int32_t* table, int b, int h, int slot, int Hkv, int S) {
+    if (!table) return ((size_t)b * Hkv + h) * S + slot;
+    int page = table[(size_t)b * (S / kPage) + slot / kPage];
+    page = page < 0 ? 0 : page;       // never taken: every slot read or written is mapped first
+    return ((size_t)page * Hkv + h) * kPage + (slot % kPage);
+}
+
 // Cached key slots of request b attended by its newest token (next_position - 1):
 // a ring holds the window in slots [0, min(len, W)); a contiguous cache in
 // slots [len - min(len, W), len).
@@ -209,4 +227,6 @@ struct kvc_handle {
     // the free pool entries
     std::vector<int32_t> xmap_h, xn_h, xfree;
     std::vector<int32_t> xlist_h, xent_h;   // mirrors of the per-head lists
+    // paged caches: host mirror of the block table and the free pages
+    std::vector<int32_t> table_h, page_free;
 };

@@ -24,7 +24,8 @@ KVC_F32, KVC_BF16 = 0, 1
 KVC_CONTIGUOUS, KVC_RING = 0, 1
 KVC_QUANT_NONE, KVC_QUANT_INT8 = 0, 1
 (KVC_EXPORT_K, KVC_EXPORT_V, KVC_EXPORT_POSITIONS, KVC_EXPORT_NEXT_POSITION, KVC_EXPORT_KQ, KVC_EXPORT_VQ,
- KVC_EXPORT_SK, KVC_EXPORT_SV, KVC_EXPORT_WITNESS, KVC_EXPORT_KTAIL, KVC_EXPORT_VTAIL, KVC_EXPORT_XMAP) = range(12)
+ KVC_EXPORT_SK, KVC_EXPORT_SV, KVC_EXPORT_WITNESS, KVC_EXPORT_KTAIL, KVC_EXPORT_VTAIL, KVC_EXPORT_XMAP,
+ KVC_EXPORT_PAGE_TABLE) = range(13)
 
 _STATUS_NAMES = {1: "KVC_ERR_ARG", 2: "KVC_ERR_CAPACITY", 3: "KVC_ERR_EVICTED", 4: "KVC_ERR_CUDA",
                  5: "KVC_ERR_UNSUPPORTED", 6: "KVC_ERR_DEVICE"}
@@ -41,7 +42,7 @@ class kvc_config(ctypes.Structure):
                 ("batch", ctypes.c_int32), ("n_q_heads", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("capacity", ctypes.c_int32), ("window", ctypes.c_int32),
                 ("max_position", ctypes.c_int32), ("rope_base", ctypes.c_float), ("max_chunk", ctypes.c_int32),
-                ("out_dtype", ctypes.c_int32), ("int8_exact_blocks", ctypes.c_int32)]
+                ("out_dtype", ctypes.c_int32), ("int8_exact_blocks", ctypes.c_int32), ("page_pool", ctypes.c_int32)]
 
 
 EXPORTED = ["kvc_state_bytes", "kvc_create", "kvc_destroy", "kvc_append", "kvc_append_rows",
@@ -130,15 +131,16 @@ def kvc_strerror(code: int) -> str:
 
 def make_config(dtype="bf16", layout="contiguous", kv_quant=None, batch=1, n_q_heads=1, n_kv_heads=1,
                 head_dim=128, capacity=1, window=0, max_position=0, rope_base=0.0, max_chunk=0,
-                out_dtype=None, int8_exact_blocks=0) -> kvc_config:
+                out_dtype=None, int8_exact_blocks=0, page_pool=0) -> kvc_config:
     """``out_dtype``: None (the cache dtype), "f32" or "bf16"; ``int8_exact_blocks``: pool
-    entries for blocks the gated fallback restores (INT8 caches)."""
+    entries for blocks the gated fallback restores (INT8 caches); ``page_pool``: pages of 16
+    slots for paged K/V storage (0 = each request owns ``capacity`` slots)."""
     od = 0 if out_dtype is None else (KVC_F32 + 1 if out_dtype == "f32" else KVC_BF16 + 1)
     return kvc_config(KVC_BF16 if dtype == "bf16" else KVC_F32,
                       KVC_RING if layout == "ring" else KVC_CONTIGUOUS,
                       KVC_QUANT_INT8 if kv_quant == "int8" else KVC_QUANT_NONE,
                       batch, n_q_heads, n_kv_heads, head_dim, capacity, window, max_position,
-                      float(rope_base), max_chunk, od, int(int8_exact_blocks))
+                      float(rope_base), max_chunk, od, int(int8_exact_blocks), int(page_pool))
 
 
 def kvc_state_bytes(cfg: kvc_config) -> int:
@@ -268,7 +270,7 @@ class Cache:
     _EXPORT_DTYPES = {KVC_EXPORT_POSITIONS: np.int32, KVC_EXPORT_NEXT_POSITION: np.int32, KVC_EXPORT_KQ: np.int8,
                       KVC_EXPORT_VQ: np.int8, KVC_EXPORT_SK: np.float32, KVC_EXPORT_SV: np.float32,
                       KVC_EXPORT_WITNESS: np.uint16, KVC_EXPORT_KTAIL: np.uint16, KVC_EXPORT_VTAIL: np.uint16,
-                      KVC_EXPORT_XMAP: np.int32}
+                      KVC_EXPORT_XMAP: np.int32, KVC_EXPORT_PAGE_TABLE: np.int32}
 
     def __init__(self, cfg: kvc_config, device="cuda", stream=None):
         self.cfg = cfg
@@ -282,10 +284,11 @@ class Cache:
         self.h = kvc_create(cfg, self.state, stream)
 
     @classmethod
-    def from_workload(cls, w, max_chunk=0, max_position=0, device="cuda", out_dtype=None, int8_exact_blocks=0):
+    def from_workload(cls, w, max_chunk=0, max_position=0, device="cuda", out_dtype=None, int8_exact_blocks=0,
+                      page_pool=0):
         cfg = make_config(w.dtype, w.layout, w.quant, w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.capacity,
                           0 if w.layout == "ring" else w.window, max_position, w.rope_base, max_chunk, out_dtype,
-                          int8_exact_blocks)
+                          int8_exact_blocks, page_pool)
         return cls(cfg, device)
 
     def close(self):
@@ -358,7 +361,8 @@ class Cache:
                   KVC_EXPORT_SK: (self.B, self.Hkv, self.S // 16), KVC_EXPORT_SV: (self.B, self.Hkv, self.S // 16),
                   KVC_EXPORT_WITNESS: (self.B, self.Hkv, self.S, 16), KVC_EXPORT_KTAIL: (self.B, self.Hkv, 16, self.d),
                   KVC_EXPORT_VTAIL: (self.B, self.Hkv, 16, self.d),
-                  KVC_EXPORT_XMAP: (self.B, self.Hkv, self.S // 16)}
+                  KVC_EXPORT_XMAP: (self.B, self.Hkv, self.S // 16),
+                  KVC_EXPORT_PAGE_TABLE: (self.B, self.S // 16)}
         return arr.reshape(shapes[which])
 
     def next_positions(self) -> np.ndarray:

@@ -59,11 +59,22 @@ def test_state_bytes_validation(lib):
         kvc.make_config("bf16", "contiguous", "int8", 1, 4, 1, 128, 64, window=32),   # INT8 attends to all
         kvc.make_config("bf16", "contiguous", None, 1, 1, 1, 128, 64, int8_exact_blocks=4),  # pool needs INT8
         kvc.make_config("bf16", "contiguous", "int8", 1, 4, 1, 128, 64, int8_exact_blocks=-1),
+        kvc.make_config("bf16", "contiguous", "int8", 1, 4, 1, 128, 64, page_pool=8),   # paged INT8
+        kvc.make_config("bf16", "contiguous", None, 1, 4, 1, 128, 72, page_pool=8),     # capacity % 16
+        kvc.make_config("bf16", "ring", None, 1, 4, 1, 128, 40, page_pool=8, max_position=64),  # W % 16
+        kvc.make_config("bf16", "contiguous", None, 1, 4, 1, 128, 64, page_pool=-1),
     ]
     for c in bad:
         with pytest.raises(kvc.KvcError) as e:
             kvc.kvc_state_bytes(c)
         assert e.value.code == kvc.KVC_ERR_ARG
+
+
+def test_paged_state_is_the_pool_not_the_capacity(lib):
+    # a paged cache sizes K/V by its pool, whatever the per-request capacity
+    big = kvc.kvc_state_bytes(kvc.make_config("bf16", "contiguous", None, 64, 32, 8, 128, 32768))
+    paged = kvc.kvc_state_bytes(kvc.make_config("bf16", "contiguous", None, 64, 32, 8, 128, 32768, page_pool=1024))
+    assert paged < big / 20
 
 
 def test_prefix_cut_matches_golden(lib):
