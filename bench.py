@@ -159,6 +159,7 @@ class DecodeBench:
     ``kvc_append`` + ``kvc_decode_attn``.  Subclasses fill the cache and count bytes."""
 
     CYCLE = 64
+    PAGED = False                       # K/V in 16-slot pages behind a block table
     kernel = "kvc_decode_attn (split-K decode + combine)"
     metric = METRIC
     unit = "GB/s"
@@ -240,7 +241,9 @@ class FullCacheBench(DecodeBench):
         if batch:
             w.batch = batch                   # smaller case for profiler captures
         self.ctx = w.extra["context"]
-        self.cache = kvc.Cache.from_workload(w, device=device)
+        # a paged cache gets exactly the pages the cycle needs: ceil((ctx + CYCLE) / 16) a request
+        pool = w.batch * -(-(self.ctx + self.CYCLE) // 16) if self.PAGED else 0
+        self.cache = kvc.Cache.from_workload(w, device=device, page_pool=pool)
         k, v = w.prefill_chunk(0, self.ctx, device=device)
         self.cache.append_rows(k, v)
         del k, v
@@ -290,7 +293,8 @@ class SlidingWindowBench(DecodeBench):
         self.W = w.capacity
         self.L = list(w.extra["lengths"])
         maxp = w.extra["max_len"] + total_steps + 64
-        self.cache = kvc.Cache.from_workload(w, max_position=maxp, device=device)
+        pool = w.batch * (self.W // 16) if self.PAGED else 0   # every ring fills its window
+        self.cache = kvc.Cache.from_workload(w, max_position=maxp, device=device, page_pool=pool)
         chunk = 4096
         for c in range((max(self.L) + chunk - 1) // chunk):
             counts = [int(min(max(L - 1 - c * chunk, 0), chunk)) for L in self.L]
@@ -434,6 +438,28 @@ class Int8GatedBench(Int8Bench):
         c["workload"] = "int8-witness-gated"
         c["gate"] = {"tau": self.TAU, "budget_blocks": self.pool_blocks(), "risky_blocks": self.risky,
                      "restored_blocks": self.restored, "ms": self.gate_ms}
+        return c
+
+
+class FullCachePagedBench(FullCacheBench):
+    """The full-cache MHA workload on a paged cache (pages handed out in a shuffled order)."""
+    PAGED = True
+
+    def config(self):
+        c = super().config()
+        c["workload"] += "-paged"
+        c["layout"] = "contiguous, paged (16-slot pages, block table)"
+        return c
+
+
+class SlidingWindowPagedBench(SlidingWindowBench):
+    """The sliding-window GQA workload on a paged ring."""
+    PAGED = True
+
+    def config(self):
+        c = super().config()
+        c["workload"] += "-paged"
+        c["layout"] = "ring, paged (16-slot pages, block table)"
         return c
 
 
@@ -583,6 +609,7 @@ class ChunkWindowBench(ChunkBench):
 
 BENCHES = {"full-cache-mha": FullCacheBench, "sliding-window-gqa": SlidingWindowBench, "int8-witness": Int8Bench,
            "bf16-at-int8-shape": Bf16AtInt8ShapeBench, "int8-witness-gated": Int8GatedBench,
+           "full-cache-mha-paged": FullCachePagedBench, "sliding-window-gqa-paged": SlidingWindowPagedBench,
            "prefix-reuse": ChunkBench, "prefix-reuse-w4096": ChunkWindowBench}
 
 
