@@ -89,6 +89,16 @@ class Workload:
         return (self.queries((B, Hq, d), "step%d" % step, device), k,
                 self.values((B, Hkv, d), "step%d" % step, device))
 
+    def token_table(self, vocab: int, device="cpu"):
+        """Rows keyed by token ID: q [vocab, Hq, d], k and v [vocab, Hkv, d] (pre-RoPE).
+
+        A prefill of token IDs ``ids`` takes rows ``k[ids]``, ``v[ids]``; equal IDs give
+        equal rows, which is what prefix reuse by token ID relies on.
+        """
+        Hq, Hkv, d = self.n_q_heads, self.n_kv_heads, self.head_dim
+        return (self.queries((vocab, Hq, d), "tokens", device), self.keys((vocab, Hkv, d), "tokens", device),
+                self.values((vocab, Hkv, d), "tokens", device))
+
     def prefill_chunk(self, chunk: int, rows: int, device="cpu"):
         """k, v [B, Hkv, rows, d] for positions chunk*rows .. chunk*rows+rows-1."""
         B, Hkv, d = self.batch, self.n_kv_heads, self.head_dim

@@ -28,6 +28,7 @@ well, with residual 0 and witness 0.
 """
 from __future__ import annotations
 
+import copy
 import math
 from typing import List
 
@@ -143,6 +144,37 @@ class DecodeOracle:
                 self.rings[b].truncate(n - cut, cut % self.capacity)
             for h in range(self.Hkv):          # restored blocks past the cut leave with their rows
                 self.restored[b][h] = {blk for blk in self.restored[b][h] if (blk + 1) * QBLOCK <= cut}
+
+    def snapshot(self, b):
+        """Request b's stored rows, ring state and restored blocks, as a private copy."""
+        ring = self.rings[b] if self.rings is not None else None
+        return copy.deepcopy((self.hk[b], self.hv[b], ring, self.restored[b]))
+
+    def load(self, b, snap, cut):
+        """Request b continues from rows [0, cut) of a snapshot (None = an empty request).
+
+        The same as putting the snapshot's state back and trimming request b to ``cut``
+        ([PREFIX] "查詢流程與快取所有權", step 4: the kept rows are copied out of the
+        store, which keeps its own).  A ring refuses a cut whose rows were evicted
+        before the snapshot was taken.  Nothing changes on error.
+        """
+        if snap is None:
+            if cut != 0:
+                raise OracleError("arg", "an empty request continues from 0")
+            snap = ([], [], RingBuffer(self.capacity) if self.rings is not None else None,
+                    [set() for _ in range(self.Hkv)])
+        hk, hv, ring, restored = copy.deepcopy(snap)
+        n = len(hk)
+        if cut < 0 or cut > n:
+            raise OracleError("arg", "cut %d outside [0, %d]" % (cut, n))
+        if ring is not None and not ring_trim_allowed(cut, n, self.capacity):
+            raise OracleError("evicted", "rows needed after cut %d were evicted" % cut)
+        self.hk[b], self.hv[b], self.restored[b] = hk, hv, restored
+        if self.rings is not None:
+            self.rings[b] = ring
+        cuts = [self.length(x) for x in range(self.B)]
+        cuts[b] = cut
+        self.trim(cuts)
 
     # ------------------------------------------------------------ attention
     def _history(self, b, kv_head, lo=0, hi=None):
