@@ -93,6 +93,9 @@ typedef struct {
                              mapped by a per-request block table, allocated on append and
                              freed by trim.  Not with INT8 or kvc_chunk_attn; capacity
                              (the per-request logical slots) must be a multiple of 16. */
+    int32_t store_slots;  /* device slots for saved prefills (kvc_store_save /
+                             kvc_store_load), each holding one request's K, V and
+                             positions; 0 = none.  Not with INT8. */
 } kvc_config;
 
 /* Bytes of the device state buffer for `cfg` (cache rows, positions,
@@ -282,6 +285,56 @@ int kvc_device_status(kvc_t h, kvc_stream_t stream, int32_t* h_status);
  * pointer is NULL where its count is positive. */
 int kvc_prefix_cut(const int64_t* h_old_ids, int32_t n_old, const int64_t* h_new_ids,
                    int32_t n_new, int32_t ring, int32_t* h_cut);
+
+/* ---- prefix store ([PREFIX] "查詢流程與快取所有權") -------------------------
+ * Policy and data are split.  A kvc_pstore_t (host only, no GPU needed) decides
+ * which stored prefill a query reuses and how many of its rows; the rows
+ * themselves live in the store slots of a handle's state (kvc_config.store_slots)
+ * and move with kvc_store_save / kvc_store_load.  A pstore slot index names the
+ * handle's store slot that holds that entry's rows. */
+typedef struct kvc_pstore* kvc_pstore_t;
+
+/* Host only.  A store of at most `capacity` prefills of caches configured as
+ * `cfg` ([PREFIX]: at most two).  The configuration (dtype, layout, window, head
+ * shape, RoPE base) is part of every entry's computation signature; a ring
+ * layout selects the sliding-window reuse rule.  KVC_ERR_ARG for capacity < 1 or
+ * an invalid cfg. */
+int kvc_pstore_create(const kvc_config* cfg, int32_t capacity, kvc_pstore_t* out);
+int kvc_pstore_destroy(kvc_pstore_t ps);
+
+/* Host only.  Records a prefill of the n_ids >= 1 token IDs h_ids under the
+ * application scope `scope` (NUL-terminated, compared byte for byte) and the
+ * caller's part of the computation signature (sig_bytes bytes at h_sig, e.g. a
+ * hash of the weights and of the implementation; h_sig may be NULL when
+ * sig_bytes is 0).  *h_slot = the slot used: the lowest free one, else the slot
+ * of the oldest entry, which is replaced (the page is silent on eviction). */
+int kvc_pstore_insert(kvc_pstore_t ps, const int64_t* h_ids, int32_t n_ids, const char* scope,
+                      const void* h_sig, int32_t sig_bytes, int32_t* h_slot);
+
+/* Host only.  Lookup of a query of n_ids >= 1 token IDs, in the page's order:
+ * entries with the same scope and signature are eligible; each offers the cut
+ * of kvc_prefix_cut (longest contiguous common prefix, at most n_ids - 1; on a
+ * ring only a whole-prefix match); the largest cut wins, ties going to the most
+ * recently inserted entry.  *h_slot = that entry's slot and *h_cut its cut, or
+ * -1 and 0 when no entry offers a row. */
+int kvc_pstore_lookup(kvc_pstore_t ps, const int64_t* h_ids, int32_t n_ids, const char* scope,
+                      const void* h_sig, int32_t sig_bytes, int32_t* h_slot, int32_t* h_cut);
+
+/* Copies request b's cache into store slot `slot` of the state: K and V rows
+ * and positions (every slot of a ring).  n must equal request b's next_position
+ * (the prefill's length, n >= 1).  KVC_ERR_UNSUPPORTED without store slots. */
+int kvc_store_save(kvc_t h, int32_t slot, int32_t b, int32_t n, kvc_stream_t stream);
+
+/* Request b continues from rows [0, cut) of store slot `slot` ([PREFIX] step 4:
+ * the kept K, V and positions are copied out of the store, which keeps its
+ * own): the slot's rows at positions below cut are copied into request b,
+ * every other slot of b is emptied, and next_position[b] = cut.  slot = -1 with
+ * cut = 0 empties request b.  Other requests are untouched.  KVC_ERR_ARG if the
+ * slot holds nothing or cut exceeds its length; KVC_ERR_EVICTED if a ring slot no
+ * longer holds rows that the token at `cut` would attend to (the kvc_trim rule);
+ * KVC_ERR_CAPACITY if a paged cache lacks pages (nothing changes).  On a ring, as
+ * after kvc_trim, the next call on the handle must append. */
+int kvc_store_load(kvc_t h, int32_t slot, int32_t b, int32_t cut, kvc_stream_t stream);
 
 /* Static description of a status code. */
 const char* kvc_strerror(int code);

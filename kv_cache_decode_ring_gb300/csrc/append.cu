@@ -341,17 +341,7 @@ cudaError_t map_pages(kvc_handle* h, const std::vector<int>& from, const std::ve
         for (int lp = 0; lp < np; ++lp) {
             const size_t idx = (size_t)b * np + lp;
             if (h->table_h[idx] >= 0) continue;
-            bool touch;
-            if (!s.ring) {
-                touch = (long long)lp * kPage < hi && (long long)(lp + 1) * kPage > lo;
-            } else if (hi - lo >= s.S) {
-                touch = true;
-            } else {                           // slots lo % S .. (hi - 1) % S, possibly wrapping
-                const long long a0 = lo % s.S, a1 = (hi - 1) % s.S;
-                const long long p0 = (long long)lp * kPage, p1 = p0 + kPage - 1;
-                touch = a0 <= a1 ? (p0 <= a1 && p1 >= a0) : (p1 >= a0 || p0 <= a1);
-            }
-            if (touch) need.push_back((int)idx);
+            if (page_touched(s, lp, lo, hi)) need.push_back((int)idx);
         }
     }
     *status = KVC_OK;

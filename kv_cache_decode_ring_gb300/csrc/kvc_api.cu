@@ -10,8 +10,6 @@
 namespace kvc {
 
 cudaError_t launch_append_rows_counts(const AppendArgs& a, const int32_t* counts, cudaStream_t st);
-cudaError_t launch_trim_cuts(int32_t* next_pos, int32_t* pos, const int32_t* cuts, int B, int S,
-                             int ring, cudaStream_t st);
 bool fast_decode_supported(const DecodeArgs& a);
 cudaError_t launch_int8_decode(kvc_handle* h, const void* q, void* out, float* cmax, float* tanh_out,
                                float* ct, cudaStream_t st);
@@ -40,6 +38,7 @@ bool make_shape(const kvc_config& c, Shape* s) {
         return false;
     if (c.int8_exact_blocks < 0 || (!int8 && c.int8_exact_blocks != 0)) return false;
     if (c.page_pool < 0 || (c.page_pool > 0 && (int8 || c.capacity % kPage))) return false;
+    if (c.store_slots < 0 || (c.store_slots > 0 && int8)) return false;
     if (int8) {
         const int g = c.n_q_heads / c.n_kv_heads;
         if ((c.head_dim != 64 && c.head_dim != 128) || (g != 1 && g != 2 && g != 4 && g != 8)) return false;
@@ -57,6 +56,7 @@ bool make_shape(const kvc_config& c, Shape* s) {
     s->max_chunk = c.max_chunk;
     s->xpool = c.int8_exact_blocks;
     s->pages = c.page_pool;
+    s->store_slots = c.store_slots;
     s->out_bf16 = c.out_dtype == 0 ? s->bf16 : c.out_dtype == KVC_BF16 + 1;
     s->split = kGenericSplit;
     if (s->bf16 && !int8 && (s->d == 64 || s->d == 128) && s->g <= 8) s->split = kFastSplit;
@@ -107,6 +107,10 @@ Layout make_layout(const Shape& s) {
     L.part_acc = take(B * Hq * s.max_splits * d * 4);
     if (s.int8) L.part_c = take(B * Hq * s.max_splits * 4);
     if (s.max_chunk > 0) L.qrot = take(2 * B * (size_t)s.max_chunk * Hq * d * 2);   // hi and lo terms
+    if (s.store_slots > 0) {
+        L.store_stride = align256(2 * Hkv * S * d * s.elem + S * 4);
+        L.store = take((size_t)s.store_slots * L.store_stride);
+    }
     L.total = o;
     return L;
 }
@@ -208,6 +212,7 @@ int kvc_create(const kvc_config* cfg, void* d_state, size_t bytes, kvc_stream_t 
     if (!h) return KVC_ERR_ARG;
     h->cfg = *cfg; h->sh = s; h->L = L; h->state = static_cast<char*>(d_state); h->bytes = bytes;
     h->np.assign(s.B, 0);
+    h->store_n.assign(s.store_slots, -1);
     h->ring_needs_append = false;
     h->has_kv_maps = false;
     if (s.split == kGqaSplit) {

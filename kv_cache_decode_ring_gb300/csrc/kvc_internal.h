@@ -49,6 +49,8 @@ struct Layout {
     size_t part_acc;  // float  [B][Hq][max_splits][d]
     size_t part_c;    // float  [B][Hq][max_splits] max_t c_t of the split   (INT8)
     size_t qrot;      // bf16 [2][B][max_chunk][Hq][d] rotated suffix queries, hi and lo terms
+    size_t store;     // store slots: each K, V [Hkv][S][d] cache dtype, then positions int32 [S]
+    size_t store_stride;  // bytes per store slot
     size_t total;
 };
 
@@ -63,6 +65,7 @@ struct Shape {
     int max_chunk;               // largest suffix of kvc_chunk_attn (0 = none)
     int xpool;                   // entries of the INT8 exact-block pool
     int pages;                   // pages of a paged cache (0 = not paged)
+    int store_slots;             // saved-prefill slots (0 = none)
 };
 
 bool make_shape(const kvc_config& c, Shape* s);
@@ -128,6 +131,19 @@ cudaError_t int8_drop_restored(kvc_handle* h, const int32_t* h_cut, cudaStream_t
 // paged caches (append.cu): map the pages that slots [from, to) of each request need
 cudaError_t map_pages(kvc_handle* h, const std::vector<int>& from, const std::vector<int>& to, cudaStream_t st,
                       int* status);
+cudaError_t launch_trim_cuts(int32_t* next_pos, int32_t* pos, const int32_t* cuts, int B, int S, int ring,
+                             cudaStream_t st);
+
+// Whether logical page lp holds a slot of positions [lo, hi) (slot = position on a
+// contiguous cache, position mod S on a ring of S slots).
+inline bool page_touched(const Shape& s, int lp, long long lo, long long hi) {
+    if (hi <= lo) return false;
+    const long long p0 = (long long)lp * kPage, p1 = p0 + kPage - 1;
+    if (!s.ring) return p0 < hi && p1 >= lo;
+    if (hi - lo >= s.S) return true;
+    const long long a0 = lo % s.S, a1 = (hi - 1) % s.S;     // possibly wrapping
+    return a0 <= a1 ? (p0 <= a1 && p1 >= a0) : (p1 >= a0 || p0 <= a1);
+}
 // INT8 exact-block decode (int8_exact.cu): the restored blocks' splits
 cudaError_t launch_int8_exact(kvc_handle* h, const void* q, float* ct, cudaStream_t st);
 // maps: required when the GQA kernel serves the shape (split == kGqaSplit)
@@ -229,4 +245,6 @@ struct kvc_handle {
     std::vector<int32_t> xlist_h, xent_h;   // mirrors of the per-head lists
     // paged caches: host mirror of the block table and the free pages
     std::vector<int32_t> table_h, page_free;
+    // prefix store: rows saved in each store slot (-1 = empty)
+    std::vector<int32_t> store_n;
 };

@@ -1,0 +1,249 @@
+// store.cu -- prefix store ([PREFIX] "LLM 機制實驗（五）：改了歷史，能否只重算變化的後綴？",
+// "查詢流程與快取所有權"): the host policy object that picks the stored prefill a
+// query reuses and how many of its rows, and the device copies of one request's
+// rows between the cache and a store slot of the state buffer.
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "kvc_internal.h"
+
+struct kvc_pstore {
+    struct Entry {
+        bool used = false;
+        uint64_t seq = 0;              // insertion order; larger = more recent
+        std::vector<int64_t> ids;
+        std::string scope;
+        std::vector<uint8_t> sig;
+    };
+    int32_t ring = 0;
+    uint64_t seq = 0;
+    std::vector<Entry> e;
+};
+
+namespace kvc {
+namespace {
+
+constexpr int kStoreRows = 32;         // cache rows per CTA of the copy kernel
+constexpr int kStoreThreads = 256;
+
+struct StoreArgs {
+    char* kc; char* vc;                // cache rows (unpaged runs or pages)
+    const int32_t* table;              // paged caches: block table, else nullptr
+    int32_t* pos;                      // cache positions [B][S]
+    int32_t* next_pos;
+    char* sk; char* sv;                // store slot rows [Hkv][S][d]
+    int32_t* spos;                     // store slot positions [S]
+    int b, Hkv, S, row_bytes;
+    int rows;                          // slots [0, rows) may hold a row to copy
+    int cut;                           // load: rows at positions below cut are kept
+    int load;                          // 1: store slot -> request b; 0: request b -> store slot
+    int empty;                         // load of nothing (request b emptied)
+};
+
+// grid (ceil(rows / kStoreRows), Hkv + 1): plane y < Hkv copies KV head y's rows,
+// plane Hkv the positions (and, on a load, next_position).
+// Save: every slot holding a row (position >= 0) goes to the store slot, with the
+// positions array.  Load: the store slot's rows at positions [0, cut) come back;
+// every other slot of request b is marked empty.
+template <typename U>
+__global__ void __launch_bounds__(kStoreThreads) store_copy_kernel(const StoreArgs a) {
+    const int h = blockIdx.y;
+    int32_t* pb = a.pos + (size_t)a.b * a.S;
+    if (h == a.Hkv) {
+        for (int s = blockIdx.x * blockDim.x + threadIdx.x; s < a.S; s += gridDim.x * blockDim.x) {
+            if (a.load) {
+                const int p = a.empty ? -1 : a.spos[s];
+                pb[s] = (p >= 0 && p < a.cut) ? p : -1;
+            } else {
+                a.spos[s] = pb[s];
+            }
+        }
+        if (a.load && blockIdx.x == 0 && threadIdx.x == 0) a.next_pos[a.b] = a.cut;
+        return;
+    }
+    if (a.empty) return;
+    const int upr = a.row_bytes / (int)sizeof(U);        // units per row
+    const int s0 = blockIdx.x * kStoreRows;
+    const int32_t* held = a.load ? a.spos : pb;          // the side whose rows are read
+    for (int i = threadIdx.x; i < kStoreRows * upr; i += blockDim.x) {
+        const int s = s0 + i / upr, u = i % upr;
+        if (s >= a.rows || s >= a.S) break;              // s grows with i
+        const int p = held[s];
+        if (p < 0 || (a.load && p >= a.cut)) continue;
+        const size_t crow = kv_row(a.table, a.b, h, s, a.Hkv, a.S);
+        const size_t srow = (size_t)h * a.S + s;
+        U* ck = reinterpret_cast<U*>(a.kc + crow * a.row_bytes) + u;
+        U* cv = reinterpret_cast<U*>(a.vc + crow * a.row_bytes) + u;
+        U* sk = reinterpret_cast<U*>(a.sk + srow * a.row_bytes) + u;
+        U* sv = reinterpret_cast<U*>(a.sv + srow * a.row_bytes) + u;
+        if (a.load) { *ck = *sk; *cv = *sv; }
+        else { *sk = *ck; *sv = *cv; }
+    }
+}
+
+cudaError_t launch_store_copy(const StoreArgs& a, cudaStream_t st) {
+    const int blocks = a.rows > 0 ? (a.rows + kStoreRows - 1) / kStoreRows : 1;
+    dim3 grid(blocks, a.Hkv + 1);
+    if (a.row_bytes % 16 == 0) store_copy_kernel<uint4><<<grid, kStoreThreads, 0, st>>>(a);
+    else store_copy_kernel<uint32_t><<<grid, kStoreThreads, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+StoreArgs store_args(kvc_handle* h, int slot, int b) {
+    const Shape& s = h->sh;
+    StoreArgs a{};
+    a.kc = h->state + h->L.k; a.vc = h->state + h->L.v;
+    a.table = s.pages ? reinterpret_cast<const int32_t*>(h->state + h->L.table) : nullptr;
+    a.pos = reinterpret_cast<int32_t*>(h->state + h->L.pos);
+    a.next_pos = reinterpret_cast<int32_t*>(h->state + h->L.next_pos);
+    if (slot >= 0) {
+        char* base = h->state + h->L.store + (size_t)slot * h->L.store_stride;
+        const size_t half = (size_t)s.Hkv * s.S * s.d * s.elem;
+        a.sk = base; a.sv = base + half;
+        a.spos = reinterpret_cast<int32_t*>(base + 2 * half);
+    }
+    a.b = b; a.Hkv = s.Hkv; a.S = s.S; a.row_bytes = s.d * s.elem;
+    return a;
+}
+
+bool valid_ids(const int64_t* ids, int32_t n) { return ids && n >= 1; }
+
+bool valid_key(const char* scope, const void* sig, int32_t sig_bytes) {
+    return scope && sig_bytes >= 0 && (sig_bytes == 0 || sig);
+}
+
+bool same_key(const kvc_pstore::Entry& e, const char* scope, const void* sig, int32_t sig_bytes) {
+    return e.scope == scope && e.sig.size() == (size_t)sig_bytes &&
+           (sig_bytes == 0 || std::memcmp(e.sig.data(), sig, sig_bytes) == 0);
+}
+
+}  // namespace
+}  // namespace kvc
+
+using namespace kvc;
+
+extern "C" {
+
+int kvc_pstore_create(const kvc_config* cfg, int32_t capacity, kvc_pstore_t* out) {
+    if (!cfg || !out || capacity < 1) return KVC_ERR_ARG;
+    Shape s;
+    if (!make_shape(*cfg, &s)) return KVC_ERR_ARG;
+    kvc_pstore* ps = new (std::nothrow) kvc_pstore();
+    if (!ps) return KVC_ERR_ARG;
+    ps->ring = s.ring;
+    ps->e.resize(capacity);
+    *out = ps;
+    return KVC_OK;
+}
+
+int kvc_pstore_destroy(kvc_pstore_t ps) {
+    if (!ps) return KVC_ERR_ARG;
+    delete ps;
+    return KVC_OK;
+}
+
+int kvc_pstore_insert(kvc_pstore_t ps, const int64_t* h_ids, int32_t n_ids, const char* scope,
+                      const void* h_sig, int32_t sig_bytes, int32_t* h_slot) {
+    if (!ps || !h_slot || !valid_ids(h_ids, n_ids) || !valid_key(scope, h_sig, sig_bytes)) return KVC_ERR_ARG;
+    int slot = -1;
+    for (size_t i = 0; i < ps->e.size() && slot < 0; ++i)
+        if (!ps->e[i].used) slot = (int)i;
+    if (slot < 0) {                                   // full: the oldest entry makes room
+        slot = 0;
+        for (size_t i = 1; i < ps->e.size(); ++i)
+            if (ps->e[i].seq < ps->e[slot].seq) slot = (int)i;
+    }
+    kvc_pstore::Entry& e = ps->e[slot];
+    e.used = true;
+    e.seq = ++ps->seq;
+    e.ids.assign(h_ids, h_ids + n_ids);
+    e.scope = scope;
+    e.sig.assign(static_cast<const uint8_t*>(h_sig), static_cast<const uint8_t*>(h_sig) + sig_bytes);
+    *h_slot = slot;
+    return KVC_OK;
+}
+
+int kvc_pstore_lookup(kvc_pstore_t ps, const int64_t* h_ids, int32_t n_ids, const char* scope,
+                      const void* h_sig, int32_t sig_bytes, int32_t* h_slot, int32_t* h_cut) {
+    if (!ps || !h_slot || !h_cut || !valid_ids(h_ids, n_ids) || !valid_key(scope, h_sig, sig_bytes))
+        return KVC_ERR_ARG;
+    int best = -1, best_cut = 0;
+    uint64_t best_seq = 0;
+    for (size_t i = 0; i < ps->e.size(); ++i) {
+        const kvc_pstore::Entry& e = ps->e[i];
+        if (!e.used || !same_key(e, scope, h_sig, sig_bytes)) continue;
+        int32_t cut = 0;
+        kvc_prefix_cut(e.ids.data(), (int32_t)e.ids.size(), h_ids, n_ids, ps->ring, &cut);
+        if (cut > best_cut || (cut == best_cut && cut > 0 && e.seq > best_seq)) {
+            best = (int)i; best_cut = cut; best_seq = e.seq;
+        }
+    }
+    *h_slot = best;
+    *h_cut = best_cut;
+    return KVC_OK;
+}
+
+int kvc_store_save(kvc_t h, int32_t slot, int32_t b, int32_t n, kvc_stream_t stream) {
+    if (!h) return KVC_ERR_ARG;
+    const Shape& s = h->sh;
+    if (s.store_slots == 0) return KVC_ERR_UNSUPPORTED;
+    if (slot < 0 || slot >= s.store_slots || b < 0 || b >= s.B || n < 1 || n != h->np[b]) return KVC_ERR_ARG;
+    StoreArgs a = store_args(h, slot, b);
+    a.rows = s.ring ? s.S : n;
+    a.load = 0;
+    if (launch_store_copy(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KVC_ERR_CUDA;
+    h->store_n[slot] = n;
+    return KVC_OK;
+}
+
+int kvc_store_load(kvc_t h, int32_t slot, int32_t b, int32_t cut, kvc_stream_t stream) {
+    if (!h) return KVC_ERR_ARG;
+    const Shape& s = h->sh;
+    if (s.store_slots == 0) return KVC_ERR_UNSUPPORTED;
+    if (b < 0 || b >= s.B || slot < -1 || slot >= s.store_slots) return KVC_ERR_ARG;
+    const int n = slot < 0 ? 0 : h->store_n[slot];
+    if (n < 0 || cut < 0 || cut > n) return KVC_ERR_ARG;
+    if (s.ring && cut > 0) {
+        // the token at `cut` attends to [cut - S + 1, cut); the slot holds [n - S, n)
+        const int lo = cut - s.S + 1 > 0 ? cut - s.S + 1 : 0;
+        const int resident = n - s.S > 0 ? n - s.S : 0;
+        if (lo < resident) return KVC_ERR_EVICTED;
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (s.pages) {
+        // request b gives back all its pages and maps those that the kept rows need
+        const int npg = s.S / kPage;
+        const long long lo = s.ring && n > s.S ? n - s.S : 0;
+        int need = 0, held = 0;
+        for (int lp = 0; lp < npg; ++lp) {
+            need += page_touched(s, lp, lo, cut) ? 1 : 0;
+            held += h->table_h[(size_t)b * npg + lp] >= 0 ? 1 : 0;
+        }
+        if (need > held + (int)h->page_free.size()) return KVC_ERR_CAPACITY;
+        for (int lp = 0; lp < npg; ++lp) {
+            int32_t& e = h->table_h[(size_t)b * npg + lp];
+            if (e >= 0) { h->page_free.push_back(e); e = -1; }
+        }
+        std::vector<int> from(h->np.begin(), h->np.end()), to(from);
+        from[b] = (int)lo; to[b] = cut;
+        int rc = KVC_OK;
+        if (map_pages(h, from, to, st, &rc) != cudaSuccess) return KVC_ERR_CUDA;
+        if (rc) return rc;               // not reached: the count above guarantees the pages
+        if (cudaMemcpyAsync(h->state + h->L.table, h->table_h.data(), h->table_h.size() * 4,
+                            cudaMemcpyHostToDevice, st) != cudaSuccess)
+            return KVC_ERR_CUDA;
+    }
+    StoreArgs a = store_args(h, slot, b);
+    a.rows = slot < 0 ? 0 : (s.ring ? s.S : cut);
+    a.cut = cut;
+    a.load = 1;
+    a.empty = slot < 0;
+    if (launch_store_copy(a, st) != cudaSuccess) return KVC_ERR_CUDA;
+    h->np[b] = cut;
+    if (s.ring) h->ring_needs_append = true;
+    return KVC_OK;
+}
+
+}  // extern "C"

@@ -42,13 +42,16 @@ class kvc_config(ctypes.Structure):
                 ("batch", ctypes.c_int32), ("n_q_heads", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("capacity", ctypes.c_int32), ("window", ctypes.c_int32),
                 ("max_position", ctypes.c_int32), ("rope_base", ctypes.c_float), ("max_chunk", ctypes.c_int32),
-                ("out_dtype", ctypes.c_int32), ("int8_exact_blocks", ctypes.c_int32), ("page_pool", ctypes.c_int32)]
+                ("out_dtype", ctypes.c_int32), ("int8_exact_blocks", ctypes.c_int32), ("page_pool", ctypes.c_int32),
+                ("store_slots", ctypes.c_int32)]
 
 
 EXPORTED = ["kvc_state_bytes", "kvc_create", "kvc_destroy", "kvc_append", "kvc_append_rows",
             "kvc_decode_attn", "kvc_trim", "kvc_chunk_attn", "kvc_export_bytes", "kvc_export",
             "kvc_next_positions", "kvc_device_status", "kvc_prefix_cut", "kvc_strerror",
-            "kvc_int8_block_risk", "kvc_int8_gate", "kvc_int8_restore"]
+            "kvc_int8_block_risk", "kvc_int8_gate", "kvc_int8_restore",
+            "kvc_pstore_create", "kvc_pstore_destroy", "kvc_pstore_insert", "kvc_pstore_lookup",
+            "kvc_store_save", "kvc_store_load"]
 
 _lock = threading.Lock()
 _lib = None
@@ -87,6 +90,12 @@ def lib() -> ctypes.CDLL:
                 "kvc_int8_block_risk": [P, P, P, P],
                 "kvc_int8_gate": [P, i32, i32, i32, ctypes.c_double, i32, P, ctypes.POINTER(i32)],
                 "kvc_int8_restore": [P, P, i32, P, P, P],
+                "kvc_pstore_create": [cfgp, i32, ctypes.POINTER(P)],
+                "kvc_pstore_destroy": [P],
+                "kvc_pstore_insert": [P, P, i32, ctypes.c_char_p, P, i32, ctypes.POINTER(i32)],
+                "kvc_pstore_lookup": [P, P, i32, ctypes.c_char_p, P, i32, ctypes.POINTER(i32), ctypes.POINTER(i32)],
+                "kvc_store_save": [P, i32, i32, i32, P],
+                "kvc_store_load": [P, i32, i32, i32, P],
             }
             for name, args in sig.items():
                 fn = getattr(L, name)
@@ -131,16 +140,17 @@ def kvc_strerror(code: int) -> str:
 
 def make_config(dtype="bf16", layout="contiguous", kv_quant=None, batch=1, n_q_heads=1, n_kv_heads=1,
                 head_dim=128, capacity=1, window=0, max_position=0, rope_base=0.0, max_chunk=0,
-                out_dtype=None, int8_exact_blocks=0, page_pool=0) -> kvc_config:
+                out_dtype=None, int8_exact_blocks=0, page_pool=0, store_slots=0) -> kvc_config:
     """``out_dtype``: None (the cache dtype), "f32" or "bf16"; ``int8_exact_blocks``: pool
     entries for blocks the gated fallback restores (INT8 caches); ``page_pool``: pages of 16
-    slots for paged K/V storage (0 = each request owns ``capacity`` slots)."""
+    slots for paged K/V storage (0 = each request owns ``capacity`` slots); ``store_slots``:
+    device slots for saved prefills (prefix store)."""
     od = 0 if out_dtype is None else (KVC_F32 + 1 if out_dtype == "f32" else KVC_BF16 + 1)
     return kvc_config(KVC_BF16 if dtype == "bf16" else KVC_F32,
                       KVC_RING if layout == "ring" else KVC_CONTIGUOUS,
                       KVC_QUANT_INT8 if kv_quant == "int8" else KVC_QUANT_NONE,
                       batch, n_q_heads, n_kv_heads, head_dim, capacity, window, max_position,
-                      float(rope_base), max_chunk, od, int(int8_exact_blocks), int(page_pool))
+                      float(rope_base), max_chunk, od, int(int8_exact_blocks), int(page_pool), int(store_slots))
 
 
 def kvc_state_bytes(cfg: kvc_config) -> int:
@@ -263,6 +273,88 @@ def kvc_prefix_cut(old_ids: Sequence[int], new_ids: Sequence[int], ring: bool = 
     return cut.value
 
 
+def _token_ids(ids) -> np.ndarray:
+    """Token IDs as int64, refusing anything that is not an integer (1.0 is not the token 1)."""
+    if isinstance(ids, torch.Tensor):
+        if ids.dtype.is_floating_point or ids.dtype == torch.bool or ids.dtype.is_complex:
+            raise TypeError("token IDs must be integers, got %s" % ids.dtype)
+        return np.ascontiguousarray(ids.detach().cpu().numpy().astype(np.int64).reshape(-1))
+    if isinstance(ids, np.ndarray):
+        if ids.dtype.kind not in "iu":
+            raise TypeError("token IDs must be integers, got %s" % ids.dtype)
+        return np.ascontiguousarray(ids.astype(np.int64).reshape(-1))
+    for x in ids:
+        if isinstance(x, bool) or not isinstance(x, (int, np.integer)):
+            raise TypeError("token IDs must be integers, got %r" % (x,))
+    return np.ascontiguousarray(np.asarray(list(ids), dtype=np.int64).reshape(-1))
+
+
+def _sig(signature) -> bytes:
+    return signature.encode() if isinstance(signature, str) else bytes(signature)
+
+
+def kvc_pstore_create(cfg: kvc_config, capacity: int) -> ctypes.c_void_p:
+    ps = ctypes.c_void_p(0)
+    _check(lib().kvc_pstore_create(ctypes.byref(cfg), int(capacity), ctypes.byref(ps)), "kvc_pstore_create")
+    return ps
+
+
+def kvc_pstore_destroy(ps) -> None:
+    _check(lib().kvc_pstore_destroy(ps), "kvc_pstore_destroy")
+
+
+def kvc_pstore_insert(ps, ids, scope: str, signature=b"") -> int:
+    a, sg = _token_ids(ids), _sig(signature)
+    slot = ctypes.c_int32(-1)
+    _check(lib().kvc_pstore_insert(ps, a.ctypes.data_as(ctypes.c_void_p) if len(a) else None, len(a),
+                                   scope.encode(), sg or None, len(sg), ctypes.byref(slot)), "kvc_pstore_insert")
+    return slot.value
+
+
+def kvc_pstore_lookup(ps, ids, scope: str, signature=b"") -> tuple:
+    a, sg = _token_ids(ids), _sig(signature)
+    slot, cut = ctypes.c_int32(-1), ctypes.c_int32(0)
+    _check(lib().kvc_pstore_lookup(ps, a.ctypes.data_as(ctypes.c_void_p) if len(a) else None, len(a),
+                                   scope.encode(), sg or None, len(sg), ctypes.byref(slot), ctypes.byref(cut)),
+           "kvc_pstore_lookup")
+    return slot.value, cut.value
+
+
+def kvc_store_save(h, slot: int, b: int, n: int, stream=None) -> None:
+    _check(lib().kvc_store_save(h, int(slot), int(b), int(n), _stream(stream)), "kvc_store_save")
+
+
+def kvc_store_load(h, slot: int, b: int, cut: int, stream=None) -> None:
+    _check(lib().kvc_store_load(h, int(slot), int(b), int(cut), _stream(stream)), "kvc_store_load")
+
+
+class PrefixStore:
+    """Host policy of the prefix store (see include/kvc.h): which stored prefill a query
+    reuses, and how many rows.  The rows live in a Cache's store slots."""
+
+    def __init__(self, cfg: kvc_config, capacity: int = 2):
+        self.capacity = capacity
+        self.ps = kvc_pstore_create(cfg, capacity)
+
+    def insert(self, ids, scope: str, signature=b"") -> int:
+        return kvc_pstore_insert(self.ps, ids, scope, signature)
+
+    def lookup(self, ids, scope: str, signature=b"") -> tuple:
+        """(slot, cut); slot -1 when nothing is reusable."""
+        return kvc_pstore_lookup(self.ps, ids, scope, signature)
+
+    def close(self):
+        if self.ps is not None and self.ps.value:
+            kvc_pstore_destroy(self.ps)
+        self.ps = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
 class Cache:
     """A KV cache of one layer on the current CUDA device: the state buffer (a torch
     uint8 tensor) plus its library handle.  Thin wrapper over the functions above."""
@@ -285,10 +377,10 @@ class Cache:
 
     @classmethod
     def from_workload(cls, w, max_chunk=0, max_position=0, device="cuda", out_dtype=None, int8_exact_blocks=0,
-                      page_pool=0):
+                      page_pool=0, store_slots=0):
         cfg = make_config(w.dtype, w.layout, w.quant, w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.capacity,
                           0 if w.layout == "ring" else w.window, max_position, w.rope_base, max_chunk, out_dtype,
-                          int8_exact_blocks, page_pool)
+                          int8_exact_blocks, page_pool, store_slots)
         return cls(cfg, device)
 
     def close(self):
@@ -385,3 +477,22 @@ class Cache:
 
     def device_status(self, stream=None) -> int:
         return kvc_device_status(self.h, stream)
+
+    # prefix store
+    def store_save(self, slot, b, n, stream=None):
+        kvc_store_save(self.h, slot, b, n, stream)
+
+    def store_load(self, slot, b, cut, stream=None):
+        kvc_store_load(self.h, slot, b, cut, stream)
+
+    def save_prefix(self, store: PrefixStore, b, ids, scope: str, signature=b"", stream=None) -> int:
+        """Records request b's prefill of ``ids`` in ``store`` and copies its rows to the slot."""
+        slot = store.insert(ids, scope, signature)
+        kvc_store_save(self.h, slot, b, len(_token_ids(ids)), stream)
+        return slot
+
+    def reuse_prefix(self, store: PrefixStore, b, ids, scope: str, signature=b"", stream=None) -> tuple:
+        """Request b continues from the longest reusable stored prefix of ``ids``: (slot, cut)."""
+        slot, cut = store.lookup(ids, scope, signature)
+        kvc_store_load(self.h, slot, b, cut, stream)
+        return slot, cut

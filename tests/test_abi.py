@@ -63,6 +63,8 @@ def test_state_bytes_validation(lib):
         kvc.make_config("bf16", "contiguous", None, 1, 4, 1, 128, 72, page_pool=8),     # capacity % 16
         kvc.make_config("bf16", "ring", None, 1, 4, 1, 128, 40, page_pool=8, max_position=64),  # W % 16
         kvc.make_config("bf16", "contiguous", None, 1, 4, 1, 128, 64, page_pool=-1),
+        kvc.make_config("bf16", "contiguous", None, 1, 4, 1, 128, 64, store_slots=-1),
+        kvc.make_config("bf16", "contiguous", "int8", 1, 4, 1, 128, 64, store_slots=2),   # store of INT8
     ]
     for c in bad:
         with pytest.raises(kvc.KvcError) as e:
@@ -122,3 +124,57 @@ def test_int8_gate_matches_oracle_selection(lib, seed):
             got = kvc.kvc_int8_gate(risk, tau, budget)
             want = gate_select({(b, h): risk[b, h] for b in range(B) for h in range(H)}, tau, budget)
             assert [tuple(x) for x in got] == want, (tau, budget)
+
+
+def _pstore(ring, capacity=2):
+    cfg = kvc.make_config("f32", "ring" if ring else "contiguous", None, 1, 1, 1, 16, 4 if ring else 16,
+                          max_position=64, rope_base=10000.0, store_slots=capacity)
+    return kvc.PrefixStore(cfg, capacity)
+
+
+def test_pstore_matrix_through_the_abi(lib):
+    from _store_cases import BRANCH, PLAIN, SCOPE, SIGNATURE, read_matrix
+    for case in read_matrix():
+        ps = _pstore(case["ring"])
+        slots = {"plain": ps.insert(PLAIN, SCOPE, SIGNATURE), "branch": ps.insert(BRANCH, SCOPE, SIGNATURE)}
+        slot, cut = ps.lookup(case["ids"], case["scope"], SIGNATURE)
+        assert cut == case["cut"], case["name"]
+        assert slot == (-1 if case["entry"] is None else slots[case["entry"]]), case["name"]
+        ps.close()
+
+
+def test_pstore_validation_and_state_bytes(lib):
+    ps = _pstore(False)
+    with pytest.raises(TypeError):
+        ps.lookup([1.0, 2], "s")                          # 1.0 is not the token 1
+    with pytest.raises(TypeError):
+        ps.insert(__import__("numpy").array([1.5, 2.0]), "s")
+    with pytest.raises(kvc.KvcError) as e:
+        ps.lookup([], "s")
+    assert e.value.code == kvc.KVC_ERR_ARG
+    assert ps.lookup([1, 2], "s") == (-1, 0)             # empty store
+    with pytest.raises(kvc.KvcError):
+        kvc.PrefixStore(kvc.make_config("bf16", "contiguous", None, 1, 1, 1, 128, 64), 0)
+    base = kvc.kvc_state_bytes(kvc.make_config("bf16", "contiguous", None, 2, 8, 2, 128, 512))
+    two = kvc.kvc_state_bytes(kvc.make_config("bf16", "contiguous", None, 2, 8, 2, 128, 512, store_slots=2))
+    assert two - base >= 2 * (2 * 2 * 512 * 128 * 2 + 512 * 4)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_pstore_matches_oracle_store(lib, seed):
+    """Random insert/lookup sequences: the C policy and the oracle's agree on every slot and cut."""
+    import random
+    from oracle.store import PrefixStore as OracleStore
+    rng = random.Random(seed)
+    for ring in (False, True):
+        cap = rng.choice([1, 2, 3])
+        ps, ref = _pstore(ring, cap), OracleStore(cap, ring=ring)
+        for _ in range(200):
+            ids = [rng.choice([1, 2, 3]) for _ in range(rng.randint(1, 6))]
+            scope, sig = rng.choice(["a", "b"]), rng.choice([b"", b"w1", b"w2"])
+            if rng.random() < 0.3:
+                assert ps.insert(ids, scope, sig) == ref.insert(ids, scope, sig, None)
+            else:
+                s_ref, c_ref = ref.lookup(ids, scope, sig)
+                assert ps.lookup(ids, scope, sig) == (-1 if s_ref is None else s_ref, c_ref), (ids, scope, sig)
+        ps.close()
