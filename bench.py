@@ -43,10 +43,10 @@ CSRC = os.path.join(ROOT, "kv_cache_decode_ring_gb300", "csrc")
 # valid only while the kernel source is the one captured (sha256 prefix), otherwise the
 # JSON line reports null.
 TRAFFIC_PER_BYTE = {
-    "full-cache-mha": ("decode_fast.cu", "f13499b510292e2d", (268699392 + 4494080) / 268632064),
-    "sliding-window-gqa": ("decode_gqa.cu", "2239c895c0ccf520", (268109824 + 4902144) / 268148736),
-    "int8-witness": ("int8.cu", "c8b085cbc8257fc3", (302596864 + 4367104) / 302551040),
-    "bf16-at-int8-shape": ("decode_gqa.cu", "2239c895c0ccf520", (536982272 + 6691584) / 536907776),
+    "full-cache-mha": ("decode_fast.cu", "acb55fd33938d9cc", (268701696 + 4940800) / 268632064),
+    "sliding-window-gqa": ("decode_gqa.cu", "08f9c44bf585eae3", (268104192 + 4806400) / 268148736),
+    "int8-witness": ("int8.cu", "6f50d90ec52b7db8", (302877952 + 4520448) / 302551040),
+    "bf16-at-int8-shape": ("decode_gqa.cu", "08f9c44bf585eae3", (537022720 + 6739968) / 536907776),
     "prefix-reuse": ("chunk.cu", "424df5ecd9751daa", (39883008 + 86784) / 22773760),
 }
 
@@ -523,7 +523,7 @@ class ChunkBench(DecodeBench):
             w.batch = batch                   # smaller case for profiler captures: the first requests
             w.extra["cuts"] = w.extra["cuts"][:batch]
         self.n = w.extra["suffix"]
-        self.cache = kvc.Cache.from_workload(w, max_chunk=self.n, device=device)
+        self.cache = self.make_cache(w, device)
         pre = w.extra["prefix"]
         for c in range(pre // 2048):
             k, v = w.keys((w.batch, w.n_kv_heads, 2048, w.head_dim), "prefix%d" % c, device), \
@@ -545,6 +545,10 @@ class ChunkBench(DecodeBench):
                 keys += p + 1 - (max(0, p - W + 1) if W else 0)
         self.flops = 4.0 * keys * Hq * d
         torch.cuda.synchronize()
+
+    def make_cache(self, w, device):
+        from kv_cache_decode_ring_gb300 import kvc
+        return kvc.Cache.from_workload(w, max_chunk=self.n, device=device)
 
     def launches_per_step(self):
         return 5                                   # trim, append rows, advance, rotate q, attention
@@ -607,10 +611,90 @@ class ChunkWindowBench(ChunkBench):
         super().__init__(device, batch, total_steps, windowed=True)
 
 
+class ChunkStoreBench(ChunkBench):
+    """The prefix-reuse workload through the prefix store: every request's 8192-row prefill is
+    saved in a store slot under its token IDs; a step looks up each request's query (the first
+    cut IDs of its prefill, then 512 new IDs) on the host, copies the kept rows back into the
+    request (kvc_store_load), and runs kvc_chunk_attn on the suffix."""
+
+    def __init__(self, device, batch=None, total_steps=0):
+        import numpy as np
+        import torch
+        from kv_cache_decode_ring_gb300 import kvc
+        super().__init__(device, batch, total_steps)
+        w, B = self.w, self.w.batch
+        self.store = kvc.PrefixStore(self.cache.cfg, B)
+        rng = np.random.default_rng(w.seed)
+        pre = w.extra["prefix"]
+        self.queries = []
+        for r in range(B):
+            ids = rng.integers(0, 1 << 31, pre, dtype=np.int64)      # token IDs labelling the prefill rows
+            slot = self.cache.save_prefix(self.store, r, ids, "bench", b"prefix-reuse")
+            assert slot == r
+            new = rng.integers(1 << 32, 1 << 33, self.n, dtype=np.int64)   # never equal to a stored ID
+            self.queries.append(np.concatenate([ids[:self.cuts[r]], new]))
+        self.load_bytes = 4 * sum(self.cuts) * w.n_kv_heads * w.head_dim * 2    # K and V, read and written
+        self.load_ev = []
+        torch.cuda.synchronize()
+
+    def make_cache(self, w, device):
+        from kv_cache_decode_ring_gb300 import kvc
+        return kvc.Cache.from_workload(w, max_chunk=self.n, device=device, store_slots=w.batch)
+
+    def launches_per_step(self):
+        return self.w.batch + 4                    # one load per request, append rows, advance, rotate q, attention
+
+    def reuse(self, ev=False):
+        import torch
+        if ev:
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+        for r in range(self.w.batch):
+            slot, cut = self.cache.reuse_prefix(self.store, r, self.queries[r], "bench", b"prefix-reuse")
+        if ev:
+            b.record()
+            self.load_ev.append((a, b))
+
+    def step(self, ev=None):
+        self.reuse(ev is not None)
+        if ev is not None:
+            ev[0].record()
+        self.cache.chunk(self.q, self.k, self.v, self.out)
+        if ev is not None:
+            ev[1].record()
+        self.done += 1
+        return 0
+
+    def e2e_step(self):
+        self.reuse()
+        self.dq.copy_(self.hq, non_blocking=True)
+        self.dk.copy_(self.hk, non_blocking=True)
+        self.dv.copy_(self.hv, non_blocking=True)
+        self.cache.chunk(self.dq, self.dk, self.dv, self.out)
+        self.hout.copy_(self.out, non_blocking=True)
+        self.done += 1
+
+    def extra_report(self, peak_hbm):
+        ms = [a.elapsed_time(b) for a, b in self.load_ev]
+        avg = sum(ms) / len(ms)
+        gbs = self.load_bytes / (avg / 1e3) / 1e9
+        return {"store_load": {"kernel": "kvc_store_load (host lookup + row copy), all requests",
+                               "bytes_per_step": self.load_bytes, "avg_ms": round(avg, 5),
+                               "achieved": round(gbs, 2), "unit": "GB/s", "peak": peak_hbm,
+                               "frac": round(gbs / peak_hbm, 4)}}
+
+    def config(self):
+        c = super().config()
+        c["workload"] = self.w.name + "-store"
+        c["store"] = "%d slots, one per request; lookup over %d entries of %d IDs" % (
+            self.w.batch, self.w.batch, self.w.extra["prefix"])
+        return c
+
+
 BENCHES = {"full-cache-mha": FullCacheBench, "sliding-window-gqa": SlidingWindowBench, "int8-witness": Int8Bench,
            "bf16-at-int8-shape": Bf16AtInt8ShapeBench, "int8-witness-gated": Int8GatedBench,
            "full-cache-mha-paged": FullCachePagedBench, "sliding-window-gqa-paged": SlidingWindowPagedBench,
-           "prefix-reuse": ChunkBench, "prefix-reuse-w4096": ChunkWindowBench}
+           "prefix-reuse": ChunkBench, "prefix-reuse-w4096": ChunkWindowBench, "prefix-reuse-store": ChunkStoreBench}
 
 
 # ----------------------------------------------------------------------------- CPU oracle
@@ -781,6 +865,8 @@ def main():
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
             "wall_s": round(wall, 3),
         }
+        if hasattr(bench, "extra_report"):
+            line.update(bench.extra_report(hbm_peak()[0]))
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
