@@ -336,6 +336,12 @@ int kvc_store_save(kvc_t h, int32_t slot, int32_t b, int32_t n, kvc_stream_t str
  * after kvc_trim, the next call on the handle must append. */
 int kvc_store_load(kvc_t h, int32_t slot, int32_t b, int32_t cut, kvc_stream_t stream);
 
+/* kvc_store_load for n requests at once (h_slots, h_b, h_cuts: host arrays of n
+ * entries; the requests distinct), in one launch per 64 requests.  Every entry
+ * is checked before anything changes; the statuses are those of kvc_store_load. */
+int kvc_store_load_batch(kvc_t h, int32_t n, const int32_t* h_slots, const int32_t* h_b,
+                         const int32_t* h_cuts, kvc_stream_t stream);
+
 /* Static description of a status code. */
 const char* kvc_strerror(int code);
 

@@ -25,86 +25,111 @@ struct kvc_pstore {
 namespace kvc {
 namespace {
 
-constexpr int kStoreRows = 32;         // cache rows per CTA of the copy kernel
+constexpr int kStoreRows = 64;         // cache rows per CTA of the copy kernel
 constexpr int kStoreThreads = 256;
+constexpr int kStoreUnroll = 4;        // row units a thread loads before it stores
+constexpr int kStoreBatch = 64;        // requests per launch of a batched load
+
+struct StoreItem {
+    int slot;                          // store slot (-1: load of nothing)
+    int b;                             // request
+    int cut;                           // load: rows at positions below cut are kept
+    int rows;                          // slots [0, rows) may hold a row to copy
+};
 
 struct StoreArgs {
     char* kc; char* vc;                // cache rows (unpaged runs or pages)
     const int32_t* table;              // paged caches: block table, else nullptr
     int32_t* pos;                      // cache positions [B][S]
     int32_t* next_pos;
-    char* sk; char* sv;                // store slot rows [Hkv][S][d]
-    int32_t* spos;                     // store slot positions [S]
-    int b, Hkv, S, row_bytes;
-    int rows;                          // slots [0, rows) may hold a row to copy
-    int cut;                           // load: rows at positions below cut are kept
-    int load;                          // 1: store slot -> request b; 0: request b -> store slot
-    int empty;                         // load of nothing (request b emptied)
+    char* store;                       // store slot 0; slot i at store + i * stride
+    size_t stride;                     // bytes per store slot: K [Hkv][S][d], V, positions [S]
+    int Hkv, S, row_bytes;
+    int load;                          // 1: store slot -> request; 0: request -> store slot
+    int n;                             // items
+    StoreItem item[kStoreBatch];
 };
 
-// grid (ceil(rows / kStoreRows), Hkv + 1): plane y < Hkv copies KV head y's rows,
-// plane Hkv the positions (and, on a load, next_position).
+// grid (ceil(max rows / kStoreRows), Hkv + 1, items): plane y < Hkv copies KV head y's
+// rows of item z, plane Hkv its positions (and, on a load, next_position).
 // Save: every slot holding a row (position >= 0) goes to the store slot, with the
 // positions array.  Load: the store slot's rows at positions [0, cut) come back;
-// every other slot of request b is marked empty.
+// every other slot of the request is marked empty.
 template <typename U>
 __global__ void __launch_bounds__(kStoreThreads) store_copy_kernel(const StoreArgs a) {
+    const StoreItem it = a.item[blockIdx.z];
     const int h = blockIdx.y;
-    int32_t* pb = a.pos + (size_t)a.b * a.S;
+    const size_t half = (size_t)a.Hkv * a.S * a.row_bytes;
+    char* sbase = it.slot >= 0 ? a.store + (size_t)it.slot * a.stride : nullptr;
+    const int32_t* spos = sbase ? reinterpret_cast<const int32_t*>(sbase + 2 * half) : nullptr;
+    int32_t* pb = a.pos + (size_t)it.b * a.S;
     if (h == a.Hkv) {
         for (int s = blockIdx.x * blockDim.x + threadIdx.x; s < a.S; s += gridDim.x * blockDim.x) {
             if (a.load) {
-                const int p = a.empty ? -1 : a.spos[s];
-                pb[s] = (p >= 0 && p < a.cut) ? p : -1;
+                const int p = spos ? spos[s] : -1;
+                pb[s] = (p >= 0 && p < it.cut) ? p : -1;
             } else {
-                a.spos[s] = pb[s];
+                reinterpret_cast<int32_t*>(sbase + 2 * half)[s] = pb[s];
             }
         }
-        if (a.load && blockIdx.x == 0 && threadIdx.x == 0) a.next_pos[a.b] = a.cut;
+        if (a.load && blockIdx.x == 0 && threadIdx.x == 0) a.next_pos[it.b] = it.cut;
         return;
     }
-    if (a.empty) return;
+    if (!sbase) return;
     const int upr = a.row_bytes / (int)sizeof(U);        // units per row
     const int s0 = blockIdx.x * kStoreRows;
-    const int32_t* held = a.load ? a.spos : pb;          // the side whose rows are read
-    for (int i = threadIdx.x; i < kStoreRows * upr; i += blockDim.x) {
-        const int s = s0 + i / upr, u = i % upr;
-        if (s >= a.rows || s >= a.S) break;              // s grows with i
-        const int p = held[s];
-        if (p < 0 || (a.load && p >= a.cut)) continue;
-        const size_t crow = kv_row(a.table, a.b, h, s, a.Hkv, a.S);
-        const size_t srow = (size_t)h * a.S + s;
-        U* ck = reinterpret_cast<U*>(a.kc + crow * a.row_bytes) + u;
-        U* cv = reinterpret_cast<U*>(a.vc + crow * a.row_bytes) + u;
-        U* sk = reinterpret_cast<U*>(a.sk + srow * a.row_bytes) + u;
-        U* sv = reinterpret_cast<U*>(a.sv + srow * a.row_bytes) + u;
-        if (a.load) { *ck = *sk; *cv = *sv; }
-        else { *sk = *ck; *sv = *cv; }
+    if (s0 >= it.rows) return;
+    const int nrows = it.rows - s0 < kStoreRows ? it.rows - s0 : kStoreRows;
+    const int total = nrows * upr;
+    const int32_t* held = a.load ? spos : pb;            // the side whose rows are read
+    for (int base = threadIdx.x; base < total; base += kStoreUnroll * kStoreThreads) {
+        U kx[kStoreUnroll], vx[kStoreUnroll];
+        U* kd[kStoreUnroll];
+        U* vd[kStoreUnroll];
+#pragma unroll
+        for (int j = 0; j < kStoreUnroll; ++j) {
+            kd[j] = nullptr;
+            const int i = base + j * kStoreThreads;
+            if (i >= total) continue;
+            const int s = s0 + i / upr, u = i % upr;
+            const int p = held[s];
+            if (p < 0 || (a.load && p >= it.cut)) continue;
+            const size_t crow = kv_row(a.table, it.b, h, s, a.Hkv, a.S);
+            const size_t srow = (size_t)h * a.S + s;
+            U* ck = reinterpret_cast<U*>(a.kc + crow * a.row_bytes) + u;
+            U* cv = reinterpret_cast<U*>(a.vc + crow * a.row_bytes) + u;
+            U* sk = reinterpret_cast<U*>(sbase + srow * a.row_bytes) + u;
+            U* sv = reinterpret_cast<U*>(sbase + half + srow * a.row_bytes) + u;
+            if (a.load) { kx[j] = *sk; vx[j] = *sv; kd[j] = ck; vd[j] = cv; }
+            else { kx[j] = *ck; vx[j] = *cv; kd[j] = sk; vd[j] = sv; }
+        }
+#pragma unroll
+        for (int j = 0; j < kStoreUnroll; ++j)
+            if (kd[j]) { *kd[j] = kx[j]; *vd[j] = vx[j]; }
     }
 }
 
 cudaError_t launch_store_copy(const StoreArgs& a, cudaStream_t st) {
-    const int blocks = a.rows > 0 ? (a.rows + kStoreRows - 1) / kStoreRows : 1;
-    dim3 grid(blocks, a.Hkv + 1);
+    int rows = 0;
+    for (int i = 0; i < a.n; ++i) rows = a.item[i].rows > rows ? a.item[i].rows : rows;
+    const int blocks = rows > 0 ? (rows + kStoreRows - 1) / kStoreRows : 1;
+    dim3 grid(blocks, a.Hkv + 1, a.n);
     if (a.row_bytes % 16 == 0) store_copy_kernel<uint4><<<grid, kStoreThreads, 0, st>>>(a);
     else store_copy_kernel<uint32_t><<<grid, kStoreThreads, 0, st>>>(a);
     return cudaGetLastError();
 }
 
-StoreArgs store_args(kvc_handle* h, int slot, int b) {
+StoreArgs store_args(kvc_handle* h, int load) {
     const Shape& s = h->sh;
     StoreArgs a{};
     a.kc = h->state + h->L.k; a.vc = h->state + h->L.v;
     a.table = s.pages ? reinterpret_cast<const int32_t*>(h->state + h->L.table) : nullptr;
     a.pos = reinterpret_cast<int32_t*>(h->state + h->L.pos);
     a.next_pos = reinterpret_cast<int32_t*>(h->state + h->L.next_pos);
-    if (slot >= 0) {
-        char* base = h->state + h->L.store + (size_t)slot * h->L.store_stride;
-        const size_t half = (size_t)s.Hkv * s.S * s.d * s.elem;
-        a.sk = base; a.sv = base + half;
-        a.spos = reinterpret_cast<int32_t*>(base + 2 * half);
-    }
-    a.b = b; a.Hkv = s.Hkv; a.S = s.S; a.row_bytes = s.d * s.elem;
+    a.store = h->state + h->L.store;
+    a.stride = h->L.store_stride;
+    a.Hkv = s.Hkv; a.S = s.S; a.row_bytes = s.d * s.elem;
+    a.load = load;
     return a;
 }
 
@@ -190,44 +215,57 @@ int kvc_store_save(kvc_t h, int32_t slot, int32_t b, int32_t n, kvc_stream_t str
     const Shape& s = h->sh;
     if (s.store_slots == 0) return KVC_ERR_UNSUPPORTED;
     if (slot < 0 || slot >= s.store_slots || b < 0 || b >= s.B || n < 1 || n != h->np[b]) return KVC_ERR_ARG;
-    StoreArgs a = store_args(h, slot, b);
-    a.rows = s.ring ? s.S : n;
-    a.load = 0;
+    StoreArgs a = store_args(h, 0);
+    a.n = 1;
+    a.item[0] = StoreItem{slot, b, 0, s.ring ? s.S : n};
     if (launch_store_copy(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KVC_ERR_CUDA;
     h->store_n[slot] = n;
     return KVC_OK;
 }
 
-int kvc_store_load(kvc_t h, int32_t slot, int32_t b, int32_t cut, kvc_stream_t stream) {
-    if (!h) return KVC_ERR_ARG;
+int kvc_store_load_batch(kvc_t h, int32_t n, const int32_t* h_slots, const int32_t* h_b, const int32_t* h_cuts,
+                         kvc_stream_t stream) {
+    if (!h || n < 0) return KVC_ERR_ARG;
     const Shape& s = h->sh;
     if (s.store_slots == 0) return KVC_ERR_UNSUPPORTED;
-    if (b < 0 || b >= s.B || slot < -1 || slot >= s.store_slots) return KVC_ERR_ARG;
-    const int n = slot < 0 ? 0 : h->store_n[slot];
-    if (n < 0 || cut < 0 || cut > n) return KVC_ERR_ARG;
-    if (s.ring && cut > 0) {
-        // the token at `cut` attends to [cut - S + 1, cut); the slot holds [n - S, n)
-        const int lo = cut - s.S + 1 > 0 ? cut - s.S + 1 : 0;
-        const int resident = n - s.S > 0 ? n - s.S : 0;
-        if (lo < resident) return KVC_ERR_EVICTED;
+    if (n == 0) return KVC_OK;
+    if (!h_slots || !h_b || !h_cuts) return KVC_ERR_ARG;
+    // every item is checked before anything changes
+    std::vector<char> seen(s.B, 0);
+    for (int i = 0; i < n; ++i) {
+        const int slot = h_slots[i], b = h_b[i], cut = h_cuts[i];
+        if (b < 0 || b >= s.B || seen[b] || slot < -1 || slot >= s.store_slots) return KVC_ERR_ARG;
+        seen[b] = 1;
+        const int len = slot < 0 ? 0 : h->store_n[slot];
+        if (len < 0 || cut < 0 || cut > len) return KVC_ERR_ARG;
+        if (s.ring && cut > 0) {
+            // the token at `cut` attends to [cut - S + 1, cut); the slot holds [len - S, len)
+            const int lo = cut - s.S + 1 > 0 ? cut - s.S + 1 : 0;
+            const int resident = len - s.S > 0 ? len - s.S : 0;
+            if (lo < resident) return KVC_ERR_EVICTED;
+        }
     }
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (s.pages) {
-        // request b gives back all its pages and maps those that the kept rows need
+        // the requests give back all their pages and map those that the kept rows need
         const int npg = s.S / kPage;
-        const long long lo = s.ring && n > s.S ? n - s.S : 0;
-        int need = 0, held = 0;
-        for (int lp = 0; lp < npg; ++lp) {
-            need += page_touched(s, lp, lo, cut) ? 1 : 0;
-            held += h->table_h[(size_t)b * npg + lp] >= 0 ? 1 : 0;
-        }
-        if (need > held + (int)h->page_free.size()) return KVC_ERR_CAPACITY;
-        for (int lp = 0; lp < npg; ++lp) {
-            int32_t& e = h->table_h[(size_t)b * npg + lp];
-            if (e >= 0) { h->page_free.push_back(e); e = -1; }
-        }
         std::vector<int> from(h->np.begin(), h->np.end()), to(from);
-        from[b] = (int)lo; to[b] = cut;
+        long long need = 0, held = 0;
+        for (int i = 0; i < n; ++i) {
+            const int b = h_b[i], len = h_slots[i] < 0 ? 0 : h->store_n[h_slots[i]];
+            const long long lo = s.ring && len > s.S ? len - s.S : 0;
+            from[b] = (int)lo; to[b] = h_cuts[i];
+            for (int lp = 0; lp < npg; ++lp) {
+                need += page_touched(s, lp, lo, h_cuts[i]) ? 1 : 0;
+                held += h->table_h[(size_t)b * npg + lp] >= 0 ? 1 : 0;
+            }
+        }
+        if (need > held + (long long)h->page_free.size()) return KVC_ERR_CAPACITY;
+        for (int i = 0; i < n; ++i)
+            for (int lp = 0; lp < npg; ++lp) {
+                int32_t& e = h->table_h[(size_t)h_b[i] * npg + lp];
+                if (e >= 0) { h->page_free.push_back(e); e = -1; }
+            }
         int rc = KVC_OK;
         if (map_pages(h, from, to, st, &rc) != cudaSuccess) return KVC_ERR_CUDA;
         if (rc) return rc;               // not reached: the count above guarantees the pages
@@ -235,15 +273,22 @@ int kvc_store_load(kvc_t h, int32_t slot, int32_t b, int32_t cut, kvc_stream_t s
                             cudaMemcpyHostToDevice, st) != cudaSuccess)
             return KVC_ERR_CUDA;
     }
-    StoreArgs a = store_args(h, slot, b);
-    a.rows = slot < 0 ? 0 : (s.ring ? s.S : cut);
-    a.cut = cut;
-    a.load = 1;
-    a.empty = slot < 0;
-    if (launch_store_copy(a, st) != cudaSuccess) return KVC_ERR_CUDA;
-    h->np[b] = cut;
+    for (int i0 = 0; i0 < n; i0 += kStoreBatch) {
+        StoreArgs a = store_args(h, 1);
+        a.n = n - i0 < kStoreBatch ? n - i0 : kStoreBatch;
+        for (int j = 0; j < a.n; ++j) {
+            const int slot = h_slots[i0 + j], cut = h_cuts[i0 + j];
+            a.item[j] = StoreItem{slot, h_b[i0 + j], cut, slot < 0 ? 0 : (s.ring ? s.S : cut)};
+        }
+        if (launch_store_copy(a, st) != cudaSuccess) return KVC_ERR_CUDA;
+    }
+    for (int i = 0; i < n; ++i) h->np[h_b[i]] = h_cuts[i];
     if (s.ring) h->ring_needs_append = true;
     return KVC_OK;
+}
+
+int kvc_store_load(kvc_t h, int32_t slot, int32_t b, int32_t cut, kvc_stream_t stream) {
+    return kvc_store_load_batch(h, 1, &slot, &b, &cut, stream);
 }
 
 }  // extern "C"

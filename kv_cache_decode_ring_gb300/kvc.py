@@ -51,7 +51,7 @@ EXPORTED = ["kvc_state_bytes", "kvc_create", "kvc_destroy", "kvc_append", "kvc_a
             "kvc_next_positions", "kvc_device_status", "kvc_prefix_cut", "kvc_strerror",
             "kvc_int8_block_risk", "kvc_int8_gate", "kvc_int8_restore",
             "kvc_pstore_create", "kvc_pstore_destroy", "kvc_pstore_insert", "kvc_pstore_lookup",
-            "kvc_store_save", "kvc_store_load"]
+            "kvc_store_save", "kvc_store_load", "kvc_store_load_batch"]
 
 _lock = threading.Lock()
 _lib = None
@@ -96,6 +96,7 @@ def lib() -> ctypes.CDLL:
                 "kvc_pstore_lookup": [P, P, i32, ctypes.c_char_p, P, i32, ctypes.POINTER(i32), ctypes.POINTER(i32)],
                 "kvc_store_save": [P, i32, i32, i32, P],
                 "kvc_store_load": [P, i32, i32, i32, P],
+                "kvc_store_load_batch": [P, i32, P, P, P, P],
             }
             for name, args in sig.items():
                 fn = getattr(L, name)
@@ -328,6 +329,15 @@ def kvc_store_load(h, slot: int, b: int, cut: int, stream=None) -> None:
     _check(lib().kvc_store_load(h, int(slot), int(b), int(cut), _stream(stream)), "kvc_store_load")
 
 
+def kvc_store_load_batch(h, slots, bs, cuts, stream=None) -> None:
+    arr = [np.ascontiguousarray(np.asarray(x, dtype=np.int32).reshape(-1)) for x in (slots, bs, cuts)]
+    n = len(arr[0])
+    if any(len(x) != n for x in arr):
+        raise ValueError("slots, requests and cuts must have one entry per load")
+    ptr = [x.ctypes.data_as(ctypes.c_void_p) if n else None for x in arr]
+    _check(lib().kvc_store_load_batch(h, n, ptr[0], ptr[1], ptr[2], _stream(stream)), "kvc_store_load_batch")
+
+
 class PrefixStore:
     """Host policy of the prefix store (see include/kvc.h): which stored prefill a query
     reuses, and how many rows.  The rows live in a Cache's store slots."""
@@ -484,6 +494,9 @@ class Cache:
 
     def store_load(self, slot, b, cut, stream=None):
         kvc_store_load(self.h, slot, b, cut, stream)
+
+    def store_load_batch(self, slots, bs, cuts, stream=None):
+        kvc_store_load_batch(self.h, slots, bs, cuts, stream)
 
     def save_prefix(self, store: PrefixStore, b, ids, scope: str, signature=b"", stream=None) -> int:
         """Records request b's prefill of ``ids`` in ``store`` and copies its rows to the slot."""

@@ -236,3 +236,36 @@ def test_store_errors_change_nothing():
     pc.store_load(0, 1, 32)                                  # 2 pages: fits
     pm.load(1, pm.snapshot(0), 32)
     check_state(pc, pm, pw)
+
+
+@pytest.mark.parametrize("paged", [False, True])
+def test_store_load_batch(paged):
+    """One batched load equals the single loads; a bad entry anywhere changes nothing."""
+    w = wl.small("store-batch", B=4, Hq=8, Hkv=2, d=64, capacity=256, rope_base=10000.0, seed=41)
+    cache = kvc.Cache.from_workload(w, store_slots=2, page_pool=4 * 256 // 16 if paged else 0)
+    model = oracle_for(w)
+    k, v = w.prefill_chunk(0, 200)
+    cache.append_rows(k.cuda(), v.cuda(), counts=[200, 77, 5, 130])
+    model.append_rows(host(k), host(v), [200, 77, 5, 130])
+    cache.store_save(0, 0, 200)
+    cache.store_save(1, 3, 130)
+    snaps = {0: model.snapshot(0), 1: model.snapshot(3)}
+    with pytest.raises(kvc.KvcError) as e:
+        cache.store_load_batch([0, 1], [2, 2], [10, 10])     # one request twice
+    assert e.value.code == kvc.KVC_ERR_ARG
+    with pytest.raises(kvc.KvcError) as e:
+        cache.store_load_batch([0, 1], [1, 2], [10, 131])    # the second is past slot 1's rows
+    assert e.value.code == kvc.KVC_ERR_ARG
+    check_state(cache, model, w)
+    loads = [(1, 0, 129), (-1, 1, 0), (0, 2, 200), (0, 3, 17)]
+    cache.store_load_batch(*zip(*loads))
+    for slot, b, cut in loads:
+        model.load(b, snaps.get(slot), cut)
+    check_state(cache, model, w)
+    for s in range(3):
+        q, k1, v1 = w.step_qkv(s)
+        cache.append(k1.cuda(), v1.cuda())
+        model.append(host(k1), host(v1))
+        assert_close(cache.decode(q.cuda()), model.decode(host(q)), w.dtype, "decode after batched load")
+    check_state(cache, model, w)
+    assert cache.device_status() == 0
