@@ -21,6 +21,12 @@ gated fallback ("SGLang 生产级落地与闭环门控修复": swap in the lossl
 from the full-precision backing store, zero its witnesses) is held exact as
 well, with residual 0 and witness 0.
 
+Tier B ([WITCERT], the subtractive-dither paragraph, and "SGLang 生产级落地与闭环门控修复"
+for the counter): codes rint(x/s + u) with a Philox dither u per element, read back
+as (code - u) s; no witnesses.  The probabilistic certificate of this tier needs a
+failure budget and a concentration formula the page does not give, so the oracle
+states no bound for it.
+
 [LEAN]    "用Lean4形式化验证滑动窗口KV Cache的正确性" (framerc.cn/news/4505248)
 [PREFIX]  "LLM 機制實驗（五）：改了歷史，能否只重算變化的後綴？" (huhohoo.com)
 [LOOP]    "KV Cache 自回归生成推理（增量更新与状态拼接）" (airsota.com/?p=549)
@@ -64,13 +70,16 @@ class DecodeOracle:
     """
 
     def __init__(self, B, Hq, Hkv, d, layout="contiguous", capacity=0, window=0,
-                 rope_base=0.0, dtype="f32", quant=None):
+                 rope_base=0.0, dtype="f32", quant=None, dither_key=(0, 0), layer=0):
         assert Hq % Hkv == 0
         self.B, self.Hq, self.Hkv, self.d = B, Hq, Hkv, d
         self.g = Hq // Hkv
         self.layout, self.capacity = layout, capacity
         self.window = capacity if layout == "ring" else window
         self.rope_base, self.dtype, self.quant = rope_base, dtype, quant
+        # Tier B (quant "int8-dither"): the Philox key, the layer and each request's ID
+        self.dither_key, self.layer = tuple(dither_key), layer
+        self.request_ids = list(range(B))
         # full history of stored rows per request: lists of [Hkv, d] fp32 arrays
         self.hk: List[List[np.ndarray]] = [[] for _ in range(B)]
         self.hv: List[List[np.ndarray]] = [[] for _ in range(B)]
@@ -134,7 +143,7 @@ class DecodeOracle:
                 raise OracleError("arg", "cut %d outside [0, %d]" % (cut, n))
             if self.rings is not None and not ring_trim_allowed(cut, n, self.capacity):
                 raise OracleError("evicted", "request %d: rows needed after cut %d are gone" % (b, cut))
-            if self.quant == "int8" and cut % QBLOCK and cut < (n // QBLOCK) * QBLOCK:
+            if self.quant in ("int8", "int8-dither") and cut % QBLOCK and cut < (n // QBLOCK) * QBLOCK:
                 raise OracleError("evicted", "request %d: cut %d splits a quantized block" % (b, cut))
         for b, cut in enumerate(cuts):
             n = self.length(b)
@@ -258,11 +267,33 @@ class DecodeOracle:
         return last_window(self.window if self.window else len(cells), cells)
 
     # ------------------------------------------------------------ INT8 tier
+    def set_request_id(self, b, rid):
+        """Tier B: the request ID in the dither counters; only while request b is empty."""
+        if self.length(b):
+            raise OracleError("arg", "request %d holds rows" % b)
+        self.request_ids[b] = int(rid) & 0xFFFFFFFF
+
+    def dither(self, b, h):
+        """Tier B: u(positions, tensor) -> [n, d] fp32 dithers of (request b, KV head h), else None."""
+        if self.quant != "int8-dither":
+            return None
+        key, rid, layer, d = self.dither_key, self.request_ids[b], self.layer, self.d
+
+        def u(p0, n, tensor):
+            return nm.dither_values(nm.dither_rows(key, rid, layer, h, p0, n, d, tensor))
+        return u
+
     def quantized_block(self, b, h, blk):
-        """(sK, codesK [16,d], sV, codesV, wit bits [16,16]) of one complete block."""
+        """(sK, codesK [16,d], sV, codesV, wit bits [16,16]) of one complete block
+        (Tier B: dithered codes and no witnesses, None)."""
         lo = blk * QBLOCK
         K = np.stack([self.hk[b][p][h] for p in range(lo, lo + QBLOCK)])
         V = np.stack([self.hv[b][p][h] for p in range(lo, lo + QBLOCK)])
+        u = self.dither(b, h)
+        if u is not None:
+            sK, cK = nm.quantize_block_dither(K, u(lo, QBLOCK, 0))
+            sV, cV = nm.quantize_block_dither(V, u(lo, QBLOCK, 1))
+            return sK, cK, sV, cV, None
         sK, cK = nm.quantize_block(K)
         sV, cV = nm.quantize_block(V)
         wit = np.stack([nm.witness_row(K[r], cK[r], sK, NBANDS) for r in range(QBLOCK)])
@@ -274,7 +305,7 @@ class DecodeOracle:
         hi = n if hi is None else hi
         K = np.stack([self.hk[b][p][h] for p in range(lo, hi)]) if hi > lo else np.zeros((0, self.d), np.float32)
         V = np.stack([self.hv[b][p][h] for p in range(lo, hi)]) if hi > lo else np.zeros((0, self.d), np.float32)
-        return int8_rows(K, V, lo, (n // QBLOCK) * QBLOCK, self.restored[b][h])
+        return int8_rows(K, V, lo, (n // QBLOCK) * QBLOCK, self.restored[b][h], self.dither(b, h))
 
     def restore(self, blocks):
         """Gated fallback ("SGLang 生产级落地与闭环门控修复"): hold the listed complete
@@ -299,11 +330,11 @@ class DecodeOracle:
             K = np.stack([self.hk[b][p][h] for p in range(lo_blk, t + 1)])
             V = np.stack([self.hv[b][p][h] for p in range(lo_blk, t + 1)])
             res[(b, hq)] = int8_decode_one(qf, K, V, lo_blk, t, self.window, (self.length(b) // QBLOCK) * QBLOCK,
-                                           self.restored[b][h])
+                                           self.restored[b][h], self.dither(b, h))
         return res
 
 
-def int8_rows(K, V, p0, nfull, restored=()):
+def int8_rows(K, V, p0, nfull, restored=(), dither=None):
     """Rows at positions p0.. of one (request, KV head) as the INT8 tier holds them.
 
     ``K``, ``V``: [n, d] exact stored rows (fp32 values of the bf16 cache); ``p0`` a
@@ -313,6 +344,11 @@ def int8_rows(K, V, p0, nfull, restored=()):
     complete blocks dequantized (code * s, exact in fp64) with their key residuals
     and witness values; the exact tail rows and restored blocks with residual 0 and
     witness 0 ([WITCERT] "频带酉性与双层证书"; "SGLang 生产级落地与闭环门控修复").
+
+    Tier B ([WITCERT], the subtractive-dither paragraph): ``dither(p0, n, tensor)``
+    gives the fp32 dithers u of n rows from position p0 (tensor 0 keys, 1 values);
+    codes are rint(x/s + u) and the rows read back as (code - u) s, exact in fp64.
+    There are no witnesses then (the returned witness values are None).
     """
     n, d = K.shape
     assert p0 % QBLOCK == 0
@@ -326,16 +362,24 @@ def int8_rows(K, V, p0, nfull, restored=()):
         if (p0 + r0) // QBLOCK in restored:
             continue
         sl = slice(r0, r0 + QBLOCK)
+        if dither is not None:
+            uK, uV = dither(p0 + r0, QBLOCK, 0), dither(p0 + r0, QBLOCK, 1)
+            sK, cK = nm.quantize_block_dither(K[sl], uK)
+            sV, cV = nm.quantize_block_dither(V[sl], uV)
+            Kd[sl] = (cK.astype(np.float64) - uK.astype(np.float64)) * np.float64(sK)
+            Vd[sl] = (cV.astype(np.float64) - uV.astype(np.float64)) * np.float64(sV)
+            R[sl] = K[sl].astype(np.float64) - Kd[sl]
+            continue
         sK, cK = nm.quantize_block(K[sl])
         sV, cV = nm.quantize_block(V[sl])
         Kd[sl] = cK.astype(np.float64) * np.float64(sK)
         Vd[sl] = cV.astype(np.float64) * np.float64(sV)
         R[sl] = K[sl].astype(np.float64) - Kd[sl]
         Wt[sl] = np.stack([nm.f16_values(nm.witness_row(K[r0 + i], cK[i], sK, NBANDS)) for i in range(QBLOCK)])
-    return Kd, Vd, K.astype(np.float64), R, Wt
+    return Kd, Vd, K.astype(np.float64), R, (None if dither is not None else Wt)
 
 
-def int8_decode_one(qf, K, V, p0, t, window, nfull, restored=()):
+def int8_decode_one(qf, K, V, p0, t, window, nfull, restored=(), dither=None):
     """INT8-tier decode of one query row over rows p0..t of one KV head, fp64.
 
     Returns {"out": attention over the dequantized rows, "out_exact": over the
@@ -343,21 +387,26 @@ def int8_decode_one(qf, K, V, p0, t, window, nfull, restored=()):
     "tv": total variation between the exact and the dequantized softmax,
     "cmax": max_t c_t, "q": the fp32 query}.  c_t = (1/sqrt d) sum_b ||q_b|| w_{t,b}
     ([WITCERT] "频带酉性与双层证书") from the fp32 query and the stored witnesses.
+    Tier B (``dither``, see :func:`int8_rows`): no witnesses, so "c" is None and
+    "cmax" 0.
     """
     d = K.shape[1]
     bw = d // NBANDS
     q64 = np.asarray(qf, dtype=np.float64)
-    Kd, Vd, Kx, R, W = int8_rows(K, V, p0, nfull, restored)
+    Kd, Vd, Kx, R, W = int8_rows(K, V, p0, nfull, restored, dither)
     Vx = V.astype(np.float64)
     out = nm.attend(q64, Kd, Vd, t, window, p0=p0)[0]
     out_exact = nm.attend(q64, Kx, Vx, t, window, p0=p0)[0]
     p_deq = nm.softmax_weights(q64, Kd, t, window, p0=p0)
     p_ex = nm.softmax_weights(q64, Kx, t, window, p0=p0)
-    qn = np.sqrt((q64.reshape(NBANDS, bw) ** 2).sum(axis=1))
-    c = (W * qn[None, :]).sum(axis=1) / math.sqrt(d)
     eps = np.abs(R @ q64) / math.sqrt(d)
     lo = 0 if not window else max(0, t - window + 1)
     vis = slice(lo - p0, None)
+    if W is None:
+        return {"out": out, "out_exact": out_exact, "c": None, "eps": eps[vis],
+                "tv": 0.5 * np.abs(p_ex - p_deq).sum(), "cmax": 0.0, "q": qf}
+    qn = np.sqrt((q64.reshape(NBANDS, bw) ** 2).sum(axis=1))
+    c = (W * qn[None, :]).sum(axis=1) / math.sqrt(d)
     return {"out": out, "out_exact": out_exact, "c": c[vis], "eps": eps[vis],
             "tv": 0.5 * np.abs(p_ex - p_deq).sum(), "cmax": float(c[vis].max()) if c[vis].size else 0.0,
             "q": qf}

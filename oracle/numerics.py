@@ -63,6 +63,10 @@ def lib():
                 "orc_quantize_block": (f32, [P, i64, P]),
                 "orc_witness_row": (i32, [P, P, f32, i32, i32, P]),
                 "orc_residual_row": (None, [P, P, f32, i32, P]),
+                "orc_philox4x32_10": (None, [P, P, P]),
+                "orc_quantize_block_dither": (f32, [P, P, i64, P]),
+                "orc_dither_rows": (None, [P, ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32, i64, i64, i32,
+                                           i32, P]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -216,6 +220,65 @@ def residual_row(x, codes, s) -> np.ndarray:
     r = np.empty_like(x)
     lib().orc_residual_row(_p(x), _p(codes), float(s), x.size, _p(r))
     return r
+
+
+def philox4x32_10(ctr, key) -> np.ndarray:
+    """Philox4x32-10 of one counter (4 uint32) under one key (2 uint32): 4 uint32 words."""
+    c = np.ascontiguousarray(np.asarray(ctr, dtype=np.uint64).astype(np.uint32))
+    k = np.ascontiguousarray(np.asarray(key, dtype=np.uint64).astype(np.uint32))
+    out = np.empty(4, dtype=np.uint32)
+    lib().orc_philox4x32_10(_p(c), _p(k), _p(out))
+    return out
+
+
+# Subtractive-dither streams ([WITCERT] Tier B: Philox keyed on the five-tuple
+# request, layer, KV head, token, channel).  The counter of one call is
+#   (position t, group + 256 * tensor, KV head + 65536 * layer, request ID)
+# with tensor 0 for keys and 1 for values, under the cache's 64-bit key.  A call
+# gives 16 bytes r (word w holds bytes 4w .. 4w + 3, least significant first);
+# a channel's dither is u = r / 256 - 1/2.
+#   keys:   group j covers channels 16 j .. 16 j + 15, byte i -> channel 16 j + i
+#   values: group j < 8 covers the channels c = 8 i + j,  byte i -> channel 8 i + j
+def dither_bytes(key, request, layer, kv_head, position, d, tensor) -> np.ndarray:
+    """The d dither bytes of one row (K: tensor 0, V: tensor 1) as uint8, one Philox call
+    at a time in Python (the plain statement of the mapping above)."""
+    out = np.empty(d, dtype=np.uint8)
+    c2 = (int(kv_head) + 65536 * int(layer)) & 0xFFFFFFFF
+    if tensor == 0:
+        for j in range(d // 16):
+            w = philox4x32_10([position, j, c2, request], key)
+            out[16 * j:16 * j + 16] = w.view(np.uint8)
+    else:
+        for j in range(8):
+            w = philox4x32_10([position, j + 256, c2, request], key)
+            by = w.view(np.uint8)
+            for i in range(d // 8):
+                out[8 * i + j] = by[i]
+    return out
+
+
+def dither_rows(key, request, layer, kv_head, p0, n, d, tensor) -> np.ndarray:
+    """dither_bytes of rows p0 .. p0+n-1, [n, d] uint8 (``orc_dither_rows``)."""
+    k = np.ascontiguousarray(np.asarray(key, dtype=np.uint64).astype(np.uint32))
+    out = np.empty((n, d), dtype=np.uint8)
+    lib().orc_dither_rows(_p(k), int(request) & 0xFFFFFFFF, int(layer), int(kv_head), int(p0), int(n), int(d),
+                          int(tensor), _p(out))
+    return out
+
+
+def dither_values(rbytes) -> np.ndarray:
+    """u = r / 256 - 1/2 (exact in fp32)."""
+    return (np.asarray(rbytes, dtype=np.float32) / np.float32(256.0) - np.float32(0.5)).astype(np.float32)
+
+
+def quantize_block_dither(x, u) -> tuple:
+    """(scale, int8 codes) of one block with the subtractive dither u; see ``orc_quantize_block_dither``."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    u = np.ascontiguousarray(u, dtype=np.float32)
+    assert u.shape == x.shape
+    codes = np.empty(x.shape, dtype=np.int8)
+    s = lib().orc_quantize_block_dither(_p(x), _p(u), x.size, _p(codes))
+    return np.float32(s), codes
 
 
 def f16_values(bits) -> np.ndarray:

@@ -283,6 +283,85 @@ float orc_quantize_block(const float* x, int64_t count, int8_t* codes)
 }
 
 /*
+ * Philox4x32-10 (J. K. Salmon, M. A. Moraes, R. O. Dror, D. E. Shaw, "Parallel
+ * Random Numbers: As Easy as 1, 2, 3", SC 2011): a counter of four 32-bit words
+ * and a key of two go through ten rounds; each round multiplies counter words 0
+ * and 2 by the round multipliers (64-bit products split into high and low
+ * halves), and recombines them with words 1 and 3 and the key by xor, after
+ * which the key is bumped by the Weyl constants.
+ */
+void orc_philox4x32_10(const uint32_t* ctr, const uint32_t* key, uint32_t* out)
+{
+    uint32_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3];
+    uint32_t k0 = key[0], k1 = key[1];
+    for (int r = 0; r < 10; ++r) {
+        const uint64_t p0 = (uint64_t)0xD2511F53u * c0;
+        const uint64_t p1 = (uint64_t)0xCD9E8D57u * c2;
+        const uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1 ^ k0;
+        const uint32_t n2 = (uint32_t)(p0 >> 32) ^ c3 ^ k1;
+        c0 = n0; c1 = (uint32_t)p1; c2 = n2; c3 = (uint32_t)p0;
+        k0 += 0x9E3779B9u; k1 += 0xBB67AE85u;
+    }
+    out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+}
+
+/*
+ * Dither bytes of n rows at positions p0 .. p0+n-1 of one (request, layer, KV head)
+ * and tensor (0 = keys, 1 = values), out[n][d].  One Philox call per (position,
+ * group) with counter (position, group + 256 tensor, KV head + 65536 layer,
+ * request); byte i of the call (word i/4, least significant byte first) is the
+ * dither of channel 16 group + i for keys (group < d/16) and of channel
+ * 8 i + group for values (group < 8).
+ */
+void orc_dither_rows(const uint32_t* key, uint32_t request, uint32_t layer, uint32_t kv_head, int64_t p0,
+                     int64_t n, int d, int tensor, uint8_t* out)
+{
+    const uint32_t c2 = kv_head + 65536u * layer;
+    for (int64_t r = 0; r < n; ++r) {
+        uint8_t* row = out + r * d;
+        const int groups = tensor == 0 ? d / 16 : 8;
+        for (int j = 0; j < groups; ++j) {
+            const uint32_t ctr[4] = {(uint32_t)(p0 + r), (uint32_t)j + 256u * (uint32_t)tensor, c2, request};
+            uint32_t w[4];
+            orc_philox4x32_10(ctr, key, w);
+            for (int i = 0; i < 16; ++i) {
+                const uint8_t byte = (uint8_t)(w[i / 4] >> (8 * (i % 4)));
+                if (tensor == 0) row[16 * j + i] = byte;
+                else if (8 * i + j < d) row[8 * i + j] = byte;
+            }
+        }
+    }
+}
+
+/*
+ * Block quantization with a subtractive dither ([WITCERT] "为了进一步压榨显存极限"
+ * paragraph, Tier B): the dither u (one per element, multiples of 2^-8 in
+ * [-1/2, 1/2)) is added before rounding and removed again on reading:
+ *   s = amax/127,  code = clamp(rint(x/s + u), -127, 127),  x_hat = (code - u) s.
+ * x/s and the addition are IEEE fp32 operations (the GPU does the same); s = 0
+ * gives codes 0.  Returns s.
+ */
+float orc_quantize_block_dither(const float* x, const float* u, int64_t count, int8_t* codes)
+{
+    float amax = 0.0f;
+    for (int64_t i = 0; i < count; ++i) {
+        float a = fabsf(x[i]);
+        if (a > amax) amax = a;
+    }
+    float s = amax / 127.0f;
+    for (int64_t i = 0; i < count; ++i) {
+        if (s == 0.0f) { codes[i] = 0; continue; }
+        volatile float y = x[i] / s;
+        volatile float z = y + u[i];
+        float r = rintf(z);
+        if (r > 127.0f) r = 127.0f;
+        if (r < -127.0f) r = -127.0f;
+        codes[i] = (int8_t)r;
+    }
+    return s;
+}
+
+/*
  * Witness of one key row ([WITCERT] "频带酉性与双层证书": w_{t,b} = ||r_{t,b}||
  * for 16 bands, fp16, 32 bytes per token and head).
  * r = x - code*s is exact in fp64 and also representable in fp32 (|r| <= s/2
