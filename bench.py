@@ -332,8 +332,7 @@ class Int8Bench(DecodeBench):
     def __init__(self, device, batch=None, total_steps=0):
         import torch
         from kv_cache_decode_ring_gb300 import kvc
-        from kv_cache_decode_ring_gb300 import workloads as wl
-        self.w = w = wl.int8_witness()
+        self.w = w = self.make_workload()
         if batch:
             w.batch = batch                   # smaller case for profiler captures
         self.ctx = w.extra["context"]
@@ -348,6 +347,10 @@ class Int8Bench(DecodeBench):
         self.cmax = torch.empty((B, Hq), device=device)
         self.tanh = torch.empty((B, Hq), device=device)
         self._inputs(device)
+
+    def make_workload(self):
+        from kv_cache_decode_ring_gb300 import workloads as wl
+        return wl.int8_witness()
 
     def pool_blocks(self):
         return 0
@@ -376,6 +379,34 @@ class Int8Bench(DecodeBench):
         return {"workload": w.name, "batch": w.batch, "n_q_heads": w.n_q_heads, "n_kv_heads": w.n_kv_heads,
                 "head_dim": w.head_dim, "layout": "contiguous int8 + witnesses", "context": "131072 + step",
                 "l2": "inputs larger than L2: %.2f GB read per step vs 129 MB L2" % (self.units() / 1e9)}
+
+
+class Int8DitherBench(Int8Bench):
+    """Tier B at the INT8 workload's shape: subtractive-dither INT8 codes and scales, no
+    witnesses (Philox key 0x85A308D3243F6A88, layer 0, request IDs 0..7); each step appends
+    one token and runs the decode, which regenerates every dither it reads."""
+
+    kernel = "kvc_decode_attn INT8 Tier B (Philox dither regenerated in the decode + combine)"
+
+    def make_workload(self):
+        from kv_cache_decode_ring_gb300 import workloads as wl
+        return wl.int8_dither()
+
+    def decode(self, q):
+        self.cache.decode(q, self.out)
+
+    def units(self):
+        """Bytes the decode reads: codes and scales of complete blocks, exact tail rows."""
+        w = self.w
+        n = self.ctx + self.done + 1
+        nfull = n // 16 * 16
+        per_head = nfull * 2 * w.head_dim + (nfull // 16) * 8 + (n - nfull) * 4 * w.head_dim
+        return w.batch * w.n_kv_heads * per_head
+
+    def config(self):
+        c = super().config()
+        c["layout"] = "contiguous int8 Tier B (subtractive dither, no witnesses)"
+        return c
 
 
 class Int8GatedBench(Int8Bench):
@@ -697,6 +728,7 @@ class ChunkStoreBench(ChunkBench):
 
 BENCHES = {"full-cache-mha": FullCacheBench, "sliding-window-gqa": SlidingWindowBench, "int8-witness": Int8Bench,
            "bf16-at-int8-shape": Bf16AtInt8ShapeBench, "int8-witness-gated": Int8GatedBench,
+           "int8-dither": Int8DitherBench,
            "full-cache-mha-paged": FullCachePagedBench, "sliding-window-gqa-paged": SlidingWindowPagedBench,
            "prefix-reuse": ChunkBench, "prefix-reuse-w4096": ChunkWindowBench, "prefix-reuse-store": ChunkStoreBench}
 

@@ -59,7 +59,7 @@ typedef void* kvc_stream_t; /* a cudaStream_t */
 /* ---- configuration --------------------------------------------------- */
 enum { KVC_F32 = 0, KVC_BF16 = 1 };
 enum { KVC_CONTIGUOUS = 0, KVC_RING = 1 };
-enum { KVC_QUANT_NONE = 0, KVC_QUANT_INT8 = 1 };
+enum { KVC_QUANT_NONE = 0, KVC_QUANT_INT8 = 1, KVC_QUANT_INT8_DITHER = 2 };
 
 typedef struct {
     int32_t dtype;        /* KVC_F32 or KVC_BF16 */
@@ -67,7 +67,8 @@ typedef struct {
                              ([LOOP] §三, preallocated (B, H, max_S, D) buffers);
                              KVC_RING: slot = position mod W, capacity = W
                              ([LEAN] §3.4 ring buffer, §2.3 lastWindow) */
-    int32_t kv_quant;     /* KVC_QUANT_NONE, or KVC_QUANT_INT8 (bf16 contiguous
+    int32_t kv_quant;     /* KVC_QUANT_NONE, KVC_QUANT_INT8_DITHER (Tier B, see
+                             dither_key_lo below) or KVC_QUANT_INT8 (bf16 contiguous
                              caches with window 0 only; [WITCERT]) */
     int32_t batch;        /* B >= 1 requests */
     int32_t n_q_heads;    /* Hq >= 1 */
@@ -96,6 +97,22 @@ typedef struct {
     int32_t store_slots;  /* device slots for saved prefills (kvc_store_save /
                              kvc_store_load), each holding one request's K, V and
                              positions; 0 = none.  Not with INT8. */
+    int32_t layer_index;  /* KVC_QUANT_INT8_DITHER: the layer in the dither counter */
+    uint32_t dither_key_lo, dither_key_hi;
+                          /* KVC_QUANT_INT8_DITHER (Tier B, [WITCERT] subtractive-
+                             dither paragraph; counter from "SGLang 生产级落地与闭环门控修复"):
+                             the Philox4x32-10 key.  Same shapes and limits as
+                             KVC_QUANT_INT8, without witnesses: element (token t,
+                             channel c) of a block is stored as
+                               code = clamp(rint(x/s + u), -127, 127), read as (code - u) s,
+                             u = r/256 - 1/2 with r a byte of the call
+                               Philox4x32-10(counter = (t, group + 256 tensor,
+                                                       kv_head + 65536 layer_index,
+                                                       request ID), key)
+                             (tensor 0 = keys: group c/16, byte c mod 16; tensor 1 =
+                             values: group c mod 8, byte c/8; byte i = bits 8(i mod 4)..
+                             of word i/4).  The request ID is b unless set by
+                             kvc_set_request_id. */
 } kvc_config;
 
 /* Bytes of the device state buffer for `cfg` (cache rows, positions,
@@ -150,6 +167,16 @@ int kvc_append_rows(kvc_t h, const void* d_k, const void* d_v, int32_t n,
  * be NULL. */
 int kvc_decode_attn(kvc_t h, const void* d_q, void* d_out, float* d_cmax, float* d_tanh,
                     float* d_ct, kvc_stream_t stream);
+/* Tier B (KVC_QUANT_INT8_DITHER) caches regenerate every dither from its counter,
+ * attend over the rows (code - u) s and the exact tail, and return no bound: the
+ * tier's probabilistic certificate needs a per-request failure budget and a
+ * concentration formula that the page does not give.  d_cmax, d_tanh and d_ct
+ * must be NULL (KVC_ERR_ARG otherwise). */
+
+/* Tier B: the request ID of request b in the dither counters, so that a
+ * request's stream does not depend on its batch slot.  Only while request b holds
+ * no rows (KVC_ERR_ARG otherwise, and for other tiers). */
+int kvc_set_request_id(kvc_t h, int32_t b, uint32_t request_id, kvc_stream_t stream);
 
 /* Decode attention that allocates nothing (the pages have no counterpart; this
  * is a deployment variant of kvc_decode_attn).

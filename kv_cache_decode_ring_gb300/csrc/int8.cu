@@ -76,6 +76,9 @@ struct Int8Args {
     float* part_c;
     float* ct;          // nullable: c_t per token [B][Hq][S]
     uint32_t* hdr;
+    const uint32_t* req_id;         // Tier B: request IDs of the dither counters
+    uint32_t layer_ctr;             // Tier B: 65536 * layer
+    uint32_t rk[20];                // Tier B: Philox round keys (k0 + r W0, k1 + r W1), r = 0..9
     int B, Hq, Hkv, d, S, max_splits;
     float scale_log2;   // log2(e)/sqrt(d)
     float inv_sqrt_d_up;
@@ -116,6 +119,45 @@ __device__ __forceinline__ void codes_to_half2(uint32_t u, uint32_t& lo, uint32_
     hi = *reinterpret_cast<const uint32_t*>(&b);
 }
 
+// Tier B: four dither bytes r -> two half2 words of -u = (128 - r)/256, exact in
+// fp16: the byte permute makes 1024 + r, and one fma gives (1024 + r)(-1/256) + 4.5.
+__device__ __forceinline__ void dither_to_half2(uint32_t r, uint32_t& lo, uint32_t& hi) {
+    uint32_t x, y;
+    asm("prmt.b32 %0, %1, 0x64646464, 0x5140;" : "=r"(x) : "r"(r));
+    asm("prmt.b32 %0, %1, 0x64646464, 0x7362;" : "=r"(y) : "r"(r));
+    const __half2 m = __halves2half2(__ushort_as_half(0x9C00), __ushort_as_half(0x9C00));   // -1/256
+    const __half2 c = __halves2half2(__ushort_as_half(0x4480), __ushort_as_half(0x4480));   // 4.5
+    const __half2 a = __hfma2(*reinterpret_cast<const __half2*>(&x), m, c);
+    const __half2 b = __hfma2(*reinterpret_cast<const __half2*>(&y), m, c);
+    lo = *reinterpret_cast<const uint32_t*>(&a);
+    hi = *reinterpret_cast<const uint32_t*>(&b);
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+    return r;
+}
+
+// Philox4x32-10 with the round keys precomputed on the host (kernel parameters, so
+// each key xor folds into the three-input xor of its round).
+// One 32 x 32 -> 64-bit product per multiplier, as the round defines it.
+__device__ __forceinline__ uint4 philox_rk(uint4 c, const uint32_t (&rk)[20]) {
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        uint64_t p0, p1;
+        asm("mul.wide.u32 %0, %1, 0xD2511F53;" : "=l"(p0) : "r"(c.x));
+        asm("mul.wide.u32 %0, %1, 0xCD9E8D57;" : "=l"(p1) : "r"(c.z));
+        c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ rk[2 * r], (uint32_t)p1,
+                       (uint32_t)(p0 >> 32) ^ c.w ^ rk[2 * r + 1], (uint32_t)p0);
+    }
+    return c;
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int w) {
+    return w == 0 ? v.x : w == 1 ? v.y : w == 2 ? v.z : v.w;
+}
+
 // 2^x with the hardware approximation (relative error about 2^-22; 2^-inf = 0)
 __device__ __forceinline__ float ex2(float x) {
     float y;
@@ -129,7 +171,7 @@ __device__ __forceinline__ void split_half(float x, __half& hi, __half& lo) {
     lo = __float2half_rn(x - __half2float(hi));
 }
 
-template <int D, int G>
+template <int D, int G, bool DITHER = false>
 struct I8 {
     static constexpr int KS = D / 16;               // k-steps of the score MMA (= m-tiles of P.V)
     static constexpr int NT = (2 * G + 7) / 8;      // 8-column tiles of (head, hi|lo) columns
@@ -137,7 +179,7 @@ struct I8 {
     static constexpr int KW = D / 16;               // K code words per lane per row (= KS)
     static constexpr int VW = D / 8;                // V code words per lane
     static constexpr int CB = kQBlock * D;          // bytes of one block's codes (K or V)
-    static constexpr int WB = kQBlock * kBands * 2;
+    static constexpr int WB = DITHER ? 0 : kQBlock * kBands * 2;     // witnesses (none in Tier B)
     static constexpr int STAGEB = 2 * CB + WB;
     static constexpr int WARPB = kStages * STAGEB;
     static constexpr int PARTF = G * (D + 3);       // floats of one warp's partial (m, l, c, acc)
@@ -160,9 +202,19 @@ struct I8 {
 
 __device__ __forceinline__ int prow(int n) { return 32 * n + (n >= 4 ? 16 : 0); }
 
-template <int D, int G>
-__global__ void __launch_bounds__(kWarps * 32, D >= 128 ? 3 : 4) int8_decode_kernel(const Int8Args a) {
-    using C = I8<D, G>;
+// DITHER: Tier B ([WITCERT] subtractive dither).  Each lane regenerates, with
+// Philox, exactly the dithers of the codes it holds: its keys are rows g and g + 8
+// of the block over the dims qd (D/4) .. + D/4 - 1, i.e. D/64 whole key groups of
+// 16 channels per row; its values are the channels = g (mod 8) of tokens 4 qd .. + 3,
+// i.e. value group g of 4 tokens.  The -u terms enter both contractions as a second
+// fp16 MMA into the same accumulators ((code - u) s = s code + s (-u)).  No
+// witnesses are read and no bound is formed.
+// Tier B with at most 4 heads per KV head fits 4 CTAs per SM (128 registers, stages
+// without witnesses): more warps to hide the latency of the Philox rounds.
+template <int D, int G, bool DITHER>
+__global__ void __launch_bounds__(kWarps * 32, (D < 128 || (DITHER && G <= 4)) ? 4 : 3)
+int8_decode_kernel(const Int8Args a) {
+    using C = I8<D, G, DITHER>;
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char* sPm = smem + C::OFF_P;                                // [warp][NT] P^T staging
     __half* sQh = reinterpret_cast<__half*>(smem + C::OFF_QH);          // [2G][D]: row 2h hi, 2h + 1 lo
@@ -288,7 +340,7 @@ __global__ void __launch_bounds__(kWarps * 32, D >= 128 ? 3 : 4) int8_decode_ker
             mbar_arrive_expect_tx(&myBar[sg], (uint32_t)C::STAGEB);
             bulk_copy_g2s(st, a.kq + (row0 + p0) * D, C::CB, &myBar[sg]);
             bulk_copy_g2s(st + C::CB, a.vq + (row0 + p0) * D, C::CB, &myBar[sg]);
-            bulk_copy_g2s(st + 2 * C::CB, a.wit + (row0 + p0) * kBands, C::WB, &myBar[sg]);
+            if (!DITHER) bulk_copy_g2s(st + 2 * C::CB, a.wit + (row0 + p0) * kBands, C::WB, &myBar[sg]);
         }
     };
     if (lane == 0) {
@@ -356,6 +408,9 @@ __global__ void __launch_bounds__(kWarps * 32, D >= 128 ? 3 : 4) int8_decode_ker
 
     // ---- per-lane fragments: g = L/4 (MMA group), qd = L%4
     const int g = lane >> 2, qd = lane & 3;
+    // Tier B counter words: KV head + 65536 layer, request ID
+    const uint32_t dc2 = (uint32_t)kvh + a.layer_ctr;
+    const uint32_t dc3 = DITHER ? a.req_id[b] : 0u;
     // score B operand (Q^T): column n = 8 nt + g = (head n/2, hi|lo n%2); k-step s
     // covers the dims qd (D/4) + 4 s .. + 3 in the lane's registers
     uint32_t qb[C::NT][C::KS][2];
@@ -433,6 +488,24 @@ __global__ void __launch_bounds__(kWarps * 32, D >= 128 ? 3 : 4) int8_decode_ker
     #pragma unroll
                 for (int nt = 0; nt < C::NT; ++nt) mma_f16(sacc[nt], a0, a1, a2, a3, qb[nt][s][0], qb[nt][s][1]);
             }
+            if constexpr (DITHER) {
+                // key group qd (D/64) + j of rows g and g + 8: words s = 4 j .. 4 j + 3
+    #pragma unroll
+                for (int j = 0; j < D / 64; ++j) {
+                    const uint32_t grp = (uint32_t)(qd * (D / 64) + j);
+                    const uint4 r0 = philox_rk(make_uint4((uint32_t)(p0 + g), grp, dc2, dc3), a.rk);
+                    const uint4 r1 = philox_rk(make_uint4((uint32_t)(p0 + g + 8), grp, dc2, dc3), a.rk);
+    #pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        uint32_t a0, a1, a2, a3;
+                        dither_to_half2(word_of(r0, w), a0, a2);
+                        dither_to_half2(word_of(r1, w), a1, a3);
+    #pragma unroll
+                        for (int nt = 0; nt < C::NT; ++nt)
+                            mma_f16(sacc[nt], a0, a1, a2, a3, qb[nt][4 * j + w][0], qb[nt][4 * j + w][1]);
+                    }
+                }
+            }
 
             // ---- online softmax of the lane's head over tokens g, g + 8; weights
             // times r_v into the P^T staging as fp16 hi + lo; and the bound
@@ -462,6 +535,7 @@ __global__ void __launch_bounds__(kWarps * 32, D >= 128 ? 3 : 4) int8_decode_ker
                 *reinterpret_cast<__half*>(pt + prow(2 * qd) + 2 * (g + 8)) = h1;
                 *reinterpret_cast<__half*>(pt + prow(2 * qd + 1) + 2 * (g + 8)) = l1;
 
+                if constexpr (DITHER) continue;                  // Tier B: no bound
                 // bound of tokens g, g + 8 for head hq, every operation rounded up
                 const int hq = 4 * nt + qd;
                 const float4* nq = reinterpret_cast<const float4*>(sNQ + min(hq, G - 1) * 20);
@@ -516,6 +590,34 @@ __global__ void __launch_bounds__(kWarps * 32, D >= 128 ? 3 : 4) int8_decode_ker
                 codes_to_half2(vw[2 * mt + 1], a1, a3);       // dim 16 mt + 8 + g
     #pragma unroll
                 for (int nt = 0; nt < C::NT; ++nt) mma_f16(acc[mt][nt], a0, a1, a2, a3, pb[nt].x, pb[nt].y);
+            }
+            if constexpr (DITHER) {
+                // value group g of tokens 4 qd + k: byte f of call k is the dither of dim
+                // 8 f + g; a 4x4 byte transpose makes word f = (tokens 4 qd .. + 3 of dim 8 f + g),
+                // the order of the code word vw[f]
+                uint4 tk[4];
+    #pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    tk[k] = philox_rk(make_uint4((uint32_t)(p0 + 4 * qd + k), 256u + (uint32_t)g, dc2, dc3), a.rk);
+    #pragma unroll
+                for (int w = 0; w < D / 32; ++w) {
+                    const uint32_t x0 = word_of(tk[0], w), x1 = word_of(tk[1], w);
+                    const uint32_t x2 = word_of(tk[2], w), x3 = word_of(tk[3], w);
+                    const uint32_t e01 = prmt(x0, x1, 0x5140), e23 = prmt(x2, x3, 0x5140);
+                    const uint32_t o01 = prmt(x0, x1, 0x7362), o23 = prmt(x2, x3, 0x7362);
+                    const uint32_t f[4] = {prmt(e01, e23, 0x5410), prmt(e01, e23, 0x7632),
+                                           prmt(o01, o23, 0x5410), prmt(o01, o23, 0x7632)};
+    #pragma unroll
+                    for (int hm = 0; hm < 2; ++hm) {          // m-tile mt = 2 w + hm: words f 4 w + 2 hm, + 1
+                        const int mt = 2 * w + hm;
+                        uint32_t a0, a1, a2, a3;
+                        dither_to_half2(f[2 * hm], a0, a2);
+                        dither_to_half2(f[2 * hm + 1], a1, a3);
+    #pragma unroll
+                        for (int nt = 0; nt < C::NT; ++nt)
+                            mma_f16(acc[mt][nt], a0, a1, a2, a3, pb[nt].x, pb[nt].y);
+                    }
+                }
             }
         }
         // this stage and the staging are free once every lane is past its reads
@@ -658,17 +760,17 @@ __global__ void __launch_bounds__(kCombineWarps * 32) int8_combine_kernel(const 
     }
 }
 
-template <int D, int G>
+template <int D, int G, bool DITHER>
 cudaError_t launch_t(const Int8Args& a, cudaStream_t st) {
-    using C = I8<D, G>;
+    using C = I8<D, G, DITHER>;
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(int8_decode_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)C::SMEM);
+        cudaError_t e = cudaFuncSetAttribute(int8_decode_kernel<D, G, DITHER>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    int8_decode_kernel<D, G><<<dim3(a.max_splits, a.Hkv, a.B), kWarps * 32, C::SMEM, st>>>(a);
+    int8_decode_kernel<D, G, DITHER><<<dim3(a.max_splits, a.Hkv, a.B), kWarps * 32, C::SMEM, st>>>(a);
     return cudaGetLastError();
 }
 
@@ -683,7 +785,13 @@ cudaError_t launch_int8_decode(kvc_handle* h, const void* q, void* out, float* c
     a.vq = reinterpret_cast<const int8_t*>(h->state + h->L.vq);
     a.sk = reinterpret_cast<const float*>(h->state + h->L.sk);
     a.sv = reinterpret_cast<const float*>(h->state + h->L.sv);
-    a.wit = reinterpret_cast<const __half*>(h->state + h->L.wit);
+    a.wit = s.dither ? nullptr : reinterpret_cast<const __half*>(h->state + h->L.wit);
+    a.req_id = reinterpret_cast<const uint32_t*>(h->state + h->L.req_id);
+    a.layer_ctr = 65536u * (uint32_t)h->cfg.layer_index;
+    for (int r = 0; r < 10; ++r) {
+        a.rk[2 * r] = h->cfg.dither_key_lo + (uint32_t)r * 0x9E3779B9u;
+        a.rk[2 * r + 1] = h->cfg.dither_key_hi + (uint32_t)r * 0xBB67AE85u;
+    }
     a.ktail = reinterpret_cast<const __nv_bfloat16*>(h->state + h->L.ktail);
     a.vtail = reinterpret_cast<const __nv_bfloat16*>(h->state + h->L.vtail);
     a.xmap = reinterpret_cast<const int32_t*>(h->state + h->L.xmap);
@@ -701,7 +809,7 @@ cudaError_t launch_int8_decode(kvc_handle* h, const void* q, void* out, float* c
     a.inv_sqrt_d_up = std::nextafter((float)(1.0 / std::sqrt((double)s.d)), 1.0f);
     cudaError_t e = cudaErrorInvalidValue;
 #define KVC_CASE(D, G) \
-    if (s.d == D && s.g == G) e = launch_t<D, G>(a, st);
+    if (s.d == D && s.g == G) e = s.dither ? launch_t<D, G, true>(a, st) : launch_t<D, G, false>(a, st);
     KVC_CASE(128, 1) KVC_CASE(128, 2) KVC_CASE(128, 4) KVC_CASE(128, 8)
     KVC_CASE(64, 1) KVC_CASE(64, 2) KVC_CASE(64, 4) KVC_CASE(64, 8)
 #undef KVC_CASE

@@ -125,6 +125,7 @@ using namespace kvc;
 
 extern "C" int kvc_int8_block_risk(kvc_t h, const float* d_ct, float* d_risk, kvc_stream_t stream) {
     if (!h || !d_ct || !d_risk || !h->sh.int8) return KVC_ERR_ARG;
+    if (h->sh.dither) return KVC_ERR_UNSUPPORTED;          // Tier B has no per-token bound
     const Shape& s = h->sh;
     const int nblk = s.S / kQBlock;
     block_risk_kernel<<<dim3((nblk + 7) / 8, s.Hkv, s.B), 256, 0, static_cast<cudaStream_t>(stream)>>>(
@@ -161,6 +162,7 @@ extern "C" int kvc_int8_gate(const float* h_risk, int32_t B, int32_t Hkv, int32_
 extern "C" int kvc_int8_restore(kvc_t h, const int32_t* h_blocks, int32_t n, const void* d_k_full,
                                 const void* d_v_full, kvc_stream_t stream) {
     if (!h || n < 0 || (n > 0 && (!h_blocks || !d_k_full || !d_v_full)) || !h->sh.int8) return KVC_ERR_ARG;
+    if (h->sh.dither) return KVC_ERR_UNSUPPORTED;
     const Shape& s = h->sh;
     const int nblk = s.S / kQBlock;
     // validate everything first: nothing is restored on error

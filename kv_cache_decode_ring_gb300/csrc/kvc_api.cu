@@ -24,7 +24,8 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 bool make_shape(const kvc_config& c, Shape* s) {
     if (c.dtype != KVC_F32 && c.dtype != KVC_BF16) return false;
     if (c.layout != KVC_CONTIGUOUS && c.layout != KVC_RING) return false;
-    if (c.kv_quant != KVC_QUANT_NONE && c.kv_quant != KVC_QUANT_INT8) return false;
+    if (c.kv_quant != KVC_QUANT_NONE && c.kv_quant != KVC_QUANT_INT8 && c.kv_quant != KVC_QUANT_INT8_DITHER)
+        return false;
     if (c.batch < 1 || c.n_q_heads < 1 || c.n_kv_heads < 1) return false;
     if (c.n_q_heads % c.n_kv_heads) return false;
     if (c.head_dim < 2 || c.head_dim > 256 || (c.head_dim & 1)) return false;
@@ -33,10 +34,13 @@ bool make_shape(const kvc_config& c, Shape* s) {
     if (!(c.rope_base >= 0.f) || std::isinf(c.rope_base)) return false;
     const bool ring = c.layout == KVC_RING;
     if (ring && c.window != 0 && c.window != c.capacity) return false;
-    const bool int8 = c.kv_quant == KVC_QUANT_INT8;
+    const bool int8 = c.kv_quant != KVC_QUANT_NONE;
+    const bool dither = c.kv_quant == KVC_QUANT_INT8_DITHER;
+    // the dither counter packs the KV head and the layer into 16 bits each
+    if (dither && (c.layer_index < 0 || c.layer_index > 65535 || c.n_kv_heads > 65536)) return false;
     if (int8 && (c.dtype != KVC_BF16 || ring || c.window != 0 || c.head_dim % kBands || c.capacity % kQBlock))
         return false;
-    if (c.int8_exact_blocks < 0 || (!int8 && c.int8_exact_blocks != 0)) return false;
+    if (c.int8_exact_blocks < 0 || ((!int8 || dither) && c.int8_exact_blocks != 0)) return false;
     if (c.page_pool < 0 || (c.page_pool > 0 && (int8 || c.capacity % kPage))) return false;
     if (c.store_slots < 0 || (c.store_slots > 0 && int8)) return false;
     if (int8) {
@@ -52,6 +56,7 @@ bool make_shape(const kvc_config& c, Shape* s) {
     s->B = c.batch; s->Hq = c.n_q_heads; s->Hkv = c.n_kv_heads; s->g = c.n_q_heads / c.n_kv_heads;
     s->d = c.head_dim; s->S = c.capacity; s->W = ring ? c.capacity : c.window;
     s->P = P; s->ring = ring; s->int8 = int8; s->rope = rope; s->bf16 = c.dtype == KVC_BF16;
+    s->dither = dither;
     s->elem = s->bf16 ? 2 : 4;
     s->max_chunk = c.max_chunk;
     s->xpool = c.int8_exact_blocks;
@@ -93,7 +98,7 @@ Layout make_layout(const Shape& s) {
         L.vq = take(B * Hkv * S * d);
         L.sk = take(B * Hkv * (S / kQBlock) * 4);
         L.sv = take(B * Hkv * (S / kQBlock) * 4);
-        L.wit = take(B * Hkv * S * kBands * 2);
+        if (!s.dither) L.wit = take(B * Hkv * S * kBands * 2);
         L.ktail = take(B * Hkv * kQBlock * d * 2);
         L.vtail = take(B * Hkv * kQBlock * d * 2);
         L.xmap = take(B * Hkv * (S / kQBlock) * 4);
@@ -102,6 +107,7 @@ Layout make_layout(const Shape& s) {
         L.xent = take(B * Hkv * kMaxRestored * 4);
         L.xpool = take((size_t)s.xpool * 2 * kQBlock * d * 2);
     }
+    L.req_id = take(B * 4);
     L.rope = take((size_t)s.P * (d / 2) * 8);
     L.part_ml = take(B * Hq * s.max_splits * 8);
     L.part_acc = take(B * Hq * s.max_splits * d * 4);
@@ -151,14 +157,17 @@ AppendArgs append_args(kvc_handle* h, const void* k, const void* v, int n) {
     else {
         a.kq = at<int8_t>(h, h->L.kq); a.vq = at<int8_t>(h, h->L.vq);
         a.sk = at<float>(h, h->L.sk); a.sv = at<float>(h, h->L.sv);
-        a.wit = at<__half>(h, h->L.wit);
+        a.wit = s.dither ? nullptr : at<__half>(h, h->L.wit);
         a.ktail = at<__nv_bfloat16>(h, h->L.ktail); a.vtail = at<__nv_bfloat16>(h, h->L.vtail);
     }
     a.rope = s.rope ? at<float2>(h, h->L.rope) : nullptr;
     a.hdr = at<uint32_t>(h, h->L.hdr);
     a.table = s.pages ? at<int32_t>(h, h->L.table) : nullptr;
+    a.req_id = at<uint32_t>(h, h->L.req_id);
+    a.key0 = h->cfg.dither_key_lo; a.key1 = h->cfg.dither_key_hi;
+    a.layer_ctr = 65536u * (uint32_t)h->cfg.layer_index;
     a.B = s.B; a.Hkv = s.Hkv; a.d = s.d; a.S = s.S; a.P = s.P;
-    a.ring = s.ring; a.bf16 = s.bf16; a.int8 = s.int8;
+    a.ring = s.ring; a.bf16 = s.bf16; a.int8 = s.int8; a.dither = s.dither;
     return a;
 }
 
@@ -249,6 +258,12 @@ int kvc_create(const kvc_config* cfg, void* d_state, size_t bytes, kvc_stream_t 
             std::swap(h->page_free[i], h->page_free[x % (uint64_t)(i + 1)]);
         }
     }
+    if (e == cudaSuccess) {
+        // request IDs of the dither counters: b until set
+        h->req_id_h.resize(s.B);
+        for (int b = 0; b < s.B; ++b) h->req_id_h[b] = (uint32_t)b;
+        e = cudaMemcpyAsync(h->state + L.req_id, h->req_id_h.data(), (size_t)s.B * 4, cudaMemcpyHostToDevice, st);
+    }
     if (e == cudaSuccess && s.int8) {
         const size_t nb = (size_t)s.B * s.Hkv * (s.S / kQBlock);
         e = cudaMemsetAsync(h->state + L.xmap, 0xff, nb * 4, st);
@@ -331,6 +346,7 @@ int kvc_decode_attn(kvc_t h, const void* d_q, void* d_out, float* d_cmax, float*
         if (h->np[b] < 1) return KVC_ERR_ARG;                 // nothing cached to attend to
     if (s.ring && h->ring_needs_append) return KVC_ERR_ARG;
     cudaStream_t st = S_(stream);
+    if (s.dither && (d_cmax || d_tanh || d_ct)) return KVC_ERR_ARG;      // Tier B returns no bound
     if (s.int8) {
         if (launch_int8_decode(h, d_q, d_out, d_cmax, d_tanh, d_ct, st) != cudaSuccess) return KVC_ERR_CUDA;
         return KVC_OK;
@@ -437,7 +453,9 @@ int kvc_export_bytes(kvc_t h, int32_t which, size_t* bytes) {
     switch (which) {
         case KVC_EXPORT_KQ: case KVC_EXPORT_VQ: *bytes = B * Hkv * S * d; return KVC_OK;
         case KVC_EXPORT_SK: case KVC_EXPORT_SV: *bytes = B * Hkv * (S / kQBlock) * 4; return KVC_OK;
-        case KVC_EXPORT_WITNESS: *bytes = B * Hkv * S * kBands * 2; return KVC_OK;
+        case KVC_EXPORT_WITNESS:
+            if (s.dither) return KVC_ERR_ARG;
+            *bytes = B * Hkv * S * kBands * 2; return KVC_OK;
         case KVC_EXPORT_KTAIL: case KVC_EXPORT_VTAIL: *bytes = B * Hkv * kQBlock * d * 2; return KVC_OK;
         case KVC_EXPORT_XMAP: *bytes = B * Hkv * (S / kQBlock) * 4; return KVC_OK;
         default: return KVC_ERR_ARG;
@@ -507,6 +525,15 @@ int kvc_export(kvc_t h, int32_t which, void* h_dst, size_t bytes, kvc_stream_t s
                 }
         }
     }
+    return KVC_OK;
+}
+
+int kvc_set_request_id(kvc_t h, int32_t b, uint32_t request_id, kvc_stream_t stream) {
+    if (!h || b < 0 || b >= h->sh.B || !h->sh.dither || h->np[b] != 0) return KVC_ERR_ARG;
+    h->req_id_h[b] = request_id;
+    if (cudaMemcpyAsync(h->state + h->L.req_id + (size_t)b * 4, &h->req_id_h[b], 4, cudaMemcpyHostToDevice,
+                        S_(stream)) != cudaSuccess)
+        return KVC_ERR_CUDA;
     return KVC_OK;
 }
 

@@ -49,6 +49,7 @@ struct Layout {
     size_t part_acc;  // float  [B][Hq][max_splits][d]
     size_t part_c;    // float  [B][Hq][max_splits] max_t c_t of the split   (INT8)
     size_t qrot;      // bf16 [2][B][max_chunk][Hq][d] rotated suffix queries, hi and lo terms
+    size_t req_id;    // uint32 [B] request IDs of the dither counters (Tier B)
     size_t store;     // store slots: each K, V [Hkv][S][d] cache dtype, then positions int32 [S]
     size_t store_stride;  // bytes per store slot
     size_t total;
@@ -59,6 +60,7 @@ struct Shape {
     int P;                       // RoPE table rows (0 = no RoPE)
     int elem;                    // bytes per cache element (non-INT8)
     bool ring, int8, rope, bf16;
+    bool dither;                 // INT8 Tier B: subtractive dither, no witnesses
     bool out_bf16;               // attention outputs in bf16 (else fp32)
     int split;                   // keys per split of the decode kernel in use
     int max_splits;
@@ -111,7 +113,10 @@ struct AppendArgs {
     const float2* rope;
     uint32_t* hdr;
     const int32_t* table; // paged caches: the block table (else nullptr)
-    int B, Hkv, d, S, P, ring, bf16, int8;
+    const uint32_t* req_id;   // Tier B: request IDs
+    uint32_t key0, key1;      // Tier B: Philox key
+    uint32_t layer_ctr;       // Tier B: 65536 * layer
+    int B, Hkv, d, S, P, ring, bf16, int8, dither;
 };
 
 // Tensor maps over the whole K and V caches, rows [B*Hkv*S][d] bf16, boxes of 64
@@ -194,6 +199,22 @@ __host__ __device__ __forceinline__ int xv_offset(int d, int t, int x) {
 }
 
 // ---- device helpers -----------------------------------------------------------
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as
+// 1, 2, 3", SC 2011): ten rounds of two 32x32 -> 64-bit products of counter words 0
+// and 2, recombined with words 1 and 3 and the key by xor; the key is bumped by the
+// Weyl constants between rounds.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
+        const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
+        c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    return c;
+}
+
 __device__ __forceinline__ float ld_elem(const void* p, size_t i, int bf16) {
     return bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(p)[i])
                 : static_cast<const float*>(p)[i];
@@ -247,4 +268,6 @@ struct kvc_handle {
     std::vector<int32_t> table_h, page_free;
     // prefix store: rows saved in each store slot (-1 = empty)
     std::vector<int32_t> store_n;
+    // Tier B: host mirror of the request IDs
+    std::vector<uint32_t> req_id_h;
 };

@@ -22,7 +22,7 @@ from . import build as _build
 KVC_OK, KVC_ERR_ARG, KVC_ERR_CAPACITY, KVC_ERR_EVICTED, KVC_ERR_CUDA, KVC_ERR_UNSUPPORTED, KVC_ERR_DEVICE = range(7)
 KVC_F32, KVC_BF16 = 0, 1
 KVC_CONTIGUOUS, KVC_RING = 0, 1
-KVC_QUANT_NONE, KVC_QUANT_INT8 = 0, 1
+KVC_QUANT_NONE, KVC_QUANT_INT8, KVC_QUANT_INT8_DITHER = 0, 1, 2
 (KVC_EXPORT_K, KVC_EXPORT_V, KVC_EXPORT_POSITIONS, KVC_EXPORT_NEXT_POSITION, KVC_EXPORT_KQ, KVC_EXPORT_VQ,
  KVC_EXPORT_SK, KVC_EXPORT_SV, KVC_EXPORT_WITNESS, KVC_EXPORT_KTAIL, KVC_EXPORT_VTAIL, KVC_EXPORT_XMAP,
  KVC_EXPORT_PAGE_TABLE) = range(13)
@@ -43,7 +43,8 @@ class kvc_config(ctypes.Structure):
                 ("head_dim", ctypes.c_int32), ("capacity", ctypes.c_int32), ("window", ctypes.c_int32),
                 ("max_position", ctypes.c_int32), ("rope_base", ctypes.c_float), ("max_chunk", ctypes.c_int32),
                 ("out_dtype", ctypes.c_int32), ("int8_exact_blocks", ctypes.c_int32), ("page_pool", ctypes.c_int32),
-                ("store_slots", ctypes.c_int32)]
+                ("store_slots", ctypes.c_int32), ("layer_index", ctypes.c_int32),
+                ("dither_key_lo", ctypes.c_uint32), ("dither_key_hi", ctypes.c_uint32)]
 
 
 EXPORTED = ["kvc_state_bytes", "kvc_create", "kvc_destroy", "kvc_append", "kvc_append_rows",
@@ -51,7 +52,7 @@ EXPORTED = ["kvc_state_bytes", "kvc_create", "kvc_destroy", "kvc_append", "kvc_a
             "kvc_next_positions", "kvc_device_status", "kvc_prefix_cut", "kvc_strerror",
             "kvc_int8_block_risk", "kvc_int8_gate", "kvc_int8_restore",
             "kvc_pstore_create", "kvc_pstore_destroy", "kvc_pstore_insert", "kvc_pstore_lookup",
-            "kvc_store_save", "kvc_store_load", "kvc_store_load_batch"]
+            "kvc_store_save", "kvc_store_load", "kvc_store_load_batch", "kvc_set_request_id"]
 
 _lock = threading.Lock()
 _lib = None
@@ -97,6 +98,7 @@ def lib() -> ctypes.CDLL:
                 "kvc_store_save": [P, i32, i32, i32, P],
                 "kvc_store_load": [P, i32, i32, i32, P],
                 "kvc_store_load_batch": [P, i32, P, P, P, P],
+                "kvc_set_request_id": [P, i32, ctypes.c_uint32, P],
             }
             for name, args in sig.items():
                 fn = getattr(L, name)
@@ -141,17 +143,21 @@ def kvc_strerror(code: int) -> str:
 
 def make_config(dtype="bf16", layout="contiguous", kv_quant=None, batch=1, n_q_heads=1, n_kv_heads=1,
                 head_dim=128, capacity=1, window=0, max_position=0, rope_base=0.0, max_chunk=0,
-                out_dtype=None, int8_exact_blocks=0, page_pool=0, store_slots=0) -> kvc_config:
+                out_dtype=None, int8_exact_blocks=0, page_pool=0, store_slots=0, layer_index=0,
+                dither_key=(0, 0)) -> kvc_config:
     """``out_dtype``: None (the cache dtype), "f32" or "bf16"; ``int8_exact_blocks``: pool
     entries for blocks the gated fallback restores (INT8 caches); ``page_pool``: pages of 16
     slots for paged K/V storage (0 = each request owns ``capacity`` slots); ``store_slots``:
-    device slots for saved prefills (prefix store)."""
+    device slots for saved prefills (prefix store).  ``kv_quant``: None, "int8" (witness
+    tier) or "int8-dither" (Tier B, with ``layer_index`` and the 64-bit Philox ``dither_key``
+    as (low, high) words)."""
     od = 0 if out_dtype is None else (KVC_F32 + 1 if out_dtype == "f32" else KVC_BF16 + 1)
     return kvc_config(KVC_BF16 if dtype == "bf16" else KVC_F32,
                       KVC_RING if layout == "ring" else KVC_CONTIGUOUS,
-                      KVC_QUANT_INT8 if kv_quant == "int8" else KVC_QUANT_NONE,
+                      {None: KVC_QUANT_NONE, "int8": KVC_QUANT_INT8, "int8-dither": KVC_QUANT_INT8_DITHER}[kv_quant],
                       batch, n_q_heads, n_kv_heads, head_dim, capacity, window, max_position,
-                      float(rope_base), max_chunk, od, int(int8_exact_blocks), int(page_pool), int(store_slots))
+                      float(rope_base), max_chunk, od, int(int8_exact_blocks), int(page_pool), int(store_slots),
+                      int(layer_index), int(dither_key[0]) & 0xFFFFFFFF, int(dither_key[1]) & 0xFFFFFFFF)
 
 
 def kvc_state_bytes(cfg: kvc_config) -> int:
@@ -329,6 +335,10 @@ def kvc_store_load(h, slot: int, b: int, cut: int, stream=None) -> None:
     _check(lib().kvc_store_load(h, int(slot), int(b), int(cut), _stream(stream)), "kvc_store_load")
 
 
+def kvc_set_request_id(h, b: int, request_id: int, stream=None) -> None:
+    _check(lib().kvc_set_request_id(h, int(b), int(request_id) & 0xFFFFFFFF, _stream(stream)), "kvc_set_request_id")
+
+
 def kvc_store_load_batch(h, slots, bs, cuts, stream=None) -> None:
     arr = [np.ascontiguousarray(np.asarray(x, dtype=np.int32).reshape(-1)) for x in (slots, bs, cuts)]
     n = len(arr[0])
@@ -390,7 +400,8 @@ class Cache:
                       page_pool=0, store_slots=0):
         cfg = make_config(w.dtype, w.layout, w.quant, w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.capacity,
                           0 if w.layout == "ring" else w.window, max_position, w.rope_base, max_chunk, out_dtype,
-                          int8_exact_blocks, page_pool, store_slots)
+                          int8_exact_blocks, page_pool, store_slots, w.extra.get("layer", 0),
+                          w.extra.get("dither_key", (0, 0)))
         return cls(cfg, device)
 
     def close(self):
@@ -487,6 +498,9 @@ class Cache:
 
     def device_status(self, stream=None) -> int:
         return kvc_device_status(self.h, stream)
+
+    def set_request_id(self, b, request_id, stream=None):
+        kvc_set_request_id(self.h, b, request_id, stream)
 
     # prefix store
     def store_save(self, slot, b, n, stream=None):

@@ -175,6 +175,15 @@ def int8_witness() -> Workload:
                     "bf16", "int8", 7, extra={"context": 131072, "steps": 16, "outliers": (4, 20.0)})
 
 
+def int8_dither() -> Workload:
+    """Tier B at the INT8 workload's shape: the same tokens, subtractive-dither INT8 codes
+    without witnesses; Philox key (0x243F6A88, 0x85A308D3), layer 0."""
+    w = int8_witness()
+    w.name, w.quant = "int8-dither-bf16", "int8-dither"
+    w.extra.update(dither_key=(0x243F6A88, 0x85A308D3), layer=0)
+    return w
+
+
 def small(name="small", B=2, Hq=4, Hkv=2, d=128, layout="contiguous", capacity=300, window=0,
           rope_base=10000.0, dtype="bf16", quant=None, seed=11, **extra) -> Workload:
     """A parity-sized workload of any shape (several tiles and a ragged tail)."""

@@ -13,6 +13,9 @@ TOL = {"f32": 1e-5, "bf16": 2e-3}
 
 
 def oracle_for(w, **kw) -> DecodeOracle:
+    if w.quant == "int8-dither":
+        kw.setdefault("dither_key", w.extra.get("dither_key", (0, 0)))
+        kw.setdefault("layer", w.extra.get("layer", 0))
     return DecodeOracle(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.layout, w.capacity,
                         0 if w.layout == "ring" else w.window, w.rope_base, w.dtype, w.quant, **kw)
 

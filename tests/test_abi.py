@@ -65,6 +65,11 @@ def test_state_bytes_validation(lib):
         kvc.make_config("bf16", "contiguous", None, 1, 4, 1, 128, 64, page_pool=-1),
         kvc.make_config("bf16", "contiguous", None, 1, 4, 1, 128, 64, store_slots=-1),
         kvc.make_config("bf16", "contiguous", "int8", 1, 4, 1, 128, 64, store_slots=2),   # store of INT8
+        kvc.make_config("bf16", "contiguous", "int8-dither", 1, 4, 1, 128, 64, int8_exact_blocks=4),  # no gate
+        kvc.make_config("bf16", "contiguous", "int8-dither", 1, 4, 1, 128, 64, layer_index=65536),   # 16-bit layer
+        kvc.make_config("bf16", "contiguous", "int8-dither", 1, 4, 1, 128, 64, layer_index=-1),
+        kvc.make_config("bf16", "ring", "int8-dither", 1, 4, 1, 128, 64),
+        kvc.make_config("f32", "contiguous", "int8-dither", 1, 4, 1, 128, 64),
     ]
     for c in bad:
         with pytest.raises(kvc.KvcError) as e:
@@ -178,3 +183,10 @@ def test_pstore_matches_oracle_store(lib, seed):
                 s_ref, c_ref = ref.lookup(ids, scope, sig)
                 assert ps.lookup(ids, scope, sig) == (-1 if s_ref is None else s_ref, c_ref), (ids, scope, sig)
         ps.close()
+
+
+def test_dither_state_has_no_witnesses(lib):
+    w8 = kvc.kvc_state_bytes(kvc.make_config("bf16", "contiguous", "int8", 2, 8, 2, 128, 4096))
+    wd = kvc.kvc_state_bytes(kvc.make_config("bf16", "contiguous", "int8-dither", 2, 8, 2, 128, 4096,
+                                             layer_index=7, dither_key=(1, 2)))
+    assert w8 - wd >= 2 * 2 * 4096 * 16 * 2 - 4096                  # 32 B per token and head fewer
