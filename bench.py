@@ -540,7 +540,7 @@ class ChunkBench(DecodeBench):
     (RoPE 10000), cuts uniform in [0, 8191] (seed 7).  A step trims every request to its cut and
     runs kvc_chunk_attn on a 512-token suffix (append, rotate, causal tcgen05 attention)."""
 
-    kernel = "kvc_chunk_attn (suffix append + query rotation + tcgen05 causal attention)"
+    kernel = "kvc_chunk_attn (suffix append + tcgen05 causal attention with the query rotation fused)"
     metric = "chunked suffix attention FLOP/s (TFLOP/s, % of bf16 tensor peak) at 1 GB300"
     unit = "TFLOP/s"
     bound = "tensor"
@@ -582,7 +582,7 @@ class ChunkBench(DecodeBench):
         return kvc.Cache.from_workload(w, max_chunk=self.n, device=device)
 
     def launches_per_step(self):
-        return 5                                   # trim, append rows, advance, rotate q, attention
+        return 4                                   # trim, append rows, advance, attention
 
     def traffic_basis(self, flops):
         w = self.w                                 # the K/V rows a step's attention reads
@@ -673,7 +673,7 @@ class ChunkStoreBench(ChunkBench):
         return kvc.Cache.from_workload(w, max_chunk=self.n, device=device, store_slots=w.batch)
 
     def launches_per_step(self):
-        return 5                                   # batched load, append rows, advance, rotate q, attention
+        return 4                                   # batched load, append rows, advance, attention
 
     def reuse(self, ev=False):
         import torch

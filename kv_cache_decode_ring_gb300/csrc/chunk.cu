@@ -11,8 +11,13 @@
 // This is a dense contraction, so it runs on the 5th-generation tensor cores:
 //  * CTA = 128 query rows of one query head (4 warps, thread = row); tiles of
 //    64 keys;
-//  * Q, K, V tiles arrive by TMA (128-byte swizzle); four K and four V stages,
-//    each refilled as soon as the MMA that read it completes;
+//  * K and V tiles arrive by TMA (128-byte swizzle), each stage refilled as soon
+//    as the MMA that read it completes; each softmax warp rotates its rows' query
+//    half from global memory (fp32 rule of the cache keys, times log2(e)/sqrt(d))
+//    and stores it into tensor memory as bf16 hi and lo;
+//  * CTAs are taken longest first (a host-sorted table of (request, query tile)
+//    items in the kernel parameters), the query heads of one item adjacent so that
+//    heads sharing a KV head read its tiles from L2;
 //  * S = Q K^T and O += P V are tcgen05.mma (bf16 in, fp32 accumulate) issued
 //    by one thread into tensor memory (two 64-column S buffers, 128-column O);
 //  * software pipeline: S of tile j + 1 is issued before the softmax of tile j
@@ -33,8 +38,11 @@
 // word, skips the remaining work and still frees its tensor memory.
 #include <cuda.h>
 
+#include <algorithm>
 #include <cmath>
 #include <mutex>
+#include <utility>
+#include <vector>
 
 #include "async_copy.h"
 #include "kvc_internal.h"
@@ -55,13 +63,13 @@ constexpr int kHalfB = kTileB / 2;
 // Operands that are not exact bf16 (the rotated query and the softmax weights)
 // enter the MMAs as two bf16 terms, hi = bf16(x) and lo = bf16(x - hi), both
 // accumulated in fp32: about 16 significant bits instead of 8.
-constexpr int OFF_Q = 0;                              // Q hi; after the copy into tensor memory:
-                                                      // row-maximum exchange, then row sums
-constexpr int OFF_QLO = OFF_Q + kTileB;               // Q lo
-constexpr int OFF_K = OFF_QLO + kTileB;               // kKStages K tiles
+constexpr int OFF_X = 0;                              // row-maximum exchange [2][2][kBM] floats
+constexpr int OFF_L = OFF_X + 4 * kBM * 4;            // row sums of the two halves [2][kBM]
+constexpr int OFF_K = 4096;                           // kKStages K tiles (1024-aligned)
 constexpr int OFF_V = OFF_K + kKStages * kTileB;      // kVStages V tiles
-constexpr int OFF_BAR = OFF_V + kVStages * kTileB;    // q, k[3], v[2], s[2], o[2], p[2], done, q in tmem
-constexpr int kBars = 1 + kKStages + kVStages + 2 + 2 + 2 + 1 + 1;
+constexpr int OFF_BAR = OFF_V + kVStages * kTileB;    // k[3], v[2], s[2], o[2], p[2], done, q in tmem
+constexpr int kBars = kKStages + kVStages + 2 + 2 + 2 + 1 + 1;
+constexpr int kMaxItems = 2048;                       // (request, query tile) items in the order table
 constexpr int OFF_MISC = OFF_BAR + 8 * kBars;         // tensor memory base, abort flag
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory per block");
@@ -76,10 +84,15 @@ constexpr uint32_t kColO = 256, kColQ = 384, kColQlo = 448;
 
 struct ChunkArgs {
     const int32_t* next_pos;   // after the append: cut + n
+    const __nv_bfloat16* q;    // [B][n][Hq][d], not rotated
+    const float2* rope;        // nullptr = no RoPE
     void* out;                 // [B][n][Hq][d]
     uint32_t* hdr;
     int B, Hq, Hkv, g, S, W, n, out_bf16;
+    int tiles;                 // query tiles per request
     float scale_log2;
+    int n_items;               // 0: natural order; else items[] = (request << 16 | tile), longest first
+    uint32_t items[kMaxItems];
 };
 
 // ---- tcgen05 wrappers -------------------------------------------------------
@@ -197,20 +210,16 @@ __device__ __forceinline__ bool pair_sync_or(int id, bool pred) {
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    chunk_attn_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmQlo,
-                      const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                      const ChunkArgs a) {
+    chunk_attn_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                      const __grid_constant__ ChunkArgs a) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    unsigned char* sQ = smem + OFF_Q;
-    unsigned char* sQlo = smem + OFF_QLO;
     unsigned char* sK = smem + OFF_K;
     unsigned char* sV = smem + OFF_V;
-    float* xmax = reinterpret_cast<float*>(smem + OFF_Q);   // [parity][half][row], after Q left
+    float* xmax = reinterpret_cast<float*>(smem + OFF_X);   // [parity][half][row]
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
-    uint64_t* bq = bar;                      // Q landed
-    uint64_t* bk = bar + 1;                  // [stage] K tile landed
+    uint64_t* bk = bar;                      // [stage] K tile landed
     uint64_t* bv = bk + kKStages;            // [stage] V tile landed
     uint64_t* bs = bv + kVStages;            // [buffer] S = Q K^T complete
     uint64_t* bo = bs + 2;                   // [buffer] O += P V complete
@@ -221,7 +230,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int b = blockIdx.z, hq = blockIdx.y, i0 = blockIdx.x * kBM;
+    // this CTA's (request, query tile, query head)
+    int b, tile;
+    const int hq = blockIdx.x % a.Hq, item = blockIdx.x / a.Hq;
+    if (a.n_items > 0) { b = (int)(a.items[item] >> 16); tile = (int)(a.items[item] & 0xFFFFu); }
+    else { b = item / a.tiles; tile = item % a.tiles; }
+    const int i0 = tile * kBM;
     const int kvh = hq / a.g;
     const int np = a.next_pos[b];
     const int cut = np - a.n;
@@ -304,16 +318,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             // copies issued and awaited so far (an abort drains the rest before exit)
             int k_issued = 0, v_issued = 0, k_waited = 0, v_waited = 0;
-            bool q_waited = false;
-            mbar_arrive_expect_tx(bq, 2 * kTileB);
-            tma_load_3d(sQ, &tmQ, 0, hq, b * a.n + i0, bq);
-            tma_load_3d(sQ + kHalfB, &tmQ, 64, hq, b * a.n + i0, bq);
-            tma_load_3d(sQlo, &tmQlo, 0, hq, b * a.n + i0, bq);
-            tma_load_3d(sQlo + kHalfB, &tmQlo, 64, hq, b * a.n + i0, bq);
             for (int j = 0; j < kKStages && j < ntiles; ++j) { load_k(j); k_issued = j + 1; }
             for (int j = 0; j < kVStages && j < ntiles; ++j) { load_v(j); v_issued = j + 1; }
-            ok = q_waited = mbar_wait(bq, 0);
-            ok = ok && mbar_wait(bqt, 0);            // the softmax warps moved Q into tensor memory
+            ok = mbar_wait(bqt, 0);                  // the softmax warps stored Q into tensor memory
             for (int j = 0; j < 2 && j < ntiles && ok; ++j) {
                 ok = mbar_wait(&bk[j], 0);
                 if (ok) { k_waited = j + 1; fence_after(); issue_s(j); }
@@ -349,7 +356,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 *abort_flag = 1;
                 atomicOr(a.hdr, kErrWait);
                 // let every copy still in flight land before the CTA can exit
-                if (!q_waited) mbar_wait(bq, 0);
                 for (int t = k_waited; t < k_issued; ++t) mbar_wait(&bk[t % kKStages], (uint32_t)((t / kKStages) & 1));
                 for (int t = v_waited; t < v_issued; ++t) mbar_wait(&bv[t % kVStages], (uint32_t)((t / kVStages) & 1));
             }
@@ -369,29 +375,53 @@ __global__ void __launch_bounds__(kThreads, 1)
         float m_ref = -INFINITY, l = 0.f;
         bool fail = false;
         {
-            // this warp's half of its rows' query (dims 64 hf .. + 63, hi and lo) from the
-            // swizzled shared-memory tile into tensor memory, bf16 pairs along columns
-            const bool w = __all_sync(0xffffffffu, mbar_wait(bq, 0));
-            if (w) {
-                uint32_t qh[32], ql[32];
+            // this warp's half of its row's query (dims 64 hf .. + 63): rotated at the row's
+            // position in fp32, times log2(e)/sqrt(d), split into bf16 hi = bf16(y) and
+            // lo = bf16(y - hi), stored into tensor memory as bf16 pairs along columns
+            uint32_t qh[32], ql[32];
+            if (row_valid) {
+                // every load first (one round trip): 8 x 16 B of the query half, 16 x 16 B
+                // of its {cos, sin} pairs
+                const uint4* qrow = reinterpret_cast<const uint4*>(
+                    a.q + (((size_t)b * a.n + i0 + row) * a.Hq + hq) * kD + 64 * hf);
+                uint4 qv[8];
+                float4 rv[16];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) qv[c] = __ldg(qrow + c);
+                if (a.rope) {
+                    const float4* rp = reinterpret_cast<const float4*>(a.rope + (size_t)p * (kD / 2) + 32 * hf);
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) rv[c] = __ldg(rp + c);
+                }
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
-                    const int off = hf * kHalfB + row * 128 + ((c ^ (row & 7)) * 16);
-                    const uint4 u = *reinterpret_cast<const uint4*>(sQ + off);
-                    const uint4 v = *reinterpret_cast<const uint4*>(sQlo + off);
-                    qh[4 * c] = u.x; qh[4 * c + 1] = u.y; qh[4 * c + 2] = u.z; qh[4 * c + 3] = u.w;
-                    ql[4 * c] = v.x; ql[4 * c + 1] = v.y; ql[4 * c + 2] = v.z; ql[4 * c + 3] = v.w;
+                    const uint32_t wq[4] = {qv[c].x, qv[c].y, qv[c].z, qv[c].w};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const __nv_bfloat162 x2 = *reinterpret_cast<const __nv_bfloat162*>(&wq[k]);
+                        const float x0 = __low2float(x2), x1 = __high2float(x2);
+                        float y0 = x0, y1 = x1;
+                        if (a.rope) {
+                            const float4 r4 = rv[(4 * c + k) >> 1];
+                            rope_pair(x0, x1, ((4 * c + k) & 1) ? make_float2(r4.z, r4.w) : make_float2(r4.x, r4.y),
+                                      y0, y1);
+                        }
+                        y0 = __fmul_rn(y0, a.scale_log2);
+                        y1 = __fmul_rn(y1, a.scale_log2);
+                        const __nv_bfloat162 h2 = __floats2bfloat162_rn(y0, y1);
+                        qh[4 * c + k] = *reinterpret_cast<const uint32_t*>(&h2);
+                        ql[4 * c + k] = pack_bf16(__fsub_rn(y0, __low2float(h2)), __fsub_rn(y1, __high2float(h2)));
+                    }
                 }
-                tmem_st32u(tmem + kColQ + 32 * hf + lane_off, qh);
-                tmem_st32u(tmem + kColQlo + 32 * hf + lane_off, ql);
-                fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bqt);
             } else {
-                fail = true;                      // the producer gives up waiting for bqt
+#pragma unroll
+                for (int e = 0; e < 32; ++e) { qh[e] = 0u; ql[e] = 0u; }
             }
-            // the Q area becomes the exchange buffer once every warp has copied its part
-            fail = fail || !__all_sync(0xffffffffu, mbar_wait(bqt, 0));
+            tmem_st32u(tmem + kColQ + 32 * hf + lane_off, qh);
+            tmem_st32u(tmem + kColQlo + 32 * hf + lane_off, ql);
+            fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bqt);
         }
         for (int j = 0; j < ntiles; ++j) {
             // (1) S_j complete; this warp's 64 scores of the row
@@ -485,8 +515,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) atomicOr(a.hdr, kErrWait);
             *abort_flag = 1;
         }
-        // partial row sums of the two halves meet in the (idle) Q lo area
-        reinterpret_cast<float*>(smem + OFF_QLO)[hf * kBM + row] = l;
+        // partial row sums of the two halves
+        reinterpret_cast<float*>(smem + OFF_L)[hf * kBM + row] = l;
     }
     __syncthreads();
     const bool aborted = *abort_flag != 0;
@@ -496,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = 32 * lg + lane;
         const uint32_t lane_off = (uint32_t)(32 * lg) << 16;
         fence_after();
-        const float* lsum = reinterpret_cast<const float*>(smem + OFF_QLO);
+        const float* lsum = reinterpret_cast<const float*>(smem + OFF_L);
         const float L = lsum[row] + lsum[kBM + row];
         const float inv = L > 0.f ? 1.f / L : 0.f;
         const size_t orow = (((size_t)b * a.n + i0 + row) * a.Hq + hq) * kD + 64 * hf;
@@ -538,31 +568,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-// Query rows rotated at their positions (fp32 rule of the cache keys), times
-// log2(e)/sqrt(d) (so that Q K^T is the logit in the log2 domain), split into
-// bf16 hi = bf16(y) and lo = bf16(y - hi).
-__global__ void rope_q_kernel(const __nv_bfloat16* q, __nv_bfloat16* qr, __nv_bfloat16* qlo,
-                              const int32_t* next_pos, const float2* rope, int n, int Hq, int d, float scale) {
-    const int b = blockIdx.y;
-    const int cut = next_pos[b] - n;
-    const size_t per_b = (size_t)n * Hq * (d / 2);
-    for (size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x; idx < per_b; idx += (size_t)gridDim.x * blockDim.x) {
-        const int i = (int)(idx / ((size_t)Hq * (d / 2)));
-        const int pr = (int)(idx % (d / 2));
-        const size_t off = (size_t)b * n * Hq * d + idx * 2;
-        const float x0 = __bfloat162float(q[off]), x1 = __bfloat162float(q[off + 1]);
-        float y0 = x0, y1 = x1;
-        if (rope) rope_pair(x0, x1, rope[(size_t)(cut + i) * (d / 2) + pr], y0, y1);
-        y0 *= scale;
-        y1 *= scale;
-        const __nv_bfloat16 h0 = __float2bfloat16_rn(y0), h1 = __float2bfloat16_rn(y1);
-        qr[off] = h0;
-        qr[off + 1] = h1;
-        qlo[off] = __float2bfloat16_rn(y0 - __bfloat162float(h0));
-        qlo[off + 1] = __float2bfloat16_rn(y1 - __bfloat162float(h1));
-    }
-}
-
 // ---- tensor maps -----------------------------------------------------------
 using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -597,38 +602,49 @@ bool chunk_supported(const Shape& s) { return s.bf16 && !s.int8 && !s.ring && s.
 
 cudaError_t launch_chunk(kvc_handle* h, const void* q, void* out, int n, cudaStream_t st) {
     const Shape& s = h->sh;
-    __nv_bfloat16* qr = reinterpret_cast<__nv_bfloat16*>(h->state + h->L.qrot);
-    __nv_bfloat16* qlo = qr + (size_t)s.B * s.max_chunk * s.Hq * s.d;
-    const int32_t* np = reinterpret_cast<const int32_t*>(h->state + h->L.next_pos);
-    const float2* rope = s.rope ? reinterpret_cast<const float2*>(h->state + h->L.rope) : nullptr;
-    const float scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)s.d));
-    rope_q_kernel<<<dim3(128, s.B), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(q), qr, qlo, np, rope, n, s.Hq,
-                                                  s.d, scale_log2);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-
-    CUtensorMap tq, tql, tk, tv;
-    const cuuint64_t qdims[3] = {(cuuint64_t)s.d, (cuuint64_t)s.Hq, (cuuint64_t)s.B * n};
-    const cuuint64_t qstr[2] = {(cuuint64_t)s.d * 2, (cuuint64_t)s.Hq * s.d * 2};
-    const cuuint32_t qbox[3] = {64, 1, kBM};
+    CUtensorMap tk, tv;
     const cuuint64_t kdims[2] = {(cuuint64_t)s.d, (cuuint64_t)s.B * s.Hkv * s.S};
     const cuuint64_t kstr[1] = {(cuuint64_t)s.d * 2};
     const cuuint32_t kbox[2] = {64, kBN};
-    if (!make_tensor_map_bf16(&tq, qr, 3, qdims, qstr, qbox) || !make_tensor_map_bf16(&tql, qlo, 3, qdims, qstr, qbox) ||
-        !make_tensor_map_bf16(&tk, h->state + h->L.k, 2, kdims, kstr, kbox) ||
+    if (!make_tensor_map_bf16(&tk, h->state + h->L.k, 2, kdims, kstr, kbox) ||
         !make_tensor_map_bf16(&tv, h->state + h->L.v, 2, kdims, kstr, kbox))
         return cudaErrorInvalidValue;
     static bool attr = false;
     if (!attr) {
-        e = cudaFuncSetAttribute(chunk_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        cudaError_t e = cudaFuncSetAttribute(chunk_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    ChunkArgs a{};
-    a.next_pos = np; a.out = out; a.hdr = reinterpret_cast<uint32_t*>(h->state + h->L.hdr);
+    // ChunkArgs carries the order table: it lives in static storage, not on the stack
+    static thread_local ChunkArgs a;
+    a = ChunkArgs{};
+    a.next_pos = reinterpret_cast<const int32_t*>(h->state + h->L.next_pos);
+    a.q = static_cast<const __nv_bfloat16*>(q);
+    a.rope = s.rope ? reinterpret_cast<const float2*>(h->state + h->L.rope) : nullptr;
+    a.out = out; a.hdr = reinterpret_cast<uint32_t*>(h->state + h->L.hdr);
     a.B = s.B; a.Hq = s.Hq; a.Hkv = s.Hkv; a.g = s.g; a.S = s.S; a.W = s.W; a.n = n; a.out_bf16 = s.out_bf16;
+    a.tiles = (n + kBM - 1) / kBM;
     a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)s.d));
-    chunk_attn_kernel<<<dim3((n + kBM - 1) / kBM, s.Hq, s.B), kThreads, SMEM_BYTES, st>>>(tq, tql, tk, tv, a);
+    // longest first: a (request, tile) item's work is its number of key tiles, from the
+    // host mirror of next_position (already advanced past the appended suffix)
+    const int items = s.B * a.tiles;
+    if (items <= kMaxItems && s.B <= 65536 && a.tiles <= 65536) {
+        std::vector<std::pair<int, uint32_t>> w(items);
+        for (int b = 0; b < s.B; ++b)
+            for (int t = 0; t < a.tiles; ++t) {
+                const int cut = h->np[b] - n, i0 = t * kBM, rows = std::min(kBM, n - i0);
+                const int p_first = cut + i0, p_last = p_first + rows - 1;
+                const int lo = s.W > 0 ? std::max(0, p_first - s.W + 1) : 0;
+                w[b * a.tiles + t] = {-((p_last + 1 - lo + kBN - 1) / kBN), ((uint32_t)b << 16) | (uint32_t)t};
+            }
+        std::stable_sort(w.begin(), w.end(),
+                         [](const std::pair<int, uint32_t>& x, const std::pair<int, uint32_t>& y) {
+                             return x.first < y.first;
+                         });
+        for (int i = 0; i < items; ++i) a.items[i] = w[i].second;
+        a.n_items = items;
+    }
+    chunk_attn_kernel<<<dim3(items * s.Hq), kThreads, SMEM_BYTES, st>>>(tk, tv, a);
     return cudaGetLastError();
 }
 

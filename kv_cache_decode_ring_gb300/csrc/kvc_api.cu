@@ -112,7 +112,6 @@ Layout make_layout(const Shape& s) {
     L.part_ml = take(B * Hq * s.max_splits * 8);
     L.part_acc = take(B * Hq * s.max_splits * d * 4);
     if (s.int8) L.part_c = take(B * Hq * s.max_splits * 4);
-    if (s.max_chunk > 0) L.qrot = take(2 * B * (size_t)s.max_chunk * Hq * d * 2);   // hi and lo terms
     if (s.store_slots > 0) {
         L.store_stride = align256(2 * Hkv * S * d * s.elem + S * 4);
         L.store = take((size_t)s.store_slots * L.store_stride);

@@ -48,7 +48,6 @@ struct Layout {
     size_t part_ml;   // float2 [B][Hq][max_splits] {m (log2 domain), l}
     size_t part_acc;  // float  [B][Hq][max_splits][d]
     size_t part_c;    // float  [B][Hq][max_splits] max_t c_t of the split   (INT8)
-    size_t qrot;      // bf16 [2][B][max_chunk][Hq][d] rotated suffix queries, hi and lo terms
     size_t req_id;    // uint32 [B] request IDs of the dither counters (Tier B)
     size_t store;     // store slots: each K, V [Hkv][S][d] cache dtype, then positions int32 [S]
     size_t store_stride;  // bytes per store slot
