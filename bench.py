@@ -45,9 +45,10 @@ CSRC = os.path.join(ROOT, "kv_cache_decode_ring_gb300", "csrc")
 TRAFFIC_PER_BYTE = {
     "full-cache-mha": ("decode_fast.cu", "acb55fd33938d9cc", (268701696 + 4940800) / 268632064),
     "sliding-window-gqa": ("decode_gqa.cu", "08f9c44bf585eae3", (268104192 + 4806400) / 268148736),
-    "int8-witness": ("int8.cu", "6f50d90ec52b7db8", (302877952 + 4520448) / 302551040),
+    "int8-witness": ("int8.cu", "a08d5ed4f1f0e494", (302863360 + 4176640) / 302551040),
     "bf16-at-int8-shape": ("decode_gqa.cu", "08f9c44bf585eae3", (537022720 + 6739968) / 536907776),
-    "prefix-reuse": ("chunk.cu", "424df5ecd9751daa", (39883008 + 86784) / 22773760),
+    "prefix-reuse": ("chunk.cu", "608963104f909744", (31902208 + 42240) / 22773760),
+    "int8-dither": ("int8.cu", "a08d5ed4f1f0e494", (269329664 + 4647680) / 268996608),
 }
 
 
