@@ -154,7 +154,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Combi
 }  // namespace
 
 cudaError_t launch_decode(const DecodeArgs& a, const CombineArgs& c, bool fast, const KvMaps* maps, cudaStream_t st) {
-    if (a.split == kGqaSplit && gqa_decode_supported(a.d, a.g)) {
+    if (a.gqa) {
         if (!maps) return cudaErrorInvalidValue;
         cudaError_t e = launch_decode_gqa(a, *maps, st);
         if (e != cudaSuccess) return e;

@@ -4,8 +4,9 @@
 // Same mathematics as decode.cu ([LOOP] §三 step; [LEAN] §2.1 window mask), with
 // the per-split partials (m, l, acc) merged by the combine kernel.
 //
-// CTA = 4 warps = a split of 512 keys.  A warp streams its 8 tiles of 16 keys
-// through three shared-memory stages: a tile is d/64 tensor copies of 64 dims x
+// CTA = 4 warps = a split of 1024 keys (2048 for caches whose requests may attend
+// to 16384 keys or more).  A warp streams its 16 (32) tiles of 16 keys through
+// three shared-memory stages: a tile is d/64 tensor copies of 64 dims x
 // 16 rows from K and as many from V, written with the 128-byte swizzle (16-byte
 // chunk c of row r at c ^ (r mod 8)), so the 8 row addresses of an ldmatrix fall
 // into 8 different bank groups.  Rows past the window's last key are copied too
@@ -32,11 +33,9 @@ namespace {
 
 constexpr int kWarps = 4;
 constexpr int kTileKeys = 16;                            // keys per stage
-constexpr int kTilesPerWarp = 8;
 constexpr int kStages = 3;                               // per warp
 constexpr float kLazyMax = 8.f;                          // log2-domain headroom of the reference maximum
-constexpr int kSplit = kWarps * kTilesPerWarp * kTileKeys;   // 512 keys per CTA
-static_assert(kSplit == kGqaSplit, "split shape");
+static_assert(kGqaSplit % (kWarps * kTileKeys) == 0 && kGqaSplitLong % (kWarps * kTileKeys) == 0, "split shape");
 
 // 2^x with the hardware approximation (relative error about 2^-22; 2^-inf = 0)
 __device__ __forceinline__ float ex2(float x) {
@@ -111,6 +110,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     key_range(len, a.S, a.W, a.ring, lo, hi);
     // a paged cache aligns its tiles to pages (keys before the window are masked)
     const int lo_t = a.table ? (lo & ~(kPage - 1)) : lo;
+    const int kSplit = a.split;                          // keys per CTA
+    const int tpw = kSplit / (kWarps * kTileKeys);       // tiles per warp
     const int nsplit = (hi - lo_t + kSplit - 1) / kSplit;
     if (split >= nsplit) return;
 
@@ -197,7 +198,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
 #pragma unroll
             for (int e = 0; e < 4; ++e) acc[mt][nt][e] = 0.f;
 
-    for (int i = 0; i < kTilesPerWarp; ++i) {
+    for (int i = 0; i < tpw; ++i) {
         const int nk = tile_nk(i);
         if (nk == 0) break;                       // later tiles of this warp are empty too
         const int kmin = lo - tile_k0(i);         // keys of the tile before the window
@@ -210,7 +211,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
             // (if issued) land before the stages are reused for the partial
             if (lane == 0) atomicOr(a.hdr, kErrWait);
             mbar_wait(&myBar[sg], par);
-            for (int j = i + 1; j < i + kStages && j < kTilesPerWarp; ++j)
+            for (int j = i + 1; j < i + kStages && j < tpw; ++j)
                 if (tile_nk(j) > 0) mbar_wait(&myBar[j % kStages], (uint32_t)((j / kStages) & 1));
             break;
         }
@@ -283,7 +284,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
         // this stage and the staging are free once every lane is past its reads
         __syncwarp();
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        if (i + kStages < kTilesPerWarp) issue(i + kStages);
+        if (i + kStages < tpw) issue(i + kStages);
     }
 
     // ---- this warp's partial into its own stage buffers (every issued tile was

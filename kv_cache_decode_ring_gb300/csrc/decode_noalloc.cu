@@ -82,13 +82,13 @@ extern "C" int kvc_decode_attn_noalloc(kvc_t h, const void* d_q, void* d_out, kv
     a.hdr = reinterpret_cast<uint32_t*>(h->state + h->L.hdr);
     a.table = s.pages ? reinterpret_cast<const int32_t*>(h->state + h->L.table) : nullptr;
     a.B = s.B; a.Hq = s.Hq; a.Hkv = s.Hkv; a.g = s.g; a.d = s.d; a.S = s.S; a.W = s.W;
-    a.max_splits = s.max_splits; a.split = s.split; a.ring = s.ring; a.bf16 = s.bf16;
+    a.max_splits = s.max_splits; a.split = s.split; a.gqa = s.gqa; a.ring = s.ring; a.bf16 = s.bf16;
     a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)s.d));
     CombineArgs c{};
     c.part_ml = a.part_ml; c.part_acc = a.part_acc; c.next_pos = a.next_pos; c.out = d_out;
     c.B = s.B; c.Hq = s.Hq; c.d = s.d; c.S = s.S; c.W = s.W; c.max_splits = s.max_splits;
     c.split = s.split; c.ring = s.ring; c.bf16 = s.out_bf16;
-    c.align_lo = s.pages > 0 && s.split == kGqaSplit;
+    c.align_lo = s.pages > 0 && s.gqa;
     const bool fast = s.split == kFastSplit && fast_decode_supported(a);
     if (launch_decode(a, c, fast, h->has_kv_maps ? &h->kv_maps : nullptr, static_cast<cudaStream_t>(stream)) !=
         cudaSuccess)

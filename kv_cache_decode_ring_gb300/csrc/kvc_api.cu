@@ -67,8 +67,9 @@ bool make_shape(const kvc_config& c, Shape* s) {
     if (s->bf16 && !int8 && (s->d == 64 || s->d == 128) && s->g <= 8) s->split = kFastSplit;
     // (its tensor copies address cache rows with signed 32-bit coordinates)
     const long long rows = s->pages ? (long long)s->pages * s->Hkv * kPage : (long long)s->B * s->Hkv * s->S;
-    if (s->bf16 && !int8 && gqa_decode_supported(s->d, s->g) && rows < (1ll << 31)) s->split = kGqaSplit;
     const long long keys = (s->W > 0 && s->W < s->S) ? s->W : s->S;
+    s->gqa = s->bf16 && !int8 && gqa_decode_supported(s->d, s->g) && rows < (1ll << 31);
+    if (s->gqa) s->split = keys >= kGqaLongKeys ? kGqaSplitLong : kGqaSplit;
     // a paged cache may start its splits up to one page before the window
     s->max_splits = (int)((keys + s->split - 1) / s->split) + (s->pages > 0 ? 1 : 0);
     if (int8) {
@@ -223,7 +224,7 @@ int kvc_create(const kvc_config* cfg, void* d_state, size_t bytes, kvc_stream_t 
     h->store_n.assign(s.store_slots, -1);
     h->ring_needs_append = false;
     h->has_kv_maps = false;
-    if (s.split == kGqaSplit) {
+    if (s.gqa) {
         // the GQA decode reads 16-row tiles of the K and V caches by tensor copy
         const cuuint64_t dims[2] = {(cuuint64_t)s.d,
                                     s.pages ? (cuuint64_t)s.pages * s.Hkv * kPage : (cuuint64_t)s.B * s.Hkv * s.S};
@@ -360,13 +361,13 @@ int kvc_decode_attn(kvc_t h, const void* d_q, void* d_out, float* d_cmax, float*
     a.hdr = at<uint32_t>(h, h->L.hdr);
     a.table = s.pages ? at<int32_t>(h, h->L.table) : nullptr;
     a.B = s.B; a.Hq = s.Hq; a.Hkv = s.Hkv; a.g = s.g; a.d = s.d; a.S = s.S; a.W = s.W;
-    a.max_splits = s.max_splits; a.split = s.split; a.ring = s.ring; a.bf16 = s.bf16;
+    a.max_splits = s.max_splits; a.split = s.split; a.gqa = s.gqa; a.ring = s.ring; a.bf16 = s.bf16;
     a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)s.d));
     CombineArgs c{};
     c.part_ml = a.part_ml; c.part_acc = a.part_acc; c.next_pos = a.next_pos; c.out = d_out;
     c.B = s.B; c.Hq = s.Hq; c.d = s.d; c.S = s.S; c.W = s.W; c.max_splits = s.max_splits;
     c.split = s.split; c.ring = s.ring; c.bf16 = s.out_bf16;
-    c.align_lo = s.pages > 0 && s.split == kGqaSplit;
+    c.align_lo = s.pages > 0 && s.gqa;
     const bool fast = s.split == kFastSplit && fast_decode_supported(a);
     if (launch_decode(a, c, fast, h->has_kv_maps ? &h->kv_maps : nullptr, st) != cudaSuccess) return KVC_ERR_CUDA;
     if (d_cmax && cudaMemsetAsync(d_cmax, 0, (size_t)s.B * s.Hq * 4, st) != cudaSuccess) return KVC_ERR_CUDA;

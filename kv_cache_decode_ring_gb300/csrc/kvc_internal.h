@@ -21,7 +21,12 @@ constexpr int kBands = 16;            // witness bands per key row
 constexpr int kGenericSplit = 64;     // keys per split, generic decode kernel
 constexpr int kFastSplit = 128;       // keys per split, bf16 fast decode kernel
 constexpr int kInt8Split = 1024;      // keys per quantized split, INT8 decode kernel
-constexpr int kGqaSplit = 512;        // keys per split, bf16 decode kernel for 4 or 8 heads per KV head
+// keys per split of the bf16 decode kernel for 4 or 8 heads per KV head: longer splits
+// when a request may attend to many keys (less per-CTA start-up per byte), shorter ones
+// otherwise (enough CTAs to fill the GPU)
+constexpr int kGqaSplit = 1024;
+constexpr int kGqaSplitLong = 2048;
+constexpr int kGqaLongKeys = 16384;
 constexpr int kMaxRestored = 1024;    // INT8 blocks restored to full precision per (request, KV head)
 constexpr int kExactBlocksPerCta = 64; // restored blocks one CTA of the exact-block decode serves
 constexpr int kExactSplits = kMaxRestored / kExactBlocksPerCta;   // their split slots per query head
@@ -66,6 +71,7 @@ struct Shape {
     int max_chunk;               // largest suffix of kvc_chunk_attn (0 = none)
     int xpool;                   // entries of the INT8 exact-block pool
     int pages;                   // pages of a paged cache (0 = not paged)
+    bool gqa;                    // the bf16 GQA decode kernel serves the shape
     int store_slots;             // saved-prefill slots (0 = none)
 };
 
@@ -84,6 +90,7 @@ struct DecodeArgs {
     uint32_t* hdr;
     const int32_t* table; // paged caches: the block table (else nullptr)
     int B, Hq, Hkv, g, d, S, W, max_splits, split;
+    int gqa;              // the GQA decode kernel serves the shape (split kGqaSplit or kGqaSplitLong)
     int ring;
     int bf16;             // cache dtype (1 = bf16, 0 = fp32)
     float scale_log2;     // log2(e) / sqrt(d)
@@ -150,7 +157,7 @@ inline bool page_touched(const Shape& s, int lp, long long lo, long long hi) {
 }
 // INT8 exact-block decode (int8_exact.cu): the restored blocks' splits
 cudaError_t launch_int8_exact(kvc_handle* h, const void* q, float* ct, cudaStream_t st);
-// maps: required when the GQA kernel serves the shape (split == kGqaSplit)
+// maps: required when the GQA kernel serves the shape (Shape::gqa)
 cudaError_t launch_decode(const DecodeArgs& d, const CombineArgs& c, bool fast, const KvMaps* maps, cudaStream_t st);
 bool chunk_supported(const Shape& s);
 bool gqa_decode_supported(int d, int g);

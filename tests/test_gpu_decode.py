@@ -78,6 +78,33 @@ CASES = [
     ("f32-gqa4-d128", 8, 2, 128, "contiguous", 600, 0, 10000.0),
 ]
 
+# GQA decode splits of 1024 keys (2048 once a request may attend to 16384 keys): lengths
+# that span several splits and end inside one, and a window that starts inside a split
+LONG_CASES = [
+    # name, Hq, Hkv, d, capacity, window, lengths
+    ("gqa4-d128-3splits", 8, 2, 128, 3200, 0, [1, 1023, 1025, 3100]),
+    ("gqa8-d64-window", 8, 1, 64, 3200, 1500, [700, 3000, 2049, 1500]),
+    ("gqa4-d128-long-split", 8, 2, 128, 16400, 0, [2047, 2049, 6000, 16390]),
+]
+
+
+@pytest.mark.parametrize("case", LONG_CASES, ids=lambda c: c[0])
+def test_gqa_split_parity(case):
+    name, Hq, Hkv, d, cap, window, lengths = case
+    w = wl.small(name, B=4, Hq=Hq, Hkv=Hkv, d=d, capacity=cap, window=window, rope_base=10000.0, seed=41)
+    cache = kvc.Cache.from_workload(w)
+    model = oracle_for(w)
+    for c0 in range(0, max(lengths), 4096):                  # prefill in chunks
+        n = min(4096, max(lengths) - c0)
+        k, v = w.prefill_chunk(c0 // 4096, n)
+        counts = [max(0, min(n, x - c0)) for x in lengths]
+        cache.append_rows(k.cuda(), v.cuda(), counts=counts)
+        model.append_rows(host(k), host(v), counts)
+    for s in range(2):
+        _step(cache, model, w, *w.step_qkv(s))
+    check_state(cache, model, w)
+    assert cache.device_status() == 0
+
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: c[0])
 def test_small_parity(case):
