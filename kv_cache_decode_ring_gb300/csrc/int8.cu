@@ -51,11 +51,11 @@ namespace kvc {
 namespace {
 
 constexpr int kWarps = 4;
-constexpr int kTilesPerWarp = 16;          // one 16-token block per tile
+// one 16-token block per tile; a warp takes split / (kWarps * 16) tiles (16 or 32)
 constexpr int kStages = 3;                 // per warp
 constexpr float kLazyMax = 8.f;            // log2-domain headroom of the reference maximum
-static_assert(kWarps * kTilesPerWarp * kQBlock == kInt8Split, "split shape");
-static_assert(kTilesPerWarp <= 32, "one tile's scales per lane");
+static_assert(kInt8Split % (kWarps * kQBlock) == 0 && kInt8SplitLong % (kWarps * kQBlock) == 0, "split shape");
+static_assert(kInt8SplitLong / (kWarps * kQBlock) <= 32, "one tile's scales per lane");
 
 struct Int8Args {
     const void* q;
@@ -80,6 +80,7 @@ struct Int8Args {
     uint32_t layer_ctr;             // Tier B: 65536 * layer
     uint32_t rk[20];                // Tier B: Philox round keys (k0 + r W0, k1 + r W1), r = 0..9
     int B, Hq, Hkv, d, S, max_splits;
+    int split;          // tokens per quantized split
     float scale_log2;   // log2(e)/sqrt(d)
     float inv_sqrt_d_up;
 };
@@ -94,6 +95,7 @@ struct Int8CombineArgs {
     float* cmax;        // nullable
     float* tanh_out;    // nullable
     int B, Hq, Hkv, d, max_splits, out_bf16;
+    int split;          // tokens per quantized split
 };
 
 // D (16x8, fp32) += A (16x16, fp16, row) . B (16x8, fp16, col)
@@ -226,7 +228,8 @@ int8_decode_kernel(const Int8Args a) {
     const int b = blockIdx.z, kvh = blockIdx.y, split = blockIdx.x;
     const int len = a.next_pos[b];
     const int nfull = len & ~(kQBlock - 1);
-    const int nsq = (nfull + kInt8Split - 1) / kInt8Split;
+    const int nsq = (nfull + a.split - 1) / a.split;
+    const int tpw = a.split / (kWarps * kQBlock);             // tiles per warp
     const bool tail_split = split == nsq;
     if (split > nsq || (tail_split && len == nfull && a.xn[(size_t)b * a.Hkv + kvh] == 0)) return;
     const int t_q = len - 1;
@@ -330,7 +333,7 @@ int8_decode_kernel(const Int8Args a) {
     unsigned char* myS = smem + warp * C::WARPB;
     uint64_t* myBar = bar + warp * kStages;
     // block of this warp's tile i (tiles of the 4 warps interleaved)
-    auto tile_blk = [&](int i) { return (split * kInt8Split) / kQBlock + i * kWarps + warp; };
+    auto tile_blk = [&](int i) { return (split * a.split) / kQBlock + i * kWarps + warp; };
     auto tile_ok = [&](int i) { return (tile_blk(i) + 1) * kQBlock <= nfull; };
     auto issue = [&](int i) {
         if (lane == 0 && tile_ok(i)) {
@@ -356,7 +359,7 @@ int8_decode_kernel(const Int8Args a) {
     // relative to the warp's largest s_V, times 2^7
     float skv = 0.f, rvv = 0.f;
     int xmv = -1;                                     // >= 0: restored, served by the exact split
-    if (lane < kTilesPerWarp && tile_ok(lane)) {
+    if (lane < tpw && tile_ok(lane)) {
         skv = a.sk[bh * (a.S / kQBlock) + tile_blk(lane)];
         rvv = a.sv[bh * (a.S / kQBlock) + tile_blk(lane)];
         xmv = a.xmap[bh * (a.S / kQBlock) + tile_blk(lane)];
@@ -442,7 +445,7 @@ int8_decode_kernel(const Int8Args a) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) acc[mt][nt][e] = 0.f;
 
-    for (int i = 0; i < kTilesPerWarp; ++i) {
+    for (int i = 0; i < tpw; ++i) {
         if (!tile_ok(i)) break;                   // later tiles of this warp are empty too
         const int sg = i % kStages;
         const uint32_t par = (uint32_t)((i / kStages) & 1);
@@ -455,7 +458,7 @@ int8_decode_kernel(const Int8Args a) {
             // (if issued) land before the stages are reused for the partial
             if (lane == 0) atomicOr(a.hdr, kErrWait);
             mbar_wait(&myBar[sg], par);
-            for (int j = i + 1; j < i + kStages && j < kTilesPerWarp; ++j)
+            for (int j = i + 1; j < i + kStages && j < tpw; ++j)
                 if (tile_ok(j)) mbar_wait(&myBar[j % kStages], (uint32_t)((j / kStages) & 1));
             break;
         }
@@ -623,7 +626,7 @@ int8_decode_kernel(const Int8Args a) {
         // this stage and the staging are free once every lane is past its reads
         __syncwarp();
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        if (i + kStages < kTilesPerWarp) issue(i + kStages);
+        if (i + kStages < tpw) issue(i + kStages);
     }
 
     // ---- this warp's partial into its stage buffers (all issued copies were awaited):
@@ -715,7 +718,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32) int8_combine_kernel(const 
     const int kvh = hq / (c.Hq / c.Hkv);
     const int nx = c.xn[(size_t)b * c.Hkv + kvh];
     // quantized splits, the exact-rows split (if it ran), the exact-block splits
-    const int ns = (nfull + kInt8Split - 1) / kInt8Split + (len > nfull || nx > 0 ? 1 : 0) +
+    const int ns = (nfull + c.split - 1) / c.split + (len > nfull || nx > 0 ? 1 : 0) +
                    (nx + kExactBlocksPerCta - 1) / kExactBlocksPerCta;
     const size_t row = (size_t)b * c.Hq + hq;
     const float2* ml = c.part_ml + row * c.max_splits;
@@ -805,6 +808,7 @@ cudaError_t launch_int8_decode(kvc_handle* h, const void* q, void* out, float* c
     a.ct = ct;
     a.hdr = reinterpret_cast<uint32_t*>(h->state + h->L.hdr);
     a.B = s.B; a.Hq = s.Hq; a.Hkv = s.Hkv; a.d = s.d; a.S = s.S; a.max_splits = s.max_splits;
+    a.split = s.split;
     a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)s.d));
     a.inv_sqrt_d_up = std::nextafter((float)(1.0 / std::sqrt((double)s.d)), 1.0f);
     cudaError_t e = cudaErrorInvalidValue;
@@ -819,6 +823,7 @@ cudaError_t launch_int8_decode(kvc_handle* h, const void* q, void* out, float* c
     c.part_ml = a.part_ml; c.part_acc = a.part_acc; c.part_c = a.part_c; c.next_pos = a.next_pos; c.xn = a.xn;
     c.out = out; c.cmax = cmax; c.tanh_out = tanh_out;
     c.B = s.B; c.Hq = s.Hq; c.Hkv = s.Hkv; c.d = s.d; c.max_splits = s.max_splits; c.out_bf16 = s.out_bf16;
+    c.split = s.split;
     int8_combine_kernel<<<dim3(s.Hq, s.B), kCombineWarps * 32, 0, st>>>(c);
     return cudaGetLastError();
 }

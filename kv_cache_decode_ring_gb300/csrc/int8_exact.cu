@@ -44,6 +44,7 @@ struct ExactArgs {
     float* ct;          // nullable
     uint32_t* hdr;
     int B, Hq, Hkv, d, S, max_splits;
+    int split;          // tokens per quantized split of the INT8 decode
     float scale_log2;
 };
 
@@ -105,7 +106,7 @@ __global__ void __launch_bounds__(kWarps * 32) int8_exact_kernel(const ExactArgs
     if (base >= nx) return;
     const int len = a.next_pos[b];
     const int nfull = len & ~(kQBlock - 1);
-    const int split = (nfull + kInt8Split - 1) / kInt8Split + 1 + blockIdx.x;
+    const int split = (nfull + a.split - 1) / a.split + 1 + blockIdx.x;
     const int t_q = len - 1;
     const size_t rowq0 = (size_t)b * a.Hq + (size_t)kvh * G;
 
@@ -344,6 +345,7 @@ cudaError_t launch_int8_exact(kvc_handle* h, const void* q, float* ct, cudaStrea
     a.ct = ct;
     a.hdr = reinterpret_cast<uint32_t*>(h->state + h->L.hdr);
     a.B = s.B; a.Hq = s.Hq; a.Hkv = s.Hkv; a.d = s.d; a.S = s.S; a.max_splits = s.max_splits;
+    a.split = s.split;
     a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)s.d));
     const int nx_ctas = (max_xn + kExactBlocksPerCta - 1) / kExactBlocksPerCta;
 #define KVC_CASE(D, G) \

@@ -73,10 +73,10 @@ bool make_shape(const kvc_config& c, Shape* s) {
     // a paged cache may start its splits up to one page before the window
     s->max_splits = (int)((keys + s->split - 1) / s->split) + (s->pages > 0 ? 1 : 0);
     if (int8) {
-        // quantized splits of kInt8Split keys, one split for the exact tail rows and,
-        // with a pool, the splits of the exact-block decode
-        s->split = kInt8Split;
-        s->max_splits = (int)((keys + kInt8Split - 1) / kInt8Split) + 1 + (s->xpool > 0 ? kExactSplits : 0);
+        // quantized splits (longer ones for long caches: less start-up per byte), one
+        // split for the exact tail rows and, with a pool, the splits of the exact-block decode
+        s->split = keys >= kInt8LongKeys ? kInt8SplitLong : kInt8Split;
+        s->max_splits = (int)((keys + s->split - 1) / s->split) + 1 + (s->xpool > 0 ? kExactSplits : 0);
     }
     return true;
 }

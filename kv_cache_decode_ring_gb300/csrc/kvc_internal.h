@@ -20,7 +20,9 @@ constexpr int kPage = 16;             // slots per page of a paged cache
 constexpr int kBands = 16;            // witness bands per key row
 constexpr int kGenericSplit = 64;     // keys per split, generic decode kernel
 constexpr int kFastSplit = 128;       // keys per split, bf16 fast decode kernel
-constexpr int kInt8Split = 1024;      // keys per quantized split, INT8 decode kernel
+constexpr int kInt8Split = 1024;      // keys per quantized split, INT8 decode kernel ...
+constexpr int kInt8SplitLong = 2048;  // ... and for caches of kInt8LongKeys slots or more
+constexpr int kInt8LongKeys = 16384;
 // keys per split of the bf16 decode kernel for 4 or 8 heads per KV head: longer splits
 // when a request may attend to many keys (less per-CTA start-up per byte), shorter ones
 // otherwise (enough CTAs to fill the GPU)

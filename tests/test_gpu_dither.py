@@ -65,13 +65,15 @@ def check_decode(cache, model, q):
     return out
 
 
-@pytest.mark.parametrize("d,Hq,Hkv", [(128, 8, 2), (128, 4, 4), (128, 16, 2), (64, 8, 2), (64, 2, 1), (128, 2, 1)])
-def test_dither_parity(d, Hq, Hkv):
-    w = _w("dither-%d-%d-%d" % (d, Hq, Hkv), B=3, Hq=Hq, Hkv=Hkv, d=d, capacity=1104, rope_base=10000.0,
+@pytest.mark.parametrize("d,Hq,Hkv,cap", [(128, 8, 2, 1104), (128, 4, 4, 1104), (128, 16, 2, 1104),
+                                           (64, 8, 2, 1104), (64, 2, 1, 1104), (128, 2, 1, 1104),
+                                           (128, 8, 2, 16400)])      # the last: 2048-token splits
+def test_dither_parity(d, Hq, Hkv, cap):
+    w = _w("dither-%d-%d-%d-%d" % (d, Hq, Hkv, cap), B=3, Hq=Hq, Hkv=Hkv, d=d, capacity=cap, rope_base=10000.0,
            seed=31, outliers=(4, 20.0))
     cache = kvc.Cache.from_workload(w, out_dtype="f32")
     model = oracle_for(w)
-    lengths = [1060, 47, 16]
+    lengths = [1060, 47, 16] if cap < 16384 else [4150, 2047, 16]
     k, v = w.prefill_chunk(0, max(lengths))
     cache.append_rows(k.cuda(), v.cuda(), counts=lengths)
     model.append_rows(host(k), host(v), lengths)

@@ -125,6 +125,26 @@ def test_int8_multi_split_parity(d, Hq, Hkv):
     assert cache.device_status() == 0
 
 
+def test_int8_long_split_parity():
+    # caches of 16384 slots or more take 2048-token splits: lengths around one and
+    # several of them, and a request of a single block
+    w = wl.small("int8-long-split", B=3, Hq=8, Hkv=2, d=128, capacity=16400, rope_base=10000.0,
+                 quant="int8", seed=37, outliers=(4, 20.0))
+    cache = kvc.Cache.from_workload(w, out_dtype="f32")
+    model = _oracle(w)
+    lengths = [2047, 6150, 16]
+    k, v = w.prefill_chunk(0, max(lengths))
+    cache.append_rows(k.cuda(), v.cuda(), counts=lengths)
+    model.append_rows(host(k), host(v), lengths)
+    check_int8_state(cache, model, requests=[0, 2])
+    for s in range(2):
+        q, k1, v1 = w.step_qkv(s)
+        cache.append(k1.cuda(), v1.cuda())
+        model.append(host(k1), host(v1))
+        check_decode(cache, model, q)
+    assert cache.device_status() == 0
+
+
 def test_int8_trim_rules_and_continue():
     w = wl.small("int8-trim", B=2, Hq=4, Hkv=2, d=128, capacity=256, rope_base=10000.0, quant="int8", seed=5)
     cache = kvc.Cache.from_workload(w, out_dtype="f32")
