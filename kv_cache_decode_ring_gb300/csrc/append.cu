@@ -157,7 +157,55 @@ __global__ void __launch_bounds__(kThreads) append_token_kernel(const AppendArgs
     }
     const int d = a.d, half = d / 2;
     const int slot = a.ring ? p % a.S : p;
-    if (!a.int8) {
+    if (!a.int8 && a.bf16 && d % 8 == 0) {
+        // 8 elements (16 bytes) per item, kU items per thread with every load issued
+        // before any arithmetic: one round trip for the whole row set
+        constexpr int kU = 4;
+        const int vec = d / 8, n = a.Hkv * vec;
+        const uint4* K = static_cast<const uint4*>(a.k);
+        const uint4* V = static_cast<const uint4*>(a.v);
+        for (int base = threadIdx.x; base < n; base += kU * blockDim.x) {
+            uint4 kx[kU], vx[kU];
+            float4 cs[kU][2];
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int idx = base + u * blockDim.x;
+                if (idx >= n) continue;
+                const int h = idx / vec, c = idx % vec;
+                kx[u] = __ldg(K + ((size_t)b * a.Hkv + h) * vec + c);
+                vx[u] = __ldg(V + ((size_t)b * a.Hkv + h) * vec + c);
+                if (a.rope) {
+                    const float4* r = reinterpret_cast<const float4*>(a.rope + (size_t)p * half + 4 * c);
+                    cs[u][0] = __ldg(r);
+                    cs[u][1] = __ldg(r + 1);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int idx = base + u * blockDim.x;
+                if (idx >= n) continue;
+                const int h = idx / vec, c = idx % vec;
+                const size_t dst = kv_row(a.table, b, h, slot, a.Hkv, a.S) * d + 8 * c;
+                uint4 ko = kx[u];
+                if (a.rope) {
+                    uint32_t w[4] = {kx[u].x, kx[u].y, kx[u].z, kx[u].w};
+                    const float2 r[4] = {make_float2(cs[u][0].x, cs[u][0].y), make_float2(cs[u][0].z, cs[u][0].w),
+                                         make_float2(cs[u][1].x, cs[u][1].y), make_float2(cs[u][1].z, cs[u][1].w)};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const __nv_bfloat162 x2 = *reinterpret_cast<const __nv_bfloat162*>(&w[e]);
+                        float y0, y1;
+                        rope_pair(__low2float(x2), __high2float(x2), r[e], y0, y1);
+                        const __nv_bfloat162 o2 = __floats2bfloat162_rn(y0, y1);
+                        w[e] = *reinterpret_cast<const uint32_t*>(&o2);
+                    }
+                    ko = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+                *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.kc) + dst) = ko;
+                *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.vc) + dst) = vx[u];
+            }
+        }
+    } else if (!a.int8) {
         for (int idx = threadIdx.x; idx < a.Hkv * half; idx += blockDim.x) {
             const int h = idx / half, i = idx % half;
             const size_t src = ((size_t)b * a.Hkv + h) * d;
