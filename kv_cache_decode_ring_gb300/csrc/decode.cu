@@ -87,67 +87,83 @@ __global__ void __launch_bounds__(kThreads) decode_generic_kernel(const DecodeAr
     }
 }
 
-// Combine: CTA per (query head, request), 8 warps.  The block reduces the
-// split maxima and denominators; then warp w sums splits w, w + 8, ... with lanes
-// over d (enough loads in flight to hide L2 latency), and the warps' sums meet
-// in shared memory.
-constexpr int kCombineWarps = 8;
+// Combine: WPR warps per (request, query head) row, 8 / WPR rows per CTA.  Each warp
+// finds the row's maximum and denominator itself with lanes over splits (the second
+// pass re-reads from L1), then accumulates every WPR-th split's partial with lanes
+// over 4-dim groups, loads unrolled; the WPR sums meet in shared memory once.  One
+// warp per row when rows have few splits (more rows in flight), four when they have
+// many (shorter chains of loads).
+constexpr int kCombineThreads = 256;
 
-__device__ __forceinline__ float block_reduce(float v, bool is_max, float* red) {
-    for (int o = 16; o; o >>= 1) {
-        const float w = __shfl_xor_sync(0xffffffffu, v, o);
-        v = is_max ? fmaxf(v, w) : v + w;
-    }
+template <int WPR>
+__global__ void __launch_bounds__(kCombineThreads) combine_rows_kernel(const CombineArgs c) {
+    constexpr int kWarpsPerRow = WPR;
+    constexpr int kRowsPerCta = kCombineThreads / 32 / WPR;
+    __shared__ float4 sacc[kRowsPerCta][kWarpsPerRow][64];          // d <= 256
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    __syncthreads();                                   // red may still be read by a previous reduction
-    if (lane == 0) red[warp] = v;
-    __syncthreads();
-    v = red[0];
-    for (int w = 1; w < kCombineWarps; ++w) v = is_max ? fmaxf(v, red[w]) : v + red[w];
-    return v;
-}
-
-__global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const CombineArgs c) {
-    __shared__ float red[kCombineWarps];
-    __shared__ float sacc[kCombineWarps][256];
-    const int hq = blockIdx.x, b = blockIdx.y;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int len = c.next_pos[b];
-    int lo, hi;
-    key_range(len, c.S, c.W, c.ring, lo, hi);
-    if (c.align_lo) lo &= ~(kPage - 1);             // the paged GQA decode's split origin
-    const int ns = (hi - lo + c.split - 1) / c.split;
-    const size_t row = (size_t)b * c.Hq + hq;
+    const int r = warp / kWarpsPerRow, w = warp % kWarpsPerRow;
+    const size_t row = (size_t)blockIdx.x * kRowsPerCta + r;
+    const bool valid = row < (size_t)c.B * c.Hq;
+    const bool vec = c.d % 4 == 0;
+    int ns = 0;
+    float mx = -INFINITY, inv = 0.f;
     const float2* ml = c.part_ml + row * c.max_splits;
-    float mx = -INFINITY;
-    for (int s = threadIdx.x; s < ns; s += blockDim.x) mx = fmaxf(mx, ml[s].x);
-    mx = block_reduce(mx, true, red);
-    float L = 0.f;
-    for (int s = threadIdx.x; s < ns; s += blockDim.x) L += ml[s].y * exp2f(ml[s].x - mx);
-    L = block_reduce(L, false, red);
-    float acc[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) acc[j] = 0.f;
-#pragma unroll 8
-    for (int s = warp; s < ns; s += kCombineWarps) {
-        const float f = exp2f(ml[s].x - mx);
-        const float* pa = c.part_acc + (row * c.max_splits + s) * c.d;
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-            if (lane + 32 * j < c.d) acc[j] = fmaf(pa[lane + 32 * j], f, acc[j]);
+    const float* pa = c.part_acc + row * c.max_splits * c.d;
+    if (valid) {
+        const int b = (int)(row / c.Hq);
+        const int len = c.next_pos[b];
+        int lo, hi;
+        key_range(len, c.S, c.W, c.ring, lo, hi);
+        if (c.align_lo) lo &= ~(kPage - 1);         // the paged GQA decode's split origin
+        ns = (hi - lo + c.split - 1) / c.split;
+        for (int s = lane; s < ns; s += 32) mx = fmaxf(mx, __ldg(ml + s).x);
+        for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        float L = 0.f;
+        for (int s = lane; s < ns; s += 32) {
+            const float2 v = __ldg(ml + s);
+            L += v.y * exp2f(v.x - mx);
+        }
+        for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+        inv = L > 0.f ? 1.f / L : 0.f;
+        if (vec) {
+            for (int i0 = 4 * lane; i0 < c.d; i0 += 128) {
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+                for (int s = w; s < ns; s += kWarpsPerRow) {
+                    const float f = exp2f(__ldg(ml + s).x - mx);
+                    const float4 x = __ldg(reinterpret_cast<const float4*>(pa + (size_t)s * c.d + i0));
+                    acc.x = fmaf(x.x, f, acc.x); acc.y = fmaf(x.y, f, acc.y);
+                    acc.z = fmaf(x.z, f, acc.z); acc.w = fmaf(x.w, f, acc.w);
+                }
+                sacc[r][w][i0 / 4] = acc;
+            }
+        }
     }
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-        if (lane + 32 * j < c.d) sacc[warp][lane + 32 * j] = acc[j];
     __syncthreads();
-    const float inv = L > 0.f ? 1.f / L : 0.f;
-    for (int i = threadIdx.x; i < c.d; i += blockDim.x) {
-        float o = 0.f;
+    if (!valid || w != 0) return;
+    if (vec) {
+        for (int i0 = 4 * lane; i0 < c.d; i0 += 128) {
+            float4 acc = sacc[r][0][i0 / 4];
 #pragma unroll
-        for (int w = 0; w < kCombineWarps; ++w) o += sacc[w][i];
-        o *= inv;
-        if (c.bf16) static_cast<__nv_bfloat16*>(c.out)[row * c.d + i] = __float2bfloat16_rn(o);
-        else static_cast<float*>(c.out)[row * c.d + i] = o;
+            for (int k = 1; k < kWarpsPerRow; ++k) {
+                const float4 x = sacc[r][k][i0 / 4];
+                acc.x += x.x; acc.y += x.y; acc.z += x.z; acc.w += x.w;
+            }
+            const float o[4] = {acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                if (c.bf16) static_cast<__nv_bfloat16*>(c.out)[row * c.d + i0 + e] = __float2bfloat16_rn(o[e]);
+                else static_cast<float*>(c.out)[row * c.d + i0 + e] = o[e];
+            }
+        }
+    } else {
+        // head dims not a multiple of 4 (small shapes): the row's first warp alone
+        for (int i = lane; i < c.d; i += 32) {
+            float acc = 0.f;
+            for (int s = 0; s < ns; ++s) acc = fmaf(__ldg(pa + (size_t)s * c.d + i), exp2f(__ldg(ml + s).x - mx), acc);
+            if (c.bf16) static_cast<__nv_bfloat16*>(c.out)[row * c.d + i] = __float2bfloat16_rn(acc * inv);
+            else static_cast<float*>(c.out)[row * c.d + i] = acc * inv;
+        }
     }
 }
 
@@ -169,7 +185,9 @@ cudaError_t launch_decode(const DecodeArgs& a, const CombineArgs& c, bool fast, 
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    combine_kernel<<<dim3(a.Hq, a.B), kCombineWarps * 32, 0, st>>>(c);
+    const size_t rows = (size_t)a.B * a.Hq;
+    if (a.max_splits <= 8) combine_rows_kernel<1><<<(unsigned)((rows + 7) / 8), kCombineThreads, 0, st>>>(c);
+    else combine_rows_kernel<4><<<(unsigned)((rows + 1) / 2), kCombineThreads, 0, st>>>(c);
     return cudaGetLastError();
 }
 
