@@ -157,13 +157,17 @@ __global__ void __launch_bounds__(kThreads) append_token_kernel(const AppendArgs
     }
     const int d = a.d, half = d / 2;
     const int slot = a.ring ? p % a.S : p;
-    if (!a.int8 && a.bf16 && d % 8 == 0) {
+    const int tslot = p % kQBlock;                     // INT8: the row's place in the exact tail
+    if (a.bf16 && d % 8 == 0) {
         // 8 elements (16 bytes) per item, kU items per thread with every load issued
-        // before any arithmetic: one round trip for the whole row set
+        // before any arithmetic: one round trip for the whole row set.  The rows go to
+        // the cache (bf16) or to the exact tail (INT8 tier).
         constexpr int kU = 4;
         const int vec = d / 8, n = a.Hkv * vec;
         const uint4* K = static_cast<const uint4*>(a.k);
         const uint4* V = static_cast<const uint4*>(a.v);
+        __nv_bfloat16* kdst = a.int8 ? a.ktail : static_cast<__nv_bfloat16*>(a.kc);
+        __nv_bfloat16* vdst = a.int8 ? a.vtail : static_cast<__nv_bfloat16*>(a.vc);
         for (int base = threadIdx.x; base < n; base += kU * blockDim.x) {
             uint4 kx[kU], vx[kU];
             float4 cs[kU][2];
@@ -185,7 +189,8 @@ __global__ void __launch_bounds__(kThreads) append_token_kernel(const AppendArgs
                 const int idx = base + u * blockDim.x;
                 if (idx >= n) continue;
                 const int h = idx / vec, c = idx % vec;
-                const size_t dst = kv_row(a.table, b, h, slot, a.Hkv, a.S) * d + 8 * c;
+                const size_t dst = (a.int8 ? (((size_t)b * a.Hkv + h) * kQBlock + tslot)
+                                           : kv_row(a.table, b, h, slot, a.Hkv, a.S)) * d + 8 * c;
                 uint4 ko = kx[u];
                 if (a.rope) {
                     uint32_t w[4] = {kx[u].x, kx[u].y, kx[u].z, kx[u].w};
@@ -201,11 +206,29 @@ __global__ void __launch_bounds__(kThreads) append_token_kernel(const AppendArgs
                     }
                     ko = make_uint4(w[0], w[1], w[2], w[3]);
                 }
-                *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.kc) + dst) = ko;
-                *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.vc) + dst) = vx[u];
+                *reinterpret_cast<uint4*>(kdst + dst) = ko;
+                *reinterpret_cast<uint4*>(vdst + dst) = vx[u];
             }
         }
-    } else if (!a.int8) {
+        if (a.int8 && tslot == kQBlock - 1) {
+            // the 16th row completes the block: every KV head quantizes its 16 tail rows
+            float* sK = smem;
+            float* sV = smem + kQBlock * d;
+            float* red = smem + 2 * kQBlock * d;
+            __threadfence_block();
+            for (int h = 0; h < a.Hkv; ++h) {
+                const size_t tail = ((size_t)b * a.Hkv + h) * kQBlock * d;
+                __syncthreads();                       // the tail rows written; smem free
+                for (int i = threadIdx.x; i < kQBlock * d; i += blockDim.x) {
+                    sK[i] = __bfloat162float(a.ktail[tail + i]);
+                    sV[i] = __bfloat162float(a.vtail[tail + i]);
+                }
+                __syncthreads();
+                quantize_block(a, sK, sV, red, b, h, p / kQBlock);
+            }
+        }
+    } else {
+        // fp32 caches and other head sizes (never INT8: that tier is bf16 with d % 16 == 0)
         for (int idx = threadIdx.x; idx < a.Hkv * half; idx += blockDim.x) {
             const int h = idx / half, i = idx % half;
             const size_t src = ((size_t)b * a.Hkv + h) * d;
@@ -215,44 +238,6 @@ __global__ void __launch_bounds__(kThreads) append_token_kernel(const AppendArgs
             store_pair(a.kc, dst + 2 * i, y0, y1, a.bf16);
             store_pair(a.vc, dst + 2 * i, ld_elem(a.v, src + 2 * i, a.bf16),
                        ld_elem(a.v, src + 2 * i + 1, a.bf16), a.bf16);
-        }
-    } else {
-        // INT8 tier (bf16 only): the row joins the exact tail; the 16th row of a
-        // block quantizes the whole block.
-        float* sK = smem;
-        float* sV = smem + kQBlock * d;
-        float* red = smem + 2 * kQBlock * d;
-        const int tslot = p % kQBlock;
-        const bool complete = tslot == kQBlock - 1;
-        for (int h = 0; h < a.Hkv; ++h) {
-            const size_t src = ((size_t)b * a.Hkv + h) * d;
-            const size_t tail = ((size_t)b * a.Hkv + h) * kQBlock * d;
-            for (int i = threadIdx.x; i < half; i += blockDim.x) {
-                float y0, y1;
-                key_pair(a, a.k, src, i, p, y0, y1);
-                const __nv_bfloat16 k0 = __float2bfloat16_rn(y0), k1 = __float2bfloat16_rn(y1);
-                const __nv_bfloat16 v0 = __float2bfloat16_rn(ld_elem(a.v, src + 2 * i, 1));
-                const __nv_bfloat16 v1 = __float2bfloat16_rn(ld_elem(a.v, src + 2 * i + 1, 1));
-                a.ktail[tail + (size_t)tslot * d + 2 * i] = k0;
-                a.ktail[tail + (size_t)tslot * d + 2 * i + 1] = k1;
-                a.vtail[tail + (size_t)tslot * d + 2 * i] = v0;
-                a.vtail[tail + (size_t)tslot * d + 2 * i + 1] = v1;
-                if (complete) {
-                    sK[tslot * d + 2 * i] = __bfloat162float(k0);
-                    sK[tslot * d + 2 * i + 1] = __bfloat162float(k1);
-                    sV[tslot * d + 2 * i] = __bfloat162float(v0);
-                    sV[tslot * d + 2 * i + 1] = __bfloat162float(v1);
-                }
-            }
-            if (complete) {
-                for (int i = threadIdx.x; i < (kQBlock - 1) * d; i += blockDim.x) {
-                    sK[i] = __bfloat162float(a.ktail[tail + i]);
-                    sV[i] = __bfloat162float(a.vtail[tail + i]);
-                }
-                __syncthreads();
-                quantize_block(a, sK, sV, red, b, h, p / kQBlock);
-                __syncthreads();
-            }
         }
     }
     __syncthreads();

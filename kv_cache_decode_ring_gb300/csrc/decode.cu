@@ -91,8 +91,8 @@ __global__ void __launch_bounds__(kThreads) decode_generic_kernel(const DecodeAr
 // finds the row's maximum and denominator itself with lanes over splits (the second
 // pass re-reads from L1), then accumulates every WPR-th split's partial with lanes
 // over 4-dim groups, loads unrolled; the WPR sums meet in shared memory once.  One
-// warp per row when rows have few splits (more rows in flight), four when they have
-// many (shorter chains of loads).
+// warp per row when rows have few splits (more rows in flight), eight when rows are
+// few and long, four otherwise.
 constexpr int kCombineThreads = 256;
 
 template <int WPR>
@@ -187,6 +187,7 @@ cudaError_t launch_decode(const DecodeArgs& a, const CombineArgs& c, bool fast, 
     }
     const size_t rows = (size_t)a.B * a.Hq;
     if (a.max_splits <= 8) combine_rows_kernel<1><<<(unsigned)((rows + 7) / 8), kCombineThreads, 0, st>>>(c);
+    else if (rows < 1024) combine_rows_kernel<8><<<(unsigned)rows, kCombineThreads, 0, st>>>(c);
     else combine_rows_kernel<4><<<(unsigned)((rows + 1) / 2), kCombineThreads, 0, st>>>(c);
     return cudaGetLastError();
 }

@@ -688,76 +688,74 @@ __device__ __forceinline__ float tanh_up(float x) {
     return fminf(t, 1.f);
 }
 
-// Combine: CTA per (query head, request), 8 warps.  The block reduces the split
-// maxima, denominators and bound maxima; then warp w sums splits w, w + 8, ...
-// with lanes over d, and the warps' sums meet in shared memory.
-constexpr int kCombineWarps = 8;
+// Combine: WPR warps per (request, query head) row, 8 / WPR rows per CTA (the design
+// of the bf16 combine): each warp finds the row's maximum, denominator and bound
+// maximum with lanes over splits, then accumulates every WPR-th split's partial with
+// lanes over 4-dim groups; the sums meet in shared memory once.
+constexpr int kCombineThreads = 256;
 
-__device__ __forceinline__ float block_reduce(float v, bool is_max, float* red) {
-    for (int o = 16; o; o >>= 1) {
-        const float w = __shfl_xor_sync(0xffffffffu, v, o);
-        v = is_max ? fmaxf(v, w) : v + w;
-    }
+template <int WPR>
+__global__ void __launch_bounds__(kCombineThreads) int8_combine_kernel(const Int8CombineArgs c) {
+    constexpr int kRows = kCombineThreads / 32 / WPR;
+    __shared__ float4 sacc[kRows][WPR][32];                       // d <= 128
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    __syncthreads();                                   // red may still be read by a previous reduction
-    if (lane == 0) red[warp] = v;
+    const int r = warp / WPR, w = warp % WPR;
+    const size_t row = (size_t)blockIdx.x * kRows + r;
+    const bool valid = row < (size_t)c.B * c.Hq;
+    float mx = -INFINITY, inv = 0.f, cm = 0.f;
+    if (valid) {
+        const int b = (int)(row / c.Hq), hq = (int)(row % c.Hq);
+        const int len = c.next_pos[b];
+        const int nfull = len & ~(kQBlock - 1);
+        const int kvh = hq / (c.Hq / c.Hkv);
+        const int nx = c.xn[(size_t)b * c.Hkv + kvh];
+        // quantized splits, the exact-rows split (if it ran), the exact-block splits
+        const int ns = (nfull + c.split - 1) / c.split + (len > nfull || nx > 0 ? 1 : 0) +
+                       (nx + kExactBlocksPerCta - 1) / kExactBlocksPerCta;
+        const float2* ml = c.part_ml + row * c.max_splits;
+        const float* pc = c.part_c + row * c.max_splits;
+        for (int s = lane; s < ns; s += 32) { mx = fmaxf(mx, __ldg(ml + s).x); cm = fmaxf(cm, __ldg(pc + s)); }
+        for (int o = 16; o; o >>= 1) {
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o));
+        }
+        float L = 0.f;
+        for (int s = lane; s < ns; s += 32) {
+            const float2 v = __ldg(ml + s);
+            L += v.y * exp2f(v.x - mx);
+        }
+        for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+        inv = L > 0.f ? 1.f / L : 0.f;
+        const float* pa = c.part_acc + row * c.max_splits * c.d;
+        for (int i0 = 4 * lane; i0 < c.d; i0 += 128) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+            for (int s = w; s < ns; s += WPR) {
+                const float f = exp2f(__ldg(ml + s).x - mx);
+                const float4 x = __ldg(reinterpret_cast<const float4*>(pa + (size_t)s * c.d + i0));
+                acc.x = fmaf(x.x, f, acc.x); acc.y = fmaf(x.y, f, acc.y);
+                acc.z = fmaf(x.z, f, acc.z); acc.w = fmaf(x.w, f, acc.w);
+            }
+            sacc[r][w][i0 / 4] = acc;
+        }
+    }
     __syncthreads();
-    v = red[0];
-    for (int w = 1; w < kCombineWarps; ++w) v = is_max ? fmaxf(v, red[w]) : v + red[w];
-    return v;
-}
-
-__global__ void __launch_bounds__(kCombineWarps * 32) int8_combine_kernel(const Int8CombineArgs c) {
-    __shared__ float red[kCombineWarps];
-    __shared__ float sacc[kCombineWarps][128];
-    const int hq = blockIdx.x, b = blockIdx.y;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int len = c.next_pos[b];
-    const int nfull = len & ~(kQBlock - 1);
-    // quantized splits at 0 .. nsq - 1, the exact tail split (if any) at nsq
-    const int kvh = hq / (c.Hq / c.Hkv);
-    const int nx = c.xn[(size_t)b * c.Hkv + kvh];
-    // quantized splits, the exact-rows split (if it ran), the exact-block splits
-    const int ns = (nfull + c.split - 1) / c.split + (len > nfull || nx > 0 ? 1 : 0) +
-                   (nx + kExactBlocksPerCta - 1) / kExactBlocksPerCta;
-    const size_t row = (size_t)b * c.Hq + hq;
-    const float2* ml = c.part_ml + row * c.max_splits;
-    const float* pc = c.part_c + row * c.max_splits;
-    float mx = -INFINITY, cm = 0.f;
-    for (int s = threadIdx.x; s < ns; s += blockDim.x) {
-        mx = fmaxf(mx, ml[s].x);
-        cm = fmaxf(cm, pc[s]);
+    if (!valid || w != 0) return;
+    for (int i0 = 4 * lane; i0 < c.d; i0 += 128) {
+        float4 acc = sacc[r][0][i0 / 4];
+#pragma unroll
+        for (int k = 1; k < WPR; ++k) {
+            const float4 x = sacc[r][k][i0 / 4];
+            acc.x += x.x; acc.y += x.y; acc.z += x.z; acc.w += x.w;
+        }
+        const float o[4] = {acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            if (c.out_bf16) static_cast<__nv_bfloat16*>(c.out)[row * c.d + i0 + e] = __float2bfloat16_rn(o[e]);
+            else static_cast<float*>(c.out)[row * c.d + i0 + e] = o[e];
+        }
     }
-    mx = block_reduce(mx, true, red);
-    cm = block_reduce(cm, true, red);
-    float L = 0.f;
-    for (int s = threadIdx.x; s < ns; s += blockDim.x) L += ml[s].y * exp2f(ml[s].x - mx);
-    L = block_reduce(L, false, red);
-    float acc[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) acc[j] = 0.f;
-#pragma unroll 8
-    for (int s = warp; s < ns; s += kCombineWarps) {
-        const float f = exp2f(ml[s].x - mx);
-        const float* pa = c.part_acc + (row * c.max_splits + s) * c.d;
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            if (lane + 32 * j < c.d) acc[j] = fmaf(pa[lane + 32 * j], f, acc[j]);
-    }
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-        if (lane + 32 * j < c.d) sacc[warp][lane + 32 * j] = acc[j];
-    __syncthreads();
-    const float inv = L > 0.f ? 1.f / L : 0.f;
-    for (int i = threadIdx.x; i < c.d; i += blockDim.x) {
-        float o = 0.f;
-#pragma unroll
-        for (int w = 0; w < kCombineWarps; ++w) o += sacc[w][i];
-        o *= inv;
-        if (c.out_bf16) static_cast<__nv_bfloat16*>(c.out)[row * c.d + i] = __float2bfloat16_rn(o);
-        else static_cast<float*>(c.out)[row * c.d + i] = o;
-    }
-    if (threadIdx.x == 0) {
+    if (lane == 0) {
         if (c.cmax) c.cmax[row] = cm;
         if (c.tanh_out) c.tanh_out[row] = tanh_up(cm);
     }
@@ -824,7 +822,10 @@ cudaError_t launch_int8_decode(kvc_handle* h, const void* q, void* out, float* c
     c.out = out; c.cmax = cmax; c.tanh_out = tanh_out;
     c.B = s.B; c.Hq = s.Hq; c.Hkv = s.Hkv; c.d = s.d; c.max_splits = s.max_splits; c.out_bf16 = s.out_bf16;
     c.split = s.split;
-    int8_combine_kernel<<<dim3(s.Hq, s.B), kCombineWarps * 32, 0, st>>>(c);
+    const size_t rows = (size_t)s.B * s.Hq;
+    if (s.max_splits <= 8) int8_combine_kernel<1><<<(unsigned)((rows + 7) / 8), kCombineThreads, 0, st>>>(c);
+    else if (rows < 1024) int8_combine_kernel<8><<<(unsigned)rows, kCombineThreads, 0, st>>>(c);
+    else int8_combine_kernel<4><<<(unsigned)((rows + 1) / 2), kCombineThreads, 0, st>>>(c);
     return cudaGetLastError();
 }
 
