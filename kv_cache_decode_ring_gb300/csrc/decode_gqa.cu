@@ -6,7 +6,7 @@
 //
 // CTA = 4 warps = a split of 1024 keys (2048 for caches whose requests may attend
 // to 16384 keys or more).  A warp streams its 16 (32) tiles of 16 keys through
-// three shared-memory stages: a tile is d/64 tensor copies of 64 dims x
+// two shared-memory stages (three CTAs per SM): a tile is d/64 tensor copies of 64 dims x
 // 16 rows from K and as many from V, written with the 128-byte swizzle (16-byte
 // chunk c of row r at c ^ (r mod 8)), so the 8 row addresses of an ldmatrix fall
 // into 8 different bank groups.  Rows past the window's last key are copied too
@@ -33,7 +33,7 @@ namespace {
 
 constexpr int kWarps = 4;
 constexpr int kTileKeys = 16;                            // keys per stage
-constexpr int kStages = 3;                               // per warp
+constexpr int kStages = 2;                               // per warp (three CTAs per SM: more warps in flight)
 constexpr float kLazyMax = 8.f;                          // log2-domain headroom of the reference maximum
 static_assert(kGqaSplit % (kWarps * kTileKeys) == 0 && kGqaSplitLong % (kWarps * kTileKeys) == 0, "split shape");
 
@@ -93,7 +93,7 @@ struct GqaCfg {
 };
 
 template <int D, int G>
-__global__ void __launch_bounds__(kWarps * 32, 2)
+__global__ void __launch_bounds__(kWarps * 32, 3)
     decode_gqa_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                       const DecodeArgs a) {
     using C = GqaCfg<D, G>;
