@@ -14,9 +14,10 @@
 // fp16 witnesses [S][16], fp32 scales [S/16]; exact bf16 tail [16][d] for the
 // rows of the incomplete block.
 //
-// Kernel shape: CTA = 4 warps = a split of 1024 tokens (64 blocks); each warp
-// streams its 16 blocks through three shared-memory stages (codes and witnesses
-// by bulk copy on the stage's mbarrier), so copies overlap arithmetic; online
+// Kernel shape: CTA = 4 warps = a split of 1024 tokens (64 blocks; 2048 for caches
+// of 16384 slots or more); each warp streams its 16 (32) blocks through two or
+// three shared-memory stages (codes and witnesses by bulk copy on the stage's
+// mbarrier; two where four CTAs fit on an SM), so copies overlap arithmetic; online
 // softmax over the warp's blocks, warps merged at the end.  One extra split
 // handles the exact tail rows of the incomplete block (c_t = 0 there).  Blocks
 // restored to full precision by the gated fallback are skipped here and served
@@ -52,7 +53,6 @@ namespace {
 
 constexpr int kWarps = 4;
 // one 16-token block per tile; a warp takes split / (kWarps * 16) tiles (16 or 32)
-constexpr int kStages = 3;                 // per warp
 constexpr float kLazyMax = 8.f;            // log2-domain headroom of the reference maximum
 static_assert(kInt8Split % (kWarps * kQBlock) == 0 && kInt8SplitLong % (kWarps * kQBlock) == 0, "split shape");
 static_assert(kInt8SplitLong / (kWarps * kQBlock) <= 32, "one tile's scales per lane");
@@ -183,7 +183,10 @@ struct I8 {
     static constexpr int CB = kQBlock * D;          // bytes of one block's codes (K or V)
     static constexpr int WB = DITHER ? 0 : kQBlock * kBands * 2;     // witnesses (none in Tier B)
     static constexpr int STAGEB = 2 * CB + WB;
-    static constexpr int WARPB = kStages * STAGEB;
+    // copy stages per warp: two at d = 128 with up to 4 heads per KV head (four CTAs per SM
+    // then fit in registers and shared memory: more warps in flight), else three
+    static constexpr int STAGES = (D == 128 && G <= 4) ? 2 : 3;
+    static constexpr int WARPB = STAGES * STAGEB;
     static constexpr int PARTF = G * (D + 3);       // floats of one warp's partial (m, l, c, acc)
     static_assert(PARTF * 4 <= WARPB, "partial must fit in the warp's stages");
     // P^T staging per warp and column tile: 8 rows of 16 fp16 tokens; row n at
@@ -192,14 +195,14 @@ struct I8 {
     static constexpr int PROWB = 288;
     // after the warps' stages: P^T staging [warp][NT] (the fp32 query during
     // preparation), fp16 query [2G][D], band norms [G][20], score factors [G],
-    // barriers [warp][kStages]
+    // barriers [warp][STAGES]
     static constexpr int OFF_P = kWarps * WARPB;
     static constexpr int PBYTES = (kWarps * NT * PROWB > G * D * 4 ? kWarps * NT * PROWB : G * D * 4);
     static constexpr int OFF_QH = OFF_P + ((PBYTES + 15) / 16) * 16;
     static constexpr int OFF_NQ = OFF_QH + 2 * G * D * 2;
     static constexpr int OFF_F = OFF_NQ + G * 20 * 4;       // norms padded to 20 floats a head
     static constexpr int OFF_BAR = OFF_F + ((G * 4 + 15) / 16) * 16;
-    static constexpr size_t SMEM = OFF_BAR + kWarps * kStages * 8 + 128;
+    static constexpr size_t SMEM = OFF_BAR + kWarps * STAGES * 8 + 128;
 };
 
 __device__ __forceinline__ int prow(int n) { return 32 * n + (n >= 4 ? 16 : 0); }
@@ -211,12 +214,12 @@ __device__ __forceinline__ int prow(int n) { return 32 * n + (n >= 4 ? 16 : 0); 
 // i.e. value group g of 4 tokens.  The -u terms enter both contractions as a second
 // fp16 MMA into the same accumulators ((code - u) s = s code + s (-u)).  No
 // witnesses are read and no bound is formed.
-// Tier B with at most 4 heads per KV head fits 4 CTAs per SM (128 registers, stages
-// without witnesses): more warps to hide the latency of the Philox rounds.
+// At most 4 heads per KV head (or d = 64) fit 4 CTAs per SM (at most 128 registers).
 template <int D, int G, bool DITHER>
-__global__ void __launch_bounds__(kWarps * 32, (D < 128 || (DITHER && G <= 4)) ? 4 : 3)
+__global__ void __launch_bounds__(kWarps * 32, (D < 128 || G <= 4) ? 4 : 3)
 int8_decode_kernel(const Int8Args a) {
     using C = I8<D, G, DITHER>;
+    constexpr int kStages = C::STAGES;
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char* sPm = smem + C::OFF_P;                                // [warp][NT] P^T staging
     __half* sQh = reinterpret_cast<__half*>(smem + C::OFF_QH);          // [2G][D]: row 2h hi, 2h + 1 lo
