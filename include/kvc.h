@@ -303,6 +303,13 @@ int kvc_next_positions(kvc_t h, int32_t* h_out);
  * gave up) and clears it. */
 int kvc_device_status(kvc_t h, kvc_stream_t stream, int32_t* h_status);
 
+/* Health check of the failure path: enqueues one CTA that waits, with the same
+ * bounded wait the kernels use for their copies, on a barrier that nothing
+ * signals.  The wait gives up after its bound (about one second), sets bit 1 of
+ * the device error word and returns; nothing faults and the context stays
+ * usable.  A following kvc_device_status reports the bit (and clears it). */
+int kvc_check_wait_path(kvc_t h, kvc_stream_t stream);
+
 /* Host only.  Rows of a stored prefill that a new query can reuse ([PREFIX]
  * "先看一次歷史編輯", "查詢流程與快取所有權", "為什麼滑窗部分命中必須回退"):
  * cut = length of the longest contiguous common prefix of old and new IDs,

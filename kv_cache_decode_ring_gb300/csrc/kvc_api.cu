@@ -5,6 +5,7 @@
 #include <vector>
 #include <new>
 
+#include "async_copy.h"
 #include "kvc_internal.h"
 
 namespace kvc {
@@ -18,6 +19,18 @@ cudaError_t launch_chunk(kvc_handle* h, const void* q, void* out, int n, cudaStr
 namespace {
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// One CTA waits on an mbarrier that nothing arrives at: the bounded wait gives up and
+// flags the error word, as a kernel whose copy never lands would.
+__global__ void wait_path_kernel(uint32_t* hdr) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && !mbar_wait(&bar, 0)) atomicOr(hdr, kErrWait);
+}
 
 }  // namespace
 
@@ -553,6 +566,12 @@ int kvc_device_status(kvc_t h, kvc_stream_t stream, int32_t* h_status) {
     if (cudaStreamSynchronize(st) != cudaSuccess) return KVC_ERR_CUDA;
     *h_status = (int32_t)word;
     return KVC_OK;
+}
+
+int kvc_check_wait_path(kvc_t h, kvc_stream_t stream) {
+    if (!h) return KVC_ERR_ARG;
+    wait_path_kernel<<<1, 32, 0, S_(stream)>>>(at<uint32_t>(h, h->L.hdr));
+    return cudaGetLastError() == cudaSuccess ? KVC_OK : KVC_ERR_CUDA;
 }
 
 int kvc_prefix_cut(const int64_t* h_old_ids, int32_t n_old, const int64_t* h_new_ids, int32_t n_new,

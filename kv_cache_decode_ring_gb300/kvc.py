@@ -52,7 +52,8 @@ EXPORTED = ["kvc_state_bytes", "kvc_create", "kvc_destroy", "kvc_append", "kvc_a
             "kvc_next_positions", "kvc_device_status", "kvc_prefix_cut", "kvc_strerror",
             "kvc_int8_block_risk", "kvc_int8_gate", "kvc_int8_restore",
             "kvc_pstore_create", "kvc_pstore_destroy", "kvc_pstore_insert", "kvc_pstore_lookup",
-            "kvc_store_save", "kvc_store_load", "kvc_store_load_batch", "kvc_set_request_id"]
+            "kvc_store_save", "kvc_store_load", "kvc_store_load_batch", "kvc_set_request_id",
+            "kvc_check_wait_path"]
 
 _lock = threading.Lock()
 _lib = None
@@ -99,6 +100,7 @@ def lib() -> ctypes.CDLL:
                 "kvc_store_load": [P, i32, i32, i32, P],
                 "kvc_store_load_batch": [P, i32, P, P, P, P],
                 "kvc_set_request_id": [P, i32, ctypes.c_uint32, P],
+                "kvc_check_wait_path": [P, P],
             }
             for name, args in sig.items():
                 fn = getattr(L, name)
@@ -266,6 +268,10 @@ def kvc_device_status(h, stream=None) -> int:
     s = ctypes.c_int32(0)
     _check(lib().kvc_device_status(h, _stream(stream), ctypes.byref(s)), "kvc_device_status")
     return s.value
+
+
+def kvc_check_wait_path(h, stream=None) -> None:
+    _check(lib().kvc_check_wait_path(h, _stream(stream)), "kvc_check_wait_path")
 
 
 def kvc_prefix_cut(old_ids: Sequence[int], new_ids: Sequence[int], ring: bool = False) -> int:
