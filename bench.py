@@ -44,11 +44,11 @@ CSRC = os.path.join(ROOT, "kv_cache_decode_ring_gb300", "csrc")
 # JSON line reports null.
 TRAFFIC_PER_BYTE = {
     "full-cache-mha": ("decode_fast.cu", "acb55fd33938d9cc", (268701696 + 4940800) / 268632064),
-    "sliding-window-gqa": ("decode_gqa.cu", "030ffef84b3a53a4", (268098816 + 4223232) / 268148736),
-    "int8-witness": ("int8.cu", "c1faf9d15978e661", (302886144 + 3227648) / 302551040),
-    "bf16-at-int8-shape": ("decode_gqa.cu", "030ffef84b3a53a4", (537017344 + 4274176) / 536907776),
+    "sliding-window-gqa": ("decode_gqa.cu", "dbb9e91011defcc8", (268103168 + 3271424) / 268148736),
+    "int8-witness": ("int8.cu", "a8334376cda3c6f8", (302861056 + 3304960) / 302551040),
+    "bf16-at-int8-shape": ("decode_gqa.cu", "dbb9e91011defcc8", (536983552 + 3351808) / 536907776),
     "prefix-reuse": ("chunk.cu", "608963104f909744", (31902208 + 42240) / 22773760),
-    "int8-dither": ("int8.cu", "c1faf9d15978e661", (269326080 + 3284224) / 268996608),
+    "int8-dither": ("int8.cu", "a8334376cda3c6f8", (269327104 + 3159296) / 268996608),
 }
 
 
