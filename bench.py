@@ -767,6 +767,20 @@ def oracle_sample(w, seconds: float, threads: int, heads_per_call=None, problem=
 
 # ----------------------------------------------------------------------------- main
 
+def replica_aggregate(ms_local, units_local, dist=None, device="cpu"):
+    """Whole-job timing of replicas: (the slowest rank's milliseconds, the units all ranks
+    processed).  Every rank runs its own copy of the workload (weak scaling, no data-path
+    collective); only these two numbers cross ranks.  `dist` is torch.distributed with an
+    initialised process group (NCCL: device "cuda"; gloo: "cpu"), or None for one process."""
+    import torch
+    t = torch.tensor([float(ms_local)], device=device, dtype=torch.float64)
+    u = torch.tensor([float(units_local)], device=device, dtype=torch.float64)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -840,13 +854,8 @@ def main():
     sampler.stop()
     ms_total = t0e.elapsed_time(t1e)
     attn_ms = [a.elapsed_time(b) for a, b in ev]
-    times = torch.tensor([ms_total], device="cuda", dtype=torch.float64)
-    tot_units = torch.tensor([float(units)], device="cuda", dtype=torch.float64)
-    if dist is not None:
-        dist.all_reduce(times, op=dist.ReduceOp.MAX)
-        dist.all_reduce(tot_units, op=dist.ReduceOp.SUM)
-    ms_total = float(times.item())
-    value = float(tot_units.item()) / (ms_total / 1e3) / scale
+    ms_total, all_units = replica_aggregate(ms_total, units, dist, "cuda")
+    value = all_units / (ms_total / 1e3) / scale
     steps_per_s = K / (ms_total / 1e3)
 
     # roofline of the decode-attention call
@@ -872,12 +881,8 @@ def main():
             bench.e2e_step()
         b.record()
         barrier()
-        ems = torch.tensor([a.elapsed_time(b)], device="cuda", dtype=torch.float64)
-        eut = torch.tensor([float(eu)], device="cuda", dtype=torch.float64)
-        if dist is not None:
-            dist.all_reduce(ems, op=dist.ReduceOp.MAX)
-            dist.all_reduce(eut, op=dist.ReduceOp.SUM)
-        e2e = {"value": round(float(eut.item()) / (float(ems.item()) / 1e3) / scale, 2), "unit": bench.unit,
+        ems, eut = replica_aggregate(a.elapsed_time(b), eu, dist, "cuda")
+        e2e = {"value": round(eut / (ems / 1e3) / scale, 2), "unit": bench.unit,
                "h2d_bytes_per_step": hb, "d2h_bytes_per_step": db, "steps": Ke}
 
     cpu = None
