@@ -205,28 +205,84 @@ class DecodeBench:
         self.done += 1
         return extra
 
+    # ---- end to end through the public API, with host buffers -----------------
+    # Every step uploads its inputs from pinned host memory and downloads its output;
+    # two device slots for each and a copy stream let one step's copies overlap its
+    # neighbours' kernels.  Subclasses say which host inputs step n uses and how a step
+    # computes from device inputs into a given output.
     def e2e_setup(self):
         import torch
         self.hq = [t.cpu().pin_memory() for t in self.q]
         self.hk = [t.cpu().pin_memory() for t in self.k]
         self.hv = [t.cpu().pin_memory() for t in self.v]
-        self.hout = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
-        self.dq = torch.empty_like(self.q[0])
-        self.dk = torch.empty_like(self.k[0])
-        self.dv = torch.empty_like(self.v[0])
-        return sum(t.numel() * t.element_size() for t in (self.hq[0], self.hk[0], self.hv[0])), \
-            self.hout.numel() * self.hout.element_size()
+        return self.e2e_init([self.hq[0], self.hk[0], self.hv[0]], self.out)
+
+    def e2e_host_inputs(self, n):
+        j = n % self.CYCLE
+        return self.hq[j], self.hk[j], self.hv[j]
+
+    def e2e_compute(self, dev, out):
+        q, k, v = dev
+        self.before_step()
+        self.cache.append(k, v)
+        keep = self.out
+        self.out = out
+        self.decode(q)
+        self.out = keep
+
+    def e2e_init(self, host_example, out_example):
+        import torch
+        self.e2e_dev = [[torch.empty(t.shape, dtype=t.dtype, device="cuda") for t in host_example] for _ in range(2)]
+        self.e2e_dout = [torch.empty_like(out_example) for _ in range(2)]
+        self.e2e_hout = [torch.empty(out_example.shape, dtype=out_example.dtype).pin_memory() for _ in range(2)]
+        self.copy_stream = torch.cuda.Stream()
+        self.ev_in = [torch.cuda.Event() for _ in range(2)]      # slot's inputs uploaded
+        self.ev_used = [torch.cuda.Event() for _ in range(2)]    # slot's inputs consumed, output written
+        self.ev_read = [torch.cuda.Event() for _ in range(2)]    # slot's output downloaded
+        self.e2e_next = None                                     # step whose inputs are in flight
+        return sum(t.numel() * t.element_size() for t in host_example), \
+            self.e2e_hout[0].numel() * self.e2e_hout[0].element_size()
+
+    def _upload(self, n):
+        """Copy stream: the inputs of step n into slot n % 2 once that slot is free."""
+        import torch
+        s = n % 2
+        with torch.cuda.stream(self.copy_stream):
+            self.copy_stream.wait_event(self.ev_used[s])
+            for dst, src in zip(self.e2e_dev[s], self.e2e_host_inputs(n)):
+                dst.copy_(src, non_blocking=True)
+            self.ev_in[s].record(self.copy_stream)
 
     def e2e_step(self):
-        j = self.done % self.CYCLE
-        self.before_step()
-        self.dq.copy_(self.hq[j], non_blocking=True)
-        self.dk.copy_(self.hk[j], non_blocking=True)
-        self.dv.copy_(self.hv[j], non_blocking=True)
-        self.cache.append(self.dk, self.dv)
-        self.decode(self.dq)
-        self.hout.copy_(self.out, non_blocking=True)
+        """One step: its inputs uploaded, its kernels, its output downloaded.  The next
+        step's upload is issued now, so it overlaps this step's kernels, and this step's
+        download overlaps the next step's kernels."""
+        import torch
+        n = self.done
+        s = n % 2
+        if self.e2e_next != n:
+            self._upload(n)
+        self._upload(n + 1)
+        self.e2e_next = n + 1
+        cur = torch.cuda.current_stream()
+        cur.wait_event(self.ev_in[s])
+        cur.wait_event(self.ev_read[s])                          # the slot's previous output downloaded
+        self.e2e_compute(self.e2e_dev[s], self.e2e_dout[s])
+        self.ev_used[s].record(cur)
+        with torch.cuda.stream(self.copy_stream):
+            self.copy_stream.wait_event(self.ev_used[s])
+            self.e2e_hout[s].copy_(self.e2e_dout[s], non_blocking=True)
+            self.ev_read[s].record(self.copy_stream)
         self.done += 1
+
+    def e2e_flush(self):
+        """The current stream waits for the last download; a pending upload is dropped
+        (the next step uploads its own inputs again)."""
+        import torch
+        done = torch.cuda.Event()
+        done.record(self.copy_stream)
+        torch.cuda.current_stream().wait_event(done)
+        self.e2e_next = None
 
 
 class FullCacheBench(DecodeBench):
@@ -606,21 +662,15 @@ class ChunkBench(DecodeBench):
         return 0
 
     def e2e_setup(self):
-        import torch
         self.hq, self.hk, self.hv = (t.cpu().pin_memory() for t in (self.q, self.k, self.v))
-        self.hout = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
-        self.dq, self.dk, self.dv = (torch.empty_like(t) for t in (self.q, self.k, self.v))
-        return sum(t.numel() * t.element_size() for t in (self.hq, self.hk, self.hv)), \
-            self.hout.numel() * self.hout.element_size()
+        return self.e2e_init([self.hq, self.hk, self.hv], self.out)
 
-    def e2e_step(self):
+    def e2e_host_inputs(self, n):
+        return self.hq, self.hk, self.hv
+
+    def e2e_compute(self, dev, out):
         self.cache.trim(self.cuts)
-        self.dq.copy_(self.hq, non_blocking=True)
-        self.dk.copy_(self.hk, non_blocking=True)
-        self.dv.copy_(self.hv, non_blocking=True)
-        self.cache.chunk(self.dq, self.dk, self.dv, self.out)
-        self.hout.copy_(self.out, non_blocking=True)
-        self.done += 1
+        self.cache.chunk(dev[0], dev[1], dev[2], out)
 
     def reset(self):
         import torch
@@ -701,14 +751,9 @@ class ChunkStoreBench(ChunkBench):
         self.done += 1
         return 0
 
-    def e2e_step(self):
+    def e2e_compute(self, dev, out):
         self.reuse()
-        self.dq.copy_(self.hq, non_blocking=True)
-        self.dk.copy_(self.hk, non_blocking=True)
-        self.dv.copy_(self.hv, non_blocking=True)
-        self.cache.chunk(self.dq, self.dk, self.dv, self.out)
-        self.hout.copy_(self.out, non_blocking=True)
-        self.done += 1
+        self.cache.chunk(dev[0], dev[1], dev[2], out)
 
     def extra_report(self, peak_hbm):
         ms = [a.elapsed_time(b) for a, b in self.load_ev]
@@ -871,6 +916,7 @@ def main():
         Ke = min(K, 400)
         for i in range(3):
             bench.e2e_step()
+        bench.e2e_flush()
         bench.reset()
         barrier()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -879,6 +925,7 @@ def main():
         for i in range(Ke):
             eu += bench.units()
             bench.e2e_step()
+        bench.e2e_flush()
         b.record()
         barrier()
         ems, eut = replica_aggregate(a.elapsed_time(b), eu, dist, "cuda")
