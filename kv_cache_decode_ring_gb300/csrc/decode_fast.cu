@@ -311,8 +311,6 @@ bool fast_decode_supported(const DecodeArgs& a) {
            a.split == kSplitKeys;
 }
 
-int fast_split_keys() { return kSplitKeys; }
-
 cudaError_t launch_decode_fast(const DecodeArgs& a, cudaStream_t st) {
     // grid.x covers the longest window the cache can hold; CTAs beyond a request's
     // splits exit at once, and the grid-stride loop keeps any length covered
