@@ -22,8 +22,8 @@ from the full-precision backing store, zero its witnesses) is held exact as
 well, with residual 0 and witness 0.
 
 Tier B ([WITCERT], the subtractive-dither paragraph, and "SGLang 生产级落地与闭环门控修复"
-for the counter): codes rint(x/s + u) with a Philox dither u per element, read back
-as (code - u) s; no witnesses.  The probabilistic certificate of this tier needs a
+for the counter): key codes rint(x/s + u) with a Philox dither u per element, read
+back as (code - u) s; values keep the plain quantizer; no witnesses.  The probabilistic certificate of this tier needs a
 failure budget and a concentration formula the page does not give, so the oracle
 states no bound for it.
 
@@ -274,25 +274,25 @@ class DecodeOracle:
         self.request_ids[b] = int(rid) & 0xFFFFFFFF
 
     def dither(self, b, h):
-        """Tier B: u(positions, tensor) -> [n, d] fp32 dithers of (request b, KV head h), else None."""
+        """Tier B: u(p0, n) -> [n, d] fp32 key dithers of (request b, KV head h), else None."""
         if self.quant != "int8-dither":
             return None
         key, rid, layer, d = self.dither_key, self.request_ids[b], self.layer, self.d
 
-        def u(p0, n, tensor):
-            return nm.dither_values(nm.dither_rows(key, rid, layer, h, p0, n, d, tensor))
+        def u(p0, n):
+            return nm.dither_values(nm.dither_rows(key, rid, layer, h, p0, n, d))
         return u
 
     def quantized_block(self, b, h, blk):
         """(sK, codesK [16,d], sV, codesV, wit bits [16,16]) of one complete block
-        (Tier B: dithered codes and no witnesses, None)."""
+        (Tier B: dithered key codes, plain value codes, no witnesses: None)."""
         lo = blk * QBLOCK
         K = np.stack([self.hk[b][p][h] for p in range(lo, lo + QBLOCK)])
         V = np.stack([self.hv[b][p][h] for p in range(lo, lo + QBLOCK)])
         u = self.dither(b, h)
         if u is not None:
-            sK, cK = nm.quantize_block_dither(K, u(lo, QBLOCK, 0))
-            sV, cV = nm.quantize_block_dither(V, u(lo, QBLOCK, 1))
+            sK, cK = nm.quantize_block_dither(K, u(lo, QBLOCK))
+            sV, cV = nm.quantize_block(V)
             return sK, cK, sV, cV, None
         sK, cK = nm.quantize_block(K)
         sV, cV = nm.quantize_block(V)
@@ -345,9 +345,9 @@ def int8_rows(K, V, p0, nfull, restored=(), dither=None):
     and witness values; the exact tail rows and restored blocks with residual 0 and
     witness 0 ([WITCERT] "频带酉性与双层证书"; "SGLang 生产级落地与闭环门控修复").
 
-    Tier B ([WITCERT], the subtractive-dither paragraph): ``dither(p0, n, tensor)``
-    gives the fp32 dithers u of n rows from position p0 (tensor 0 keys, 1 values);
-    codes are rint(x/s + u) and the rows read back as (code - u) s, exact in fp64.
+    Tier B ([WITCERT], the subtractive-dither paragraph): ``dither(p0, n)`` gives the
+    fp32 key dithers u of n rows from position p0; key codes are rint(x/s + u) and the
+    keys read back as (code - u) s, exact in fp64; values keep the plain quantizer.
     There are no witnesses then (the returned witness values are None).
     """
     n, d = K.shape
@@ -363,11 +363,11 @@ def int8_rows(K, V, p0, nfull, restored=(), dither=None):
             continue
         sl = slice(r0, r0 + QBLOCK)
         if dither is not None:
-            uK, uV = dither(p0 + r0, QBLOCK, 0), dither(p0 + r0, QBLOCK, 1)
+            uK = dither(p0 + r0, QBLOCK)
             sK, cK = nm.quantize_block_dither(K[sl], uK)
-            sV, cV = nm.quantize_block_dither(V[sl], uV)
+            sV, cV = nm.quantize_block(V[sl])
             Kd[sl] = (cK.astype(np.float64) - uK.astype(np.float64)) * np.float64(sK)
-            Vd[sl] = (cV.astype(np.float64) - uV.astype(np.float64)) * np.float64(sV)
+            Vd[sl] = cV.astype(np.float64) * np.float64(sV)
             R[sl] = K[sl].astype(np.float64) - Kd[sl]
             continue
         sK, cK = nm.quantize_block(K[sl])

@@ -66,7 +66,7 @@ def lib():
                 "orc_philox4x32_10": (None, [P, P, P]),
                 "orc_quantize_block_dither": (f32, [P, P, i64, P]),
                 "orc_dither_rows": (None, [P, ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32, i64, i64, i32,
-                                           i32, P]),
+                                           P]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -232,37 +232,30 @@ def philox4x32_10(ctr, key) -> np.ndarray:
 
 
 # Subtractive-dither streams ([WITCERT] Tier B: Philox keyed on the five-tuple
-# request, layer, KV head, token, channel).  The counter of one call is
-#   (position t, group + 256 * tensor, KV head + 65536 * layer, request ID)
-# with tensor 0 for keys and 1 for values, under the cache's 64-bit key.  A call
-# gives 16 bytes r (word w holds bytes 4w .. 4w + 3, least significant first);
-# a channel's dither is u = r / 256 - 1/2.
-#   keys:   group j covers channels 16 j .. 16 j + 15, byte i -> channel 16 j + i
-#   values: group j < 8 covers the channels c = 8 i + j,  byte i -> channel 8 i + j
-def dither_bytes(key, request, layer, kv_head, position, d, tensor) -> np.ndarray:
-    """The d dither bytes of one row (K: tensor 0, V: tensor 1) as uint8, one Philox call
-    at a time in Python (the plain statement of the mapping above)."""
+# request, layer, KV head, token, channel).  Keys are dithered; values keep the plain
+# block quantizer (the tier's certificate concerns the logits, i.e. the keys, and the
+# page's counter has no key/value field).  The counter of one call is
+#   (position t, channel group, KV head + 65536 * layer, request ID)
+# under the cache's 64-bit key; group j covers channels 16 j .. 16 j + 15, and byte i of
+# the call (word i/4, least significant byte first) is channel 16 j + i; a channel's
+# dither is u = r / 256 - 1/2.
+def dither_bytes(key, request, layer, kv_head, position, d) -> np.ndarray:
+    """The d key dither bytes of one row as uint8, one Philox call at a time in Python
+    (the plain statement of the mapping above)."""
     out = np.empty(d, dtype=np.uint8)
     c2 = (int(kv_head) + 65536 * int(layer)) & 0xFFFFFFFF
-    if tensor == 0:
-        for j in range(d // 16):
-            w = philox4x32_10([position, j, c2, request], key)
-            out[16 * j:16 * j + 16] = w.view(np.uint8)
-    else:
-        for j in range(8):
-            w = philox4x32_10([position, j + 256, c2, request], key)
-            by = w.view(np.uint8)
-            for i in range(d // 8):
-                out[8 * i + j] = by[i]
+    for j in range(d // 16):
+        w = philox4x32_10([position, j, c2, request], key)
+        out[16 * j:16 * j + 16] = w.view(np.uint8)
     return out
 
 
-def dither_rows(key, request, layer, kv_head, p0, n, d, tensor) -> np.ndarray:
+def dither_rows(key, request, layer, kv_head, p0, n, d) -> np.ndarray:
     """dither_bytes of rows p0 .. p0+n-1, [n, d] uint8 (``orc_dither_rows``)."""
     k = np.ascontiguousarray(np.asarray(key, dtype=np.uint64).astype(np.uint32))
     out = np.empty((n, d), dtype=np.uint8)
     lib().orc_dither_rows(_p(k), int(request) & 0xFFFFFFFF, int(layer), int(kv_head), int(p0), int(n), int(d),
-                          int(tensor), _p(out))
+                          _p(out))
     return out
 
 

@@ -306,29 +306,22 @@ void orc_philox4x32_10(const uint32_t* ctr, const uint32_t* key, uint32_t* out)
 }
 
 /*
- * Dither bytes of n rows at positions p0 .. p0+n-1 of one (request, layer, KV head)
- * and tensor (0 = keys, 1 = values), out[n][d].  One Philox call per (position,
- * group) with counter (position, group + 256 tensor, KV head + 65536 layer,
- * request); byte i of the call (word i/4, least significant byte first) is the
- * dither of channel 16 group + i for keys (group < d/16) and of channel
- * 8 i + group for values (group < 8).
+ * Key dither bytes of n rows at positions p0 .. p0+n-1 of one (request, layer, KV
+ * head), out[n][d].  One Philox call per (position, group of 16 channels) with the
+ * five-tuple counter (position, group, KV head + 65536 layer, request); byte i of the
+ * call (word i/4, least significant byte first) is the dither of channel 16 group + i.
  */
 void orc_dither_rows(const uint32_t* key, uint32_t request, uint32_t layer, uint32_t kv_head, int64_t p0,
-                     int64_t n, int d, int tensor, uint8_t* out)
+                     int64_t n, int d, uint8_t* out)
 {
     const uint32_t c2 = kv_head + 65536u * layer;
     for (int64_t r = 0; r < n; ++r) {
         uint8_t* row = out + r * d;
-        const int groups = tensor == 0 ? d / 16 : 8;
-        for (int j = 0; j < groups; ++j) {
-            const uint32_t ctr[4] = {(uint32_t)(p0 + r), (uint32_t)j + 256u * (uint32_t)tensor, c2, request};
+        for (int j = 0; j < d / 16; ++j) {
+            const uint32_t ctr[4] = {(uint32_t)(p0 + r), (uint32_t)j, c2, request};
             uint32_t w[4];
             orc_philox4x32_10(ctr, key, w);
-            for (int i = 0; i < 16; ++i) {
-                const uint8_t byte = (uint8_t)(w[i / 4] >> (8 * (i % 4)));
-                if (tensor == 0) row[16 * j + i] = byte;
-                else if (8 * i + j < d) row[8 * i + j] = byte;
-            }
+            for (int i = 0; i < 16; ++i) row[16 * j + i] = (uint8_t)(w[i / 4] >> (8 * (i % 4)));
         }
     }
 }

@@ -39,26 +39,23 @@ def test_philox_known_answers(case):
 def test_dither_rows_state_the_mapping():
     key = (0x12345678, 0x9abcdef0)
     for d in (64, 128):
-        for tensor in (0, 1):
-            rows = nm.dither_rows(key, 7, 3, 5, 1000, 6, d, tensor)
-            for r in range(6):
-                assert np.array_equal(rows[r], nm.dither_bytes(key, 7, 3, 5, 1000 + r, d, tensor))
-    # the key channels: byte i of call (t, group j) is channel 16 j + i; values: channel 8 i + j
+        rows = nm.dither_rows(key, 7, 3, 5, 1000, 6, d)
+        for r in range(6):
+            assert np.array_equal(rows[r], nm.dither_bytes(key, 7, 3, 5, 1000 + r, d))
+    # byte i of the call for (token 42, group 1, KV head 5 of layer 3, request 7) is channel 16 + i
     w = nm.philox4x32_10([42, 1, 5 + 65536 * 3, 7], key).view(np.uint8)
-    assert np.array_equal(nm.dither_bytes(key, 7, 3, 5, 42, 128, 0)[16:32], w)
-    w = nm.philox4x32_10([42, 256 + 3, 5 + 65536 * 3, 7], key).view(np.uint8)
-    assert np.array_equal(nm.dither_bytes(key, 7, 3, 5, 42, 128, 1)[3::8], w)
+    assert np.array_equal(nm.dither_bytes(key, 7, 3, 5, 42, 128)[16:32], w)
 
 
 def test_dither_streams_are_distinct_and_uniform():
     key = (1, 2)
-    base = nm.dither_rows(key, 0, 0, 0, 0, 64, 128, 0)
-    # every field of the five-tuple (and the tensor) selects another stream
-    for other in (nm.dither_rows(key, 1, 0, 0, 0, 64, 128, 0), nm.dither_rows(key, 0, 1, 0, 0, 64, 128, 0),
-                  nm.dither_rows(key, 0, 0, 1, 0, 64, 128, 0), nm.dither_rows(key, 0, 0, 0, 1, 64, 128, 0),
-                  nm.dither_rows(key, 0, 0, 0, 0, 64, 128, 1), nm.dither_rows((1, 3), 0, 0, 0, 0, 64, 128, 0)):
+    base = nm.dither_rows(key, 0, 0, 0, 0, 64, 128)
+    # every field of the five-tuple (and the key) selects another stream
+    for other in (nm.dither_rows(key, 1, 0, 0, 0, 64, 128), nm.dither_rows(key, 0, 1, 0, 0, 64, 128),
+                  nm.dither_rows(key, 0, 0, 1, 0, 64, 128), nm.dither_rows(key, 0, 0, 0, 1, 64, 128),
+                  nm.dither_rows((1, 3), 0, 0, 0, 0, 64, 128)):
         assert (other != base).mean() > 0.99 - 1 / 256 - 0.01
-    big = nm.dither_rows(key, 9, 0, 2, 0, 2048, 128, 0).reshape(-1)        # 262144 bytes
+    big = nm.dither_rows(key, 9, 0, 2, 0, 2048, 128).reshape(-1)           # 262144 bytes
     hist = np.bincount(big, minlength=256)
     chi2 = ((hist - big.size / 256) ** 2 / (big.size / 256)).sum()
     assert chi2 < 255 + 6 * math.sqrt(2 * 255)                              # about 6 sigma
@@ -89,7 +86,7 @@ def test_subtractive_dither_error_is_bounded_uniform_and_data_independent():
             k[0, 0] = 127.0                                   # amax = 127 s with s = 1/8
             x = ((k + np.float32(frac)) / np.float32(8.0)).astype(np.float32)
             x[0, 0] = np.float32(127.0 / 8.0)
-            u = nm.dither_values(nm.dither_rows(key, blk, 0, 0, 16 * blk, 16, 128, 0))
+            u = nm.dither_values(nm.dither_rows(key, blk, 0, 0, 16 * blk, 16, 128))
             s, c = nm.quantize_block_dither(x, u)
             assert s == np.float32(127.0 / 8.0) / np.float32(127.0)
             xh = (c.astype(np.float64) - u.astype(np.float64)) * np.float64(s)
@@ -112,16 +109,16 @@ def test_tier_b_decode_is_attention_over_dequantized_rows():
     q = rng.standard_normal(d).astype(np.float32)
     key, rid, layer, h = (11, 12), 4, 2, 1
 
-    def u(p0, m, tensor):
-        return nm.dither_values(nm.dither_rows(key, rid, layer, h, p0, m, d, tensor))
+    def u(p0, m):
+        return nm.dither_values(nm.dither_rows(key, rid, layer, h, p0, m, d))
     res = int8_decode_one(q, K, V, 0, n - 1, 0, (n // QBLOCK) * QBLOCK, (), u)
     Kd, Vd = K.astype(np.float64).copy(), V.astype(np.float64).copy()
     for blk in range(n // QBLOCK):
         sl = slice(blk * QBLOCK, (blk + 1) * QBLOCK)
-        sK, cK = nm.quantize_block_dither(K[sl], u(blk * QBLOCK, QBLOCK, 0))
-        sV, cV = nm.quantize_block_dither(V[sl], u(blk * QBLOCK, QBLOCK, 1))
-        Kd[sl] = (cK - u(blk * QBLOCK, QBLOCK, 0).astype(np.float64)) * float(sK)
-        Vd[sl] = (cV - u(blk * QBLOCK, QBLOCK, 1).astype(np.float64)) * float(sV)
+        sK, cK = nm.quantize_block_dither(K[sl], u(blk * QBLOCK, QBLOCK))
+        sV, cV = nm.quantize_block(V[sl])                  # values: the plain quantizer
+        Kd[sl] = (cK - u(blk * QBLOCK, QBLOCK).astype(np.float64)) * float(sK)
+        Vd[sl] = cV * float(sV)
     lg = Kd @ q.astype(np.float64) / math.sqrt(d)
     p = np.exp(lg - lg.max())
     assert np.allclose(res["out"], (p[:, None] * Vd).sum(0) / p.sum(), rtol=1e-12, atol=1e-12)
