@@ -102,16 +102,15 @@ typedef struct {
                           /* KVC_QUANT_INT8_DITHER (Tier B, [WITCERT] subtractive-
                              dither paragraph; counter from "SGLang 生产级落地与闭环门控修复"):
                              the Philox4x32-10 key.  Same shapes and limits as
-                             KVC_QUANT_INT8, without witnesses: element (token t,
+                             KVC_QUANT_INT8, without witnesses: key element (token t,
                              channel c) of a block is stored as
                                code = clamp(rint(x/s + u), -127, 127), read as (code - u) s,
-                             u = r/256 - 1/2 with r a byte of the call
-                               Philox4x32-10(counter = (t, group + 256 tensor,
+                             u = r/256 - 1/2 with r byte c mod 16 of the call
+                               Philox4x32-10(counter = (t, c/16,
                                                        kv_head + 65536 layer_index,
                                                        request ID), key)
-                             (tensor 0 = keys: group c/16, byte c mod 16; tensor 1 =
-                             values: group c mod 8, byte c/8; byte i = bits 8(i mod 4)..
-                             of word i/4).  The request ID is b unless set by
+                             (byte i = bits 8(i mod 4) .. of word i/4); values keep the
+                             plain block quantizer.  The request ID is b unless set by
                              kvc_set_request_id. */
 } kvc_config;
 

@@ -64,29 +64,24 @@ __device__ __forceinline__ void store_pair(void* dst, size_t off, float y0, floa
 // fma computes it exactly; band norms are summed in index order with every
 // operation rounded toward +inf and stored as fp16 rounded up, so the witness
 // is never below the true residual norm.
-// Tier B ([WITCERT] subtractive dither): code = clamp(rint(x/s + u)), u = r/256 - 1/2
-// from the block's Philox calls (one per thread, bytes staged in shared memory:
-// keys take group c/16 byte c mod 16, values group c mod 8 byte c/8); no witnesses.
+// Tier B ([WITCERT] subtractive dither): key code = clamp(rint(x/s + u)), u = r/256 - 1/2
+// from the block's Philox calls (one per thread, bytes staged in shared memory; channel
+// c takes byte c mod 16 of group c/16); values keep the plain quantizer; no witnesses.
 // ---------------------------------------------------------------------------
 __device__ void quantize_block(const AppendArgs& a, const float* sK, const float* sV, float* red,
                                int b, int h, int blk) {
     const int d = a.d, n = kQBlock * d;
-    uint8_t* du = reinterpret_cast<uint8_t*>(red + 64);        // [2][16][d] dither bytes (Tier B)
+    uint8_t* du = reinterpret_cast<uint8_t*>(red + 64);        // [16][d] key dither bytes (Tier B)
     if (a.dither) {
-        const int kg = d / 16, per = kg + 8;
+        const int kg = d / 16;
         const uint32_t c2 = (uint32_t)h + a.layer_ctr, c3 = a.req_id[b];
-        for (int i = threadIdx.x; i < kQBlock * per; i += blockDim.x) {
-            const int t = i / per, j = i % per;
-            const bool val = j >= kg;
-            const uint32_t grp = val ? (uint32_t)(j - kg) + 256u : (uint32_t)j;
-            const uint4 r = philox4x32_10(make_uint4((uint32_t)(blk * kQBlock + t), grp, c2, c3), a.key0, a.key1);
+        for (int i = threadIdx.x; i < kQBlock * kg; i += blockDim.x) {
+            const int t = i / kg, j = i % kg;
+            const uint4 r = philox4x32_10(make_uint4((uint32_t)(blk * kQBlock + t), (uint32_t)j, c2, c3), a.key0,
+                                          a.key1);
             const uint32_t w[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                const uint8_t by = (uint8_t)(w[e >> 2] >> (8 * (e & 3)));
-                if (!val) du[t * d + 16 * j + e] = by;
-                else if (8 * e + (j - kg) < d) du[n + t * d + 8 * e + (j - kg)] = by;
-            }
+            for (int e = 0; e < 16; ++e) du[t * d + 16 * j + e] = (uint8_t)(w[e >> 2] >> (8 * (e & 3)));
         }
     }
     float mk = 0.f, mv = 0.f;
@@ -118,10 +113,7 @@ __device__ void quantize_block(const AppendArgs& a, const float* sK, const float
         int ck = 0, cv = 0;
         float yk = s_k != 0.f ? __fdiv_rn(sK[i], s_k) : 0.f;
         float yv = s_v != 0.f ? __fdiv_rn(sV[i], s_v) : 0.f;
-        if (a.dither) {                                  // u = r/256 - 1/2, exact in fp32
-            yk = __fadd_rn(yk, __fmaf_rn((float)du[i], 0.00390625f, -0.5f));
-            yv = __fadd_rn(yv, __fmaf_rn((float)du[n + i], 0.00390625f, -0.5f));
-        }
+        if (a.dither) yk = __fadd_rn(yk, __fmaf_rn((float)du[i], 0.00390625f, -0.5f));   // u = r/256 - 1/2, exact
         if (s_k != 0.f) ck = max(-127, min(127, __float2int_rn(yk)));
         if (s_v != 0.f) cv = max(-127, min(127, __float2int_rn(yv)));
         const int t = i / d, dim = i % d;
@@ -371,8 +363,8 @@ __global__ void trim_kernel(int32_t* next_pos, int32_t* pos, const Group g, int 
     if (threadIdx.x == 0) next_pos[b] = cut;
 }
 
-// rows of K and V in fp32, the reduction slots, and the dither bytes of Tier B
-size_t quant_smem(int d) { return (size_t)(2 * kQBlock * d + 64) * sizeof(float) + 2 * kQBlock * d; }
+// rows of K and V in fp32, the reduction slots, and the key dither bytes of Tier B
+size_t quant_smem(int d) { return (size_t)(2 * kQBlock * d + 64) * sizeof(float) + kQBlock * d; }
 
 // ---- paged caches: the block table ------------------------------------------
 constexpr int kTableBatch = 256;

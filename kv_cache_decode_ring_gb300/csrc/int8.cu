@@ -135,12 +135,6 @@ __device__ __forceinline__ void dither_to_half2(uint32_t r, uint32_t& lo, uint32
     hi = *reinterpret_cast<const uint32_t*>(&b);
 }
 
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-    uint32_t r;
-    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
-    return r;
-}
-
 // Philox4x32-10 with the round keys precomputed on the host (kernel parameters, so
 // each key xor folds into the three-input xor of its round).
 // One 32 x 32 -> 64-bit product per multiplier, as the round defines it.
@@ -207,12 +201,11 @@ struct I8 {
 
 __device__ __forceinline__ int prow(int n) { return 32 * n + (n >= 4 ? 16 : 0); }
 
-// DITHER: Tier B ([WITCERT] subtractive dither).  Each lane regenerates, with
-// Philox, exactly the dithers of the codes it holds: its keys are rows g and g + 8
-// of the block over the dims qd (D/4) .. + D/4 - 1, i.e. D/64 whole key groups of
-// 16 channels per row; its values are the channels = g (mod 8) of tokens 4 qd .. + 3,
-// i.e. value group g of 4 tokens.  The -u terms enter both contractions as a second
-// fp16 MMA into the same accumulators ((code - u) s = s code + s (-u)).  No
+// DITHER: Tier B ([WITCERT] subtractive dither on the keys).  Each lane regenerates,
+// with Philox, exactly the dithers of the key codes it holds: rows g and g + 8 of the
+// block over the dims qd (D/4) .. + D/4 - 1, i.e. D/64 whole groups of 16 channels
+// per row.  The -u terms enter the score contraction as a second fp16 MMA into the
+// same accumulator ((code - u) s = s code + s (-u)); values are plain codes.  No
 // witnesses are read and no bound is formed.
 // At most 4 heads per KV head (or d = 64) fit 4 CTAs per SM (at most 128 registers).
 template <int D, int G, bool DITHER>
@@ -596,34 +589,6 @@ int8_decode_kernel(const Int8Args a) {
                 codes_to_half2(vw[2 * mt + 1], a1, a3);       // dim 16 mt + 8 + g
     #pragma unroll
                 for (int nt = 0; nt < C::NT; ++nt) mma_f16(acc[mt][nt], a0, a1, a2, a3, pb[nt].x, pb[nt].y);
-            }
-            if constexpr (DITHER) {
-                // value group g of tokens 4 qd + k: byte f of call k is the dither of dim
-                // 8 f + g; a 4x4 byte transpose makes word f = (tokens 4 qd .. + 3 of dim 8 f + g),
-                // the order of the code word vw[f]
-                uint4 tk[4];
-    #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    tk[k] = philox_rk(make_uint4((uint32_t)(p0 + 4 * qd + k), 256u + (uint32_t)g, dc2, dc3), a.rk);
-    #pragma unroll
-                for (int w = 0; w < D / 32; ++w) {
-                    const uint32_t x0 = word_of(tk[0], w), x1 = word_of(tk[1], w);
-                    const uint32_t x2 = word_of(tk[2], w), x3 = word_of(tk[3], w);
-                    const uint32_t e01 = prmt(x0, x1, 0x5140), e23 = prmt(x2, x3, 0x5140);
-                    const uint32_t o01 = prmt(x0, x1, 0x7362), o23 = prmt(x2, x3, 0x7362);
-                    const uint32_t f[4] = {prmt(e01, e23, 0x5410), prmt(e01, e23, 0x7632),
-                                           prmt(o01, o23, 0x5410), prmt(o01, o23, 0x7632)};
-    #pragma unroll
-                    for (int hm = 0; hm < 2; ++hm) {          // m-tile mt = 2 w + hm: words f 4 w + 2 hm, + 1
-                        const int mt = 2 * w + hm;
-                        uint32_t a0, a1, a2, a3;
-                        dither_to_half2(f[2 * hm], a0, a2);
-                        dither_to_half2(f[2 * hm + 1], a1, a3);
-    #pragma unroll
-                        for (int nt = 0; nt < C::NT; ++nt)
-                            mma_f16(acc[mt][nt], a0, a1, a2, a3, pb[nt].x, pb[nt].y);
-                    }
-                }
             }
         }
         // this stage and the staging are free once every lane is past its reads
