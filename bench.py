@@ -43,12 +43,12 @@ CSRC = os.path.join(ROOT, "kv_cache_decode_ring_gb300", "csrc")
 # valid only while the kernel source is the one captured (sha256 prefix), otherwise the
 # JSON line reports null.
 TRAFFIC_PER_BYTE = {
-    "full-cache-mha": ("decode_fast.cu", "acb55fd33938d9cc", (268701696 + 4940800) / 268632064),
+    "full-cache-mha": ("decode_fast.cu", "9191b1eec481bc84", (268700160 + 4500992) / 268632064),
     "sliding-window-gqa": ("decode_gqa.cu", "dbb9e91011defcc8", (268103168 + 3271424) / 268148736),
-    "int8-witness": ("int8.cu", "a8334376cda3c6f8", (302861056 + 3304960) / 302551040),
+    "int8-witness": ("int8.cu", "f1d095edcb359003", (302861568 + 3226112) / 302551040),
     "bf16-at-int8-shape": ("decode_gqa.cu", "dbb9e91011defcc8", (536983552 + 3351808) / 536907776),
     "prefix-reuse": ("chunk.cu", "608963104f909744", (31902208 + 42240) / 22773760),
-    "int8-dither": ("int8.cu", "a8334376cda3c6f8", (269327104 + 3159296) / 268996608),
+    "int8-dither": ("int8.cu", "f1d095edcb359003", (269315584 + 3224832) / 268996608),
 }
 
 
