@@ -125,9 +125,15 @@ def rope_rotate(x, positions, base: float) -> np.ndarray:
     pos = np.asarray(positions, dtype=np.int64).reshape(-1)
     if pos.size != rows.shape[0]:
         pos = np.broadcast_to(pos.reshape(()) if pos.size == 1 else pos, x.shape[:-1]).reshape(-1)
-    cs = np.empty((rows.shape[0], d // 2, 2), dtype=np.float32)
-    for u in np.unique(pos):
-        cs[pos == u] = rope_cos_sin(base, d, int(u), 1)[0]
+    # each distinct position's {cos, sin} row once (a position's row does not depend on the
+    # others computed with it), then gathered per row
+    uniq, inv = np.unique(pos, return_inverse=True)
+    if uniq.size and uniq[-1] - uniq[0] < 4 * uniq.size + 64:
+        table = rope_cos_sin(base, d, int(uniq[0]), int(uniq[-1] - uniq[0]) + 1)[uniq - uniq[0]]
+    else:
+        table = np.stack([rope_cos_sin(base, d, int(u), 1)[0] for u in uniq]) if uniq.size else \
+            np.empty((0, d // 2, 2), dtype=np.float32)
+    cs = np.ascontiguousarray(table[inv.reshape(-1)], dtype=np.float32)
     y = np.empty_like(rows)
     if rows.shape[0]:
         lib().orc_rope_rotate(_p(rows), _p(cs), rows.shape[0], d, _p(y))

@@ -4,10 +4,13 @@ The oracle cannot redo every head, so sampled (request, head) outputs are checke
 one by one against fp64 attention over the generator's own rows (never the GPU
 cache), plus closed-form checks of positions that hold at any size.
 
-Full-cache MHA decode: B=32, H=32, d=128, contiguous 8192, context 4096 + 128 steps.
+Full-cache MHA decode: B=32, H=32, d=128, contiguous 8192, context 4096 + 128 steps;
+contiguous rows, or 16-slot pages behind a block table (as the paged bench lines).
 Sliding-window GQA decode: B=64, Hq=32, Hkv=8, d=128, ring W=4096, RoPE 10000,
 per-request lengths L_b uniform in [1, 32768]; and one request run from
 position 0 to 32767 through the not-full, exactly-full and first-replacement steps.
+INT8 with witnesses (before and after one gated fallback), and Tier B: B=8, Hq=32,
+Hkv=8, d=128, context 131072 + 16 steps.
 """
 import numpy as np
 import pytest
@@ -32,10 +35,12 @@ def _rows(model, x_np, positions):
     return model.stored_rows(x_np, positions).astype(np.float64)
 
 
-def test_full_cache_mha_sampled():
+@pytest.mark.parametrize("paged", [False, True], ids=["contiguous", "paged"])
+def test_full_cache_mha_sampled(paged):
     w = wl.full_cache_mha()
     ctx = w.extra["context"]
-    cache = kvc.Cache.from_workload(w)
+    # paged: exactly the 16-slot pages the 128 steps need, as many as the bench's pool per step
+    cache = kvc.Cache.from_workload(w, page_pool=w.batch * -(-(ctx + 128) // 16) if paged else 0)
     model = oracle_for(w)            # used for its row and query definitions only
     k, v = w.prefill_chunk(0, ctx, device="cuda")
     cache.append_rows(k, v)
@@ -55,7 +60,7 @@ def test_full_cache_mha_sampled():
         if s not in check_at:
             continue
         t = ctx + s
-        o = out.float().cpu()
+        o = out.cpu()                                            # bf16: its own rounding allowed
         for (b, h) in sample:
             K = np.concatenate([_rows(model, hk[(b, h)], np.arange(ctx)),
                                 _rows(model, np.stack(steps_k[(b, h)]), np.arange(ctx, t + 1))])
@@ -79,11 +84,12 @@ def _ring_positions_ok(pos_row, length, W):
     return np.array_equal(pos_row, want)
 
 
-def test_sliding_window_gqa_sampled():
+@pytest.mark.parametrize("paged", [False, True], ids=["ring", "paged-ring"])
+def test_sliding_window_gqa_sampled(paged):
     w = wl.sliding_window_gqa()
     W, Lmax = w.capacity, w.extra["max_len"]
     lengths = w.extra["lengths"]                   # current token at L_b - 1
-    cache = kvc.Cache.from_workload(w, max_position=Lmax)
+    cache = kvc.Cache.from_workload(w, max_position=Lmax, page_pool=w.batch * (W // 16) if paged else 0)
     model = oracle_for(w)
     rng = np.random.default_rng(1)
     bs = sorted(set([int(np.argmax(lengths)), int(np.argmin(lengths))] + list(rng.integers(0, 64, 6))))
@@ -107,7 +113,7 @@ def test_sliding_window_gqa_sampled():
         del k, v
     q, k1, v1 = w.step_qkv(0, device="cuda")
     cache.append(k1, v1)
-    out = cache.decode(q).float().cpu()
+    out = cache.decode(q).cpu()                 # bf16: its own rounding allowed
     g = w.n_q_heads // w.n_kv_heads
     pos = cache.export(kvc.KVC_EXPORT_POSITIONS)
     for b in range(64):
@@ -143,7 +149,7 @@ def test_one_request_through_the_ring_phases():
         hist_k.append(host(k1[0])); hist_v.append(host(v1[0]))
         if t not in check:
             continue
-        out = cache.decode(q).float().cpu()
+        out = cache.decode(q).cpu()
         lo = max(0, t - W + 1)
         for h in (0, 5):
             Kin = np.stack([x[h] for x in hist_k[lo:t + 1]])
@@ -188,7 +194,7 @@ def test_int8_witness_sampled():
             continue
         t = ctx + s
         nfull = (t + 1) // QBLOCK * QBLOCK
-        o, cm, tc = out.float().cpu(), cmax.cpu().numpy(), th.cpu().numpy()
+        o, cm, tc = out.cpu(), cmax.cpu().numpy(), th.cpu().numpy()       # o in bf16: its own rounding allowed
         for (b, h) in sample:
             Kin = np.concatenate(keep[(b, h)][0]); Vin = np.concatenate(keep[(b, h)][1])
             K = model.stored_rows(Kin, np.arange(t + 1))
@@ -217,15 +223,161 @@ def test_int8_witness_sampled():
     assert cache.device_status() == 0
 
 
-@pytest.mark.parametrize("windowed", [False, True], ids=["full", "w4096"])
-def test_prefix_reuse_sampled(windowed):
-    # 16 requests with an 8192-token prefix (Hq=32, Hkv=8, d=128, RoPE 10000), trimmed at seeded
-    # cuts in [0, 8191], then a 512-token suffix by kvc_chunk_attn; sampled rows against the oracle,
-    # and the stale-next_position control (planted on the CPU) must exceed the tolerance
+def test_int8_gated_sampled():
+    # The INT8 workload after one gated fallback, as the gated bench line runs it: a decode
+    # with per-token c_t, the block risk, the gate at tau = 0.2 with a budget of 1 % of the
+    # complete blocks, the restore from a bf16 backing store of the same rows; then decode
+    # steps with the restored blocks served exactly.  Risk (a max) and the selection are
+    # checked exactly, the outputs of the heads with the most and the fewest restored blocks
+    # against the oracle.
+    import copy
+    from oracle.model import QBLOCK, int8_decode_one, block_risk, gate_select
+    w = wl.int8_witness()
+    ctx, chunk = w.extra["context"], 8192
+    B, Hq, Hkv = w.batch, w.n_q_heads, w.n_kv_heads
+    g = Hq // Hkv
+    budget = int(0.01 * B * Hkv * (ctx // QBLOCK))
+    cache = kvc.Cache.from_workload(w, int8_exact_blocks=budget)
+    wb = copy.copy(w)
+    wb.quant = None
+    full = kvc.Cache.from_workload(wb)
+    for c in range(ctx // chunk):
+        k, v = w.prefill_chunk(c, chunk, device="cuda")
+        cache.append_rows(k, v)
+        full.append_rows(k, v)
+        del k, v
+    kf = torch.from_numpy(full.export(kvc.KVC_EXPORT_K).view(np.int16)).view(torch.bfloat16).cuda()
+    vf = torch.from_numpy(full.export(kvc.KVC_EXPORT_V).view(np.int16)).view(torch.bfloat16).cuda()
+    full.close()
+    steps = [w.step_qkv(s, device="cuda") for s in range(4)]
+    q, k1, v1 = steps[0]
+    cache.append(k1, v1)
+    S = cache.S
+    ct = torch.zeros((B, Hq, S), device="cuda")
+    cmax = torch.empty((B, Hq), device="cuda")
+    th = torch.empty((B, Hq), device="cuda")
+    cache.decode(q, None, cmax, th, ct)
+    risk = cache.block_risk(ct).cpu().numpy()
+    ct_h = ct.cpu().numpy()
+    del ct
+    t = ctx
+    for b in range(B):
+        for h in range(Hkv):
+            want = block_risk(ct_h[b, h * g:(h + 1) * g, :t + 1], t + 1)
+            assert np.array_equal(risk[b, h, :len(want)], want.astype(np.float32)), (b, h)
+            assert not risk[b, h, len(want):].any(), (b, h)           # incomplete blocks: no risk
+    sel = kvc.kvc_int8_gate(risk, 0.2, budget)
+    want = gate_select({(b, h): risk[b, h].astype(np.float64) for b in range(B) for h in range(Hkv)}, 0.2, budget)
+    assert [tuple(int(x) for x in r) for r in sel] == want
+    cache.restore(sel, kf, vf)
+    del kf, vf
+    torch.cuda.empty_cache()
+    restored = {(b, h): set() for b in range(B) for h in range(Hkv)}
+    for b, h, blk in want:
+        restored[(b, h)].add(blk)
+    counts = sorted(restored, key=lambda bh: (len(restored[bh]), bh))
+    sample = [counts[-1], counts[0]]
+    assert len(restored[sample[0]]) > 0
+    # the sampled heads' rows, regenerated from the workload's generator
+    Kin = {bh: [] for bh in sample}
+    Vin = {bh: [] for bh in sample}
+    for c in range(ctx // chunk):
+        k, v = w.prefill_chunk(c, chunk, device="cuda")
+        for (b, h) in sample:
+            Kin[(b, h)].append(host(k[b, h])); Vin[(b, h)].append(host(v[b, h]))
+        del k, v
+    model = oracle_for(w)
+    for s in range(4):
+        q, k1, v1 = steps[s]
+        if s:
+            cache.append(k1, v1)
+        out = cache.decode(q, None, cmax, th).cpu()             # bf16: its own rounding allowed
+        cm = cmax.cpu().numpy()
+        for (b, h) in sample:
+            Kin[(b, h)].append(host(k1[b, h])[None]); Vin[(b, h)].append(host(v1[b, h])[None])
+        if s not in (0, 3):
+            continue
+        t = ctx + s
+        nfull = (t + 1) // QBLOCK * QBLOCK
+        for (b, h) in sample:
+            K = model.stored_rows(np.concatenate(Kin[(b, h)]), np.arange(t + 1))
+            V = nm.bf16_to_f32(np.concatenate(Vin[(b, h)]))
+            for hq in (h * g, h * g + g - 1):
+                qr = model.query_rows(host(q[b, hq])[None], [t])[0]
+                r = int8_decode_one(qr, K, V, 0, t, 0, nfull, restored[(b, h)])
+                assert_close(out[b, hq][None], r["out"][None], "bf16", "gated s=%d b=%d h=%d" % (s, b, hq))
+                assert cm[b, hq] >= r["cmax"] * (1 - 1e-12) and cm[b, hq] <= r["cmax"] * (1 + 1e-5)
+    assert cache.device_status() == 0
+
+
+def test_int8_dither_sampled():
+    # Tier B at the INT8 workload's shape: the same tokens, keys quantized with the
+    # subtractive dither of the (position, channel group, KV head + 65536 layer, request ID)
+    # Philox counter, values plain, no witnesses; context 131072, then 16 one-token steps
+    from oracle.model import QBLOCK, int8_decode_one
+    w = wl.int8_dither()
+    ctx = w.extra["context"]
+    cache = kvc.Cache.from_workload(w)
+    model = oracle_for(w)
+    g = w.n_q_heads // w.n_kv_heads
+    sample = [(0, 0), (3, 7), (7, 2)]
+    keep = {bh: ([], []) for bh in sample}
+    chunk = 8192
+    for c in range(ctx // chunk):
+        k, v = w.prefill_chunk(c, chunk, device="cuda")
+        cache.append_rows(k, v)
+        for (b, h) in sample:
+            keep[(b, h)][0].append(host(k[b, h])); keep[(b, h)][1].append(host(v[b, h]))
+        del k, v
+    for s in range(16):
+        q, k1, v1 = w.step_qkv(s, device="cuda")
+        cache.append(k1, v1)
+        out = cache.decode(q)
+        for (b, h) in sample:
+            keep[(b, h)][0].append(host(k1[b, h])[None]); keep[(b, h)][1].append(host(v1[b, h])[None])
+        if s not in (0, 15):
+            continue
+        t = ctx + s
+        nfull = (t + 1) // QBLOCK * QBLOCK
+        o = out.cpu()                                            # bf16: its own rounding allowed
+        for (b, h) in sample:
+            Kin = np.concatenate(keep[(b, h)][0]); Vin = np.concatenate(keep[(b, h)][1])
+            K = model.stored_rows(Kin, np.arange(t + 1))
+            V = nm.bf16_to_f32(Vin)
+            for hq in (h * g, h * g + g - 1):
+                qr = model.query_rows(host(q[b, hq])[None], [t])[0]
+                r = int8_decode_one(qr, K, V, 0, t, 0, nfull, dither=model.dither(b, h))
+                assert r["c"] is None
+                assert_close(o[b, hq][None], r["out"][None], "bf16", "tier B full s=%d b=%d h=%d" % (s, b, hq))
+    # a sample of blocks bit-exact: dithered key codes, plain value codes, scales
+    KQ = cache.export(kvc.KVC_EXPORT_KQ); SK = cache.export(kvc.KVC_EXPORT_SK)
+    VQ = cache.export(kvc.KVC_EXPORT_VQ); SV = cache.export(kvc.KVC_EXPORT_SV)
+    for (b, h) in sample:
+        Kin = np.concatenate(keep[(b, h)][0]); Vin = np.concatenate(keep[(b, h)][1])
+        u = model.dither(b, h)
+        n = Kin.shape[0]
+        for blk in (0, 1, 4095, 8191, n // QBLOCK - 1):
+            pos = np.arange(blk * QBLOCK, (blk + 1) * QBLOCK)
+            sK, cK = nm.quantize_block_dither(model.stored_rows(Kin[pos], pos), u(blk * QBLOCK, QBLOCK))
+            sV, cV = nm.quantize_block(nm.bf16_to_f32(Vin[pos]))
+            assert SK[b, h, blk] == sK and np.array_equal(KQ[b, h, pos], cK), (b, h, blk)
+            assert SV[b, h, blk] == sV and np.array_equal(VQ[b, h, pos], cV), (b, h, blk)
+    assert cache.device_status() == 0
+
+
+@pytest.mark.parametrize("windowed,via", [(False, "trim"), (True, "trim"), (False, "store")],
+                         ids=["full", "w4096", "full-store"])
+def test_prefix_reuse_sampled(windowed, via):
+    # 16 requests with an 8192-token prefix (Hq=32, Hkv=8, d=128, RoPE 10000), cut at seeded
+    # points in [0, 8191], then a 512-token suffix by kvc_chunk_attn; sampled rows against the oracle,
+    # and the stale-next_position control (planted on the CPU) must exceed the tolerance.
+    # via "trim": kvc_trim; via "store": every prefill saved under its token IDs, the requests
+    # then refilled with other rows, and each cut taken back by a host lookup and one batched
+    # load, as the store bench line runs it
     w = wl.prefix_reuse(windowed)
     n, pre, W = w.extra["suffix"], w.extra["prefix"], w.window
     cuts = w.extra["cuts"]
-    cache = kvc.Cache.from_workload(w, max_chunk=n)
+    cache = kvc.Cache.from_workload(w, max_chunk=n, store_slots=w.batch if via == "store" else 0)
     model = oracle_for(w)
     g = w.n_q_heads // w.n_kv_heads
     reqs = [int(np.argmin(cuts)), int(np.argmax(cuts)), 3, 11]
@@ -238,7 +390,26 @@ def test_prefix_reuse_sampled(windowed):
         for (r, h) in keep:
             keep[(r, h)].append((host(k[r, h]), host(v[r, h])))
         del k, v
-    cache.trim(cuts)
+    if via == "trim":
+        cache.trim(cuts)
+    else:
+        store = kvc.PrefixStore(cache.cfg, w.batch)
+        rng = np.random.default_rng(w.seed)
+        queries = []
+        for r in range(w.batch):
+            ids = rng.integers(0, 1 << 31, pre, dtype=np.int64)
+            assert cache.save_prefix(store, r, ids, "test", b"prefix-reuse") == r
+            queries.append(np.concatenate([ids[:cuts[r]], rng.integers(1 << 32, 1 << 33, n, dtype=np.int64)]))
+        cache.trim([0] * w.batch)
+        k = w.keys((w.batch, w.n_kv_heads, 2048, w.head_dim), "other", "cuda")
+        v = w.values((w.batch, w.n_kv_heads, 2048, w.head_dim), "other", "cuda")
+        cache.append_rows(k, v)
+        del k, v
+        found = [store.lookup(x, "test", b"prefix-reuse") for x in queries]
+        assert [f[0] for f in found] == list(range(w.batch)) and [f[1] for f in found] == list(cuts)
+        cache.store_load_batch([f[0] for f in found], list(range(w.batch)), [f[1] for f in found])
+        assert np.array_equal(cache.export(kvc.KVC_EXPORT_NEXT_POSITION), np.asarray(cuts))
+        store.close()
     q = w.queries((w.batch, n, w.n_q_heads, w.head_dim), "suffix", "cuda")
     k = w.keys((w.batch, n, w.n_kv_heads, w.head_dim), "suffix", "cuda")
     v = w.values((w.batch, n, w.n_kv_heads, w.head_dim), "suffix", "cuda")
