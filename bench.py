@@ -49,6 +49,12 @@ TRAFFIC_PER_BYTE = {
     "bf16-at-int8-shape": ("decode_gqa.cu", "dbb9e91011defcc8", (536983552 + 3351808) / 536907776),
     "prefix-reuse": ("chunk.cu", "608963104f909744", (31902208 + 42240) / 22773760),
     "int8-dither": ("int8.cu", "f1d095edcb359003", (269315584 + 3224832) / 268996608),
+    "full-cache-mha-paged": ("decode_fast.cu", "9191b1eec481bc84", (268715008 + 4348416) / 268632064),
+    "sliding-window-gqa-paged": ("decode_gqa.cu", "dbb9e91011defcc8", (268094464 + 2689536) / 268148736),
+    "prefix-reuse-store": ("chunk.cu", "608963104f909744", (31902208 + 42240) / 22773760),   # the same chunk launch
+    # the store's batched row copy (8 requests' cuts, 297.9 MB read + written): writes still in L2
+    # at the end of the launch are not counted, so the ratio is below 1
+    "store-load": ("store.cu", "a9b53245c164e7d1", (149262592 + 101474048) / 297918464),
 }
 
 
@@ -762,7 +768,8 @@ class ChunkStoreBench(ChunkBench):
         return {"store_load": {"kernel": "host lookups + kvc_store_load_batch (row copy of every request)",
                                "bytes_per_step": self.load_bytes, "avg_ms": round(avg, 5),
                                "achieved": round(gbs, 2), "unit": "GB/s", "peak": peak_hbm,
-                               "frac": round(gbs / peak_hbm, 4)}}
+                               "frac": round(gbs / peak_hbm, 4),
+                               "traffic": traffic_per_launch("store-load", self.load_bytes)}}
 
     def config(self):
         c = super().config()
