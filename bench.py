@@ -444,6 +444,33 @@ class Int8Bench(DecodeBench):
                 "l2": "inputs larger than L2: %.2f GB read per step vs 129 MB L2" % (self.units() / 1e9)}
 
 
+class Int8CtBench(Int8Bench):
+    """The INT8 workload with the decode also writing every cached token's c_t (fp32
+    [B][Hq][capacity]), the input of the gated fallback's block risk: the same reads plus
+    B x Hq x n_keys x 4 bytes written per step."""
+
+    kernel = "kvc_decode_attn INT8 with per-token c_t (fused decode + witness bound + c_t write + combine)"
+
+    def __init__(self, device, batch=None, total_steps=0):
+        import torch
+        super().__init__(device, batch, total_steps)
+        self.ct = torch.zeros((self.w.batch, self.w.n_q_heads, self.cache.S), device=device)
+
+    def decode(self, q):
+        self.cache.decode(q, self.out, self.cmax, self.tanh, self.ct)
+
+    def units(self):
+        w = self.w
+        return super().units() + w.batch * w.n_q_heads * (self.ctx + self.done + 1) * 4
+
+    def config(self):
+        c = super().config()
+        c["workload"] = "int8-witness-ct"
+        c["ct"] = "fp32 c_t of every cached token written per step (%.3f GB)" % (
+            self.w.batch * self.w.n_q_heads * (self.ctx + 1) * 4 / 1e9)
+        return c
+
+
 class Int8DitherBench(Int8Bench):
     """Tier B at the INT8 workload's shape: subtractive-dither INT8 codes and scales, no
     witnesses (Philox key 0x85A308D3243F6A88, layer 0, request IDs 0..7); each step appends
@@ -781,7 +808,7 @@ class ChunkStoreBench(ChunkBench):
 
 BENCHES = {"full-cache-mha": FullCacheBench, "sliding-window-gqa": SlidingWindowBench, "int8-witness": Int8Bench,
            "bf16-at-int8-shape": Bf16AtInt8ShapeBench, "int8-witness-gated": Int8GatedBench,
-           "int8-dither": Int8DitherBench,
+           "int8-dither": Int8DitherBench, "int8-witness-ct": Int8CtBench,
            "full-cache-mha-paged": FullCachePagedBench, "sliding-window-gqa-paged": SlidingWindowPagedBench,
            "prefix-reuse": ChunkBench, "prefix-reuse-w4096": ChunkWindowBench, "prefix-reuse-store": ChunkStoreBench}
 
