@@ -85,7 +85,19 @@ __global__ void __launch_bounds__(kWarps * 32, 3) decode_fast_kernel(const Decod
     const __nv_bfloat16* Vg = static_cast<const __nv_bfloat16*>(a.v);
     unsigned char* myK = sK + warp_ * C::TILEB;
     unsigned char* myV = sV + warp_ * C::TILEB;
-    // lane 0 of each warp: copy its K/V rows of `split` (returns the key count)
+    // paged: lane 0 loads the page numbers of its warp's tile of a split one split ahead
+    // of the copies, so the block table's latency passes while the current split computes
+    constexpr int kRuns = kTile / kPage + 1;              // pages a tile can touch
+    int pf[kRuns];
+    auto fetch_pages = [&](int split) {
+        const int k0 = lo + split * kSplitKeys + warp_ * kTile;
+        const int nk = max(0, min(kTile, hi - k0));
+        const int32_t* trow = a.table + (size_t)b * (a.S / kPage);
+#pragma unroll
+        for (int j = 0; j < kRuns; ++j)
+            pf[j] = (nk > 0 && (k0 / kPage + j) * kPage < k0 + nk) ? trow[k0 / kPage + j] : 0;
+    };
+    // lane 0 of each warp: copy its K/V rows of `split` (paged: from the pages in pf)
     auto issue = [&](int split) {
         const int k0 = lo + split * kSplitKeys + warp_ * kTile;
         const int nk = max(0, min(kTile, hi - k0));
@@ -96,10 +108,13 @@ __global__ void __launch_bounds__(kWarps * 32, 3) decode_fast_kernel(const Decod
                 bulk_copy_g2s(myK, Kg + (head_row0 + k0) * D, bytes, &bar[warp_]);
                 bulk_copy_g2s(myV, Vg + (head_row0 + k0) * D, bytes, &bar[warp_]);
             } else {
-                // paged: one copy per run of rows inside one page
-                for (int r = 0; r < nk;) {
+                // one copy per run of rows inside one page
+#pragma unroll
+                for (int j = 0, r = 0; j < kRuns; ++j) {
+                    if (r >= nk) break;
                     const int run = min(nk - r, kPage - (k0 + r) % kPage);
-                    const size_t row = kv_row(a.table, b, kvh, k0 + r, a.Hkv, a.S);
+                    const int page = pf[j] < 0 ? 0 : pf[j];    // never taken: every slot read is mapped
+                    const size_t row = ((size_t)page * a.Hkv + kvh) * kPage + (k0 + r) % kPage;
                     bulk_copy_g2s(myK + r * C::ROWB, Kg + row * D, (uint32_t)run * C::ROWB, &bar[warp_]);
                     bulk_copy_g2s(myV + r * C::ROWB, Vg + row * D, (uint32_t)run * C::ROWB, &bar[warp_]);
                     r += run;
@@ -112,7 +127,10 @@ __global__ void __launch_bounds__(kWarps * 32, 3) decode_fast_kernel(const Decod
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncwarp();
+    const bool pager = a.table && (threadIdx.x & 31) == 0;
+    if (pager) fetch_pages(blockIdx.x);
     issue(blockIdx.x);                       // the first split's rows start moving at once
+    if (pager && (int)(blockIdx.x + gridDim.x) < nsplit) fetch_pages(blockIdx.x + gridDim.x);
 
     // Query of the G heads, rotated at t = len - 1, fp32, times log2(e)/sqrt(d): once per CTA
     {
@@ -285,7 +303,10 @@ __global__ void __launch_bounds__(kWarps * 32, 3) decode_fast_kernel(const Decod
         // accesses before the async-proxy writes
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncthreads();
-        if (split + (int)gridDim.x < nsplit) issue(split + gridDim.x);
+        if (split + (int)gridDim.x < nsplit) {
+            issue(split + gridDim.x);
+            if (pager && split + 2 * (int)gridDim.x < nsplit) fetch_pages(split + 2 * gridDim.x);
+        }
     }
 }
 

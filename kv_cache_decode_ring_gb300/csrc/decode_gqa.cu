@@ -36,6 +36,7 @@ constexpr int kTileKeys = 16;                            // keys per stage
 constexpr int kStages = 2;                               // per warp (three CTAs per SM: more warps in flight)
 constexpr float kLazyMax = 8.f;                          // log2-domain headroom of the reference maximum
 static_assert(kGqaSplit % (kWarps * kTileKeys) == 0 && kGqaSplitLong % (kWarps * kTileKeys) == 0, "split shape");
+static_assert(kGqaSplitLong / (kWarps * kTileKeys) <= 32, "a warp's tiles (their pages) fit in its lanes");
 
 // 2^x with the hardware approximation (relative error about 2^-22; 2^-inf = 0)
 __device__ __forceinline__ float ex2(float x) {
@@ -121,12 +122,20 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
     // keys of this warp's tile i: 16 consecutive rows, tiles of the 4 warps interleaved
     auto tile_k0 = [&](int i) { return lo_t + split * kSplit + (i * kWarps + warp) * kTileKeys; };
     auto tile_nk = [&](int i) { return max(0, min(kTileKeys, hi - tile_k0(i))); };
-    // lane 0: the tile's K and V boxes (always 16 full rows) on the stage's barrier
+    // paged: lane i holds the page of the warp's tile i (a tile is one page), all loaded in
+    // one round trip at the start instead of one table read before each tile's copies
+    int tpage = 0;
+    if (a.table && lane < tpw && tile_nk(lane) > 0)
+        tpage = a.table[(size_t)b * (a.S / kPage) + tile_k0(lane) / kPage];
+    // lane 0: the tile's K and V boxes (always 16 full rows) on the stage's barrier;
+    // called by the whole warp
     auto issue = [&](int i) {
+        const int pg = __shfl_sync(0xffffffffu, tpage, i & 31);
         if (lane == 0 && tile_nk(i) > 0) {
             const int sg = i % kStages;
             unsigned char* st = myS + sg * C::STAGEB;
-            const int row = a.table ? (int)kv_row(a.table, b, kvh, tile_k0(i), a.Hkv, a.S) : head_row0 + tile_k0(i);
+            // page < 0 is never taken: every slot read is mapped
+            const int row = a.table ? ((pg < 0 ? 0 : pg) * a.Hkv + kvh) * kPage : head_row0 + tile_k0(i);
             mbar_arrive_expect_tx(&myBar[sg], (uint32_t)C::STAGEB);
 #pragma unroll
             for (int j = 0; j < C::NBOX; ++j) {
