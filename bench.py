@@ -291,6 +291,15 @@ class DecodeBench:
         self.e2e_next = None
 
 
+def full_cache_config(w, ctx, cycle):
+    """The full-cache MHA line's config (both arms print it)."""
+    return {"workload": w.name, "batch": w.batch, "n_q_heads": w.n_q_heads, "n_kv_heads": w.n_kv_heads,
+            "head_dim": w.head_dim, "layout": "contiguous", "max_seq_len": w.capacity,
+            "context": "%d + step (cycles %d..%d keys)" % (ctx, ctx + 1, ctx + cycle),
+            "l2": "inputs larger than L2: %.2f GB of K/V read per step vs 129 MB L2"
+                  % (kv_bytes_per_step([ctx + 1] * w.batch, w.n_kv_heads, w.head_dim) / 1e9)}
+
+
 class FullCacheBench(DecodeBench):
     """Full-cache MHA decode, bf16: B=32, H=32, d=128, contiguous 8192, context 4096 + steps;
     every 128 steps the requests are trimmed back to 4096."""
@@ -334,12 +343,7 @@ class FullCacheBench(DecodeBench):
         return self.ctx + 1, 1
 
     def config(self):
-        w = self.w
-        return {"workload": w.name, "batch": w.batch, "n_q_heads": w.n_q_heads, "n_kv_heads": w.n_kv_heads,
-                "head_dim": w.head_dim, "layout": "contiguous", "max_seq_len": w.capacity,
-                "context": "%d + step (cycles %d..%d keys)" % (self.ctx, self.ctx + 1, self.ctx + self.CYCLE),
-                "l2": "inputs larger than L2: %.2f GB of K/V read per step vs 129 MB L2"
-                      % (kv_bytes_per_step([self.ctx + 1] * w.batch, w.n_kv_heads, w.head_dim) / 1e9)}
+        return full_cache_config(self.w, self.ctx, self.CYCLE)
 
 
 class SlidingWindowBench(DecodeBench):
@@ -1032,8 +1036,7 @@ def run_reference(args, world, threads):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "steps_per_s": round(value * 1e9 / full_step, 6),
-            "config": {"workload": w.name, "batch": w.batch, "n_q_heads": w.n_q_heads, "n_kv_heads": w.n_kv_heads,
-                       "head_dim": d, "context": ctx},
+            "config": full_cache_config(w, w.extra["context"], FullCacheBench.CYCLE),
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
