@@ -155,7 +155,15 @@ def test_prefix_cut_golden(case):
     # projections = layers(2) x Q/K/V(3) x recomputed tokens
     assert proj == 6 * (len(new) - cut) and full == 6 * len(new)
     if old == "store":
-        pytest.skip("needs the prefix store lookup (scope and signature), not part of the cut rule")
+        # the two stored branches of the page's store under one scope; the query comes from
+        # another scope, so no entry is eligible and everything is recomputed
+        from oracle.store import PrefixStore
+        store = PrefixStore(2, ring=bool(ring))
+        store.insert(list(range(1, 9)), "scope-a", b"sig", None)
+        store.insert([1, 2, 3, 4, 5, 20, 21, 22], "scope-a", b"sig", None)
+        assert store.lookup(new, "scope-b", b"sig") == (None, cut)
+        assert store.lookup(new, "scope-a", b"sig")[1] == 8          # the same query in the stored scope
+        return
     assert prefix_cut([int(x) for x in old.split()], new, ring=bool(ring)) == cut
 
 
