@@ -43,14 +43,14 @@ CSRC = os.path.join(ROOT, "kv_cache_decode_ring_gb300", "csrc")
 # valid only while the kernel source is the one captured (sha256 prefix), otherwise the
 # JSON line reports null.
 TRAFFIC_PER_BYTE = {
-    "full-cache-mha": ("decode_fast.cu", "0cd43ce3b495a8f4", (268704000 + 4368896) / 268632064),
-    "sliding-window-gqa": ("decode_gqa.cu", "cc010024203cf19e", (268077824 + 2954752) / 268148736),
-    "int8-witness": ("int8.cu", "f1d095edcb359003", (302861568 + 3226112) / 302551040),
-    "bf16-at-int8-shape": ("decode_gqa.cu", "cc010024203cf19e", (536976128 + 3329280) / 536907776),
+    "full-cache-mha": ("decode_fast.cu", "1c1f7c30fe290db7", (268705792 + 4242432) / 268632064),
+    "sliding-window-gqa": ("decode_gqa.cu", "596f2f658be07ec0", (268078080 + 3044096) / 268148736),
+    "int8-witness": ("int8.cu", "eee2ad4f635aa8ef", (302890240 + 3080192) / 302551040),
+    "bf16-at-int8-shape": ("decode_gqa.cu", "596f2f658be07ec0", (536977152 + 3369984) / 536907776),
     "prefix-reuse": ("chunk.cu", "608963104f909744", (31902208 + 42240) / 22773760),
-    "int8-dither": ("int8.cu", "f1d095edcb359003", (269315584 + 3224832) / 268996608),
-    "full-cache-mha-paged": ("decode_fast.cu", "0cd43ce3b495a8f4", (268708096 + 4215808) / 268632064),
-    "sliding-window-gqa-paged": ("decode_gqa.cu", "cc010024203cf19e", (268095488 + 2968832) / 268148736),
+    "int8-dither": ("int8.cu", "eee2ad4f635aa8ef", (269303808 + 2704128) / 268996608),
+    "full-cache-mha-paged": ("decode_fast.cu", "1c1f7c30fe290db7", (268710400 + 4297984) / 268632064),
+    "sliding-window-gqa-paged": ("decode_gqa.cu", "596f2f658be07ec0", (268096512 + 3033344) / 268148736),
     "prefix-reuse-store": ("chunk.cu", "608963104f909744", (31902208 + 42240) / 22773760),   # the same chunk launch
     # the store's batched row copy (8 requests' cuts, 297.9 MB read + written): writes still in L2
     # at the end of the launch are not counted, so the ratio is below 1

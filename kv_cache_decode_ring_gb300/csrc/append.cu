@@ -141,6 +141,8 @@ __device__ void quantize_block(const AppendArgs& a, const float* sK, const float
 // advances next_position[b] (one writer per request: no cross-CTA race).
 __global__ void __launch_bounds__(kThreads) append_token_kernel(const AppendArgs a) {
     extern __shared__ float smem[];
+    dep_wait();                                        // launched dependent: see launch_dep
+    dep_release();
     const int b = blockIdx.x;
     const int p = a.next_pos[b];
     if (!position_ok(a, p)) {
@@ -424,8 +426,7 @@ cudaError_t map_pages(kvc_handle* h, const std::vector<int>& from, const std::ve
 
 cudaError_t launch_append_token(const AppendArgs& a, cudaStream_t st) {
     const size_t smem = a.int8 ? quant_smem(a.d) : 0;
-    append_token_kernel<<<a.B, kThreads, smem, st>>>(a);
-    return cudaGetLastError();
+    return launch_dep(append_token_kernel, dim3(a.B), dim3(kThreads), smem, st, a);
 }
 
 cudaError_t launch_append_rows_group(const AppendArgs& a, const Group& g, cudaStream_t st) {

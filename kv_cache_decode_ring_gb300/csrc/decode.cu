@@ -100,6 +100,8 @@ __global__ void __launch_bounds__(kCombineThreads) combine_rows_kernel(const Com
     constexpr int kWarpsPerRow = WPR;
     constexpr int kRowsPerCta = kCombineThreads / 32 / WPR;
     __shared__ float4 sacc[kRowsPerCta][kWarpsPerRow][64];          // d <= 256
+    dep_wait();                                                      // launched dependent: see launch_dep
+    dep_release();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = warp / kWarpsPerRow, w = warp % kWarpsPerRow;
     const size_t row = (size_t)blockIdx.x * kRowsPerCta + r;
@@ -186,10 +188,10 @@ cudaError_t launch_decode(const DecodeArgs& a, const CombineArgs& c, bool fast, 
         if (e != cudaSuccess) return e;
     }
     const size_t rows = (size_t)a.B * a.Hq;
-    if (a.max_splits <= 8) combine_rows_kernel<1><<<(unsigned)((rows + 7) / 8), kCombineThreads, 0, st>>>(c);
-    else if (rows < 1024) combine_rows_kernel<8><<<(unsigned)rows, kCombineThreads, 0, st>>>(c);
-    else combine_rows_kernel<4><<<(unsigned)((rows + 1) / 2), kCombineThreads, 0, st>>>(c);
-    return cudaGetLastError();
+    if (a.max_splits <= 8)
+        return launch_dep(combine_rows_kernel<1>, dim3((unsigned)((rows + 7) / 8)), dim3(kCombineThreads), 0, st, c);
+    if (rows < 1024) return launch_dep(combine_rows_kernel<8>, dim3((unsigned)rows), dim3(kCombineThreads), 0, st, c);
+    return launch_dep(combine_rows_kernel<4>, dim3((unsigned)((rows + 1) / 2)), dim3(kCombineThreads), 0, st, c);
 }
 
 }  // namespace kvc

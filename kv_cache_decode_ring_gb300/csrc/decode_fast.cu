@@ -73,6 +73,8 @@ __global__ void __launch_bounds__(kWarps * 32, 3) decode_fast_kernel(const Decod
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.z, kvh = blockIdx.y;
+    dep_wait();                              // launched dependent: see launch_dep
+    dep_release();
     const int len = a.next_pos[b];
     int lo, hi;
     key_range(len, a.S, a.W, a.ring, lo, hi);
@@ -321,8 +323,7 @@ cudaError_t launch_t(const DecodeArgs& a, int grid_x, cudaStream_t st) {
         attr = true;
     }
     dim3 grid(grid_x, a.Hkv, a.B);
-    decode_fast_kernel<D, G><<<grid, kWarps * 32, C::SMEM, st>>>(a);
-    return cudaGetLastError();
+    return launch_dep(decode_fast_kernel<D, G>, grid, dim3(kWarps * 32), C::SMEM, st, a);
 }
 
 }  // namespace

@@ -106,6 +106,8 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.z, kvh = blockIdx.y, split = blockIdx.x;
+    dep_wait();                                          // launched dependent: see launch_dep
+    dep_release();
     const int len = a.next_pos[b];
     int lo, hi;
     key_range(len, a.S, a.W, a.ring, lo, hi);
@@ -345,8 +347,8 @@ cudaError_t launch_t(const DecodeArgs& a, const KvMaps& m, cudaStream_t st) {
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    decode_gqa_kernel<D, G><<<dim3(a.max_splits, a.Hkv, a.B), kWarps * 32, C::SMEM, st>>>(m.k, m.v, a);
-    return cudaGetLastError();
+    return launch_dep(decode_gqa_kernel<D, G>, dim3(a.max_splits, a.Hkv, a.B), dim3(kWarps * 32), C::SMEM, st,
+                      m.k, m.v, a);
 }
 
 }  // namespace

@@ -222,6 +222,8 @@ int8_decode_kernel(const Int8Args a) {
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.z, kvh = blockIdx.y, split = blockIdx.x;
+    dep_wait();                                                          // launched dependent: see launch_dep
+    dep_release();
     const int len = a.next_pos[b];
     const int nfull = len & ~(kQBlock - 1);
     const int nsq = (nfull + a.split - 1) / a.split;
@@ -666,6 +668,8 @@ template <int WPR>
 __global__ void __launch_bounds__(kCombineThreads) int8_combine_kernel(const Int8CombineArgs c) {
     constexpr int kRows = kCombineThreads / 32 / WPR;
     __shared__ float4 sacc[kRows][WPR][32];                       // d <= 128
+    dep_wait();                                                    // launched dependent: see launch_dep
+    dep_release();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = warp / WPR, w = warp % WPR;
     const size_t row = (size_t)blockIdx.x * kRows + r;
@@ -739,8 +743,8 @@ cudaError_t launch_t(const Int8Args& a, cudaStream_t st) {
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    int8_decode_kernel<D, G, DITHER><<<dim3(a.max_splits, a.Hkv, a.B), kWarps * 32, C::SMEM, st>>>(a);
-    return cudaGetLastError();
+    return launch_dep(int8_decode_kernel<D, G, DITHER>, dim3(a.max_splits, a.Hkv, a.B), dim3(kWarps * 32), C::SMEM,
+                      st, a);
 }
 
 }  // namespace
@@ -791,10 +795,13 @@ cudaError_t launch_int8_decode(kvc_handle* h, const void* q, void* out, float* c
     c.B = s.B; c.Hq = s.Hq; c.Hkv = s.Hkv; c.d = s.d; c.max_splits = s.max_splits; c.out_bf16 = s.out_bf16;
     c.split = s.split;
     const size_t rows = (size_t)s.B * s.Hq;
-    if (s.max_splits <= 8) int8_combine_kernel<1><<<(unsigned)((rows + 7) / 8), kCombineThreads, 0, st>>>(c);
-    else if (rows < 1024) int8_combine_kernel<8><<<(unsigned)rows, kCombineThreads, 0, st>>>(c);
-    else int8_combine_kernel<4><<<(unsigned)((rows + 1) / 2), kCombineThreads, 0, st>>>(c);
-    return cudaGetLastError();
+    if (s.max_splits <= 8)
+        e = launch_dep(int8_combine_kernel<1>, dim3((unsigned)((rows + 7) / 8)), dim3(kCombineThreads), 0, st, c);
+    else if (rows < 1024)
+        e = launch_dep(int8_combine_kernel<8>, dim3((unsigned)rows), dim3(kCombineThreads), 0, st, c);
+    else
+        e = launch_dep(int8_combine_kernel<4>, dim3((unsigned)((rows + 1) / 2)), dim3(kCombineThreads), 0, st, c);
+    return e;
 }
 
 }  // namespace kvc
