@@ -269,6 +269,51 @@ __global__ void __launch_bounds__(kThreads) append_rows_kernel(const AppendArgs 
     if (h == 0 && i == 0) a.pos[(size_t)b * a.S + slot] = (int)p;
 }
 
+// Many bf16 rows per request, 16 bytes (8 elements) per thread: d/8 threads per row.
+// Same per-pair arithmetic and rounding as append_rows_kernel (RoPE in fp32, one bf16
+// rounding per element; values copied bit for bit); the inputs are 16-byte aligned.
+__global__ void __launch_bounds__(kThreads) append_rows_vec_kernel(const AppendArgs a, const Group g) {
+    const int bi = blockIdx.z, b = g.b0 + bi, h = blockIdx.y;
+    const int cnt = g.val[bi];
+    const int np = a.next_pos[b];
+    const int vec = a.d / 8;
+    const int rows_per_cta = kThreads / vec;
+    const int r = blockIdx.x * rows_per_cta + threadIdx.x / vec;
+    const int c = threadIdx.x % vec;
+    if (threadIdx.x >= rows_per_cta * vec || r >= cnt) return;
+    if (a.ring && r < cnt - a.S) return;            // overwritten later in this call
+    const long long p = (long long)np + r;
+    if (!position_ok(a, p)) {
+        flag(a.hdr, kErrPosition);
+        return;
+    }
+    const int slot = a.ring ? (int)(p % a.S) : (int)p;
+    const size_t src = (size_t)b * a.sb + (size_t)h * a.sh + (size_t)r * a.sr + 8 * (size_t)c;
+    const uint4 kx = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.k) + src));
+    const uint4 vx = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.v) + src));
+    uint4 ko = kx;
+    if (a.rope) {
+        const float4* rp = reinterpret_cast<const float4*>(a.rope + (size_t)p * (a.d / 2) + 4 * c);
+        const float4 c0 = __ldg(rp), c1 = __ldg(rp + 1);
+        uint32_t w[4] = {kx.x, kx.y, kx.z, kx.w};
+        const float2 cs[4] = {make_float2(c0.x, c0.y), make_float2(c0.z, c0.w),
+                              make_float2(c1.x, c1.y), make_float2(c1.z, c1.w)};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const __nv_bfloat162 x2 = *reinterpret_cast<const __nv_bfloat162*>(&w[e]);
+            float y0, y1;
+            rope_pair(__low2float(x2), __high2float(x2), cs[e], y0, y1);
+            const __nv_bfloat162 o2 = __floats2bfloat162_rn(y0, y1);
+            w[e] = *reinterpret_cast<const uint32_t*>(&o2);
+        }
+        ko = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    const size_t dst = kv_row(a.table, b, h, slot, a.Hkv, a.S) * a.d + 8 * (size_t)c;
+    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.kc) + dst) = ko;
+    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.vc) + dst) = vx;
+    if (h == 0 && c == 0) a.pos[(size_t)b * a.S + slot] = (int)p;
+}
+
 // INT8 rows, phase 1: every 16-position block that the new rows complete.
 // CTA (block index from floor(np/16), KV head, request).  Rows below np come
 // from the tail, the rest from the input.  Phase 2 (tail_kernel) writes the
@@ -431,10 +476,19 @@ cudaError_t launch_append_token(const AppendArgs& a, cudaStream_t st) {
 
 cudaError_t launch_append_rows_group(const AppendArgs& a, const Group& g, cudaStream_t st) {
     if (!a.int8) {
-        const int half = a.d / 2;
-        const int rows_per_cta = kThreads / half > 0 ? kThreads / half : 1;
-        dim3 grid((a.n + rows_per_cta - 1) / rows_per_cta, a.Hkv, g.nb);
-        append_rows_kernel<<<grid, kThreads, 0, st>>>(a, g);
+        const bool vec = a.bf16 && a.d % 8 == 0 && a.d / 8 <= kThreads &&
+                         reinterpret_cast<uintptr_t>(a.k) % 16 == 0 && reinterpret_cast<uintptr_t>(a.v) % 16 == 0 &&
+                         a.sb % 8 == 0 && a.sh % 8 == 0 && a.sr % 8 == 0;
+        if (vec) {
+            const int rows_per_cta = kThreads / (a.d / 8);
+            dim3 grid((a.n + rows_per_cta - 1) / rows_per_cta, a.Hkv, g.nb);
+            append_rows_vec_kernel<<<grid, kThreads, 0, st>>>(a, g);
+        } else {
+            const int half = a.d / 2;
+            const int rows_per_cta = kThreads / half > 0 ? kThreads / half : 1;
+            dim3 grid((a.n + rows_per_cta - 1) / rows_per_cta, a.Hkv, g.nb);
+            append_rows_kernel<<<grid, kThreads, 0, st>>>(a, g);
+        }
         advance_kernel<<<(g.nb + 255) / 256, 256, 0, st>>>(a.next_pos, g);
     } else {
         dim3 grid((a.n + kQBlock - 1) / kQBlock + 1, a.Hkv, g.nb);
