@@ -18,10 +18,14 @@ Layout of the package:
 * ``listmodel``  -- the cache as a list (lastWindow, step, run, ringToList), the
                     physical ring, the prefix cut and the trim rules.
 * ``numerics``   -- ctypes front end of ``oracle.c``: bf16/fp16 rounding, RoPE,
-                    fp64 masked attention, INT8 quantizer and witnesses.
+                    fp64 masked attention, INT8 quantizer and witnesses, Philox4x32-10
+                    and the Tier B dither streams.
 * ``model``      -- a whole decode-step oracle built from the two: per request the
                     full history of cells, decode by masked attention over it, the
-                    expected physical cache state, trim, chunk, the INT8 tier.
+                    expected physical cache state, trim, chunk, the INT8 tier, its
+                    gated fallback (block risk, gate selection, restore) and Tier B.
+* ``store``      -- the prefix store: bounded entries, scope and signature
+                    eligibility, the longest reusable prefix, the newest on ties.
 
 Every function here that has no independent pin says so in its docstring
 ("parity unpinned"); all others are pinned by ``tests/test_oracle_*.py``.
