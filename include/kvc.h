@@ -20,7 +20,12 @@
  *    stream).  Compute calls only enqueue work and return; none waits for the
  *    GPU, except kvc_create (uploads tables), kvc_export and
  *    kvc_device_status (read back).  One handle serves one stream at a time:
- *    calls on one handle from different streams race on its state.
+ *    calls on one handle from different streams race on its state.  The
+ *    decode-path kernels (append, decode, combine) start as programmatic
+ *    dependent launches.  They may be scheduled while the previous kernel on the
+ *    stream drains, but they wait for it to complete before touching memory.
+ *    So the order of work on a stream, and CUDA graph capture, behave as with
+ *    ordinary launches.
  *  - Element types: KVC_F32 = IEEE fp32, KVC_BF16 = bfloat16.  q, k and v
  *    use the cache dtype; outputs use kvc_config.out_dtype (default: the
  *    cache dtype).
