@@ -214,6 +214,7 @@ int kvc_set_request_id(kvc_t h, int32_t b, uint32_t request_id, kvc_stream_t str
  *   - KVC_ERR_UNSUPPORTED for an INT8 cache.
  * It calls no cudaMalloc, cudaFree or other allocating routine. */
 #define KVC_NOALLOC_SCRATCH_BYTES (64u << 20)
+/* See the comment above KVC_NOALLOC_SCRATCH_BYTES: d_q, d_out as for kvc_decode_attn. */
 int kvc_decode_attn_noalloc(kvc_t h, const void* d_q, void* d_out, kvc_stream_t stream);
 
 /* Continue every request from next_position = h_cut[b] ([PREFIX]
@@ -295,7 +296,13 @@ enum {
                                      page, -1 = none (paged caches; K and V exports are
                                      gathered through it into [B][Hkv][capacity][d]) */
 };
+/* *bytes = the size of export `which` for this handle.  KVC_ERR_ARG for a null
+ * pointer or an export the cache does not hold (K/V of an INT8 cache, INT8 arrays
+ * of a bf16/fp32 cache, the page table of an unpaged cache). */
 int kvc_export_bytes(kvc_t h, int32_t which, size_t* bytes);
+/* Copy export `which` into h_dst (host, `bytes` = kvc_export_bytes exactly, else
+ * KVC_ERR_ARG), after the work already queued on `stream`; returns when the copy
+ * is complete. */
 int kvc_export(kvc_t h, int32_t which, void* h_dst, size_t bytes, kvc_stream_t stream);
 
 /* Host mirror of next_position (B entries), kept by the handle.  Enqueued but
@@ -338,6 +345,8 @@ typedef struct kvc_pstore* kvc_pstore_t;
  * layout selects the sliding-window reuse rule.  KVC_ERR_ARG for capacity < 1 or
  * an invalid cfg. */
 int kvc_pstore_create(const kvc_config* cfg, int32_t capacity, kvc_pstore_t* out);
+/* Host only.  Frees the store (its entries' IDs, scopes and signatures); the rows
+ * in the handle's store slots are untouched.  KVC_ERR_ARG for NULL. */
 int kvc_pstore_destroy(kvc_pstore_t ps);
 
 /* Host only.  Records a prefill of the n_ids >= 1 token IDs h_ids under the
