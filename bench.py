@@ -1001,6 +1001,11 @@ def main():
 
 
 def run_reference(args, world, threads):
+    if args.workload != "full-cache-mha":
+        # the reference arm times the oracle on the default line only
+        print(json.dumps({"impl": "reference", "unavailable": "the reference arm (the CPU oracle) times the "
+                          "full-cache-mha line only, not %s" % args.workload}), flush=True)
+        return 0
     from kv_cache_decode_ring_gb300 import workloads as wl
     from oracle import numerics as nm
     nm.build()

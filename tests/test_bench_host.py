@@ -50,3 +50,13 @@ def test_both_arms_share_the_full_cache_config():
     c = bench.full_cache_config(w, w.extra["context"], bench.FullCacheBench.CYCLE)
     assert c["workload"] == "full-cache-mha-bf16" and c["batch"] == 32 and c["head_dim"] == 128
     assert c["max_seq_len"] == 8192 and c["context"] == "4096 + step (cycles 4097..4224 keys)"
+
+
+def test_reference_arm_names_the_lines_it_does_not_time():
+    import json
+    import subprocess
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
+                        "int8-witness", "--steps", "1", "--warmup", "0"], capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and "full-cache-mha" in line["unavailable"]
