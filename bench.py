@@ -16,6 +16,12 @@ e2e      = the same metric through the C ABI with host buffers: every step copie
 roofline = the decode-attention call (split-K kernel + combine) timed with CUDA
            events on its stream; algorithmic bytes = KV bytes + q + out per call.
 
+lines    = (default run only) the same measurement, value and roofline with its own
+           clocks, for the INT8 + witness decode, the sliding-window GQA decode, the
+           chunked suffix attention (full and W = 4096) and the INT8 Tier B decode.
+
+--gpus N without torchrun starts N ranks under torch.distributed.run, one replica of
+the workload per GPU (weak scaling, no collective on the data path).
 --impl reference times the CPU oracle instead (fp64 attention by definition, on
 the host cores) on a bounded sample of the same workload.
 """
@@ -864,32 +870,154 @@ def replica_aggregate(ms_local, units_local, dist=None, device="cpu"):
     return float(t.item()), float(u.item())
 
 
-def main():
+# Lines that the default run times after the headline one, each in the same way (warm-up,
+# K timed steps with CUDA events around the dominant call, clocks sampled meanwhile).
+EXTRA_LINES = ("int8-witness", "sliding-window-gqa", "prefix-reuse", "prefix-reuse-w4096", "int8-dither")
+
+
+def time_steps(bench, K, warmup, local_rank, dist):
+    """W untimed steps, then K timed steps bracketed by a barrier and a synchronize on both
+    sides; the dominant call of every step is bracketed by its own pair of CUDA events on
+    the stream it is launched on.  Returns the slowest rank's milliseconds, the units all
+    ranks processed, this rank's per-step units and call milliseconds, launches and clocks."""
+    import torch
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(warmup):
+        bench.step()
+    bench.reset()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    t0e, t1e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(gpu_index(local_rank))
+    sampler.start()
+    time.sleep(0.3)
+    barrier()
+    wall0 = time.perf_counter()
+    t0e.record()
+    units, launches, step_units = 0, 0, []
+    for i in range(K):
+        u = bench.units()
+        launches += bench.launches_per_step() + bench.step(ev[i])
+        units += u
+        step_units.append(u)
+    t1e.record()
+    barrier()
+    wall = time.perf_counter() - wall0
+    sampler.stop()
+    ms_total, all_units = replica_aggregate(t0e.elapsed_time(t1e), units, dist, "cuda")
+    return {"ms": ms_total, "units": all_units, "step_units": step_units,
+            "call_ms": [a.elapsed_time(b) for a, b in ev], "launches": launches, "clocks": sampler.summary(),
+            "wall": wall}
+
+
+def line_summary(bench, workload, t, K):
+    """Throughput of the timed steps and the roofline of the dominant call."""
+    peak, peak_kind = hbm_peak() if bench.bound == "hbm" else tensor_peak()
+    scale = 1e9 if bench.unit == "GB/s" else 1e12
+    value = t["units"] / (t["ms"] / 1e3) / scale
+    call_units = sum(u + bench.io_bytes() for u in t["step_units"]) / K
+    call_ms = sum(t["call_ms"]) / K
+    achieved = call_units / (call_ms / 1e3) / scale
+    return {
+        "value": round(value, 2), "unit": bench.unit, "ms_per_step": round(t["ms"] / K, 5), "steps": K,
+        "steps_per_s": round(K / (t["ms"] / 1e3), 2), "frac_of_%s_peak" % peak_kind: round(value / peak, 4),
+        "roofline": {"bound": bench.bound, "achieved": round(achieved, 2), "peak": peak, "unit": bench.unit,
+                     "frac": round(achieved / peak, 4),
+                     "traffic": traffic_per_launch(workload, bench.traffic_basis(call_units)),
+                     "kernel": bench.kernel, "peak_kind": peak_kind,
+                     "%s_per_launch" % ("bytes" if bench.unit == "GB/s" else "flops"): int(call_units),
+                     "avg_launch_ms": round(call_ms, 5)},
+        "gpu_launches": t["launches"], "clocks": t["clocks"], "config": bench.config(),
+    }
+
+
+def free_port() -> int:
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def launch_replicas(n: int, argv) -> int:
+    """Start n ranks of this script under torch.distributed.run (one per GPU, rendezvous
+    on 127.0.0.1); rank 0 prints the line."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", str(n),
+           "--master-addr", "127.0.0.1", "--master-port", str(free_port()), os.path.abspath(__file__)] + list(argv)
+    return subprocess.call(cmd)
+
+
+def dry_run(args, world, rank):
+    """The replica launcher without a GPU: every rank joins a gloo group, runs K trivial
+    CPU steps and reports one unit per step; rank 0 prints the aggregate line.  Tests use
+    it to check that --gpus N really starts N ranks."""
+    import torch
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    x = torch.ones(1024)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        x = x * 1.0
+    ms = (time.perf_counter() - t0) * 1e3
+    ms, units = replica_aggregate(max(ms, 1e-6), args.steps, dist, "cpu")
+    ranks = replica_aggregate(0.0, 1.0, dist, "cpu")[1]
+    if rank == 0:
+        print(json.dumps({"metric": "dry run of the replica launcher (no GPU work)", "value": units / (ms / 1e3),
+                          "unit": "steps/s", "n_gpus": world, "ranks_run": int(ranks), "steps": args.steps,
+                          "warmup": args.warmup, "dry_run": True}), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    argv = sys.argv[1:] if argv is None else list(argv)
     ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--gpus", type=int, default=None,
+                    help="replicas, one per GPU (default: WORLD_SIZE under torchrun, else 1); without "
+                         "torchrun, N > 1 starts N ranks itself")
     ap.add_argument("--steps", type=int, default=1500)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="kvc", choices=["kvc", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-lines", action="store_true",
+                    help="time only the chosen workload (the default run also times %s)" % ", ".join(EXTRA_LINES))
+    ap.add_argument("--dry-run", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--batch", type=int, default=0, help="override the batch (profiling a smaller case)")
     ap.add_argument("--workload", default="full-cache-mha", choices=sorted(BENCHES),
-                    help="full-cache-mha (the headline line), sliding-window-gqa or int8-witness")
-    args = ap.parse_args()
+                    help="full-cache-mha (the headline line) or any other workload")
+    args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
+    env_world = os.environ.get("WORLD_SIZE")
+    if env_world is None and args.gpus is not None and args.gpus > 1:
+        return launch_replicas(args.gpus, argv)
+    world = int(env_world) if env_world is not None else 1
+    if args.gpus is not None and args.gpus != world:
+        print("bench.py: --gpus %d disagrees with WORLD_SIZE=%d" % (args.gpus, world), file=sys.stderr)
+        return 2
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
 
+    if args.dry_run:
+        return dry_run(args, world, rank)
     if args.impl == "reference":
         if rank != 0:
             return 0
         return run_reference(args, world, threads)
 
     import torch
+    if local_rank >= torch.cuda.device_count():
+        print("bench.py: rank %d has no GPU (%d visible)" % (local_rank, torch.cuda.device_count()), file=sys.stderr)
+        return 2
     torch.cuda.set_device(local_rank)
     dist = None
     if world > 1:
@@ -900,51 +1028,9 @@ def main():
     build()
     e2e_steps = 0 if args.no_e2e else min(args.steps, 400) + 3
     bench = BENCHES[args.workload]("cuda", args.batch, args.warmup + args.steps + e2e_steps)
-    peak, peak_kind = hbm_peak() if bench.bound == "hbm" else tensor_peak()
-    scale = 1e9 if bench.unit == "GB/s" else 1e12
-
-    def barrier():
-        if dist is not None:
-            dist.barrier()
-        torch.cuda.synchronize()
-
-    # warm-up
-    launches = 0
-    for i in range(args.warmup):
-        bench.step()
-    bench.reset()
-
-    # timed region
     K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    t0e, t1e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    sampler = ClockSampler(gpu_index(local_rank))
-    sampler.start()
-    time.sleep(0.3)
-    barrier()
-    wall0 = time.perf_counter()
-    t0e.record()
-    units = 0
-    step_units = []
-    for i in range(K):
-        u = bench.units()
-        launches += bench.launches_per_step() + bench.step(ev[i])
-        units += u
-        step_units.append(u)
-    t1e.record()
-    barrier()
-    wall = time.perf_counter() - wall0
-    sampler.stop()
-    ms_total = t0e.elapsed_time(t1e)
-    attn_ms = [a.elapsed_time(b) for a, b in ev]
-    ms_total, all_units = replica_aggregate(ms_total, units, dist, "cuda")
-    value = all_units / (ms_total / 1e3) / scale
-    steps_per_s = K / (ms_total / 1e3)
-
-    # roofline of the decode-attention call
-    attn_bytes = sum(u + bench.io_bytes() for u in step_units) / K
-    attn_avg_ms = sum(attn_ms) / len(attn_ms)
-    achieved = attn_bytes / (attn_avg_ms / 1e3) / scale
+    t = time_steps(bench, K, args.warmup, local_rank, dist)
+    head = line_summary(bench, args.workload, t, K)
 
     # end-to-end through the ABI with host buffers
     e2e = None
@@ -956,7 +1042,9 @@ def main():
             bench.e2e_step()
         bench.e2e_flush()
         bench.reset()
-        barrier()
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
         eu = 0
@@ -965,8 +1053,11 @@ def main():
             bench.e2e_step()
         bench.e2e_flush()
         b.record()
-        barrier()
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
         ems, eut = replica_aggregate(a.elapsed_time(b), eu, dist, "cuda")
+        scale = 1e9 if bench.unit == "GB/s" else 1e12
         e2e = {"value": round(eut / (ems / 1e3) / scale, 2), "unit": bench.unit,
                "h2d_bytes_per_step": hb, "d2h_bytes_per_step": db, "steps": Ke}
 
@@ -975,25 +1066,34 @@ def main():
         gbps, el, nprob, desc = oracle_sample(bench.w, args.cpu_seconds, threads, problem=bench.cpu_problem())
         cpu = {"value": round(gbps, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
                "sample": desc + ", %.1f s" % el}
+    extra = bench.extra_report(hbm_peak()[0]) if hasattr(bench, "extra_report") else {}
+    bench = None
+    torch.cuda.empty_cache()
 
-    clocks = sampler.summary()
+    # the other lines the decode step's targets name, timed the same way
+    lines = {}
+    if args.workload == "full-cache-mha" and not args.no_lines and not args.batch:
+        for name in EXTRA_LINES:
+            lb = BENCHES[name]("cuda", 0, args.warmup + K)
+            lines[name] = line_summary(lb, name, time_steps(lb, K, args.warmup, local_rank, dist), K)
+            lb = None
+            torch.cuda.empty_cache()
+
     if rank == 0:
         line = {
-            "metric": bench.metric, "value": round(value, 2), "unit": bench.unit, "n_gpus": world, "steps": K,
-            "warmup": args.warmup, "ms_per_step": round(ms_total / K, 5), "higher_is_better": True,
+            "metric": BENCHES[args.workload].metric,
+            "value": head["value"], "unit": head["unit"], "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "steps_per_s": round(steps_per_s, 2), "frac_of_%s_peak" % peak_kind: round(value / peak, 4),
-            "config": bench.config(),
-            "roofline": {"bound": bench.bound, "achieved": round(achieved, 2), "peak": peak, "unit": bench.unit,
-                         "frac": round(achieved / peak, 4),
-                         "traffic": traffic_per_launch(args.workload, bench.traffic_basis(attn_bytes)),
-                         "kernel": bench.kernel, "peak_kind": peak_kind,
-                         "bytes_per_launch": int(attn_bytes), "avg_launch_ms": round(attn_avg_ms, 5)},
-            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
-            "wall_s": round(wall, 3),
+            "steps_per_s": head["steps_per_s"],
         }
-        if hasattr(bench, "extra_report"):
-            line.update(bench.extra_report(hbm_peak()[0]))
+        line.update({k: v for k, v in head.items() if k.startswith("frac_of_")})
+        line.update({"config": head["config"], "roofline": head["roofline"], "cpu_baseline": cpu, "e2e": e2e,
+                     "gpu_launches": head["gpu_launches"],
+                     "clocks": head["clocks"], "wall_s": round(t["wall"], 3)})
+        line.update(extra)
+        if lines:
+            line["lines"] = lines
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()

@@ -60,3 +60,38 @@ def test_reference_arm_names_the_lines_it_does_not_time():
     assert r.returncode == 0
     line = json.loads(r.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference" and "full-cache-mha" in line["unavailable"]
+
+
+def _run_bench(args, env=None, timeout=300):
+    import json
+    import subprocess
+    e = dict(os.environ)
+    for k in ("WORLD_SIZE", "RANK", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT"):
+        e.pop(k, None)
+    e.update(env or {})
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py")] + args, capture_output=True, text=True,
+                       timeout=timeout, env=e)
+    lines = [l for l in r.stdout.strip().splitlines() if l.startswith("{")]
+    return r.returncode, (json.loads(lines[-1]) if lines else None), r.stderr
+
+
+def test_gpus_flag_starts_that_many_ranks():
+    # without torchrun, --gpus 2 starts two ranks itself (gloo in the dry run, no GPU work);
+    # the line counts the ranks that really ran
+    rc, line, err = _run_bench(["--gpus", "2", "--dry-run", "--steps", "3", "--warmup", "3"])
+    assert rc == 0, err
+    assert line["n_gpus"] == 2 and line["ranks_run"] == 2 and line["dry_run"]
+    rc, line, err = _run_bench(["--dry-run", "--steps", "3"])
+    assert rc == 0 and line["n_gpus"] == 1 and line["ranks_run"] == 1
+
+
+def test_gpus_flag_must_agree_with_the_launcher():
+    rc, line, err = _run_bench(["--gpus", "3", "--dry-run", "--steps", "1"],
+                               env={"WORLD_SIZE": "2", "RANK": "0", "LOCAL_RANK": "0"})
+    assert rc == 2 and line is None and "disagrees" in err
+
+
+def test_default_run_times_every_targeted_line():
+    # the INT8 decode, the sliding-window GQA decode and the chunk kernel each get a line
+    for name in ("int8-witness", "sliding-window-gqa", "prefix-reuse", "prefix-reuse-w4096", "int8-dither"):
+        assert name in bench.EXTRA_LINES and name in bench.BENCHES
