@@ -203,12 +203,21 @@ int kvc_set_request_id(kvc_t h, int32_t b, uint32_t request_id, kvc_stream_t str
  *     partial it reads, so nothing has to start at zero.
  *   - Calls that overlap on the GPU race on the array, even on different
  *     handles or streams: serialise them.
+ *   - The looked-up address is kept for the life of the process.  A device
+ *     reset (cudaDeviceReset, or the primary context torn down and made again)
+ *     unloads the array, so this entry point must not be called after one.
  *
  * Errors:
  *   - KVC_ERR_CAPACITY if the problem needs more than the array holds, that is
- *     if B*Hq*splits*(8 + 4*d) bytes (+ alignment) exceed KVC_NOALLOC_SCRATCH_BYTES,
- *     with splits = ceil(min(capacity, window) / 128) for bf16 d=64/128 caches,
- *     else / 64.
+ *     if B*Hq*splits*(8 + 4*d) bytes (+ 256 bytes of alignment) exceed
+ *     KVC_NOALLOC_SCRATCH_BYTES, with
+ *       splits = ceil(min(capacity, window) / split) + (page_pool > 0 ? 1 : 0)
+ *     (window 0 = capacity), where split is the decode kernel's keys per split:
+ *       1024, or 2048 when min(capacity, window) >= 16384, for bf16 caches with
+ *         d = 64 or 128 and 4 or 8 query heads per KV head;
+ *       128 for the other bf16 caches with d = 64 or 128 and at most 8 query
+ *         heads per KV head;
+ *       64 otherwise.
  *   - KVC_ERR_ARG for the cases kvc_decode_attn refuses, or if the current device
  *     is not the handle's.
  *   - KVC_ERR_UNSUPPORTED for an INT8 cache.

@@ -199,9 +199,15 @@ def test_capacity_and_argument_errors():
     assert cache.device_status() == 0
 
 
-@pytest.mark.parametrize("case", [CASES[1], CASES[4], CASES[3], CASES[6]], ids=lambda c: c[0] + "-out-f32")
+STRICT_CASES = [CASES[0], ("gqa2-d128", 8, 4, 128, "contiguous", 1024, 0, 10000.0), CASES[1], CASES[4], CASES[3],
+                CASES[6]]
+
+
+@pytest.mark.parametrize("case", STRICT_CASES, ids=lambda c: c[0] + "-out-f32")
 def test_f32_outputs_strict_tolerance(case):
-    # bf16 cache, fp32 outputs: no output rounding, so the plain 2e-3 bound applies
+    # bf16 cache, fp32 outputs: no output rounding, so the plain 2e-3 bound applies; one
+    # case for every bf16 decode kernel (g = 1 and 2 at d = 128: the bulk-copy kernel; g = 4
+    # and 8: the tensor-copy kernel; ring; the generic kernel at d = 96)
     name, Hq, Hkv, d, layout, cap, window, rope = case
     w = wl.small(name, B=3, Hq=Hq, Hkv=Hkv, d=d, layout=layout, capacity=cap, window=window,
                  rope_base=rope, seed=41)

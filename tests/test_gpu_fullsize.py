@@ -1,8 +1,9 @@
 """Parity at the workloads' full sizes, in the launch configuration bench.py times.
 
-The oracle cannot redo every head, so sampled (request, head) outputs are checked
-one by one against fp64 attention over the generator's own rows (never the GPU
-cache), plus closed-form checks of positions that hold at any size.
+The bf16 decodes are checked at every (request, head) of their checked steps; the
+INT8 and chunk workloads, whose oracle is slower, at sampled heads.  References are
+fp64 attention over the generator's own rows (never the GPU cache), plus closed-form
+checks of positions that hold at any size.
 
 Full-cache MHA decode: B=32, H=32, d=128, contiguous 8192, context 4096 + 128 steps;
 contiguous rows, or 16-slot pages behind a block table (as the paged bench lines).
@@ -35,39 +36,44 @@ def _rows(model, x_np, positions):
     return model.stored_rows(x_np, positions).astype(np.float64)
 
 
+def _threads():
+    import os
+    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+
+
 @pytest.mark.parametrize("paged", [False, True], ids=["contiguous", "paged"])
-def test_full_cache_mha_sampled(paged):
+def test_full_cache_mha_every_head(paged):
+    # every (request, head) of the checked steps against fp64 attention (no RoPE: the cache
+    # rows are the generator's bf16 values, kept on the host as bit patterns)
     w = wl.full_cache_mha()
     ctx = w.extra["context"]
+    B, H, d = w.batch, w.n_q_heads, w.head_dim
     # paged: exactly the 16-slot pages the 128 steps need, as many as the bench's pool per step
-    cache = kvc.Cache.from_workload(w, page_pool=w.batch * -(-(ctx + 128) // 16) if paged else 0)
-    model = oracle_for(w)            # used for its row and query definitions only
+    cache = kvc.Cache.from_workload(w, page_pool=B * -(-(ctx + 128) // 16) if paged else 0)
     k, v = w.prefill_chunk(0, ctx, device="cuda")
     cache.append_rows(k, v)
-    rng = np.random.default_rng(0)
-    sample = [(0, 0), (31, 31), (7, 19)] + [tuple(x) for x in rng.integers(0, 32, (9, 2))]
-    hk = {bh: host(k[bh[0], bh[1]]) for bh in sample}
-    hv = {bh: host(v[bh[0], bh[1]]) for bh in sample}
-    steps_k, steps_v = {bh: [] for bh in sample}, {bh: [] for bh in sample}
+    hK = np.empty((B, H, ctx + 128, d), dtype=np.uint16)
+    hV = np.empty_like(hK)
+    hK[:, :, :ctx] = host(k)
+    hV[:, :, :ctx] = host(v)
+    del k, v
     check_at = {0, 1, 63, 127}
     for s in range(128):
         q, k1, v1 = w.step_qkv(s, device="cuda")
         cache.append(k1, v1)
         out = cache.decode(q)
-        for bh in sample:
-            steps_k[bh].append(host(k1[bh[0], bh[1]]))
-            steps_v[bh].append(host(v1[bh[0], bh[1]]))
+        hK[:, :, ctx + s] = host(k1)
+        hV[:, :, ctx + s] = host(v1)
         if s not in check_at:
             continue
         t = ctx + s
-        o = out.cpu()                                            # bf16: its own rounding allowed
-        for (b, h) in sample:
-            K = np.concatenate([_rows(model, hk[(b, h)], np.arange(ctx)),
-                                _rows(model, np.stack(steps_k[(b, h)]), np.arange(ctx, t + 1))])
-            V = np.concatenate([nm.bf16_to_f32(hv[(b, h)]), nm.bf16_to_f32(np.stack(steps_v[(b, h)]))]).astype(np.float64)
-            qr = model.query_rows(host(q[b, h])[None], [t]).astype(np.float64)
-            ref = nm.attend(qr, K, V, t, 0)
-            assert_close(o[b, h][None], ref, "bf16", "full-cache step %d (b=%d, h=%d)" % (s, b, h))
+        qf = nm.bf16_to_f32(host(q)).astype(np.float64)                 # [B, H, d]
+        probs = [(b, h) for b in range(B) for h in range(H)]
+        ref = nm.attend_many([qf[b, h][None] for b, h in probs], [hK[b, h, :t + 1] for b, h in probs],
+                             [hV[b, h, :t + 1] for b, h in probs], [t] * len(probs), 0, None,
+                             nthreads=_threads())
+        ref = np.stack(ref).reshape(B, H, d)
+        assert_close(out.cpu(), ref, "bf16", "full-cache step %d, every (request, head)" % s)
     # positions after 128 steps: slot p holds p for p < ctx + 128 (closed form, every request)
     pos = cache.export(kvc.KVC_EXPORT_POSITIONS)
     want = np.where(np.arange(w.capacity) < ctx + 128, np.arange(w.capacity), -1)
@@ -85,17 +91,17 @@ def _ring_positions_ok(pos_row, length, W):
 
 
 @pytest.mark.parametrize("paged", [False, True], ids=["ring", "paged-ring"])
-def test_sliding_window_gqa_sampled(paged):
+def test_sliding_window_gqa_every_head(paged):
+    # every request and every query head at the decode step, against fp64 attention over the
+    # window rows as the oracle stores them (rotated at their positions, rounded to bf16)
     w = wl.sliding_window_gqa()
     W, Lmax = w.capacity, w.extra["max_len"]
+    B, Hq, Hkv, d = w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim
     lengths = w.extra["lengths"]                   # current token at L_b - 1
-    cache = kvc.Cache.from_workload(w, max_position=Lmax, page_pool=w.batch * (W // 16) if paged else 0)
+    cache = kvc.Cache.from_workload(w, max_position=Lmax, page_pool=B * (W // 16) if paged else 0)
     model = oracle_for(w)
-    rng = np.random.default_rng(1)
-    bs = sorted(set([int(np.argmax(lengths)), int(np.argmin(lengths))] + list(rng.integers(0, 64, 6))))
-    hs = [0, 3, 7]
-    keep_k = {(b, h): [] for b in bs for h in hs}
-    keep_v = {(b, h): [] for b in bs for h in hs}
+    # the generator's rows of every request's window (bf16 bit patterns, [Hkv, n, d])
+    keep_k, keep_v = [[] for _ in range(B)], [[] for _ in range(B)]
     chunk = 4096
     for c in range((Lmax + chunk - 1) // chunk):
         counts = [int(min(max(L - 1 - c * chunk, 0), chunk)) for L in lengths]
@@ -103,34 +109,37 @@ def test_sliding_window_gqa_sampled(paged):
             continue
         k, v = w.prefill_chunk(c, chunk, device="cuda")
         cache.append_rows(k, v, counts=counts)
-        for b in bs:
+        hk, hv = host(k), host(v)
+        for b in range(B):
             lo = max(0, lengths[b] - W) - c * chunk   # first window row inside this chunk
             a_, z_ = max(0, lo), counts[b]
             if z_ > a_:
-                for h in hs:
-                    keep_k[(b, h)].append((c * chunk + a_, host(k[b, h, a_:z_])))
-                    keep_v[(b, h)].append((c * chunk + a_, host(v[b, h, a_:z_])))
-        del k, v
+                keep_k[b].append(hk[b, :, a_:z_])
+                keep_v[b].append(hv[b, :, a_:z_])
+        del k, v, hk, hv
     q, k1, v1 = w.step_qkv(0, device="cuda")
     cache.append(k1, v1)
     out = cache.decode(q).cpu()                 # bf16: its own rounding allowed
-    g = w.n_q_heads // w.n_kv_heads
+    g = Hq // Hkv
     pos = cache.export(kvc.KVC_EXPORT_POSITIONS)
-    for b in range(64):
+    for b in range(B):
         assert _ring_positions_ok(pos[b], lengths[b], W), b
-    for b in bs:
+    hq, hk1, hv1 = host(q), host(k1), host(v1)
+    ref = np.empty((B, Hq, d))
+    for b in range(B):
         t = lengths[b] - 1
         lo = max(0, t - W + 1)
-        for h in hs:
-            parts_k = [(p0, x) for p0, x in keep_k[(b, h)]]
-            Kin = np.concatenate([x for _, x in parts_k] + [host(k1[b, h])[None]]) if parts_k else host(k1[b, h])[None]
-            Vin = np.concatenate([x for _, x in keep_v[(b, h)]] + [host(v1[b, h])[None]])
-            assert Kin.shape[0] == t + 1 - lo
-            K = _rows(model, Kin, np.arange(lo, t + 1))
-            V = nm.bf16_to_f32(Vin).astype(np.float64)
-            qr = model.query_rows(host(q[b, h * g:(h + 1) * g]), np.full(g, t)).astype(np.float64)
-            ref = nm.attend(qr, K, V, t, W, p0=lo)
-            assert_close(out[b, h * g:(h + 1) * g], ref, "bf16", "sliding b=%d h=%d L=%d" % (b, h, lengths[b]))
+        Kin = np.concatenate(keep_k[b] + [hk1[b][:, None]], axis=1)       # [Hkv, n, d]
+        Vin = np.concatenate(keep_v[b] + [hv1[b][:, None]], axis=1)
+        assert Kin.shape[1] == t + 1 - lo
+        K = _rows(model, Kin, np.broadcast_to(np.arange(lo, t + 1), Kin.shape[:2]))
+        V = nm.bf16_to_f32(Vin).astype(np.float64)
+        qr = model.query_rows(hq[b], np.full(Hq, t)).astype(np.float64)   # [Hq, d]
+        r = nm.attend_many([qr[h * g:(h + 1) * g] for h in range(Hkv)], [K[h] for h in range(Hkv)],
+                           [V[h] for h in range(Hkv)], [t] * Hkv, W, [lo] * Hkv, nthreads=_threads())
+        ref[b] = np.concatenate(r)
+        keep_k[b] = keep_v[b] = None
+    assert_close(out, ref, "bf16", "sliding window, every (request, head)")
     assert cache.device_status() == 0
 
 
