@@ -97,8 +97,8 @@ typedef struct {
                              request owns `capacity` slots; > 0 = K and V live in a pool
                              of page_pool pages of 16 slots (all KV heads of one request)
                              mapped by a per-request block table, allocated on append and
-                             freed by trim.  Not with INT8 or kvc_chunk_attn; capacity
-                             (the per-request logical slots) must be a multiple of 16. */
+                             freed by trim.  Not with INT8; capacity (the
+                             per-request logical slots) must be a multiple of 16. */
     int32_t store_slots;  /* device slots for saved prefills (kvc_store_save /
                              kvc_store_load), each holding one request's K, V and
                              positions; 0 = none.  Not with INT8. */
@@ -242,7 +242,15 @@ int kvc_trim(kvc_t h, const int32_t* h_cut, kvc_stream_t stream);
  * positions [max(0, p-W+1), p]:
  *     d_q [B][n][Hq][d], d_k, d_v [B][n][Hkv][d]  ->  d_out [B][n][Hq][d].
  * Row i equals what kvc_decode_attn returns for that query after appending
- * rows 0..i.  Contiguous bf16 caches without INT8; n <= max_chunk. */
+ * rows 0..i.  bf16 caches with head_dim 128, contiguous (paged or not), without
+ * INT8; n <= max_chunk.
+ * The tensor-core products take fp16 operands: the query (rotated, times
+ * log2(e)/sqrt(d)), the softmax weights and the K and V rows.  Every K and V row
+ * of the keys the call reads, and every scaled query, must be below 65520 in
+ * magnitude (the fp16 range); otherwise bit 2 of the device error word is set and
+ * the output is not valid.  Nothing else is lost: K and V values in
+ * [2^-14, 65504] are exact in fp16, smaller ones keep an absolute error of at
+ * most 2^-25. */
 int kvc_chunk_attn(kvc_t h, const void* d_q, const void* d_k, const void* d_v, int32_t n,
                    void* d_out, kvc_stream_t stream);
 
@@ -320,7 +328,8 @@ int kvc_next_positions(kvc_t h, int32_t* h_out);
 
 /* Waits for `stream`, then returns the device error word (0 = none; bit 0: a
  * kernel met a position outside the cache or RoPE table; bit 1: a bounded wait
- * gave up) and clears it. */
+ * gave up; bit 2: kvc_chunk_attn met an operand beyond the fp16 range) and
+ * clears it. */
 int kvc_device_status(kvc_t h, kvc_stream_t stream, int32_t* h_status);
 
 /* Health check of the failure path: enqueues one CTA that waits, with the same

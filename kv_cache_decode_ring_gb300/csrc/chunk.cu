@@ -4,38 +4,48 @@
 // suffix tokens[cut:] are computed in one chunk from next_position = cut:
 // suffix query i sits at position p = cut + i and attends to cached positions
 // [max(0, p - W + 1), p] (W = 0: all), exactly what a one-token decode at p
-// would see ([LEAN] §2.1 masks).  The suffix K/V rows are appended to the
-// contiguous cache first, so every key a query needs lies in one contiguous
-// run of cache rows.
+// would see ([LEAN] §2.1 masks).  The suffix K/V rows are appended to the cache
+// first, so every key a query needs is in the cache.
 //
-// This is a dense contraction, so it runs on the 5th-generation tensor cores:
-//  * CTA = 128 query rows of one query head (4 warps, thread = row); tiles of
-//    64 keys;
-//  * K and V tiles arrive by TMA (128-byte swizzle), each stage refilled as soon
-//    as the MMA that read it completes; each softmax warp rotates its rows' query
-//    half from global memory (fp32 rule of the cache keys, times log2(e)/sqrt(d))
-//    and stores it into tensor memory as bf16 hi and lo;
+// This is a dense contraction, so it runs on the 5th-generation tensor cores.
+//  * CTA = 128 query rows of two query heads that share one KV head (two "slots";
+//    the second is idle when the group has an odd number of heads).  Both slots
+//    read the same K and V tiles of 128 keys, walked backwards from the diagonal.
+//  * 16 warps: warps 0-3 and 4-7 run the softmax of slot 0 and slot 1 (thread =
+//    query row = tensor-memory lane); warps 8-11, 14 and 15 convert K and V tiles from
+//    bf16 to fp16 in shared memory; warp 12 issues the tensor copies; one thread of
+//    warp 13 issues every tcgen05.mma.  Register shares: 184 for the softmax warps, 72 for
+//    the others (setmaxnreg).
+//  * Tensor memory (512 columns): S of slot 0 and slot 1 in [0, 128) and
+//    [128, 256), fp32; the softmax writes P as fp16 pairs over the first 64 columns
+//    of its S buffer (the A operand of P.V); O of slot 0 and 1 in [256, 384) and
+//    [384, 512).  Q of both slots sits in shared memory (A operand of S = Q K^T).
+//  * Operands are fp16 on both products: the rotated query times log2(e)/sqrt(d)
+//    (relative error 2^-11), the softmax weights (<= 2^8), and the K and V rows,
+//    which are exact in fp16 for magnitudes in [2^-14, 65504] (smaller ones lose
+//    relative precision, at most 2^-25 absolute).  A query, key or value of
+//    magnitude 65520 or more would overflow: the kernel flags the device error word
+//    (kErrRange) and the call's output is not valid.
+//  * Rows of a tile outside the keys the CTA attends to (before the earliest
+//    window start, past the last suffix row, or before position 0) are zeroed by
+//    the converters, so a masked weight of 0 never meets a non-finite value.
+//  * Pipeline per slot: S(j) -> softmax(j) -> P.V(j) -> S(j+1) (S(j+1) overwrites
+//    the columns P.V(j) reads, so it waits for P.V(j) to complete); the two slots
+//    interleave on the tensor pipe, so one slot's MMAs run while the other's
+//    softmax works.
+//  * A row's reference maximum moves only when a tile exceeds it by more than 2^8
+//    (log2 domain), so weights stay <= 2^8 and O is rarely rescaled (by the
+//    softmax thread itself: at that point no P.V of its slot is in flight).
+//  * Key tiles start on 16-key boundaries.  A contiguous cache is read with two
+//    128-row tensor copies per tile; a paged cache with one 16-row copy per page
+//    and half (the block table gives the page), skipping pages before position 0.
 //  * CTAs are taken longest first (a host-sorted table of (request, query tile)
-//    items in the kernel parameters), the query heads of one item adjacent so that
-//    heads sharing a KV head read its tiles from L2;
-//  * S = Q K^T and O += P V are tcgen05.mma (bf16 in, fp32 accumulate) issued
-//    by one thread into tensor memory (two 64-column S buffers, 128-column O);
-//  * software pipeline: S of tile j + 1 is issued before the softmax of tile j
-//    and P V of tile j after it, so the tensor cores work while the threads run
-//    the softmax; two P buffers let P of tile j + 1 be written while P V of
-//    tile j still reads its own;
-//  * each thread reads its S row from tensor memory, applies the causal and
-//    window masks by absolute position, runs the online softmax in fp32 (log2
-//    domain) and writes its P row to shared memory for the next MMA.  A row's
-//    reference maximum moves only when a tile exceeds it by more than 2^8, so
-//    the O rescale in tensor memory (which must wait for the pending P V) is
-//    rare;
-//  * the rotated query and P are not exact in bf16, so each enters its MMA as
-//    two bf16 terms (hi, lo) accumulated in fp32 (about 16 significant bits);
-//  * K/V tiles are walked backwards from the diagonal;
-//  * tcgen05.ld/st are warp-collective: every lane of a warp issues them.
+//    items in the kernel parameters), the head pairs of one KV head adjacent so
+//    that they read its tiles from L2.
 // Every mbarrier wait is bounded; on expiry the kernel flags the device error
-// word, skips the remaining work and still frees its tensor memory.
+// word, skips the remaining work, waits (bounded) for its copies and MMAs in
+// flight and still frees its tensor memory.  tcgen05.ld/st are warp-collective:
+// every lane of a warp issues them.
 #include <cuda.h>
 
 #include <algorithm>
@@ -50,37 +60,49 @@
 namespace kvc {
 namespace {
 
-constexpr int kBM = 128;          // query rows per CTA
-constexpr int kBN = 128;          // keys per tile
-constexpr int kD = 128;           // head dim of this kernel
-constexpr int kSoftmaxWarps = 8;   // two per tensor-memory lane group
-constexpr int kThreads = (kSoftmaxWarps + 1) * 32;   // + one producer warp
-constexpr int kKStages = 3;       // K tile stages (free once S of the tile is complete)
-constexpr int kVStages = 2;       // V tile stages (free once P V of the tile is complete)
-constexpr float kLazyMax = 8.f;   // log2-domain headroom of a row's reference maximum
-constexpr int kTileB = 128 * kD * 2;     // 32 KB: two 64-dim halves of [128 rows][128 B]
+constexpr int kBM = 128;            // query rows per slot
+constexpr int kBN = 128;            // keys per tile
+constexpr int kD = 128;             // head dim of this kernel
+constexpr int kSlots = 2;           // query heads per CTA (sharing a KV head)
+constexpr int kWarpTma = 12;
+constexpr int kWarpMma = 13;
+constexpr int kThreads = 16 * 32;
+constexpr int kConvWarps = 6;       // warps 8-11, 14 and 15
+constexpr int kConvThreads = 32 * kConvWarps;
+constexpr int kKStages = 2;
+constexpr int kVStages = 2;
+constexpr float kLazyMax = 8.f;     // log2-domain headroom of a row's reference maximum
+constexpr int kTileB = kBN * kD * 2;     // 32 KB: two 64-dim halves of [128 rows][128 B]
 constexpr int kHalfB = kTileB / 2;
-// Operands that are not exact bf16 (the rotated query and the softmax weights)
-// enter the MMAs as two bf16 terms, hi = bf16(x) and lo = bf16(x - hi), both
-// accumulated in fp32: about 16 significant bits instead of 8.
-constexpr int OFF_X = 0;                              // row-maximum exchange [2][2][kBM] floats
-constexpr int OFF_L = OFF_X + 4 * kBM * 4;            // row sums of the two halves [2][kBM]
-constexpr int OFF_K = 4096;                           // kKStages K tiles (1024-aligned)
-constexpr int OFF_V = OFF_K + kKStages * kTileB;      // kVStages V tiles
-constexpr int OFF_BAR = OFF_V + kVStages * kTileB;    // k[3], v[2], s[2], o[2], p[2], done, q in tmem
-constexpr int kBars = kKStages + kVStages + 2 + 2 + 2 + 1 + 1;
-constexpr int kMaxItems = 2048;                       // (request, query tile) items in the order table
-constexpr int OFF_MISC = OFF_BAR + 8 * kBars;         // tensor memory base, abort flag
-constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+constexpr int kGroupB = 16 * 128;        // 16 rows of one half
+constexpr int kRegSoftmax = 184, kRegOther = 72;
+static_assert(4 * 32 * (2 * kRegSoftmax + 2 * kRegOther) == 65536, "register split sums to the launch's registers");
+
+constexpr int OFF_Q = 0;                               // Q of the two slots (fp16, 128-byte swizzle)
+constexpr int OFF_K = OFF_Q + kSlots * kTileB;         // K stages
+constexpr int OFF_V = OFF_K + kKStages * kTileB;       // V stages
+constexpr int OFF_BAR = OFF_V + kVStages * kTileB;
+enum {
+    B_KFULL = 0,                        // [stage] K copied
+    B_KCONV = B_KFULL + kKStages,       // [stage] K converted (every converter warp)
+    B_KFREE = B_KCONV + kKStages,       // [stage] both S MMAs of the tile complete
+    B_VFULL = B_KFREE + kKStages,
+    B_VCONV = B_VFULL + kVStages,
+    B_VFREE = B_VCONV + kVStages,       // [stage] both P.V MMAs of the tile complete
+    B_SFULL = B_VFREE + kVStages,       // [slot] S complete
+    B_PFULL = B_SFULL + kSlots,         // [slot] P written (4 softmax warps)
+    B_ODONE = B_PFULL + kSlots,         // [slot] P.V complete
+    B_QREADY = B_ODONE + kSlots,        // Q of both slots in shared memory (8 softmax warps)
+    B_DONE = B_QREADY + 1,              // every MMA issued so far complete (abort path)
+    kBars = B_DONE + 1
+};
+constexpr int OFF_MISC = OFF_BAR + 8 * kBars;          // tensor memory base, abort flag
+constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;       // + alignment slack of the dynamic base
 static_assert(SMEM_BYTES <= 232448, "shared memory per block");
-// Tensor memory (512 columns, 128 lanes = query rows):
-//   S/P buffers [0, 128), [128, 256): S of a tile in fp32; the softmax warp serving
-//     keys 64 h .. + 63 overwrites its 64 columns with P as bf16 pairs (hi in the first
-//     32, lo in the next 32), the A operand of P V;
-//   O [256, 384) fp32; Q hi [384, 448) and Q lo [448, 512) as bf16 pairs, the A
-//   operand of S.  Only K and V tiles are shared-memory operands.
+constexpr int kMaxItems = 2048;                        // (request, query tile) items in the order table
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColO = 256, kColQ = 384, kColQlo = 448;
+constexpr uint32_t kColO = 256;
+constexpr float kF16Limit = 65520.f;                   // rounds to infinity in fp16
 
 struct ChunkArgs {
     const int32_t* next_pos;   // after the append: cut + n
@@ -88,8 +110,10 @@ struct ChunkArgs {
     const float2* rope;        // nullptr = no RoPE
     void* out;                 // [B][n][Hq][d]
     uint32_t* hdr;
+    const int32_t* table;      // paged caches: block table [B][S/16] (else nullptr)
     int B, Hq, Hkv, g, S, W, n, out_bf16;
     int tiles;                 // query tiles per request
+    int pairs;                 // head pairs per KV head, ceil(g / 2)
     float scale_log2;
     int n_items;               // 0: natural order; else items[] = (request << 16 | tile), longest first
     uint32_t items[kMaxItems];
@@ -106,17 +130,25 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo) {
            ((uint64_t)(1024u >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
-// Instruction descriptor, kind::f16: D fp32 (bit 4), A and B bf16 (bits 7, 10),
-// B MN-major when b_mn (bit 16), N >> 3 (bits 17-22), M >> 4 (bits 24-28).
-__host__ __device__ constexpr uint32_t instr_desc(int M, int N, bool b_mn) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
-           ((uint32_t)(M >> 4) << 24);
+// Instruction descriptor, kind::f16 with A and B fp16 (format 0 in bits 7-9 and
+// 10-12) and D fp32 (bit 4); B MN-major when b_mn (bit 16), N >> 3 (bits 17-22),
+// M >> 4 (bits 24-28).
+__host__ __device__ constexpr uint32_t instr_desc_f16(int M, int N, bool b_mn) {
+    return (1u << 4) | ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-// D (tensor memory) (+)= A (tensor memory, bf16 pairs along columns, row m in lane m)
-// . B (shared memory descriptor)
-__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
-                                            int acc) {
+// D (tensor memory) (+)= A (shared memory descriptor) . B (shared memory descriptor)
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, int acc) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+// D (tensor memory) (+)= A (tensor memory, 16-bit pairs along columns, row m in
+// lane m) . B (shared memory descriptor)
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc, int acc) {
     asm volatile(
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
         " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n"
@@ -131,10 +163,10 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
 
 __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
-// 32 consecutive fp32 columns of this thread's tensor-memory lane
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
-    uint32_t r[32];
+// 32 consecutive 32-bit columns of this thread's tensor-memory lane (no wait)
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
         "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
@@ -143,29 +175,31 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
           "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
           "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
+// the same, into fp32 registers
+__device__ __forceinline__ void tmem_ld32f(uint32_t taddr, float* v) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]), "=f"(v[6]), "=f"(v[7]),
+          "=f"(v[8]), "=f"(v[9]), "=f"(v[10]), "=f"(v[11]), "=f"(v[12]), "=f"(v[13]), "=f"(v[14]), "=f"(v[15]),
+          "=f"(v[16]), "=f"(v[17]), "=f"(v[18]), "=f"(v[19]), "=f"(v[20]), "=f"(v[21]), "=f"(v[22]), "=f"(v[23]),
+          "=f"(v[24]), "=f"(v[25]), "=f"(v[26]), "=f"(v[27]), "=f"(v[28]), "=f"(v[29]), "=f"(v[30]), "=f"(v[31])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* v) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
         "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};"
-        ::"r"(taddr), "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
-          "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
-          "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
-          "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
-          "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
-          "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
-          "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
-          "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
-          "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
-          "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
-          "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+        ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+          "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]),
+          "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]),
+          "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
         : "memory");
-    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // 2^x with the hardware approximation (relative error about 2^-22; 2^-inf = 0)
 __device__ __forceinline__ float ex2(float x) {
@@ -174,24 +208,9 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-// 16 consecutive 32-bit columns of this thread's tensor-memory lane
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* v) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
-        "%14, %15, %16};"
-        ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
-          "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
-        : "memory");
-    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t* v) {
-    tmem_st16(taddr, v);
-    tmem_st16(taddr + 16, v + 16);
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
-    __nv_bfloat162 t = __floats2bfloat162_rn(a, b);
+// two fp32 values rounded to fp16 (nearest even), a in the low half
+__device__ __forceinline__ uint32_t pack_f16(float a, float b) {
+    __half2 t = __floats2half2_rn(a, b);
     return *reinterpret_cast<uint32_t*>(&t);
 }
 
@@ -199,14 +218,51 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
-// Barrier `id` over the 64 threads of a warp pair; returns the OR of `pred` over them.
-__device__ __forceinline__ bool pair_sync_or(int id, bool pred) {
-    uint32_t r;
+// Non-blocking check that phase `parity` of an mbarrier has completed.
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
     asm volatile(
-        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n barrier.red.or.pred q, %2, 64, p;\n"
-        " selp.u32 %0, 1, 0, q;\n}\n"
-        : "=r"(r) : "r"((uint32_t)pred), "r"(id) : "memory");
-    return r != 0;
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Convert one stage (a K or V tile) from bf16 to fp16 in place.  The kConvThreads
+// converter threads take 16-byte chunks t, t + kConvThreads, ..., four at a time (all
+// loads first); a chunk's row is its key (chunk q: half q / 1024, row (q mod 1024) / 8).
+// Rows whose key lies outside [klo, khi] are zeroed.  `hmax` keeps the largest fp16
+// magnitude written (infinity once a value overflowed).
+__device__ __forceinline__ void convert_tile(unsigned char* tile, int t, int kb, int klo, int khi, __half2& hmax) {
+    constexpr int kChunks = kTileB / 16;
+    const bool all_valid = kb >= klo && kb + kBN - 1 <= khi;
+#pragma unroll 1
+    for (int q0 = t; q0 < kChunks; q0 += 4 * kConvThreads) {
+        uint4 u[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int q = q0 + e * kConvThreads;
+            if (q < kChunks) u[e] = *reinterpret_cast<const uint4*>(tile + 16 * q);
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int q = q0 + e * kConvThreads;
+            if (q >= kChunks) continue;
+            const int key = kb + ((q & 1023) >> 3);
+            uint4 o = make_uint4(0u, 0u, 0u, 0u);
+            if (all_valid || (key >= klo && key <= khi)) {
+                uint32_t w[4] = {u[e].x, u[e].y, u[e].z, u[e].w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    w[k] = pack_f16(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xffff0000u));
+                    hmax = __hmax2(hmax, __habs2(*reinterpret_cast<const __half2*>(&w[k])));
+                }
+                o = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+            *reinterpret_cast<uint4*>(tile + 16 * q) = o;
+        }
+    }
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -215,44 +271,51 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    unsigned char* sQ = smem + OFF_Q;
     unsigned char* sK = smem + OFF_K;
     unsigned char* sV = smem + OFF_V;
-    float* xmax = reinterpret_cast<float*>(smem + OFF_X);   // [parity][half][row]
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
-    uint64_t* bk = bar;                      // [stage] K tile landed
-    uint64_t* bv = bk + kKStages;            // [stage] V tile landed
-    uint64_t* bs = bv + kVStages;            // [buffer] S = Q K^T complete
-    uint64_t* bo = bs + 2;                   // [buffer] O += P V complete
-    uint64_t* bp = bo + 2;                   // [buffer] P written by the 8 softmax warps
-    uint64_t* bdone = bp + 2;                // every MMA issued so far complete (abort path)
-    uint64_t* bqt = bdone + 1;               // Q copied into tensor memory by the 8 softmax warps
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // this CTA's (request, query tile, query head)
+    // this CTA's (request, query tile) item and head pair
+    const int per_item = a.Hkv * a.pairs;
+    const int item = blockIdx.x / per_item, hp = blockIdx.x % per_item;
+    const int kvh = hp / a.pairs, pi = hp % a.pairs;
+    const int nslots = (2 * pi + 1 < a.g) ? 2 : 1;
     int b, tile;
-    const int hq = blockIdx.x % a.Hq, item = blockIdx.x / a.Hq;
     if (a.n_items > 0) { b = (int)(a.items[item] >> 16); tile = (int)(a.items[item] & 0xFFFFu); }
     else { b = item / a.tiles; tile = item % a.tiles; }
     const int i0 = tile * kBM;
-    const int kvh = hq / a.g;
     const int np = a.next_pos[b];
     const int cut = np - a.n;
     const int rows = min(kBM, a.n - i0);
     const int p_first = cut + i0, p_last = cut + i0 + rows - 1;
-    const int lo = a.W > 0 ? max(0, p_first - a.W + 1) : 0;
-    const int ntiles = (p_last + 1 - lo + kBN - 1) / kBN;
-    const int head_row0 = (b * a.Hkv + kvh) * a.S;
+    // keys the CTA attends to: [kmin, p_last]; tiles end at kt (16-aligned) and walk back
+    const int kmin = a.W > 0 ? max(0, p_first - a.W + 1) : 0;
+    const int key_lo_max = a.W > 0 ? max(0, p_last - a.W + 1) : 0;
+    const int kt = (p_last + 16) & ~15;
+    const int ntiles = (kt - (kmin & ~15) + kBN - 1) / kBN;
 
     if (tid == 0) {
-        for (int i = 0; i < kBars; ++i) mbar_init(&bar[i], 1);
-        for (int i = 0; i < 2; ++i) mbar_init(&bp[i], kSoftmaxWarps);
-        mbar_init(bqt, kSoftmaxWarps);
+        for (int s = 0; s < kKStages; ++s) {
+            mbar_init(&bar[B_KFULL + s], 1); mbar_init(&bar[B_KCONV + s], kConvWarps);
+            mbar_init(&bar[B_KFREE + s], 1);
+        }
+        for (int s = 0; s < kVStages; ++s) {
+            mbar_init(&bar[B_VFULL + s], 1); mbar_init(&bar[B_VCONV + s], kConvWarps);
+            mbar_init(&bar[B_VFREE + s], 1);
+        }
+        for (int s = 0; s < kSlots; ++s) {
+            mbar_init(&bar[B_SFULL + s], 1); mbar_init(&bar[B_PFULL + s], 4); mbar_init(&bar[B_ODONE + s], 1);
+        }
+        mbar_init(&bar[B_QREADY], 8);
+        mbar_init(&bar[B_DONE], 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == kSoftmaxWarps) {
+    if (warp == kWarpMma) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
                      ::"r"(smem_u32(tmem_slot)), "r"(kTmemCols) : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
@@ -261,145 +324,57 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tO = tmem + kColO;
+    // every warpgroup changes its register share together
+    if (warp < 8) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegSoftmax));
+    else asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegOther));
 
-    if (warp == kSoftmaxWarps) {
-        // ================= producer: one thread issues every copy and every MMA
-        if (lane == 0) {
-            constexpr uint32_t idesc_qk = instr_desc(kBM, kBN, false);
-            constexpr uint32_t idesc_pv = instr_desc(kBM, kD, true);
-            auto kbase_of = [&](int j) { return p_last + 1 - kBN * (j + 1); };
-            auto load_k = [&](int j) {
-                const int st = j % kKStages;
-                mbar_arrive_expect_tx(&bk[st], kTileB);
-                tma_load_2d(sK + st * kTileB, &tmK, 0, head_row0 + kbase_of(j), &bk[st]);
-                tma_load_2d(sK + st * kTileB + kHalfB, &tmK, 64, head_row0 + kbase_of(j), &bk[st]);
-            };
-            auto load_v = [&](int j) {
-                const int st = j % kVStages;
-                mbar_arrive_expect_tx(&bv[st], kTileB);
-                tma_load_2d(sV + st * kTileB, &tmV, 0, head_row0 + kbase_of(j), &bv[st]);
-                tma_load_2d(sV + st * kTileB + kHalfB, &tmV, 64, head_row0 + kbase_of(j), &bv[st]);
-            };
-            // descriptors of stage 0; stage and k-step offsets move only the start address
-            // field (bytes / 16, no carry: shared addresses stay below 256 KB)
-            const uint64_t kdesc0 = smem_desc(smem_u32(sK), 16), vdesc0 = smem_desc(smem_u32(sV), kHalfB);
-            // S_j = Q_hi K_j^T + Q_lo K_j^T into S/P buffer j % 2 (Q: dims 16 s .. + 15 in
-            // columns 8 s .. + 7 of its region)
-            auto issue_s = [&](int j) {
-                const uint64_t kd = kdesc0 + (uint64_t)((j % kKStages) * (kTileB >> 4));
-                const uint32_t d = tmem + 128 * (j & 1);
-#pragma unroll
-                for (int s = 0; s < kD / 16; ++s)
-                    mma_bf16_ts(d, tmem + kColQ + 8 * s, kd + (uint64_t)(((s >> 2) * kHalfB + (s & 3) * 32) >> 4),
-                                idesc_qk, s > 0);
-#pragma unroll
-                for (int s = 0; s < kD / 16; ++s)
-                    mma_bf16_ts(d, tmem + kColQlo + 8 * s, kd + (uint64_t)(((s >> 2) * kHalfB + (s & 3) * 32) >> 4),
-                                idesc_qk, 1);
-                mma_commit(&bs[j & 1]);
-            };
-            // O += P_hi V_j + P_lo V_j: keys 16 s2 .. + 15 of P sit in columns
-            // 64 (s2 / 4) + 8 (s2 % 4) .. + 7 of S/P buffer j % 2 (lo 32 columns further)
-            auto issue_pv = [&](int j) {
-                const uint32_t pb = tmem + 128 * (j & 1);
-                const uint64_t vd = vdesc0 + (uint64_t)((j % kVStages) * (kTileB >> 4));
-#pragma unroll
-                for (int s2 = 0; s2 < kBN / 16; ++s2)
-                    mma_bf16_ts(tO, pb + 64 * (s2 >> 2) + 8 * (s2 & 3), vd + (uint64_t)((s2 * 2048) >> 4), idesc_pv,
-                                (j > 0 || s2 > 0));
-#pragma unroll
-                for (int s2 = 0; s2 < kBN / 16; ++s2)
-                    mma_bf16_ts(tO, pb + 64 * (s2 >> 2) + 32 + 8 * (s2 & 3), vd + (uint64_t)((s2 * 2048) >> 4),
-                                idesc_pv, 1);
-                mma_commit(&bo[j & 1]);
-            };
+    auto kbase = [&](int j) { return kt - kBN * (j + 1); };   // first key of tile j
 
-            bool ok = true;
-            // copies issued and awaited so far (an abort drains the rest before exit)
-            int k_issued = 0, v_issued = 0, k_waited = 0, v_waited = 0;
-            for (int j = 0; j < kKStages && j < ntiles; ++j) { load_k(j); k_issued = j + 1; }
-            for (int j = 0; j < kVStages && j < ntiles; ++j) { load_v(j); v_issued = j + 1; }
-            ok = mbar_wait(bqt, 0);                  // the softmax warps stored Q into tensor memory
-            for (int j = 0; j < 2 && j < ntiles && ok; ++j) {
-                ok = mbar_wait(&bk[j], 0);
-                if (ok) { k_waited = j + 1; fence_after(); issue_s(j); }
-            }
-            for (int j = 0; j < ntiles && ok; ++j) {
-                if (*abort_flag) { ok = false; break; }
-                // P_j written: the softmax warps read S_j, so S_j is complete and the K stage
-                // of tile j is free: fetch K of tile j + kKStages
-                ok = mbar_wait(&bp[j & 1], (uint32_t)((j >> 1) & 1));
-                if (!ok) break;
-                if (j + kKStages < ntiles) { load_k(j + kKStages); k_issued = j + kKStages + 1; }
-                // O += P_j V_j
-                ok = mbar_wait(&bv[j % kVStages], (uint32_t)((j / kVStages) & 1));
-                if (!ok) break;
-                v_waited = j + 1;
-                fence_after();
-                issue_pv(j);
-                if (j + 2 < ntiles) {
-                    // S_{j+2} overwrites P_j's buffer: wait for P V_j (which also frees the
-                    // V stage of tile j), then fetch V of tile j + 2 and issue S_{j+2}
-                    ok = mbar_wait(&bo[j & 1], (uint32_t)((j >> 1) & 1));
-                    if (!ok) break;
-                    load_v(j + 2);
-                    v_issued = j + 3;
-                    ok = mbar_wait(&bk[(j + 2) % kKStages], (uint32_t)(((j + 2) / kKStages) & 1));
-                    if (!ok) break;
-                    k_waited = j + 3;
-                    fence_after();
-                    issue_s(j + 2);
-                }
-            }
-            if (!ok) {
-                *abort_flag = 1;
-                atomicOr(a.hdr, kErrWait);
-                // let every copy still in flight land before the CTA can exit
-                for (int t = k_waited; t < k_issued; ++t) mbar_wait(&bk[t % kKStages], (uint32_t)((t / kKStages) & 1));
-                for (int t = v_waited; t < v_issued; ++t) mbar_wait(&bv[t % kVStages], (uint32_t)((t / kVStages) & 1));
-            }
-        }
-    } else {
-        // ================= softmax warps: warp w serves rows 32 (w % 4) .. + 31 (its
-        // tensor-memory lanes) and keys 64 (w / 4) .. + 63 of every tile; the two warps of
-        // a row pair exchange their halves' maxima through shared memory
-        const int lg = warp & 3, hf = warp >> 2;
-        const int row = 32 * lg + lane;            // query row = tensor-memory lane
+    if (warp < 8) {
+        // ================= softmax: warp w serves slot w / 4, rows 32 (w % 4) .. + 31
+        const int slot = warp >> 2, lg = warp & 3;
+        const int row = 32 * lg + lane;
         const uint32_t lane_off = (uint32_t)(32 * lg) << 16;
-        const int p = cut + i0 + row;               // its absolute position
-        const bool row_valid = row < rows;
+        const uint32_t tS = tmem + 128 * slot + lane_off;
+        const uint32_t tO = tmem + kColO + 128 * slot + lane_off;
+        const bool slot_valid = slot < nslots;
+        const int hq = kvh * a.g + 2 * pi + slot;
+        const int p = cut + i0 + row;
+        const bool row_valid = slot_valid && row < rows;
         const int key_lo = a.W > 0 ? max(0, p - a.W + 1) : 0;
-        const int key_lo_max = a.W > 0 ? max(0, p_last - a.W + 1) : 0;   // the CTA's largest key_lo
-        const int pair_bar = 1 + lg;               // named barrier of the pair (0 = __syncthreads)
-        float m_ref = -INFINITY, l = 0.f;
         bool fail = false;
         {
-            // this warp's half of its row's query (dims 64 hf .. + 63): rotated at the row's
-            // position in fp32, times log2(e)/sqrt(d), split into bf16 hi = bf16(y) and
-            // lo = bf16(y - hi), stored into tensor memory as bf16 pairs along columns
-            uint32_t qh[32], ql[32];
-            if (row_valid) {
-                // every load first (one round trip): 8 x 16 B of the query half, 16 x 16 B
-                // of its {cos, sin} pairs
-                const uint4* qrow = reinterpret_cast<const uint4*>(
-                    a.q + (((size_t)b * a.n + i0 + row) * a.Hq + hq) * kD + 64 * hf);
+            // the row's query, rotated at p in fp32, times log2(e)/sqrt(d), rounded to fp16
+            // and stored in the slot's Q tile (128-byte swizzle: 16-byte chunk c of row r at
+            // c ^ (r mod 8)), two 64-dim halves with all loads of a half in one round trip
+            float qmax = 0.f;
+            unsigned char* qt = sQ + slot * kTileB;
+#pragma unroll 1
+            for (int hf = 0; hf < 2; ++hf) {
                 uint4 qv[8];
                 float4 rv[16];
 #pragma unroll
-                for (int c = 0; c < 8; ++c) qv[c] = __ldg(qrow + c);
-                if (a.rope) {
-                    const float4* rp = reinterpret_cast<const float4*>(a.rope + (size_t)p * (kD / 2) + 32 * hf);
+                for (int c = 0; c < 8; ++c) qv[c] = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-                    for (int c = 0; c < 16; ++c) rv[c] = __ldg(rp + c);
+                for (int c = 0; c < 16; ++c) rv[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (row_valid) {
+                    const uint4* qrow = reinterpret_cast<const uint4*>(
+                        a.q + (((size_t)b * a.n + i0 + row) * a.Hq + hq) * kD + 64 * hf);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) qv[c] = __ldg(qrow + c);
+                    if (a.rope) {
+                        const float4* rp = reinterpret_cast<const float4*>(a.rope + (size_t)p * (kD / 2) + 32 * hf);
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) rv[c] = __ldg(rp + c);
+                    }
                 }
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
-                    const uint32_t wq[4] = {qv[c].x, qv[c].y, qv[c].z, qv[c].w};
+                    uint32_t wq[4] = {qv[c].x, qv[c].y, qv[c].z, qv[c].w};
+                    uint32_t h4[4];
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
-                        const __nv_bfloat162 x2 = *reinterpret_cast<const __nv_bfloat162*>(&wq[k]);
-                        const float x0 = __low2float(x2), x1 = __high2float(x2);
+                        const float x0 = __uint_as_float(wq[k] << 16), x1 = __uint_as_float(wq[k] & 0xffff0000u);
                         float y0 = x0, y1 = x1;
                         if (a.rope) {
                             const float4 r4 = rv[(4 * c + k) >> 1];
@@ -408,161 +383,281 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         y0 = __fmul_rn(y0, a.scale_log2);
                         y1 = __fmul_rn(y1, a.scale_log2);
-                        const __nv_bfloat162 h2 = __floats2bfloat162_rn(y0, y1);
-                        qh[4 * c + k] = *reinterpret_cast<const uint32_t*>(&h2);
-                        ql[4 * c + k] = pack_bf16(__fsub_rn(y0, __low2float(h2)), __fsub_rn(y1, __high2float(h2)));
+                        qmax = fmaxf(qmax, fmaxf(fabsf(y0), fabsf(y1)));
+                        h4[k] = row_valid ? pack_f16(y0, y1) : 0u;
                     }
+                    *reinterpret_cast<uint4*>(qt + hf * kHalfB + row * 128 + ((c ^ (row & 7)) << 4)) =
+                        make_uint4(h4[0], h4[1], h4[2], h4[3]);
                 }
-            } else {
-#pragma unroll
-                for (int e = 0; e < 32; ++e) { qh[e] = 0u; ql[e] = 0u; }
             }
-            tmem_st32u(tmem + kColQ + 32 * hf + lane_off, qh);
-            tmem_st32u(tmem + kColQlo + 32 * hf + lane_off, ql);
-            fence_before();
+            if (row_valid && qmax >= kF16Limit) atomicOr(a.hdr, kErrRange);
+            fence_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bqt);
+            if (lane == 0) mbar_arrive(&bar[B_QREADY]);
         }
-        for (int j = 0; j < ntiles; ++j) {
-            // (1) S_j complete; this warp's 64 scores of the row
-            bool w = !fail && mbar_wait(&bs[j & 1], (uint32_t)((j >> 1) & 1)) && !*abort_flag;
-            w = __all_sync(0xffffffffu, w);
-            float sm[kBN / 2];
-            float mx = -INFINITY;
-            const int kb = p_last + 1 - kBN * (j + 1) + 64 * hf;         // first key of this half
-            const uint32_t tSj = tmem + 128 * (j & 1) + 64 * hf + lane_off;
-            if (w) {
+        float m_ref = -INFINITY, l = 0.f;
+        if (slot_valid) {
+            for (int j = 0; j < ntiles; ++j) {
+                bool w = mbar_wait(&bar[B_SFULL + slot], (uint32_t)(j & 1)) && !*abort_flag;
+                if (!__all_sync(0xffffffffu, w)) { fail = true; break; }
                 fence_after();
-                tmem_ld32(tSj, sm);
-                tmem_ld32(tSj + 32, sm + 32);
-                if (kb - 64 * hf >= key_lo_max && kb - 64 * hf + kBN - 1 <= p_first) {
-                    // every key of the tile is visible to every row of the CTA
+                float s[kBN];
+                tmem_ld32f(tS, s);
+                tmem_ld32f(tS + 32, s + 32);
+                tmem_ld32f(tS + 64, s + 64);
+                tmem_ld32f(tS + 96, s + 96);
+                tmem_wait_ld();
+                const int kb = kbase(j);
+                if (!(kb >= key_lo_max && kb + kBN - 1 <= p_first && row_valid)) {
+                    // some key of the tile is masked for some row of the CTA
 #pragma unroll
-                    for (int c = 0; c < kBN / 2; ++c) mx = fmaxf(mx, sm[c]);
-                } else {
-#pragma unroll
-                    for (int c = 0; c < kBN / 2; ++c) {
+                    for (int c = 0; c < kBN; ++c) {
                         const bool vis = row_valid && kb + c >= key_lo && kb + c <= p;
-                        sm[c] = vis ? sm[c] : -INFINITY;
-                        mx = fmaxf(mx, sm[c]);
+                        s[c] = vis ? s[c] : -INFINITY;
                     }
                 }
-            }
-            // (2) exchange the halves' maxima (and any failure) with the partner warp
-            xmax[((j & 1) * 2 + hf) * kBM + row] = mx;
-            if (pair_sync_or(pair_bar, !w)) { fail = true; break; }
-            mx = fmaxf(mx, xmax[((j & 1) * 2 + (1 - hf)) * kBM + row]);
-            // (3) the reference maximum moves only when the tile exceeds it by more than kLazyMax
-            bool grow = false;
-            float alpha = 1.f;
-            if (mx > m_ref + kLazyMax) {           // also the first visible tile (m_ref = -inf)
-                grow = m_ref != -INFINITY;        // O and l hold earlier tiles only then
-                alpha = grow ? exp2f(m_ref - mx) : 1.f;
-                m_ref = mx;
-            }
-            const float base = m_ref == -INFINITY ? 0.f : m_ref;
-            float2 rs2 = make_float2(0.f, 0.f);
+                // row maximum as a tree (eight independent chains, then three steps)
+                float m8[8];
 #pragma unroll
-            for (int c = 0; c < kBN / 2; c += 2) {
-                sm[c] = ex2(sm[c] - base);         // masked keys: 0
-                sm[c + 1] = ex2(sm[c + 1] - base);
-                rs2 = __fadd2_rn(rs2, make_float2(sm[c], sm[c + 1]));
-            }
-            l = l * alpha + (rs2.x + rs2.y);
-            // (4) O may be rescaled only once P V of tile j - 1 is complete
-            // (tcgen05.ld/st: whole warps)
-            const bool any_grow = __any_sync(0xffffffffu, grow);
-            if (any_grow) {
-                if (!__all_sync(0xffffffffu, mbar_wait(&bo[(j - 1) & 1], (uint32_t)(((j - 1) >> 1) & 1)))) {
-                    fail = true;                   // the partner learns at the next exchange
-                } else {
-                    fence_after();
+                for (int e = 0; e < 8; ++e) m8[e] = s[e];
+#pragma unroll
+                for (int c = 8; c < kBN; c += 8)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) m8[e] = fmaxf(m8[e], s[c + e]);
+                const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                       fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+                // the reference maximum moves only when the tile exceeds it by more than kLazyMax;
+                // then O (complete up to P.V of tile j - 1: S of this tile waited for it) is rescaled
+                bool grow = false;
+                float alpha = 1.f;
+                if (mx > m_ref + kLazyMax) {
+                    grow = m_ref != -INFINITY;
+                    alpha = grow ? ex2(m_ref - mx) : 1.f;
+                    m_ref = mx;
+                }
+                if (__any_sync(0xffffffffu, grow)) {
                     const float f = grow ? alpha : 1.f;
+#pragma unroll 1
+                    for (int c = 0; c < kD; c += 32) {
+                        uint32_t o[32];
+                        tmem_ld32(tO + c, o);
+                        tmem_wait_ld();
 #pragma unroll
-                    for (int c = 0; c < kD / 2; c += 32) {
-                        float o[32];
-                        tmem_ld32(tO + lane_off + 64 * hf + c, o);
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+                        tmem_st32(tO + c, o);
+                    }
+                    tmem_wait_st();
+                }
+                const float base = m_ref == -INFINITY ? 0.f : m_ref;
+                uint32_t pk[kBN / 2];
+                float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                make_float2(0.f, 0.f)};
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] *= f;
-                        tmem_st32(tO + lane_off + 64 * hf + c, o);
+                for (int e = 0; e < kBN / 2; ++e) {
+                    const float p0 = ex2(s[2 * e] - base), p1 = ex2(s[2 * e + 1] - base);   // masked keys: 0
+                    rs[e & 3] = __fadd2_rn(rs[e & 3], make_float2(p0, p1));
+                    pk[e] = pack_f16(p0, p1);
+                }
+                const float2 r01 = __fadd2_rn(rs[0], rs[1]), r23 = __fadd2_rn(rs[2], rs[3]);
+                const float2 r4 = __fadd2_rn(r01, r23);
+                l = l * alpha + (r4.x + r4.y);
+                tmem_st32(tS, pk);
+                tmem_st32(tS + 32, pk + 32);
+                tmem_wait_st();
+                fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar[B_PFULL + slot]);
+            }
+            // the last P.V complete before O is read
+            if (!fail && ntiles > 0) {
+                const bool w = mbar_wait(&bar[B_ODONE + slot], (uint32_t)((ntiles - 1) & 1));
+                fail = !__all_sync(0xffffffffu, w);
+            }
+            if (fail) {
+                if (lane == 0) atomicOr(a.hdr, kErrWait);
+                *abort_flag = 1;
+            } else if (!*abort_flag) {
+                // epilogue: O / l
+                fence_after();
+                const float inv = l > 0.f ? 1.f / l : 0.f;
+                const size_t orow = (((size_t)b * a.n + i0 + row) * a.Hq + hq) * kD;
+#pragma unroll 1
+                for (int c = 0; c < kD; c += 32) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + c, o);
+                    tmem_wait_ld();
+                    if (!row_valid) continue;
+                    if (a.out_bf16) {
+                        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + orow + c);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            uint32_t u[4];
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                __nv_bfloat162 t2 = __floats2bfloat162_rn(__uint_as_float(o[8 * e + 2 * k]) * inv,
+                                                                          __uint_as_float(o[8 * e + 2 * k + 1]) * inv);
+                                u[k] = *reinterpret_cast<uint32_t*>(&t2);
+                            }
+                            dst[e] = make_uint4(u[0], u[1], u[2], u[3]);
+                        }
+                    } else {
+                        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + orow + c);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            dst[e] = make_float4(__uint_as_float(o[4 * e]) * inv, __uint_as_float(o[4 * e + 1]) * inv,
+                                                 __uint_as_float(o[4 * e + 2]) * inv,
+                                                 __uint_as_float(o[4 * e + 3]) * inv);
                     }
                 }
             }
-            if (fail) continue;                    // skip the write; the next exchange ends the loop
-            // (5) this warp's 64 keys of the P row over its own S columns: hi and lo bf16
-            // pairs (keys 64 hf + 2 e, + 1 in column e; lo 32 columns further)
-            uint32_t hi[32], lo2[32];
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                const float2 x = make_float2(sm[2 * e], sm[2 * e + 1]);
-                const __nv_bfloat162 h2 = __floats2bfloat162_rn(x.x, x.y);
-                const float2 r = __ffma2_rn(__bfloat1622float2(h2), make_float2(-1.f, -1.f), x);   // x - hi, exact
-                hi[e] = *reinterpret_cast<const uint32_t*>(&h2);
-                lo2[e] = pack_bf16(r.x, r.y);
-            }
-            tmem_st32u(tSj, hi);
-            tmem_st32u(tSj + 32, lo2);
-            fence_before();
+        }
+    } else if (warp < kWarpTma || warp > kWarpMma) {
+        // ================= converters (warps 8-11, 14, 15): K and V tiles bf16 -> fp16 in place
+        const int t = warp < kWarpTma ? tid - 8 * 32 : tid - 10 * 32;
+        __half2 hmax = __float2half2_rn(0.f);
+        bool ok = true;
+        for (int j = 0; j < ntiles && ok; ++j) {
+            const int kb = kbase(j);
+            const int ks = j % kKStages, vs = j % kVStages;
+            ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_KFULL + ks], (uint32_t)((j / kKStages) & 1)) &&
+                                             !*abort_flag);
+            if (!ok) break;
+            convert_tile(sK + ks * kTileB, t, kb, kmin, p_last, hmax);
+            fence_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bp[j & 1]);
+            if (lane == 0) mbar_arrive(&bar[B_KCONV + ks]);
+            ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_VFULL + vs], (uint32_t)((j / kVStages) & 1)) &&
+                                             !*abort_flag);
+            if (!ok) break;
+            convert_tile(sV + vs * kTileB, t, kb, kmin, p_last, hmax);
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar[B_VCONV + vs]);
         }
-        // the last P V complete before O is read
-        if (!fail && ntiles > 0) {
-            const bool w = mbar_wait(&bo[(ntiles - 1) & 1], (uint32_t)(((ntiles - 1) >> 1) & 1));
-            fail = !__all_sync(0xffffffffu, w);
-        }
-        if (fail) {
+        if (!ok) {
             if (lane == 0) atomicOr(a.hdr, kErrWait);
             *abort_flag = 1;
         }
-        // partial row sums of the two halves
-        reinterpret_cast<float*>(smem + OFF_L)[hf * kBM + row] = l;
-    }
-    __syncthreads();
-    const bool aborted = *abort_flag != 0;
-    if (warp < kSoftmaxWarps && !aborted) {
-        // ---- epilogue: O / l; warp w stores columns 64 (w / 4) .. + 63 of its rows
-        const int lg = warp & 3, hf = warp >> 2;
-        const int row = 32 * lg + lane;
-        const uint32_t lane_off = (uint32_t)(32 * lg) << 16;
-        fence_after();
-        const float* lsum = reinterpret_cast<const float*>(smem + OFF_L);
-        const float L = lsum[row] + lsum[kBM + row];
-        const float inv = L > 0.f ? 1.f / L : 0.f;
-        const size_t orow = (((size_t)b * a.n + i0 + row) * a.Hq + hq) * kD + 64 * hf;
-#pragma unroll
-        for (int c = 0; c < kD / 2; c += 32) {
-            float o[32];
-            tmem_ld32(tO + lane_off + 64 * hf + c, o);
-            if (row >= rows) continue;
-            if (a.out_bf16) {
-                uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + orow + c);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    uint4 u;
-                    u.x = pack_bf16(o[8 * e + 0] * inv, o[8 * e + 1] * inv);
-                    u.y = pack_bf16(o[8 * e + 2] * inv, o[8 * e + 3] * inv);
-                    u.z = pack_bf16(o[8 * e + 4] * inv, o[8 * e + 5] * inv);
-                    u.w = pack_bf16(o[8 * e + 6] * inv, o[8 * e + 7] * inv);
-                    dst[e] = u;
+        const float2 hm = __half22float2(hmax);
+        if (__any_sync(0xffffffffu, fmaxf(hm.x, hm.y) >= kF16Limit) && lane == 0) atomicOr(a.hdr, kErrRange);
+    } else if (warp == kWarpTma) {
+        // ================= tensor copies of K and V tiles
+        if (lane == 0) {
+            const int head_row0 = (b * a.Hkv + kvh) * a.S;
+            const int npages = a.S / kPage;
+            // one tile of one tensor into `dst`: two 128-row copies (contiguous cache) or one
+            // 16-row copy per page and half (paged cache; pages before position 0 skipped)
+            auto load_tile = [&](const CUtensorMap* tm, unsigned char* dst, uint64_t* full, int kb) {
+                if (!a.table) {
+                    mbar_arrive_expect_tx(full, kTileB);
+                    tma_load_2d(dst, tm, 0, head_row0 + kb, full);
+                    tma_load_2d(dst + kHalfB, tm, 64, head_row0 + kb, full);
+                    return;
                 }
-            } else {
-                float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + orow + c);
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    dst[e] = make_float4(o[4 * e] * inv, o[4 * e + 1] * inv, o[4 * e + 2] * inv, o[4 * e + 3] * inv);
+                const int g0 = kb < 0 ? (-kb) / 16 : 0;
+                mbar_arrive_expect_tx(full, (uint32_t)(kBN / 16 - g0) * 2 * kGroupB);
+                for (int gi = g0; gi < kBN / 16; ++gi) {
+                    const int lp = (kb >> 4) + gi;
+                    int page = lp < npages ? a.table[(size_t)b * npages + lp] : -1;
+                    page = page < 0 ? 0 : page;      // never taken: every page the CTA reads is mapped
+                    const int r = (page * a.Hkv + kvh) * kPage;
+                    tma_load_2d(dst + gi * kGroupB, tm, 0, r, full);
+                    tma_load_2d(dst + kHalfB + gi * kGroupB, tm, 64, r, full);
+                }
+            };
+            bool ok = true;
+            int k_issued = 0, v_issued = 0;
+            for (int j = 0; j < ntiles && ok; ++j) {
+                const int ks = j % kKStages, vs = j % kVStages;
+                if (j >= kKStages) ok = mbar_wait(&bar[B_KFREE + ks], (uint32_t)((j / kKStages - 1) & 1));
+                if (!ok || *abort_flag) { ok = false; break; }
+                load_tile(&tmK, sK + ks * kTileB, &bar[B_KFULL + ks], kbase(j));
+                k_issued = j + 1;
+                if (j >= kVStages) ok = mbar_wait(&bar[B_VFREE + vs], (uint32_t)((j / kVStages - 1) & 1));
+                if (!ok || *abort_flag) { ok = false; break; }
+                load_tile(&tmV, sV + vs * kTileB, &bar[B_VFULL + vs], kbase(j));
+                v_issued = j + 1;
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                atomicOr(a.hdr, kErrWait);
+                // the last copy issued into each stage lands before the CTA can exit
+                for (int t = max(0, k_issued - kKStages); t < k_issued; ++t)
+                    mbar_wait(&bar[B_KFULL + t % kKStages], (uint32_t)((t / kKStages) & 1));
+                for (int t = max(0, v_issued - kVStages); t < v_issued; ++t)
+                    mbar_wait(&bar[B_VFULL + t % kVStages], (uint32_t)((t / kVStages) & 1));
             }
         }
-    }
-    if (warp == kSoftmaxWarps && aborted && lane == 0) {
-        // make sure no tensor-core operation still targets our columns before freeing
-        // them: a commit tracks every MMA this thread issued
-        mma_commit(bdone);
-        mbar_wait(bdone, 0);
+    } else if (warp == kWarpMma) {
+        // ================= one thread issues every MMA, whichever is ready first
+        if (lane == 0) {
+            constexpr uint32_t idesc_qk = instr_desc_f16(kBM, kBN, false);
+            constexpr uint32_t idesc_pv = instr_desc_f16(kBM, kD, true);
+            // descriptors of slot 0 / stage 0; other slots, stages and k-steps move only the
+            // start address field (bytes / 16, no carry: shared addresses stay below 256 KB)
+            const uint64_t qdesc0 = smem_desc(smem_u32(sQ), 16), kdesc0 = smem_desc(smem_u32(sK), 16);
+            const uint64_t vdesc0 = smem_desc(smem_u32(sV), kHalfB);
+            auto koff = [](int s) { return (uint64_t)(((s >> 2) * kHalfB + (s & 3) * 32) >> 4); };
+            // S_i(j) = Q_i K_j^T into S buffer i (dims 16 s .. + 15 per instruction)
+            auto issue_s = [&](int i, int j) {
+                const uint64_t qd = qdesc0 + (uint64_t)(i * (kTileB >> 4));
+                const uint64_t kd = kdesc0 + (uint64_t)((j % kKStages) * (kTileB >> 4));
+#pragma unroll
+                for (int s = 0; s < kD / 16; ++s) mma_ss(tmem + 128 * i, qd + koff(s), kd + koff(s), idesc_qk, s > 0);
+                mma_commit(&bar[B_SFULL + i]);
+            };
+            // O_i += P_i(j) V_j: keys 16 s .. + 15 of P sit in columns 8 s .. + 7 of S buffer i
+            auto issue_pv = [&](int i, int j) {
+                const uint64_t vd = vdesc0 + (uint64_t)((j % kVStages) * (kTileB >> 4));
+#pragma unroll
+                for (int s = 0; s < kBN / 16; ++s)
+                    mma_ts(tmem + kColO + 128 * i, tmem + 128 * i + 8 * s, vd + (uint64_t)((s * 2048) >> 4), idesc_pv,
+                           (j > 0 || s > 0));
+                mma_commit(&bar[B_ODONE + i]);
+            };
+            // per slot: S(j) -> [softmax writes P(j)] -> P.V(j) -> S(j + 1) once P.V(j) is
+            // complete (S(j + 1) overwrites the P columns P.V(j) reads); the slots alternate
+            auto wait_ok = [&](uint64_t* bar_, uint32_t parity) { return mbar_wait(bar_, parity) && !*abort_flag; };
+            bool ok = wait_ok(&bar[B_QREADY], 0) && wait_ok(&bar[B_KCONV], 0);
+            if (ok) {
+                fence_after();
+                for (int i = 0; i < nslots; ++i) issue_s(i, 0);
+                mma_commit(&bar[B_KFREE]);
+            }
+            for (int j = 0; j < ntiles && ok; ++j) {
+                const int vs = j % kVStages, ks1 = (j + 1) % kKStages;
+                ok = wait_ok(&bar[B_VCONV + vs], (uint32_t)((j / kVStages) & 1));
+                for (int i = 0; i < nslots && ok; ++i) {
+                    ok = wait_ok(&bar[B_PFULL + i], (uint32_t)(j & 1));
+                    if (!ok) break;
+                    fence_after();
+                    issue_pv(i, j);
+                    if (j + 1 < ntiles) {
+                        if (i == 0) ok = wait_ok(&bar[B_KCONV + ks1], (uint32_t)(((j + 1) / kKStages) & 1));
+                        if (ok) ok = wait_ok(&bar[B_ODONE + i], (uint32_t)(j & 1));
+                        if (!ok) break;
+                        fence_after();
+                        issue_s(i, j + 1);
+                    }
+                }
+                if (!ok) break;
+                mma_commit(&bar[B_VFREE + vs]);                       // both P.V of tile j issued
+                if (j + 1 < ntiles) mma_commit(&bar[B_KFREE + ks1]);  // both S of tile j + 1 issued
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                atomicOr(a.hdr, kErrWait);
+            }
+            // no tensor-core operation may still target our columns when they are freed:
+            // a commit tracks every MMA this thread issued
+            mma_commit(&bar[B_DONE]);
+            mbar_wait(&bar[B_DONE], 0);
+        }
     }
     fence_before();
     __syncthreads();
-    if (warp == kSoftmaxWarps) {
+    if (warp == kWarpMma) {
+        __syncwarp();
         fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
     }
@@ -603,9 +698,10 @@ bool chunk_supported(const Shape& s) { return s.bf16 && !s.int8 && !s.ring && s.
 cudaError_t launch_chunk(kvc_handle* h, const void* q, void* out, int n, cudaStream_t st) {
     const Shape& s = h->sh;
     CUtensorMap tk, tv;
-    const cuuint64_t kdims[2] = {(cuuint64_t)s.d, (cuuint64_t)s.B * s.Hkv * s.S};
+    const cuuint64_t rows = s.pages ? (cuuint64_t)s.pages * s.Hkv * kPage : (cuuint64_t)s.B * s.Hkv * s.S;
+    const cuuint64_t kdims[2] = {(cuuint64_t)s.d, rows};
     const cuuint64_t kstr[1] = {(cuuint64_t)s.d * 2};
-    const cuuint32_t kbox[2] = {64, kBN};
+    const cuuint32_t kbox[2] = {64, s.pages ? (cuuint32_t)kPage : (cuuint32_t)kBN};
     if (!make_tensor_map_bf16(&tk, h->state + h->L.k, 2, kdims, kstr, kbox) ||
         !make_tensor_map_bf16(&tv, h->state + h->L.v, 2, kdims, kstr, kbox))
         return cudaErrorInvalidValue;
@@ -622,8 +718,10 @@ cudaError_t launch_chunk(kvc_handle* h, const void* q, void* out, int n, cudaStr
     a.q = static_cast<const __nv_bfloat16*>(q);
     a.rope = s.rope ? reinterpret_cast<const float2*>(h->state + h->L.rope) : nullptr;
     a.out = out; a.hdr = reinterpret_cast<uint32_t*>(h->state + h->L.hdr);
+    a.table = s.pages ? reinterpret_cast<const int32_t*>(h->state + h->L.table) : nullptr;
     a.B = s.B; a.Hq = s.Hq; a.Hkv = s.Hkv; a.g = s.g; a.S = s.S; a.W = s.W; a.n = n; a.out_bf16 = s.out_bf16;
     a.tiles = (n + kBM - 1) / kBM;
+    a.pairs = (s.g + 1) / 2;
     a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)s.d));
     // longest first: a (request, tile) item's work is its number of key tiles, from the
     // host mirror of next_position (already advanced past the appended suffix)
@@ -634,8 +732,9 @@ cudaError_t launch_chunk(kvc_handle* h, const void* q, void* out, int n, cudaStr
             for (int t = 0; t < a.tiles; ++t) {
                 const int cut = h->np[b] - n, i0 = t * kBM, rows = std::min(kBM, n - i0);
                 const int p_first = cut + i0, p_last = p_first + rows - 1;
-                const int lo = s.W > 0 ? std::max(0, p_first - s.W + 1) : 0;
-                w[b * a.tiles + t] = {-((p_last + 1 - lo + kBN - 1) / kBN), ((uint32_t)b << 16) | (uint32_t)t};
+                const int kmin = s.W > 0 ? std::max(0, p_first - s.W + 1) : 0;
+                const int kt = (p_last + 16) & ~15;
+                w[b * a.tiles + t] = {-((kt - (kmin & ~15) + kBN - 1) / kBN), ((uint32_t)b << 16) | (uint32_t)t};
             }
         std::stable_sort(w.begin(), w.end(),
                          [](const std::pair<int, uint32_t>& x, const std::pair<int, uint32_t>& y) {
@@ -644,7 +743,7 @@ cudaError_t launch_chunk(kvc_handle* h, const void* q, void* out, int n, cudaStr
         for (int i = 0; i < items; ++i) a.items[i] = w[i].second;
         a.n_items = items;
     }
-    chunk_attn_kernel<<<dim3(items * s.Hq), kThreads, SMEM_BYTES, st>>>(tk, tv, a);
+    chunk_attn_kernel<<<dim3(items * s.Hkv * a.pairs), kThreads, SMEM_BYTES, st>>>(tk, tv, a);
     return cudaGetLastError();
 }
 

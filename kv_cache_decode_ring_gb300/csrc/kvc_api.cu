@@ -431,12 +431,18 @@ int kvc_chunk_attn(kvc_t h, const void* d_q, const void* d_k, const void* d_v, i
     if (!h || !d_q || !d_k || !d_v || !d_out || n < 1) return KVC_ERR_ARG;
     if (!aligned16(d_q) || !aligned16(d_k) || !aligned16(d_v) || !aligned16(d_out)) return KVC_ERR_ARG;
     const Shape& s = h->sh;
-    if (!chunk_supported(s) || s.pages) return KVC_ERR_UNSUPPORTED;
+    if (!chunk_supported(s)) return KVC_ERR_UNSUPPORTED;
     if (n > s.max_chunk) return KVC_ERR_ARG;
     int rc = check_capacity(h, nullptr, n);
     if (rc) return rc;
-    // the suffix rows join the cache first (rotated keys, positions cut .. cut+n-1) ...
     cudaStream_t st = S_(stream);
+    if (s.pages) {
+        std::vector<int> from(h->np.begin(), h->np.end()), to(from);
+        for (auto& t : to) t += n;
+        if (map_pages(h, from, to, st, &rc) != cudaSuccess) return KVC_ERR_CUDA;
+        if (rc) return rc;
+    }
+    // the suffix rows join the cache first (rotated keys, positions cut .. cut+n-1) ...
     h->counts.assign(s.B, n);
     AppendArgs a = append_args(h, d_k, d_v, n);
     a.sb = (size_t)n * s.Hkv * s.d; a.sh = s.d; a.sr = (size_t)s.Hkv * s.d;   // [B][n][Hkv][d]

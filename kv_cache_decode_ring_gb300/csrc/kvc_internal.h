@@ -34,6 +34,7 @@ constexpr int kExactBlocksPerCta = 64; // restored blocks one CTA of the exact-b
 constexpr int kExactSplits = kMaxRestored / kExactBlocksPerCta;   // their split slots per query head
 constexpr uint32_t kErrPosition = 1u; // device error bits (sticky, cleared by kvc_device_status)
 constexpr uint32_t kErrWait = 2u;
+constexpr uint32_t kErrRange = 4u;    // a chunk-attention operand beyond the fp16 range
 
 // Byte offsets of the arrays inside the caller's state buffer (256-B aligned).
 struct Layout {

@@ -23,8 +23,8 @@ def built():
     build.build()
 
 
-def _prefilled(w, lengths, cuts, max_chunk, out_dtype=None):
-    cache = kvc.Cache.from_workload(w, max_chunk=max_chunk, out_dtype=out_dtype)
+def _prefilled(w, lengths, cuts, max_chunk, out_dtype=None, page_pool=0):
+    cache = kvc.Cache.from_workload(w, max_chunk=max_chunk, out_dtype=out_dtype, page_pool=page_pool)
     model = oracle_for(w)
     k, v = w.prefill_chunk(0, max(lengths))
     cache.append_rows(k.cuda(), v.cuda(), counts=lengths)
@@ -39,19 +39,31 @@ def _suffix(w, n, tag="suffix"):
     return (w.queries((B, n, Hq, d), tag), w.keys((B, n, Hkv, d), tag), w.values((B, n, Hkv, d), tag))
 
 
-@pytest.mark.parametrize("window", [0, 100])
-def test_chunk_matches_recompute(window):
-    w = wl.small("chunk-w%d" % window, B=3, Hq=8, Hkv=2, d=128, capacity=1024, window=window,
+CHUNK_CASES = [
+    # name, Hq, Hkv, capacity, window, paged
+    ("gqa4", 8, 2, 1024, 0, False),
+    ("gqa4-w100", 8, 2, 1024, 100, False),
+    ("gqa3-odd-pair", 6, 2, 1000, 0, False),      # a CTA's second head slot idle; capacity not a multiple of 16
+    ("mha-w300", 3, 3, 1024, 300, False),
+    ("gqa4-paged", 8, 2, 1024, 0, True),
+    ("gqa4-w100-paged", 8, 2, 1024, 100, True),
+]
+
+
+@pytest.mark.parametrize("case", CHUNK_CASES, ids=lambda c: c[0])
+def test_chunk_matches_recompute(case):
+    name, Hq, Hkv, cap, window, paged = case
+    w = wl.small("chunk-" + name, B=3, Hq=Hq, Hkv=Hkv, d=128, capacity=cap, window=window,
                  rope_base=10000.0, seed=17)
     lengths, cuts, n = [600, 300, 40], [413, 0, 40], 200
-    cache, model = _prefilled(w, lengths, cuts, n, out_dtype="f32")
+    cache, model = _prefilled(w, lengths, cuts, n, out_dtype="f32", page_pool=3 * (cap // 16) if paged else 0)
     q, k, v = _suffix(w, n)
     out = cache.chunk(q.cuda(), k.cuda(), v.cuda())
     torch.cuda.synchronize()
     ref = model.chunk(host(q), host(k), host(v))
     err = np.abs(out.double().cpu().numpy() - ref)
     print("chunk max abs err %.3e, max rel excess %.3f" % (err.max(), (err / (2e-3 + 2e-3 * np.abs(ref))).max()))
-    assert_close(out, ref, "bf16", "chunk W=%d" % window)
+    assert_close(out, ref, "bf16", "chunk %s" % name)
     check_state(cache, model, w)
     assert list(cache.next_positions()) == [c + n for c in cuts]
     assert cache.device_status() == 0
@@ -106,3 +118,30 @@ def test_chunk_rejects_bad_shapes():
     with pytest.raises(kvc.KvcError) as e:
         c2.chunk(q.cuda(), k.cuda(), v.cuda())      # n > max_chunk
     assert e.value.code == kvc.KVC_ERR_ARG
+
+
+def test_chunk_bf16_outputs_and_longer_prefix():
+    # bf16 outputs (the bench's format) over a prefix of several thousand keys, cuts
+    # on and off 16-key and 128-key boundaries
+    w = wl.small("chunk-long", B=4, Hq=8, Hkv=2, d=128, capacity=4096, rope_base=10000.0, seed=29)
+    lengths, cuts, n = [3000, 2500, 4000, 1000], [2048, 1999, 3456, 1], 300
+    cache, model = _prefilled(w, lengths, cuts, n)
+    q, k, v = _suffix(w, n)
+    out = cache.chunk(q.cuda(), k.cuda(), v.cuda())
+    assert out.dtype == torch.bfloat16
+    ref = model.chunk(host(q), host(k), host(v))
+    assert_close(out, ref, "bf16", "chunk bf16 out")
+    assert cache.device_status() == 0
+
+
+def test_chunk_flags_values_beyond_fp16_range():
+    # the products take fp16 operands: a value row beyond 65504 is reported in the
+    # device error word (bit 2), not silently rounded
+    w = wl.small("chunk-range", B=1, Hq=4, Hkv=2, d=128, capacity=256, rope_base=10000.0, seed=5)
+    cache, model = _prefilled(w, [64], [64], 32)
+    q, k, v = _suffix(w, 32)
+    v = v.clone()
+    v[0, 5, 1, 7] = 1.0e6
+    cache.chunk(q.cuda(), k.cuda(), v.cuda())
+    assert cache.device_status() == 4
+    assert cache.device_status() == 0          # read and cleared
