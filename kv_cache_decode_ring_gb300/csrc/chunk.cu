@@ -214,10 +214,6 @@ __device__ __forceinline__ uint32_t pack_f16(float a, float b) {
     return *reinterpret_cast<uint32_t*>(&t);
 }
 
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
 // Non-blocking check that phase `parity` of an mbarrier has completed.
 __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
@@ -228,6 +224,23 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+
+// Bounded wait (about one second) that polls without suspending: for the single
+// thread that issues the MMAs, whose reaction time is on every tile's critical path.
+__device__ __forceinline__ bool mbar_spin(uint64_t* bar, uint32_t parity) {
+    if (mbar_test(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t it = 0; it < (1u << 30); ++it) {
+        if (mbar_test(bar, parity)) return true;
+        if ((it & 1023u) == 1023u && global_ns() - t0 > 1000000000ull) break;
+    }
+    return false;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 
 // Convert one stage (a K or V tile) from bf16 to fp16 in place.  The kConvThreads
 // converter threads take 16-byte chunks t, t + kConvThreads, ..., four at a time (all
@@ -617,7 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             // per slot: S(j) -> [softmax writes P(j)] -> P.V(j) -> S(j + 1) once P.V(j) is
             // complete (S(j + 1) overwrites the P columns P.V(j) reads); the slots alternate
-            auto wait_ok = [&](uint64_t* bar_, uint32_t parity) { return mbar_wait(bar_, parity) && !*abort_flag; };
+            auto wait_ok = [&](uint64_t* bar_, uint32_t parity) { return mbar_spin(bar_, parity) && !*abort_flag; };
             bool ok = wait_ok(&bar[B_QREADY], 0) && wait_ok(&bar[B_KCONV], 0);
             if (ok) {
                 fence_after();
