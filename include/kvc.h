@@ -73,8 +73,12 @@ typedef struct {
                              KVC_RING: slot = position mod W, capacity = W
                              ([LEAN] §3.4 ring buffer, §2.3 lastWindow) */
     int32_t kv_quant;     /* KVC_QUANT_NONE, KVC_QUANT_INT8_DITHER (Tier B, see
-                             dither_key_lo below) or KVC_QUANT_INT8 (bf16 contiguous
-                             caches with window 0 only; [WITCERT]) */
+                             dither_key_lo below) or KVC_QUANT_INT8 ([WITCERT]; bf16
+                             caches, contiguous with any window or a ring.  Blocks are
+                             16 positions; a ring of W slots, W % 16 == 0, keeps block n
+                             in block slot n mod W/16 and holds the newest W/16
+                             complete blocks plus the exact rows of the incomplete
+                             one, which covers its window [LEAN] §3.4) */
     int32_t batch;        /* B >= 1 requests */
     int32_t n_q_heads;    /* Hq >= 1 */
     int32_t n_kv_heads;   /* Hkv >= 1, Hq % Hkv == 0; query head h reads KV head h / (Hq/Hkv) */
@@ -91,7 +95,8 @@ typedef struct {
                              KVC_BF16 (+1 is added so that 0 keeps the default):
                              pass KVC_F32 + 1 or KVC_BF16 + 1 */
     int32_t int8_exact_blocks; /* INT8 only: capacity of the pool of blocks restored
-                             to full precision by kvc_int8_restore (0 = none) */
+                             to full precision by kvc_int8_restore (0 = none).
+                             Contiguous caches with window 0 only. */
     int32_t page_pool;    /* paged K/V storage ([LEAN] §6.1 block table; [LOOP] §八 Q1,
                              16-token pages mapped on demand): 0 = each
                              request owns `capacity` slots; > 0 = K and V live in a pool
@@ -166,7 +171,9 @@ int kvc_append_rows(kvc_t h, const void* d_k, const void* d_v, int32_t n,
  * computed with upward rounding so that c_t >= |q . r_t| / sqrt(d) for the
  * stored residual r_t, hence attention total variation <= d_tanh
  * ([WITCERT] "为什么在线监控 KV 误差如此困难？").  d_ct (nullable) receives c_t
- * as [B][Hq][capacity] indexed by slot (slots outside the window untouched).
+ * as [B][Hq][capacity] indexed by slot: the tokens of the window, and 0 for the
+ * tokens before the window start that share its first block; other slots are not
+ * written.  With a window (or a ring), max_t runs over the window only.
  * For non-quantized caches d_cmax/d_tanh (nullable) receive 0 and d_ct must
  * be NULL. */
 int kvc_decode_attn(kvc_t h, const void* d_q, void* d_out, float* d_cmax, float* d_tanh,
@@ -270,7 +277,9 @@ int kvc_chunk_attn(kvc_t h, const void* d_q, const void* d_k, const void* d_v, i
  * k of d_ct[b][hq][t] (the per-token bound of the last kvc_decode_attn on this cache,
  * [B][Hq][capacity] fp32), for every complete block of request b; 0 elsewhere.
  * d_risk: fp32 [B][Hkv][capacity/16], device.  Async on `stream`.
- * KVC_ERR_ARG: not an INT8 cache, or a null pointer. */
+ * KVC_ERR_ARG: not an INT8 cache, or a null pointer.  KVC_ERR_UNSUPPORTED: Tier B,
+ * a ring or a window (the gated fallback serves contiguous caches that attend to
+ * their whole history). */
 int kvc_int8_block_risk(kvc_t h, const float* d_ct, float* d_risk, kvc_stream_t stream);
 
 /* Host only.  Every (request, KV head, block) of h_risk ([B][Hkv][nblk] fp32, host)

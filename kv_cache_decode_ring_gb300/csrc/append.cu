@@ -68,8 +68,11 @@ __device__ __forceinline__ void store_pair(void* dst, size_t off, float y0, floa
 // from the block's Philox calls (one per thread, bytes staged in shared memory; channel
 // c takes byte c mod 16 of group c/16); values keep the plain quantizer; no witnesses.
 // ---------------------------------------------------------------------------
+// `blk` is the absolute block number (it keys the dither counters); the block is stored
+// in block slot blk (contiguous) or blk mod S/16 (ring).
 __device__ void quantize_block(const AppendArgs& a, const float* sK, const float* sV, float* red,
                                int b, int h, int blk) {
+    const int pblk = a.ring ? blk % (a.S / kQBlock) : blk;
     const int d = a.d, n = kQBlock * d;
     uint8_t* du = reinterpret_cast<uint8_t*>(red + 64);        // [16][d] key dither bytes (Tier B)
     if (a.dither) {
@@ -101,10 +104,10 @@ __device__ void quantize_block(const AppendArgs& a, const float* sK, const float
     for (int w = 0; w < nw; ++w) { mk = fmaxf(mk, red[w]); mv = fmaxf(mv, red[32 + w]); }
     const float s_k = __fdiv_rn(mk, 127.0f), s_v = __fdiv_rn(mv, 127.0f);
     const size_t bh = (size_t)b * a.Hkv + h;
-    const size_t row0 = bh * a.S + (size_t)blk * kQBlock;
+    const size_t row0 = bh * a.S + (size_t)pblk * kQBlock;
     if (threadIdx.x == 0) {
-        a.sk[bh * (a.S / kQBlock) + blk] = s_k;
-        a.sv[bh * (a.S / kQBlock) + blk] = s_v;
+        a.sk[bh * (a.S / kQBlock) + pblk] = s_k;
+        a.sv[bh * (a.S / kQBlock) + pblk] = s_v;
     }
     // codes stored biased (c + 128) at the block positions kq_offset / vq_offset
     uint8_t* kb = reinterpret_cast<uint8_t*>(a.kq) + row0 * d;
@@ -326,6 +329,8 @@ __global__ void __launch_bounds__(kThreads) quantize_rows_kernel(const AppendArg
     const int blk = np / kQBlock + blockIdx.x;
     const int p0 = blk * kQBlock;
     if (p0 + kQBlock > np + cnt) return;             // block not completed by this call
+    // a ring keeps the newest S/16 complete blocks: one overwritten later in this call is skipped
+    if (a.ring && p0 < ((np + cnt) / kQBlock) * kQBlock - a.S) return;
     if (!position_ok(a, (long long)p0 + kQBlock - 1)) {
         if (threadIdx.x == 0) flag(a.hdr, kErrPosition);
         return;
@@ -357,7 +362,8 @@ __global__ void __launch_bounds__(kThreads) quantize_rows_kernel(const AppendArg
     __syncthreads();
     quantize_block(a, sK, sV, red, b, h, blk);
     if (h == 0)
-        for (int r = threadIdx.x; r < kQBlock; r += blockDim.x) a.pos[(size_t)b * a.S + p0 + r] = p0 + r;
+        for (int r = threadIdx.x; r < kQBlock; r += blockDim.x)
+            a.pos[(size_t)b * a.S + (a.ring ? (p0 + r) % a.S : p0 + r)] = p0 + r;
 }
 
 // INT8 rows, phase 2 (one CTA per request): rows of the last, incomplete block
@@ -382,7 +388,7 @@ __global__ void __launch_bounds__(kThreads) tail_kernel(const AppendArgs a, cons
         a.ktail[tail + 2 * i + 1] = __float2bfloat16_rn(k1);
         a.vtail[tail + 2 * i] = __float2bfloat16_rn(ld_elem(a.v, src + 2 * i, 1));
         a.vtail[tail + 2 * i + 1] = __float2bfloat16_rn(ld_elem(a.v, src + 2 * i + 1, 1));
-        if (h == 0 && i == 0 && p < a.S) a.pos[(size_t)b * a.S + p] = p;
+        if (h == 0 && i == 0 && (a.ring || p < a.S)) a.pos[(size_t)b * a.S + (a.ring ? p % a.S : p)] = p;
     }
     __syncthreads();
     if (threadIdx.x == 0) a.next_pos[b] = end;

@@ -80,6 +80,7 @@ struct Int8Args {
     uint32_t layer_ctr;             // Tier B: 65536 * layer
     uint32_t rk[20];                // Tier B: Philox round keys (k0 + r W0, k1 + r W1), r = 0..9
     int B, Hq, Hkv, d, S, max_splits;
+    int W, ring;        // attention window (0 = all; a ring's is its size) and layout
     int split;          // tokens per quantized split
     float scale_log2;   // log2(e)/sqrt(d)
     float inv_sqrt_d_up;
@@ -94,7 +95,8 @@ struct Int8CombineArgs {
     void* out;
     float* cmax;        // nullable
     float* tanh_out;    // nullable
-    int B, Hq, Hkv, d, max_splits, out_bf16;
+    int B, Hq, Hkv, d, S, max_splits, out_bf16;
+    int W, ring;
     int split;          // tokens per quantized split
 };
 
@@ -226,7 +228,10 @@ int8_decode_kernel(const Int8Args a) {
     dep_release();
     const int len = a.next_pos[b];
     const int nfull = len & ~(kQBlock - 1);
-    const int nsq = (nfull + a.split - 1) / a.split;
+    // the window's complete blocks: physical block slots [blo, bhi) (see int8_window)
+    const Int8Window iw = int8_window(len, a.S, a.W, a.ring);
+    const int bps = a.split / kQBlock;                        // blocks per split
+    const int nsq = (iw.bhi - iw.blo + bps - 1) / bps;
     const int tpw = a.split / (kWarps * kQBlock);             // tiles per warp
     const bool tail_split = split == nsq;
     if (split > nsq || (tail_split && len == nfull && a.xn[(size_t)b * a.Hkv + kvh] == 0)) return;
@@ -266,7 +271,7 @@ int8_decode_kernel(const Int8Args a) {
         }
         for (int r0 = 0; r0 < total; r0 += 32) {
             const int r = r0 + lane;
-            const bool valid = r < total;
+            const bool valid = r < total && nfull + r >= iw.lo;     // rows before the window are masked
             float s[G];
 #pragma unroll
             for (int h = 0; h < G; ++h) s[h] = -INFINITY;
@@ -280,8 +285,9 @@ int8_decode_kernel(const Int8Args a) {
                 }
                 if (a.ct) {
                     const int p = row_pos(r);
+                    const int slot = a.ring ? p % a.S : p;          // a ring's slot of position p
 #pragma unroll
-                    for (int h = 0; h < G; ++h) a.ct[(rowq0 + h) * a.S + p] = 0.f;
+                    for (int h = 0; h < G; ++h) a.ct[(rowq0 + h) * a.S + slot] = 0.f;
                 }
             }
             float alpha[G];
@@ -289,7 +295,7 @@ int8_decode_kernel(const Int8Args a) {
             for (int h = 0; h < G; ++h) {
                 float mx = s[h];
                 for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-                const float mn = fmaxf(m[h], mx);                 // finite: the chunk has a valid row
+                const float mn = fmaxf(m[h], mx);                 // finite: the chunk holds the newest row
                 alpha[h] = exp2f(m[h] - mn);                      // 0 on the first chunk
                 const float p = valid ? exp2f(s[h] - mn) : 0.f;
                 float ls = p;
@@ -331,8 +337,8 @@ int8_decode_kernel(const Int8Args a) {
     unsigned char* myS = smem + warp * C::WARPB;
     uint64_t* myBar = bar + warp * kStages;
     // block of this warp's tile i (tiles of the 4 warps interleaved)
-    auto tile_blk = [&](int i) { return (split * a.split) / kQBlock + i * kWarps + warp; };
-    auto tile_ok = [&](int i) { return (tile_blk(i) + 1) * kQBlock <= nfull; };
+    auto tile_blk = [&](int i) { return iw.blo + split * bps + i * kWarps + warp; };
+    auto tile_ok = [&](int i) { return tile_blk(i) < iw.bhi; };
     auto issue = [&](int i) {
         if (lane == 0 && tile_ok(i)) {
             const size_t p0 = (size_t)tile_blk(i) * kQBlock;
@@ -450,7 +456,10 @@ int8_decode_kernel(const Int8Args a) {
         const unsigned char* tK = myS + sg * C::STAGEB;
         const unsigned char* tV = tK + C::CB;
         const uint4* tW = reinterpret_cast<const uint4*>(tK + 2 * C::CB);
-        const int p0 = tile_blk(i) * kQBlock;
+        const int p0 = tile_blk(i) * kQBlock;                          // first slot of the block
+        const int pa = int8_abs_block(iw, tile_blk(i), a.ring) * kQBlock;  // its first position
+        // tokens g and g + 8 of the block before the window start are masked (first block only)
+        const bool vis0 = pa + g >= iw.lo, vis1 = pa + g + 8 >= iw.lo;
         if (!mbar_wait(&myBar[sg], par)) {
             // give up: flag it, and let this stage's copy and the later stages'
             // (if issued) land before the stages are reused for the partial
@@ -494,8 +503,8 @@ int8_decode_kernel(const Int8Args a) {
     #pragma unroll
                 for (int j = 0; j < D / 64; ++j) {
                     const uint32_t grp = (uint32_t)(qd * (D / 64) + j);
-                    const uint4 r0 = philox_rk(make_uint4((uint32_t)(p0 + g), grp, dc2, dc3), a.rk);
-                    const uint4 r1 = philox_rk(make_uint4((uint32_t)(p0 + g + 8), grp, dc2, dc3), a.rk);
+                    const uint4 r0 = philox_rk(make_uint4((uint32_t)(pa + g), grp, dc2, dc3), a.rk);
+                    const uint4 r1 = philox_rk(make_uint4((uint32_t)(pa + g + 8), grp, dc2, dc3), a.rk);
     #pragma unroll
                     for (int w = 0; w < 4; ++w) {
                         uint32_t a0, a1, a2, a3;
@@ -515,8 +524,8 @@ int8_decode_kernel(const Int8Args a) {
     #pragma unroll
             for (int nt = 0; nt < C::HPL; ++nt) {
                 const float f = fq[nt] * s_k;
-                const float s0 = (sacc[nt][0] + sacc[nt][1]) * f;
-                const float s1 = (sacc[nt][2] + sacc[nt][3]) * f;
+                const float s0 = vis0 ? (sacc[nt][0] + sacc[nt][1]) * f : -INFINITY;
+                const float s1 = vis1 ? (sacc[nt][2] + sacc[nt][3]) * f : -INFINITY;
                 float bm = fmaxf(s0, s1);
                 bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
                 bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
@@ -555,6 +564,8 @@ int8_decode_kernel(const Int8Args a) {
                     }
                     cb[tt] = __fmul_ru(__fadd_ru(c2.x, c2.y), a.inv_sqrt_d_up);
                 }
+                cb[0] = vis0 ? cb[0] : 0.f;                     // outside the window: no bound
+                cb[1] = vis1 ? cb[1] : 0.f;
                 c_w[nt] = fmaxf(c_w[nt], fmaxf(cb[0], cb[1]));
                 if (a.ct && hq < G) {
                     a.ct[(rowq0 + hq) * a.S + p0 + g] = cb[0];
@@ -681,8 +692,10 @@ __global__ void __launch_bounds__(kCombineThreads) int8_combine_kernel(const Int
         const int nfull = len & ~(kQBlock - 1);
         const int kvh = hq / (c.Hq / c.Hkv);
         const int nx = c.xn[(size_t)b * c.Hkv + kvh];
+        const Int8Window iw = int8_window(len, c.S, c.W, c.ring);
+        const int bps = c.split / kQBlock;
         // quantized splits, the exact-rows split (if it ran), the exact-block splits
-        const int ns = (nfull + c.split - 1) / c.split + (len > nfull || nx > 0 ? 1 : 0) +
+        const int ns = (iw.bhi - iw.blo + bps - 1) / bps + (len > nfull || nx > 0 ? 1 : 0) +
                        (nx + kExactBlocksPerCta - 1) / kExactBlocksPerCta;
         const float2* ml = c.part_ml + row * c.max_splits;
         const float* pc = c.part_c + row * c.max_splits;
@@ -778,6 +791,7 @@ cudaError_t launch_int8_decode(kvc_handle* h, const void* q, void* out, float* c
     a.ct = ct;
     a.hdr = reinterpret_cast<uint32_t*>(h->state + h->L.hdr);
     a.B = s.B; a.Hq = s.Hq; a.Hkv = s.Hkv; a.d = s.d; a.S = s.S; a.max_splits = s.max_splits;
+    a.W = s.W; a.ring = s.ring;
     a.split = s.split;
     a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)s.d));
     a.inv_sqrt_d_up = std::nextafter((float)(1.0 / std::sqrt((double)s.d)), 1.0f);
@@ -792,7 +806,8 @@ cudaError_t launch_int8_decode(kvc_handle* h, const void* q, void* out, float* c
     Int8CombineArgs c{};
     c.part_ml = a.part_ml; c.part_acc = a.part_acc; c.part_c = a.part_c; c.next_pos = a.next_pos; c.xn = a.xn;
     c.out = out; c.cmax = cmax; c.tanh_out = tanh_out;
-    c.B = s.B; c.Hq = s.Hq; c.Hkv = s.Hkv; c.d = s.d; c.max_splits = s.max_splits; c.out_bf16 = s.out_bf16;
+    c.B = s.B; c.Hq = s.Hq; c.Hkv = s.Hkv; c.d = s.d; c.S = s.S; c.max_splits = s.max_splits;
+    c.out_bf16 = s.out_bf16; c.W = s.W; c.ring = s.ring;
     c.split = s.split;
     const size_t rows = (size_t)s.B * s.Hq;
     if (s.max_splits <= 8)

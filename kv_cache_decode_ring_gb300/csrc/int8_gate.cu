@@ -126,6 +126,8 @@ using namespace kvc;
 extern "C" int kvc_int8_block_risk(kvc_t h, const float* d_ct, float* d_risk, kvc_stream_t stream) {
     if (!h || !d_ct || !d_risk || !h->sh.int8) return KVC_ERR_ARG;
     if (h->sh.dither) return KVC_ERR_UNSUPPORTED;          // Tier B has no per-token bound
+    // the gate restores blocks of contiguous caches that attend to their whole history
+    if (h->sh.ring || h->sh.W > 0) return KVC_ERR_UNSUPPORTED;
     const Shape& s = h->sh;
     const int nblk = s.S / kQBlock;
     block_risk_kernel<<<dim3((nblk + 7) / 8, s.Hkv, s.B), 256, 0, static_cast<cudaStream_t>(stream)>>>(

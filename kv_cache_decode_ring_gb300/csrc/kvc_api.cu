@@ -51,9 +51,11 @@ bool make_shape(const kvc_config& c, Shape* s) {
     const bool dither = c.kv_quant == KVC_QUANT_INT8_DITHER;
     // the dither counter packs the KV head and the layer into 16 bits each
     if (dither && (c.layer_index < 0 || c.layer_index > 65535 || c.n_kv_heads > 65536)) return false;
-    if (int8 && (c.dtype != KVC_BF16 || ring || c.window != 0 || c.head_dim % kBands || c.capacity % kQBlock))
+    if (int8 && (c.dtype != KVC_BF16 || c.head_dim % kBands || c.capacity % kQBlock)) return false;
+    // the gated fallback's pool serves contiguous caches attending to their whole history
+    if (c.int8_exact_blocks < 0 ||
+        ((!int8 || dither || ring || c.window != 0) && c.int8_exact_blocks != 0))
         return false;
-    if (c.int8_exact_blocks < 0 || ((!int8 || dither) && c.int8_exact_blocks != 0)) return false;
     if (c.page_pool < 0 || (c.page_pool > 0 && (int8 || c.capacity % kPage))) return false;
     if (c.store_slots < 0 || (c.store_slots > 0 && int8)) return false;
     if (int8) {
@@ -87,9 +89,12 @@ bool make_shape(const kvc_config& c, Shape* s) {
     s->max_splits = (int)((keys + s->split - 1) / s->split) + (s->pages > 0 ? 1 : 0);
     if (int8) {
         // quantized splits (longer ones for long caches: less start-up per byte), one
-        // split for the exact tail rows and, with a pool, the splits of the exact-block decode
-        s->split = keys >= kInt8LongKeys ? kInt8SplitLong : kInt8Split;
-        s->max_splits = (int)((keys + s->split - 1) / s->split) + 1 + (s->xpool > 0 ? kExactSplits : 0);
+        // split for the exact tail rows and, with a pool, the splits of the exact-block decode.
+        // A window of W positions on a contiguous cache touches at most W/16 + 2 blocks.
+        const long long qkeys = (!ring && s->W > 0 && (long long)s->W + 2 * kQBlock < s->S)
+                                    ? (long long)s->W + 2 * kQBlock : s->S;
+        s->split = qkeys >= kInt8LongKeys ? kInt8SplitLong : kInt8Split;
+        s->max_splits = (int)((qkeys + s->split - 1) / s->split) + 1 + (s->xpool > 0 ? kExactSplits : 0);
     }
     return true;
 }

@@ -270,6 +270,35 @@ __device__ __forceinline__ size_t kv_row(const int32_t* table, int b, int h, int
     return ((size_t)page * Hkv + h) * kPage + (slot % kPage);
 }
 
+// INT8 tier: the complete 16-position blocks that the newest token of a request (at
+// len - 1) attends to.  A contiguous cache stores block n in block slot n; a ring of S
+// slots (S a multiple of 16) stores block n in block slot n mod (S/16), so a slot
+// holds the newest complete block congruent to it.  Physical block slots [blo, bhi)
+// hold the blocks read; positions below `lo` (the window start) are masked, which can
+// only cut into the first of them.  The rows [nfull, len) of the incomplete block live
+// in the exact tail.
+struct Int8Window {
+    int blo, bhi;      // physical block slots read
+    int lo;            // first visible position
+    int nfb;           // complete blocks written so far (absolute count)
+    int nbk;           // block slots of the cache
+};
+__host__ __device__ __forceinline__ Int8Window int8_window(int len, int S, int W, int ring) {
+    Int8Window w;
+    w.nfb = len / kQBlock;
+    w.nbk = S / kQBlock;
+    w.lo = (W > 0 && len > W) ? len - W : 0;
+    if (ring) { w.blo = 0; w.bhi = w.nfb < w.nbk ? w.nfb : w.nbk; }
+    else { w.blo = w.lo / kQBlock; w.bhi = w.nfb; }
+    if (w.bhi < w.blo) w.bhi = w.blo;
+    return w;
+}
+// Absolute block number held by physical block slot k.
+__host__ __device__ __forceinline__ int int8_abs_block(const Int8Window& w, int k, int ring) {
+    if (!ring || w.nfb <= w.nbk) return k;
+    return (w.nfb - 1) - ((w.nfb - 1 - k) % w.nbk);
+}
+
 // Cached key slots of request b attended by its newest token (next_position - 1):
 // a ring holds the window in slots [0, min(len, W)); a contiguous cache in
 // slots [len - min(len, W), len).

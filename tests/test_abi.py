@@ -54,9 +54,11 @@ def test_state_bytes_validation(lib):
         kvc.make_config("bf16", "ring", None, 1, 1, 1, 128, 64, rope_base=1e4),  # ring RoPE needs max_position
         kvc.make_config("f32", "contiguous", "int8", 1, 1, 1, 128, 64),         # INT8 needs bf16
         kvc.make_config("bf16", "contiguous", "int8", 1, 1, 1, 128, 60),        # INT8 capacity % 16
-        kvc.make_config("bf16", "ring", "int8", 1, 1, 1, 128, 64),              # INT8 contiguous only
+        kvc.make_config("bf16", "ring", "int8", 1, 1, 1, 128, 72),              # INT8 ring W % 16
+        kvc.make_config("bf16", "ring", "int8", 1, 4, 1, 128, 64, int8_exact_blocks=4),   # gate on a ring
         kvc.make_config("bf16", "contiguous", None, 0, 1, 1, 128, 64),          # empty batch
-        kvc.make_config("bf16", "contiguous", "int8", 1, 4, 1, 128, 64, window=32),   # INT8 attends to all
+        kvc.make_config("bf16", "contiguous", "int8", 1, 4, 1, 128, 64, window=32,
+                        int8_exact_blocks=4),                                    # gate with a window
         kvc.make_config("bf16", "contiguous", None, 1, 1, 1, 128, 64, int8_exact_blocks=4),  # pool needs INT8
         kvc.make_config("bf16", "contiguous", "int8", 1, 4, 1, 128, 64, int8_exact_blocks=-1),
         kvc.make_config("bf16", "contiguous", "int8", 1, 4, 1, 128, 64, page_pool=8),   # paged INT8
@@ -68,9 +70,14 @@ def test_state_bytes_validation(lib):
         kvc.make_config("bf16", "contiguous", "int8-dither", 1, 4, 1, 128, 64, int8_exact_blocks=4),  # no gate
         kvc.make_config("bf16", "contiguous", "int8-dither", 1, 4, 1, 128, 64, layer_index=65536),   # 16-bit layer
         kvc.make_config("bf16", "contiguous", "int8-dither", 1, 4, 1, 128, 64, layer_index=-1),
-        kvc.make_config("bf16", "ring", "int8-dither", 1, 4, 1, 128, 64),
+        kvc.make_config("bf16", "ring", "int8-dither", 1, 4, 1, 128, 56),
         kvc.make_config("f32", "contiguous", "int8-dither", 1, 4, 1, 128, 64),
     ]
+    # the INT8 tiers on a ring (W % 16 == 0) or with a window
+    for c in [kvc.make_config("bf16", "ring", "int8", 1, 4, 1, 128, 64),
+              kvc.make_config("bf16", "ring", "int8-dither", 1, 4, 1, 128, 64),
+              kvc.make_config("bf16", "contiguous", "int8", 1, 4, 1, 128, 64, window=8)]:
+        assert kvc.kvc_state_bytes(c) > 0
     for c in bad:
         with pytest.raises(kvc.KvcError) as e:
             kvc.kvc_state_bytes(c)

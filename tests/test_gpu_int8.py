@@ -293,3 +293,139 @@ def test_int8_restore_errors():
     cache.restore([(0, 0, 1), (0, 0, 1)], kf, vf)                    # duplicates count once
     cache.restore([(0, 0, 1), (0, 0, 3)], kf, vf)                    # already restored: skipped
     assert (cache.export(kvc.KVC_EXPORT_XMAP) >= 0).sum() == 2
+
+
+# ---- windowed and ring INT8 caches ------------------------------------------------------
+def _oracle_layout(w):
+    return DecodeOracle(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.layout, w.capacity,
+                        0 if w.layout == "ring" else w.window, w.rope_base, "bf16", w.quant,
+                        dither_key=w.extra.get("dither_key", (0, 0)))
+
+
+def check_int8_ring_state(cache, model):
+    """A ring of S slots keeps block n in block slot n mod S/16: the newest S/16 complete
+    blocks, their codes, scales and witnesses bit-exact, and the exact tail rows."""
+    KQ = cache.export(kvc.KVC_EXPORT_KQ); VQ = cache.export(kvc.KVC_EXPORT_VQ)
+    SK = cache.export(kvc.KVC_EXPORT_SK); SV = cache.export(kvc.KVC_EXPORT_SV)
+    WT = cache.export(kvc.KVC_EXPORT_WITNESS) if model.quant == "int8" else None
+    KT = cache.export(kvc.KVC_EXPORT_KTAIL)
+    assert np.array_equal(cache.export(kvc.KVC_EXPORT_POSITIONS), model.expected_positions())
+    nbk = model.capacity // QBLOCK
+    for b in range(model.B):
+        n = model.length(b)
+        nfb = n // QBLOCK
+        for h in range(model.Hkv):
+            for blk in range(max(0, nfb - nbk), nfb):
+                sK, cK, sV, cV, wit = model.quantized_block(b, h, blk)
+                k = blk % nbk
+                sl = slice(k * QBLOCK, (k + 1) * QBLOCK)
+                assert SK[b, h, k] == sK and SV[b, h, k] == sV, (b, h, blk)
+                assert np.array_equal(KQ[b, h, sl], cK) and np.array_equal(VQ[b, h, sl], cV), (b, h, blk)
+                if WT is not None:
+                    assert np.array_equal(WT[b, h, sl], wit), (b, h, blk)
+            for p in range(nfb * QBLOCK, n):
+                assert np.array_equal(KT[b, h, p % QBLOCK], nm.f32_to_bf16(model.hk[b][p][h])), (b, h, p)
+
+
+def check_decode_window(cache, model, q, ring):
+    """Outputs against attention over the dequantized window; c_t of every token in the
+    window (slot = position, or position mod S on a ring) sound and tight; max_t c_t over
+    the window; TV <= tanh(max c_t)."""
+    B, Hq, S = model.B, model.Hq, model.capacity
+    out = torch.empty((B, Hq, model.d), dtype=torch.float32, device="cuda")
+    bound = model.quant == "int8"
+    cmax = torch.full((B, Hq), -1.0, device="cuda") if bound else None
+    th = torch.full((B, Hq), -1.0, device="cuda") if bound else None
+    ct = torch.full((B, Hq, S), -7.0, device="cuda") if bound else None
+    kvc.kvc_decode_attn(cache.h, q.cuda(), out, cmax, th, ct)
+    res = model.decode_int8(host(q))
+    for (b, hq), r in res.items():
+        assert_close(out[b, hq][None], r["out"][None], "bf16", "int8 window decode b=%d h=%d" % (b, hq))
+        if not bound:
+            continue
+        t = model.length(b) - 1
+        lo = max(0, t - model.window + 1)
+        slots = np.arange(lo, t + 1) % S if ring else np.arange(lo, t + 1)
+        c_gpu = ct[b, hq].cpu().numpy().astype(np.float64)[slots]
+        assert c_gpu.shape == r["c"].shape
+        assert np.all(c_gpu >= r["eps"]), (b, hq)
+        assert np.all(c_gpu >= r["c"] * (1 - 1e-12)), (b, hq)
+        assert np.all(c_gpu <= r["c"] * (1 + 1e-5) + 1e-30), (b, hq)
+        cm, tc = float(cmax[b, hq]), float(th[b, hq])
+        assert cm >= r["cmax"] * (1 - 1e-12) and cm <= r["cmax"] * (1 + 1e-5) + 1e-30, (b, hq)
+        assert tc >= math.tanh(cm) * (1 - 1e-7) and tc <= 1.0
+        assert r["tv"] <= tc, (b, hq, r["tv"], tc)
+
+
+@pytest.mark.parametrize("window", [8, 100, 1000], ids=["w8-inside-a-block", "w100", "w1000"])
+def test_int8_windowed_contiguous(window):
+    # blocks wholly before the window are skipped, the first block is masked per token,
+    # and a window shorter than a block sits in the exact tail
+    w = wl.small("int8-w%d" % window, B=3, Hq=8, Hkv=2, d=128, capacity=1536, window=window,
+                 rope_base=10000.0, quant="int8", seed=23, outliers=(4, 20.0))
+    cache = kvc.Cache.from_workload(w, out_dtype="f32")
+    model = _oracle_layout(w)
+    lengths = [1, 250, 1300]
+    k, v = w.prefill_chunk(0, max(lengths))
+    cache.append_rows(k.cuda(), v.cuda(), counts=lengths)
+    model.append_rows(host(k), host(v), lengths)
+    check_int8_state(cache, model)
+    for s in range(18):                                  # crosses a block completion
+        q, k1, v1 = w.step_qkv(s)
+        cache.append(k1.cuda(), v1.cuda())
+        model.append(host(k1), host(v1))
+        check_decode_window(cache, model, q, ring=False)
+    check_int8_state(cache, model)
+    assert cache.device_status() == 0
+
+
+@pytest.mark.parametrize("quant", ["int8", "int8-dither"])
+def test_int8_ring_through_first_replacement(quant):
+    # W = 64 slots (4 blocks): the not-full phase, the first block overwritten, the window
+    # cutting into the oldest block; a prefill longer than the ring (its early blocks are
+    # never stored) and one-token appends
+    extra = {"outliers": (4, 20.0)}
+    if quant == "int8-dither":
+        extra.update(dither_key=(0x243F6A88, 0x85A308D3), layer=0)
+    w = wl.small("int8-ring-" + quant, B=3, Hq=8, Hkv=2, d=128, layout="ring", capacity=64, window=64,
+                 rope_base=10000.0, quant=quant, seed=31, **extra)
+    cache = kvc.Cache.from_workload(w, max_position=512, out_dtype="f32")
+    model = _oracle_layout(w)
+    lengths = [3, 70, 150]
+    k, v = w.prefill_chunk(0, max(lengths))
+    cache.append_rows(k.cuda(), v.cuda(), counts=lengths)
+    model.append_rows(host(k), host(v), lengths)
+    check_int8_ring_state(cache, model)
+    for s in range(90):
+        q, k1, v1 = w.step_qkv(s)
+        cache.append(k1.cuda(), v1.cuda())
+        model.append(host(k1), host(v1))
+        if s % 5 == 0 or s < 20:
+            check_decode_window(cache, model, q, ring=True)
+        if s % 15 == 14:
+            check_int8_ring_state(cache, model)
+    assert cache.device_status() == 0
+
+
+def test_int8_ring_trim_rules():
+    # a ring trim must keep what the next query needs; an INT8 trim must not split a block
+    w = wl.small("int8-ring-trim", B=2, Hq=4, Hkv=1, d=128, layout="ring", capacity=64, window=64,
+                 rope_base=10000.0, quant="int8", seed=37)
+    cache = kvc.Cache.from_workload(w, max_position=512, out_dtype="f32")
+    model = _oracle_layout(w)
+    k, v = w.prefill_chunk(0, 40)
+    cache.append_rows(k.cuda(), v.cuda())
+    model.append_rows(host(k), host(v), [40, 40])
+    with pytest.raises(kvc.KvcError) as e:
+        cache.trim([20, 40])                           # splits a quantized block
+    assert e.value.code == kvc.KVC_ERR_EVICTED
+    cache.trim([32, 39])                               # a block boundary; inside the exact tail
+    model.trim([32, 39])
+    check_int8_ring_state(cache, model)
+    for s in range(40):                                # wrap the ring after the trim
+        q, k1, v1 = w.step_qkv(s)
+        cache.append(k1.cuda(), v1.cuda())
+        model.append(host(k1), host(v1))
+        check_decode_window(cache, model, q, ring=True)
+    check_int8_ring_state(cache, model)
+    assert cache.device_status() == 0

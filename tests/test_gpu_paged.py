@@ -134,11 +134,21 @@ def test_paged_ring_phases_every_step():
     assert (tab >= 0).all() and len(np.unique(tab)) == 4       # a full ring holds its two pages
 
 
-def test_paged_chunk_is_unsupported():
+def test_paged_chunk_maps_its_pages():
+    # the chunk's suffix rows take pages from the pool like any append (its attention reads
+    # them through the block table: parity in test_gpu_chunk.py); a pool too small refuses
+    # the call before anything changes
     w = wl.small("paged-chunk", B=1, Hq=8, Hkv=2, d=128, capacity=256, rope_base=10000.0, seed=3)
-    cache = kvc.Cache.from_workload(w, max_chunk=16, page_pool=16)
-    q = torch.zeros((1, 16, 8, 128), dtype=torch.bfloat16, device="cuda")
-    kv = torch.zeros((1, 16, 2, 128), dtype=torch.bfloat16, device="cuda")
+    cache = kvc.Cache.from_workload(w, max_chunk=32, page_pool=2)
+    q = torch.zeros((1, 20, 8, 128), dtype=torch.bfloat16, device="cuda")
+    kv = torch.zeros((1, 20, 2, 128), dtype=torch.bfloat16, device="cuda")
+    cache.chunk(q, kv, kv)
+    tab = cache.export(kvc.KVC_EXPORT_PAGE_TABLE)[0]
+    assert (tab[:2] >= 0).all() and (tab[2:] == -1).all()         # positions 0..19: two pages
+    q2 = torch.zeros((1, 32, 8, 128), dtype=torch.bfloat16, device="cuda")
+    kv2 = torch.zeros((1, 32, 2, 128), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(kvc.KvcError) as e:
-        cache.chunk(q, kv, kv)
-    assert e.value.code == kvc.KVC_ERR_UNSUPPORTED
+        cache.chunk(q2, kv2, kv2)                                   # positions 20..51 need two more pages
+    assert e.value.code == kvc.KVC_ERR_CAPACITY
+    assert list(cache.next_positions()) == [20]
+    assert cache.device_status() == 0
