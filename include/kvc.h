@@ -90,7 +90,7 @@ typedef struct {
     int32_t max_position; /* RoPE table length; every position must stay below it.
                              0 = capacity (contiguous).  Required for a ring with RoPE. */
     float rope_base;      /* rotary base (e.g. 10000); 0 = keys and queries not rotated */
-    int32_t max_chunk;    /* largest n for kvc_chunk_attn (sizes its workspace) */
+    int32_t max_chunk;    /* largest n for kvc_chunk_attn (sizes a ring's staging rows) */
     int32_t out_dtype;    /* attention outputs: 0 = the cache dtype, else KVC_F32 or
                              KVC_BF16 (+1 is added so that 0 keeps the default):
                              pass KVC_F32 + 1 or KVC_BF16 + 1 */
@@ -249,8 +249,12 @@ int kvc_trim(kvc_t h, const int32_t* h_cut, kvc_stream_t stream);
  * positions [max(0, p-W+1), p]:
  *     d_q [B][n][Hq][d], d_k, d_v [B][n][Hkv][d]  ->  d_out [B][n][Hq][d].
  * Row i equals what kvc_decode_attn returns for that query after appending
- * rows 0..i.  bf16 caches with head_dim 128, contiguous (paged or not), without
- * INT8; n <= max_chunk.
+ * rows 0..i.  bf16 caches with head_dim 128, without INT8: contiguous, or a ring
+ * whose size W is a multiple of 16 (paged or not); n <= max_chunk.  On a ring the
+ * suffix may be longer than W: appending it first would evict rows that early
+ * suffix queries need ([LEAN] §3.4), so the call stages the rotated suffix rows
+ * in the state buffer (sized by max_chunk), attends, and then appends them; the
+ * ring ends as n one-token appends would leave it.
  * The tensor-core products take fp16 operands: the query (rotated, times
  * log2(e)/sqrt(d)), the softmax weights and the K and V rows.  Every K and V row
  * of the keys the call reads, and every scaled query, must be below 65520 in

@@ -4,8 +4,13 @@
 // suffix tokens[cut:] are computed in one chunk from next_position = cut:
 // suffix query i sits at position p = cut + i and attends to cached positions
 // [max(0, p - W + 1), p] (W = 0: all), exactly what a one-token decode at p
-// would see ([LEAN] §2.1 masks).  The suffix K/V rows are appended to the cache
-// first, so every key a query needs is in the cache.
+// would see ([LEAN] §2.1 masks).  On a contiguous cache the suffix K/V rows are
+// appended first, so every key a query needs is in the cache.  A ring of W slots
+// would evict, while appending, rows that the early suffix queries still need
+// ([LEAN] §3.4): there the suffix rows are staged, rotated, in a workspace that
+// also holds the resident rows from the cut rounded down to 16, the queries read
+// positions below that from the ring and the rest from the workspace, and the
+// suffix is appended to the ring afterwards.
 //
 // This is a dense contraction, so it runs on the 5th-generation tensor cores.
 //  * CTA = 128 query rows of two query heads that share one KV head (two "slots";
@@ -37,8 +42,9 @@
 //    (log2 domain), so weights stay <= 2^8 and O is rarely rescaled (by the
 //    softmax thread itself: at that point no P.V of its slot is in flight).
 //  * Key tiles start on 16-key boundaries.  A contiguous cache is read with two
-//    128-row tensor copies per tile; a paged cache with one 16-row copy per page
-//    and half (the block table gives the page), skipping pages before position 0.
+//    128-row tensor copies per tile; paged caches and rings with one 16-row copy per
+//    16 positions and half (from the page the block table gives, the ring slot, or
+//    the staging rows), skipping positions before 0.
 //  * CTAs are taken longest first (a host-sorted table of (request, query tile)
 //    items in the kernel parameters), the head pairs of one KV head adjacent so
 //    that they read its tiles from L2.
@@ -112,6 +118,9 @@ struct ChunkArgs {
     uint32_t* hdr;
     const int32_t* table;      // paged caches: block table [B][S/16] (else nullptr)
     int B, Hq, Hkv, g, S, W, n, out_bf16;
+    int ring;                  // keys below the cut (rounded down to 16) from the ring, the rest staged
+    int n_appended;            // suffix rows next_position already counts (contiguous: n; ring: 0)
+    int ws_rows;               // staging rows per (request, KV head) (ring)
     int tiles;                 // query tiles per request
     int pairs;                 // head pairs per KV head, ceil(g / 2)
     float scale_log2;
@@ -280,6 +289,7 @@ __device__ __forceinline__ void convert_tile(unsigned char* tile, int t, int kb,
 
 __global__ void __launch_bounds__(kThreads, 1)
     chunk_attn_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                      const __grid_constant__ CUtensorMap tmWK, const __grid_constant__ CUtensorMap tmWV,
                       const __grid_constant__ ChunkArgs a) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -302,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     else { b = item / a.tiles; tile = item % a.tiles; }
     const int i0 = tile * kBM;
     const int np = a.next_pos[b];
-    const int cut = np - a.n;
+    const int cut = np - a.n_appended;
     const int rows = min(kBM, a.n - i0);
     const int p_first = cut + i0, p_last = cut + i0 + rows - 1;
     // keys the CTA attends to: [kmin, p_last]; tiles end at kt (16-aligned) and walk back
@@ -559,9 +569,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int head_row0 = (b * a.Hkv + kvh) * a.S;
             const int npages = a.S / kPage;
             // one tile of one tensor into `dst`: two 128-row copies (contiguous cache) or one
-            // 16-row copy per page and half (paged cache; pages before position 0 skipped)
-            auto load_tile = [&](const CUtensorMap* tm, unsigned char* dst, uint64_t* full, int kb) {
-                if (!a.table) {
+            // 16-row copy per 16 positions and half: the page of a paged cache, the slot of a
+            // ring, or the staging rows at and after the ring's cut rounded down to 16
+            // (positions before 0 are skipped)
+            const int cal = cut & ~15;
+            const int ws_row0 = (b * a.Hkv + kvh) * a.ws_rows;
+            auto load_tile = [&](const CUtensorMap* tm, const CUtensorMap* tmw, unsigned char* dst, uint64_t* full,
+                                 int kb) {
+                if (!a.table && !a.ring) {
                     mbar_arrive_expect_tx(full, kTileB);
                     tma_load_2d(dst, tm, 0, head_row0 + kb, full);
                     tma_load_2d(dst + kHalfB, tm, 64, head_row0 + kb, full);
@@ -570,12 +585,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int g0 = kb < 0 ? (-kb) / 16 : 0;
                 mbar_arrive_expect_tx(full, (uint32_t)(kBN / 16 - g0) * 2 * kGroupB);
                 for (int gi = g0; gi < kBN / 16; ++gi) {
-                    const int lp = (kb >> 4) + gi;
-                    int page = lp < npages ? a.table[(size_t)b * npages + lp] : -1;
-                    page = page < 0 ? 0 : page;      // never taken: every page the CTA reads is mapped
-                    const int r = (page * a.Hkv + kvh) * kPage;
-                    tma_load_2d(dst + gi * kGroupB, tm, 0, r, full);
-                    tma_load_2d(dst + kHalfB + gi * kGroupB, tm, 64, r, full);
+                    const int pos = kb + 16 * gi;
+                    const CUtensorMap* m = tm;
+                    int r;
+                    if (a.ring && pos >= cal) {
+                        m = tmw;
+                        r = ws_row0 + (pos - cal);
+                    } else {
+                        const int slot = a.ring ? pos % a.S : pos;
+                        if (a.table) {
+                            int page = a.table[(size_t)b * npages + slot / kPage];
+                            page = page < 0 ? 0 : page;      // never taken: every page the CTA reads is mapped
+                            r = (page * a.Hkv + kvh) * kPage;
+                        } else {
+                            r = head_row0 + slot;
+                        }
+                    }
+                    tma_load_2d(dst + gi * kGroupB, m, 0, r, full);
+                    tma_load_2d(dst + kHalfB + gi * kGroupB, m, 64, r, full);
                 }
             };
             bool ok = true;
@@ -584,11 +611,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int ks = j % kKStages, vs = j % kVStages;
                 if (j >= kKStages) ok = mbar_wait(&bar[B_KFREE + ks], (uint32_t)((j / kKStages - 1) & 1));
                 if (!ok || *abort_flag) { ok = false; break; }
-                load_tile(&tmK, sK + ks * kTileB, &bar[B_KFULL + ks], kbase(j));
+                load_tile(&tmK, &tmWK, sK + ks * kTileB, &bar[B_KFULL + ks], kbase(j));
                 k_issued = j + 1;
                 if (j >= kVStages) ok = mbar_wait(&bar[B_VFREE + vs], (uint32_t)((j / kVStages - 1) & 1));
                 if (!ok || *abort_flag) { ok = false; break; }
-                load_tile(&tmV, sV + vs * kTileB, &bar[B_VFULL + vs], kbase(j));
+                load_tile(&tmV, &tmWV, sV + vs * kTileB, &bar[B_VFULL + vs], kbase(j));
                 v_issued = j + 1;
             }
             if (!ok) {
@@ -676,6 +703,61 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// ---- ring staging --------------------------------------------------------------
+struct StageArgs {
+    const __nv_bfloat16* kc;   // cache rows
+    const __nv_bfloat16* vc;
+    const int32_t* table;      // paged: block table (else nullptr)
+    const __nv_bfloat16* k;    // suffix [B][n][Hkv][d], keys not rotated
+    const __nv_bfloat16* v;
+    const float2* rope;        // nullptr = no RoPE
+    __nv_bfloat16* wk;         // staging [B][Hkv][ws_rows][d]
+    __nv_bfloat16* wv;
+    const int32_t* next_pos;   // the cut (before the append)
+    int Hkv, S, n, ws_rows;
+};
+
+// Staging row r of (request b, KV head h) holds position cal + r, cal = cut rounded
+// down to 16: rows below the cut copied from the ring, suffix rows rotated at their
+// position (fp32, each product and sum rounded once, then bf16 round to nearest:
+// the append's arithmetic).  16 bytes per thread, 8 rows per CTA of 128 threads.
+__global__ void __launch_bounds__(128) chunk_stage_kernel(const StageArgs a) {
+    const int b = blockIdx.z, h = blockIdx.y;
+    const int r = blockIdx.x * 8 + (threadIdx.x >> 4), c = threadIdx.x & 15;
+    const int cut = a.next_pos[b], cal = cut & ~15;
+    if (r >= cut - cal + a.n) return;
+    const int pos = cal + r;
+    uint4 ko, vo;
+    if (pos < cut) {
+        const size_t src = kv_row(a.table, b, h, pos % a.S, a.Hkv, a.S) * kD + 8 * (size_t)c;
+        ko = *reinterpret_cast<const uint4*>(a.kc + src);
+        vo = *reinterpret_cast<const uint4*>(a.vc + src);
+    } else {
+        const size_t src = (((size_t)b * a.n + (pos - cut)) * a.Hkv + h) * kD + 8 * (size_t)c;
+        ko = __ldg(reinterpret_cast<const uint4*>(a.k + src));
+        vo = __ldg(reinterpret_cast<const uint4*>(a.v + src));
+        if (a.rope) {
+            const float4* rp = reinterpret_cast<const float4*>(a.rope + (size_t)pos * (kD / 2) + 4 * c);
+            const float4 c0 = __ldg(rp), c1 = __ldg(rp + 1);
+            uint32_t w[4] = {ko.x, ko.y, ko.z, ko.w};
+            const float2 cs[4] = {make_float2(c0.x, c0.y), make_float2(c0.z, c0.w), make_float2(c1.x, c1.y),
+                                  make_float2(c1.z, c1.w)};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const __nv_bfloat162 x2 = *reinterpret_cast<const __nv_bfloat162*>(&w[e]);
+                float y0, y1;
+                rope_pair(__low2float(x2), __high2float(x2), cs[e], y0, y1);
+                const __nv_bfloat162 o2 = __floats2bfloat162_rn(y0, y1);
+                w[e] = *reinterpret_cast<const uint32_t*>(&o2);
+            }
+            ko = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    }
+    const size_t dst = (((size_t)b * a.Hkv + h) * a.ws_rows + r) * kD + 8 * (size_t)c;
+    *reinterpret_cast<uint4*>(a.wk + dst) = ko;
+    *reinterpret_cast<uint4*>(a.wv + dst) = vo;
+}
+
 // ---- tensor maps -----------------------------------------------------------
 using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -706,18 +788,45 @@ bool make_tensor_map_bf16(CUtensorMap* tm, void* base, int rank, const cuuint64_
            CUDA_SUCCESS;
 }
 
-bool chunk_supported(const Shape& s) { return s.bf16 && !s.int8 && !s.ring && s.d == kD; }
+bool chunk_supported(const Shape& s) { return s.bf16 && !s.int8 && s.d == kD && (!s.ring || s.S % 16 == 0); }
 
-cudaError_t launch_chunk(kvc_handle* h, const void* q, void* out, int n, cudaStream_t st) {
+cudaError_t launch_chunk(kvc_handle* h, const void* q, const void* k, const void* v, void* out, int n,
+                         cudaStream_t st) {
     const Shape& s = h->sh;
-    CUtensorMap tk, tv;
+    const int ws = chunk_ws_rows(s);
+    CUtensorMap tk, tv, twk, twv;
     const cuuint64_t rows = s.pages ? (cuuint64_t)s.pages * s.Hkv * kPage : (cuuint64_t)s.B * s.Hkv * s.S;
     const cuuint64_t kdims[2] = {(cuuint64_t)s.d, rows};
     const cuuint64_t kstr[1] = {(cuuint64_t)s.d * 2};
-    const cuuint32_t kbox[2] = {64, s.pages ? (cuuint32_t)kPage : (cuuint32_t)kBN};
+    const cuuint32_t kbox[2] = {64, (s.pages || s.ring) ? (cuuint32_t)kPage : (cuuint32_t)kBN};
     if (!make_tensor_map_bf16(&tk, h->state + h->L.k, 2, kdims, kstr, kbox) ||
         !make_tensor_map_bf16(&tv, h->state + h->L.v, 2, kdims, kstr, kbox))
         return cudaErrorInvalidValue;
+    twk = tk; twv = tv;
+    if (s.ring) {
+        // staging rows, then the suffix attention reads them beside the ring
+        const size_t half = (size_t)s.B * s.Hkv * ws * s.d;
+        __nv_bfloat16* wk = reinterpret_cast<__nv_bfloat16*>(h->state + h->L.cws);
+        const cuuint64_t wdims[2] = {(cuuint64_t)s.d, (cuuint64_t)s.B * s.Hkv * ws};
+        const cuuint32_t wbox[2] = {64, (cuuint32_t)kPage};
+        if (!make_tensor_map_bf16(&twk, wk, 2, wdims, kstr, wbox) ||
+            !make_tensor_map_bf16(&twv, wk + half, 2, wdims, kstr, wbox))
+            return cudaErrorInvalidValue;
+        StageArgs sa{};
+        sa.kc = reinterpret_cast<const __nv_bfloat16*>(h->state + h->L.k);
+        sa.vc = reinterpret_cast<const __nv_bfloat16*>(h->state + h->L.v);
+        sa.table = s.pages ? reinterpret_cast<const int32_t*>(h->state + h->L.table) : nullptr;
+        sa.k = static_cast<const __nv_bfloat16*>(k);
+        sa.v = static_cast<const __nv_bfloat16*>(v);
+        sa.rope = s.rope ? reinterpret_cast<const float2*>(h->state + h->L.rope) : nullptr;
+        sa.wk = wk;
+        sa.wv = wk + half;
+        sa.next_pos = reinterpret_cast<const int32_t*>(h->state + h->L.next_pos);
+        sa.Hkv = s.Hkv; sa.S = s.S; sa.n = n; sa.ws_rows = ws;
+        chunk_stage_kernel<<<dim3((n + 15 + 7) / 8, s.Hkv, s.B), 128, 0, st>>>(sa);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
     static bool attr = false;
     if (!attr) {
         cudaError_t e = cudaFuncSetAttribute(chunk_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
@@ -733,6 +842,7 @@ cudaError_t launch_chunk(kvc_handle* h, const void* q, void* out, int n, cudaStr
     a.out = out; a.hdr = reinterpret_cast<uint32_t*>(h->state + h->L.hdr);
     a.table = s.pages ? reinterpret_cast<const int32_t*>(h->state + h->L.table) : nullptr;
     a.B = s.B; a.Hq = s.Hq; a.Hkv = s.Hkv; a.g = s.g; a.S = s.S; a.W = s.W; a.n = n; a.out_bf16 = s.out_bf16;
+    a.ring = s.ring; a.n_appended = s.ring ? 0 : n; a.ws_rows = ws;
     a.tiles = (n + kBM - 1) / kBM;
     a.pairs = (s.g + 1) / 2;
     a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)s.d));
@@ -743,7 +853,7 @@ cudaError_t launch_chunk(kvc_handle* h, const void* q, void* out, int n, cudaStr
         std::vector<std::pair<int, uint32_t>> w(items);
         for (int b = 0; b < s.B; ++b)
             for (int t = 0; t < a.tiles; ++t) {
-                const int cut = h->np[b] - n, i0 = t * kBM, rows = std::min(kBM, n - i0);
+                const int cut = h->np[b] - a.n_appended, i0 = t * kBM, rows = std::min(kBM, n - i0);
                 const int p_first = cut + i0, p_last = p_first + rows - 1;
                 const int kmin = s.W > 0 ? std::max(0, p_first - s.W + 1) : 0;
                 const int kt = (p_last + 16) & ~15;
@@ -756,7 +866,7 @@ cudaError_t launch_chunk(kvc_handle* h, const void* q, void* out, int n, cudaStr
         for (int i = 0; i < items; ++i) a.items[i] = w[i].second;
         a.n_items = items;
     }
-    chunk_attn_kernel<<<dim3(items * s.Hkv * a.pairs), kThreads, SMEM_BYTES, st>>>(tk, tv, a);
+    chunk_attn_kernel<<<dim3(items * s.Hkv * a.pairs), kThreads, SMEM_BYTES, st>>>(tk, tv, twk, twv, a);
     return cudaGetLastError();
 }
 

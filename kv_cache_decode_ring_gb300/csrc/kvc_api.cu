@@ -14,7 +14,6 @@ cudaError_t launch_append_rows_counts(const AppendArgs& a, const int32_t* counts
 bool fast_decode_supported(const DecodeArgs& a);
 cudaError_t launch_int8_decode(kvc_handle* h, const void* q, void* out, float* cmax, float* tanh_out,
                                float* ct, cudaStream_t st);
-cudaError_t launch_chunk(kvc_handle* h, const void* q, void* out, int n, cudaStream_t st);
 
 namespace {
 
@@ -131,6 +130,8 @@ Layout make_layout(const Shape& s) {
     L.part_ml = take(B * Hq * s.max_splits * 8);
     L.part_acc = take(B * Hq * s.max_splits * d * 4);
     if (s.int8) L.part_c = take(B * Hq * s.max_splits * 4);
+    if (s.ring && s.bf16 && !s.int8 && s.max_chunk > 0)
+        L.cws = take(2 * B * Hkv * (size_t)chunk_ws_rows(s) * d * 2);
     if (s.store_slots > 0) {
         L.store_stride = align256(2 * Hkv * S * d * s.elem + S * 4);
         L.store = take((size_t)s.store_slots * L.store_stride);
@@ -447,14 +448,23 @@ int kvc_chunk_attn(kvc_t h, const void* d_q, const void* d_k, const void* d_v, i
         if (map_pages(h, from, to, st, &rc) != cudaSuccess) return KVC_ERR_CUDA;
         if (rc) return rc;
     }
-    // the suffix rows join the cache first (rotated keys, positions cut .. cut+n-1) ...
     h->counts.assign(s.B, n);
     AppendArgs a = append_args(h, d_k, d_v, n);
     a.sb = (size_t)n * s.Hkv * s.d; a.sh = s.d; a.sr = (size_t)s.Hkv * s.d;   // [B][n][Hkv][d]
+    if (s.ring) {
+        // a ring would evict rows that the early suffix queries still need: the suffix is
+        // staged beside the resident rows, attended, and only then appended
+        if (launch_chunk(h, d_q, d_k, d_v, d_out, n, st) != cudaSuccess) return KVC_ERR_CUDA;
+        if (launch_append_rows_counts(a, h->counts.data(), st) != cudaSuccess) return KVC_ERR_CUDA;
+        for (auto& p : h->np) p += n;
+        h->ring_needs_append = false;
+        return KVC_OK;
+    }
+    // the suffix rows join the cache first (rotated keys, positions cut .. cut+n-1) ...
     if (launch_append_rows_counts(a, h->counts.data(), st) != cudaSuccess) return KVC_ERR_CUDA;
     for (auto& p : h->np) p += n;
     // ... then every suffix query attends over its window
-    if (launch_chunk(h, d_q, d_out, n, st) != cudaSuccess) return KVC_ERR_CUDA;
+    if (launch_chunk(h, d_q, d_k, d_v, d_out, n, st) != cudaSuccess) return KVC_ERR_CUDA;
     return KVC_OK;
 }
 

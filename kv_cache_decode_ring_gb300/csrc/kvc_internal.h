@@ -57,6 +57,7 @@ struct Layout {
     size_t part_acc;  // float  [B][Hq][max_splits][d]
     size_t part_c;    // float  [B][Hq][max_splits] max_t c_t of the split   (INT8)
     size_t req_id;    // uint32 [B] request IDs of the dither counters (Tier B)
+    size_t cws;       // ring caches with kvc_chunk_attn: K then V staging [B][Hkv][chunk_ws_rows][d] bf16
     size_t store;     // store slots: each K, V [Hkv][S][d] cache dtype, then positions int32 [S]
     size_t store_stride;  // bytes per store slot
     size_t total;
@@ -79,6 +80,9 @@ struct Shape {
 };
 
 bool make_shape(const kvc_config& c, Shape* s);
+// Rows per (request, KV head) of a ring's chunk staging: positions from the cut rounded
+// down to 16 up to the last suffix row rounded up to 16.
+inline int chunk_ws_rows(const Shape& s) { return ((s.max_chunk + 15) & ~15) + 32; }
 Layout make_layout(const Shape& s);
 
 // Arguments of the decode kernels (everything by value; no host pointers).
@@ -165,6 +169,11 @@ cudaError_t launch_decode(const DecodeArgs& d, const CombineArgs& c, bool fast, 
 bool chunk_supported(const Shape& s);
 bool gqa_decode_supported(int d, int g);
 cudaError_t launch_decode_gqa(const DecodeArgs& a, const KvMaps& maps, cudaStream_t st);
+// Chunked suffix attention (chunk.cu).  A contiguous cache has already appended the n
+// suffix rows; a ring first stages them (rotated) next to its resident rows and
+// appends them after the attention (the caller does).
+cudaError_t launch_chunk(kvc_handle* h, const void* q, const void* k, const void* v, void* out, int n,
+                         cudaStream_t st);
 
 // ---- INT8 code storage --------------------------------------------------------
 // Inside one 16-token block of one (request, KV head) the 16*d code bytes are

@@ -145,3 +145,42 @@ def test_chunk_flags_values_beyond_fp16_range():
     cache.chunk(q.cuda(), k.cuda(), v.cuda())
     assert cache.device_status() == 4
     assert cache.device_status() == 0          # read and cleared
+
+
+RING_CASES = [
+    # name, capacity W, lengths before, cuts (None = no trim), n, paged
+    ("ring-wrapped-no-trim", 256, [600, 300, 257], None, 200, False),
+    ("ring-not-full-trim", 256, [200, 130, 40], [77, 130, 0], 300, False),   # the suffix wraps the ring
+    ("ring-suffix-longer-than-w", 128, [100, 5, 300], None, 300, False),
+    ("ring-paged", 256, [600, 300, 257], None, 200, True),
+]
+
+
+@pytest.mark.parametrize("case", RING_CASES, ids=lambda c: c[0])
+def test_ring_chunk_matches_recompute(case):
+    # on a ring the suffix rows are staged, attended beside the resident rows, then
+    # appended: outputs against the oracle's one-token-at-a-time continuation, and the
+    # ring's slots and positions afterwards bit-exact
+    name, W, lengths, cuts, n, paged = case
+    w = wl.small("chunk-" + name, B=3, Hq=8, Hkv=2, d=128, layout="ring", capacity=W, window=W,
+                 rope_base=10000.0, seed=43)
+    cache = kvc.Cache.from_workload(w, max_chunk=n, max_position=4096, out_dtype="f32",
+                                    page_pool=3 * (W // 16) if paged else 0)
+    model = oracle_for(w)
+    k, v = w.prefill_chunk(0, max(lengths))
+    cache.append_rows(k.cuda(), v.cuda(), counts=lengths)
+    model.append_rows(host(k), host(v), lengths)
+    if cuts is not None:
+        cache.trim(cuts)
+        model.trim(cuts)
+    q, ks, vs = _suffix(w, n)
+    out = cache.chunk(q.cuda(), ks.cuda(), vs.cuda())
+    ref = model.chunk(host(q), host(ks), host(vs))
+    assert_close(out, ref, "bf16", "ring chunk %s" % name)
+    check_state(cache, model, w)
+    # and the ring keeps decoding from there
+    q1, k1, v1 = w.step_qkv(0)
+    cache.append(k1.cuda(), v1.cuda())
+    model.append(host(k1), host(v1))
+    assert_close(cache.decode(q1.cuda()), model.decode(host(q1)), "bf16", "decode after the ring chunk")
+    assert cache.device_status() == 0
