@@ -102,8 +102,10 @@ typedef struct {
                              request owns `capacity` slots; > 0 = K and V live in a pool
                              of page_pool pages of 16 slots (all KV heads of one request)
                              mapped by a per-request block table, allocated on append and
-                             freed by trim.  Not with INT8; capacity (the
-                             per-request logical slots) must be a multiple of 16. */
+                             freed by trim; capacity (the per-request logical
+                             slots) must be a multiple of 16.  With INT8 a page holds
+                             one quantization block of every KV head (codes, scales,
+                             witnesses); the exact tail stays per request; no gate pool. */
     int32_t store_slots;  /* device slots for saved prefills (kvc_store_save /
                              kvc_store_load), each holding one request's K, V and
                              positions; 0 = none.  Not with INT8. */

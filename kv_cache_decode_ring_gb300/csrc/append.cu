@@ -103,11 +103,11 @@ __device__ void quantize_block(const AppendArgs& a, const float* sK, const float
     mk = 0.f; mv = 0.f;
     for (int w = 0; w < nw; ++w) { mk = fmaxf(mk, red[w]); mv = fmaxf(mv, red[32 + w]); }
     const float s_k = __fdiv_rn(mk, 127.0f), s_v = __fdiv_rn(mv, 127.0f);
-    const size_t bh = (size_t)b * a.Hkv + h;
-    const size_t row0 = bh * a.S + (size_t)pblk * kQBlock;
+    const size_t lin = int8_block(a.table, b, h, pblk, a.Hkv, a.S);
+    const size_t row0 = lin * kQBlock;
     if (threadIdx.x == 0) {
-        a.sk[bh * (a.S / kQBlock) + pblk] = s_k;
-        a.sv[bh * (a.S / kQBlock) + pblk] = s_v;
+        a.sk[lin] = s_k;
+        a.sv[lin] = s_v;
     }
     // codes stored biased (c + 128) at the block positions kq_offset / vq_offset
     uint8_t* kb = reinterpret_cast<uint8_t*>(a.kq) + row0 * d;

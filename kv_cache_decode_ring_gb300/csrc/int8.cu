@@ -77,6 +77,7 @@ struct Int8Args {
     float* ct;          // nullable: c_t per token [B][Hq][S]
     uint32_t* hdr;
     const uint32_t* req_id;         // Tier B: request IDs of the dither counters
+    const int32_t* table;           // paged caches: the block table (a page is one block)
     uint32_t layer_ctr;             // Tier B: 65536 * layer
     uint32_t rk[20];                // Tier B: Philox round keys (k0 + r W0, k1 + r W1), r = 0..9
     int B, Hq, Hkv, d, S, max_splits;
@@ -333,7 +334,6 @@ int8_decode_kernel(const Int8Args a) {
 
     // ---- quantized split ----------------------------------------------------
     const size_t bh = (size_t)b * a.Hkv + kvh;
-    const size_t row0 = bh * a.S;
     unsigned char* myS = smem + warp * C::WARPB;
     uint64_t* myBar = bar + warp * kStages;
     // block of this warp's tile i (tiles of the 4 warps interleaved)
@@ -341,13 +341,13 @@ int8_decode_kernel(const Int8Args a) {
     auto tile_ok = [&](int i) { return tile_blk(i) < iw.bhi; };
     auto issue = [&](int i) {
         if (lane == 0 && tile_ok(i)) {
-            const size_t p0 = (size_t)tile_blk(i) * kQBlock;
+            const size_t r0 = int8_block(a.table, b, kvh, tile_blk(i), a.Hkv, a.S) * kQBlock;   // its first row
             const int sg = i % kStages;
             unsigned char* st = myS + sg * C::STAGEB;
             mbar_arrive_expect_tx(&myBar[sg], (uint32_t)C::STAGEB);
-            bulk_copy_g2s(st, a.kq + (row0 + p0) * D, C::CB, &myBar[sg]);
-            bulk_copy_g2s(st + C::CB, a.vq + (row0 + p0) * D, C::CB, &myBar[sg]);
-            if (!DITHER) bulk_copy_g2s(st + 2 * C::CB, a.wit + (row0 + p0) * kBands, C::WB, &myBar[sg]);
+            bulk_copy_g2s(st, a.kq + r0 * D, C::CB, &myBar[sg]);
+            bulk_copy_g2s(st + C::CB, a.vq + r0 * D, C::CB, &myBar[sg]);
+            if (!DITHER) bulk_copy_g2s(st + 2 * C::CB, a.wit + r0 * kBands, C::WB, &myBar[sg]);
         }
     };
     if (lane == 0) {
@@ -364,8 +364,9 @@ int8_decode_kernel(const Int8Args a) {
     float skv = 0.f, rvv = 0.f;
     int xmv = -1;                                     // >= 0: restored, served by the exact split
     if (lane < tpw && tile_ok(lane)) {
-        skv = a.sk[bh * (a.S / kQBlock) + tile_blk(lane)];
-        rvv = a.sv[bh * (a.S / kQBlock) + tile_blk(lane)];
+        const size_t lin = int8_block(a.table, b, kvh, tile_blk(lane), a.Hkv, a.S);
+        skv = a.sk[lin];
+        rvv = a.sv[lin];
         xmv = a.xmap[bh * (a.S / kQBlock) + tile_blk(lane)];
     }
     float svmax = rvv;
@@ -773,6 +774,7 @@ cudaError_t launch_int8_decode(kvc_handle* h, const void* q, void* out, float* c
     a.sv = reinterpret_cast<const float*>(h->state + h->L.sv);
     a.wit = s.dither ? nullptr : reinterpret_cast<const __half*>(h->state + h->L.wit);
     a.req_id = reinterpret_cast<const uint32_t*>(h->state + h->L.req_id);
+    a.table = s.pages ? reinterpret_cast<const int32_t*>(h->state + h->L.table) : nullptr;
     a.layer_ctr = 65536u * (uint32_t)h->cfg.layer_index;
     for (int r = 0; r < 10; ++r) {
         a.rk[2 * r] = h->cfg.dither_key_lo + (uint32_t)r * 0x9E3779B9u;

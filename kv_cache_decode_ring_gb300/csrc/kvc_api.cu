@@ -55,7 +55,8 @@ bool make_shape(const kvc_config& c, Shape* s) {
     if (c.int8_exact_blocks < 0 ||
         ((!int8 || dither || ring || c.window != 0) && c.int8_exact_blocks != 0))
         return false;
-    if (c.page_pool < 0 || (c.page_pool > 0 && (int8 || c.capacity % kPage))) return false;
+    if (c.page_pool < 0 || (c.page_pool > 0 && c.capacity % kPage)) return false;
+    if (c.page_pool > 0 && c.int8_exact_blocks != 0) return false;   // the gate's pool: unpaged caches
     if (c.store_slots < 0 || (c.store_slots > 0 && int8)) return false;
     if (int8) {
         const int g = c.n_q_heads / c.n_kv_heads;
@@ -112,11 +113,14 @@ Layout make_layout(const Shape& s) {
         L.v = take(rows * d * s.elem);
         if (s.pages) L.table = take(B * (S / kPage) * 4);
     } else {
-        L.kq = take(B * Hkv * S * d);
-        L.vq = take(B * Hkv * S * d);
-        L.sk = take(B * Hkv * (S / kQBlock) * 4);
-        L.sv = take(B * Hkv * (S / kQBlock) * 4);
-        if (!s.dither) L.wit = take(B * Hkv * S * kBands * 2);
+        // quantized blocks: [B][Hkv][S/16], or [pages][Hkv] on a paged cache
+        const size_t blocks = s.pages ? (size_t)s.pages * Hkv : B * Hkv * (S / kQBlock);
+        L.kq = take(blocks * kQBlock * d);
+        L.vq = take(blocks * kQBlock * d);
+        L.sk = take(blocks * 4);
+        L.sv = take(blocks * 4);
+        if (!s.dither) L.wit = take(blocks * kQBlock * kBands * 2);
+        if (s.pages) L.table = take(B * (S / kPage) * 4);
         L.ktail = take(B * Hkv * kQBlock * d * 2);
         L.vtail = take(B * Hkv * kQBlock * d * 2);
         L.xmap = take(B * Hkv * (S / kQBlock) * 4);
@@ -540,10 +544,33 @@ int kvc_export(kvc_t h, int32_t which, void* h_dst, size_t bytes, kvc_stream_t s
         return KVC_OK;
     }
     const bool codes = which == KVC_EXPORT_KQ || which == KVC_EXPORT_VQ;
+    const bool paged_blocks = h->sh.pages && h->sh.int8 &&
+                              (codes || which == KVC_EXPORT_SK || which == KVC_EXPORT_SV || which == KVC_EXPORT_WITNESS);
     std::vector<uint8_t> raw(codes ? need : 0);
     void* dst = codes ? static_cast<void*>(raw.data()) : h_dst;
-    if (cudaMemcpyAsync(dst, h->state + off, need, cudaMemcpyDeviceToHost, st) != cudaSuccess) return KVC_ERR_CUDA;
-    if (cudaStreamSynchronize(st) != cudaSuccess) return KVC_ERR_CUDA;
+    if (paged_blocks) {
+        // quantized blocks live in pages ([pages][Hkv] blocks): gather them into the logical
+        // [B][Hkv][capacity/16] block order through the host mirror of the block table
+        const Shape& s = h->sh;
+        const size_t npg = s.S / kPage, per = need / ((size_t)s.B * s.Hkv * npg);
+        std::vector<uint8_t> pool((size_t)s.pages * s.Hkv * per);
+        if (cudaMemcpyAsync(pool.data(), h->state + off, pool.size(), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+            return KVC_ERR_CUDA;
+        if (cudaStreamSynchronize(st) != cudaSuccess) return KVC_ERR_CUDA;
+        uint8_t* o = static_cast<uint8_t*>(dst);
+        std::memset(o, 0, need);
+        for (int b = 0; b < s.B; ++b)
+            for (size_t lp = 0; lp < npg; ++lp) {
+                const int page = h->table_h[b * npg + lp];
+                if (page < 0) continue;
+                for (int hh = 0; hh < s.Hkv; ++hh)
+                    std::memcpy(o + (((size_t)b * s.Hkv + hh) * npg + lp) * per,
+                                pool.data() + ((size_t)page * s.Hkv + hh) * per, per);
+            }
+    } else {
+        if (cudaMemcpyAsync(dst, h->state + off, need, cudaMemcpyDeviceToHost, st) != cudaSuccess) return KVC_ERR_CUDA;
+        if (cudaStreamSynchronize(st) != cudaSuccess) return KVC_ERR_CUDA;
+    }
     if (codes) {
         // stored biased in the decode's block order; exported signed, token-major [S][d]
         const int d = h->sh.d;

@@ -302,6 +302,17 @@ __host__ __device__ __forceinline__ Int8Window int8_window(int len, int S, int W
     if (w.bhi < w.blo) w.bhi = w.blo;
     return w;
 }
+// Linear index of the quantization block in block slot k of (request b, KV head h):
+// blocks [B][Hkv][S/16], or, on a paged cache (a 16-slot page is one block), the
+// page the block table maps times Hkv plus h.  Codes sit at 16 d bytes per block,
+// witnesses at 16 x 16 halves, scales at one float.
+__host__ __device__ __forceinline__ size_t int8_block(const int32_t* table, int b, int h, int k, int Hkv, int S) {
+    if (!table) return ((size_t)b * Hkv + h) * (S / kQBlock) + k;
+    int page = table[(size_t)b * (S / kQBlock) + k];
+    page = page < 0 ? 0 : page;       // never taken: every block read or written is mapped first
+    return (size_t)page * Hkv + h;
+}
+
 // Absolute block number held by physical block slot k.
 __host__ __device__ __forceinline__ int int8_abs_block(const Int8Window& w, int k, int ring) {
     if (!ring || w.nfb <= w.nbk) return k;

@@ -61,7 +61,8 @@ def test_state_bytes_validation(lib):
                         int8_exact_blocks=4),                                    # gate with a window
         kvc.make_config("bf16", "contiguous", None, 1, 1, 1, 128, 64, int8_exact_blocks=4),  # pool needs INT8
         kvc.make_config("bf16", "contiguous", "int8", 1, 4, 1, 128, 64, int8_exact_blocks=-1),
-        kvc.make_config("bf16", "contiguous", "int8", 1, 4, 1, 128, 64, page_pool=8),   # paged INT8
+        kvc.make_config("bf16", "contiguous", "int8", 1, 4, 1, 128, 64, page_pool=8,
+                        int8_exact_blocks=4),                                    # gate pool of a paged cache
         kvc.make_config("bf16", "contiguous", None, 1, 4, 1, 128, 72, page_pool=8),     # capacity % 16
         kvc.make_config("bf16", "ring", None, 1, 4, 1, 128, 40, page_pool=8, max_position=64),  # W % 16
         kvc.make_config("bf16", "contiguous", None, 1, 4, 1, 128, 64, page_pool=-1),
@@ -76,7 +77,9 @@ def test_state_bytes_validation(lib):
     # the INT8 tiers on a ring (W % 16 == 0) or with a window
     for c in [kvc.make_config("bf16", "ring", "int8", 1, 4, 1, 128, 64),
               kvc.make_config("bf16", "ring", "int8-dither", 1, 4, 1, 128, 64),
-              kvc.make_config("bf16", "contiguous", "int8", 1, 4, 1, 128, 64, window=8)]:
+              kvc.make_config("bf16", "contiguous", "int8", 1, 4, 1, 128, 64, window=8),
+              kvc.make_config("bf16", "contiguous", "int8", 1, 4, 1, 128, 64, page_pool=8),
+              kvc.make_config("bf16", "ring", "int8-dither", 1, 4, 1, 128, 64, page_pool=8)]:
         assert kvc.kvc_state_bytes(c) > 0
     for c in bad:
         with pytest.raises(kvc.KvcError) as e:

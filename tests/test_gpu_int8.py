@@ -344,7 +344,7 @@ def check_decode_window(cache, model, q, ring):
         if not bound:
             continue
         t = model.length(b) - 1
-        lo = max(0, t - model.window + 1)
+        lo = max(0, t - model.window + 1) if model.window else 0
         slots = np.arange(lo, t + 1) % S if ring else np.arange(lo, t + 1)
         c_gpu = ct[b, hq].cpu().numpy().astype(np.float64)[slots]
         assert c_gpu.shape == r["c"].shape
@@ -428,4 +428,45 @@ def test_int8_ring_trim_rules():
         model.append(host(k1), host(v1))
         check_decode_window(cache, model, q, ring=True)
     check_int8_ring_state(cache, model)
+    assert cache.device_status() == 0
+
+
+
+@pytest.mark.parametrize("layout,quant", [("contiguous", "int8"), ("ring", "int8"), ("ring", "int8-dither")])
+def test_int8_paged(layout, quant):
+    # a 16-slot page holds one quantization block of every KV head: codes, scales and
+    # witnesses gathered through the block table equal the unpaged layout's, bit for bit
+    extra = {"outliers": (4, 20.0)}
+    if quant == "int8-dither":
+        extra.update(dither_key=(0x243F6A88, 0x85A308D3), layer=0)
+    W = 128
+    w = wl.small("int8-paged-%s-%s" % (layout, quant), B=3, Hq=8, Hkv=2, d=128, layout=layout,
+                 capacity=512 if layout == "contiguous" else W, window=0 if layout == "contiguous" else W,
+                 rope_base=10000.0, quant=quant, seed=47, **extra)
+    cap = w.capacity
+    cache = kvc.Cache.from_workload(w, out_dtype="f32", page_pool=3 * cap // 16,
+                                    max_position=1024 if layout == "ring" else 0)
+    model = _oracle_layout(w)
+    lengths = [3, 200, 300] if layout == "ring" else [3, 200, 400]
+    k, v = w.prefill_chunk(0, max(lengths))
+    cache.append_rows(k.cuda(), v.cuda(), counts=lengths)
+    model.append_rows(host(k), host(v), lengths)
+    check = check_int8_ring_state if layout == "ring" else check_int8_state
+    check(cache, model)
+    for s in range(20):
+        q, k1, v1 = w.step_qkv(s)
+        cache.append(k1.cuda(), v1.cuda())
+        model.append(host(k1), host(v1))
+        check_decode_window(cache, model, q, ring=layout == "ring")
+    check(cache, model)
+    if layout == "contiguous":
+        cache.trim([0, 192, 400])                       # block boundaries: pages past the cut return
+        model.trim([0, 192, 400])
+        tab = cache.export(kvc.KVC_EXPORT_PAGE_TABLE)
+        assert (tab[0] < 0).all() and (tab[1, :12] >= 0).all() and (tab[1, 12:] < 0).all()
+        q, k1, v1 = w.step_qkv(50)
+        cache.append(k1.cuda(), v1.cuda())
+        model.append(host(k1), host(v1))
+        check_decode_window(cache, model, q, ring=False)
+        check(cache, model)
     assert cache.device_status() == 0
