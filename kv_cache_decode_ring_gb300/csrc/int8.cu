@@ -211,7 +211,10 @@ __device__ __forceinline__ int prow(int n) { return 32 * n + (n >= 4 ? 16 : 0); 
 // same accumulator ((code - u) s = s code + s (-u)); values are plain codes.  No
 // witnesses are read and no bound is formed.
 // At most 4 heads per KV head (or d = 64) fit 4 CTAs per SM (at most 128 registers).
-template <int D, int G, bool DITHER>
+// GEN: a windowed, ring or paged cache (block slots from int8_window, blocks through the
+// table, the first block masked before the window start); without it the kernel serves
+// a contiguous cache attending to its whole history with none of that arithmetic.
+template <int D, int G, bool DITHER, bool GEN>
 __global__ void __launch_bounds__(kWarps * 32, (D < 128 || G <= 4) ? 4 : 3)
 int8_decode_kernel(const Int8Args a) {
     using C = I8<D, G, DITHER>;
@@ -230,7 +233,8 @@ int8_decode_kernel(const Int8Args a) {
     const int len = a.next_pos[b];
     const int nfull = len & ~(kQBlock - 1);
     // the window's complete blocks: physical block slots [blo, bhi) (see int8_window)
-    const Int8Window iw = int8_window(len, a.S, a.W, a.ring);
+    const Int8Window iw = GEN ? int8_window(len, a.S, a.W, a.ring)
+                              : Int8Window{0, len / kQBlock, 0, len / kQBlock, a.S / kQBlock};
     const int bps = a.split / kQBlock;                        // blocks per split
     const int nsq = (iw.bhi - iw.blo + bps - 1) / bps;
     const int tpw = a.split / (kWarps * kQBlock);             // tiles per warp
@@ -272,7 +276,7 @@ int8_decode_kernel(const Int8Args a) {
         }
         for (int r0 = 0; r0 < total; r0 += 32) {
             const int r = r0 + lane;
-            const bool valid = r < total && nfull + r >= iw.lo;     // rows before the window are masked
+            const bool valid = r < total && (!GEN || nfull + r >= iw.lo);   // rows before the window: masked
             float s[G];
 #pragma unroll
             for (int h = 0; h < G; ++h) s[h] = -INFINITY;
@@ -286,7 +290,7 @@ int8_decode_kernel(const Int8Args a) {
                 }
                 if (a.ct) {
                     const int p = row_pos(r);
-                    const int slot = a.ring ? p % a.S : p;          // a ring's slot of position p
+                    const int slot = (GEN && a.ring) ? p % a.S : p;   // a ring's slot of position p
 #pragma unroll
                     for (int h = 0; h < G; ++h) a.ct[(rowq0 + h) * a.S + slot] = 0.f;
                 }
@@ -341,7 +345,8 @@ int8_decode_kernel(const Int8Args a) {
     auto tile_ok = [&](int i) { return tile_blk(i) < iw.bhi; };
     auto issue = [&](int i) {
         if (lane == 0 && tile_ok(i)) {
-            const size_t r0 = int8_block(a.table, b, kvh, tile_blk(i), a.Hkv, a.S) * kQBlock;   // its first row
+            const size_t r0 = (GEN ? int8_block(a.table, b, kvh, tile_blk(i), a.Hkv, a.S)
+                                   : bh * (a.S / kQBlock) + tile_blk(i)) * kQBlock;   // its first row
             const int sg = i % kStages;
             unsigned char* st = myS + sg * C::STAGEB;
             mbar_arrive_expect_tx(&myBar[sg], (uint32_t)C::STAGEB);
@@ -364,7 +369,8 @@ int8_decode_kernel(const Int8Args a) {
     float skv = 0.f, rvv = 0.f;
     int xmv = -1;                                     // >= 0: restored, served by the exact split
     if (lane < tpw && tile_ok(lane)) {
-        const size_t lin = int8_block(a.table, b, kvh, tile_blk(lane), a.Hkv, a.S);
+        const size_t lin = GEN ? int8_block(a.table, b, kvh, tile_blk(lane), a.Hkv, a.S)
+                               : bh * (a.S / kQBlock) + tile_blk(lane);
         skv = a.sk[lin];
         rvv = a.sv[lin];
         xmv = a.xmap[bh * (a.S / kQBlock) + tile_blk(lane)];
@@ -458,9 +464,9 @@ int8_decode_kernel(const Int8Args a) {
         const unsigned char* tV = tK + C::CB;
         const uint4* tW = reinterpret_cast<const uint4*>(tK + 2 * C::CB);
         const int p0 = tile_blk(i) * kQBlock;                          // first slot of the block
-        const int pa = int8_abs_block(iw, tile_blk(i), a.ring) * kQBlock;  // its first position
+        const int pa = GEN ? int8_abs_block(iw, tile_blk(i), a.ring) * kQBlock : p0;   // its first position
         // tokens g and g + 8 of the block before the window start are masked (first block only)
-        const bool vis0 = pa + g >= iw.lo, vis1 = pa + g + 8 >= iw.lo;
+        const bool vis0 = !GEN || pa + g >= iw.lo, vis1 = !GEN || pa + g + 8 >= iw.lo;
         if (!mbar_wait(&myBar[sg], par)) {
             // give up: flag it, and let this stage's copy and the later stages'
             // (if issued) land before the stages are reused for the partial
@@ -747,18 +753,24 @@ __global__ void __launch_bounds__(kCombineThreads) int8_combine_kernel(const Int
     }
 }
 
-template <int D, int G, bool DITHER>
+template <int D, int G, bool DITHER, bool GEN>
 cudaError_t launch_t(const Int8Args& a, cudaStream_t st) {
     using C = I8<D, G, DITHER>;
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(int8_decode_kernel<D, G, DITHER>,
+        cudaError_t e = cudaFuncSetAttribute(int8_decode_kernel<D, G, DITHER, GEN>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    return launch_dep(int8_decode_kernel<D, G, DITHER>, dim3(a.max_splits, a.Hkv, a.B), dim3(kWarps * 32), C::SMEM,
-                      st, a);
+    return launch_dep(int8_decode_kernel<D, G, DITHER, GEN>, dim3(a.max_splits, a.Hkv, a.B), dim3(kWarps * 32),
+                      C::SMEM, st, a);
+}
+
+template <int D, int G>
+cudaError_t launch_dg(const Int8Args& a, bool dither, bool gen, cudaStream_t st) {
+    if (dither) return gen ? launch_t<D, G, true, true>(a, st) : launch_t<D, G, true, false>(a, st);
+    return gen ? launch_t<D, G, false, true>(a, st) : launch_t<D, G, false, false>(a, st);
 }
 
 }  // namespace
@@ -798,8 +810,9 @@ cudaError_t launch_int8_decode(kvc_handle* h, const void* q, void* out, float* c
     a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)s.d));
     a.inv_sqrt_d_up = std::nextafter((float)(1.0 / std::sqrt((double)s.d)), 1.0f);
     cudaError_t e = cudaErrorInvalidValue;
+    const bool gen = s.W > 0 || s.ring || s.pages > 0;
 #define KVC_CASE(D, G) \
-    if (s.d == D && s.g == G) e = s.dither ? launch_t<D, G, true>(a, st) : launch_t<D, G, false>(a, st);
+    if (s.d == D && s.g == G) e = launch_dg<D, G>(a, s.dither, gen, st);
     KVC_CASE(128, 1) KVC_CASE(128, 2) KVC_CASE(128, 4) KVC_CASE(128, 8)
     KVC_CASE(64, 1) KVC_CASE(64, 2) KVC_CASE(64, 4) KVC_CASE(64, 8)
 #undef KVC_CASE
