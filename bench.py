@@ -51,13 +51,13 @@ CSRC = os.path.join(ROOT, "kv_cache_decode_ring_gb300", "csrc")
 TRAFFIC_PER_BYTE = {
     "full-cache-mha": ("decode_fast.cu", "1c1f7c30fe290db7", (268705792 + 4242432) / 268632064),
     "sliding-window-gqa": ("decode_gqa.cu", "596f2f658be07ec0", (268078080 + 3044096) / 268148736),
-    "int8-witness": ("int8.cu", "6689f77f2208db06", (302858752 + 2735872) / 302551040),
+    "int8-witness": ("int8.cu", "b69593888a94c142", (302879488 + 2675712) / 302551040),
     "bf16-at-int8-shape": ("decode_gqa.cu", "596f2f658be07ec0", (536977152 + 3369984) / 536907776),
     # (the chunk's reads also include the query, 16.8 MB in this 4-request capture, which the
     # K/V basis leaves out)
     "prefix-reuse": ("chunk.cu", "ca7cbdfb723f37c8", (82870528 + 2781184) / 60850176),
     "prefix-reuse-w4096": ("chunk.cu", "ca7cbdfb723f37c8", (76614400 + 2631936) / 60850176),
-    "int8-dither": ("int8.cu", "6689f77f2208db06", (269308160 + 3011840) / 268996608),
+    "int8-dither": ("int8.cu", "b69593888a94c142", (269337344 + 2988800) / 268996608),
     "full-cache-mha-paged": ("decode_fast.cu", "1c1f7c30fe290db7", (268710400 + 4297984) / 268632064),
     "sliding-window-gqa-paged": ("decode_gqa.cu", "596f2f658be07ec0", (268096512 + 3033344) / 268148736),
     "prefix-reuse-store": ("chunk.cu", "ca7cbdfb723f37c8", (82870528 + 2781184) / 60850176),   # the same chunk launch
