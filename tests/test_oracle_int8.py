@@ -175,3 +175,109 @@ def test_int8_trim_rules():
     assert m.length(0) == 35
     m.trim([16])                                              # block boundary
     assert m.length(0) == 16
+
+
+# ---- the window of the INT8 tier (max_t c_t over the window; [LEAN] §2.1 masks) ----------
+def _hand_window(m, q_bits, t, lo, h_q):
+    """Attention of query head h_q of request 0 over positions [lo, t] assembled by hand:
+    complete blocks dequantized with the block quantizer, tail rows exact, plain fp64
+    softmax; c_t from the witnesses and the query's band norms."""
+    g = m.Hq // m.Hkv
+    h = h_q // g
+    nfull = (m.length(0) // QBLOCK) * QBLOCK
+    qf = m.query_rows(np.asarray(q_bits)[0, h_q:h_q + 1], np.full(1, t))[0].astype(np.float64)
+    K, V, C = [], [], []
+    qn = np.sqrt((qf.reshape(NBANDS, -1) ** 2).sum(axis=1))
+    for p in range(lo, t + 1):
+        if p < nfull:
+            b0 = (p // QBLOCK) * QBLOCK
+            Kb = np.stack([m.hk[0][x][h] for x in range(b0, b0 + QBLOCK)])
+            Vb = np.stack([m.hv[0][x][h] for x in range(b0, b0 + QBLOCK)])
+            sK, cK = nm.quantize_block(Kb)
+            sV, cV = nm.quantize_block(Vb)
+            r = p - b0
+            K.append(cK[r].astype(np.float64) * np.float64(sK))
+            V.append(cV[r].astype(np.float64) * np.float64(sV))
+            w = nm.f16_values(nm.witness_row(Kb[r], cK[r], sK, NBANDS)).astype(np.float64)
+            C.append((w * qn).sum() / math.sqrt(m.d))
+        else:
+            K.append(m.hk[0][p][h].astype(np.float64))
+            V.append(m.hv[0][p][h].astype(np.float64))
+            C.append(0.0)
+    K, V = np.stack(K), np.stack(V)
+    s = K @ qf / math.sqrt(m.d)
+    e = np.exp(s - s.max())
+    return (e @ V) / e.sum(), np.array(C)
+
+
+@pytest.mark.parametrize("window,T", [(20, 70), (16, 64), (5, 70), (40, 37)])
+def test_windowed_decode_by_hand(window, T):
+    # the window starts inside a block, on a block boundary, inside the exact tail, and
+    # before position 0 (all rows visible)
+    rng = np.random.default_rng(40 + window)
+    m = _int8_model(rng, T=T, outliers=True, window=window)
+    q = nm.f32_to_bf16(rng.standard_normal((1, 4, 128)).astype(np.float32))
+    res = m.decode_int8(q)
+    t = T - 1
+    lo = max(0, t - window + 1)
+    for (b, hq), r in res.items():
+        out, c = _hand_window(m, q, t, lo, hq)
+        assert np.allclose(r["out"], out, rtol=1e-12, atol=1e-12)
+        assert np.allclose(r["c"], c, rtol=1e-12, atol=0) and r["c"].shape == (t + 1 - lo,)
+        assert r["cmax"] == pytest.approx(c.max(), rel=1e-12)
+        assert np.all(r["eps"] <= r["c"] * (1 + 1e-12)) and r["tv"] <= math.tanh(r["cmax"])
+
+
+def test_window_reductions():
+    rng = np.random.default_rng(50)
+    full = _int8_model(rng, T=70, window=0)
+    rng = np.random.default_rng(50)
+    wide = _int8_model(rng, T=70, window=1000)
+    rng = np.random.default_rng(50)
+    one = _int8_model(rng, T=70, window=1)
+    q = nm.f32_to_bf16(np.random.default_rng(51).standard_normal((1, 4, 128)).astype(np.float32))
+    a, b, c = full.decode_int8(q), wide.decode_int8(q), one.decode_int8(q)
+    for key in a:
+        # a window covering every position is the unwindowed tier
+        assert np.array_equal(a[key]["out"], b[key]["out"]) and a[key]["cmax"] == b[key]["cmax"]
+        # one visible key (position 69, in the exact tail): its value row, exactly; no bound
+        h = key[1] // 2
+        assert np.array_equal(c[key]["out"], one.hv[0][69][h].astype(np.float64))
+        assert c[key]["cmax"] == 0.0 and c[key]["tv"] == 0.0
+
+
+def test_window_max_ignores_tokens_before_the_window():
+    # a token with a large residual just before the window start raises the unwindowed
+    # bound but not the windowed one
+    B, Hq, Hkv, d = 1, 2, 1, 128
+    rng = np.random.default_rng(52)
+    rows = [rng.standard_normal((1, 1, d)).astype(np.float32) for _ in range(48)]
+    rows[10][0, 0, 3] = 3000.0                       # block 0: huge scale, large residuals elsewhere
+    def build(window):
+        m = DecodeOracle(B, Hq, Hkv, d, "contiguous", 64, window, 0.0, "bf16", "int8")
+        for k in rows:
+            m.append(nm.f32_to_bf16(k), nm.f32_to_bf16(k))
+        return m
+    q = nm.f32_to_bf16(np.ones((1, 2, d), np.float32))
+    allw = build(0).decode_int8(q)
+    win = build(30).decode_int8(q)                   # positions 18..47: blocks 1 and 2 only
+    for key in allw:
+        assert win[key]["cmax"] < allw[key]["cmax"] / 10
+
+
+def test_ring_int8_equals_windowed_contiguous():
+    # a ring of W slots attends to the same window as a contiguous cache with window W
+    W, T = 32, 90
+    rng = np.random.default_rng(53)
+    ring = DecodeOracle(1, 4, 2, 128, "ring", W, 0, 10000.0, "bf16", "int8")
+    cont = DecodeOracle(1, 4, 2, 128, "contiguous", 256, W, 10000.0, "bf16", "int8")
+    for t in range(T):
+        k = nm.f32_to_bf16(rng.standard_normal((1, 2, 128)).astype(np.float32))
+        v = nm.f32_to_bf16(rng.standard_normal((1, 2, 128)).astype(np.float32))
+        ring.append(k, v)
+        cont.append(k, v)
+        if t in (3, 31, 32, 47, 89):
+            q = nm.f32_to_bf16(rng.standard_normal((1, 4, 128)).astype(np.float32))
+            a, b = ring.decode_int8(q), cont.decode_int8(q)
+            for key in a:
+                assert np.array_equal(a[key]["out"], b[key]["out"]) and np.array_equal(a[key]["c"], b[key]["c"])
