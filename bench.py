@@ -457,6 +457,50 @@ class Int8Bench(DecodeBench):
                 "l2": "inputs larger than L2: %.2f GB read per step vs 129 MB L2" % (self.units() / 1e9)}
 
 
+class Int8RingBench(Int8Bench):
+    """INT8 + witness on a ring of 32768 slots at the INT8 workload's shape: the 131072-token
+    prefill streams through the ring (blocks overwritten within the call are never stored),
+    then each step appends one token and runs the fused decode over the window."""
+
+    kernel = "kvc_decode_attn INT8 on a ring (fused decode + witness bound + combine)"
+
+    def __init__(self, device, batch=None, total_steps=0):
+        import torch
+        from kv_cache_decode_ring_gb300 import kvc
+        from kv_cache_decode_ring_gb300 import workloads as wl
+        self.w = w = wl.int8_witness_ring()
+        if batch:
+            w.batch = batch                   # smaller case for profiler captures
+        self.ctx = w.extra["context"]
+        self.W = w.capacity
+        self.cache = kvc.Cache.from_workload(w, device=device, max_position=self.ctx + total_steps + 64)
+        chunk = 8192
+        for c in range(self.ctx // chunk):
+            k, v = w.prefill_chunk(c, chunk, device=device)
+            self.cache.append_rows(k, v)
+            del k, v
+        B, Hq = w.batch, w.n_q_heads
+        self.cmax = torch.empty((B, Hq), device=device)
+        self.tanh = torch.empty((B, Hq), device=device)
+        self._inputs(device)
+
+    def units(self):
+        """Bytes the fused decode reads: the ring's complete blocks (codes, witnesses, scales) and
+        the exact tail rows."""
+        w = self.w
+        n = self.ctx + self.done + 1
+        nblk = min(n // 16, self.W // 16)
+        per_head = nblk * 16 * (2 * w.head_dim + 32) + nblk * 8 + (n - n // 16 * 16) * 4 * w.head_dim
+        return w.batch * w.n_kv_heads * per_head
+
+    def config(self):
+        c = super().config()
+        c["workload"] = self.w.name
+        c["layout"] = "ring of %d slots, int8 + witnesses" % self.W
+        c["context"] = "131072 + step positions, window %d" % self.W
+        return c
+
+
 class Int8CtBench(Int8Bench):
     """The INT8 workload with the decode also writing every cached token's c_t (fp32
     [B][Hq][capacity]), the input of the gated fallback's block risk: the same reads plus
@@ -821,7 +865,7 @@ class ChunkStoreBench(ChunkBench):
 
 BENCHES = {"full-cache-mha": FullCacheBench, "sliding-window-gqa": SlidingWindowBench, "int8-witness": Int8Bench,
            "bf16-at-int8-shape": Bf16AtInt8ShapeBench, "int8-witness-gated": Int8GatedBench,
-           "int8-dither": Int8DitherBench, "int8-witness-ct": Int8CtBench,
+           "int8-dither": Int8DitherBench, "int8-witness-ct": Int8CtBench, "int8-witness-ring": Int8RingBench,
            "full-cache-mha-paged": FullCachePagedBench, "sliding-window-gqa-paged": SlidingWindowPagedBench,
            "prefix-reuse": ChunkBench, "prefix-reuse-w4096": ChunkWindowBench, "prefix-reuse-store": ChunkStoreBench}
 

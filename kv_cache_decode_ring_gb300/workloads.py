@@ -175,6 +175,15 @@ def int8_witness() -> Workload:
                     "bf16", "int8", 7, extra={"context": 131072, "steps": 16, "outliers": (4, 20.0)})
 
 
+def int8_witness_ring() -> Workload:
+    """The INT8 + witness workload on a sliding-window ring of W = 32768 slots: the same
+    tokens (context 131072, 4 outlier channels per head x 20, RoPE 10000, seed 7), of which
+    the ring keeps the newest 2048 complete blocks and the exact tail."""
+    w = int8_witness()
+    w.name, w.layout, w.capacity, w.window = "int8-witness-ring-bf16", "ring", 32768, 32768
+    return w
+
+
 def int8_dither() -> Workload:
     """Tier B at the INT8 workload's shape: the same tokens, subtractive-dither INT8 codes
     without witnesses; Philox key (0x243F6A88, 0x85A308D3), layer 0."""

@@ -232,6 +232,73 @@ def test_int8_witness_sampled():
     assert cache.device_status() == 0
 
 
+def test_int8_witness_ring_sampled():
+    # INT8 + witness on a ring of 32768 slots at the INT8 workload's shape (the bench's
+    # int8-witness-ring line): 131072 positions streamed through the ring, then 16 steps;
+    # sampled heads against the oracle over the window, and a sample of ring block slots
+    # bit-exact (block n in slot n mod 2048)
+    import math
+    from oracle.model import QBLOCK, int8_decode_one
+    w = wl.int8_witness_ring()
+    ctx, W = w.extra["context"], w.capacity
+    cache = kvc.Cache.from_workload(w, max_position=ctx + 64)
+    model = oracle_for(w)
+    g = w.n_q_heads // w.n_kv_heads
+    sample = [(0, 0), (6, 5)]
+    keep = {bh: ([], []) for bh in sample}          # rows from position ctx - W - 16 on
+    chunk, first = 8192, ctx - W - 16
+    for c in range(ctx // chunk):
+        k, v = w.prefill_chunk(c, chunk, device="cuda")
+        cache.append_rows(k, v)
+        a_ = max(0, first - c * chunk)
+        if a_ < chunk:
+            for (b, h) in sample:
+                keep[(b, h)][0].append(host(k[b, h, a_:])); keep[(b, h)][1].append(host(v[b, h, a_:]))
+        del k, v
+    cmax = torch.empty((w.batch, w.n_q_heads), device="cuda")
+    th = torch.empty((w.batch, w.n_q_heads), device="cuda")
+    for s in range(16):
+        q, k1, v1 = w.step_qkv(s, device="cuda")
+        cache.append(k1, v1)
+        out = cache.decode(q, None, cmax, th)
+        for (b, h) in sample:
+            keep[(b, h)][0].append(host(k1[b, h])[None]); keep[(b, h)][1].append(host(v1[b, h])[None])
+        if s not in (0, 15):
+            continue
+        t = ctx + s
+        nfull = (t + 1) // QBLOCK * QBLOCK
+        lo = t - W + 1
+        p0 = lo // QBLOCK * QBLOCK
+        o, cm, tc = out.cpu(), cmax.cpu().numpy(), th.cpu().numpy()
+        for (b, h) in sample:
+            Kin = np.concatenate(keep[(b, h)][0]); Vin = np.concatenate(keep[(b, h)][1])
+            Kin, Vin = Kin[p0 - first:], Vin[p0 - first:]
+            K = model.stored_rows(Kin, np.arange(p0, t + 1))
+            V = nm.bf16_to_f32(Vin)
+            for hq in (h * g, h * g + g - 1):
+                qr = model.query_rows(host(q[b, hq])[None], [t])[0]
+                r = int8_decode_one(qr, K, V, p0, t, W, nfull)
+                assert_close(o[b, hq][None], r["out"][None], "bf16", "int8 ring s=%d b=%d h=%d" % (s, b, hq))
+                assert cm[b, hq] >= r["cmax"] * (1 - 1e-12) and cm[b, hq] <= r["cmax"] * (1 + 1e-5)
+                assert tc[b, hq] >= math.tanh(cm[b, hq]) * (1 - 1e-7) and r["tv"] <= tc[b, hq]
+    from oracle import numerics as onm
+    KQ = cache.export(kvc.KVC_EXPORT_KQ); SK = cache.export(kvc.KVC_EXPORT_SK)
+    WT = cache.export(kvc.KVC_EXPORT_WITNESS)
+    nfb = (ctx + 16) // QBLOCK
+    for (b, h) in sample:
+        Kin = np.concatenate(keep[(b, h)][0])
+        for blk in (nfb - W // QBLOCK, nfb - 1000, nfb - 1):
+            pos = np.arange(blk * QBLOCK, (blk + 1) * QBLOCK)
+            Kb = model.stored_rows(Kin[pos - first], pos)
+            sK, cK = onm.quantize_block(Kb)
+            slot = blk % (W // QBLOCK)
+            sl = slice(slot * QBLOCK, (slot + 1) * QBLOCK)
+            assert SK[b, h, slot] == sK and np.array_equal(KQ[b, h, sl], cK), (b, h, blk)
+            wit = np.stack([onm.witness_row(Kb[i], cK[i], sK) for i in range(QBLOCK)])
+            assert np.array_equal(WT[b, h, sl], wit), (b, h, blk)
+    assert cache.device_status() == 0
+
+
 def test_int8_gated_sampled():
     # The INT8 workload after one gated fallback, as the gated bench line runs it: a decode
     # with per-token c_t, the block risk, the gate at tau = 0.2 with a budget of 1 % of the
