@@ -217,6 +217,13 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// max(a, b, c) in one instruction
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 // two fp32 values rounded to fp16 (nearest even), a in the low half
 __device__ __forceinline__ uint32_t pack_f16(float a, float b) {
     __half2 t = __floats2half2_rn(a, b);
@@ -439,16 +446,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         s[c] = vis ? s[c] : -INFINITY;
                     }
                 }
-                // row maximum as a tree (eight independent chains, then three steps)
+                // row maximum: eight independent chains of three-input maxima, then a tree
                 float m8[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) m8[e] = s[e];
+                for (int e = 0; e < 8; ++e) m8[e] = fmaxf(s[e], s[8 + e]);
 #pragma unroll
-                for (int c = 8; c < kBN; c += 8)
+                for (int c = 16; c < kBN; c += 16)
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) m8[e] = fmaxf(m8[e], s[c + e]);
-                const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                                       fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+                    for (int e = 0; e < 8; ++e) m8[e] = fmax3(m8[e], s[c + e], s[c + 8 + e]);
+                const float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
                 // the reference maximum moves only when the tile exceeds it by more than kLazyMax;
                 // then O (complete up to P.V of tile j - 1: S of this tile waited for it) is rescaled
                 bool grow = false;
@@ -475,9 +481,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t pk[kBN / 2];
                 float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                                 make_float2(0.f, 0.f)};
+                const float2 nb2 = make_float2(-base, -base);
 #pragma unroll
                 for (int e = 0; e < kBN / 2; ++e) {
-                    const float p0 = ex2(s[2 * e] - base), p1 = ex2(s[2 * e + 1] - base);   // masked keys: 0
+                    const float2 x = __fadd2_rn(make_float2(s[2 * e], s[2 * e + 1]), nb2);    // s - base, packed
+                    const float p0 = ex2(x.x), p1 = ex2(x.y);                                  // masked keys: 0
                     rs[e & 3] = __fadd2_rn(rs[e & 3], make_float2(p0, p1));
                     pk[e] = pack_f16(p0, p1);
                 }
