@@ -124,6 +124,12 @@ typedef struct {
                              (byte i = bits 8(i mod 4) .. of word i/4); values keep the
                              plain block quantizer.  The request ID is b unless set by
                              kvc_set_request_id. */
+    int32_t int8_split;   /* INT8 tiers: positions per quantized split of the decode (a
+                             CTA's share of one request and KV head), a multiple of 64
+                             in [1024, 2048]; 0 = 2048 when the cache (or a contiguous
+                             cache's window + 32) spans 16384 slots or more, else 1024.
+                             A tuning knob only: results do not depend on it beyond
+                             fp32 rounding order.  Must be 0 without INT8. */
 } kvc_config;
 
 /* Bytes of the device state buffer for `cfg` (cache rows, positions,

@@ -15,13 +15,14 @@
 // rows of the incomplete block.
 //
 // Kernel shape: CTA = 4 warps = a split of 1024 tokens (64 blocks; 2048 for caches
-// of 16384 slots or more); each warp streams its 16 (32) blocks through two or
-// three shared-memory stages (codes and witnesses by bulk copy on the stage's
-// mbarrier; two where four CTAs fit on an SM), so copies overlap arithmetic; online
-// softmax over the warp's blocks, warps merged at the end.  One extra split
-// handles the exact tail rows of the incomplete block (c_t = 0 there).  Blocks
-// restored to full precision by the gated fallback are skipped here and served
-// by the exact-block decode (int8_exact.cu), whose splits follow.
+// of 16384 slots or more; any multiple of 64 in between if configured); each warp
+// streams its 16 to 32 blocks through two or three shared-memory stages (codes and
+// witnesses by bulk copy on the stage's mbarrier; two where four CTAs fit on an SM),
+// so copies overlap arithmetic; online softmax over the warp's blocks, warps merged
+// at the end.  One extra split handles the exact tail rows of the incomplete block
+// (c_t = 0 there).  Blocks restored to full precision by the gated fallback are
+// skipped here and served by the exact-block decode (int8_exact.cu), whose splits
+// follow.
 //
 // Both contractions of a block run on the tensor cores as fp16 MMAs with fp32
 // accumulation (m16n8k16), operands built in registers:
@@ -52,7 +53,7 @@ namespace kvc {
 namespace {
 
 constexpr int kWarps = 4;
-// one 16-token block per tile; a warp takes split / (kWarps * 16) tiles (16 or 32)
+// one 16-token block per tile; a warp takes split / (kWarps * 16) tiles (16 to 32)
 constexpr float kLazyMax = 8.f;            // log2-domain headroom of the reference maximum
 static_assert(kInt8Split % (kWarps * kQBlock) == 0 && kInt8SplitLong % (kWarps * kQBlock) == 0, "split shape");
 static_assert(kInt8SplitLong / (kWarps * kQBlock) <= 32, "one tile's scales per lane");
@@ -83,6 +84,7 @@ struct Int8Args {
     int B, Hq, Hkv, d, S, max_splits;
     int W, ring;        // attention window (0 = all; a ring's is its size) and layout
     int split;          // tokens per quantized split
+    int grid;           // grid columns: quantized splits + the exact-tail split
     float scale_log2;   // log2(e)/sqrt(d)
     float inv_sqrt_d_up;
 };
@@ -763,7 +765,7 @@ cudaError_t launch_t(const Int8Args& a, cudaStream_t st) {
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    return launch_dep(int8_decode_kernel<D, G, DITHER, GEN>, dim3(a.max_splits, a.Hkv, a.B), dim3(kWarps * 32),
+    return launch_dep(int8_decode_kernel<D, G, DITHER, GEN>, dim3(a.grid, a.Hkv, a.B), dim3(kWarps * 32),
                       C::SMEM, st, a);
 }
 
@@ -807,6 +809,7 @@ cudaError_t launch_int8_decode(kvc_handle* h, const void* q, void* out, float* c
     a.B = s.B; a.Hq = s.Hq; a.Hkv = s.Hkv; a.d = s.d; a.S = s.S; a.max_splits = s.max_splits;
     a.W = s.W; a.ring = s.ring;
     a.split = s.split;
+    a.grid = int8_grid(s);
     a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)s.d));
     a.inv_sqrt_d_up = std::nextafter((float)(1.0 / std::sqrt((double)s.d)), 1.0f);
     cudaError_t e = cudaErrorInvalidValue;

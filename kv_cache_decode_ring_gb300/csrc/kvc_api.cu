@@ -57,6 +57,9 @@ bool make_shape(const kvc_config& c, Shape* s) {
         return false;
     if (c.page_pool < 0 || (c.page_pool > 0 && c.capacity % kPage)) return false;
     if (c.page_pool > 0 && c.int8_exact_blocks != 0) return false;   // the gate's pool: unpaged caches
+    if (c.int8_split != 0 && (!int8 || c.int8_split % 64 != 0 || c.int8_split < kInt8Split ||
+                              c.int8_split > kInt8SplitLong))
+        return false;
     if (c.store_slots < 0 || (c.store_slots > 0 && int8)) return false;
     if (int8) {
         const int g = c.n_q_heads / c.n_kv_heads;
@@ -88,12 +91,11 @@ bool make_shape(const kvc_config& c, Shape* s) {
     // a paged cache may start its splits up to one page before the window
     s->max_splits = (int)((keys + s->split - 1) / s->split) + (s->pages > 0 ? 1 : 0);
     if (int8) {
-        // quantized splits (longer ones for long caches: less start-up per byte), one
-        // split for the exact tail rows and, with a pool, the splits of the exact-block decode.
-        // A window of W positions on a contiguous cache touches at most W/16 + 2 blocks.
-        const long long qkeys = (!ring && s->W > 0 && (long long)s->W + 2 * kQBlock < s->S)
-                                    ? (long long)s->W + 2 * kQBlock : s->S;
-        s->split = qkeys >= kInt8LongKeys ? kInt8SplitLong : kInt8Split;
+        // quantized splits (longer ones for long caches: less start-up per byte; a longer
+        // split measured faster than one that fills the SMs' last wave of CTAs better), one
+        // split for the exact tail rows and, with a pool, the splits of the exact-block decode
+        const long long qkeys = int8_qkeys(*s);
+        s->split = c.int8_split ? c.int8_split : qkeys >= kInt8LongKeys ? kInt8SplitLong : kInt8Split;
         s->max_splits = (int)((qkeys + s->split - 1) / s->split) + 1 + (s->xpool > 0 ? kExactSplits : 0);
     }
     return true;

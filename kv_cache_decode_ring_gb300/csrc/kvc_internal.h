@@ -79,6 +79,17 @@ struct Shape {
     int store_slots;             // saved-prefill slots (0 = none)
 };
 
+// INT8 decode: the slots its quantized splits cover.  A window of W positions on a
+// contiguous cache touches at most W/16 + 2 blocks; a ring or an unwindowed cache, all S.
+inline long long int8_qkeys(const Shape& s) {
+    return (!s.ring && s.W > 0 && (long long)s.W + 2 * kQBlock < s.S) ? (long long)s.W + 2 * kQBlock : s.S;
+}
+// ... and the columns of its grid: the quantized splits of `split` tokens, then the exact-tail split
+inline int int8_grid(const Shape& s) {
+    const long long bps = s.split / kQBlock;
+    return (int)(((int8_qkeys(s) + kQBlock - 1) / kQBlock + bps - 1) / bps) + 1;
+}
+
 bool make_shape(const kvc_config& c, Shape* s);
 // Rows per (request, KV head) of a ring's chunk staging: positions from the cut rounded
 // down to 16 up to the last suffix row rounded up to 16.

@@ -44,7 +44,8 @@ class kvc_config(ctypes.Structure):
                 ("max_position", ctypes.c_int32), ("rope_base", ctypes.c_float), ("max_chunk", ctypes.c_int32),
                 ("out_dtype", ctypes.c_int32), ("int8_exact_blocks", ctypes.c_int32), ("page_pool", ctypes.c_int32),
                 ("store_slots", ctypes.c_int32), ("layer_index", ctypes.c_int32),
-                ("dither_key_lo", ctypes.c_uint32), ("dither_key_hi", ctypes.c_uint32)]
+                ("dither_key_lo", ctypes.c_uint32), ("dither_key_hi", ctypes.c_uint32),
+                ("int8_split", ctypes.c_int32)]
 
 
 EXPORTED = ["kvc_state_bytes", "kvc_create", "kvc_destroy", "kvc_append", "kvc_append_rows",
@@ -146,20 +147,22 @@ def kvc_strerror(code: int) -> str:
 def make_config(dtype="bf16", layout="contiguous", kv_quant=None, batch=1, n_q_heads=1, n_kv_heads=1,
                 head_dim=128, capacity=1, window=0, max_position=0, rope_base=0.0, max_chunk=0,
                 out_dtype=None, int8_exact_blocks=0, page_pool=0, store_slots=0, layer_index=0,
-                dither_key=(0, 0)) -> kvc_config:
+                dither_key=(0, 0), int8_split=0) -> kvc_config:
     """``out_dtype``: None (the cache dtype), "f32" or "bf16"; ``int8_exact_blocks``: pool
     entries for blocks the gated fallback restores (INT8 caches); ``page_pool``: pages of 16
     slots for paged K/V storage (0 = each request owns ``capacity`` slots); ``store_slots``:
     device slots for saved prefills (prefix store).  ``kv_quant``: None, "int8" (witness
     tier) or "int8-dither" (Tier B, with ``layer_index`` and the 64-bit Philox ``dither_key``
-    as (low, high) words)."""
+    as (low, high) words); ``int8_split``: positions per quantized split of the INT8 decode
+    (a multiple of 64 in [1024, 2048]; 0 = chosen for the device)."""
     od = 0 if out_dtype is None else (KVC_F32 + 1 if out_dtype == "f32" else KVC_BF16 + 1)
     return kvc_config(KVC_BF16 if dtype == "bf16" else KVC_F32,
                       KVC_RING if layout == "ring" else KVC_CONTIGUOUS,
                       {None: KVC_QUANT_NONE, "int8": KVC_QUANT_INT8, "int8-dither": KVC_QUANT_INT8_DITHER}[kv_quant],
                       batch, n_q_heads, n_kv_heads, head_dim, capacity, window, max_position,
                       float(rope_base), max_chunk, od, int(int8_exact_blocks), int(page_pool), int(store_slots),
-                      int(layer_index), int(dither_key[0]) & 0xFFFFFFFF, int(dither_key[1]) & 0xFFFFFFFF)
+                      int(layer_index), int(dither_key[0]) & 0xFFFFFFFF, int(dither_key[1]) & 0xFFFFFFFF,
+                      int(int8_split))
 
 
 def kvc_state_bytes(cfg: kvc_config) -> int:
@@ -403,11 +406,11 @@ class Cache:
 
     @classmethod
     def from_workload(cls, w, max_chunk=0, max_position=0, device="cuda", out_dtype=None, int8_exact_blocks=0,
-                      page_pool=0, store_slots=0):
+                      page_pool=0, store_slots=0, int8_split=0):
         cfg = make_config(w.dtype, w.layout, w.quant, w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.capacity,
                           0 if w.layout == "ring" else w.window, max_position, w.rope_base, max_chunk, out_dtype,
                           int8_exact_blocks, page_pool, store_slots, w.extra.get("layer", 0),
-                          w.extra.get("dither_key", (0, 0)))
+                          w.extra.get("dither_key", (0, 0)), int8_split)
         return cls(cfg, device)
 
     def close(self):

@@ -126,11 +126,11 @@ def test_int8_multi_split_parity(d, Hq, Hkv):
 
 
 def test_int8_long_split_parity():
-    # caches of 16384 slots or more take 2048-token splits: lengths around one and
-    # several of them, and a request of a single block
+    # 2048-token splits: lengths around one and several of them, and a request of a
+    # single block
     w = wl.small("int8-long-split", B=3, Hq=8, Hkv=2, d=128, capacity=16400, rope_base=10000.0,
                  quant="int8", seed=37, outliers=(4, 20.0))
-    cache = kvc.Cache.from_workload(w, out_dtype="f32")
+    cache = kvc.Cache.from_workload(w, out_dtype="f32", int8_split=2048)
     model = _oracle(w)
     lengths = [2047, 6150, 16]
     k, v = w.prefill_chunk(0, max(lengths))
@@ -142,6 +142,33 @@ def test_int8_long_split_parity():
         cache.append(k1.cuda(), v1.cuda())
         model.append(host(k1), host(v1))
         check_decode(cache, model, q)
+    assert cache.device_status() == 0
+
+
+@pytest.mark.parametrize("layout", ["contiguous", "window", "ring"])
+@pytest.mark.parametrize("split", [1088, 1600, 1984])
+def test_int8_split_lengths(split, layout):
+    # the decode's split length is a multiple of 64 positions between 1024 and 2048 (chosen
+    # per device unless configured): odd numbers of tiles per warp, requests ending inside,
+    # at and just past a split, a window starting inside a split, a ring past its wrap
+    ring = layout == "ring"
+    cap = 4096 if ring else 6160
+    w = wl.small("int8-split-%d-%s" % (split, layout), B=4, Hq=8, Hkv=2, d=128, layout="ring" if ring else "contiguous",
+                 capacity=cap, window=cap if ring else (2500 if layout == "window" else 0), rope_base=10000.0,
+                 quant="int8", seed=41, outliers=(4, 20.0))
+    cache = kvc.Cache.from_workload(w, max_position=8192 if ring else 0, out_dtype="f32", int8_split=split)
+    model = _oracle_layout(w)
+    lengths = [split - 1, 2 * split + 17, 16, cap + split + 33] if ring else [split - 1, 2 * split + 17, 16, 3 * split]
+    k, v = w.prefill_chunk(0, max(lengths))
+    cache.append_rows(k.cuda(), v.cuda(), counts=lengths)
+    model.append_rows(host(k), host(v), lengths)
+    for s in range(2):
+        q, k1, v1 = w.step_qkv(s)
+        cache.append(k1.cuda(), v1.cuda())
+        model.append(host(k1), host(v1))
+        check_decode_window(cache, model, q, ring=ring)
+    if ring:
+        check_int8_ring_state(cache, model)
     assert cache.device_status() == 0
 
 
