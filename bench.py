@@ -51,19 +51,19 @@ CSRC = os.path.join(ROOT, "kv_cache_decode_ring_gb300", "csrc")
 TRAFFIC_PER_BYTE = {
     "full-cache-mha": ("decode_fast.cu", "1c1f7c30fe290db7", (268705792 + 4242432) / 268632064),
     "sliding-window-gqa": ("decode_gqa.cu", "596f2f658be07ec0", (268078080 + 3044096) / 268148736),
-    "int8-witness": ("int8.cu", "b69593888a94c142", (302879488 + 2675712) / 302551040),
+    "int8-witness": ("int8.cu", "6fae76895f96ec4f", (302859264 + 3017984) / 302551040),
     "bf16-at-int8-shape": ("decode_gqa.cu", "596f2f658be07ec0", (536977152 + 3369984) / 536907776),
     # (the chunk's reads also include the query, 16.8 MB in this 4-request capture, which the
     # K/V basis leaves out)
     "prefix-reuse": ("chunk.cu", "a83a030e240a769c", (80662528 + 2573568) / 60850176),
     "prefix-reuse-w4096": ("chunk.cu", "a83a030e240a769c", (74514432 + 2152448) / 60850176),
-    "int8-dither": ("int8.cu", "b69593888a94c142", (269337344 + 2988800) / 268996608),
+    "int8-dither": ("int8.cu", "6fae76895f96ec4f", (269305088 + 3097088) / 268996608),
     "full-cache-mha-paged": ("decode_fast.cu", "1c1f7c30fe290db7", (268710400 + 4297984) / 268632064),
     "sliding-window-gqa-paged": ("decode_gqa.cu", "596f2f658be07ec0", (268096512 + 3033344) / 268148736),
     "prefix-reuse-store": ("chunk.cu", "a83a030e240a769c", (80662528 + 2573568) / 60850176),   # the same chunk launch
     # the store's batched row copy (8 requests' cuts, 297.9 MB read + written): writes still in L2
     # at the end of the launch are not counted, so the ratio is below 1
-    "store-load": ("store.cu", "a9b53245c164e7d1", (149262592 + 101474048) / 297918464),
+    "store-load": ("store.cu", "87899089531c77de", (149272064 + 95416064) / 297918464),
 }
 
 

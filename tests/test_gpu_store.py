@@ -269,3 +269,30 @@ def test_store_load_batch(paged):
         assert_close(cache.decode(q.cuda()), model.decode(host(q)), w.dtype, "decode after batched load")
     check_state(cache, model, w)
     assert cache.device_status() == 0
+
+
+@pytest.mark.parametrize("dtype,d", [("bf16", 6), ("bf16", 96), ("f32", 256)], ids=["12B-rows", "192B-rows", "1KB-rows"])
+def test_store_row_widths(dtype, d):
+    """Rows that are not 16-byte multiples (copied by words), and rows of 192 and 1024 bytes
+    (copied through shared memory in runs): a save and loads whose cuts end inside, at and
+    past a 64-row run."""
+    w = wl.small("store-rows-%s-%d" % (dtype, d), B=3, Hq=4, Hkv=2, d=d, capacity=320, rope_base=10000.0,
+                 dtype=dtype, seed=43)
+    cache = kvc.Cache.from_workload(w, store_slots=1)
+    model = oracle_for(w)
+    k, v = w.prefill_chunk(0, 300)
+    cache.append_rows(k.cuda(), v.cuda(), counts=[300, 3, 70])
+    model.append_rows(host(k), host(v), [300, 3, 70])
+    cache.store_save(0, 0, 300)
+    snap = model.snapshot(0)
+    cache.store_load_batch([0, 0], [1, 2], [137, 64])
+    model.load(1, snap, 137)
+    model.load(2, snap, 64)
+    check_state(cache, model, w)
+    for s in range(3):
+        q, k1, v1 = w.step_qkv(s)
+        cache.append(k1.cuda(), v1.cuda())
+        model.append(host(k1), host(v1))
+        assert_close(cache.decode(q.cuda()), model.decode(host(q)), w.dtype, "decode after load")
+    check_state(cache, model, w)
+    assert cache.device_status() == 0
