@@ -326,7 +326,7 @@ def test_int8_restore_errors():
 def _oracle_layout(w):
     return DecodeOracle(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.layout, w.capacity,
                         0 if w.layout == "ring" else w.window, w.rope_base, "bf16", w.quant,
-                        dither_key=w.extra.get("dither_key", (0, 0)))
+                        dither_key=w.extra.get("dither_key", (0, 0)), layer=w.extra.get("layer", 0))
 
 
 def check_int8_ring_state(cache, model):
