@@ -919,7 +919,8 @@ def replica_aggregate(ms_local, units_local, dist=None, device="cpu"):
 
 # Lines that the default run times after the headline one, each in the same way (warm-up,
 # K timed steps with CUDA events around the dominant call, clocks sampled meanwhile).
-EXTRA_LINES = ("int8-witness", "sliding-window-gqa", "prefix-reuse", "prefix-reuse-w4096", "int8-dither")
+EXTRA_LINES = ("int8-witness", "sliding-window-gqa", "prefix-reuse", "prefix-reuse-w4096", "int8-dither",
+               "prefix-reuse-store", "int8-witness-ring")
 
 
 def time_steps(bench, K, warmup, local_rank, dist):
@@ -1123,6 +1124,8 @@ def main(argv=None):
         for name in EXTRA_LINES:
             lb = BENCHES[name]("cuda", 0, args.warmup + K)
             lines[name] = line_summary(lb, name, time_steps(lb, K, args.warmup, local_rank, dist), K)
+            if hasattr(lb, "extra_report"):
+                lines[name].update(lb.extra_report(hbm_peak()[0]))
             lb = None
             torch.cuda.empty_cache()
 

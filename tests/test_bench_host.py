@@ -93,5 +93,6 @@ def test_gpus_flag_must_agree_with_the_launcher():
 
 def test_default_run_times_every_targeted_line():
     # the INT8 decode, the sliding-window GQA decode and the chunk kernel each get a line
-    for name in ("int8-witness", "sliding-window-gqa", "prefix-reuse", "prefix-reuse-w4096", "int8-dither"):
+    for name in ("int8-witness", "sliding-window-gqa", "prefix-reuse", "prefix-reuse-w4096", "int8-dither",
+                 "prefix-reuse-store", "int8-witness-ring"):
         assert name in bench.EXTRA_LINES and name in bench.BENCHES
