@@ -58,6 +58,8 @@ TRAFFIC_PER_BYTE = {
     "prefix-reuse": ("chunk.cu", "a83a030e240a769c", (80662528 + 2573568) / 60850176),
     "prefix-reuse-w4096": ("chunk.cu", "a83a030e240a769c", (74514432 + 2152448) / 60850176),
     "int8-dither": ("int8.cu", "6fae76895f96ec4f", (269305088 + 3097088) / 268996608),
+    # (2 requests: 16 x (2048 blocks of codes, witnesses and scales + 3 tail rows) = 151.28 MB)
+    "int8-witness-ring": ("int8.cu", "6fae76895f96ec4f", (151492864 + 3013888) / 151281664),
     "full-cache-mha-paged": ("decode_fast.cu", "1c1f7c30fe290db7", (268710400 + 4297984) / 268632064),
     "sliding-window-gqa-paged": ("decode_gqa.cu", "596f2f658be07ec0", (268096512 + 3033344) / 268148736),
     "prefix-reuse-store": ("chunk.cu", "a83a030e240a769c", (80662528 + 2573568) / 60850176),   # the same chunk launch
