@@ -225,16 +225,19 @@ def _backing_store(w, k, v, lengths, extra):
     return kf, vf
 
 
-def test_int8_gated_fallback():
+@pytest.mark.parametrize("cap,lengths,split,pool,cuts", [
+    (512, [300, 263], 0, 96, [160, 64]),
+    (2624, [2500, 1100], 1088, 512, [1600, 64]),     # several quantized splits before the exact-block ones
+], ids=["one-split", "split-1088"])
+def test_int8_gated_fallback(cap, lengths, split, pool, cuts):
     # [WITCERT] "SGLang 生产级落地与闭环门控修复": risk from the decode's c_t, gate at tau,
     # restore the chosen blocks from the backing store; their tokens become exact (c_t = 0)
     # and every head's tanh(max c_t) drops to tau or below
     tau = 0.2
-    w = wl.small("int8-gate", B=2, Hq=8, Hkv=2, d=128, capacity=512, rope_base=10000.0, quant="int8",
+    w = wl.small("int8-gate", B=2, Hq=8, Hkv=2, d=128, capacity=cap, rope_base=10000.0, quant="int8",
                  seed=13, outliers=(4, 20.0))
-    cache = kvc.Cache.from_workload(w, out_dtype="f32", int8_exact_blocks=96)
+    cache = kvc.Cache.from_workload(w, out_dtype="f32", int8_exact_blocks=pool, int8_split=split)
     model = _oracle(w)
-    lengths = [300, 263]
     k, v = w.prefill_chunk(0, max(lengths))
     cache.append_rows(k.cuda(), v.cuda(), counts=lengths)
     model.append_rows(host(k), host(v), lengths)
@@ -259,7 +262,7 @@ def test_int8_gated_fallback():
                 want = ctn[b, h * g:(h + 1) * g, blk * 16:blk * 16 + 16].max() if (blk + 1) * 16 <= nfull else 0.0
                 assert risk[b, h, blk] == want, (b, h, blk)
     sel = kvc.kvc_int8_gate(risk, tau, 1000)
-    assert 0 < len(sel) <= 96
+    assert 0 < len(sel) <= pool
     top = kvc.kvc_int8_gate(risk, tau, 5)                           # a budget keeps the riskiest
     assert np.array_equal(top, sel[:5])
     kf, vf = _backing_store(w, k, v, lengths, [(k1, v1)])
@@ -287,7 +290,6 @@ def test_int8_gated_fallback():
         cache.append(k1.cuda(), v1.cuda())
         model.append(host(k1), host(v1))
         check_decode(cache, model, q)
-    cuts = [160, 64]
     cache.trim(cuts)
     model.trim(cuts)
     xm = cache.export(kvc.KVC_EXPORT_XMAP)
