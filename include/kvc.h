@@ -81,7 +81,10 @@ typedef struct {
                              one, which covers its window [LEAN] §3.4) */
     int32_t batch;        /* B >= 1 requests */
     int32_t n_q_heads;    /* Hq >= 1 */
-    int32_t n_kv_heads;   /* Hkv >= 1, Hq % Hkv == 0; query head h reads KV head h / (Hq/Hkv) */
+    int32_t n_kv_heads;   /* Hkv >= 1, Hq % Hkv == 0; query head h reads KV head h / (Hq/Hkv).
+                             Shapes served by the generic decode (fp32 caches; bf16 with d
+                             other than 64/128 or more than 8 query heads per KV head)
+                             need g (d + 64) 4 <= 232448 bytes of shared memory, g = Hq/Hkv */
     int32_t head_dim;     /* d: even, 2..256; INT8 needs d % 16 == 0 */
     int32_t capacity;     /* slots per (request, KV head); INT8 needs capacity % 16 == 0 */
     int32_t window;       /* attention window W: 0 = full history (contiguous only);

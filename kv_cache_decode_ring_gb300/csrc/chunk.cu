@@ -835,12 +835,7 @@ cudaError_t launch_chunk(kvc_handle* h, const void* q, const void* k, const void
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(chunk_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    if (cudaError_t e = allow_smem(reinterpret_cast<const void*>(chunk_attn_kernel), SMEM_BYTES)) return e;
     // ChunkArgs carries the order table: it lives in static storage, not on the stack
     static thread_local ChunkArgs a;
     a = ChunkArgs{};

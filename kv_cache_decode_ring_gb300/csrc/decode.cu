@@ -182,6 +182,11 @@ cudaError_t launch_decode(const DecodeArgs& a, const CombineArgs& c, bool fast, 
     } else {
         dim3 grid(a.max_splits, a.Hkv, a.B);
         const size_t smem = (size_t)a.g * (a.d + a.split) * sizeof(float);
+        // (the grant is always the largest, so shapes of different sizes never narrow it)
+        const void* k = a.bf16 ? reinterpret_cast<const void*>(decode_generic_kernel<1>)
+                               : reinterpret_cast<const void*>(decode_generic_kernel<0>);
+        if (smem > 48 * 1024)
+            if (cudaError_t e = allow_smem(k, kMaxSmemPerBlock)) return e;
         if (a.bf16) decode_generic_kernel<1><<<grid, kThreads, smem, st>>>(a);
         else decode_generic_kernel<0><<<grid, kThreads, smem, st>>>(a);
         cudaError_t e = cudaGetLastError();

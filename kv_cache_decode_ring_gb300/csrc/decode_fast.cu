@@ -315,13 +315,7 @@ __global__ void __launch_bounds__(kWarps * 32, 3) decode_fast_kernel(const Decod
 template <int D, int G>
 cudaError_t launch_t(const DecodeArgs& a, int grid_x, cudaStream_t st) {
     using C = Cfg<D, G>;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(decode_fast_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)C::SMEM);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    if (cudaError_t e = allow_smem(reinterpret_cast<const void*>(decode_fast_kernel<D, G>), C::SMEM)) return e;
     dim3 grid(grid_x, a.Hkv, a.B);
     return launch_dep(decode_fast_kernel<D, G>, grid, dim3(kWarps * 32), C::SMEM, st, a);
 }

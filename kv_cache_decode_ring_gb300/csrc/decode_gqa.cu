@@ -340,13 +340,7 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
 template <int D, int G>
 cudaError_t launch_t(const DecodeArgs& a, const KvMaps& m, cudaStream_t st) {
     using C = GqaCfg<D, G>;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(decode_gqa_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)C::SMEM);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    if (cudaError_t e = allow_smem(reinterpret_cast<const void*>(decode_gqa_kernel<D, G>), C::SMEM)) return e;
     return launch_dep(decode_gqa_kernel<D, G>, dim3(a.max_splits, a.Hkv, a.B), dim3(kWarps * 32), C::SMEM, st,
                       m.k, m.v, a);
 }

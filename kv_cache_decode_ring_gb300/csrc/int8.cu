@@ -758,13 +758,8 @@ __global__ void __launch_bounds__(kCombineThreads) int8_combine_kernel(const Int
 template <int D, int G, bool DITHER, bool GEN>
 cudaError_t launch_t(const Int8Args& a, cudaStream_t st) {
     using C = I8<D, G, DITHER>;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(int8_decode_kernel<D, G, DITHER, GEN>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    const void* k = reinterpret_cast<const void*>(int8_decode_kernel<D, G, DITHER, GEN>);
+    if (cudaError_t e = allow_smem(k, C::SMEM)) return e;
     return launch_dep(int8_decode_kernel<D, G, DITHER, GEN>, dim3(a.grid, a.Hkv, a.B), dim3(kWarps * 32),
                       C::SMEM, st, a);
 }

@@ -313,13 +313,7 @@ __global__ void __launch_bounds__(kWarps * 32) int8_exact_kernel(const ExactArgs
 template <int D, int G>
 cudaError_t launch_t(const ExactArgs& a, int nx_ctas, cudaStream_t st) {
     using C = XC<D, G>;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(int8_exact_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)C::SMEM);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    if (cudaError_t e = allow_smem(reinterpret_cast<const void*>(int8_exact_kernel<D, G>), C::SMEM)) return e;
     int8_exact_kernel<D, G><<<dim3(nx_ctas, a.Hkv, a.B), kWarps * 32, C::SMEM, st>>>(a);
     return cudaGetLastError();
 }

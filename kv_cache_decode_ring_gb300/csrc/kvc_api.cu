@@ -2,13 +2,28 @@
 // mirror of next_position, RoPE table, and kernel launches.
 #include <cmath>
 #include <cstring>
-#include <vector>
 #include <new>
+#include <vector>
 
 #include "async_copy.h"
 #include "kvc_internal.h"
 
 namespace kvc {
+
+cudaError_t allow_smem(const void* kernel, size_t bytes) {
+    // each thread remembers the grants it made (a few kernels): no lock on the launch path;
+    // setting the attribute again from another thread is harmless
+    struct Grant { const void* kernel; int device; size_t bytes; };
+    thread_local std::vector<Grant> granted;
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    for (const Grant& g : granted)
+        if (g.kernel == kernel && g.device == dev && g.bytes >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e == cudaSuccess) granted.push_back(Grant{kernel, dev, bytes});
+    return e;
+}
 
 cudaError_t launch_append_rows_counts(const AppendArgs& a, const int32_t* counts, cudaStream_t st);
 bool fast_decode_supported(const DecodeArgs& a);
@@ -88,6 +103,8 @@ bool make_shape(const kvc_config& c, Shape* s) {
     const long long keys = (s->W > 0 && s->W < s->S) ? s->W : s->S;
     s->gqa = s->bf16 && !int8 && gqa_decode_supported(s->d, s->g) && rows < (1ll << 31);
     if (s->gqa) s->split = keys >= kGqaLongKeys ? kGqaSplitLong : kGqaSplit;
+    // the generic decode holds a CTA's g queries and g x split scores in shared memory
+    if (!int8 && s->split == kGenericSplit && (size_t)s->g * (s->d + kGenericSplit) * 4 > kMaxSmemPerBlock) return false;
     // a paged cache may start its splits up to one page before the window
     s->max_splits = (int)((keys + s->split - 1) / s->split) + (s->pages > 0 ? 1 : 0);
     if (int8) {

@@ -19,6 +19,7 @@ constexpr int kQBlock = 16;           // tokens per INT8 quantization block
 constexpr int kPage = 16;             // slots per page of a paged cache
 constexpr int kBands = 16;            // witness bands per key row
 constexpr int kGenericSplit = 64;     // keys per split, generic decode kernel
+constexpr size_t kMaxSmemPerBlock = 232448;   // dynamic shared memory a block may be granted (227 KB)
 constexpr int kFastSplit = 128;       // keys per split, bf16 fast decode kernel
 constexpr int kInt8Split = 1024;      // keys per quantized split, INT8 decode kernel ...
 constexpr int kInt8SplitLong = 2048;  // ... and for caches of kInt8LongKeys slots or more
@@ -252,6 +253,11 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
 // in a kernel launched the ordinary way.
 __device__ __forceinline__ void dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void dep_release() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Grants `kernel` `bytes` of dynamic shared memory on the current device, once per
+// (kernel, device, size) and calling thread (kvc_api.cu).  Kernels above 48 KB need it;
+// each kernel always asks for the same size, so no grant ever narrows another.
+cudaError_t allow_smem(const void* kernel, size_t bytes);
 
 template <typename... Params, typename... Args>
 inline cudaError_t launch_dep(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,

@@ -77,6 +77,7 @@ def test_state_bytes_validation(lib):
         kvc.make_config("bf16", "contiguous", "int8", 1, 4, 1, 128, 64, int8_split=1000),  # not a multiple of 64
         kvc.make_config("bf16", "contiguous", "int8", 1, 4, 1, 128, 64, int8_split=960),   # below 1024
         kvc.make_config("bf16", "contiguous", "int8", 1, 4, 1, 128, 64, int8_split=2112),  # above 2048
+        kvc.make_config("f32", "contiguous", None, 1, 256, 1, 256, 64),         # generic decode: 320 KB of smem
     ]
     # the INT8 tiers on a ring (W % 16 == 0) or with a window
     for c in [kvc.make_config("bf16", "ring", "int8", 1, 4, 1, 128, 64),
@@ -85,7 +86,8 @@ def test_state_bytes_validation(lib):
               kvc.make_config("bf16", "contiguous", "int8", 1, 4, 1, 128, 64, page_pool=8),
               kvc.make_config("bf16", "ring", "int8-dither", 1, 4, 1, 128, 64, page_pool=8),
               kvc.make_config("bf16", "contiguous", "int8", 1, 4, 1, 128, 64, int8_split=1088),
-              kvc.make_config("bf16", "ring", "int8-dither", 1, 4, 1, 128, 64, int8_split=2048)]:
+              kvc.make_config("bf16", "ring", "int8-dither", 1, 4, 1, 128, 64, int8_split=2048),
+              kvc.make_config("f32", "contiguous", None, 1, 181, 1, 256, 64)]:           # 227 KB: the limit
         assert kvc.kvc_state_bytes(c) > 0
     for c in bad:
         with pytest.raises(kvc.KvcError) as e:

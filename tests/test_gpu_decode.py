@@ -224,3 +224,22 @@ def test_f32_outputs_strict_tolerance(case):
         out = cache.decode(q.cuda())
         assert out.dtype == torch.float32
         assert_close(out, model.decode(host(q)), "bf16", "decode f32 out")
+
+
+@pytest.mark.parametrize("dtype,Hq,d", [("f32", 64, 256), ("bf16", 160, 96)], ids=["f32-g64-d256", "bf16-g160-d96"])
+def test_generic_decode_beyond_48kb_shared_memory(dtype, Hq, d):
+    # the generic kernel keeps g queries and g x 64 scores per CTA in shared memory: 80 KB
+    # (fp32, g = 64, d = 256) and 100 KB (bf16, g = 160, d = 96), above the 48 KB default
+    w = wl.small("generic-smem-%s" % dtype, B=2, Hq=Hq, Hkv=1, d=d, capacity=200, rope_base=10000.0,
+                 dtype=dtype, seed=19)
+    cache = kvc.Cache.from_workload(w)
+    model = oracle_for(w)
+    k, v = w.prefill_chunk(0, 150)
+    cache.append_rows(k.cuda(), v.cuda(), counts=[150, 70])
+    model.append_rows(host(k), host(v), [150, 70])
+    for s in range(2):
+        q, k1, v1 = w.step_qkv(s)
+        cache.append(k1.cuda(), v1.cuda())
+        model.append(host(k1), host(v1))
+        assert_close(cache.decode(q.cuda()), model.decode(host(q)), dtype, "generic smem decode step %d" % s)
+    assert cache.device_status() == 0
