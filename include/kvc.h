@@ -16,6 +16,9 @@
  *    kvc_create() and kvc_destroy() neither allocate nor free device memory.
  *  - Pointers named d_* are device pointers, h_* host pointers.  Device
  *    inputs must be 16-byte aligned and densely packed in the stated layout.
+ *  - Devices: a handle lives on the device that was current at kvc_create();
+ *    every later call on it that touches the device must run with that device
+ *    current, else it returns KVC_ERR_ARG and enqueues nothing.
  *  - Streams: kvc_stream_t is a cudaStream_t (NULL = the legacy default
  *    stream).  Compute calls only enqueue work and return; none waits for the
  *    GPU, except kvc_create (uploads tables), kvc_export and

@@ -124,7 +124,7 @@ cudaError_t int8_drop_restored(kvc_handle* h, const int32_t* h_cut, cudaStream_t
 using namespace kvc;
 
 extern "C" int kvc_int8_block_risk(kvc_t h, const float* d_ct, float* d_risk, kvc_stream_t stream) {
-    if (!h || !d_ct || !d_risk || !h->sh.int8) return KVC_ERR_ARG;
+    if (!h || !on_device(h) || !d_ct || !d_risk || !h->sh.int8) return KVC_ERR_ARG;
     if (h->sh.dither) return KVC_ERR_UNSUPPORTED;          // Tier B has no per-token bound
     // the gate restores blocks of contiguous caches that attend to their whole history
     if (h->sh.ring || h->sh.W > 0) return KVC_ERR_UNSUPPORTED;
@@ -163,7 +163,8 @@ extern "C" int kvc_int8_gate(const float* h_risk, int32_t B, int32_t Hkv, int32_
 
 extern "C" int kvc_int8_restore(kvc_t h, const int32_t* h_blocks, int32_t n, const void* d_k_full,
                                 const void* d_v_full, kvc_stream_t stream) {
-    if (!h || n < 0 || (n > 0 && (!h_blocks || !d_k_full || !d_v_full)) || !h->sh.int8) return KVC_ERR_ARG;
+    if (!h || !on_device(h) || n < 0 || (n > 0 && (!h_blocks || !d_k_full || !d_v_full)) || !h->sh.int8)
+        return KVC_ERR_ARG;
     if (h->sh.dither) return KVC_ERR_UNSUPPORTED;
     const Shape& s = h->sh;
     const int nblk = s.S / kQBlock;

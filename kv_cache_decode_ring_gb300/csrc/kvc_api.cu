@@ -335,7 +335,7 @@ int kvc_destroy(kvc_t h) {
 }
 
 int kvc_append(kvc_t h, const void* d_k, const void* d_v, kvc_stream_t stream) {
-    if (!h || !d_k || !d_v || !aligned16(d_k) || !aligned16(d_v)) return KVC_ERR_ARG;
+    if (!h || !on_device(h) || !d_k || !d_v || !aligned16(d_k) || !aligned16(d_v)) return KVC_ERR_ARG;
     int rc = check_capacity(h, nullptr, 1);
     if (rc) return rc;
     if (h->sh.pages) {
@@ -354,7 +354,7 @@ int kvc_append(kvc_t h, const void* d_k, const void* d_v, kvc_stream_t stream) {
 
 int kvc_append_rows(kvc_t h, const void* d_k, const void* d_v, int32_t n, const int32_t* h_counts,
                     kvc_stream_t stream) {
-    if (!h || n < 0 || !aligned16(d_k) || !aligned16(d_v)) return KVC_ERR_ARG;
+    if (!h || !on_device(h) || n < 0 || !aligned16(d_k) || !aligned16(d_v)) return KVC_ERR_ARG;
     if (n == 0) return KVC_OK;
     if (!d_k || !d_v) return KVC_ERR_ARG;
     const Shape& s = h->sh;
@@ -382,7 +382,7 @@ int kvc_append_rows(kvc_t h, const void* d_k, const void* d_v, int32_t n, const 
 
 int kvc_decode_attn(kvc_t h, const void* d_q, void* d_out, float* d_cmax, float* d_tanh, float* d_ct,
                     kvc_stream_t stream) {
-    if (!h || !d_q || !d_out || !aligned16(d_q) || !aligned16(d_out)) return KVC_ERR_ARG;
+    if (!h || !on_device(h) || !d_q || !d_out || !aligned16(d_q) || !aligned16(d_out)) return KVC_ERR_ARG;
     const Shape& s = h->sh;
     for (int b = 0; b < s.B; ++b)
         if (h->np[b] < 1) return KVC_ERR_ARG;                 // nothing cached to attend to
@@ -418,7 +418,7 @@ int kvc_decode_attn(kvc_t h, const void* d_q, void* d_out, float* d_cmax, float*
 }
 
 int kvc_trim(kvc_t h, const int32_t* h_cut, kvc_stream_t stream) {
-    if (!h || !h_cut) return KVC_ERR_ARG;
+    if (!h || !on_device(h) || !h_cut) return KVC_ERR_ARG;
     const Shape& s = h->sh;
     for (int b = 0; b < s.B; ++b) {
         const int cut = h_cut[b], np = h->np[b];
@@ -457,7 +457,7 @@ int kvc_trim(kvc_t h, const int32_t* h_cut, kvc_stream_t stream) {
 
 int kvc_chunk_attn(kvc_t h, const void* d_q, const void* d_k, const void* d_v, int32_t n, void* d_out,
                    kvc_stream_t stream) {
-    if (!h || !d_q || !d_k || !d_v || !d_out || n < 1) return KVC_ERR_ARG;
+    if (!h || !on_device(h) || !d_q || !d_k || !d_v || !d_out || n < 1) return KVC_ERR_ARG;
     if (!aligned16(d_q) || !aligned16(d_k) || !aligned16(d_v) || !aligned16(d_out)) return KVC_ERR_ARG;
     const Shape& s = h->sh;
     if (!chunk_supported(s)) return KVC_ERR_UNSUPPORTED;
@@ -523,7 +523,7 @@ int kvc_export(kvc_t h, int32_t which, void* h_dst, size_t bytes, kvc_stream_t s
     size_t need = 0;
     int rc = kvc_export_bytes(h, which, &need);
     if (rc) return rc;
-    if (!h_dst || bytes != need) return KVC_ERR_ARG;
+    if (!h_dst || bytes != need || !on_device(h)) return KVC_ERR_ARG;
     size_t off = 0;
     switch (which) {
         case KVC_EXPORT_K: off = h->L.k; break;
@@ -609,7 +609,7 @@ int kvc_export(kvc_t h, int32_t which, void* h_dst, size_t bytes, kvc_stream_t s
 }
 
 int kvc_set_request_id(kvc_t h, int32_t b, uint32_t request_id, kvc_stream_t stream) {
-    if (!h || b < 0 || b >= h->sh.B || !h->sh.dither || h->np[b] != 0) return KVC_ERR_ARG;
+    if (!h || !on_device(h) || b < 0 || b >= h->sh.B || !h->sh.dither || h->np[b] != 0) return KVC_ERR_ARG;
     h->req_id_h[b] = request_id;
     if (cudaMemcpyAsync(h->state + h->L.req_id + (size_t)b * 4, &h->req_id_h[b], 4, cudaMemcpyHostToDevice,
                         S_(stream)) != cudaSuccess)
@@ -624,7 +624,7 @@ int kvc_next_positions(kvc_t h, int32_t* h_out) {
 }
 
 int kvc_device_status(kvc_t h, kvc_stream_t stream, int32_t* h_status) {
-    if (!h || !h_status) return KVC_ERR_ARG;
+    if (!h || !on_device(h) || !h_status) return KVC_ERR_ARG;
     cudaStream_t st = S_(stream);
     uint32_t word = 0;
     if (cudaMemcpyAsync(&word, h->state + h->L.hdr, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess) return KVC_ERR_CUDA;
@@ -636,7 +636,7 @@ int kvc_device_status(kvc_t h, kvc_stream_t stream, int32_t* h_status) {
 }
 
 int kvc_check_wait_path(kvc_t h, kvc_stream_t stream) {
-    if (!h) return KVC_ERR_ARG;
+    if (!h || !on_device(h)) return KVC_ERR_ARG;
     wait_path_kernel<<<1, 32, 0, S_(stream)>>>(at<uint32_t>(h, h->L.hdr));
     return cudaGetLastError() == cudaSuccess ? KVC_OK : KVC_ERR_CUDA;
 }

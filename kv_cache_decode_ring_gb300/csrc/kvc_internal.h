@@ -371,3 +371,10 @@ struct kvc_handle {
     // Tier B: host mirror of the request IDs
     std::vector<uint32_t> req_id_h;
 };
+
+// Calls that enqueue device work run with the handle's device current (its buffers live
+// there); anything else is refused with KVC_ERR_ARG rather than launched elsewhere.
+inline bool on_device(const kvc_handle* h) {
+    int dev = -1;
+    return cudaGetDevice(&dev) == cudaSuccess && dev == h->device;
+}

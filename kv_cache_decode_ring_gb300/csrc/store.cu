@@ -225,7 +225,7 @@ int kvc_pstore_lookup(kvc_pstore_t ps, const int64_t* h_ids, int32_t n_ids, cons
 }
 
 int kvc_store_save(kvc_t h, int32_t slot, int32_t b, int32_t n, kvc_stream_t stream) {
-    if (!h) return KVC_ERR_ARG;
+    if (!h || !on_device(h)) return KVC_ERR_ARG;
     const Shape& s = h->sh;
     if (s.store_slots == 0) return KVC_ERR_UNSUPPORTED;
     if (slot < 0 || slot >= s.store_slots || b < 0 || b >= s.B || n < 1 || n != h->np[b]) return KVC_ERR_ARG;
@@ -239,7 +239,7 @@ int kvc_store_save(kvc_t h, int32_t slot, int32_t b, int32_t n, kvc_stream_t str
 
 int kvc_store_load_batch(kvc_t h, int32_t n, const int32_t* h_slots, const int32_t* h_b, const int32_t* h_cuts,
                          kvc_stream_t stream) {
-    if (!h || n < 0) return KVC_ERR_ARG;
+    if (!h || !on_device(h) || n < 0) return KVC_ERR_ARG;
     const Shape& s = h->sh;
     if (s.store_slots == 0) return KVC_ERR_UNSUPPORTED;
     if (n == 0) return KVC_OK;
