@@ -49,23 +49,23 @@ CSRC = os.path.join(ROOT, "kv_cache_decode_ring_gb300", "csrc")
 # valid only while the kernel source is the one captured (sha256 prefix), otherwise the
 # JSON line reports null.
 TRAFFIC_PER_BYTE = {
-    "full-cache-mha": ("decode_fast.cu", "1c1f7c30fe290db7", (268705792 + 4242432) / 268632064),
-    "sliding-window-gqa": ("decode_gqa.cu", "596f2f658be07ec0", (268078080 + 3044096) / 268148736),
-    "int8-witness": ("int8.cu", "6fae76895f96ec4f", (302859264 + 3017984) / 302551040),
-    "bf16-at-int8-shape": ("decode_gqa.cu", "596f2f658be07ec0", (536977152 + 3369984) / 536907776),
+    "full-cache-mha": ("decode_fast.cu", "ea05ecaf8cc06944", (268707328 + 4217088) / 268632064),
+    "sliding-window-gqa": ("decode_gqa.cu", "68a52c99893be10e", (268102912 + 3000064) / 268148736),
+    "int8-witness": ("int8.cu", "0a3cba71d3802962", (302857728 + 2995968) / 302551040),
+    "bf16-at-int8-shape": ("decode_gqa.cu", "68a52c99893be10e", (536976640 + 3210240) / 536907776),
     # (the chunk's reads also include the query, 16.8 MB in this 4-request capture, which the
     # K/V basis leaves out)
-    "prefix-reuse": ("chunk.cu", "a83a030e240a769c", (80662528 + 2573568) / 60850176),
-    "prefix-reuse-w4096": ("chunk.cu", "a83a030e240a769c", (74514432 + 2152448) / 60850176),
-    "int8-dither": ("int8.cu", "6fae76895f96ec4f", (269305088 + 3097088) / 268996608),
+    "prefix-reuse": ("chunk.cu", "de37e058599ee090", (83959552 + 3649792) / 60850176),
+    "prefix-reuse-w4096": ("chunk.cu", "de37e058599ee090", (77292288 + 3273984) / 60850176),
+    "int8-dither": ("int8.cu", "0a3cba71d3802962", (269303552 + 2982400) / 268996608),
     # (2 requests: 16 x (2048 blocks of codes, witnesses and scales + 3 tail rows) = 151.28 MB)
-    "int8-witness-ring": ("int8.cu", "6fae76895f96ec4f", (151492864 + 3013888) / 151281664),
-    "full-cache-mha-paged": ("decode_fast.cu", "1c1f7c30fe290db7", (268710400 + 4297984) / 268632064),
-    "sliding-window-gqa-paged": ("decode_gqa.cu", "596f2f658be07ec0", (268096512 + 3033344) / 268148736),
-    "prefix-reuse-store": ("chunk.cu", "a83a030e240a769c", (80662528 + 2573568) / 60850176),   # the same chunk launch
+    "int8-witness-ring": ("int8.cu", "0a3cba71d3802962", (151493632 + 2989312) / 151281664),
+    "full-cache-mha-paged": ("decode_fast.cu", "ea05ecaf8cc06944", (268708608 + 4353280) / 268632064),
+    "sliding-window-gqa-paged": ("decode_gqa.cu", "68a52c99893be10e", (268100608 + 2968064) / 268148736),
+    "prefix-reuse-store": ("chunk.cu", "de37e058599ee090", (83959552 + 3649792) / 60850176),   # the same chunk launch
     # the store's batched row copy (8 requests' cuts, 297.9 MB read + written): writes still in L2
     # at the end of the launch are not counted, so the ratio is below 1
-    "store-load": ("store.cu", "87899089531c77de", (149272064 + 95416064) / 297918464),
+    "store-load": ("store.cu", "817adec9d1411abf", (149277440 + 95578624) / 297918464),
 }
 
 
