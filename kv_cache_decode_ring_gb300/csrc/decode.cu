@@ -87,19 +87,21 @@ __global__ void __launch_bounds__(kThreads) decode_generic_kernel(const DecodeAr
     }
 }
 
-// Combine: WPR warps per (request, query head) row, 8 / WPR rows per CTA.  Each warp
-// finds the row's maximum and denominator itself with lanes over splits (the second
-// pass re-reads from L1), then accumulates every WPR-th split's partial with lanes
-// over 4-dim groups, loads unrolled; the WPR sums meet in shared memory once.  One
-// warp per row when rows have few splits (more rows in flight), eight when rows are
-// few and long, four otherwise.
+// Combine: WPR warps per (request, query head) row, 8 / WPR rows per CTA.  One pass over
+// the splits: warp w takes the splits w, w + WPR, ..., kU at a time with every load of a
+// round issued together, and keeps a running maximum, denominator and weighted sum (lanes
+// over 4-dim groups), rescaled when a round raises the maximum; the WPR warps' (m, l, acc)
+// meet in shared memory once.  One warp per row when rows have few splits (more rows in
+// flight), eight when rows are few and long, four otherwise.
 constexpr int kCombineThreads = 256;
+constexpr int kCombineU = 4;            // splits a warp loads per round
 
 template <int WPR>
 __global__ void __launch_bounds__(kCombineThreads) combine_rows_kernel(const CombineArgs c) {
     constexpr int kWarpsPerRow = WPR;
     constexpr int kRowsPerCta = kCombineThreads / 32 / WPR;
     __shared__ float4 sacc[kRowsPerCta][kWarpsPerRow][64];          // d <= 256
+    __shared__ float2 sml[kRowsPerCta][kWarpsPerRow];               // each warp's (m, l)
     dep_wait();                                                      // launched dependent: see launch_dep
     dep_release();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -108,7 +110,6 @@ __global__ void __launch_bounds__(kCombineThreads) combine_rows_kernel(const Com
     const bool valid = row < (size_t)c.B * c.Hq;
     const bool vec = c.d % 4 == 0;
     int ns = 0;
-    float mx = -INFINITY, inv = 0.f;
     const float2* ml = c.part_ml + row * c.max_splits;
     const float* pa = c.part_acc + row * c.max_splits * c.d;
     if (valid) {
@@ -118,38 +119,69 @@ __global__ void __launch_bounds__(kCombineThreads) combine_rows_kernel(const Com
         key_range(len, c.S, c.W, c.ring, lo, hi);
         if (c.align_lo) lo &= ~(kPage - 1);         // the paged GQA decode's split origin
         ns = (hi - lo + c.split - 1) / c.split;
-        for (int s = lane; s < ns; s += 32) mx = fmaxf(mx, __ldg(ml + s).x);
-        for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        float L = 0.f;
-        for (int s = lane; s < ns; s += 32) {
-            const float2 v = __ldg(ml + s);
-            L += v.y * exp2f(v.x - mx);
-        }
-        for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-        inv = L > 0.f ? 1.f / L : 0.f;
-        if (vec) {
-            for (int i0 = 4 * lane; i0 < c.d; i0 += 128) {
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-                for (int s = w; s < ns; s += kWarpsPerRow) {
-                    const float f = exp2f(__ldg(ml + s).x - mx);
-                    const float4 x = __ldg(reinterpret_cast<const float4*>(pa + (size_t)s * c.d + i0));
-                    acc.x = fmaf(x.x, f, acc.x); acc.y = fmaf(x.y, f, acc.y);
-                    acc.z = fmaf(x.z, f, acc.z); acc.w = fmaf(x.w, f, acc.w);
+    }
+    if (valid && vec) {
+        float m = -INFINITY, l = 0.f;
+        float4 acc[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+        for (int s0 = w; s0 < ns; s0 += kWarpsPerRow * kCombineU) {
+            float2 v[kCombineU];
+            float4 x[kCombineU][2];
+#pragma unroll
+            for (int u = 0; u < kCombineU; ++u) {
+                const int s = s0 + u * kWarpsPerRow;
+                v[u] = s < ns ? __ldg(ml + s) : make_float2(-INFINITY, 0.f);
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const int i0 = 4 * lane + 128 * k;
+                    x[u][k] = (s < ns && i0 < c.d) ? __ldg(reinterpret_cast<const float4*>(pa + (size_t)s * c.d + i0))
+                                                   : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
-                sacc[r][w][i0 / 4] = acc;
             }
+            float mn = m;
+#pragma unroll
+            for (int u = 0; u < kCombineU; ++u) mn = fmaxf(mn, v[u].x);
+            if (mn == -INFINITY) continue;                      // no keys in any split so far
+            const float sc = exp2f(m - mn);                     // 0 while m was -inf
+            l *= sc;
+#pragma unroll
+            for (int k = 0; k < 2; ++k) { acc[k].x *= sc; acc[k].y *= sc; acc[k].z *= sc; acc[k].w *= sc; }
+#pragma unroll
+            for (int u = 0; u < kCombineU; ++u) {
+                const float f = exp2f(v[u].x - mn);               // 0 for an empty split
+                l = fmaf(v[u].y, f, l);
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    acc[k].x = fmaf(x[u][k].x, f, acc[k].x); acc[k].y = fmaf(x[u][k].y, f, acc[k].y);
+                    acc[k].z = fmaf(x[u][k].z, f, acc[k].z); acc[k].w = fmaf(x[u][k].w, f, acc[k].w);
+                }
+            }
+            m = mn;
         }
+        if (lane == 0) sml[r][w] = make_float2(m, l);
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+            if (4 * lane + 128 * k < c.d) sacc[r][w][lane + 32 * k] = acc[k];
     }
     __syncthreads();
     if (!valid || w != 0) return;
     if (vec) {
-        for (int i0 = 4 * lane; i0 < c.d; i0 += 128) {
-            float4 acc = sacc[r][0][i0 / 4];
+        float M = -INFINITY;
 #pragma unroll
-            for (int k = 1; k < kWarpsPerRow; ++k) {
+        for (int k = 0; k < kWarpsPerRow; ++k) M = fmaxf(M, sml[r][k].x);
+        float f[kWarpsPerRow], L = 0.f;
+#pragma unroll
+        for (int k = 0; k < kWarpsPerRow; ++k) {
+            f[k] = sml[r][k].x == -INFINITY ? 0.f : exp2f(sml[r][k].x - M);
+            L = fmaf(sml[r][k].y, f[k], L);
+        }
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        for (int i0 = 4 * lane; i0 < c.d; i0 += 128) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int k = 0; k < kWarpsPerRow; ++k) {
                 const float4 x = sacc[r][k][i0 / 4];
-                acc.x += x.x; acc.y += x.y; acc.z += x.z; acc.w += x.w;
+                acc.x = fmaf(x.x, f[k], acc.x); acc.y = fmaf(x.y, f[k], acc.y);
+                acc.z = fmaf(x.z, f[k], acc.z); acc.w = fmaf(x.w, f[k], acc.w);
             }
             const float o[4] = {acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv};
 #pragma unroll
@@ -159,7 +191,17 @@ __global__ void __launch_bounds__(kCombineThreads) combine_rows_kernel(const Com
             }
         }
     } else {
-        // head dims not a multiple of 4 (small shapes): the row's first warp alone
+        // head dims not a multiple of 4 (small shapes): the row's first warp alone, two passes
+        float mx = -INFINITY;
+        for (int s = lane; s < ns; s += 32) mx = fmaxf(mx, __ldg(ml + s).x);
+        for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        float L = 0.f;
+        for (int s = lane; s < ns; s += 32) {
+            const float2 v = __ldg(ml + s);
+            L += v.y * exp2f(v.x - mx);
+        }
+        for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+        const float inv = L > 0.f ? 1.f / L : 0.f;
         for (int i = lane; i < c.d; i += 32) {
             float acc = 0.f;
             for (int s = 0; s < ns; ++s) acc = fmaf(__ldg(pa + (size_t)s * c.d + i), exp2f(__ldg(ml + s).x - mx), acc);

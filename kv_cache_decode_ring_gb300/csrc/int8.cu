@@ -678,23 +678,25 @@ __device__ __forceinline__ float tanh_up(float x) {
     return fminf(t, 1.f);
 }
 
-// Combine: WPR warps per (request, query head) row, 8 / WPR rows per CTA (the design
-// of the bf16 combine): each warp finds the row's maximum, denominator and bound
-// maximum with lanes over splits, then accumulates every WPR-th split's partial with
-// lanes over 4-dim groups; the sums meet in shared memory once.
+// Combine: WPR warps per (request, query head) row, 8 / WPR rows per CTA (the design of
+// the bf16 combine): one pass over the splits, warp w taking the splits w, w + WPR, ...,
+// kU at a time with every load of a round issued together, keeping a running maximum,
+// denominator, weighted sum (lanes over 4-dim groups) and bound maximum; the WPR warps'
+// results meet in shared memory once.
 constexpr int kCombineThreads = 256;
+constexpr int kCombineU = 4;            // splits a warp loads per round
 
 template <int WPR>
 __global__ void __launch_bounds__(kCombineThreads) int8_combine_kernel(const Int8CombineArgs c) {
     constexpr int kRows = kCombineThreads / 32 / WPR;
     __shared__ float4 sacc[kRows][WPR][32];                       // d <= 128
+    __shared__ float4 sml[kRows][WPR];                            // each warp's (m, l, max c)
     dep_wait();                                                    // launched dependent: see launch_dep
     dep_release();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = warp / WPR, w = warp % WPR;
     const size_t row = (size_t)blockIdx.x * kRows + r;
     const bool valid = row < (size_t)c.B * c.Hq;
-    float mx = -INFINITY, inv = 0.f, cm = 0.f;
     if (valid) {
         const int b = (int)(row / c.Hq), hq = (int)(row % c.Hq);
         const int len = c.next_pos[b];
@@ -708,39 +710,59 @@ __global__ void __launch_bounds__(kCombineThreads) int8_combine_kernel(const Int
                        (nx + kExactBlocksPerCta - 1) / kExactBlocksPerCta;
         const float2* ml = c.part_ml + row * c.max_splits;
         const float* pc = c.part_c + row * c.max_splits;
-        for (int s = lane; s < ns; s += 32) { mx = fmaxf(mx, __ldg(ml + s).x); cm = fmaxf(cm, __ldg(pc + s)); }
-        for (int o = 16; o; o >>= 1) {
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-            cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o));
-        }
-        float L = 0.f;
-        for (int s = lane; s < ns; s += 32) {
-            const float2 v = __ldg(ml + s);
-            L += v.y * exp2f(v.x - mx);
-        }
-        for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-        inv = L > 0.f ? 1.f / L : 0.f;
         const float* pa = c.part_acc + row * c.max_splits * c.d;
-        for (int i0 = 4 * lane; i0 < c.d; i0 += 128) {
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-            for (int s = w; s < ns; s += WPR) {
-                const float f = exp2f(__ldg(ml + s).x - mx);
-                const float4 x = __ldg(reinterpret_cast<const float4*>(pa + (size_t)s * c.d + i0));
-                acc.x = fmaf(x.x, f, acc.x); acc.y = fmaf(x.y, f, acc.y);
-                acc.z = fmaf(x.z, f, acc.z); acc.w = fmaf(x.w, f, acc.w);
+        const int i0 = 4 * lane;                                  // (d <= 128: one 4-dim group a lane)
+        float m = -INFINITY, l = 0.f, cm = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int s0 = w; s0 < ns; s0 += WPR * kCombineU) {
+            float2 v[kCombineU];
+            float4 x[kCombineU];
+#pragma unroll
+            for (int u = 0; u < kCombineU; ++u) {
+                const int s = s0 + u * WPR;
+                v[u] = s < ns ? __ldg(ml + s) : make_float2(-INFINITY, 0.f);
+                cm = fmaxf(cm, s < ns ? __ldg(pc + s) : 0.f);
+                x[u] = (s < ns && i0 < c.d) ? __ldg(reinterpret_cast<const float4*>(pa + (size_t)s * c.d + i0))
+                                            : make_float4(0.f, 0.f, 0.f, 0.f);
             }
-            sacc[r][w][i0 / 4] = acc;
+            float mn = m;
+#pragma unroll
+            for (int u = 0; u < kCombineU; ++u) mn = fmaxf(mn, v[u].x);
+            if (mn == -INFINITY) continue;                      // no keys in any split so far
+            const float sc = exp2f(m - mn);                     // 0 while m was -inf
+            l *= sc;
+            acc.x *= sc; acc.y *= sc; acc.z *= sc; acc.w *= sc;
+#pragma unroll
+            for (int u = 0; u < kCombineU; ++u) {
+                const float f = exp2f(v[u].x - mn);               // 0 for an empty split
+                l = fmaf(v[u].y, f, l);
+                acc.x = fmaf(x[u].x, f, acc.x); acc.y = fmaf(x[u].y, f, acc.y);
+                acc.z = fmaf(x[u].z, f, acc.z); acc.w = fmaf(x[u].w, f, acc.w);
+            }
+            m = mn;
         }
+        if (lane == 0) sml[r][w] = make_float4(m, l, cm, 0.f);
+        if (i0 < c.d) sacc[r][w][lane] = acc;
     }
     __syncthreads();
     if (!valid || w != 0) return;
-    for (int i0 = 4 * lane; i0 < c.d; i0 += 128) {
-        float4 acc = sacc[r][0][i0 / 4];
+    float M = -INFINITY, cm = 0.f;
 #pragma unroll
-        for (int k = 1; k < WPR; ++k) {
+    for (int k = 0; k < WPR; ++k) { M = fmaxf(M, sml[r][k].x); cm = fmaxf(cm, sml[r][k].z); }
+    float f[WPR], L = 0.f;
+#pragma unroll
+    for (int k = 0; k < WPR; ++k) {
+        f[k] = sml[r][k].x == -INFINITY ? 0.f : exp2f(sml[r][k].x - M);
+        L = fmaf(sml[r][k].y, f[k], L);
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    for (int i0 = 4 * lane; i0 < c.d; i0 += 128) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < WPR; ++k) {
             const float4 x = sacc[r][k][i0 / 4];
-            acc.x += x.x; acc.y += x.y; acc.z += x.z; acc.w += x.w;
+            acc.x = fmaf(x.x, f[k], acc.x); acc.y = fmaf(x.y, f[k], acc.y);
+            acc.z = fmaf(x.z, f[k], acc.z); acc.w = fmaf(x.w, f[k], acc.w);
         }
         const float o[4] = {acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv};
 #pragma unroll
