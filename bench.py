@@ -51,15 +51,15 @@ CSRC = os.path.join(ROOT, "kv_cache_decode_ring_gb300", "csrc")
 TRAFFIC_PER_BYTE = {
     "full-cache-mha": ("decode_fast.cu", "ea05ecaf8cc06944", (268707328 + 4217088) / 268632064),
     "sliding-window-gqa": ("decode_gqa.cu", "68a52c99893be10e", (268102912 + 3000064) / 268148736),
-    "int8-witness": ("int8.cu", "0a3cba71d3802962", (302857728 + 2995968) / 302551040),
+    "int8-witness": ("int8.cu", "8753292bf0d3a988", (302857984 + 2983168) / 302551040),
     "bf16-at-int8-shape": ("decode_gqa.cu", "68a52c99893be10e", (536976640 + 3210240) / 536907776),
     # (the chunk's reads also include the query, 16.8 MB in this 4-request capture, which the
     # K/V basis leaves out)
     "prefix-reuse": ("chunk.cu", "de37e058599ee090", (83959552 + 3649792) / 60850176),
     "prefix-reuse-w4096": ("chunk.cu", "de37e058599ee090", (77292288 + 3273984) / 60850176),
-    "int8-dither": ("int8.cu", "0a3cba71d3802962", (269303552 + 2982400) / 268996608),
+    "int8-dither": ("int8.cu", "8753292bf0d3a988", (269328128 + 3047936) / 268996608),
     # (2 requests: 16 x (2048 blocks of codes, witnesses and scales + 3 tail rows) = 151.28 MB)
-    "int8-witness-ring": ("int8.cu", "0a3cba71d3802962", (151493632 + 2989312) / 151281664),
+    "int8-witness-ring": ("int8.cu", "8753292bf0d3a988", (151496448 + 3245312) / 151281664),
     "full-cache-mha-paged": ("decode_fast.cu", "ea05ecaf8cc06944", (268708608 + 4353280) / 268632064),
     "sliding-window-gqa-paged": ("decode_gqa.cu", "68a52c99893be10e", (268100608 + 2968064) / 268148736),
     "prefix-reuse-store": ("chunk.cu", "de37e058599ee090", (83959552 + 3649792) / 60850176),   # the same chunk launch
