@@ -252,7 +252,9 @@ class DecodeBench:
         self.e2e_dev = [[torch.empty(t.shape, dtype=t.dtype, device="cuda") for t in host_example] for _ in range(2)]
         self.e2e_dout = [torch.empty_like(out_example) for _ in range(2)]
         self.e2e_hout = [torch.empty(out_example.shape, dtype=out_example.dtype).pin_memory() for _ in range(2)]
-        self.copy_stream = torch.cuda.Stream()
+        # uploads and downloads on streams of their own, so the two copy directions overlap
+        self.up_stream = torch.cuda.Stream()
+        self.down_stream = torch.cuda.Stream()
         self.ev_in = [torch.cuda.Event() for _ in range(2)]      # slot's inputs uploaded
         self.ev_used = [torch.cuda.Event() for _ in range(2)]    # slot's inputs consumed, output written
         self.ev_read = [torch.cuda.Event() for _ in range(2)]    # slot's output downloaded
@@ -261,14 +263,14 @@ class DecodeBench:
             self.e2e_hout[0].numel() * self.e2e_hout[0].element_size()
 
     def _upload(self, n):
-        """Copy stream: the inputs of step n into slot n % 2 once that slot is free."""
+        """Upload stream: the inputs of step n into slot n % 2 once that slot is free."""
         import torch
         s = n % 2
-        with torch.cuda.stream(self.copy_stream):
-            self.copy_stream.wait_event(self.ev_used[s])
+        with torch.cuda.stream(self.up_stream):
+            self.up_stream.wait_event(self.ev_used[s])
             for dst, src in zip(self.e2e_dev[s], self.e2e_host_inputs(n)):
                 dst.copy_(src, non_blocking=True)
-            self.ev_in[s].record(self.copy_stream)
+            self.ev_in[s].record(self.up_stream)
 
     def e2e_step(self):
         """One step: its inputs uploaded, its kernels, its output downloaded.  The next
@@ -286,19 +288,20 @@ class DecodeBench:
         cur.wait_event(self.ev_read[s])                          # the slot's previous output downloaded
         self.e2e_compute(self.e2e_dev[s], self.e2e_dout[s])
         self.ev_used[s].record(cur)
-        with torch.cuda.stream(self.copy_stream):
-            self.copy_stream.wait_event(self.ev_used[s])
+        with torch.cuda.stream(self.down_stream):
+            self.down_stream.wait_event(self.ev_used[s])
             self.e2e_hout[s].copy_(self.e2e_dout[s], non_blocking=True)
-            self.ev_read[s].record(self.copy_stream)
+            self.ev_read[s].record(self.down_stream)
         self.done += 1
 
     def e2e_flush(self):
         """The current stream waits for the last download; a pending upload is dropped
         (the next step uploads its own inputs again)."""
         import torch
-        done = torch.cuda.Event()
-        done.record(self.copy_stream)
-        torch.cuda.current_stream().wait_event(done)
+        for st in (self.up_stream, self.down_stream):
+            done = torch.cuda.Event()
+            done.record(st)
+            torch.cuda.current_stream().wait_event(done)
         self.e2e_next = None
 
 
