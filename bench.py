@@ -928,11 +928,21 @@ EXTRA_LINES = ("int8-witness", "sliding-window-gqa", "prefix-reuse", "prefix-reu
                "prefix-reuse-store", "int8-witness-ring")
 
 
+def call_samples(K):
+    """The timed steps whose dominant call is bracketed by CUDA events: every 8th (every 4th
+    below 64 steps) from the second on.  The first step follows the synchronize that opens
+    the timed region, so its launches start from an idle GPU."""
+    stride = 8 if K >= 64 else 4
+    return list(range(1, K, stride)) or [0]
+
+
 def time_steps(bench, K, warmup, local_rank, dist):
     """W untimed steps, then K timed steps bracketed by a barrier and a synchronize on both
-    sides; the dominant call of every step is bracketed by its own pair of CUDA events on
-    the stream it is launched on.  Returns the slowest rank's milliseconds, the units all
-    ranks processed, this rank's per-step units and call milliseconds, launches and clocks."""
+    sides.  The dominant call of the steps call_samples(K) names is bracketed by its own
+    pair of CUDA events on the stream it is launched on: an event between two kernels keeps
+    the second from starting as a dependent launch during the first's tail, so events on
+    every step would add their own gaps (7-8 us a step) to the step time they measure.  Returns the slowest rank's milliseconds, the units all
+    ranks processed, the sampled steps' units and call milliseconds, launches and clocks."""
     import torch
 
     def barrier():
@@ -943,7 +953,8 @@ def time_steps(bench, K, warmup, local_rank, dist):
     for _ in range(warmup):
         bench.step()
     bench.reset()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    sampled = call_samples(K)
+    ev = {i: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for i in sampled}
     t0e, t1e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(gpu_index(local_rank))
     sampler.start()
@@ -954,16 +965,18 @@ def time_steps(bench, K, warmup, local_rank, dist):
     units, launches, step_units = 0, 0, []
     for i in range(K):
         u = bench.units()
-        launches += bench.launches_per_step() + bench.step(ev[i])
+        launches += bench.launches_per_step() + bench.step(ev.get(i))
         units += u
-        step_units.append(u)
+        if i in ev:
+            step_units.append(u)
     t1e.record()
     barrier()
     wall = time.perf_counter() - wall0
     sampler.stop()
     ms_total, all_units = replica_aggregate(t0e.elapsed_time(t1e), units, dist, "cuda")
     return {"ms": ms_total, "units": all_units, "step_units": step_units,
-            "call_ms": [a.elapsed_time(b) for a, b in ev], "launches": launches, "clocks": sampler.summary(),
+            "call_ms": [ev[i][0].elapsed_time(ev[i][1]) for i in sampled], "launches": launches,
+            "clocks": sampler.summary(),
             "wall": wall}
 
 
@@ -972,8 +985,9 @@ def line_summary(bench, workload, t, K):
     peak, peak_kind = hbm_peak() if bench.bound == "hbm" else tensor_peak()
     scale = 1e9 if bench.unit == "GB/s" else 1e12
     value = t["units"] / (t["ms"] / 1e3) / scale
-    call_units = sum(u + bench.io_bytes() for u in t["step_units"]) / K
-    call_ms = sum(t["call_ms"]) / K
+    n = len(t["call_ms"])                                   # the sampled calls
+    call_units = sum(u + bench.io_bytes() for u in t["step_units"]) / n
+    call_ms = sum(t["call_ms"]) / n
     achieved = call_units / (call_ms / 1e3) / scale
     return {
         "value": round(value, 2), "unit": bench.unit, "ms_per_step": round(t["ms"] / K, 5), "steps": K,
@@ -983,7 +997,7 @@ def line_summary(bench, workload, t, K):
                      "traffic": traffic_per_launch(workload, bench.traffic_basis(call_units)),
                      "kernel": bench.kernel, "peak_kind": peak_kind,
                      "%s_per_launch" % ("bytes" if bench.unit == "GB/s" else "flops"): int(call_units),
-                     "avg_launch_ms": round(call_ms, 5)},
+                     "avg_launch_ms": round(call_ms, 5), "launches_timed": n},
         "gpu_launches": t["launches"], "clocks": t["clocks"], "config": bench.config(),
     }
 

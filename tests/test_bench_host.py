@@ -96,3 +96,12 @@ def test_default_run_times_every_targeted_line():
     for name in ("int8-witness", "sliding-window-gqa", "prefix-reuse", "prefix-reuse-w4096", "int8-dither",
                  "prefix-reuse-store", "int8-witness-ring"):
         assert name in bench.EXTRA_LINES and name in bench.BENCHES
+
+
+def test_call_samples_skip_the_first_step_and_thin_out():
+    # the dominant call is timed on a sample of the steps (events between kernels cost the
+    # dependent launches their overlap); never the first step after the synchronize
+    assert bench.call_samples(1) == [0]
+    assert bench.call_samples(20) == [1, 5, 9, 13, 17]
+    s = bench.call_samples(1500)
+    assert s[0] == 1 and all(b - a == 8 for a, b in zip(s, s[1:])) and s[-1] < 1500
