@@ -941,8 +941,9 @@ def time_steps(bench, K, warmup, local_rank, dist):
     sides.  The dominant call of the steps call_samples(K) names is bracketed by its own
     pair of CUDA events on the stream it is launched on: an event between two kernels keeps
     the second from starting as a dependent launch during the first's tail, so events on
-    every step would add their own gaps (7-8 us a step) to the step time they measure.  Returns the slowest rank's milliseconds, the units all
-    ranks processed, the sampled steps' units and call milliseconds, launches and clocks."""
+    every step would add their own gaps (7-8 us a step) to the step time they measure.
+    Returns the slowest rank's milliseconds, the units all ranks processed, the sampled
+    steps' units and call milliseconds, launches and clocks."""
     import torch
 
     def barrier():

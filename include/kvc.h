@@ -176,8 +176,8 @@ int kvc_append_rows(kvc_t h, const void* d_k, const void* d_v, int32_t n,
  * cached positions [max(0, t-W+1), t]:
  *     out = softmax(q . K^T / sqrt(d)) . V            d_out: [B][Hq][d]
  * evaluated as split-K flash decoding with an online softmax and a cross-split
- * combine, fp32 accumulation, rounded once to the output dtype.  Needs at least one cached token per request, and
- * on a ring an append after any trim.
+ * combine, fp32 accumulation, rounded once to the output dtype.  Needs at least
+ * one cached token per request, and on a ring an append after any trim.
  * INT8 caches also return, per (request, query head), the witness bound
  * ([WITCERT] "频带酉性与双层证书"):
  *     c_t = (1/sqrt d) sum_b ||q_b|| w_{t,b}   for every cached token in the window,

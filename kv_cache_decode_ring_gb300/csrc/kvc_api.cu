@@ -104,7 +104,8 @@ bool make_shape(const kvc_config& c, Shape* s) {
     s->gqa = s->bf16 && !int8 && gqa_decode_supported(s->d, s->g) && rows < (1ll << 31);
     if (s->gqa) s->split = keys >= kGqaLongKeys ? kGqaSplitLong : kGqaSplit;
     // the generic decode holds a CTA's g queries and g x split scores in shared memory
-    if (!int8 && s->split == kGenericSplit && (size_t)s->g * (s->d + kGenericSplit) * 4 > kMaxSmemPerBlock) return false;
+    if (!int8 && s->split == kGenericSplit && (size_t)s->g * (s->d + kGenericSplit) * 4 > kMaxSmemPerBlock)
+        return false;
     // a paged cache may start its splits up to one page before the window
     s->max_splits = (int)((keys + s->split - 1) / s->split) + (s->pages > 0 ? 1 : 0);
     if (int8) {
