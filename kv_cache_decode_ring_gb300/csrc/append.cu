@@ -140,18 +140,23 @@ __device__ void quantize_block(const AppendArgs& a, const float* sK, const float
     }
 }
 
-// One token per request.  CTA b writes every KV head of request b, then
-// advances next_position[b] (one writer per request: no cross-CTA race).
+// One token per request.  CTA (b, y) writes KV heads [y hpc, (y + 1) hpc) of request b
+// (and, for the INT8 tiers, quantizes their blocks when the row completes one).  Every
+// CTA of the request reads next_position[b] first; the last of them to finish (an
+// arrival counter, reset by that CTA) writes positions[slot] and advances
+// next_position[b], so no CTA can read the advanced value.
 __global__ void __launch_bounds__(kThreads) append_token_kernel(const AppendArgs a) {
     extern __shared__ float smem[];
     dep_wait();                                        // launched dependent: see launch_dep
     dep_release();
     const int b = blockIdx.x;
     const int p = a.next_pos[b];
-    if (!position_ok(a, p)) {
-        if (threadIdx.x == 0) flag(a.hdr, kErrPosition);
+    if (!position_ok(a, p)) {                          // (every CTA of the request returns here)
+        if (threadIdx.x == 0 && blockIdx.y == 0) flag(a.hdr, kErrPosition);
         return;
     }
+    const int h0 = blockIdx.y * a.hpc;
+    const int nh = min(a.Hkv - h0, a.hpc);             // KV heads of this CTA (>= 1)
     const int d = a.d, half = d / 2;
     const int slot = a.ring ? p % a.S : p;
     const int tslot = p % kQBlock;                     // INT8: the row's place in the exact tail
@@ -160,7 +165,7 @@ __global__ void __launch_bounds__(kThreads) append_token_kernel(const AppendArgs
         // before any arithmetic: one round trip for the whole row set.  The rows go to
         // the cache (bf16) or to the exact tail (INT8 tier).
         constexpr int kU = 4;
-        const int vec = d / 8, n = a.Hkv * vec;
+        const int vec = d / 8, n = nh * vec;
         const uint4* K = static_cast<const uint4*>(a.k);
         const uint4* V = static_cast<const uint4*>(a.v);
         __nv_bfloat16* kdst = a.int8 ? a.ktail : static_cast<__nv_bfloat16*>(a.kc);
@@ -172,7 +177,7 @@ __global__ void __launch_bounds__(kThreads) append_token_kernel(const AppendArgs
             for (int u = 0; u < kU; ++u) {
                 const int idx = base + u * blockDim.x;
                 if (idx >= n) continue;
-                const int h = idx / vec, c = idx % vec;
+                const int h = h0 + idx / vec, c = idx % vec;
                 kx[u] = __ldg(K + ((size_t)b * a.Hkv + h) * vec + c);
                 vx[u] = __ldg(V + ((size_t)b * a.Hkv + h) * vec + c);
                 if (a.rope) {
@@ -185,7 +190,7 @@ __global__ void __launch_bounds__(kThreads) append_token_kernel(const AppendArgs
             for (int u = 0; u < kU; ++u) {
                 const int idx = base + u * blockDim.x;
                 if (idx >= n) continue;
-                const int h = idx / vec, c = idx % vec;
+                const int h = h0 + idx / vec, c = idx % vec;
                 const size_t dst = (a.int8 ? (((size_t)b * a.Hkv + h) * kQBlock + tslot)
                                            : kv_row(a.table, b, h, slot, a.Hkv, a.S)) * d + 8 * c;
                 uint4 ko = kx[u];
@@ -213,7 +218,7 @@ __global__ void __launch_bounds__(kThreads) append_token_kernel(const AppendArgs
             float* sV = smem + kQBlock * d;
             float* red = smem + 2 * kQBlock * d;
             __threadfence_block();
-            for (int h = 0; h < a.Hkv; ++h) {
+            for (int h = h0; h < h0 + nh; ++h) {
                 const size_t tail = ((size_t)b * a.Hkv + h) * kQBlock * d;
                 __syncthreads();                       // the tail rows written; smem free
                 for (int i = threadIdx.x; i < kQBlock * d; i += blockDim.x) {
@@ -226,8 +231,8 @@ __global__ void __launch_bounds__(kThreads) append_token_kernel(const AppendArgs
         }
     } else {
         // fp32 caches and other head sizes (never INT8: that tier is bf16 with d % 16 == 0)
-        for (int idx = threadIdx.x; idx < a.Hkv * half; idx += blockDim.x) {
-            const int h = idx / half, i = idx % half;
+        for (int idx = threadIdx.x; idx < nh * half; idx += blockDim.x) {
+            const int h = h0 + idx / half, i = idx % half;
             const size_t src = ((size_t)b * a.Hkv + h) * d;
             const size_t dst = kv_row(a.table, b, h, slot, a.Hkv, a.S) * d;
             float y0, y1;
@@ -239,8 +244,19 @@ __global__ void __launch_bounds__(kThreads) append_token_kernel(const AppendArgs
     }
     __syncthreads();
     if (threadIdx.x == 0) {
-        a.pos[(size_t)b * a.S + slot] = p;
-        a.next_pos[b] = p + 1;
+        bool last = gridDim.y == 1;
+        if (!last) {
+            __threadfence();                            // this CTA's rows, before its arrival
+            last = atomicAdd(&a.arrive[b], 1) == (int)gridDim.y - 1;
+            if (last) {
+                a.arrive[b] = 0;
+                __threadfence();
+            }
+        }
+        if (last) {
+            a.pos[(size_t)b * a.S + slot] = p;
+            a.next_pos[b] = p + 1;
+        }
     }
 }
 
@@ -477,7 +493,7 @@ cudaError_t map_pages(kvc_handle* h, const std::vector<int>& from, const std::ve
 
 cudaError_t launch_append_token(const AppendArgs& a, cudaStream_t st) {
     const size_t smem = a.int8 ? quant_smem(a.d) : 0;
-    return launch_dep(append_token_kernel, dim3(a.B), dim3(kThreads), smem, st, a);
+    return launch_dep(append_token_kernel, dim3(a.B, (a.Hkv + a.hpc - 1) / a.hpc), dim3(kThreads), smem, st, a);
 }
 
 cudaError_t launch_append_rows_group(const AppendArgs& a, const Group& g, cudaStream_t st) {

@@ -150,6 +150,7 @@ Layout make_layout(const Shape& s) {
         L.xpool = take((size_t)s.xpool * 2 * kQBlock * d * 2);
     }
     L.req_id = take(B * 4);
+    L.arrive = take(B * 4);
     L.rope = take((size_t)s.P * (d / 2) * 8);
     L.part_ml = take(B * Hq * s.max_splits * 8);
     L.part_acc = take(B * Hq * s.max_splits * d * 4);
@@ -211,6 +212,11 @@ AppendArgs append_args(kvc_handle* h, const void* k, const void* v, int n) {
     a.layer_ctr = 65536u * (uint32_t)h->cfg.layer_index;
     a.B = s.B; a.Hkv = s.Hkv; a.d = s.d; a.S = s.S; a.P = s.P;
     a.ring = s.ring; a.bf16 = s.bf16; a.int8 = s.int8; a.dither = s.dither;
+    a.arrive = at<int32_t>(h, h->L.arrive);
+    // a one-token append into an INT8 cache quantizes a block per KV head every 16th row: up to
+    // 8 CTAs per request share that work; a bf16/fp32 append is one CTA per request (its arrival
+    // fence and counter cost more than the rows: sliding-window GQA step 0.1626 against 0.1594 ms)
+    a.hpc = s.int8 ? (s.Hkv + 7) / 8 : s.Hkv;
     return a;
 }
 

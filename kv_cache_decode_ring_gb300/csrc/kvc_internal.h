@@ -58,6 +58,7 @@ struct Layout {
     size_t part_acc;  // float  [B][Hq][max_splits][d]
     size_t part_c;    // float  [B][Hq][max_splits] max_t c_t of the split   (INT8)
     size_t req_id;    // uint32 [B] request IDs of the dither counters (Tier B)
+    size_t arrive;    // int32 [B] CTAs of a one-token append done (0 between calls)
     size_t cws;       // ring caches with kvc_chunk_attn: K then V staging [B][Hkv][chunk_ws_rows][d] bf16
     size_t store;     // store slots: each K, V [Hkv][S][d] cache dtype, then positions int32 [S]
     size_t store_stride;  // bytes per store slot
@@ -142,6 +143,8 @@ struct AppendArgs {
     uint32_t key0, key1;      // Tier B: Philox key
     uint32_t layer_ctr;       // Tier B: 65536 * layer
     int B, Hkv, d, S, P, ring, bf16, int8, dither;
+    int32_t* arrive;          // [B] one-token append: CTAs of the request done (0 between calls)
+    int hpc;                  // one-token append: KV heads per CTA
 };
 
 // Tensor maps over the whole K and V caches, rows [B*Hkv*S][d] bf16, boxes of 64
