@@ -208,3 +208,22 @@ def test_dither_state_has_no_witnesses(lib):
     wd = kvc.kvc_state_bytes(kvc.make_config("bf16", "contiguous", "int8-dither", 2, 8, 2, 128, 4096,
                                              layer_index=7, dither_key=(1, 2)))
     assert w8 - wd >= 2 * 2 * 4096 * 16 * 2 - 4096                  # 32 B per token and head fewer
+
+
+def test_config_struct_matches_the_header():
+    # the ctypes mirror of kvc_config lists the header's fields in the header's order,
+    # with 32-bit members throughout (a mismatch would shift every later field)
+    import ctypes
+    src = open(os.path.join(ROOT, "include", "kvc.h")).read()
+    start = src.index("typedef struct {", src.index("configuration")) + len("typedef struct {")
+    body = src[start:src.index("} kvc_config;")]
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    fields = []
+    for decl in body.split(";"):
+        m = re.match(r"\s*(int32_t|uint32_t|float)\s+(.+)", decl.strip(), flags=re.S)
+        if m:
+            fields += [(m.group(1), n.strip()) for n in m.group(2).split(",")]
+    mirror = kvc.kvc_config._fields_
+    assert [n for _, n in fields] == [n for n, _ in mirror]
+    ctype = {"int32_t": ctypes.c_int32, "uint32_t": ctypes.c_uint32, "float": ctypes.c_float}
+    assert [ctype[t] for t, _ in fields] == [t for _, t in mirror]
